@@ -1,0 +1,292 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each check ties the oracle to something other than itself: torch's
+scaled_dot_product_attention / logsumexp / silu / gelu and autograd on a
+padded dense formulation, finite differences of the oracle's own forward,
+closed forms, invariants, and brute-force enumeration for the tile schedule.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from jagged_attention_recsys_gdpa_gb300 import inputs
+from tests import dense_ref as R
+
+SOFTMAX, SILU, GELU = 0, 1, 2
+NONE, CAUSAL, WINDOW = 0, 1, 3  # WINDOW value as passed: causal | window bits
+
+
+def _batch(lq, lkv, H, D, seed, std=1.0):
+    lq = np.asarray(lq, dtype=np.int64)
+    lkv = np.asarray(lkv, dtype=np.int64)
+    qo, ko = inputs.offsets(lq), inputs.offsets(lkv)
+    q = inputs.values((int(qo[-1]), H, D), std, seed)
+    k = inputs.values((int(ko[-1]), H, D), std, seed + 1)
+    v = inputs.values((int(ko[-1]), H, D), std, seed + 2)
+    do = inputs.values((int(qo[-1]), H, D), 1.0, seed + 3)
+    return qo, ko, q, k, v, do
+
+
+SELF_LENS = ([3, 17, 1, 40, 9], [3, 17, 1, 40, 9])
+CROSS_LENS = ([5, 12, 7, 1, 20], [9, 4, 30, 6, 2])
+
+
+@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 1), (WINDOW, 5), (WINDOW, 64)])
+@pytest.mark.parametrize("lens", [SELF_LENS, CROSS_LENS], ids=["self", "cross"])
+def test_softmax_matches_torch_sdpa(mask, window, lens):
+    H, D = 2, 16
+    qo, ko, q, k, v, _ = _batch(*lens, H, D, seed=11)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = oracle.fwd(qo, ko, q, k, v, H=H, D=D, act=SOFTMAX, mask=mask, window=window, scale=scale)
+    ref = R.sdpa_per_sequence(R.to_f64(q), R.to_f64(k), R.to_f64(v), list(qo), list(ko), mask, window, scale)
+    ref = ref.numpy()
+    # rows with no visible key, from the mask definition (SDPA's own value there varies by version)
+    empty_rows = np.concatenate([~R.mask_matrix(int(qo[b + 1] - qo[b]), int(ko[b + 1] - ko[b]), mask, window)
+                                 .numpy().any(axis=1) for b in range(len(qo) - 1)])
+    empty = np.broadcast_to(empty_rows[:, None], (len(empty_rows), H))
+    np.testing.assert_allclose(o[~empty], ref[~empty], rtol=1e-12, atol=1e-12)
+    assert np.all(o[empty] == 0.0)
+    # log-sum-exp against torch.logsumexp of the masked scores
+    _, lse_ref = R.dense_forward(R.to_f64(q), R.to_f64(k), R.to_f64(v), qo, ko, SOFTMAX, mask, window, scale, False)
+    lse_ref = lse_ref.numpy()
+    assert np.array_equal(np.isneginf(lse), np.isneginf(lse_ref))
+    fin = np.isfinite(lse_ref)
+    np.testing.assert_allclose(lse[fin], lse_ref[fin], rtol=1e-12, atol=1e-12)
+    assert np.array_equal(np.isneginf(lse), empty)
+
+
+@pytest.mark.parametrize("act", [SILU, GELU])
+@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 4)])
+@pytest.mark.parametrize("norm", [False, True])
+@pytest.mark.parametrize("lens", [SELF_LENS, CROSS_LENS], ids=["self", "cross"])
+def test_pointwise_matches_padded_dense(act, mask, window, norm, lens):
+    H, D = 2, 8
+    qo, ko, q, k, v, _ = _batch(*lens, H, D, seed=5, std=0.8)
+    scale = 0.37
+    o, _ = oracle.fwd(qo, ko, q, k, v, H=H, D=D, act=act, mask=mask, window=window, scale=scale, norm_by_lkv=norm)
+    ref, _ = R.dense_forward(R.to_f64(q), R.to_f64(k), R.to_f64(v), qo, ko, act, mask, window, scale, norm)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("act", [SOFTMAX, SILU, GELU])
+@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 3)])
+@pytest.mark.parametrize("lens", [SELF_LENS, CROSS_LENS], ids=["self", "cross"])
+def test_grads_match_torch_autograd(act, mask, window, lens):
+    H, D = 2, 8
+    qo, ko, q, k, v, do = _batch(*lens, H, D, seed=23, std=0.9)
+    scale = 1.0 / math.sqrt(D)
+    norm = act != SOFTMAX
+    dq, dk, dv = oracle.bwd(qo, ko, q, k, v, do, H=H, D=D, act=act, mask=mask, window=window, scale=scale,
+                            norm_by_lkv=norm)
+    gq, gk, gv = R.dense_grads(R.to_f64(q), R.to_f64(k), R.to_f64(v), R.to_f64(do), qo, ko, act, mask, window,
+                               scale, norm)
+    for a, b in ((dq, gq), (dk, gk), (dv, gv)):
+        np.testing.assert_allclose(a, b.numpy(), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("act", [SOFTMAX, SILU, GELU])
+@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 2)])
+def test_grads_finite_differences(act, mask, window):
+    """Central differences of L = sum(o * dO) through the oracle's forward."""
+    H, D = 1, 4
+    rng = np.random.default_rng(3)
+    lq, lkv = [4, 0, 3, 5], [6, 2, 3, 0]
+    qo, ko = inputs.offsets(np.array(lq)), inputs.offsets(np.array(lkv))
+    q = rng.standard_normal((qo[-1], H, D))
+    k = rng.standard_normal((ko[-1], H, D))
+    v = rng.standard_normal((ko[-1], H, D))
+    do = rng.standard_normal((qo[-1], H, D))
+    kw = dict(H=H, D=D, act=act, mask=mask, window=window, scale=0.6, norm_by_lkv=True)
+    grads = oracle.bwd(qo, ko, q, k, v, do, **kw)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.fwd(qo, ko, qq, kk, vv, **kw)
+        return float((o * do).sum())
+
+    eps = 1e-6
+    for which, (x, g) in enumerate(zip((q, k, v), grads)):
+        for idx in itertools.product(*(range(s) for s in x.shape)):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = [q, k, v]
+            args_m = [q, k, v]
+            args_p[which], args_m[which] = xp, xm
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - g[idx]) <= 1e-6 + 1e-6 * abs(fd), (which, idx, fd, g[idx])
+
+
+def test_closed_forms_softmax():
+    H, D = 2, 16
+    lens = [5, 1, 33, 8]
+    qo, ko, q, k, v, _ = _batch(lens, lens, H, D, seed=2)
+    ones = torch.ones_like(v)
+    # rows of p sum to one: V = 1 gives O = 1 for every mask
+    for mask, w in ((NONE, 0), (CAUSAL, 0), (WINDOW, 3)):
+        o, _ = oracle.fwd(qo, ko, q, k, ones, H=H, D=D, act=SOFTMAX, mask=mask, window=w)
+        np.testing.assert_allclose(o, 1.0, rtol=0, atol=1e-13)
+    # window 1: each row sees only its own key -> o_i = v_i, lse_i = s_ii
+    o, lse = oracle.fwd(qo, ko, q, k, v, H=H, D=D, act=SOFTMAX, mask=WINDOW, window=1)
+    np.testing.assert_array_equal(o, R.to_f64(v).numpy())
+    s_ii = (R.to_f64(q) * R.to_f64(k)).sum(-1).numpy() / math.sqrt(D)
+    np.testing.assert_allclose(lse, s_ii, rtol=1e-13, atol=1e-13)
+    # window >= L equals plain causal
+    oc, lc = oracle.fwd(qo, ko, q, k, v, H=H, D=D, act=SOFTMAX, mask=CAUSAL)
+    ow, lw = oracle.fwd(qo, ko, q, k, v, H=H, D=D, act=SOFTMAX, mask=WINDOW, window=max(lens))
+    np.testing.assert_array_equal(oc, ow)
+    np.testing.assert_array_equal(lc, lw)
+    # a single key: o = v_0 whatever the query
+    qo1, ko1 = inputs.offsets(np.array([4, 7])), inputs.offsets(np.array([1, 1]))
+    q1 = inputs.values((11, H, D), 1.0, 9)
+    k1 = inputs.values((2, H, D), 1.0, 10)
+    v1 = inputs.values((2, H, D), 1.0, 11)
+    o1, _ = oracle.fwd(qo1, ko1, q1, k1, v1, H=H, D=D, act=SOFTMAX, mask=NONE)
+    vv = R.to_f64(v1).numpy()
+    np.testing.assert_array_equal(o1[:4], np.broadcast_to(vv[0], (4, H, D)))
+    np.testing.assert_array_equal(o1[4:], np.broadcast_to(vv[1], (7, H, D)))
+
+
+@pytest.mark.parametrize("act,fn", [(SILU, F.silu), (GELU, lambda t: F.gelu(t, approximate="tanh"))])
+def test_activation_values_against_torch(act, fn):
+    """D=1, one query and one key with q=x, k=1, v=1, scale=1: o = act(x)."""
+    xs = np.linspace(-9.0, 9.0, 73)
+    n = len(xs)
+    qo = inputs.offsets(np.ones(n, dtype=np.int64))
+    q = xs.reshape(n, 1, 1).copy()
+    k = np.ones((n, 1, 1))
+    v = np.ones((n, 1, 1))
+    o, _ = oracle.fwd(qo, qo, q, k, v, H=1, D=1, act=act, mask=NONE, scale=1.0)
+    ref = fn(torch.from_numpy(xs)).numpy()
+    np.testing.assert_allclose(o[:, 0, 0], ref, rtol=1e-14, atol=1e-15)
+    # zero queries give zero scores, act(0) = 0, so O = 0
+    H, D = 2, 8
+    qo2, ko2, q2, k2, v2, _ = _batch([3, 4], [5, 2], H, D, seed=1)
+    o2, _ = oracle.fwd(qo2, ko2, torch.zeros_like(q2), k2, v2, H=H, D=D, act=act, mask=NONE)
+    assert np.all(o2 == 0.0)
+
+
+@pytest.mark.parametrize("act", [SOFTMAX, SILU, GELU])
+def test_permutation_equivariance(act):
+    H, D = 2, 8
+    lq, lkv = np.array([4, 9, 1, 6]), np.array([7, 9, 3, 6])
+    qo, ko, q, k, v, do = _batch(lq, lkv, H, D, seed=8)
+    kw = dict(H=H, D=D, act=act, mask=NONE, norm_by_lkv=True)
+    o, lse = oracle.fwd(qo, ko, q, k, v, **kw)
+    dq, dk, dv = oracle.bwd(qo, ko, q, k, v, do, **kw)
+    perm = [2, 0, 3, 1]
+
+    def permute(x, off, lens):
+        return torch.cat([x[off[b] : off[b + 1]] for b in perm], 0)
+
+    qo2, ko2 = inputs.offsets(lq[perm]), inputs.offsets(lkv[perm])
+    P = lambda x, off, lens: permute(torch.as_tensor(x), off, lens)
+    o2, lse2 = oracle.fwd(qo2, ko2, P(q, qo, lq), P(k, ko, lkv), P(v, ko, lkv), **kw)
+    g2 = oracle.bwd(qo2, ko2, P(q, qo, lq), P(k, ko, lkv), P(v, ko, lkv), P(do, qo, lq), **kw)
+    np.testing.assert_array_equal(o2, P(o, qo, lq).numpy())
+    np.testing.assert_array_equal(lse2, P(lse, qo, lq).numpy())
+    np.testing.assert_array_equal(g2[0], P(dq, qo, lq).numpy())
+    np.testing.assert_array_equal(g2[1], P(dk, ko, lkv).numpy())
+    np.testing.assert_array_equal(g2[2], P(dv, ko, lkv).numpy())
+
+
+@pytest.mark.parametrize("act", [SOFTMAX, SILU, GELU])
+def test_empty_sequences(act):
+    H, D = 2, 8
+    lq, lkv = np.array([0, 5, 3, 0, 4]), np.array([3, 0, 6, 0, 4])
+    qo, ko, q, k, v, do = _batch(lq, lkv, H, D, seed=4)
+    kw = dict(H=H, D=D, act=act, mask=NONE)
+    o, lse = oracle.fwd(qo, ko, q, k, v, **kw)
+    dq, dk, dv = oracle.bwd(qo, ko, q, k, v, do, **kw)
+    rows_no_keys = slice(qo[1], qo[2])  # sequence 1 has queries but no keys
+    assert np.all(o[rows_no_keys] == 0.0)
+    assert np.all(dq[rows_no_keys] == 0.0)
+    if act == SOFTMAX:
+        assert np.all(np.isneginf(lse[rows_no_keys]))
+    keys_no_queries = slice(ko[0], ko[1])  # sequence 0 has keys but no queries
+    assert np.all(dk[keys_no_queries] == 0.0) and np.all(dv[keys_no_queries] == 0.0)
+    # the non-empty sequences are unaffected by their empty neighbours
+    qo2, ko2 = inputs.offsets(lq[[2, 4]]), inputs.offsets(lkv[[2, 4]])
+    sel_q = torch.cat([q[qo[2] : qo[3]], q[qo[4] : qo[5]]])
+    sel_k = torch.cat([k[ko[2] : ko[3]], k[ko[4] : ko[5]]])
+    sel_v = torch.cat([v[ko[2] : ko[3]], v[ko[4] : ko[5]]])
+    o2, _ = oracle.fwd(qo2, ko2, sel_q, sel_k, sel_v, **kw)
+    np.testing.assert_array_equal(o2, np.concatenate([o[qo[2] : qo[3]], o[qo[4] : qo[5]]]))
+
+
+def test_softmax_dv_column_sum():
+    """Each softmax row of p sums to one, so sum_j dV_j = sum_i dO_i per (b, h)."""
+    H, D = 2, 8
+    lens = [6, 13, 2]
+    qo, ko, q, k, v, do = _batch(lens, lens, H, D, seed=6)
+    for mask, w in ((NONE, 0), (CAUSAL, 0), (WINDOW, 4)):
+        _, _, dv = oracle.bwd(qo, ko, q, k, v, do, H=H, D=D, act=SOFTMAX, mask=mask, window=w)
+        g = R.to_f64(do).numpy()
+        for b in range(len(lens)):
+            np.testing.assert_allclose(dv[ko[b] : ko[b + 1]].sum(0), g[qo[b] : qo[b + 1]].sum(0), rtol=1e-12,
+                                       atol=1e-12)
+
+
+def test_count_pairs_closed_forms():
+    lens = np.array([1, 7, 30, 129, 0])
+    off = inputs.offsets(lens)
+    assert oracle.count_pairs(off, off, NONE) == int((lens * lens).sum())
+    assert oracle.count_pairs(off, off, CAUSAL) == int((lens * (lens + 1) // 2).sum())
+    W = 10
+    expect = sum(sum(min(i + 1, W) for i in range(L)) for L in lens)
+    assert oracle.count_pairs(off, off, WINDOW, W) == expect
+    lq, lk = np.array([3, 5]), np.array([5, 3])
+    # bottom-right causal with Lq=3, Lkv=5: row i sees i + 3 keys; Lq=5, Lkv=3: max(0, i - 1)
+    assert oracle.count_pairs(inputs.offsets(lq), inputs.offsets(lk), CAUSAL) == (3 + 4 + 5) + (0 + 0 + 1 + 2 + 3)
+
+
+def _brute_schedule(qo, ko, mask, window, BM, BN, transposed):
+    """Every (b, row tile) with the column tiles that hold an allowed pair."""
+    tiles = []
+    for b in range(len(qo) - 1):
+        lq, lk = int(qo[b + 1] - qo[b]), int(ko[b + 1] - ko[b])
+        m = R.mask_matrix(lq, lk, mask, window).numpy()
+        if transposed:
+            m = m.T
+        nrows = m.shape[0]
+        for t in range(-(-nrows // BM)):
+            cols = np.nonzero(m[t * BM : (t + 1) * BM].any(axis=0))[0]
+            if len(cols):
+                tiles.append((b, t, cols.min() // BN, cols.max() // BN + 1))
+            else:
+                tiles.append((b, t, 0, 0))
+    return tiles
+
+
+@pytest.mark.parametrize("transposed", [False, True])
+@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 3), (WINDOW, 9)])
+def test_schedule_twin_brute_force(transposed, mask, window):
+    rng = np.random.default_rng(17)
+    for trial in range(6):
+        B = int(rng.integers(1, 7))
+        lq = rng.integers(0, 40, size=B)
+        lk = lq.copy() if trial % 2 == 0 else rng.integers(0, 40, size=B)
+        qo, ko = inputs.offsets(lq), inputs.offsets(lk)
+        BM, BN = (8, 4) if trial < 3 else (4, 8)
+        got = oracle.schedule(qo, ko, mask=mask, window=window, BM=BM, BN=BN, transposed=transposed)
+        want = _brute_schedule(qo, ko, mask, window, BM, BN, transposed)
+        # same multiset of tiles, each (b, row tile) exactly once
+        assert sorted(map(tuple, got.tolist())) == sorted(want)
+        assert len({(r[0], r[1]) for r in got.tolist()}) == len(got)
+        # longest first, ties in (b, row tile) order
+        keys = [(-(r[3] - r[2]), r[0], r[1]) for r in got.tolist()]
+        assert keys == sorted(keys)
+
+
+def test_schedule_cost_cap_orders_by_index():
+    lens = np.array([40, 300, 64])
+    off = inputs.offsets(lens)
+    got = oracle.schedule(off, off, mask=NONE, BM=16, BN=4, cost_cap=20)
+    costs = np.minimum(got[:, 3] - got[:, 2], 20)
+    assert np.all(np.diff(costs) <= 0)
+    capped = got[costs == 20]
+    assert [tuple(r[:2]) for r in capped.tolist()] == sorted(tuple(r[:2]) for r in capped.tolist())
