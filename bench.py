@@ -1,0 +1,372 @@
+"""Benchmark: jagged attention forward + backward on one GB300 per rank.
+
+One step = one pass of the whole hot path over one batch: device schedule,
+forward (O, LSE), and backward (Di, dK/dV, dQ) of the JFA self-attention
+workload (128 jagged sequences, lognormal lengths with median 1024 clipped to
+[64, 16384], H=4, D=128, causal + sliding window 256, bf16, seed = rank).
+
+Prints one JSON line. value = effective (unpadded, unmasked) TFLOP/s of the
+step (forward 4*D*H*pairs + backward 10*D*H*pairs) summed over ranks / max
+rank time. Inputs are already resident in HBM for `value`; `e2e` repeats the
+measurement through the public Python API with pinned host buffers and the
+host<->device copies inside the timed region. `--impl reference` times the
+CPU oracle instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective (unpadded) attention TFLOPs fwd/bwd; % of GB300 BF16 tensor peak"
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def setup_dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group(backend=os.environ.get("JATTN_BENCH_BACKEND", "nccl"))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sample_sequences(lq, lkv, pairs, H, D, target_flops, seed=0):
+    """Seeded random sequences whose fwd+bwd effective FLOPs reach target_flops."""
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(len(lq))
+    chosen, acc = [], 0.0
+    for b in order:
+        chosen.append(int(b))
+        acc += 14.0 * D * H * float(pairs[b])
+        if acc >= target_flops:
+            break
+    return sorted(chosen), acc
+
+
+def cpu_oracle_step(x_cpu, w, seqs):
+    """One oracle fwd+bwd over the given sequences of a CPU input set; returns seconds."""
+    import torch
+
+    import oracle
+    from jagged_attention_recsys_gdpa_gb300 import inputs
+
+    qo = x_cpu["q_off"].numpy()
+    ko = x_cpu["kv_off"].numpy()
+    rq = np.concatenate([np.arange(qo[b], qo[b + 1]) for b in seqs])
+    rk = np.concatenate([np.arange(ko[b], ko[b + 1]) for b in seqs])
+    lq = np.array([qo[b + 1] - qo[b] for b in seqs])
+    lk = np.array([ko[b + 1] - ko[b] for b in seqs])
+    sub_qo, sub_ko = inputs.offsets(lq), inputs.offsets(lk)
+    tq, tk = torch.from_numpy(rq), torch.from_numpy(rk)
+    q, k, v, do = (x_cpu["q"].index_select(0, tq), x_cpu["k"].index_select(0, tk), x_cpu["v"].index_select(0, tk),
+                   x_cpu["do"].index_select(0, tq))
+    kw = dict(H=w.H, D=w.D, act=w.act, mask=w.mask, window=w.window, norm_by_lkv=w.norm_by_lkv)
+    t0 = time.perf_counter()
+    oracle.fwd(sub_qo, sub_ko, q, k, v, **kw)
+    oracle.bwd(sub_qo, sub_ko, q, k, v, do, **kw)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, ws, rank):
+    """The CPU oracle timed on this host's cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    from jagged_attention_recsys_gdpa_gb300 import flops, inputs
+
+    oracle.build()
+    w = inputs.WORKLOADS[args.workload]
+    x = inputs.make(args.workload, seed=0, device="cpu")
+    pairs = flops.pairs_per_sequence(x["lq"], x["lkv"], w.mask, w.window)
+    seqs, eff = sample_sequences(x["lq"], x["lkv"], pairs, w.H, w.D, args.ref_step_flops)
+    for _ in range(args.warmup):
+        cpu_oracle_step(x, w, seqs)
+    times = [cpu_oracle_step(x, w, seqs) for _ in range(args.steps)]
+    total = sum(times)
+    value = eff * args.steps / total / 1e12
+    cores = oracle.num_threads()
+    sample = (f"{len(seqs)} of {len(x['lq'])} sequences ({int(pairs[seqs].sum())} allowed pairs per head), "
+              f"fwd+bwd in fp64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded lengths and values)",
+        "config": {"workload": args.workload, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="jfa")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-flops", type=float, default=1.5e11, help="effective FLOPs of the CPU-baseline sample")
+    ap.add_argument("--ref-step-flops", type=float, default=2.0e10, help="effective FLOPs per reference step")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    ws, rank, local = setup_dist()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    import torch
+
+    import jagged_attention_recsys_gdpa_gb300 as J
+    from jagged_attention_recsys_gdpa_gb300 import _binding as BND
+    from jagged_attention_recsys_gdpa_gb300 import flops, inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    BND.load()
+    w = inputs.WORKLOADS[args.workload]
+    x = inputs.make(args.workload, seed=rank, device=dev)
+    causal = bool(w.mask & 1)
+    window = w.window if w.mask & 2 else 0
+    kw = dict(act=w.act, causal=causal, window=window, norm_by_lkv=w.norm_by_lkv)
+    pairs_b = flops.pairs_per_sequence(x["lq"], x["lkv"], w.mask, w.window)
+    pairs = int(pairs_b.sum())
+    f_fwd, f_bwd = flops.effective_flops(pairs, w.H, w.D)
+    tq, tk = int(x["lq"].sum()), int(x["lkv"].sum())
+    work = flops.kernel_work(tq, tk, pairs, w.H, w.D, w.act == 0)
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(tq, w.H, dtype=torch.float32, device=dev) if w.act == 0 else None
+    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], out=o, lse=lse, **kw)
+        J.backward(x["q"], x["k"], x["v"], o, lse, x["do"], x["q_off"], x["kv_off"], dq=dq, dk=dk, dv=dv, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = J.device_status(dev)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {BND.error_string(st)}")
+
+    # per-kernel events for the timed steps
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    for evs in kev:
+        for e in evs:
+            e.record(stream)  # creates the underlying CUDA events
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        BND.profile_events(kev[i])
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    BND.profile_events(None)
+    clocks = sampler.stop()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms_max = max_over_ranks(ms, ws, dev)
+    st = J.device_status(dev)
+    if st != 0:
+        raise RuntimeError(f"device status after timing: {BND.error_string(st)}")
+    kt = {
+        "fwd": sum(e[0].elapsed_time(e[1]) for e in kev) / args.steps,
+        "dkdv": sum(e[2].elapsed_time(e[3]) for e in kev) / args.steps,
+        "dq": sum(e[4].elapsed_time(e[5]) for e in kev) / args.steps,
+    }
+    fwd_ms_all = ms  # whole step
+    value = (f_fwd + f_bwd) * ws / (ms_max * 1e-3) / 1e12
+    peaks = load_peaks()
+
+    # roofline of the dominant kernel
+    dom = max(kt, key=kt.get)
+    wk = work[dom]
+    t_s = kt[dom] * 1e-3
+    t_hbm = wk["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = wk["flops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": wk["bytes"] / t_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": wk["flops"] / t_s / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = dom
+    roof["peak_source"] = peaks["source"] + " (burst)"
+
+    # end to end through the public API: pinned host inputs, copies inside the timed region
+    host = {k: x[k].cpu().pin_memory() for k in ("q_off", "kv_off", "q", "k", "v", "do")}
+    out_host = {"o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                "dq": torch.empty(dq.shape, dtype=dq.dtype).pin_memory(),
+                "dk": torch.empty(dk.shape, dtype=dk.dtype).pin_memory(),
+                "dv": torch.empty(dv.shape, dtype=dv.dtype).pin_memory()}
+    if lse is not None:
+        out_host["lse"] = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        d = {k: t.to(dev, non_blocking=True) for k, t in host.items()}
+        oo, ll = J.forward(d["q"], d["k"], d["v"], d["q_off"], d["kv_off"], **kw)
+        gq, gk, gv = J.backward(d["q"], d["k"], d["v"], oo, ll, d["do"], d["q_off"], d["kv_off"], **kw)
+        out_host["o"].copy_(oo, non_blocking=True)
+        out_host["dq"].copy_(gq, non_blocking=True)
+        out_host["dk"].copy_(gk, non_blocking=True)
+        out_host["dv"].copy_(gv, non_blocking=True)
+        if ll is not None:
+            out_host["lse"].copy_(ll, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, ws, dev)
+    e2e_value = (f_fwd + f_bwd) * ws / (e2e_ms * 1e-3) / 1e12
+
+    cpu_base = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        x_cpu = {k: (x[k].cpu() if hasattr(x[k], "cpu") else x[k]) for k in ("q_off", "kv_off", "q", "k", "v", "do")}
+        seqs, eff = sample_sequences(x["lq"], x["lkv"], pairs_b, w.H, w.D, args.cpu_flops)
+        secs = cpu_oracle_step(x_cpu, w, seqs)
+        cpu_base = {
+            "value": eff / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(seqs)} of {len(x['lq'])} sequences, fwd+bwd in fp64, {secs:.1f} s",
+        }
+
+    if rank == 0:
+        peak_tf = peaks["bf16_tflops"]
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded lengths and values)",
+            "config": {
+                "workload": f"{args.workload}: B={len(x['lq'])}, H={w.H}, D={w.D}, "
+                            f"{'softmax' if w.act == 0 else ('silu' if w.act == 1 else 'gelu')}, "
+                            f"mask={'causal' if w.mask == 1 else ('causal+window' if w.mask == 3 else 'none')}"
+                            + (f" {w.window}" if w.mask & 2 else ""),
+                "total_q": tq, "total_kv": tk, "pairs_per_head": pairs,
+                "l2": f"inputs larger than L2 ({tq * w.H * w.D * 2 / 1e6:.0f} MB per bf16 tensor)",
+                "parallelism": f"replicas x{ws} (independent batches, no collective)",
+            },
+            "fwd_tflops": f_fwd / (kt["fwd"] * 1e-3) / 1e12,
+            "bwd_tflops": f_bwd / ((kt["dkdv"] + kt["dq"]) * 1e-3) / 1e12,
+            "pct_of_bf16_peak": 100.0 * value / peak_tf,
+            "kernel_ms": kt,
+            "step_overhead_ms": fwd_ms_all - sum(kt.values()),
+            "roofline": roof,
+            "cpu_baseline": cpu_base,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": (5 + (11 if w.act == 0 else 10)) * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+/*
+ * jattn: jagged generalized dot-product attention on one GB300 (sm_103a).
+ *
+ * The operation ("GEM Training" engineering post, section "Jagged Sequence
+ * Flash Attention": attention computed directly on variable-length jagged
+ * tensors, with asymmetric query and key/value lengths, without padding;
+ * section "Generalized Dot-Product Attention (GDPA)": the same two matrix
+ * products with an element-wise GELU or SiLU in place of the softmax, one
+ * kernel for self-, cross- and pooling attention; section "BlockAttention":
+ * sliding windows for long self-attention). For every sequence b and head h,
+ * with query rows i < Lq(b), key rows j < Lkv(b), delta = Lkv - Lq:
+ *
+ *   allowed(i, j)  causal: j <= i + delta;  window W: 0 <= i + delta - j < W
+ *   s_ij = scale * <q_i, k_j>
+ *   JATTN_SOFTMAX     o_i = sum_j softmax_j(s_ij) v_j over allowed j,
+ *                     lse_i = ln sum_j exp(s_ij)  (no allowed key: o_i = 0,
+ *                     lse_i = -inf)
+ *   JATTN_SILU / JATTN_GELU_TANH
+ *                     o_i = c * sum_{allowed j} act(s_ij) v_j, c = 1/Lkv(b)
+ *                     when norm_by_lkv, else 1
+ *
+ * and the backward pass gives dQ, dK, dV of a loss L from dO = dL/dO.
+ *
+ * Data layout. Jagged tensors are dense row-major [total, H, D] arrays of
+ * bf16 (passed as uint16_t bit patterns) whose rows for sequence b are
+ * off[b] .. off[b+1]-1; offsets are int64 [B+1] device arrays with off[0] = 0,
+ * non-decreasing, off[B] = total. Self-attention passes the same offsets (and
+ * may pass the same pointer) for queries and keys. lse is fp32 [total_q, H].
+ * Every pointer argument except `p`, `bytes` and `device_status` is a DEVICE
+ * pointer; value tensors must be 16-byte aligned.
+ *
+ * Ownership. The caller owns every buffer, including the workspace; the
+ * library allocates no device memory, launches only on `stream` (a
+ * cudaStream_t passed as void*, NULL = legacy default stream) and never
+ * synchronises it in jattn_fwd / jattn_bwd. Calls are asynchronous: errors
+ * that only the device can see (bad offsets, an expired bounded wait) are
+ * written to a status word in the workspace and read by jattn_get_status.
+ * Kernels never trap.
+ *
+ * Return codes: JATTN_OK or a JATTN_ERR_* value; jattn_error_string names it.
+ */
+#ifndef JATTN_H
+#define JATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Activation between the two products. */
+enum {
+  JATTN_SOFTMAX = 0,   /* row softmax (Jagged Flash Attention) */
+  JATTN_SILU = 1,      /* x / (1 + e^-x) (GDPA) */
+  JATTN_GELU_TANH = 2  /* x/2 (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))) (GDPA) */
+};
+
+/* Mask bits. JATTN_MASK_WINDOW must be combined with JATTN_MASK_CAUSAL. */
+enum { JATTN_MASK_NONE = 0, JATTN_MASK_CAUSAL = 1, JATTN_MASK_WINDOW = 2 };
+
+enum {
+  JATTN_OK = 0,
+  JATTN_ERR_INVALID = 1,     /* bad argument detected on the host */
+  JATTN_ERR_CUDA = 2,        /* a CUDA runtime call failed (launch, attribute) */
+  JATTN_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned */
+  JATTN_ERR_ALIGN = 4,       /* a value tensor is not 16-byte aligned */
+  JATTN_ERR_OFFSETS = 5,     /* device: offsets not a valid prefix sum of the totals */
+  JATTN_ERR_TIMEOUT = 6,     /* device: a bounded pipeline wait expired */
+  JATTN_ERR_UNSUPPORTED = 7  /* device is not sm_103 / no kernel image */
+};
+
+typedef struct {
+  int64_t B;          /* number of sequences (>= 1) */
+  int64_t total_q;    /* query rows = q_off[B] (>= 0) */
+  int64_t total_kv;   /* key/value rows = kv_off[B] (>= 0) */
+  int H;              /* heads (>= 1) */
+  int D;              /* head dim: 64 or 128 */
+  int act;            /* JATTN_SOFTMAX / JATTN_SILU / JATTN_GELU_TANH */
+  int mask;           /* JATTN_MASK_* bits: 0, CAUSAL, or CAUSAL|WINDOW */
+  int window;         /* W >= 1 when the window bit is set, else ignored */
+  float scale;        /* > 0; 0 selects 1/sqrt(D) */
+  int norm_by_lkv;    /* pointwise activations only: multiply by 1/Lkv(b) */
+} jattn_params_t;
+
+/* Bytes of workspace jattn_fwd / jattn_bwd need for these sizes (depends on
+ * B, total_q, total_kv, H and act only). The workspace must be 256-byte
+ * aligned device memory whose first 256 bytes (the device status word) are
+ * zero before its first use; jattn_get_status clears them again. Returns
+ * JATTN_ERR_INVALID on bad params. */
+int jattn_workspace_size(const jattn_params_t* p, size_t* bytes);
+
+/* Forward. Reads q [total_q,H,D], k and v [total_kv,H,D]; writes every row of
+ * o [total_q,H,D] and, for JATTN_SOFTMAX, lse [total_q,H] (must be non-NULL
+ * then; ignored otherwise). Host-side checks return JATTN_ERR_INVALID /
+ * JATTN_ERR_ALIGN / JATTN_ERR_WORKSPACE without launching. Device-side
+ * offset errors leave o unspecified and set the status word. */
+int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
+              const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse, void* workspace,
+              size_t workspace_bytes, void* stream);
+
+/* Backward. Inputs as for jattn_fwd plus the forward's o and lse (softmax
+ * only; ignored for pointwise activations) and dout [total_q,H,D]. Writes
+ * every row of dq [total_q,H,D], dk and dv [total_kv,H,D]; key rows that no
+ * query sees get zero gradients. The workspace may be the forward's. */
+int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
+              const uint16_t* k, const uint16_t* v, const uint16_t* o, const float* lse, const uint16_t* dout,
+              uint16_t* dq, uint16_t* dk, uint16_t* dv, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Longest-first tile schedule ("GEM Training" post, GDPA section: valid tiles
+ * are precomputed, empty ones skipped, and the rest spread over the SMs so
+ * no SM gets a much longer share). Builds the schedule the kernels use into
+ * the workspace and copies it to `tiles` (device int32 [max_tiles][4]: b,
+ * row tile, first column tile, end column tile) and its length to
+ * `n_tiles` (device int32). Rows are query tiles of `row_tile` rows and
+ * columns key tiles of `col_tile` rows; with `transposed` the roles swap.
+ * Order: column-tile count (capped at 1023) descending, then (b, row tile).
+ * max_tiles must be at least jattn_max_tiles(p, row_tile, transposed). */
+int jattn_schedule(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, int row_tile,
+                   int col_tile, int transposed, int32_t* tiles, int64_t max_tiles, int32_t* n_tiles,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Upper bound on the number of tiles jattn_schedule can produce. */
+int64_t jattn_max_tiles(const jattn_params_t* p, int row_tile, int transposed);
+
+/* Synchronises `stream`, then reads and clears the device status word of
+ * `workspace` into *device_status (JATTN_OK or JATTN_ERR_OFFSETS /
+ * JATTN_ERR_TIMEOUT). Returns JATTN_ERR_CUDA if the stream reports an error. */
+int jattn_get_status(void* workspace, void* stream, int* device_status);
+
+/* Static, human-readable name of a return / status code. */
+const char* jattn_error_string(int code);
+
+/* For the calling thread: which CUDA step failed most recently and the
+ * runtime's message (empty if none). Valid until the next failing call. */
+const char* jattn_last_error(void);
+
+/* Profiling hook: `events` points to six cudaEvent_t (passed as void*) that
+ * later calls record on their stream right before and right after the
+ * forward, dK/dV and dQ kernel launches (in that order); NULL turns it off.
+ * Used to time those kernels with events on the stream they run on. */
+void jattn_profile_events(void* const* events);
+
+/* Test hook: after this call, bounded waits in the kernels give up after
+ * `timeout_ns` nanoseconds (0 restores the default of two seconds), and
+ * flag bit 0 makes the next launches skip the query-tile copy so that the
+ * first wait on it runs out. Used to check that an expired wait reports
+ * JATTN_ERR_TIMEOUT and leaves the context usable. */
+void jattn_debug_set(int flags, uint64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JATTN_H */

@@ -1,0 +1,148 @@
+"""Jagged generalized dot-product attention for one GB300 (sm_103a).
+
+Public API (thin wrappers over the C-ABI library ``libjattn``; every step of
+the computation runs in its CUDA kernels):
+
+* ``attention(q, k, v, q_off, kv_off, act=..., causal=..., window=..., scale=..., norm_by_lkv=...)``
+  autograd-enabled jagged attention returning O.
+* ``forward(...)`` -> (O, LSE) and ``backward(...)`` -> (dQ, dK, dV): the raw passes.
+* ``schedule(...)``: the device-built longest-first tile list.
+
+Tensors: q [total_q, H, D], k / v [total_kv, H, D] in bf16 on a CUDA device;
+q_off / kv_off int64 [B+1] prefix sums on the same device. D is 64 or 128.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _binding as B
+
+SOFTMAX, SILU, GELU_TANH = B.SOFTMAX, B.SILU, B.GELU_TANH
+MASK_NONE, MASK_CAUSAL, MASK_WINDOW = B.MASK_NONE, B.MASK_CAUSAL, B.MASK_WINDOW
+JattnError = B.JattnError
+
+_ACTS = {"softmax": SOFTMAX, "silu": SILU, "gelu": GELU_TANH, "gelu_tanh": GELU_TANH}
+
+_ws_cache: dict = {}
+
+
+def _act(a) -> int:
+    return _ACTS[a] if isinstance(a, str) else int(a)
+
+
+def _mask(causal: bool, window: int) -> int:
+    if window and window > 0:
+        return MASK_CAUSAL | MASK_WINDOW
+    return MASK_CAUSAL if causal else MASK_NONE
+
+
+def _check(q, k, v, q_off, kv_off):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 3 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor [total, H, D]")
+    for name, t in (("q_off", q_off), ("kv_off", kv_off)):
+        if t.dtype != torch.int64 or not t.is_cuda or t.dim() != 1:
+            raise ValueError(f"{name} must be a CUDA int64 tensor [B+1]")
+    if q_off.numel() != kv_off.numel() or q_off.numel() < 2:
+        raise ValueError("q_off and kv_off must both have B+1 >= 2 entries")
+    if k.shape != v.shape or q.shape[1:] != k.shape[1:]:
+        raise ValueError("q, k, v must share H and D; k and v must have the same shape")
+
+
+def make_params(q, k, q_off, act, mask, window, scale, norm_by_lkv) -> B.Params:
+    return B.params(q_off.numel() - 1, q.shape[0], k.shape[0], q.shape[1], q.shape[2], act, mask,
+                    window if mask & MASK_WINDOW else 0, scale, norm_by_lkv)
+
+
+def workspace(p: B.Params, device) -> torch.Tensor:
+    """Cached zero-initialised workspace of at least the size ``p`` needs."""
+    need = B.workspace_size(p)
+    dev = torch.device(device)
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+        _ws_cache[key] = ws
+    return ws
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def forward(q, k, v, q_off, kv_off, act="softmax", causal=False, window=0, scale=None, norm_by_lkv=False,
+            out=None, lse=None):
+    """Forward pass. Returns (O [total_q,H,D] bf16, LSE [total_q,H] fp32 or None)."""
+    _check(q, k, v, q_off, kv_off)
+    a = _act(act)
+    p = make_params(q, k, q_off, a, _mask(causal, window), window, scale, norm_by_lkv)
+    o = out if out is not None else torch.empty_like(q)
+    if a == SOFTMAX and lse is None:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    ws = workspace(p, q.device)
+    B.fwd(p, q_off, kv_off, q, k, v, o, lse if a == SOFTMAX else None, ws.data_ptr(), ws.numel(),
+          _stream(q.device))
+    return o, (lse if a == SOFTMAX else None)
+
+
+def backward(q, k, v, o, lse, do, q_off, kv_off, act="softmax", causal=False, window=0, scale=None,
+             norm_by_lkv=False, dq=None, dk=None, dv=None):
+    """Backward pass. Returns (dQ, dK, dV) bf16."""
+    _check(q, k, v, q_off, kv_off)
+    a = _act(act)
+    p = make_params(q, k, q_off, a, _mask(causal, window), window, scale, norm_by_lkv)
+    dq = dq if dq is not None else torch.empty_like(q)
+    dk = dk if dk is not None else torch.empty_like(k)
+    dv = dv if dv is not None else torch.empty_like(v)
+    do = do.contiguous()
+    ws = workspace(p, q.device)
+    B.bwd(p, q_off, kv_off, q, k, v, o if a == SOFTMAX else None, lse if a == SOFTMAX else None, do, dq, dk,
+          dv, ws.data_ptr(), ws.numel(), _stream(q.device))
+    return dq, dk, dv
+
+
+class _JaggedAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv):
+        o, lse = forward(q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv)
+        ctx.save_for_backward(q, k, v, o, lse if lse is not None else o.new_empty(0), q_off, kv_off)
+        ctx.cfg = (act, causal, window, scale, norm_by_lkv)
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse, q_off, kv_off = ctx.saved_tensors
+        act, causal, window, scale, norm_by_lkv = ctx.cfg
+        dq, dk, dv = backward(q, k, v, o, lse if lse.numel() else None, do, q_off, kv_off, act, causal, window,
+                              scale, norm_by_lkv)
+        return dq, dk, dv, None, None, None, None, None, None, None
+
+
+def attention(q, k, v, q_off, kv_off, act="softmax", causal=False, window=0, scale=None, norm_by_lkv=False):
+    """Jagged attention with autograd: O = act(scale Q K^T masked) V per sequence."""
+    return _JaggedAttention.apply(q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv)
+
+
+def schedule(q_off, kv_off, H, D=128, causal=False, window=0, row_tile=128, col_tile=128, transposed=False,
+             total_q=None, total_kv=None):
+    """The longest-first tile list the kernels consume: int32 [n, 4] (b, row tile, col lo, col hi)."""
+    tq = int(total_q) if total_q is not None else int(q_off[-1].item())
+    tk = int(total_kv) if total_kv is not None else int(kv_off[-1].item())
+    p = B.params(q_off.numel() - 1, tq, tk, H, D, SOFTMAX, _mask(causal, window), window, 0.0, False)
+    mt = B.max_tiles(p, row_tile, transposed)
+    tiles = torch.zeros(mt, 4, dtype=torch.int32, device=q_off.device)
+    n = torch.zeros(1, dtype=torch.int32, device=q_off.device)
+    ws = workspace(p, q_off.device)
+    B.schedule(p, q_off, kv_off, row_tile, col_tile, transposed, tiles, mt, n, ws.data_ptr(), ws.numel(),
+               _stream(q_off.device))
+    return tiles[: int(n.item())]
+
+
+def device_status(device=None) -> int:
+    """Read and clear the device status word of the cached workspace (syncs)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    ws = _ws_cache.get(key)
+    if ws is None:
+        return 0
+    return B.get_status(ws.data_ptr(), _stream(dev))

@@ -1,0 +1,162 @@
+"""ctypes binding of libjattn (argument marshalling only).
+
+Every computation runs in the CUDA library; this module only converts torch
+tensors to raw pointers and sizes, passes the current CUDA stream, and turns
+non-zero return codes into exceptions. The library must exist: there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+SOFTMAX, SILU, GELU_TANH = 0, 1, 2
+MASK_NONE, MASK_CAUSAL, MASK_WINDOW = 0, 1, 2
+
+EXPORTED = (
+    "jattn_workspace_size",
+    "jattn_fwd",
+    "jattn_bwd",
+    "jattn_schedule",
+    "jattn_max_tiles",
+    "jattn_get_status",
+    "jattn_error_string",
+    "jattn_last_error",
+    "jattn_profile_events",
+    "jattn_debug_set",
+)
+
+
+class Params(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int64),
+        ("total_q", ctypes.c_int64),
+        ("total_kv", ctypes.c_int64),
+        ("H", ctypes.c_int),
+        ("D", ctypes.c_int),
+        ("act", ctypes.c_int),
+        ("mask", ctypes.c_int),
+        ("window", ctypes.c_int),
+        ("scale", ctypes.c_float),
+        ("norm_by_lkv", ctypes.c_int),
+    ]
+
+
+class JattnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        detail = ""
+        if code == 2:
+            detail = " [" + load().jattn_last_error().decode() + "]"
+        super().__init__(f"{where}: {error_string(code)} (code {code}){detail}")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load libjattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"libjattn.so not found at {path}; build it with "
+            "`python -m jagged_attention_recsys_gdpa_gb300.build` (no CPU fallback exists)"
+        )
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(Params)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.jattn_workspace_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+    lib.jattn_workspace_size.restype = i32
+    lib.jattn_fwd.argtypes = [P] + [vp] * 7 + [vp, ctypes.c_size_t, vp]
+    lib.jattn_fwd.restype = i32
+    lib.jattn_bwd.argtypes = [P] + [vp] * 11 + [vp, ctypes.c_size_t, vp]
+    lib.jattn_bwd.restype = i32
+    lib.jattn_schedule.argtypes = [P, vp, vp, i32, i32, i32, vp, i64, vp, vp, ctypes.c_size_t, vp]
+    lib.jattn_schedule.restype = i32
+    lib.jattn_max_tiles.argtypes = [P, i32, i32]
+    lib.jattn_max_tiles.restype = i64
+    lib.jattn_get_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
+    lib.jattn_get_status.restype = i32
+    lib.jattn_error_string.argtypes = [i32]
+    lib.jattn_error_string.restype = ctypes.c_char_p
+    lib.jattn_last_error.argtypes = []
+    lib.jattn_last_error.restype = ctypes.c_char_p
+    lib.jattn_profile_events.argtypes = [ctypes.POINTER(vp)]
+    lib.jattn_profile_events.restype = None
+    lib.jattn_debug_set.argtypes = [i32, ctypes.c_uint64]
+    lib.jattn_debug_set.restype = None
+    _lib = lib
+    return lib
+
+
+def error_string(code: int) -> str:
+    return load().jattn_error_string(int(code)).decode()
+
+
+def check(code: int, where: str):
+    if code != 0:
+        raise JattnError(code, where)
+
+
+def params(B, total_q, total_kv, H, D, act, mask, window, scale, norm_by_lkv) -> Params:
+    return Params(int(B), int(total_q), int(total_kv), int(H), int(D), int(act), int(mask), int(window),
+                  float(scale or 0.0), int(bool(norm_by_lkv)))
+
+
+def workspace_size(p: Params) -> int:
+    n = ctypes.c_size_t(0)
+    check(load().jattn_workspace_size(ctypes.byref(p), ctypes.byref(n)), "jattn_workspace_size")
+    return int(n.value)
+
+
+def ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def fwd(p: Params, q_off, kv_off, q, k, v, o, lse, ws, ws_bytes: int, stream: int):
+    check(load().jattn_fwd(ctypes.byref(p), ptr(q_off), ptr(kv_off), ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse),
+                           ws, ws_bytes, stream), "jattn_fwd")
+
+
+def bwd(p: Params, q_off, kv_off, q, k, v, o, lse, do, dq, dk, dv, ws, ws_bytes: int, stream: int):
+    check(load().jattn_bwd(ctypes.byref(p), ptr(q_off), ptr(kv_off), ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse),
+                           ptr(do), ptr(dq), ptr(dk), ptr(dv), ws, ws_bytes, stream), "jattn_bwd")
+
+
+def schedule(p: Params, q_off, kv_off, row_tile, col_tile, transposed, tiles, max_tiles, n_tiles, ws, ws_bytes,
+             stream):
+    check(load().jattn_schedule(ctypes.byref(p), ptr(q_off), ptr(kv_off), int(row_tile), int(col_tile),
+                                int(bool(transposed)), ptr(tiles), int(max_tiles), ptr(n_tiles), ws, ws_bytes,
+                                stream), "jattn_schedule")
+
+
+def max_tiles(p: Params, row_tile: int, transposed: bool) -> int:
+    return int(load().jattn_max_tiles(ctypes.byref(p), int(row_tile), int(bool(transposed))))
+
+
+def get_status(ws, stream) -> int:
+    s = ctypes.c_int(0)
+    check(load().jattn_get_status(ws, stream, ctypes.byref(s)), "jattn_get_status")
+    return int(s.value)
+
+
+def debug_set(flags: int, timeout_ns: int):
+    load().jattn_debug_set(int(flags), int(timeout_ns))
+
+
+def profile_events(events):
+    """Record the six given torch.cuda.Event objects around the main kernels (None: off)."""
+    if events is None:
+        load().jattn_profile_events(None)
+        return
+    arr = (ctypes.c_void_p * 6)(*[e.cuda_event for e in events])
+    load().jattn_profile_events(arr)

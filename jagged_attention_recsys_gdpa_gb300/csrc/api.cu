@@ -1,0 +1,360 @@
+// C-ABI entry points of libjattn: argument checks, workspace layout, TMA
+// descriptors and kernel launches on the caller's stream.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/jattn.h"
+#include "common.cuh"
+#include "kernels.h"
+#include "sched.h"
+
+namespace jattn {
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+thread_local char g_last_error[256] = "";
+int g_debug_flags = 0;
+uint64_t g_timeout_ns = kDefaultTimeoutNs;
+// Optional events recorded around the main kernels: [fwd, dkdv, dq] x [begin, end].
+cudaEvent_t g_prof[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+
+void prof(int i, cudaStream_t st) {
+  if (g_prof[i]) cudaEventRecord(g_prof[i], st);
+}
+
+size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Record which CUDA step failed (readable through jattn_last_error).
+int cuda_fail(const char* what, cudaError_t e) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", what, cudaGetErrorString(e), static_cast<int>(e));
+  return JATTN_ERR_CUDA;
+}
+
+// Errors left by earlier, unrelated runtime calls on this thread must not be
+// mistaken for a failed launch of ours.
+void clear_stale_error() { (void)cudaGetLastError(); }
+
+struct Layout {
+  size_t status, sched_fwd, sched_q, sched_kv, di, total;
+  int64_t tiles_fwd, tiles_q, tiles_kv;
+};
+
+Layout layout_for(const jattn_params_t& p) {
+  Layout L{};
+  const int fwd_rows = fwd_rows_per_item();
+  L.tiles_fwd = sched_max_tiles(p.B, p.total_q, fwd_rows);
+  L.tiles_q = sched_max_tiles(p.B, p.total_q, kTile);
+  L.tiles_kv = sched_max_tiles(p.B, p.total_kv, kTile);
+  size_t off = 0;
+  L.status = off;
+  off += 256;
+  L.sched_fwd = off;
+  off += al256(sched_ws_bytes(p.B, L.tiles_fwd));
+  L.sched_q = off;
+  off += al256(sched_ws_bytes(p.B, L.tiles_q));
+  L.sched_kv = off;
+  off += al256(sched_ws_bytes(p.B, L.tiles_kv));
+  L.di = off;
+  if (p.act == JATTN_SOFTMAX) off += al256(sizeof(float) * static_cast<size_t>(p.total_q) * p.H);
+  L.total = off;
+  return L;
+}
+
+int check_params(const jattn_params_t* p) {
+  if (!p) return JATTN_ERR_INVALID;
+  if (p->B < 1 || p->total_q < 0 || p->total_kv < 0 || p->H < 1) return JATTN_ERR_INVALID;
+  if (p->D != 64 && p->D != 128) return JATTN_ERR_INVALID;
+  if (p->act != JATTN_SOFTMAX && p->act != JATTN_SILU && p->act != JATTN_GELU_TANH) return JATTN_ERR_INVALID;
+  if (p->mask != JATTN_MASK_NONE && p->mask != JATTN_MASK_CAUSAL &&
+      p->mask != (JATTN_MASK_CAUSAL | JATTN_MASK_WINDOW))
+    return JATTN_ERR_INVALID;
+  if ((p->mask & JATTN_MASK_WINDOW) && p->window < 1) return JATTN_ERR_INVALID;
+  if (!(p->scale >= 0.0f) || !std::isfinite(p->scale)) return JATTN_ERR_INVALID;
+  if (p->norm_by_lkv != 0 && p->norm_by_lkv != 1) return JATTN_ERR_INVALID;
+  if (p->norm_by_lkv && p->act == JATTN_SOFTMAX) return JATTN_ERR_INVALID;
+  // TMA row coordinates and per-sequence row indices are 32-bit.
+  if (p->total_q >= (int64_t(1) << 31) || p->total_kv >= (int64_t(1) << 31)) return JATTN_ERR_INVALID;
+  if (static_cast<int64_t>(p->H) * p->D * 2 >= (int64_t(1) << 31)) return JATTN_ERR_INVALID;
+  return JATTN_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+int check_ws(const jattn_params_t* p, void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return JATTN_ERR_WORKSPACE;
+  if (ws_bytes < layout_for(*p).total) return JATTN_ERR_WORKSPACE;
+  return JATTN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+struct DeviceInfo {
+  int sms = 0;
+  bool ok = false;
+};
+DeviceInfo g_dev[64];
+std::mutex g_dev_mu;
+
+int device_info(DeviceInfo& out) {
+  int dev = 0;
+  cudaError_t e0 = cudaGetDevice(&dev);
+  if (e0 != cudaSuccess) return cuda_fail("cudaGetDevice", e0);
+  if (dev < 0 || dev >= 64) return JATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> g(g_dev_mu);
+  if (!g_dev[dev].ok) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return cuda_fail("cudaDeviceGetAttribute", cudaGetLastError());
+    if (major != 10 || minor != 3) return JATTN_ERR_UNSUPPORTED;
+    g_dev[dev].sms = sms;
+    g_dev[dev].ok = true;
+  }
+  out = g_dev[dev];
+  return JATTN_OK;
+}
+
+int encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? JATTN_OK : JATTN_ERR_CUDA;
+}
+
+// 2-D view [rows, H*D] of a jagged bf16 tensor; boxes of 128 rows x 64
+// columns (128 bytes) with the 128-byte swizzle the MMA descriptors expect.
+int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int H, int D) {
+  std::memset(m, 0, sizeof(*m));
+  if (rows == 0) return JATTN_OK;  // never dereferenced: no tile is scheduled
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * D, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * D * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? JATTN_OK : JATTN_ERR_CUDA;
+}
+
+AttnArgs base_args(const jattn_params_t& p, const int64_t* q_off, const int64_t* kv_off, void* ws) {
+  AttnArgs a{};
+  a.q_off = q_off;
+  a.kv_off = kv_off;
+  a.H = p.H;
+  a.mask = p.mask;
+  a.window = (p.mask & JATTN_MASK_WINDOW) ? p.window : 0;
+  const float scale = p.scale > 0.0f ? p.scale : 1.0f / std::sqrt(static_cast<float>(p.D));
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.norm_by_lkv = p.norm_by_lkv;
+  a.status = reinterpret_cast<DevStatus*>(static_cast<char*>(ws));
+  a.timeout_ns = g_timeout_ns;
+  a.debug_flags = g_debug_flags;
+  return a;
+}
+
+int grid_for(const DeviceInfo& d, int64_t max_tiles, int H) {
+  const int64_t items = max_tiles * H;
+  return static_cast<int>(items < d.sms ? (items > 0 ? items : 1) : d.sms);
+}
+
+}  // namespace
+}  // namespace jattn
+
+using namespace jattn;
+
+extern "C" {
+
+int jattn_workspace_size(const jattn_params_t* p, size_t* bytes) {
+  if (!bytes) return JATTN_ERR_INVALID;
+  const int rc = check_params(p);
+  if (rc != JATTN_OK) return rc;
+  *bytes = layout_for(*p).total;
+  return JATTN_OK;
+}
+
+int64_t jattn_max_tiles(const jattn_params_t* p, int row_tile, int transposed) {
+  if (check_params(p) != JATTN_OK || row_tile < 1) return -1;
+  return sched_max_tiles(p->B, transposed ? p->total_kv : p->total_q, row_tile);
+}
+
+int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
+              const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse, void* ws, size_t ws_bytes,
+              void* stream) {
+  int rc = check_params(p);
+  if (rc != JATTN_OK) return rc;
+  if (!q_off || !kv_off) return JATTN_ERR_INVALID;
+  if ((p->total_q > 0 && (!q || !o)) || (p->total_kv > 0 && (!k || !v))) return JATTN_ERR_INVALID;
+  if (p->act == JATTN_SOFTMAX && p->total_q > 0 && !lse) return JATTN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return JATTN_ERR_ALIGN;
+  if ((rc = check_ws(p, ws, ws_bytes)) != JATTN_OK) return rc;
+  DeviceInfo dev;
+  if ((rc = device_info(dev)) != JATTN_OK) return rc;
+  if ((rc = encoder()) != JATTN_OK) return rc;
+  clear_stale_error();
+  if (p->total_q == 0) return JATTN_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Layout L = layout_for(*p);
+  char* base = static_cast<char*>(ws);
+  const SchedView sv = sched_carve(base + L.sched_fwd, p->B, L.tiles_fwd);
+  AttnArgs a = base_args(*p, q_off, kv_off, ws);
+  cudaError_t e;
+  if ((e = sched_launch(sv, q_off, kv_off, p->B, p->total_q, p->total_kv, fwd_rows_per_item(), kTile, p->mask,
+                        a.window, 0, a.status, st)) != cudaSuccess)
+    return cuda_fail("schedule launch", e);
+  CUtensorMap mq, mk, mv;
+  if (make_map(&mq, q, p->total_q, p->H, p->D) || make_map(&mk, k, p->total_kv, p->H, p->D) ||
+      make_map(&mv, v, p->total_kv, p->H, p->D))
+    return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+  a.tiles = sv.sorted;
+  a.n_tiles = sv.n_tiles;
+  a.out0 = reinterpret_cast<__nv_bfloat16*>(o);
+  a.f0 = lse;
+  prof(0, st);
+  if ((e = launch_fwd(p->D, p->act, mq, mk, mv, a, grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
+    return cuda_fail("forward kernel launch", e);
+  prof(1, st);
+  return JATTN_OK;
+}
+
+int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
+              const uint16_t* k, const uint16_t* v, const uint16_t* o, const float* lse, const uint16_t* dout,
+              uint16_t* dq, uint16_t* dk, uint16_t* dv, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_params(p);
+  if (rc != JATTN_OK) return rc;
+  if (!q_off || !kv_off) return JATTN_ERR_INVALID;
+  if (p->total_q > 0 && (!q || !dout || !dq)) return JATTN_ERR_INVALID;
+  if (p->total_kv > 0 && (!k || !v || !dk || !dv)) return JATTN_ERR_INVALID;
+  if (p->act == JATTN_SOFTMAX && p->total_q > 0 && (!o || !lse)) return JATTN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv))
+    return JATTN_ERR_ALIGN;
+  if ((rc = check_ws(p, ws, ws_bytes)) != JATTN_OK) return rc;
+  DeviceInfo dev;
+  if ((rc = device_info(dev)) != JATTN_OK) return rc;
+  if ((rc = encoder()) != JATTN_OK) return rc;
+  clear_stale_error();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Layout L = layout_for(*p);
+  char* base = static_cast<char*>(ws);
+  AttnArgs a = base_args(*p, q_off, kv_off, ws);
+  float* di = (p->act == JATTN_SOFTMAX) ? reinterpret_cast<float*>(base + L.di) : nullptr;
+  cudaError_t e;
+  if (di && (e = launch_bwd_di(o, dout, di, p->total_q, p->H, p->D, st)) != cudaSuccess)
+    return cuda_fail("Di kernel launch", e);
+  CUtensorMap mq, mk, mv, mdo;
+  if (make_map(&mq, q, p->total_q, p->H, p->D) || make_map(&mk, k, p->total_kv, p->H, p->D) ||
+      make_map(&mv, v, p->total_kv, p->H, p->D) || make_map(&mdo, dout, p->total_q, p->H, p->D))
+    return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+  a.f0 = const_cast<float*>(lse);
+  a.f1 = di;
+  if (p->total_kv > 0) {
+    const SchedView kv = sched_carve(base + L.sched_kv, p->B, L.tiles_kv);
+    if ((e = sched_launch(kv, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 1,
+                          a.status, st)) != cudaSuccess)
+      return cuda_fail("key-tile schedule launch", e);
+    a.tiles = kv.sorted;
+    a.n_tiles = kv.n_tiles;
+    a.out0 = reinterpret_cast<__nv_bfloat16*>(dk);
+    a.out1 = reinterpret_cast<__nv_bfloat16*>(dv);
+    prof(2, st);
+    if ((e = launch_bwd_dkdv(p->D, p->act, mq, mk, mv, mdo, a, grid_for(dev, L.tiles_kv, p->H), st)) !=
+        cudaSuccess)
+      return cuda_fail("dK/dV kernel launch", e);
+    prof(3, st);
+  }
+  if (p->total_q > 0) {
+    const SchedView qs = sched_carve(base + L.sched_q, p->B, L.tiles_q);
+    if ((e = sched_launch(qs, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 0,
+                          a.status, st)) != cudaSuccess)
+      return cuda_fail("query-tile schedule launch", e);
+    a.tiles = qs.sorted;
+    a.n_tiles = qs.n_tiles;
+    a.out0 = reinterpret_cast<__nv_bfloat16*>(dq);
+    a.out1 = nullptr;
+    prof(4, st);
+    if ((e = launch_bwd_dq(p->D, p->act, mq, mk, mv, mdo, a, grid_for(dev, L.tiles_q, p->H), st)) != cudaSuccess)
+      return cuda_fail("dQ kernel launch", e);
+    prof(5, st);
+  }
+  return JATTN_OK;
+}
+
+int jattn_schedule(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, int row_tile,
+                   int col_tile, int transposed, int32_t* tiles, int64_t max_tiles, int32_t* n_tiles, void* ws,
+                   size_t ws_bytes, void* stream) {
+  int rc = check_params(p);
+  if (rc != JATTN_OK) return rc;
+  if (row_tile < kTile || col_tile < 1 || !q_off || !kv_off || !tiles || !n_tiles) return JATTN_ERR_INVALID;
+  if ((rc = check_ws(p, ws, ws_bytes)) != JATTN_OK) return rc;
+  const int64_t need = sched_max_tiles(p->B, transposed ? p->total_kv : p->total_q, row_tile);
+  if (max_tiles < need) return JATTN_ERR_INVALID;
+  clear_stale_error();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Layout L = layout_for(*p);
+  char* base = static_cast<char*>(ws);
+  // The row_tile = 128 regions are the largest; a coarser tiling fits in them.
+  const SchedView sv = sched_carve(base + (transposed ? L.sched_kv : L.sched_q), p->B,
+                                   transposed ? L.tiles_kv : L.tiles_q);
+  const int window = (p->mask & JATTN_MASK_WINDOW) ? p->window : 0;
+  if (sched_launch(sv, q_off, kv_off, p->B, p->total_q, p->total_kv, row_tile, col_tile, p->mask, window,
+                   transposed ? 1 : 0, reinterpret_cast<DevStatus*>(base), st) != cudaSuccess)
+    return JATTN_ERR_CUDA;
+  if (cudaMemcpyAsync(tiles, sv.sorted, sizeof(int4) * need, cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(n_tiles, sv.n_tiles, sizeof(int), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return JATTN_ERR_CUDA;
+  return JATTN_OK;
+}
+
+int jattn_get_status(void* ws, void* stream, int* device_status) {
+  if (!ws || !device_status) return JATTN_ERR_INVALID;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DevStatus h{};
+  if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return JATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return JATTN_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), st) != cudaSuccess) return JATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return JATTN_ERR_CUDA;
+  *device_status = h.code;
+  return JATTN_OK;
+}
+
+const char* jattn_error_string(int code) {
+  switch (code) {
+    case JATTN_OK: return "ok";
+    case JATTN_ERR_INVALID: return "invalid argument";
+    case JATTN_ERR_CUDA: return "CUDA runtime error";
+    case JATTN_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+    case JATTN_ERR_ALIGN: return "value tensor not 16-byte aligned";
+    case JATTN_ERR_OFFSETS: return "offsets are not a valid prefix sum of the row totals";
+    case JATTN_ERR_TIMEOUT: return "a bounded pipeline wait expired";
+    case JATTN_ERR_UNSUPPORTED: return "device is not sm_103";
+    default: return "unknown error code";
+  }
+}
+
+const char* jattn_last_error(void) { return g_last_error; }
+
+void jattn_profile_events(void* const* events) {
+  for (int i = 0; i < 6; ++i) g_prof[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+}
+
+void jattn_debug_set(int flags, uint64_t timeout_ns) {
+  g_debug_flags = flags;
+  g_timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
+}
+
+}  // extern "C"

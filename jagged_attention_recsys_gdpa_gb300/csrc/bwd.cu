@@ -1,0 +1,766 @@
+// Backward pass of jagged generalized dot-product attention on sm_103a.
+//
+// "GEM Training" post, section "Jagged Sequence Flash Attention", bullet on
+// backward parallelisation: for many sequences x heads the fastest scheme is
+// not to split a sequence's key range across CTAs and to compute dQ in its
+// own pass (split dQ / dK-dV), so that no atomic adds are needed. Here:
+//   di    Di = rowsum(dO * O) per query row and head (softmax only)
+//   dkdv  one item = (sequence, 128-key tile, head); walks the query tiles
+//         that can see it: S^T = K Q^T, dP^T = V dO^T, P^T and dS^T from the
+//         activation, dV += P^T dO, dK += dS^T Q (all accumulated in TMEM)
+//   dq    one item = (sequence, 128-query tile, head); walks its key tiles:
+//         S = Q K^T, dP = dO V^T, dS, dQ += dS K
+// Both MMA kernels are persistent and warp-specialised: warp 0 issues TMA
+// copies, warp 1 issues tcgen05 MMAs, warps 2-5 (one TMEM lane per thread)
+// apply the activation and its derivative and write P / dS back to TMEM as
+// bf16, where the next MMA reads them as its A operand.
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace jattn {
+
+namespace {
+
+constexpr int kThreads = 192;  // 6 warps
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+__device__ __forceinline__ void wg_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// act(x) and act'(x) for the pointwise activations.
+template <int ACT>
+__device__ __forceinline__ void act_and_grad(float x, float& f, float& g) {
+  if constexpr (ACT == JATTN_SILU) {
+    const float sg = __fdividef(1.0f, 1.0f + ex2_approx(-x * kLog2e));
+    f = x * sg;
+    g = sg * fmaf(x, 1.0f - sg, 1.0f);
+  } else {
+    const float k0 = 0.7978845608028654f, k1 = 0.044715f;
+    const float x2 = x * x;
+    const float t = tanh_approx(k0 * fmaf(k1 * x2, x, x));
+    f = 0.5f * x * (1.0f + t);
+    g = fmaf(0.5f * x * (1.0f - t * t) * k0, fmaf(3.0f * k1, x2, 1.0f), 0.5f * (1.0f + t));
+  }
+}
+
+// Store one 128-bit-vectorised bf16 row chunk of 32 fp32 values times `mul`.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&v)[32], float mul) {
+  uint32_t w[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) d[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+}
+
+__device__ __forceinline__ void zero_row(__nv_bfloat16* dst, int D) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  for (int e = 0; e < D / 8; ++e) d[e] = make_uint4(0, 0, 0, 0);
+}
+
+struct BwdItem {
+  int b, rt, lo, hi, h, lq, lkv;
+  int64_t q0, k0;
+};
+
+__device__ __forceinline__ bool load_bwd_item(const AttnArgs& a, long long round, BwdItem& it) {
+  const long long n_items = static_cast<long long>(*a.n_tiles) * a.H;
+  const long long k = zigzag_item(round, blockIdx.x, gridDim.x);
+  if (k >= n_items) return false;
+  const int4 t = a.tiles[k / a.H];
+  it.h = static_cast<int>(k % a.H);
+  it.b = t.x;
+  it.rt = t.y;
+  it.lo = t.z;
+  it.hi = t.w;
+  it.q0 = a.q_off[it.b];
+  it.k0 = a.kv_off[it.b];
+  it.lq = static_cast<int>(a.q_off[it.b + 1] - it.q0);
+  it.lkv = static_cast<int>(a.kv_off[it.b + 1] - it.k0);
+  return true;
+}
+
+// ---------------------------------------------------------------------------- Di
+// One group of D/8 threads per (row, head): each thread reads 16 bytes of O
+// and of dO, the group reduces with shuffles.
+__global__ void __launch_bounds__(256) di_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
+                                                 float* __restrict__ di, int64_t n_rowheads, int D) {
+  const int group = D / 8;
+  const int64_t gid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
+  const int64_t rh = gid / group;
+  const int part = static_cast<int>(gid % group);
+  float acc = 0.0f;
+  if (rh < n_rowheads) {
+    const uint4 x = o[rh * group + part], y = dout[rh * group + part];
+    const __nv_bfloat162* xa = reinterpret_cast<const __nv_bfloat162*>(&x);
+    const __nv_bfloat162* ya = reinterpret_cast<const __nv_bfloat162*>(&y);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 fx = __bfloat1622float2(xa[e]), fy = __bfloat1622float2(ya[e]);
+      acc = fmaf(fx.x, fy.x, acc);
+      acc = fmaf(fx.y, fy.y, acc);
+    }
+  }
+  for (int off = group / 2; off > 0; off >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, off, group);
+  if (rh < n_rowheads && part == 0) di[rh] = acc;
+}
+
+// ---------------------------------------------------------------------------- dK / dV
+template <int D>
+struct DkdvCfg {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kQOff = 2 * kTileBytes;                          // stage s: Q at kQOff + s * 2 tiles
+  static constexpr int kDOOff = 3 * kTileBytes;                         //          dO right after Q
+  static constexpr int kLseOff = 2 * kTileBytes + kStages * 2 * kTileBytes;  // [2][128] lse2, [2][128] Di
+  static constexpr int kBarOff = kLseOff + 4 * kTile * 4;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  static constexpr uint32_t kSCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
+};
+
+struct DkdvBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t qd_full[3], qd_empty[3];
+  uint64_t s_full, dp_full, p_ready, ds_ready, acc_full, acc_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D, int ACT>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                const AttnArgs a) {
+  using C = DkdvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DkdvBars* bars = reinterpret_cast<DkdvBars*>(sm + C::kBarOff);
+  float* s_lse = reinterpret_cast<float*>(sm + C::kLseOff);  // [2][128]
+  float* s_di = s_lse + 2 * kTile;                           // [2][128]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &bars->abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->qd_full[s], 1);
+      mbar_init(&bars->qd_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, kTile);
+    mbar_init(&bars->ds_ready, kTile);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, kTile);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t item_cnt = 0, qd_it = 0;
+      bool kv_armed = false;
+      BwdItem it;
+      for (long long r = 0; load_bwd_item(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!wait_bar(&bars->kv_empty, (item_cnt & 1) ^ 1, abort_flag, a, 40)) break;
+        ++item_cnt;
+        const int yk = static_cast<int>(it.k0) + it.rt * kTile;
+        if (!(a.debug_flags & 1)) {
+          mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTileBytes);
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_2d(sm + C::kKOff + c * kTile * 128, &tmK, &bars->kv_full, it.h * D + c * 64, yk);
+            tma_load_2d(sm + C::kVOff + c * kTile * 128, &tmV, &bars->kv_full, it.h * D + c * 64, yk);
+          }
+          kv_armed = true;
+        }
+        bool ok = true;
+        for (int i = it.lo; i < it.hi; ++i, ++qd_it) {
+          const int s = qd_it % C::kStages;
+          if (!(ok = wait_bar(&bars->qd_empty[s], ((qd_it / C::kStages) & 1) ^ 1, abort_flag, a, 41))) break;
+          const int yq = static_cast<int>(it.q0) + i * kTile;
+          mbar_arrive_expect_tx(&bars->qd_full[s], 2 * C::kTileBytes);
+          uint8_t* st = sm + C::kQOff + s * 2 * C::kTileBytes;
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_2d(st + c * kTile * 128, &tmQ, &bars->qd_full[s], it.h * D + c * 64, yq);
+            tma_load_2d(st + C::kTileBytes + c * kTile * 128, &tmDO, &bars->qd_full[s], it.h * D + c * 64, yq);
+          }
+        }
+        if (!ok) break;
+      }
+      if (kv_armed) drain_wait(&bars->kv_full, (item_cnt - 1) & 1, a.timeout_ns);
+      for (uint32_t i = (qd_it > (uint32_t)C::kStages ? qd_it - C::kStages : 0); i < qd_it; ++i)
+        drain_wait(&bars->qd_full[i % C::kStages], (i / C::kStages) & 1, a.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kTile, kTile, false, false);
+      constexpr uint32_t idAcc = idesc_bf16_f32(kTile, D, false, true);
+      const uint32_t sK = smem_u32(sm + C::kKOff), sV = smem_u32(sm + C::kVOff);
+      const uint32_t sQ0 = smem_u32(sm + C::kQOff);
+      uint32_t item_cnt = 0, qd_it = 0, p_cnt = 0, ds_cnt = 0, acc_cnt = 0;
+      bool ok = true;
+      BwdItem it;
+      auto sQ = [&](int s) { return sQ0 + s * 2 * C::kTileBytes; };
+      auto sDO = [&](int s) { return sQ0 + s * 2 * C::kTileBytes + C::kTileBytes; };
+      auto kmajor = [](uint32_t base, int kk) {
+        return sdesc_sw128(base + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
+      };
+      auto issue_s = [&](int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kSCol, kmajor(sK, kk), kmajor(sQ(s), kk), idS, kk > 0);
+        mma_commit(&bars->s_full);
+      };
+      auto issue_dp = [&](int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kDPCol, kmajor(sV, kk), kmajor(sDO(s), kk), idS, kk > 0);
+        mma_commit(&bars->dp_full);
+      };
+      for (long long r = 0; ok && load_bwd_item(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!(ok = wait_bar(&bars->kv_full, item_cnt & 1, abort_flag, a, 50))) break;
+        ++item_cnt;
+        tc_fence_after();
+        {
+          const int s = qd_it % C::kStages;
+          if (!(ok = wait_bar(&bars->qd_full[s], (qd_it / C::kStages) & 1, abort_flag, a, 51))) break;
+          tc_fence_after();
+          issue_s(s);
+          issue_dp(s);
+        }
+        for (int i = it.lo; i < it.hi; ++i, ++qd_it) {
+          const int s = qd_it % C::kStages;
+          const bool more = i + 1 < it.hi;
+          const int s1 = (qd_it + 1) % C::kStages;
+          if (i == it.lo) {
+            if (!(ok = wait_bar(&bars->acc_empty, (acc_cnt & 1) ^ 1, abort_flag, a, 52))) break;
+          }
+          if (!(ok = wait_bar(&bars->p_ready, p_cnt & 1, abort_flag, a, 53))) break;
+          ++p_cnt;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tmem + C::kDVCol, tmem + C::kSCol + kk * 8,
+                   sdesc_sw128(sDO(s) + kk * 16 * 128, kTile * 128, 1024), idAcc, (kk > 0 || i > it.lo) ? 1u : 0u);
+          if (more) {
+            if (!(ok = wait_bar(&bars->qd_full[s1], ((qd_it + 1) / C::kStages) & 1, abort_flag, a, 54))) break;
+            tc_fence_after();
+            issue_s(s1);
+          }
+          if (!(ok = wait_bar(&bars->ds_ready, ds_cnt & 1, abort_flag, a, 55))) break;
+          ++ds_cnt;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tmem + C::kDKCol, tmem + C::kDPCol + kk * 8,
+                   sdesc_sw128(sQ(s) + kk * 16 * 128, kTile * 128, 1024), idAcc, (kk > 0 || i > it.lo) ? 1u : 0u);
+          mma_commit(&bars->qd_empty[s]);
+          if (more) issue_dp(s1);
+        }
+        if (!ok) break;
+        mma_commit(&bars->acc_full);
+        ++acc_cnt;
+        mma_commit(&bars->kv_empty);
+      }
+      mma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0, a.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    const int row = 32 * (warp & 3) + lane;
+    const int tid = threadIdx.x - 64;  // 0..127 within the warpgroup
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    uint32_t s_cnt = 0, acc_cnt = 0, step = 0;
+    BwdItem it;
+    for (long long r = 0; load_bwd_item(a, r, it); ++r) {
+      const int jl = it.rt * kTile + row;  // sequence-local key row of this thread
+      const bool valid = jl < it.lkv;
+      const int delta = it.lkv - it.lq;
+      int ilo, ihi;
+      query_interval(jl, delta, it.lq, a.mask, a.window, ilo, ihi);
+      if (!valid) ihi = ilo;  // rows past the sequence contribute nothing
+      const int64_t gk = it.k0 + jl;
+      __nv_bfloat16* dk_row = a.out0 + (gk * a.H + it.h) * D;
+      __nv_bfloat16* dv_row = a.out1 + (gk * a.H + it.h) * D;
+      bool ok = true;
+      for (int i = it.lo; i < it.hi; ++i, ++step) {
+        // this step's log-sum-exp (log2 units) and Di for the 128 query columns
+        float* lse_buf = s_lse + (step & 1) * kTile;
+        float* di_buf = s_di + (step & 1) * kTile;
+        if constexpr (ACT == JATTN_SOFTMAX) {
+          const int iq = i * kTile + tid;
+          float l2 = 0.0f, dd = 0.0f;
+          if (iq < it.lq) {
+            const int64_t gi = (it.q0 + iq) * a.H + it.h;
+            l2 = a.f0[gi] * kLog2e;
+            dd = a.f1[gi];
+          }
+          lse_buf[tid] = l2;
+          di_buf[tid] = dd;
+        }
+        wg_sync();
+        ok = wait_bar(&bars->s_full, s_cnt & 1, abort_flag, a, 60);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        float p[kTile];  // P^T (softmax) or act'(x) (pointwise), fp32
+        {
+          uint32_t* pu = reinterpret_cast<uint32_t*>(p);
+#pragma unroll
+          for (int c = 0; c < kTile / 32; ++c)
+            tmem_ld32(tmem + lane_base + C::kSCol + c * 32, *reinterpret_cast<uint32_t(*)[32]>(pu + c * 32));
+          tmem_ld_wait();
+        }
+        const int clo = ilo - i * kTile, chi = ihi - i * kTile;
+        const bool edge = clo > 0 || chi < kTile;
+#pragma unroll
+        for (int c0 = 0; c0 < kTile; c0 += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int c = c0 + e;
+            float f0, f1;
+            if constexpr (ACT == JATTN_SOFTMAX) {
+              f0 = ex2_approx(fmaf(p[c], a.scale_log2, -lse_buf[c]));
+              f1 = ex2_approx(fmaf(p[c + 1], a.scale_log2, -lse_buf[c + 1]));
+              if (edge) {
+                f0 = (c >= clo && c < chi) ? f0 : 0.0f;
+                f1 = (c + 1 >= clo && c + 1 < chi) ? f1 : 0.0f;
+              }
+              p[c] = f0;
+              p[c + 1] = f1;
+            } else {
+              float g0, g1;
+              act_and_grad<ACT>(p[c] * a.scale, f0, g0);
+              act_and_grad<ACT>(p[c + 1] * a.scale, f1, g1);
+              if (edge) {
+                const bool a0 = c >= clo && c < chi, a1 = c + 1 >= clo && c + 1 < chi;
+                f0 = a0 ? f0 : 0.0f;
+                g0 = a0 ? g0 : 0.0f;
+                f1 = a1 ? f1 : 0.0f;
+                g1 = a1 ? g1 : 0.0f;
+              }
+              p[c] = g0;
+              p[c + 1] = g1;
+            }
+            pk[e / 2] = pack_bf16x2(f0, f1);
+          }
+          tmem_st16(tmem + lane_base + C::kSCol + c0 / 2, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_ready);
+
+        ok = wait_bar(&bars->dp_full, s_cnt & 1, abort_flag, a, 61);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ++s_cnt;
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < kTile; c0 += 32) {
+          uint32_t dp[32];
+          tmem_ld32(tmem + lane_base + C::kDPCol + c0, dp);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int c = c0 + e;
+            float d0, d1;
+            if constexpr (ACT == JATTN_SOFTMAX) {
+              d0 = p[c] * (__uint_as_float(dp[e]) - di_buf[c]);
+              d1 = p[c + 1] * (__uint_as_float(dp[e + 1]) - di_buf[c + 1]);
+            } else {
+              d0 = p[c] * __uint_as_float(dp[e]);
+              d1 = p[c + 1] * __uint_as_float(dp[e + 1]);
+            }
+            pk[e / 2] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(tmem + lane_base + C::kDPCol + c0 / 2, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->ds_ready);
+      }
+      if (!ok) break;
+      const float cn = (ACT != JATTN_SOFTMAX && a.norm_by_lkv && it.lkv > 0) ? 1.0f / it.lkv : 1.0f;
+      if (it.hi > it.lo) {
+        ok = wait_bar(&bars->acc_full, acc_cnt & 1, abort_flag, a, 62);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ++acc_cnt;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + C::kDVCol + c * 32, v);
+          tmem_ld_wait();
+          if (valid) store_row32(dv_row + c * 32, v, cn);
+          tmem_ld32(tmem + lane_base + C::kDKCol + c * 32, v);
+          tmem_ld_wait();
+          if (valid) store_row32(dk_row + c * 32, v, cn * a.scale);
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->acc_empty);
+      } else if (valid) {
+        zero_row(dk_row, D);
+        zero_row(dv_row, D);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------- dQ
+template <int D>
+struct DqCfg {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kQOff = 0;
+  static constexpr int kDOOff = kTileBytes;
+  static constexpr int kKOff = 2 * kTileBytes;  // stage s: K at kKOff + s * 2 tiles, V right after
+  static constexpr int kBarOff = 2 * kTileBytes + kStages * 2 * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  static constexpr uint32_t kSCol = 0, kDPCol = 256, kDQCol = 384;  // S double-buffered at 0 and 128
+};
+
+struct DqBars {
+  uint64_t qd_full, qd_empty;
+  uint64_t kv_full[3], kv_empty[3];
+  uint64_t s_full[2], dp_full, ds_ready, acc_full, acc_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D, int ACT>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+              const AttnArgs a) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DqBars* bars = reinterpret_cast<DqBars*>(sm + C::kBarOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &bars->abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->qd_full, 1);
+    mbar_init(&bars->qd_empty, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->ds_ready, kTile);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, kTile);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t item_cnt = 0, kv_it = 0;
+      bool q_armed = false;
+      BwdItem it;
+      for (long long r = 0; load_bwd_item(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!wait_bar(&bars->qd_empty, (item_cnt & 1) ^ 1, abort_flag, a, 70)) break;
+        ++item_cnt;
+        const int yq = static_cast<int>(it.q0) + it.rt * kTile;
+        if (!(a.debug_flags & 1)) {
+          mbar_arrive_expect_tx(&bars->qd_full, 2 * C::kTileBytes);
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_2d(sm + C::kQOff + c * kTile * 128, &tmQ, &bars->qd_full, it.h * D + c * 64, yq);
+            tma_load_2d(sm + C::kDOOff + c * kTile * 128, &tmDO, &bars->qd_full, it.h * D + c * 64, yq);
+          }
+          q_armed = true;
+        }
+        bool ok = true;
+        for (int j = it.lo; j < it.hi; ++j, ++kv_it) {
+          const int s = kv_it % C::kStages;
+          if (!(ok = wait_bar(&bars->kv_empty[s], ((kv_it / C::kStages) & 1) ^ 1, abort_flag, a, 71))) break;
+          const int yk = static_cast<int>(it.k0) + j * kTile;
+          mbar_arrive_expect_tx(&bars->kv_full[s], 2 * C::kTileBytes);
+          uint8_t* st = sm + C::kKOff + s * 2 * C::kTileBytes;
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_2d(st + c * kTile * 128, &tmK, &bars->kv_full[s], it.h * D + c * 64, yk);
+            tma_load_2d(st + C::kTileBytes + c * kTile * 128, &tmV, &bars->kv_full[s], it.h * D + c * 64, yk);
+          }
+        }
+        if (!ok) break;
+      }
+      if (q_armed) drain_wait(&bars->qd_full, (item_cnt - 1) & 1, a.timeout_ns);
+      for (uint32_t i = (kv_it > (uint32_t)C::kStages ? kv_it - C::kStages : 0); i < kv_it; ++i)
+        drain_wait(&bars->kv_full[i % C::kStages], (i / C::kStages) & 1, a.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kTile, kTile, false, false);
+      constexpr uint32_t idAcc = idesc_bf16_f32(kTile, D, false, true);
+      const uint32_t sQ = smem_u32(sm + C::kQOff), sDO = smem_u32(sm + C::kDOOff), sKV = smem_u32(sm + C::kKOff);
+      uint32_t item_cnt = 0, kv_it = 0, ds_cnt = 0, acc_cnt = 0, step = 0;
+      bool ok = true;
+      BwdItem it;
+      auto sK = [&](int s) { return sKV + s * 2 * C::kTileBytes; };
+      auto sV = [&](int s) { return sKV + s * 2 * C::kTileBytes + C::kTileBytes; };
+      auto kmajor = [](uint32_t base, int kk) {
+        return sdesc_sw128(base + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
+      };
+      auto issue_s = [&](int s, uint32_t st) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::kSCol + (st & 1) * kTile, kmajor(sQ, kk), kmajor(sK(s), kk), idS, kk > 0);
+        mma_commit(&bars->s_full[st & 1]);
+      };
+      auto issue_dp = [&](int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kDPCol, kmajor(sDO, kk), kmajor(sV(s), kk), idS, kk > 0);
+        mma_commit(&bars->dp_full);
+      };
+      for (long long r = 0; ok && load_bwd_item(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!(ok = wait_bar(&bars->qd_full, item_cnt & 1, abort_flag, a, 80))) break;
+        ++item_cnt;
+        tc_fence_after();
+        {
+          const int s = kv_it % C::kStages;
+          if (!(ok = wait_bar(&bars->kv_full[s], (kv_it / C::kStages) & 1, abort_flag, a, 81))) break;
+          tc_fence_after();
+          issue_s(s, step);
+          issue_dp(s);
+        }
+        for (int j = it.lo; j < it.hi; ++j, ++kv_it, ++step) {
+          const int s = kv_it % C::kStages;
+          const bool more = j + 1 < it.hi;
+          const int s1 = (kv_it + 1) % C::kStages;
+          if (more) {
+            if (!(ok = wait_bar(&bars->kv_full[s1], ((kv_it + 1) / C::kStages) & 1, abort_flag, a, 82))) break;
+            tc_fence_after();
+            issue_s(s1, step + 1);
+          }
+          if (j == it.lo) {
+            if (!(ok = wait_bar(&bars->acc_empty, (acc_cnt & 1) ^ 1, abort_flag, a, 83))) break;
+          }
+          if (!(ok = wait_bar(&bars->ds_ready, ds_cnt & 1, abort_flag, a, 84))) break;
+          ++ds_cnt;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tmem + C::kDQCol, tmem + C::kDPCol + kk * 8,
+                   sdesc_sw128(sK(s) + kk * 16 * 128, kTile * 128, 1024), idAcc, (kk > 0 || j > it.lo) ? 1u : 0u);
+          mma_commit(&bars->kv_empty[s]);
+          if (more) issue_dp(s1);
+        }
+        if (!ok) break;
+        mma_commit(&bars->acc_full);
+        ++acc_cnt;
+        mma_commit(&bars->qd_empty);
+      }
+      mma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0, a.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    const int row = 32 * (warp & 3) + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    uint32_t step = 0, dp_cnt = 0, acc_cnt = 0;
+    BwdItem it;
+    for (long long r = 0; load_bwd_item(a, r, it); ++r) {
+      const int il = it.rt * kTile + row;
+      const bool valid = il < it.lq;
+      const int delta = it.lkv - it.lq;
+      int klo, khi;
+      key_interval(il, delta, it.lkv, a.mask, a.window, klo, khi);
+      if (!valid) khi = klo;
+      const int64_t gi = (it.q0 + il) * a.H + it.h;
+      float lse2 = 0.0f, di = 0.0f;
+      if constexpr (ACT == JATTN_SOFTMAX) {
+        if (valid && khi > klo) {
+          lse2 = a.f0[gi] * kLog2e;
+          di = a.f1[gi];
+        }
+      }
+      __nv_bfloat16* dq_row = a.out0 + gi * D;
+      bool ok = true;
+      for (int j = it.lo; j < it.hi; ++j, ++step) {
+        ok = wait_bar(&bars->s_full[step & 1], (step >> 1) & 1, abort_flag, a, 90);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        float p[kTile];
+        {
+          uint32_t* pu = reinterpret_cast<uint32_t*>(p);
+#pragma unroll
+          for (int c = 0; c < kTile / 32; ++c)
+            tmem_ld32(tmem + lane_base + C::kSCol + (step & 1) * kTile + c * 32,
+                      *reinterpret_cast<uint32_t(*)[32]>(pu + c * 32));
+          tmem_ld_wait();
+        }
+        const int clo = klo - j * kTile, chi = khi - j * kTile;
+        const bool edge = clo > 0 || chi < kTile;
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) {
+          float v;
+          if constexpr (ACT == JATTN_SOFTMAX) {
+            v = ex2_approx(fmaf(p[c], a.scale_log2, -lse2));
+          } else {
+            float f;
+            act_and_grad<ACT>(p[c] * a.scale, f, v);
+          }
+          if (edge) v = (c >= clo && c < chi) ? v : 0.0f;
+          p[c] = v;
+        }
+        ok = wait_bar(&bars->dp_full, dp_cnt & 1, abort_flag, a, 91);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ++dp_cnt;
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < kTile; c0 += 32) {
+          uint32_t dp[32];
+          tmem_ld32(tmem + lane_base + C::kDPCol + c0, dp);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int c = c0 + e;
+            float d0, d1;
+            if constexpr (ACT == JATTN_SOFTMAX) {
+              d0 = p[c] * (__uint_as_float(dp[e]) - di);
+              d1 = p[c + 1] * (__uint_as_float(dp[e + 1]) - di);
+            } else {
+              d0 = p[c] * __uint_as_float(dp[e]);
+              d1 = p[c + 1] * __uint_as_float(dp[e + 1]);
+            }
+            pk[e / 2] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(tmem + lane_base + C::kDPCol + c0 / 2, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->ds_ready);
+      }
+      if (!ok) break;
+      const float cn = (ACT != JATTN_SOFTMAX && a.norm_by_lkv && it.lkv > 0) ? 1.0f / it.lkv : 1.0f;
+      if (it.hi > it.lo) {
+        ok = wait_bar(&bars->acc_full, acc_cnt & 1, abort_flag, a, 92);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ++acc_cnt;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + C::kDQCol + c * 32, v);
+          tmem_ld_wait();
+          if (valid) store_row32(dq_row + c * 32, v, cn * a.scale);
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->acc_empty);
+      } else if (valid) {
+        zero_row(dq_row, D);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+template <typename K>
+cudaError_t launch4(K kern, int smem, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                    const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, stream>>>(q, k, v, dout, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_di(const void* o, const void* dout, float* di, int64_t rows, int H, int D,
+                          cudaStream_t stream) {
+  const int64_t n = rows * H;
+  if (n == 0) return cudaSuccess;
+  const int64_t threads = n * (D / 8);
+  const int64_t blocks = (threads + 255) / 256;
+  di_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<const uint4*>(o),
+                                                               static_cast<const uint4*>(dout), di, n, D);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream) {
+  if (D == 128) {
+    constexpr int sm = DkdvCfg<128>::kSmemBytes;
+    if (act == JATTN_SOFTMAX) return launch4(dkdv_kernel<128, JATTN_SOFTMAX>, sm, q, k, v, dout, a, grid, stream);
+    if (act == JATTN_SILU) return launch4(dkdv_kernel<128, JATTN_SILU>, sm, q, k, v, dout, a, grid, stream);
+    return launch4(dkdv_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, a, grid, stream);
+  }
+  constexpr int sm = DkdvCfg<64>::kSmemBytes;
+  if (act == JATTN_SOFTMAX) return launch4(dkdv_kernel<64, JATTN_SOFTMAX>, sm, q, k, v, dout, a, grid, stream);
+  if (act == JATTN_SILU) return launch4(dkdv_kernel<64, JATTN_SILU>, sm, q, k, v, dout, a, grid, stream);
+  return launch4(dkdv_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, a, grid, stream);
+}
+
+cudaError_t launch_bwd_dq(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream) {
+  if (D == 128) {
+    constexpr int sm = DqCfg<128>::kSmemBytes;
+    if (act == JATTN_SOFTMAX) return launch4(dq_kernel<128, JATTN_SOFTMAX>, sm, q, k, v, dout, a, grid, stream);
+    if (act == JATTN_SILU) return launch4(dq_kernel<128, JATTN_SILU>, sm, q, k, v, dout, a, grid, stream);
+    return launch4(dq_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, a, grid, stream);
+  }
+  constexpr int sm = DqCfg<64>::kSmemBytes;
+  if (act == JATTN_SOFTMAX) return launch4(dq_kernel<64, JATTN_SOFTMAX>, sm, q, k, v, dout, a, grid, stream);
+  if (act == JATTN_SILU) return launch4(dq_kernel<64, JATTN_SILU>, sm, q, k, v, dout, a, grid, stream);
+  return launch4(dq_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, a, grid, stream);
+}
+
+}  // namespace jattn

@@ -1,0 +1,126 @@
+// Shared device-side definitions for the jagged attention kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/jattn.h"
+#include "ptx.cuh"
+
+namespace jattn {
+
+constexpr int kTile = 128;        // rows of a Q tile, rows of a K/V tile
+constexpr int kCostBuckets = 1024;  // schedule cost is capped at kCostBuckets - 1
+constexpr int kSchedBlock = 256;    // tiles per block in the schedule kernels
+
+// Status words in the first 256 bytes of the workspace.
+struct DevStatus {
+  int code;    // first error recorded (JATTN_OK when clean)
+  int where;   // which wait / check set it
+  int detail;  // sequence index or other detail
+  int pad;
+};
+
+// Everything a persistent attention kernel needs besides its tensor maps.
+struct AttnArgs {
+  const int64_t* q_off;
+  const int64_t* kv_off;
+  const int4* tiles;       // sorted schedule: (b, row tile, col tile lo, col tile hi)
+  const int* n_tiles;      // device count of tiles
+  int H;
+  int mask;
+  int window;
+  float scale;             // softmax scale applied to q.k
+  float scale_log2;        // scale * log2(e)
+  int norm_by_lkv;
+  // outputs / extra inputs (meaning depends on the kernel)
+  __nv_bfloat16* out0;
+  __nv_bfloat16* out1;
+  float* f0;               // lse (fwd) / lse (bwd)
+  const float* f1;         // Di (bwd)
+  const __nv_bfloat16* in0;
+  const __nv_bfloat16* in1;
+  DevStatus* status;
+  uint64_t timeout_ns;
+  int debug_flags;
+};
+
+// Visible key interval [lo, hi) of sequence-local query row i
+// (bottom-right aligned, delta = Lkv - Lq). Window implies causal.
+__device__ __forceinline__ void key_interval(int i, int delta, int lkv, int mask, int window, int& lo, int& hi) {
+  lo = 0;
+  hi = lkv;
+  if (mask & (JATTN_MASK_CAUSAL | JATTN_MASK_WINDOW)) hi = min(hi, i + delta + 1);
+  if (mask & JATTN_MASK_WINDOW) lo = max(lo, i + delta - window + 1);
+}
+
+// Visible query interval [lo, hi) of sequence-local key row j.
+__device__ __forceinline__ void query_interval(int j, int delta, int lq, int mask, int window, int& lo, int& hi) {
+  lo = 0;
+  hi = lq;
+  if (mask & (JATTN_MASK_CAUSAL | JATTN_MASK_WINDOW)) lo = max(lo, j - delta);
+  if (mask & JATTN_MASK_WINDOW) hi = min(hi, j - delta + window);
+}
+
+// Column-tile range of row tile rt (of row_tile rows) of one sequence (see the interval rules in
+// key_interval / query_interval; both ends are monotone in the row index, so
+// the union over the non-empty rows of a tile is [lo(first), hi(last))).
+__device__ __forceinline__ void tile_range(int lq, int lkv, int rt, int row_tile, int col_tile, int mask,
+                                           int window, int transposed, int& c_lo, int& c_hi) {
+  const int delta = lkv - lq;
+  const bool causal = mask & (JATTN_MASK_CAUSAL | JATTN_MASK_WINDOW);
+  const bool win = mask & JATTN_MASK_WINDOW;
+  const int nrows = transposed ? lkv : lq;
+  const int ncols = transposed ? lq : lkv;
+  int first = rt * row_tile;
+  int last = min((rt + 1) * row_tile, nrows) - 1;
+  c_lo = c_hi = 0;
+  if (ncols == 0 || first > last) return;
+  int lo, hi, lo2, hi2;
+  if (!transposed) {
+    if (causal) first = max(first, -delta);
+    if (win) last = min(last, lkv - 1 - delta + window - 1);
+    if (first > last) return;
+    key_interval(first, delta, lkv, mask, window, lo, hi);
+    key_interval(last, delta, lkv, mask, window, lo2, hi2);
+  } else {
+    if (win) first = max(first, delta - window + 1);
+    if (causal) last = min(last, lq + delta - 1);
+    if (first > last) return;
+    query_interval(first, delta, lq, mask, window, lo, hi);
+    query_interval(last, delta, lq, mask, window, lo2, hi2);
+  }
+  c_lo = lo / col_tile;
+  c_hi = (hi2 + col_tile - 1) / col_tile;
+}
+
+__device__ __forceinline__ void record_error(DevStatus* st, int code, int where, int detail) {
+  if (atomicCAS(&st->code, 0, code) == 0) {
+    st->where = where;
+    st->detail = detail;
+  }
+}
+
+// Bounded mbarrier wait. Returns false (and raises the CTA abort flag and the
+// device status) once `timeout_ns` elapses or another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         const AttnArgs& a, int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > a.timeout_ns) {
+      *abort_flag = 1;
+      record_error(a.status, JATTN_ERR_TIMEOUT, where, blockIdx.x);
+      return false;
+    }
+  }
+}
+
+// Persistent-grid zigzag: the k-th item (k = round * G + pos) processed by CTA g.
+__device__ __forceinline__ long long zigzag_item(long long round, int g, int G) {
+  return round * G + ((round & 1) ? (G - 1 - g) : g);
+}
+
+}  // namespace jattn

@@ -1,0 +1,449 @@
+// Forward pass of jagged generalized dot-product attention on sm_103a.
+//
+// "GEM Training" post, section "Jagged Sequence Flash Attention" (FlashAttention
+// run directly on the unpadded jagged tensors, warp specialisation, TMA and a
+// persistent grid) and section "Generalized Dot-Product Attention" (the same
+// two products with GELU/SiLU in place of softmax, which drops the online
+// correction stage).
+//
+// One persistent CTA per SM walks the longest-first schedule. A work item is
+// (sequence, 256-query block, head): two 128-row query tiles that share every
+// K/V tile the producer streams in. Roles:
+//   warp 0      TMA producer: Q tiles once per item, K/V tiles into a ring
+//   warp 1      tcgen05 issuer: S_t = Q_t K_j^T into TMEM, O_t += P_t V_j
+//               with P_t read straight from TMEM
+//   warps 2-5   activation warpgroup for query tile 0
+//   warps 6-9   activation warpgroup for query tile 1
+// The two activation warpgroups ping-pong: while one turns its S tile into P,
+// the tensor core works on the other tile's products. TMEM columns:
+// [S0 | S1 | O0 | O1]; P_t (bf16 pairs) overwrites the first half of S_t.
+// Softmax rescaling of O is lazy: the running maximum only moves (and O is
+// rescaled in TMEM) when a row's maximum grows by more than 2^8.
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace jattn {
+
+namespace {
+
+constexpr int kNQ = 2;          // query tiles per item
+constexpr int kThreads = 320;   // 10 warps
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kTileBytes = kTile * D * 2;   // one 128-row tile of Q, K or V
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kNQ * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kOCol = 2 * kTile;  // O_t at kOCol + t * D
+};
+
+struct FwdBars {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], v_full[4], kv_empty[4];
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + ex2_approx(-x * 1.4426950408889634f)); }
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float gelu_f(float x) {
+  const float u = 0.7978845608028654f * fmaf(0.044715f * x * x, x, x);
+  return 0.5f * x * (1.0f + tanh_approx(u));
+}
+
+// Wait bounded by time, ignoring the abort flag (teardown of in-flight copies).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+struct ItemInfo {
+  int b, qb, lo, hi, h;
+  int lq, lkv;
+  int64_t q0, k0;
+  int t_lo[kNQ], t_hi[kNQ];  // per query tile key-tile range (empty: lo == hi)
+  bool t_rows[kNQ];          // tile has at least one query row
+};
+
+__device__ __forceinline__ bool load_item(const AttnArgs& a, long long round, ItemInfo& it) {
+  const long long n_items = static_cast<long long>(*a.n_tiles) * a.H;
+  const long long k = zigzag_item(round, blockIdx.x, gridDim.x);
+  if (k >= n_items) return false;
+  const int4 t = a.tiles[k / a.H];
+  it.h = static_cast<int>(k % a.H);
+  it.b = t.x;
+  it.qb = t.y;
+  it.lo = t.z;
+  it.hi = t.w;
+  it.q0 = a.q_off[it.b];
+  it.k0 = a.kv_off[it.b];
+  it.lq = static_cast<int>(a.q_off[it.b + 1] - it.q0);
+  it.lkv = static_cast<int>(a.kv_off[it.b + 1] - it.k0);
+#pragma unroll
+  for (int q = 0; q < kNQ; ++q) {
+    const int rt = it.qb * kNQ + q;
+    it.t_rows[q] = rt * kTile < it.lq;
+    tile_range(it.lq, it.lkv, rt, kTile, kTile, a.mask, a.window, 0, it.t_lo[q], it.t_hi[q]);
+  }
+  return true;
+}
+
+template <int D, int ACT>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  FwdBars* bars = reinterpret_cast<FwdBars*>(sm + C::kBarOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &bars->abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], kTile);
+      mbar_init(&bars->o_full[t], 1);
+      mbar_init(&bars->o_empty[t], kTile);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t kv_it = 0, q_it = 0;
+      bool q_armed = false;
+      ItemInfo it;
+      for (long long r = 0; load_item(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!wait_bar(&bars->q_empty, (q_it & 1) ^ 1, abort_flag, a, 10)) break;
+        if (!(a.debug_flags & 1)) {
+          int nbytes = 0;
+          for (int q = 0; q < kNQ; ++q) nbytes += it.t_rows[q] ? C::kTileBytes : 0;
+          mbar_arrive_expect_tx(&bars->q_full, nbytes);
+          for (int q = 0; q < kNQ; ++q) {
+            if (!it.t_rows[q]) continue;
+            const int y = static_cast<int>(it.q0) + (it.qb * kNQ + q) * kTile;
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_2d(sm + C::kQOff + q * C::kTileBytes + c * kTile * 128, &tmQ, &bars->q_full,
+                          it.h * D + c * 64, y);
+          }
+          q_armed = true;
+        }
+        ++q_it;
+        bool ok = true;
+        for (int j = it.lo; j < it.hi; ++j, ++kv_it) {
+          const int s = kv_it % C::kStages;
+          if (!wait_bar(&bars->kv_empty[s], ((kv_it / C::kStages) & 1) ^ 1, abort_flag, a, 11)) {
+            ok = false;
+            break;
+          }
+          const int y = static_cast<int>(it.k0) + j * kTile;
+          mbar_arrive_expect_tx(&bars->k_full[s], C::kTileBytes);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(sm + C::kKOff + s * C::kTileBytes + c * kTile * 128, &tmK, &bars->k_full[s],
+                        it.h * D + c * 64, y);
+          mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(sm + C::kVOff + s * C::kTileBytes + c * kTile * 128, &tmV, &bars->v_full[s],
+                        it.h * D + c * 64, y);
+        }
+        if (!ok) break;
+      }
+      // Let every copy this thread started land before the CTA can exit.
+      if (q_armed) drain_wait(&bars->q_full, (q_it - 1) & 1, a.timeout_ns);
+      for (uint32_t i = (kv_it > (uint32_t)C::kStages ? kv_it - C::kStages : 0); i < kv_it; ++i) {
+        drain_wait(&bars->k_full[i % C::kStages], (i / C::kStages) & 1, a.timeout_ns);
+        drain_wait(&bars->v_full[i % C::kStages], (i / C::kStages) & 1, a.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kTile, kTile, false, false);
+      constexpr uint32_t idPV = idesc_bf16_f32(kTile, D, false, true);
+      const uint32_t sQ = smem_u32(sm + C::kQOff), sK = smem_u32(sm + C::kKOff), sV = smem_u32(sm + C::kVOff);
+      uint32_t kv_it = 0, q_it = 0, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+      uint32_t k_waited = 0;  // 1 + index of the last K load whose barrier was waited
+      bool ok = true;
+      ItemInfo it;
+      auto issue_s = [&](int q, int stage) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_ss(tmem + q * kTile, sdesc_sw128(sQ + q * C::kTileBytes + off, 16, 1024),
+                 sdesc_sw128(sK + stage * C::kTileBytes + off, 16, 1024), idS, kk > 0);
+        }
+        mma_commit(&bars->s_full[q]);
+      };
+      for (long long r = 0; ok && load_item(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!(ok = wait_bar(&bars->q_full, q_it & 1, abort_flag, a, 20))) break;
+        ++q_it;
+        tc_fence_after();
+        // Each K tile's full barrier is waited exactly once, in load order.
+        auto wait_k = [&](uint32_t idx) -> bool {
+          if (k_waited == idx + 1) return true;
+          if (!wait_bar(&bars->k_full[idx % C::kStages], (idx / C::kStages) & 1, abort_flag, a, 21)) return false;
+          tc_fence_after();
+          k_waited = idx + 1;
+          return true;
+        };
+        if (!(ok = wait_k(kv_it))) break;
+        for (int q = 0; q < kNQ; ++q)
+          if (it.t_lo[q] <= it.lo && it.lo < it.t_hi[q]) issue_s(q, kv_it % C::kStages);
+        for (int j = it.lo; j < it.hi && ok; ++j, ++kv_it) {
+          const int s = kv_it % C::kStages;
+          const int s1 = (kv_it + 1) % C::kStages;
+          if (!(ok = wait_k(kv_it))) break;
+          if (!(ok = wait_bar(&bars->v_full[s], (kv_it / C::kStages) & 1, abort_flag, a, 22))) break;
+          tc_fence_after();
+          for (int q = 0; q < kNQ && ok; ++q) {
+            if (it.t_lo[q] <= j && j < it.t_hi[q]) {
+              if (j == it.t_lo[q]) {
+                if (!(ok = wait_bar(&bars->o_empty[q], (o_cnt[q] & 1) ^ 1, abort_flag, a, 23))) break;
+              }
+              if (!(ok = wait_bar(&bars->p_full[q], p_cnt[q] & 1, abort_flag, a, 24))) break;
+              ++p_cnt[q];
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk) {
+                mma_ts(tmem + C::kOCol + q * D, tmem + q * kTile + kk * 8,
+                       sdesc_sw128(sV + s * C::kTileBytes + kk * 16 * 128, kTile * 128, 1024), idPV,
+                       (kk > 0 || j > it.t_lo[q]) ? 1u : 0u);
+              }
+              if (j + 1 == it.t_hi[q]) {
+                mma_commit(&bars->o_full[q]);
+                ++o_cnt[q];
+              }
+            }
+            if (j + 1 < it.hi && it.t_lo[q] <= j + 1 && j + 1 < it.t_hi[q]) {
+              if (!(ok = wait_k(kv_it + 1))) break;
+              issue_s(q, s1);
+            }
+          }
+          mma_commit(&bars->kv_empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&bars->q_empty);
+      }
+      // Every MMA this thread issued completes before TMEM is released.
+      mma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0, a.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ activation warpgroups
+    const int q = (warp - 2) >> 2;                 // query tile of this warpgroup
+    const int row = 32 * (warp & 3) + lane;         // TMEM lane == tile row
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t tS = tmem + lane_base + q * kTile;
+    const uint32_t tO = tmem + lane_base + C::kOCol + q * D;
+    uint32_t s_cnt = 0, o_cnt = 0;
+    ItemInfo it;
+    for (long long r = 0; load_item(a, r, it); ++r) {
+      if (!it.t_rows[q]) continue;
+      const int row_local = (it.qb * kNQ + q) * kTile + row;
+      const bool valid = row_local < it.lq;
+      const int64_t grow = it.q0 + row_local;
+      const int delta = it.lkv - it.lq;
+      int klo, khi;
+      key_interval(row_local, delta, it.lkv, a.mask, a.window, klo, khi);
+      const int n = (it.hi > it.lo) ? (it.t_hi[q] - it.t_lo[q]) : 0;
+      float m_run = -INFINITY, l_run = 0.0f;
+      bool ok = true;
+      for (int j = it.t_lo[q]; j < it.t_lo[q] + n; ++j) {
+        ok = wait_bar(&bars->s_full[q], s_cnt & 1, abort_flag, a, 30);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ++s_cnt;
+        tc_fence_after();
+        float s[kTile];
+        {
+          uint32_t* su = reinterpret_cast<uint32_t*>(s);
+#pragma unroll
+          for (int c = 0; c < kTile / 32; ++c)
+            tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(su + c * 32));
+          tmem_ld_wait();
+        }
+        const int clo = klo - j * kTile, chi = khi - j * kTile;
+        const bool edge = clo > 0 || chi < kTile;
+        uint32_t pk[kTile / 2];
+        if constexpr (ACT == JATTN_SOFTMAX) {
+          if (edge) {
+#pragma unroll
+            for (int c = 0; c < kTile; ++c) s[c] = (c >= clo && c < chi) ? s[c] : -INFINITY;
+          }
+          float mx = s[0];
+#pragma unroll
+          for (int c = 1; c < kTile; ++c) mx = fmaxf(mx, s[c]);
+          const float m_new = mx * a.scale_log2;
+          bool rescale = false;
+          float alpha = 1.0f;
+          if (m_run == -INFINITY) {
+            m_run = m_new;  // O and l hold nothing yet for this row
+          } else if (m_new > m_run + kRescaleLog2) {
+            alpha = ex2_approx(m_run - m_new);
+            rescale = true;
+            m_run = m_new;
+            l_run *= alpha;
+          }
+          if (__any_sync(0xffffffffu, rescale)) {
+            // The previous P V product of this tile has completed: the S tile
+            // just waited for was issued after it.
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st32(tO + c * 32, o);
+            }
+            tmem_st_wait();
+          }
+          const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
+          float lsum = 0.0f;
+#pragma unroll
+          for (int c = 0; c < kTile; c += 2) {
+            const float p0 = ex2_approx(fmaf(s[c], a.scale_log2, -mref));
+            const float p1 = ex2_approx(fmaf(s[c + 1], a.scale_log2, -mref));
+            lsum += p0 + p1;
+            pk[c / 2] = pack_bf16x2(p0, p1);
+          }
+          l_run += lsum;
+        } else {
+#pragma unroll
+          for (int c = 0; c < kTile; c += 2) {
+            const float x0 = s[c] * a.scale, x1 = s[c + 1] * a.scale;
+            float p0 = (ACT == JATTN_SILU) ? silu_f(x0) : gelu_f(x0);
+            float p1 = (ACT == JATTN_SILU) ? silu_f(x1) : gelu_f(x1);
+            if (edge) {
+              p0 = (c >= clo && c < chi) ? p0 : 0.0f;
+              p1 = (c + 1 >= clo && c + 1 < chi) ? p1 : 0.0f;
+            }
+            pk[c / 2] = pack_bf16x2(p0, p1);
+          }
+        }
+        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(pk));
+        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[q]);
+      }
+      if (!ok) break;
+      // ---------------- epilogue
+      float oscale;
+      if constexpr (ACT == JATTN_SOFTMAX) {
+        oscale = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+      } else {
+        oscale = (a.norm_by_lkv && it.lkv > 0) ? 1.0f / static_cast<float>(it.lkv) : 1.0f;
+      }
+      __nv_bfloat16* orow = a.out0 + (grow * a.H + it.h) * D;
+      if (n > 0) {
+        ok = wait_bar(&bars->o_full[q], o_cnt & 1, abort_flag, a, 31);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ++o_cnt;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * oscale, __uint_as_float(o[2 * e + 1]) * oscale);
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->o_empty[q]);
+      } else if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+        for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+      }
+      if constexpr (ACT == JATTN_SOFTMAX) {
+        if (valid) {
+          const float lse = (l_run > 0.0f) ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+          a.f0[grow * a.H + it.h] = lse;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+}  // namespace
+
+template <int D, int ACT>
+static cudaError_t launch_fwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const AttnArgs& a, int grid, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = fwd_kernel<D, ACT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const AttnArgs& a, int grid, cudaStream_t stream) {
+  if (D == 128) {
+    if (act == JATTN_SOFTMAX) return launch_fwd_t<128, JATTN_SOFTMAX>(q, k, v, a, grid, stream);
+    if (act == JATTN_SILU) return launch_fwd_t<128, JATTN_SILU>(q, k, v, a, grid, stream);
+    return launch_fwd_t<128, JATTN_GELU_TANH>(q, k, v, a, grid, stream);
+  }
+  if (act == JATTN_SOFTMAX) return launch_fwd_t<64, JATTN_SOFTMAX>(q, k, v, a, grid, stream);
+  if (act == JATTN_SILU) return launch_fwd_t<64, JATTN_SILU>(q, k, v, a, grid, stream);
+  return launch_fwd_t<64, JATTN_GELU_TANH>(q, k, v, a, grid, stream);
+}
+
+int fwd_rows_per_item() { return kNQ * kTile; }
+
+}  // namespace jattn

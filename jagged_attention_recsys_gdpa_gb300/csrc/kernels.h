@@ -1,0 +1,25 @@
+// Host-side launchers of the attention kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace jattn {
+
+struct AttnArgs;
+
+// Forward: schedule rows are blocks of fwd_rows_per_item() query rows.
+cudaError_t launch_fwd(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const AttnArgs& a, int grid, cudaStream_t stream);
+int fwd_rows_per_item();
+
+// Backward: Di = rowsum(dO * O) (softmax only).
+cudaError_t launch_bwd_di(const void* o, const void* dout, float* di, int64_t rows, int H, int D,
+                          cudaStream_t stream);
+// dK, dV over key tiles (transposed schedule, 128-row key tiles).
+cudaError_t launch_bwd_dkdv(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream);
+// dQ over query tiles (128-row query tiles).
+cudaError_t launch_bwd_dq(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream);
+
+}  // namespace jattn

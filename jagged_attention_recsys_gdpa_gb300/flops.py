@@ -1,0 +1,53 @@
+"""Work accounting for jagged attention: allowed (query, key) pairs, effective
+FLOPs and algorithmic HBM bytes.
+
+Effective FLOPs count only unpadded, unmasked work, with the usual attention
+convention: forward 4*D per allowed pair and head (two products of 2*D),
+backward 10*D (five products: the score recompute, dP, dV, dK and dQ).
+Activation arithmetic is not counted.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def pairs_per_sequence(lq, lkv, mask: int, window: int) -> np.ndarray:
+    """Allowed (i, j) pairs of each sequence (one head). mask bits: 1 causal, 2 window."""
+    lq = np.asarray(lq, dtype=np.int64)
+    lkv = np.asarray(lkv, dtype=np.int64)
+    out = np.zeros(len(lq), dtype=np.int64)
+    causal = bool(mask & 3)
+    win = bool(mask & 2)
+    for b in range(len(lq)):
+        n, m = int(lq[b]), int(lkv[b])
+        if n == 0 or m == 0:
+            continue
+        i = np.arange(n, dtype=np.int64)
+        delta = m - n
+        hi = np.minimum(m, i + delta + 1) if causal else np.full(n, m, dtype=np.int64)
+        lo = np.maximum(0, i + delta - window + 1) if win else np.zeros(n, dtype=np.int64)
+        out[b] = int(np.maximum(hi - lo, 0).sum())
+    return out
+
+
+def effective_flops(pairs: int, H: int, D: int):
+    """(forward, backward) effective FLOPs for `pairs` allowed pairs per head."""
+    return 4.0 * D * H * pairs, 10.0 * D * H * pairs
+
+
+def kernel_work(total_q: int, total_kv: int, pairs: int, H: int, D: int, softmax: bool):
+    """Algorithmic FLOPs and HBM bytes of each kernel (each byte read or written once).
+
+    forward: reads Q, K, V, writes O (+ LSE)
+    dkdv:    reads Q, K, V, dO (+ LSE, Di), writes dK, dV; products S, dP, dV, dK
+    dq:      reads Q, K, V, dO (+ LSE, Di), writes dQ; the dQ product (its score
+             and dP recompute are not algorithmic work)
+    """
+    e = 2 * H * D  # bytes of one row of a [total, H, D] bf16 tensor
+    stats = 4 * H * total_q
+    return {
+        "fwd": {"flops": 4.0 * D * H * pairs, "bytes": e * (2 * total_q + 2 * total_kv) + (stats if softmax else 0)},
+        "dkdv": {"flops": 8.0 * D * H * pairs,
+                 "bytes": e * (2 * total_q + 4 * total_kv) + (2 * stats if softmax else 0)},
+        "dq": {"flops": 2.0 * D * H * pairs, "bytes": e * (3 * total_q + 2 * total_kv) + (2 * stats if softmax else 0)},
+    }

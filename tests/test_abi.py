@@ -1,0 +1,88 @@
+"""The C-ABI library loads and exports what include/jattn.h declares; host-side
+argument checks return their error codes without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from jagged_attention_recsys_gdpa_gb300 import _binding as B
+from jagged_attention_recsys_gdpa_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "jattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(jattn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("jattn_workspace_size", "jattn_fwd", "jattn_bwd", "jattn_get_status", "jattn_error_string"):
+        assert n in names
+    assert set(names) == set(B.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def _params(**kw):
+    base = dict(B=2, total_q=10, total_kv=10, H=2, D=128, act=0, mask=1, window=0, scale=0.0, norm_by_lkv=0)
+    base.update(kw)
+    return B.params(**base)
+
+
+def test_workspace_size_and_validation(lib):
+    n = B.workspace_size(_params())
+    assert n > 256 and n % 256 == 0
+    bad = [
+        dict(D=96), dict(D=0), dict(H=0), dict(B=0), dict(total_q=-1), dict(act=3), dict(mask=2), dict(mask=3),
+        dict(mask=4), dict(scale=-1.0), dict(scale=float("nan")), dict(act=0, norm_by_lkv=1),
+        dict(total_q=1 << 31),
+    ]
+    for kw in bad:
+        size = ctypes.c_size_t(0)
+        p = _params(**kw)
+        assert lib.jattn_workspace_size(ctypes.byref(p), ctypes.byref(size)) == 1, kw
+    ok = _params(mask=3, window=4)
+    assert B.workspace_size(ok) > 0
+    # softmax needs room for Di; pointwise does not
+    assert B.workspace_size(_params(total_q=100000)) > B.workspace_size(_params(total_q=100000, act=1))
+
+
+def test_host_side_errors_before_any_launch(lib):
+    p = _params()
+    f = 1 << 20  # never dereferenced: every call below must fail on the host first
+    big = 1 << 30
+
+    def fwd(q_off=f, kv_off=f, q=f, k=f, v=f, o=f, lse=f, ws=f, ws_bytes=big, pp=p):
+        return lib.jattn_fwd(ctypes.byref(pp), q_off, kv_off, q, k, v, o, lse, ws, ws_bytes, None)
+
+    assert fwd(q_off=None) == 1
+    assert fwd(q=f + 2) == 4
+    assert fwd(ws=None) == 3
+    assert fwd(ws=f + 16) == 3
+    assert fwd(ws_bytes=64) == 3
+    assert fwd(lse=None) == 1
+    assert fwd(pp=_params(D=80)) == 1
+    pb = _params(D=80)
+    assert lib.jattn_bwd(ctypes.byref(pb), *([f] * 11), f, big, None) == 1
+    assert lib.jattn_bwd(ctypes.byref(p), f, f, f, f, f, f, f, f, f + 8, f, f, f, big, None) == 4
+    assert lib.jattn_bwd(ctypes.byref(p), f, f, f, f, f, None, f, f, f, f, f, f, big, None) == 1
+
+
+def test_error_strings(lib):
+    for code in range(8):
+        assert B.error_string(code)
+    assert B.error_string(99) == "unknown error code"

@@ -1,0 +1,122 @@
+"""CUDA path vs the CPU oracle on the same seeded bf16 inputs, element by
+element, at sizes that span several 128-row tiles with ragged tails."""
+import numpy as np
+import pytest
+import torch
+
+from jagged_attention_recsys_gdpa_gb300 import inputs
+from tests import gpu_helpers as G
+
+pytestmark = pytest.mark.gpu
+
+SOFTMAX, SILU, GELU = 0, 1, 2
+NONE, CAUSAL, WIN = 0, 1, 3
+
+SELF_LENS = [1, 127, 128, 129, 255, 256, 257, 300, 513, 1000]
+CROSS_LQ = [100, 300, 5, 700, 257, 1]
+CROSS_LKV = [20, 128, 1, 257, 130, 64]
+
+
+def _w(act, mask, window, D, H=2, norm=False, std=1.0):
+    return inputs.Workload("case", H, D, act, mask, window, norm, std, True)
+
+
+def _check(w, lq, lkv, seed=0, backward=True):
+    cpu = G.cpu_inputs(w, lq, lkv, seed)
+    g = G.gpu_run(G.to_cuda(cpu), w, backward)
+    r = G.oracle_run(cpu, w, backward)
+    G.compare(g, r, w, backward)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("act", [SOFTMAX, SILU, GELU])
+@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WIN, 1), (WIN, 200)])
+def test_self_attention(act, mask, window, D):
+    norm = act != SOFTMAX
+    _check(_w(act, mask, window, D, norm=norm, std=1.0 if act == SOFTMAX else 0.5), SELF_LENS, SELF_LENS)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("act", [SOFTMAX, SILU, GELU])
+@pytest.mark.parametrize("mask", [NONE, CAUSAL])
+def test_cross_attention(act, mask, D):
+    _check(_w(act, mask, 0, D, norm=act != SOFTMAX), CROSS_LQ, CROSS_LKV, seed=3)
+
+
+@pytest.mark.parametrize("act", [SOFTMAX, GELU])
+def test_pma_short_queries_long_keys(act):
+    lq = [32, 32, 32, 32]
+    lkv = [100, 1000, 3000, 129]
+    _check(_w(act, NONE, 0, 128, H=3, norm=act != SOFTMAX, std=0.5), lq, lkv, seed=5)
+
+
+def test_tiny_config():
+    w = inputs.WORKLOADS["tiny"]
+    lq, lkv = inputs.lengths("tiny")
+    _check(w, lq, lkv, seed=0)
+
+
+@pytest.mark.parametrize("act", [SOFTMAX, SILU])
+def test_empty_and_degenerate_sequences(act):
+    # empty queries, empty keys, a single row, causal with Lq > Lkv (rows that see nothing)
+    lq = [0, 5, 130, 1, 0, 200, 3]
+    lkv = [4, 0, 130, 1, 0, 60, 9]
+    _check(_w(act, CAUSAL, 0, 128, norm=act != SOFTMAX), lq, lkv, seed=7)
+    _check(_w(act, NONE, 0, 64, norm=act != SOFTMAX), lq, lkv, seed=8)
+    _check(_w(act, WIN, 7, 128, norm=act != SOFTMAX), lq, lkv, seed=9)
+
+
+def test_window_at_least_length_equals_causal():
+    w1 = _w(SOFTMAX, CAUSAL, 0, 128)
+    w2 = _w(SOFTMAX, WIN, 5000, 128)
+    cpu = G.cpu_inputs(w1, SELF_LENS, SELF_LENS, 11)
+    a = G.gpu_run(G.to_cuda(cpu), w1)
+    b = G.gpu_run(G.to_cuda(cpu), w2)
+    for k in ("o", "lse", "dq", "dk", "dv"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_deterministic_repeat():
+    w = _w(SOFTMAX, WIN, 100, 128)
+    cpu = G.cpu_inputs(w, SELF_LENS, SELF_LENS, 12)
+    x = G.to_cuda(cpu)
+    a = G.gpu_run(x, w)
+    b = G.gpu_run(x, w)
+    for k in ("o", "lse", "dq", "dk", "dv"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_autograd_function():
+    import jagged_attention_recsys_gdpa_gb300 as J
+
+    w = _w(GELU, NONE, 0, 128, norm=True, std=0.5)
+    cpu = G.cpu_inputs(w, CROSS_LQ, CROSS_LKV, 13)
+    x = G.to_cuda(cpu)
+    q = x["q"].clone().requires_grad_(True)
+    k = x["k"].clone().requires_grad_(True)
+    v = x["v"].clone().requires_grad_(True)
+    o = J.attention(q, k, v, x["q_off"], x["kv_off"], act="gelu", norm_by_lkv=True)
+    o.backward(x["do"])
+    r = G.oracle_run(cpu, w)
+    G.assert_close(G.to64(o), r["o"], "O")
+    G.assert_close(G.to64(q.grad), r["dq"], "dQ")
+    G.assert_close(G.to64(k.grad), r["dk"], "dK")
+    G.assert_close(G.to64(v.grad), r["dv"], "dV")
+
+
+def test_outputs_only_touch_their_rows():
+    """Canary rows around the outputs stay untouched (bounds check of every store)."""
+    import jagged_attention_recsys_gdpa_gb300 as J
+
+    w = _w(SOFTMAX, CAUSAL, 0, 128)
+    cpu = G.cpu_inputs(w, SELF_LENS, SELF_LENS, 14)
+    x = G.to_cuda(cpu)
+    T = x["q"].shape[0]
+    pad = 7
+    big = torch.full((T + 2 * pad, 2, 128), 3.0, dtype=torch.bfloat16, device="cuda")
+    o = big[pad : pad + T]
+    lse_big = torch.full((T + 2 * pad, 2), 5.0, dtype=torch.float32, device="cuda")
+    J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], causal=True, out=o, lse=lse_big[pad : pad + T])
+    torch.cuda.synchronize()
+    assert torch.all(big[:pad] == 3.0) and torch.all(big[pad + T :] == 3.0)
+    assert torch.all(lse_big[:pad] == 5.0) and torch.all(lse_big[pad + T :] == 5.0)
