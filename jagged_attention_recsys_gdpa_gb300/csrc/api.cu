@@ -108,6 +108,9 @@ int device_info(DeviceInfo& out) {
   cudaError_t e0 = cudaGetDevice(&dev);
   if (e0 != cudaSuccess) return cuda_fail("cudaGetDevice", e0);
   if (dev < 0 || dev >= 64) return JATTN_ERR_CUDA;
+  // Make the device's primary context current on this thread (a fresh thread,
+  // e.g. an autograd worker, may have none yet; tensor-map encoding needs it).
+  if ((e0 = cudaSetDevice(dev)) != cudaSuccess) return cuda_fail("cudaSetDevice", e0);
   std::lock_guard<std::mutex> g(g_dev_mu);
   if (!g_dev[dev].ok) {
     int major = 0, minor = 0, sms = 0;

@@ -299,8 +299,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x - 64;  // 0..127 within the warpgroup
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     uint32_t s_cnt = 0, acc_cnt = 0, step = 0;
-    BwdItem it;
-    for (long long r = 0; load_bwd_item(a, r, it); ++r) {
+    BwdItem it, nit;
+    // LSE (log2 units) and Di of query row i*128 + tid of an item, loaded into
+    // registers one step before they are needed.
+    auto fetch = [&](const BwdItem& x, int i, float& l2, float& dd) {
+      l2 = 0.0f;
+      dd = 0.0f;
+      if constexpr (ACT == JATTN_SOFTMAX) {
+        const int iq = i * kTile + tid;
+        if (iq < x.lq) {
+          const int64_t gi = (x.q0 + iq) * a.H + x.h;
+          l2 = a.f0[gi] * kLog2e;
+          dd = a.f1[gi];
+        }
+      }
+    };
+    float pf_l2 = 0.0f, pf_dd = 0.0f;
+    long long pf_item = -1;  // round whose first step the prefetched values belong to
+    bool have = load_bwd_item(a, 0, it);
+    for (long long r = 0; have; ++r, it = nit) {
+      const bool have_next = load_bwd_item(a, r + 1, nit);
+      if (it.hi > it.lo && pf_item != r) fetch(it, it.lo, pf_l2, pf_dd);
       const int jl = it.rt * kTile + row;  // sequence-local key row of this thread
       const bool valid = jl < it.lkv;
       const int delta = it.lkv - it.lq;
@@ -316,17 +335,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* lse_buf = s_lse + (step & 1) * kTile;
         float* di_buf = s_di + (step & 1) * kTile;
         if constexpr (ACT == JATTN_SOFTMAX) {
-          const int iq = i * kTile + tid;
-          float l2 = 0.0f, dd = 0.0f;
-          if (iq < it.lq) {
-            const int64_t gi = (it.q0 + iq) * a.H + it.h;
-            l2 = a.f0[gi] * kLog2e;
-            dd = a.f1[gi];
+          lse_buf[tid] = pf_l2;
+          di_buf[tid] = pf_dd;
+          if (i + 1 < it.hi) {
+            fetch(it, i + 1, pf_l2, pf_dd);
+          } else if (have_next && nit.hi > nit.lo) {
+            fetch(nit, nit.lo, pf_l2, pf_dd);
+            pf_item = r + 1;
           }
-          lse_buf[tid] = l2;
-          di_buf[tid] = dd;
+          wg_sync();
         }
-        wg_sync();
         ok = wait_bar(&bars->s_full, s_cnt & 1, abort_flag, a, 60);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -433,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         zero_row(dk_row, D);
         zero_row(dv_row, D);
       }
+      have = have_next;
     }
   }
 

@@ -8,12 +8,14 @@
 //
 // One persistent CTA per SM walks the longest-first schedule. A work item is
 // (sequence, 256-query block, head): two 128-row query tiles that share every
-// K/V tile the producer streams in. Roles:
-//   warp 0      TMA producer: Q tiles once per item, K/V tiles into a ring
+// K/V tile the producer streams in. Roles (12 warps, three warpgroups):
+//   warp 0      TMA producer: Q tiles once per item, K and V tiles into two
+//               rings (K one tile ahead of V)
 //   warp 1      tcgen05 issuer: S_t = Q_t K_j^T into TMEM, O_t += P_t V_j
 //               with P_t read straight from TMEM
-//   warps 2-5   activation warpgroup for query tile 0
-//   warps 6-9   activation warpgroup for query tile 1
+//   warps 2-3   idle (their warpgroup gives its registers to the others)
+//   warps 4-7   activation warpgroup for query tile 0
+//   warps 8-11  activation warpgroup for query tile 1
 // The two activation warpgroups ping-pong: while one turns its S tile into P,
 // the tensor core works on the other tile's products. TMEM columns:
 // [S0 | S1 | O0 | O1]; P_t (bf16 pairs) overwrites the first half of S_t.
@@ -29,25 +31,30 @@ namespace jattn {
 namespace {
 
 constexpr int kNQ = 2;          // query tiles per item
-constexpr int kThreads = 320;   // 10 warps
+constexpr int kThreads = 384;   // 12 warps: control warpgroup + two activation warpgroups
 constexpr float kRescaleLog2 = 8.0f;
+// Register split (setmaxnreg): 384 threads x 168 at launch = 64512 =
+// 128 x 40 (control warpgroup) + 256 x 232 (activation warpgroups).
+constexpr int kCtlRegs = 104;
+constexpr int kActRegs = 200;
 
 template <int D>
 struct FwdCfg {
   static constexpr int kTileBytes = kTile * D * 2;   // one 128-row tile of Q, K or V
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kKStages = (D == 128) ? 3 : 6;
+  static constexpr int kVStages = (D == 128) ? 2 : 4;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kNQ * kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 2 * kTile;  // O_t at kOCol + t * D
 };
 
 struct FwdBars {
   uint64_t q_full, q_empty;
-  uint64_t k_full[4], v_full[4], kv_empty[4];
+  uint64_t k_full[6], k_empty[6], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -118,10 +125,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -142,18 +152,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  if (warp < 4) {
+  // The register split is set per warpgroup, at the same instruction for all
+  // warps of the warpgroup, in the branch that holds the role's code.
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      uint32_t kv_it = 0, q_it = 0;
-      bool q_armed = false;
+      uint32_t k_it = 0, v_it = 0, q_it = 0;
+      bool q_armed = false, ok = true;
       ItemInfo it;
-      for (long long r = 0; load_item(a, r, it); ++r) {
+      auto load_k = [&](int j) -> bool {
+        const int s = k_it % C::kKStages;
+        if (!wait_bar(&bars->k_empty[s], ((k_it / C::kKStages) & 1) ^ 1, abort_flag, a, 11)) return false;
+        mbar_arrive_expect_tx(&bars->k_full[s], C::kTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(sm + C::kKOff + s * C::kTileBytes + c * kTile * 128, &tmK, &bars->k_full[s],
+                      it.h * D + c * 64, static_cast<int>(it.k0) + j * kTile);
+        ++k_it;
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int s = v_it % C::kVStages;
+        if (!wait_bar(&bars->v_empty[s], ((v_it / C::kVStages) & 1) ^ 1, abort_flag, a, 12)) return false;
+        mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(sm + C::kVOff + s * C::kTileBytes + c * kTile * 128, &tmV, &bars->v_full[s],
+                      it.h * D + c * 64, static_cast<int>(it.k0) + j * kTile);
+        ++v_it;
+        return true;
+      };
+      for (long long r = 0; ok && load_item(a, r, it); ++r) {
         if (it.hi <= it.lo) continue;
-        if (!wait_bar(&bars->q_empty, (q_it & 1) ^ 1, abort_flag, a, 10)) break;
+        if (!(ok = wait_bar(&bars->q_empty, (q_it & 1) ^ 1, abort_flag, a, 10))) break;
         if (!(a.debug_flags & 1)) {
           int nbytes = 0;
           for (int q = 0; q < kNQ; ++q) nbytes += it.t_rows[q] ? C::kTileBytes : 0;
@@ -168,31 +202,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_armed = true;
         }
         ++q_it;
-        bool ok = true;
-        for (int j = it.lo; j < it.hi; ++j, ++kv_it) {
-          const int s = kv_it % C::kStages;
-          if (!wait_bar(&bars->kv_empty[s], ((kv_it / C::kStages) & 1) ^ 1, abort_flag, a, 11)) {
-            ok = false;
-            break;
-          }
-          const int y = static_cast<int>(it.k0) + j * kTile;
-          mbar_arrive_expect_tx(&bars->k_full[s], C::kTileBytes);
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(sm + C::kKOff + s * C::kTileBytes + c * kTile * 128, &tmK, &bars->k_full[s],
-                        it.h * D + c * 64, y);
-          mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(sm + C::kVOff + s * C::kTileBytes + c * kTile * 128, &tmV, &bars->v_full[s],
-                        it.h * D + c * 64, y);
+        // K runs one tile ahead of V: S(j+1) and P(j)V(j) are issued together.
+        if (!(ok = load_k(it.lo))) break;
+        for (int j = it.lo; j < it.hi && ok; ++j) {
+          if (j + 1 < it.hi && !(ok = load_k(j + 1))) break;
+          ok = load_v(j);
         }
-        if (!ok) break;
       }
       // Let every copy this thread started land before the CTA can exit.
       if (q_armed) drain_wait(&bars->q_full, (q_it - 1) & 1, a.timeout_ns);
-      for (uint32_t i = (kv_it > (uint32_t)C::kStages ? kv_it - C::kStages : 0); i < kv_it; ++i) {
-        drain_wait(&bars->k_full[i % C::kStages], (i / C::kStages) & 1, a.timeout_ns);
-        drain_wait(&bars->v_full[i % C::kStages], (i / C::kStages) & 1, a.timeout_ns);
-      }
+      for (uint32_t i = (k_it > (uint32_t)C::kKStages ? k_it - C::kKStages : 0); i < k_it; ++i)
+        drain_wait(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1, a.timeout_ns);
+      for (uint32_t i = (v_it > (uint32_t)C::kVStages ? v_it - C::kVStages : 0); i < v_it; ++i)
+        drain_wait(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1, a.timeout_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -201,16 +223,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idS = idesc_bf16_f32(kTile, kTile, false, false);
       constexpr uint32_t idPV = idesc_bf16_f32(kTile, D, false, true);
       const uint32_t sQ = smem_u32(sm + C::kQOff), sK = smem_u32(sm + C::kKOff), sV = smem_u32(sm + C::kVOff);
-      uint32_t kv_it = 0, q_it = 0, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+      uint32_t k_used = 0, v_used = 0, q_it = 0, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
       uint32_t k_waited = 0;  // 1 + index of the last K load whose barrier was waited
       bool ok = true;
       ItemInfo it;
-      auto issue_s = [&](int q, int stage) {
+      auto wait_k = [&](uint32_t idx) -> bool {
+        if (k_waited == idx + 1) return true;
+        if (!wait_bar(&bars->k_full[idx % C::kKStages], (idx / C::kKStages) & 1, abort_flag, a, 21)) return false;
+        tc_fence_after();
+        k_waited = idx + 1;
+        return true;
+      };
+      auto issue_s = [&](int q, uint32_t kidx) {
+        const uint32_t kb = sK + (kidx % C::kKStages) * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
           mma_ss(tmem + q * kTile, sdesc_sw128(sQ + q * C::kTileBytes + off, 16, 1024),
-                 sdesc_sw128(sK + stage * C::kTileBytes + off, 16, 1024), idS, kk > 0);
+                 sdesc_sw128(kb + off, 16, 1024), idS, kk > 0);
         }
         mma_commit(&bars->s_full[q]);
       };
@@ -219,24 +249,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait_bar(&bars->q_full, q_it & 1, abort_flag, a, 20))) break;
         ++q_it;
         tc_fence_after();
-        // Each K tile's full barrier is waited exactly once, in load order.
-        auto wait_k = [&](uint32_t idx) -> bool {
-          if (k_waited == idx + 1) return true;
-          if (!wait_bar(&bars->k_full[idx % C::kStages], (idx / C::kStages) & 1, abort_flag, a, 21)) return false;
-          tc_fence_after();
-          k_waited = idx + 1;
-          return true;
-        };
-        if (!(ok = wait_k(kv_it))) break;
+        const uint32_t k0 = k_used, v0 = v_used;  // global load indices of this item's first K / V
+        if (!(ok = wait_k(k0))) break;
+#pragma unroll
         for (int q = 0; q < kNQ; ++q)
-          if (it.t_lo[q] <= it.lo && it.lo < it.t_hi[q]) issue_s(q, kv_it % C::kStages);
-        for (int j = it.lo; j < it.hi && ok; ++j, ++kv_it) {
-          const int s = kv_it % C::kStages;
-          const int s1 = (kv_it + 1) % C::kStages;
-          if (!(ok = wait_k(kv_it))) break;
-          if (!(ok = wait_bar(&bars->v_full[s], (kv_it / C::kStages) & 1, abort_flag, a, 22))) break;
+          if (it.t_lo[q] <= it.lo && it.lo < it.t_hi[q]) issue_s(q, k0);
+        mma_commit(&bars->k_empty[k0 % C::kKStages]);
+        // Q is free for the next item once the item's last S product completes.
+        if (it.hi - it.lo == 1) mma_commit(&bars->q_empty);
+        for (int j = it.lo; j < it.hi && ok; ++j) {
+          const uint32_t vi = v0 + (j - it.lo), ki1 = k0 + (j - it.lo) + 1;
+          const int vs = vi % C::kVStages;
+          if (!(ok = wait_bar(&bars->v_full[vs], (vi / C::kVStages) & 1, abort_flag, a, 22))) break;
           tc_fence_after();
-          for (int q = 0; q < kNQ && ok; ++q) {
+          if (j + 1 < it.hi && !(ok = wait_k(ki1))) break;
+#pragma unroll
+          for (int q = 0; q < kNQ; ++q) {
+            if (!ok) break;
             if (it.t_lo[q] <= j && j < it.t_hi[q]) {
               if (j == it.t_lo[q]) {
                 if (!(ok = wait_bar(&bars->o_empty[q], (o_cnt[q] & 1) ^ 1, abort_flag, a, 23))) break;
@@ -247,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < kTile / 16; ++kk) {
                 mma_ts(tmem + C::kOCol + q * D, tmem + q * kTile + kk * 8,
-                       sdesc_sw128(sV + s * C::kTileBytes + kk * 16 * 128, kTile * 128, 1024), idPV,
+                       sdesc_sw128(sV + vs * C::kTileBytes + kk * 16 * 128, kTile * 128, 1024), idPV,
                        (kk > 0 || j > it.t_lo[q]) ? 1u : 0u);
               }
               if (j + 1 == it.t_hi[q]) {
@@ -255,24 +284,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++o_cnt[q];
               }
             }
-            if (j + 1 < it.hi && it.t_lo[q] <= j + 1 && j + 1 < it.t_hi[q]) {
-              if (!(ok = wait_k(kv_it + 1))) break;
-              issue_s(q, s1);
-            }
+            if (j + 1 < it.hi && it.t_lo[q] <= j + 1 && j + 1 < it.t_hi[q]) issue_s(q, ki1);
           }
-          mma_commit(&bars->kv_empty[s]);
+          if (!ok) break;
+          if (j + 1 < it.hi) mma_commit(&bars->k_empty[ki1 % C::kKStages]);
+          if (j + 2 == it.hi) mma_commit(&bars->q_empty);
+          mma_commit(&bars->v_empty[vs]);
         }
         if (!ok) break;
-        mma_commit(&bars->q_empty);
+        k_used += it.hi - it.lo;
+        v_used += it.hi - it.lo;
       }
       // Every MMA this thread issued completes before TMEM is released.
       mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0, a.timeout_ns);
     }
     __syncwarp();
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kActRegs));
     // ------------------------------------------------------------ activation warpgroups
-    const int q = (warp - 2) >> 2;                 // query tile of this warpgroup
+    const int q = (warp - 4) >> 2;                 // query tile of this warpgroup
     const int row = 32 * (warp & 3) + lane;         // TMEM lane == tile row
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tS = tmem + lane_base + q * kTile;
@@ -280,17 +312,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t s_cnt = 0, o_cnt = 0;
     ItemInfo it;
     for (long long r = 0; load_item(a, r, it); ++r) {
-      if (!it.t_rows[q]) continue;
+      const bool has_rows = q ? it.t_rows[1] : it.t_rows[0];
+      const int t_lo = q ? it.t_lo[1] : it.t_lo[0];
+      const int t_hi = q ? it.t_hi[1] : it.t_hi[0];
+      if (!has_rows) continue;
       const int row_local = (it.qb * kNQ + q) * kTile + row;
       const bool valid = row_local < it.lq;
       const int64_t grow = it.q0 + row_local;
       const int delta = it.lkv - it.lq;
       int klo, khi;
       key_interval(row_local, delta, it.lkv, a.mask, a.window, klo, khi);
-      const int n = (it.hi > it.lo) ? (it.t_hi[q] - it.t_lo[q]) : 0;
+      const int n = (it.hi > it.lo) ? (t_hi - t_lo) : 0;
       float m_run = -INFINITY, l_run = 0.0f;
       bool ok = true;
-      for (int j = it.t_lo[q]; j < it.t_lo[q] + n; ++j) {
+      for (int j = t_lo; j < t_lo + n; ++j) {
         ok = wait_bar(&bars->s_full[q], s_cnt & 1, abort_flag, a, 30);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -306,15 +341,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int clo = klo - j * kTile, chi = khi - j * kTile;
         const bool edge = clo > 0 || chi < kTile;
-        uint32_t pk[kTile / 2];
         if constexpr (ACT == JATTN_SOFTMAX) {
           if (edge) {
 #pragma unroll
             for (int c = 0; c < kTile; ++c) s[c] = (c >= clo && c < chi) ? s[c] : -INFINITY;
           }
-          float mx = s[0];
+          // row maximum as a tree over 8 independent partial maxima
+          float mp[8];
 #pragma unroll
-          for (int c = 1; c < kTile; ++c) mx = fmaxf(mx, s[c]);
+          for (int e = 0; e < 8; ++e) mp[e] = s[e];
+#pragma unroll
+          for (int c = 8; c < kTile; c += 8)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mp[e] = fmaxf(mp[e], s[c + e]);
+          const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                 fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
           const float m_new = mx * a.scale_log2;
           bool rescale = false;
           float alpha = 1.0f;
@@ -330,41 +371,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The previous P V product of this tile has completed: the S tile
             // just waited for was issued after it.
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(tO + c * 32, o);
+            for (int c = 0; c < D / 16; ++c) {
+              uint32_t o[16];
+              tmem_ld16(tO + c * 16, o);
               tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tmem_st32(tO + c * 32, o);
+              for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st16(tO + c * 16, o);
             }
             tmem_st_wait();
           }
           const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
-          float lsum = 0.0f;
+          float ls[8];
 #pragma unroll
-          for (int c = 0; c < kTile; c += 2) {
-            const float p0 = ex2_approx(fmaf(s[c], a.scale_log2, -mref));
-            const float p1 = ex2_approx(fmaf(s[c + 1], a.scale_log2, -mref));
-            lsum += p0 + p1;
-            pk[c / 2] = pack_bf16x2(p0, p1);
+          for (int e = 0; e < 8; ++e) ls[e] = 0.0f;
+#pragma unroll
+          for (int c0 = 0; c0 < kTile; c0 += 32) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float p0 = ex2_approx(fmaf(s[c0 + e], a.scale_log2, -mref));
+              const float p1 = ex2_approx(fmaf(s[c0 + e + 1], a.scale_log2, -mref));
+              ls[(e >> 1) & 7] += p0 + p1;
+              pk[e / 2] = pack_bf16x2(p0, p1);
+            }
+            // P columns [c0/2, c0/2+16) only overlap S columns already read
+            tmem_st16(tS + c0 / 2, pk);
           }
-          l_run += lsum;
+          l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         } else {
 #pragma unroll
-          for (int c = 0; c < kTile; c += 2) {
-            const float x0 = s[c] * a.scale, x1 = s[c + 1] * a.scale;
-            float p0 = (ACT == JATTN_SILU) ? silu_f(x0) : gelu_f(x0);
-            float p1 = (ACT == JATTN_SILU) ? silu_f(x1) : gelu_f(x1);
-            if (edge) {
-              p0 = (c >= clo && c < chi) ? p0 : 0.0f;
-              p1 = (c + 1 >= clo && c + 1 < chi) ? p1 : 0.0f;
+          for (int c0 = 0; c0 < kTile; c0 += 32) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const int c = c0 + e;
+              const float x0 = s[c] * a.scale, x1 = s[c + 1] * a.scale;
+              float p0 = (ACT == JATTN_SILU) ? silu_f(x0) : gelu_f(x0);
+              float p1 = (ACT == JATTN_SILU) ? silu_f(x1) : gelu_f(x1);
+              if (edge) {
+                p0 = (c >= clo && c < chi) ? p0 : 0.0f;
+                p1 = (c + 1 >= clo && c + 1 < chi) ? p1 : 0.0f;
+              }
+              pk[e / 2] = pack_bf16x2(p0, p1);
             }
-            pk[c / 2] = pack_bf16x2(p0, p1);
+            tmem_st16(tS + c0 / 2, pk);
           }
         }
-        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(pk));
-        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->p_full[q]);

@@ -24,7 +24,7 @@ def test_bad_offsets_set_status():
     w, x, _ = _small()
     assert J.device_status() in (0, JATTN_ERR_OFFSETS, JATTN_ERR_TIMEOUT)  # clear anything earlier
     bad = x["q_off"].clone()
-    bad[1], bad[2] = bad[2], bad[1]  # non-monotone
+    bad[1] = bad[2] + 1  # offsets decrease from entry 1 to entry 2
     J.forward(x["q"], x["k"], x["v"], bad, bad, causal=True)
     assert J.device_status() == JATTN_ERR_OFFSETS
     end = x["q_off"].clone()
