@@ -67,7 +67,8 @@ enum {
   JATTN_ERR_ALIGN = 4,       /* a value tensor is not 16-byte aligned */
   JATTN_ERR_OFFSETS = 5,     /* device: offsets not a valid prefix sum of the totals */
   JATTN_ERR_TIMEOUT = 6,     /* device: a bounded pipeline wait expired */
-  JATTN_ERR_UNSUPPORTED = 7  /* device is not sm_103 / no kernel image */
+  JATTN_ERR_UNSUPPORTED = 7, /* device is not sm_103 / no kernel image */
+  JATTN_ERR_TOO_LARGE = 8    /* jattn_fwd_noalloc: problem needs more than the library's scratch */
 };
 
 typedef struct {
@@ -134,6 +135,38 @@ const char* jattn_error_string(int code);
 /* For the calling thread: which CUDA step failed most recently and the
  * runtime's message (empty if none). Valid until the next failing call. */
 const char* jattn_last_error(void);
+
+/* Allocation-free forward. No counterpart in the paper: this is a library
+ * service. Some callers cannot allocate device memory at the point where
+ * they run attention: an application whose memory is carved up in advance by
+ * its own pool and that forbids allocations outside it, a plugin invoked by a
+ * host runtime that owns all device memory, or a latency-critical serving
+ * loop that must never block in the allocator. For them this entry point
+ * computes exactly what jattn_fwd computes (same kernels, same results) but
+ * takes no workspace: its scratch (the status word and the tile schedule) is
+ * a fixed array of JATTN_NOALLOC_SCRATCH_BYTES inside the library, which
+ * every GPU that loads the library holds until the process exits. The
+ * caller still owns q, k, v, offsets, o and lse (same layout and rules as
+ * jattn_fwd) and may pass `device_status`, a device int that receives the
+ * status word (JATTN_OK / JATTN_ERR_OFFSETS / JATTN_ERR_TIMEOUT) once the
+ * call's work on `stream` completes; NULL skips it.
+ *
+ * Limits and rules:
+ *  - The schedule needs about 48 bytes per 256 query rows plus 4 bytes per
+ *    sequence: 256 + 4*(B+1) + 48*(total_q/256 + B + 1) bytes, rounded up
+ *    per buffer. Calls that need more return JATTN_ERR_TOO_LARGE (and
+ *    jattn_last_error says how much) without launching anything.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call reuses the same array; each call clears the status word
+ *    first. Calls whose work overlaps on the GPU (other streams, other host
+ *    threads) race on the array: serialise them.
+ *  - No cudaMalloc, cudaFree or other allocating call is made. */
+#define JATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+int jattn_fwd_noalloc(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
+                      const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse, int* device_status,
+                      void* stream);
 
 /* Profiling hook: `events` points to six cudaEvent_t (passed as void*) that
  * later calls record on their stream right before and right after the

@@ -18,6 +18,7 @@ MASK_NONE, MASK_CAUSAL, MASK_WINDOW = 0, 1, 2
 EXPORTED = (
     "jattn_workspace_size",
     "jattn_fwd",
+    "jattn_fwd_noalloc",
     "jattn_bwd",
     "jattn_schedule",
     "jattn_max_tiles",
@@ -48,7 +49,7 @@ class JattnError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
         detail = ""
-        if code == 2:
+        if code in (2, 8):
             detail = " [" + load().jattn_last_error().decode() + "]"
         super().__init__(f"{where}: {error_string(code)} (code {code}){detail}")
 
@@ -78,6 +79,8 @@ def load(path: str | None = None):
     lib.jattn_workspace_size.restype = i32
     lib.jattn_fwd.argtypes = [P] + [vp] * 7 + [vp, ctypes.c_size_t, vp]
     lib.jattn_fwd.restype = i32
+    lib.jattn_fwd_noalloc.argtypes = [P] + [vp] * 8 + [vp]
+    lib.jattn_fwd_noalloc.restype = i32
     lib.jattn_bwd.argtypes = [P] + [vp] * 11 + [vp, ctypes.c_size_t, vp]
     lib.jattn_bwd.restype = i32
     lib.jattn_schedule.argtypes = [P, vp, vp, i32, i32, i32, vp, i64, vp, vp, ctypes.c_size_t, vp]
@@ -125,6 +128,12 @@ def ptr(t) -> int | None:
 def fwd(p: Params, q_off, kv_off, q, k, v, o, lse, ws, ws_bytes: int, stream: int):
     check(load().jattn_fwd(ctypes.byref(p), ptr(q_off), ptr(kv_off), ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse),
                            ws, ws_bytes, stream), "jattn_fwd")
+
+
+def fwd_noalloc(p: Params, q_off, kv_off, q, k, v, o, lse, device_status, stream: int):
+    """Forward without a workspace (scratch held by the library); see jattn_fwd_noalloc."""
+    check(load().jattn_fwd_noalloc(ctypes.byref(p), ptr(q_off), ptr(kv_off), ptr(q), ptr(k), ptr(v), ptr(o),
+                                   ptr(lse), ptr(device_status), stream), "jattn_fwd_noalloc")
 
 
 def bwd(p: Params, q_off, kv_off, q, k, v, o, lse, do, dq, dk, dv, ws, ws_bytes: int, stream: int):

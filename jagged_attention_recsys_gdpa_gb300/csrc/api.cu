@@ -178,6 +178,38 @@ int grid_for(const DeviceInfo& d, int64_t max_tiles, int H) {
 }  // namespace
 }  // namespace jattn
 
+// ---------------------------------------------------------------- allocation-free forward
+// Scratch of jattn_fwd_noalloc (status word + forward tile schedule), held in
+// the library's own device memory so that its callers allocate nothing.
+static __device__ __align__(256) unsigned char jattn_noalloc_scratch[JATTN_NOALLOC_SCRATCH_BYTES];
+
+namespace jattn {
+namespace {
+
+// Device address of the scratch array, looked up once per device (with that
+// device current). Host code may not use the symbol itself as an address.
+void* g_noalloc_addr[64] = {};
+std::mutex g_noalloc_mu;
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  if (dev < 0 || dev >= 64) return JATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> g(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, jattn_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = g_noalloc_addr[dev];
+  return JATTN_OK;
+}
+
+}  // namespace
+}  // namespace jattn
+
 using namespace jattn;
 
 extern "C" {
@@ -231,6 +263,56 @@ int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
   if ((e = launch_fwd(p->D, p->act, mq, mk, mv, a, grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
     return cuda_fail("forward kernel launch", e);
   prof(1, st);
+  return JATTN_OK;
+}
+
+int jattn_fwd_noalloc(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
+                      const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse, int* device_status,
+                      void* stream) {
+  int rc = check_params(p);
+  if (rc != JATTN_OK) return rc;
+  if (!q_off || !kv_off) return JATTN_ERR_INVALID;
+  if ((p->total_q > 0 && (!q || !o)) || (p->total_kv > 0 && (!k || !v))) return JATTN_ERR_INVALID;
+  if (p->act == JATTN_SOFTMAX && p->total_q > 0 && !lse) return JATTN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return JATTN_ERR_ALIGN;
+  const Layout L = layout_for(*p);
+  const size_t need = 256 + sched_ws_bytes(p->B, L.tiles_fwd);
+  if (need > JATTN_NOALLOC_SCRATCH_BYTES) {
+    snprintf(g_last_error, sizeof(g_last_error), "jattn_fwd_noalloc needs %zu bytes of scratch; the library holds %zu",
+             need, static_cast<size_t>(JATTN_NOALLOC_SCRATCH_BYTES));
+    return JATTN_ERR_TOO_LARGE;
+  }
+  DeviceInfo dev;
+  if ((rc = device_info(dev)) != JATTN_OK) return rc;
+  if ((rc = encoder()) != JATTN_OK) return rc;
+  void* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch)) != JATTN_OK) return rc;
+  clear_stale_error();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  // The status word must start at zero; the schedule buffers are fully rewritten.
+  if ((e = cudaMemsetAsync(scratch, 0, 256, st)) != cudaSuccess) return cuda_fail("status clear", e);
+  if (p->total_q > 0) {
+    char* base = static_cast<char*>(scratch);
+    const SchedView sv = sched_carve(base + 256, p->B, L.tiles_fwd);
+    AttnArgs a = base_args(*p, q_off, kv_off, scratch);
+    if ((e = sched_launch(sv, q_off, kv_off, p->B, p->total_q, p->total_kv, fwd_rows_per_item(), kTile, p->mask,
+                          a.window, 0, a.status, st)) != cudaSuccess)
+      return cuda_fail("schedule launch", e);
+    CUtensorMap mq, mk, mv;
+    if (make_map(&mq, q, p->total_q, p->H, p->D) || make_map(&mk, k, p->total_kv, p->H, p->D) ||
+        make_map(&mv, v, p->total_kv, p->H, p->D))
+      return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+    a.tiles = sv.sorted;
+    a.n_tiles = sv.n_tiles;
+    a.out0 = reinterpret_cast<__nv_bfloat16*>(o);
+    a.f0 = lse;
+    if ((e = launch_fwd(p->D, p->act, mq, mk, mv, a, grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
+      return cuda_fail("forward kernel launch", e);
+  }
+  if (device_status &&
+      (e = cudaMemcpyAsync(device_status, scratch, sizeof(int), cudaMemcpyDeviceToDevice, st)) != cudaSuccess)
+    return cuda_fail("status copy", e);
   return JATTN_OK;
 }
 
@@ -345,6 +427,7 @@ const char* jattn_error_string(int code) {
     case JATTN_ERR_OFFSETS: return "offsets are not a valid prefix sum of the row totals";
     case JATTN_ERR_TIMEOUT: return "a bounded pipeline wait expired";
     case JATTN_ERR_UNSUPPORTED: return "device is not sm_103";
+    case JATTN_ERR_TOO_LARGE: return "problem needs more scratch than the allocation-free entry point holds";
     default: return "unknown error code";
   }
 }

@@ -82,7 +82,15 @@ def test_host_side_errors_before_any_launch(lib):
     assert lib.jattn_bwd(ctypes.byref(p), f, f, f, f, f, None, f, f, f, f, f, f, big, None) == 1
 
 
+def test_noalloc_rejects_problems_beyond_its_scratch(lib):
+    f = 1 << 20  # never dereferenced: the size check comes before any device work
+    p = _params(B=1, total_q=1 << 30, total_kv=16)
+    rc = lib.jattn_fwd_noalloc(ctypes.byref(p), f, f, f, f, f, f, f, None, None)
+    assert rc == 8
+    assert b"bytes of scratch" in lib.jattn_last_error()
+
+
 def test_error_strings(lib):
-    for code in range(8):
+    for code in range(9):
         assert B.error_string(code)
     assert B.error_string(99) == "unknown error code"
