@@ -11,9 +11,12 @@
 //   dq    one item = (sequence, 128-query tile, head); walks its key tiles:
 //         S = Q K^T, dP = dO V^T, dS, dQ += dS K
 // Both MMA kernels are persistent and warp-specialised: warp 0 issues TMA
-// copies, warp 1 issues tcgen05 MMAs, warps 2-5 (one TMEM lane per thread)
-// apply the activation and its derivative and write P / dS back to TMEM as
-// bf16, where the next MMA reads them as its A operand.
+// copies, warp 1 issues tcgen05 MMAs, and two activation warpgroups (warps
+// 4-7 and 8-11; one TMEM lane per thread) split every 128-column score tile
+// in halves, apply the activation and its derivative, and write P / dS back
+// to TMEM as bf16 in their own column ranges, where the next MMA reads them
+// as its A operand. Two warps per scheduler hide the latency of the
+// transcendental and conversion instructions that one warp cannot.
 #include <cstdint>
 
 #include "common.cuh"
@@ -23,7 +26,13 @@ namespace jattn {
 
 namespace {
 
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 2-3 idle, warps 4-7 and 8-11 activation
+// Register split (setmaxnreg, per warpgroup): 384 x 168 at launch = 64512 =
+// 128 x 104 (control warpgroup) + 256 x 200 (activation warpgroups).
+constexpr int kCtlRegs = 104;
+constexpr int kActRegs = 200;
+constexpr int kNG = 2;          // activation warpgroups; they split each score tile's columns
+constexpr int kCols = kTile / kNG;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
@@ -33,7 +42,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
-__device__ __forceinline__ void wg_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier of one activation warpgroup (ids 1 and 2).
+__device__ __forceinline__ void wg_sync(int g) { asm volatile("bar.sync %0, 128;" ::"r"(g + 1) : "memory"); }
 
 __device__ __forceinline__ float tanh_approx(float x) {
   float y;
@@ -120,14 +130,18 @@ __global__ void __launch_bounds__(256) di_kernel(const uint4* __restrict__ o, co
 }
 
 // ---------------------------------------------------------------------------- dK / dV
+// TMEM address of the A operand for K-step kk of a 128-column score tile
+// whose bf16 pairs were written by the two activation warpgroups: group g
+// packs score columns [64g, 64g+64) into TMEM columns [base+64g, base+64g+32).
+__device__ __forceinline__ uint32_t split_a(uint32_t base, int kk) { return base + (kk >> 2) * 64 + (kk & 3) * 8; }
+
 template <int D>
 struct DkdvCfg {
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kStages = (D == 128) ? 2 : 3;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kTileBytes;
-  static constexpr int kQOff = 2 * kTileBytes;                          // stage s: Q at kQOff + s * 2 tiles
-  static constexpr int kDOOff = 3 * kTileBytes;                         //          dO right after Q
+  static constexpr int kQOff = 2 * kTileBytes;                               // stage s: Q, then dO
   static constexpr int kLseOff = 2 * kTileBytes + kStages * 2 * kTileBytes;  // [2][128] lse2, [2][128] Di
   static constexpr int kBarOff = kLseOff + 4 * kTile * 4;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
@@ -166,10 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_ready, kTile);
-    mbar_init(&bars->ds_ready, kTile);
+    mbar_init(&bars->p_ready, kNG * kTile);
+    mbar_init(&bars->ds_ready, kNG * kTile);
     mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, kTile);
+    mbar_init(&bars->acc_empty, kNG * kTile);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -183,14 +197,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
   if (warp == 0) {
     if (lane == 0) {
       uint32_t item_cnt = 0, qd_it = 0;
-      bool kv_armed = false;
-      BwdItem it;
-      for (long long r = 0; load_bwd_item(a, r, it); ++r) {
+      bool kv_armed = false, ok = true;
+      BwdItem it, nit;
+      bool have = load_bwd_item(a, 0, it), have_next = false;
+      for (long long r = 0; have && ok; ++r, it = nit, have = have_next) {
+        have_next = load_bwd_item(a, r + 1, nit);  // in flight while this item is served
         if (it.hi <= it.lo) continue;
-        if (!wait_bar(&bars->kv_empty, (item_cnt & 1) ^ 1, abort_flag, a, 40)) break;
+        if (!(ok = wait_bar(&bars->kv_empty, (item_cnt & 1) ^ 1, abort_flag, a, 40))) break;
         ++item_cnt;
         const int yk = static_cast<int>(it.k0) + it.rt * kTile;
         if (!(a.debug_flags & 1)) {
@@ -201,7 +219,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           kv_armed = true;
         }
-        bool ok = true;
         for (int i = it.lo; i < it.hi; ++i, ++qd_it) {
           const int s = qd_it % C::kStages;
           if (!(ok = wait_bar(&bars->qd_empty[s], ((qd_it / C::kStages) & 1) ^ 1, abort_flag, a, 41))) break;
@@ -213,7 +230,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(st + C::kTileBytes + c * kTile * 128, &tmDO, &bars->qd_full[s], it.h * D + c * 64, yq);
           }
         }
-        if (!ok) break;
       }
       if (kv_armed) drain_wait(&bars->kv_full, (item_cnt - 1) & 1, a.timeout_ns);
       for (uint32_t i = (qd_it > (uint32_t)C::kStages ? qd_it - C::kStages : 0); i < qd_it; ++i)
@@ -228,7 +244,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sQ0 = smem_u32(sm + C::kQOff);
       uint32_t item_cnt = 0, qd_it = 0, p_cnt = 0, ds_cnt = 0, acc_cnt = 0;
       bool ok = true;
-      BwdItem it;
       auto sQ = [&](int s) { return sQ0 + s * 2 * C::kTileBytes; };
       auto sDO = [&](int s) { return sQ0 + s * 2 * C::kTileBytes + C::kTileBytes; };
       auto kmajor = [](uint32_t base, int kk) {
@@ -244,7 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kDPCol, kmajor(sV, kk), kmajor(sDO(s), kk), idS, kk > 0);
         mma_commit(&bars->dp_full);
       };
-      for (long long r = 0; ok && load_bwd_item(a, r, it); ++r) {
+      BwdItem it, nit;
+      bool have = load_bwd_item(a, 0, it), have_next = false;
+      for (long long r = 0; have && ok; ++r, it = nit, have = have_next) {
+        have_next = load_bwd_item(a, r + 1, nit);
         if (it.hi <= it.lo) continue;
         if (!(ok = wait_bar(&bars->kv_full, item_cnt & 1, abort_flag, a, 50))) break;
         ++item_cnt;
@@ -268,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + C::kDVCol, tmem + C::kSCol + kk * 8,
+            mma_ts(tmem + C::kDVCol, split_a(tmem + C::kSCol, kk),
                    sdesc_sw128(sDO(s) + kk * 16 * 128, kTile * 128, 1024), idAcc, (kk > 0 || i > it.lo) ? 1u : 0u);
           if (more) {
             if (!(ok = wait_bar(&bars->qd_full[s1], ((qd_it + 1) / C::kStages) & 1, abort_flag, a, 54))) break;
@@ -280,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + C::kDKCol, tmem + C::kDPCol + kk * 8,
+            mma_ts(tmem + C::kDKCol, split_a(tmem + C::kDPCol, kk),
                    sdesc_sw128(sQ(s) + kk * 16 * 128, kTile * 128, 1024), idAcc, (kk > 0 || i > it.lo) ? 1u : 0u);
           mma_commit(&bars->qd_empty[s]);
           if (more) issue_dp(s1);
@@ -294,20 +312,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(&bars->drain, 0, a.timeout_ns);
     }
     __syncwarp();
+  }
   } else {
-    const int row = 32 * (warp & 3) + lane;
-    const int tid = threadIdx.x - 64;  // 0..127 within the warpgroup
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kActRegs));
+    const int g = (warp - 4) >> 2;                   // activation group: score columns [64g, 64g+64)
+    const int gt = threadIdx.x - 128 - kTile * g;    // 0..127 within the group
+    const int row = 32 * (warp & 3) + lane;          // TMEM lane == key row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t tSg = tmem + lane_base + C::kSCol + kCols * g;
+    const uint32_t tDPg = tmem + lane_base + C::kDPCol + kCols * g;
     uint32_t s_cnt = 0, acc_cnt = 0, step = 0;
-    BwdItem it, nit;
-    // LSE (log2 units) and Di of query row i*128 + tid of an item, loaded into
-    // registers one step before they are needed.
+    // LSE (log2 units) and Di of query row i*128 + 64g + gt (gt < 64) of an
+    // item, loaded into registers one step before they are needed.
     auto fetch = [&](const BwdItem& x, int i, float& l2, float& dd) {
       l2 = 0.0f;
       dd = 0.0f;
       if constexpr (ACT == JATTN_SOFTMAX) {
-        const int iq = i * kTile + tid;
-        if (iq < x.lq) {
+        const int iq = i * kTile + kCols * g + gt;
+        if (gt < kCols && iq < x.lq) {
           const int64_t gi = (x.q0 + iq) * a.H + x.h;
           l2 = a.f0[gi] * kLog2e;
           dd = a.f1[gi];
@@ -316,9 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     float pf_l2 = 0.0f, pf_dd = 0.0f;
     long long pf_item = -1;  // round whose first step the prefetched values belong to
-    bool have = load_bwd_item(a, 0, it);
-    for (long long r = 0; have; ++r, it = nit) {
-      const bool have_next = load_bwd_item(a, r + 1, nit);
+    BwdItem it, nit;
+    bool have = load_bwd_item(a, 0, it), have_next = false;
+    for (long long r = 0; have; ++r, it = nit, have = have_next) {
+      have_next = load_bwd_item(a, r + 1, nit);
       if (it.hi > it.lo && pf_item != r) fetch(it, it.lo, pf_l2, pf_dd);
       const int jl = it.rt * kTile + row;  // sequence-local key row of this thread
       const bool valid = jl < it.lkv;
@@ -327,40 +350,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       query_interval(jl, delta, it.lq, a.mask, a.window, ilo, ihi);
       if (!valid) ihi = ilo;  // rows past the sequence contribute nothing
       const int64_t gk = it.k0 + jl;
-      __nv_bfloat16* dk_row = a.out0 + (gk * a.H + it.h) * D;
-      __nv_bfloat16* dv_row = a.out1 + (gk * a.H + it.h) * D;
+      __nv_bfloat16* out_row = (g == 0 ? a.out1 : a.out0) + (gk * a.H + it.h) * D;  // group 0: dV, 1: dK
       bool ok = true;
       for (int i = it.lo; i < it.hi; ++i, ++step) {
-        // this step's log-sum-exp (log2 units) and Di for the 128 query columns
-        float* lse_buf = s_lse + (step & 1) * kTile;
-        float* di_buf = s_di + (step & 1) * kTile;
+        float* lse_buf = s_lse + (step & 1) * kTile + kCols * g;
+        float* di_buf = s_di + (step & 1) * kTile + kCols * g;
         if constexpr (ACT == JATTN_SOFTMAX) {
-          lse_buf[tid] = pf_l2;
-          di_buf[tid] = pf_dd;
+          if (gt < kCols) {
+            lse_buf[gt] = pf_l2;
+            di_buf[gt] = pf_dd;
+          }
           if (i + 1 < it.hi) {
             fetch(it, i + 1, pf_l2, pf_dd);
           } else if (have_next && nit.hi > nit.lo) {
             fetch(nit, nit.lo, pf_l2, pf_dd);
             pf_item = r + 1;
           }
-          wg_sync();
+          wg_sync(g);
         }
         ok = wait_bar(&bars->s_full, s_cnt & 1, abort_flag, a, 60);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        float p[kTile];  // P^T (softmax) or act'(x) (pointwise), fp32
+        float p[kCols];  // P^T (softmax) or act'(x) (pointwise) of this group's columns, fp32
         {
           uint32_t* pu = reinterpret_cast<uint32_t*>(p);
 #pragma unroll
-          for (int c = 0; c < kTile / 32; ++c)
-            tmem_ld32(tmem + lane_base + C::kSCol + c * 32, *reinterpret_cast<uint32_t(*)[32]>(pu + c * 32));
+          for (int c = 0; c < kCols / 32; ++c)
+            tmem_ld32(tSg + c * 32, *reinterpret_cast<uint32_t(*)[32]>(pu + c * 32));
           tmem_ld_wait();
         }
-        const int clo = ilo - i * kTile, chi = ihi - i * kTile;
-        const bool edge = clo > 0 || chi < kTile;
+        const int clo = ilo - i * kTile - kCols * g, chi = ihi - i * kTile - kCols * g;
+        const bool edge = clo > 0 || chi < kCols;
 #pragma unroll
-        for (int c0 = 0; c0 < kTile; c0 += 32) {
+        for (int c0 = 0; c0 < kCols; c0 += 32) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
@@ -391,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pk[e / 2] = pack_bf16x2(f0, f1);
           }
-          tmem_st16(tmem + lane_base + C::kSCol + c0 / 2, pk);
+          tmem_st16(tSg + c0 / 2, pk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -402,26 +425,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++s_cnt;
         tc_fence_after();
+        {
+          uint32_t dp[kCols];
 #pragma unroll
-        for (int c0 = 0; c0 < kTile; c0 += 32) {
-          uint32_t dp[32];
-          tmem_ld32(tmem + lane_base + C::kDPCol + c0, dp);
+          for (int c = 0; c < kCols / 32; ++c) tmem_ld32(tDPg + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dp + c * 32));
           tmem_ld_wait();
-          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int c = c0 + e;
-            float d0, d1;
-            if constexpr (ACT == JATTN_SOFTMAX) {
-              d0 = p[c] * (__uint_as_float(dp[e]) - di_buf[c]);
-              d1 = p[c + 1] * (__uint_as_float(dp[e + 1]) - di_buf[c + 1]);
-            } else {
-              d0 = p[c] * __uint_as_float(dp[e]);
-              d1 = p[c + 1] * __uint_as_float(dp[e + 1]);
+          for (int c0 = 0; c0 < kCols; c0 += 32) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const int c = c0 + e;
+              float d0, d1;
+              if constexpr (ACT == JATTN_SOFTMAX) {
+                d0 = p[c] * (__uint_as_float(dp[c]) - di_buf[c]);
+                d1 = p[c + 1] * (__uint_as_float(dp[c + 1]) - di_buf[c + 1]);
+              } else {
+                d0 = p[c] * __uint_as_float(dp[c]);
+                d1 = p[c + 1] * __uint_as_float(dp[c + 1]);
+              }
+              pk[e / 2] = pack_bf16x2(d0, d1);
             }
-            pk[e / 2] = pack_bf16x2(d0, d1);
+            tmem_st16(tDPg + c0 / 2, pk);
           }
-          tmem_st16(tmem + lane_base + C::kDPCol + c0 / 2, pk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -435,23 +461,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++acc_cnt;
         tc_fence_after();
+        const uint32_t tAcc = tmem + lane_base + (g == 0 ? C::kDVCol : C::kDKCol);
+        const float mul = (g == 0) ? cn : cn * a.scale;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_base + C::kDVCol + c * 32, v);
+          tmem_ld32(tAcc + c * 32, v);
           tmem_ld_wait();
-          if (valid) store_row32(dv_row + c * 32, v, cn);
-          tmem_ld32(tmem + lane_base + C::kDKCol + c * 32, v);
-          tmem_ld_wait();
-          if (valid) store_row32(dk_row + c * 32, v, cn * a.scale);
+          if (valid) store_row32(out_row + c * 32, v, mul);
         }
         tc_fence_before();
         mbar_arrive(&bars->acc_empty);
       } else if (valid) {
-        zero_row(dk_row, D);
-        zero_row(dv_row, D);
+        zero_row(out_row, D);
       }
-      have = have_next;
     }
   }
 
@@ -504,9 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->s_full[0], 1);
     mbar_init(&bars->s_full[1], 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->ds_ready, kTile);
+    mbar_init(&bars->ds_ready, kNG * kTile);
     mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, kTile);
+    mbar_init(&bars->acc_empty, kNG * kTile);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -520,14 +543,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
   if (warp == 0) {
     if (lane == 0) {
       uint32_t item_cnt = 0, kv_it = 0;
-      bool q_armed = false;
-      BwdItem it;
-      for (long long r = 0; load_bwd_item(a, r, it); ++r) {
+      bool q_armed = false, ok = true;
+      BwdItem it, nit;
+      bool have = load_bwd_item(a, 0, it), have_next = false;
+      for (long long r = 0; have && ok; ++r, it = nit, have = have_next) {
+        have_next = load_bwd_item(a, r + 1, nit);
         if (it.hi <= it.lo) continue;
-        if (!wait_bar(&bars->qd_empty, (item_cnt & 1) ^ 1, abort_flag, a, 70)) break;
+        if (!(ok = wait_bar(&bars->qd_empty, (item_cnt & 1) ^ 1, abort_flag, a, 70))) break;
         ++item_cnt;
         const int yq = static_cast<int>(it.q0) + it.rt * kTile;
         if (!(a.debug_flags & 1)) {
@@ -538,7 +565,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           q_armed = true;
         }
-        bool ok = true;
         for (int j = it.lo; j < it.hi; ++j, ++kv_it) {
           const int s = kv_it % C::kStages;
           if (!(ok = wait_bar(&bars->kv_empty[s], ((kv_it / C::kStages) & 1) ^ 1, abort_flag, a, 71))) break;
@@ -550,7 +576,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(st + C::kTileBytes + c * kTile * 128, &tmV, &bars->kv_full[s], it.h * D + c * 64, yk);
           }
         }
-        if (!ok) break;
       }
       if (q_armed) drain_wait(&bars->qd_full, (item_cnt - 1) & 1, a.timeout_ns);
       for (uint32_t i = (kv_it > (uint32_t)C::kStages ? kv_it - C::kStages : 0); i < kv_it; ++i)
@@ -564,7 +589,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sQ = smem_u32(sm + C::kQOff), sDO = smem_u32(sm + C::kDOOff), sKV = smem_u32(sm + C::kKOff);
       uint32_t item_cnt = 0, kv_it = 0, ds_cnt = 0, acc_cnt = 0, step = 0;
       bool ok = true;
-      BwdItem it;
       auto sK = [&](int s) { return sKV + s * 2 * C::kTileBytes; };
       auto sV = [&](int s) { return sKV + s * 2 * C::kTileBytes + C::kTileBytes; };
       auto kmajor = [](uint32_t base, int kk) {
@@ -581,7 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kDPCol, kmajor(sDO, kk), kmajor(sV(s), kk), idS, kk > 0);
         mma_commit(&bars->dp_full);
       };
-      for (long long r = 0; ok && load_bwd_item(a, r, it); ++r) {
+      BwdItem it, nit;
+      bool have = load_bwd_item(a, 0, it), have_next = false;
+      for (long long r = 0; have && ok; ++r, it = nit, have = have_next) {
+        have_next = load_bwd_item(a, r + 1, nit);
         if (it.hi <= it.lo) continue;
         if (!(ok = wait_bar(&bars->qd_full, item_cnt & 1, abort_flag, a, 80))) break;
         ++item_cnt;
@@ -610,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + C::kDQCol, tmem + C::kDPCol + kk * 8,
+            mma_ts(tmem + C::kDQCol, split_a(tmem + C::kDPCol, kk),
                    sdesc_sw128(sK(s) + kk * 16 * 128, kTile * 128, 1024), idAcc, (kk > 0 || j > it.lo) ? 1u : 0u);
           mma_commit(&bars->kv_empty[s]);
           if (more) issue_dp(s1);
@@ -624,12 +651,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(&bars->drain, 0, a.timeout_ns);
     }
     __syncwarp();
+  }
   } else {
-    const int row = 32 * (warp & 3) + lane;
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kActRegs));
+    const int g = (warp - 4) >> 2;                  // activation group: score columns [64g, 64g+64)
+    const int row = 32 * (warp & 3) + lane;         // TMEM lane == query row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t tDPg = tmem + lane_base + C::kDPCol + kCols * g;
     uint32_t step = 0, dp_cnt = 0, acc_cnt = 0;
-    BwdItem it;
-    for (long long r = 0; load_bwd_item(a, r, it); ++r) {
+    BwdItem it, nit;
+    bool have = load_bwd_item(a, 0, it), have_next = false;
+    for (long long r = 0; have; ++r, it = nit, have = have_next) {
+      have_next = load_bwd_item(a, r + 1, nit);
       const int il = it.rt * kTile + row;
       const bool valid = il < it.lq;
       const int delta = it.lkv - it.lq;
@@ -644,26 +677,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           di = a.f1[gi];
         }
       }
-      __nv_bfloat16* dq_row = a.out0 + gi * D;
+      __nv_bfloat16* dq_half = a.out0 + gi * D + (D / 2) * g;  // group g stores dQ columns [gD/2, (g+1)D/2)
       bool ok = true;
       for (int j = it.lo; j < it.hi; ++j, ++step) {
         ok = wait_bar(&bars->s_full[step & 1], (step >> 1) & 1, abort_flag, a, 90);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        float p[kTile];
+        float p[kCols];
         {
           uint32_t* pu = reinterpret_cast<uint32_t*>(p);
 #pragma unroll
-          for (int c = 0; c < kTile / 32; ++c)
-            tmem_ld32(tmem + lane_base + C::kSCol + (step & 1) * kTile + c * 32,
+          for (int c = 0; c < kCols / 32; ++c)
+            tmem_ld32(tmem + lane_base + C::kSCol + (step & 1) * kTile + kCols * g + c * 32,
                       *reinterpret_cast<uint32_t(*)[32]>(pu + c * 32));
           tmem_ld_wait();
         }
-        const int clo = klo - j * kTile, chi = khi - j * kTile;
-        const bool edge = clo > 0 || chi < kTile;
+        const int clo = klo - j * kTile - kCols * g, chi = khi - j * kTile - kCols * g;
+        const bool edge = clo > 0 || chi < kCols;
 #pragma unroll
-        for (int c = 0; c < kTile; ++c) {
+        for (int c = 0; c < kCols; ++c) {
           float v;
           if constexpr (ACT == JATTN_SOFTMAX) {
             v = ex2_approx(fmaf(p[c], a.scale_log2, -lse2));
@@ -679,26 +712,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++dp_cnt;
         tc_fence_after();
+        {
+          uint32_t dp[kCols];
 #pragma unroll
-        for (int c0 = 0; c0 < kTile; c0 += 32) {
-          uint32_t dp[32];
-          tmem_ld32(tmem + lane_base + C::kDPCol + c0, dp);
+          for (int c = 0; c < kCols / 32; ++c) tmem_ld32(tDPg + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dp + c * 32));
           tmem_ld_wait();
-          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int c = c0 + e;
-            float d0, d1;
-            if constexpr (ACT == JATTN_SOFTMAX) {
-              d0 = p[c] * (__uint_as_float(dp[e]) - di);
-              d1 = p[c + 1] * (__uint_as_float(dp[e + 1]) - di);
-            } else {
-              d0 = p[c] * __uint_as_float(dp[e]);
-              d1 = p[c + 1] * __uint_as_float(dp[e + 1]);
+          for (int c0 = 0; c0 < kCols; c0 += 32) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const int c = c0 + e;
+              float d0, d1;
+              if constexpr (ACT == JATTN_SOFTMAX) {
+                d0 = p[c] * (__uint_as_float(dp[c]) - di);
+                d1 = p[c + 1] * (__uint_as_float(dp[c + 1]) - di);
+              } else {
+                d0 = p[c] * __uint_as_float(dp[c]);
+                d1 = p[c + 1] * __uint_as_float(dp[c + 1]);
+              }
+              pk[e / 2] = pack_bf16x2(d0, d1);
             }
-            pk[e / 2] = pack_bf16x2(d0, d1);
+            tmem_st16(tDPg + c0 / 2, pk);
           }
-          tmem_st16(tmem + lane_base + C::kDPCol + c0 / 2, pk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -713,16 +749,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++acc_cnt;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_base + C::kDQCol + c * 32, v);
+          tmem_ld32(tmem + lane_base + C::kDQCol + (D / 2) * g + c * 32, v);
           tmem_ld_wait();
-          if (valid) store_row32(dq_row + c * 32, v, cn * a.scale);
+          if (valid) store_row32(dq_half + c * 32, v, cn * a.scale);
         }
         tc_fence_before();
         mbar_arrive(&bars->acc_empty);
       } else if (valid) {
-        zero_row(dq_row, D);
+        uint4* d = reinterpret_cast<uint4*>(dq_half);
+        for (int e = 0; e < D / 16; ++e) d[e] = make_uint4(0, 0, 0, 0);
       }
     }
   }
