@@ -211,7 +211,8 @@ def main():
     dev = torch.device("cuda", local)
     BND.load()
     w = inputs.WORKLOADS[args.workload]
-    x = inputs.make(args.workload, seed=rank, device=dev)
+    # weak scaling: every rank gets the same lengths (seed 0), its own values (seed = rank)
+    x = inputs.make(args.workload, seed=rank, device=dev, lens=inputs.lengths(args.workload, 0))
     causal = bool(w.mask & 1)
     window = w.window if w.mask & 2 else 0
     kw = dict(act=w.act, causal=causal, window=window, norm_by_lkv=w.norm_by_lkv)
