@@ -33,6 +33,30 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+# DRAM bytes (read + write) per launch measured by ncu on the jfa workload
+# (profiles/<kernel>_kernel_jfa.md). Reported only while the kernel source
+# still has the sha1 prefix recorded at capture time; otherwise null.
+NCU_TRAFFIC = {
+    ("jfa", "fwd"): ("fwd.cu", "f07cdb0b3618", 747544576 + 194030336),
+    ("jfa", "dkdv"): ("bwd.cu", "ddf07b1501df", 980258048 + 407777024),
+    ("jfa", "dq"): ("bwd.cu", "ddf07b1501df", 978268672 + 197619456),
+}
+
+
+def ncu_traffic(workload: str, kernel: str):
+    import hashlib
+
+    entry = NCU_TRAFFIC.get((workload, kernel))
+    if entry is None:
+        return None
+    src, sha, nbytes = entry
+    path = os.path.join(ROOT, "jagged_attention_recsys_gdpa_gb300", "csrc", src)
+    with open(path, "rb") as f:
+        if hashlib.sha1(f.read()).hexdigest()[:12] != sha:
+            return None
+    return nbytes
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -283,7 +307,9 @@ def main():
         roof = {"bound": "tensor", "achieved": wk["flops"] / t_s / 1e12, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = ncu_traffic(args.workload, dom)
+    roof["traffic_unit"] = "bytes per launch (ncu dram read + write)"
+    roof["algorithmic"] = wk["bytes"] if roof["bound"] == "hbm" else wk["flops"]
     roof["kernel"] = dom
     roof["peak_source"] = peaks["source"] + " (burst)"
 
