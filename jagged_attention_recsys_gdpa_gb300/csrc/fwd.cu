@@ -61,11 +61,16 @@ struct FwdBars {
   int abort_flag;
 };
 
-__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + ex2_approx(-x * 1.4426950408889634f)); }
 __device__ __forceinline__ float tanh_approx(float x) {
   float y;
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// x * sigmoid(x) with sigmoid(x) = (1 + tanh(x/2)) / 2: one transcendental
+// instead of an exponential and a reciprocal.
+__device__ __forceinline__ float silu_f(float x) {
+  const float h = 0.5f * x;
+  return fmaf(h, tanh_approx(h), h);
 }
 __device__ __forceinline__ float gelu_f(float x) {
   const float u = 0.7978845608028654f * fmaf(0.044715f * x * x, x, x);
@@ -346,16 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < kTile; ++c) s[c] = (c >= clo && c < chi) ? s[c] : -INFINITY;
           }
-          // row maximum as a tree over 8 independent partial maxima
-          float mp[8];
+          // row maximum: four independent chains of three-input maxima
+          float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) mp[e] = s[e];
+          for (int c = 0; c < kTile; c += 8)
 #pragma unroll
-          for (int c = 8; c < kTile; c += 8)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) mp[e] = fmaxf(mp[e], s[c + e]);
-          const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                                 fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+            for (int e = 0; e < 4; ++e) mp[e] = fmax3(mp[e], s[c + 2 * e], s[c + 2 * e + 1]);
+          const float mx = fmax3(mp[0], mp[1], fmaxf(mp[2], mp[3]));
           const float m_new = mx * a.scale_log2;
           bool rescale = false;
           float alpha = 1.0f;
@@ -382,23 +384,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
           }
           const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
-          float ls[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) ls[e] = 0.0f;
+          // exponent arguments and row sums two lanes at a time (f32x2)
+          const uint64_t c2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-mref, -mref);
+          uint64_t ls2[4] = {0, 0, 0, 0};
 #pragma unroll
           for (int c0 = 0; c0 < kTile; c0 += 32) {
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
-              const float p0 = ex2_approx(fmaf(s[c0 + e], a.scale_log2, -mref));
-              const float p1 = ex2_approx(fmaf(s[c0 + e + 1], a.scale_log2, -mref));
-              ls[(e >> 1) & 7] += p0 + p1;
+              float x0, x1;
+              f2_split(ffma2(f2(s[c0 + e], s[c0 + e + 1]), c2, nm2), x0, x1);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              ls2[(e >> 1) & 3] = fadd2(ls2[(e >> 1) & 3], f2(p0, p1));
               pk[e / 2] = pack_bf16x2(p0, p1);
             }
             // P columns [c0/2, c0/2+16) only overlap S columns already read
             tmem_st16(tS + c0 / 2, pk);
           }
-          l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+          float l0, l1;
+          f2_split(fadd2(fadd2(ls2[0], ls2[1]), fadd2(ls2[2], ls2[3])), l0, l1);
+          l_run += l0 + l1;
         } else {
 #pragma unroll
           for (int c0 = 0; c0 < kTile; c0 += 32) {
