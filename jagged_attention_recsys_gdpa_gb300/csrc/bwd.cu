@@ -356,9 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* lse_buf = s_lse + (step & 1) * kTile + kCols * g;
         float* di_buf = s_di + (step & 1) * kTile + kCols * g;
         if constexpr (ACT == JATTN_SOFTMAX) {
-          if (gt < kCols) {
-            lse_buf[gt] = pf_l2;
-            di_buf[gt] = pf_dd;
+          if (gt < kCols) {  // stored negated: the activation adds them pairwise
+            lse_buf[gt] = -pf_l2;
+            di_buf[gt] = -pf_dd;
           }
           if (i + 1 < it.hi) {
             fetch(it, i + 1, pf_l2, pf_dd);
@@ -382,6 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int clo = ilo - i * kTile - kCols * g, chi = ihi - i * kTile - kCols * g;
         const bool edge = clo > 0 || chi < kCols;
+        const uint64_t c2 = f2(a.scale_log2, a.scale_log2);
+        const uint64_t* nlse2 = reinterpret_cast<const uint64_t*>(lse_buf);  // (-lse, -lse) pairs
 #pragma unroll
         for (int c0 = 0; c0 < kCols; c0 += 32) {
           uint32_t pk[16];
@@ -390,8 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c = c0 + e;
             float f0, f1;
             if constexpr (ACT == JATTN_SOFTMAX) {
-              f0 = ex2_approx(fmaf(p[c], a.scale_log2, -lse_buf[c]));
-              f1 = ex2_approx(fmaf(p[c + 1], a.scale_log2, -lse_buf[c + 1]));
+              float x0, x1;
+              f2_split(ffma2(f2(p[c], p[c + 1]), c2, nlse2[c / 2]), x0, x1);
+              f0 = ex2_approx(x0);
+              f1 = ex2_approx(x1);
               if (edge) {
                 f0 = (c >= clo && c < chi) ? f0 : 0.0f;
                 f1 = (c + 1 >= clo && c + 1 < chi) ? f1 : 0.0f;
@@ -438,8 +442,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int c = c0 + e;
               float d0, d1;
               if constexpr (ACT == JATTN_SOFTMAX) {
-                d0 = p[c] * (__uint_as_float(dp[c]) - di_buf[c]);
-                d1 = p[c + 1] * (__uint_as_float(dp[c + 1]) - di_buf[c + 1]);
+                const uint64_t ndi2 = reinterpret_cast<const uint64_t*>(di_buf)[c / 2];
+                f2_split(fmul2(f2(p[c], p[c + 1]),
+                               fadd2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), ndi2)), d0, d1);
               } else {
                 d0 = p[c] * __uint_as_float(dp[c]);
                 d1 = p[c + 1] * __uint_as_float(dp[c + 1]);
@@ -695,18 +700,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int clo = klo - j * kTile - kCols * g, chi = khi - j * kTile - kCols * g;
         const bool edge = clo > 0 || chi < kCols;
+        const uint64_t c2 = f2(a.scale_log2, a.scale_log2), nl2 = f2(-lse2, -lse2);
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) {
-          float v;
+        for (int c = 0; c < kCols; c += 2) {
+          float v0, v1;
           if constexpr (ACT == JATTN_SOFTMAX) {
-            v = ex2_approx(fmaf(p[c], a.scale_log2, -lse2));
+            float x0, x1;
+            f2_split(ffma2(f2(p[c], p[c + 1]), c2, nl2), x0, x1);
+            v0 = ex2_approx(x0);
+            v1 = ex2_approx(x1);
           } else {
             float f;
-            act_and_grad<ACT>(p[c] * a.scale, f, v);
+            act_and_grad<ACT>(p[c] * a.scale, f, v0);
+            act_and_grad<ACT>(p[c + 1] * a.scale, f, v1);
           }
-          if (edge) v = (c >= clo && c < chi) ? v : 0.0f;
-          p[c] = v;
+          if (edge) {
+            v0 = (c >= clo && c < chi) ? v0 : 0.0f;
+            v1 = (c + 1 >= clo && c + 1 < chi) ? v1 : 0.0f;
+          }
+          p[c] = v0;
+          p[c + 1] = v1;
         }
+        const uint64_t ndi2 = f2(-di, -di);
         ok = wait_bar(&bars->dp_full, dp_cnt & 1, abort_flag, a, 91);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -725,8 +740,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int c = c0 + e;
               float d0, d1;
               if constexpr (ACT == JATTN_SOFTMAX) {
-                d0 = p[c] * (__uint_as_float(dp[c]) - di);
-                d1 = p[c + 1] * (__uint_as_float(dp[c + 1]) - di);
+                f2_split(fmul2(f2(p[c], p[c + 1]),
+                               fadd2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), ndi2)), d0, d1);
               } else {
                 d0 = p[c] * __uint_as_float(dp[c]);
                 d1 = p[c + 1] * __uint_as_float(dp[c + 1]);
