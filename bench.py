@@ -216,6 +216,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="jfa")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph of the step")
     ap.add_argument("--cpu-flops", type=float, default=1.5e11, help="effective FLOPs of the CPU-baseline sample")
     ap.add_argument("--ref-step-flops", type=float, default=2.0e10, help="effective FLOPs per reference step")
     args = ap.parse_args()
@@ -261,12 +262,46 @@ def main():
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {BND.error_string(st)}")
 
-    # per-kernel events for the timed steps
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    # Per-kernel durations: events recorded by the library around its three
+    # main kernels, on the stream they run on, over eager steps.
+    n_ev = min(args.steps, 50)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_ev)]
     for evs in kev:
         for e in evs:
             e.record(stream)  # creates the underlying CUDA events
     torch.cuda.synchronize()
+    for i in range(n_ev):
+        BND.profile_events(kev[i])
+        step()
+    torch.cuda.synchronize()
+    BND.profile_events(None)
+    kt = {
+        "fwd": sum(e[0].elapsed_time(e[1]) for e in kev) / n_ev,
+        "dkdv": sum(e[2].elapsed_time(e[3]) for e in kev) / n_ev,
+        "dq": sum(e[4].elapsed_time(e[5]) for e in kev) / n_ev,
+    }
+
+    # The step (16 launches: schedules, forward, Di, dK/dV, dQ) captured once
+    # as a CUDA graph and replayed, so launch gaps between its short kernels
+    # disappear; eager launches are used if capture is not possible.
+    run = step
+    execution = "eager"
+    if not args.eager:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+                step()
+            graph.replay()
+            torch.cuda.synchronize()
+            run = graph.replay
+            execution = "cuda_graph"
+        except Exception as exc:  # noqa: BLE001 - fall back to eager launches
+            execution = f"eager (graph capture failed: {type(exc).__name__})"
+            torch.cuda.synchronize()
+    for _ in range(2):
+        run()
+    torch.cuda.synchronize()
+
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     time.sleep(0.3)
@@ -274,23 +309,16 @@ def main():
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
-        BND.profile_events(kev[i])
-        step()
+        run()
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
-    BND.profile_events(None)
     clocks = sampler.stop()
     ms = t_start.elapsed_time(t_end) / args.steps
     ms_max = max_over_ranks(ms, ws, dev)
     st = J.device_status(dev)
     if st != 0:
         raise RuntimeError(f"device status after timing: {BND.error_string(st)}")
-    kt = {
-        "fwd": sum(e[0].elapsed_time(e[1]) for e in kev) / args.steps,
-        "dkdv": sum(e[2].elapsed_time(e[3]) for e in kev) / args.steps,
-        "dq": sum(e[4].elapsed_time(e[5]) for e in kev) / args.steps,
-    }
     fwd_ms_all = ms  # whole step
     value = (f_fwd + f_bwd) * ws / (ms_max * 1e-3) / 1e12
     peaks = load_peaks()
@@ -376,6 +404,7 @@ def main():
                 "total_q": tq, "total_kv": tk, "pairs_per_head": pairs,
                 "l2": f"inputs larger than L2 ({tq * w.H * w.D * 2 / 1e6:.0f} MB per bf16 tensor)",
                 "parallelism": f"replicas x{ws} (independent batches, no collective)",
+                "execution": execution,
             },
             "fwd_tflops": f_fwd / (kt["fwd"] * 1e-3) / 1e12,
             "bwd_tflops": f_bwd / ((kt["dkdv"] + kt["dq"]) * 1e-3) / 1e12,
