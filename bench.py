@@ -37,9 +37,9 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # (profiles/<kernel>_kernel_jfa.md). Reported only while the kernel source
 # still has the sha1 prefix recorded at capture time; otherwise null.
 NCU_TRAFFIC = {
-    ("jfa", "fwd"): ("fwd.cu", "f07cdb0b3618", 747544576 + 194030336),
-    ("jfa", "dkdv"): ("bwd.cu", "ddf07b1501df", 980258048 + 407777024),
-    ("jfa", "dq"): ("bwd.cu", "ddf07b1501df", 978268672 + 197619456),
+    ("jfa", "fwd"): ("fwd.cu", "99c1b58bbe1e", 942044928),
+    ("jfa", "dkdv"): ("bwd.cu", "132aa1515203", 1387580672),
+    ("jfa", "dq"): ("bwd.cu", "132aa1515203", 1176221696),
 }
 
 
