@@ -178,7 +178,10 @@ void jattn_profile_events(void* const* events);
  * `timeout_ns` nanoseconds (0 restores the default of two seconds), and
  * flag bit 0 makes the next launches skip the query-tile copy so that the
  * first wait on it runs out. Used to check that an expired wait reports
- * JATTN_ERR_TIMEOUT and leaves the context usable. */
+ * JATTN_ERR_TIMEOUT and leaves the context usable. Flag bit 1 (bit 2) makes
+ * the forward use the column-split (ping-pong) arrangement of its activation
+ * warps whatever the shapes, so both can be checked on the same inputs;
+ * results agree within floating-point rounding order. */
 void jattn_debug_set(int flags, uint64_t timeout_ns);
 
 #ifdef __cplusplus

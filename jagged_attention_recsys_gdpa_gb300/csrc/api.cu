@@ -21,6 +21,15 @@ namespace {
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 thread_local char g_last_error[256] = "";
 int g_debug_flags = 0;
+
+// Forward activation arrangement: the column split when sequences average at
+// most one 128-row query tile (most items then hold a single tile), else the
+// ping-pong between two query tiles. Debug flag bits 1 / 2 force either one.
+bool fwd_split(const jattn_params_t& p) {
+  if (g_debug_flags & 2) return true;
+  if (g_debug_flags & 4) return false;
+  return p.total_q <= static_cast<int64_t>(kTile) * p.B;
+}
 uint64_t g_timeout_ns = kDefaultTimeoutNs;
 // Optional events recorded around the main kernels: [fwd, dkdv, dq] x [begin, end].
 cudaEvent_t g_prof[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
@@ -260,7 +269,7 @@ int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
   a.out0 = reinterpret_cast<__nv_bfloat16*>(o);
   a.f0 = lse;
   prof(0, st);
-  if ((e = launch_fwd(p->D, p->act, mq, mk, mv, a, grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
+  if ((e = launch_fwd(p->D, p->act, fwd_split(*p), mq, mk, mv, a, grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
     return cuda_fail("forward kernel launch", e);
   prof(1, st);
   return JATTN_OK;
@@ -307,7 +316,7 @@ int jattn_fwd_noalloc(const jattn_params_t* p, const int64_t* q_off, const int64
     a.n_tiles = sv.n_tiles;
     a.out0 = reinterpret_cast<__nv_bfloat16*>(o);
     a.f0 = lse;
-    if ((e = launch_fwd(p->D, p->act, mq, mk, mv, a, grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
+    if ((e = launch_fwd(p->D, p->act, fwd_split(*p), mq, mk, mv, a, grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
       return cuda_fail("forward kernel launch", e);
   }
   if (device_status &&

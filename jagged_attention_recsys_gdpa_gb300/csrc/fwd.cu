@@ -14,11 +14,17 @@
 //   warp 1      tcgen05 issuer: S_t = Q_t K_j^T into TMEM, O_t += P_t V_j
 //               with P_t read straight from TMEM
 //   warps 2-3   idle (their warpgroup gives its registers to the others)
-//   warps 4-7   activation warpgroup for query tile 0
-//   warps 8-11  activation warpgroup for query tile 1
-// The two activation warpgroups ping-pong: while one turns its S tile into P,
-// the tensor core works on the other tile's products. TMEM columns:
-// [S0 | S1 | O0 | O1]; P_t (bf16 pairs) overwrites the first half of S_t.
+//   warps 4-11  two activation warpgroups, in one of two arrangements:
+//     ping-pong     warpgroup t owns query tile t: while one turns its S tile
+//                   into P, the tensor core works on the other tile's products.
+//                   P_t (bf16 pairs) overwrites S_t columns 0-63.
+//     column split  both warpgroups work on every S tile, key columns 0-63 and
+//                   64-127; P of each half overwrites the first 32 of the half's
+//                   own S columns (0-31, 64-95), and softmax row maxima and sums
+//                   are combined through shared memory. Items that hold a single
+//                   query tile (short queries, e.g. pooling attention) keep all
+//                   eight warps busy this way; the host picks the arrangement.
+// TMEM columns: [S0 | S1 | O0 | O1].
 // Softmax rescaling of O is lazy: the running maximum only moves (and O is
 // rescaled in TMEM) when a row's maximum grows by more than 2^8.
 #include <cstdint>
@@ -47,7 +53,8 @@ struct FwdCfg {
   static constexpr int kKOff = kQOff + kNQ * kTileBytes;
   static constexpr int kVOff = kKOff + kKStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-  static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + alignment slack
+  static constexpr int kXchOff = kBarOff + 512;                 // [2 slots][2 halves][128 rows] fp32
+  static constexpr int kSmemBytes = kXchOff + 2 * 2 * kTile * 4;  // base is 1024-aligned (checked)
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 2 * kTile;  // O_t at kOCol + t * D
 };
@@ -59,7 +66,10 @@ struct FwdBars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  volatile int okx[2][2][4];  // exchange slot, column half, lane quarter: partner still ok
 };
+static_assert(sizeof(FwdBars) <= 512, "barrier block overflows its slot");
+static_assert(FwdCfg<128>::kSmemBytes <= 227 * 1024 && FwdCfg<64>::kSmemBytes <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ float tanh_approx(float x) {
   float y;
@@ -116,13 +126,19 @@ __device__ __forceinline__ bool load_item(const AttnArgs& a, long long round, It
   return true;
 }
 
-template <int D, int ACT>
+template <int D, int ACT, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
   using C = FwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // The tiles need 1024-byte alignment and the layout leaves no slack for
+  // realigning, so a misaligned dynamic shared memory base is an error.
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) record_error(a.status, JATTN_ERR_UNSUPPORTED, 19, blockIdx.x);
+    return;
+  }
+  uint8_t* sm = smem_raw;
   FwdBars* bars = reinterpret_cast<FwdBars*>(sm + C::kBarOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &bars->abort_flag;
@@ -140,9 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], kTile);
+      mbar_init(&bars->p_full[t], (SPLIT ? 2 : 1) * kTile);
       mbar_init(&bars->o_full[t], 1);
-      mbar_init(&bars->o_empty[t], kTile);
+      mbar_init(&bars->o_empty[t], (SPLIT ? 2 : 1) * kTile);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -280,7 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
 #pragma unroll
               for (int kk = 0; kk < kTile / 16; ++kk) {
-                mma_ts(tmem + C::kOCol + q * D, tmem + q * kTile + kk * 8,
+                // P of key columns 16kk.. sits at column 8kk; with the column split,
+                // at 8kk + 32 for the second half
+                mma_ts(tmem + C::kOCol + q * D, tmem + q * kTile + kk * 8 + ((SPLIT && kk >= kTile / 32) ? 32 : 0),
                        sdesc_sw128(sV + vs * C::kTileBytes + kk * 16 * 128, kTile * 128, 1024), idPV,
                        (kk > 0 || j > it.t_lo[q]) ? 1u : 0u);
               }
@@ -308,170 +326,388 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kActRegs));
-    // ------------------------------------------------------------ activation warpgroups
-    const int q = (warp - 4) >> 2;                 // query tile of this warpgroup
-    const int row = 32 * (warp & 3) + lane;         // TMEM lane == tile row
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t tS = tmem + lane_base + q * kTile;
-    const uint32_t tO = tmem + lane_base + C::kOCol + q * D;
-    uint32_t s_cnt = 0, o_cnt = 0;
-    ItemInfo it;
-    for (long long r = 0; load_item(a, r, it); ++r) {
-      const bool has_rows = q ? it.t_rows[1] : it.t_rows[0];
-      const int t_lo = q ? it.t_lo[1] : it.t_lo[0];
-      const int t_hi = q ? it.t_hi[1] : it.t_hi[0];
-      if (!has_rows) continue;
-      const int row_local = (it.qb * kNQ + q) * kTile + row;
-      const bool valid = row_local < it.lq;
-      const int64_t grow = it.q0 + row_local;
-      const int delta = it.lkv - it.lq;
-      int klo, khi;
-      key_interval(row_local, delta, it.lkv, a.mask, a.window, klo, khi);
-      const int n = (it.hi > it.lo) ? (t_hi - t_lo) : 0;
-      float m_run = -INFINITY, l_run = 0.0f;
+    if constexpr (SPLIT) {
+      // ------------------------------------------------------------ activation warpgroups
+      // Both warpgroups work on every S tile, one column half each: warpgroup
+      // `half` owns key columns [64 half, 64 half + 64) of S_t and O columns
+      // [D/2 half, D/2 half + D/2) of O_t. Warp w and warp w ^ 4 hold the same
+      // rows; for softmax they combine row maxima (every tile) and row sums
+      // (epilogue) through shared memory.
+      const int half = (warp - 4) >> 2;
+      const int quarter = warp & 3;                   // TMEM lane quarter
+      const int row = 32 * quarter + lane;            // TMEM lane == tile row
+      const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+      constexpr int kHalfCols = kTile / 2;            // S columns of one half
+      constexpr int kOHalf = D / 2;                   // O columns of one half
+      float* xch = reinterpret_cast<float*>(sm + C::kXchOff);
+      uint32_t s_cnt[kNQ] = {0, 0}, o_cnt[kNQ] = {0, 0}, x_cnt = 0;
+      // Row exchange with the partner warp. Both partners always reach the named
+      // barrier and leave it with the same `okr`. Two slots, alternating: a slot is
+      // rewritten only after the partner has passed the barrier that follows its read.
+      auto exchange = [&](float v, bool& okr) -> float {
+        const int slot = x_cnt & 1;
+        ++x_cnt;
+        xch[(slot * 2 + half) * kTile + row] = v;
+        if (lane == 0) bars->okx[slot][half][quarter] = okr ? 1 : 0;
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+        okr = okr && (bars->okx[slot][half ^ 1][quarter] != 0);
+        return xch[(slot * 2 + (half ^ 1)) * kTile + row];
+      };
       bool ok = true;
-      for (int j = t_lo; j < t_lo + n; ++j) {
-        ok = wait_bar(&bars->s_full[q], s_cnt & 1, abort_flag, a, 30);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        ++s_cnt;
-        tc_fence_after();
-        float s[kTile];
-        {
-          uint32_t* su = reinterpret_cast<uint32_t*>(s);
-#pragma unroll
-          for (int c = 0; c < kTile / 32; ++c)
-            tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(su + c * 32));
-          tmem_ld_wait();
+      ItemInfo it;
+      for (long long r = 0; ok && load_item(a, r, it); ++r) {
+        const int delta = it.lkv - it.lq;
+        int klo[kNQ], khi[kNQ];
+        float m_run[kNQ], l_run[kNQ];
+  #pragma unroll
+        for (int q = 0; q < kNQ; ++q) {
+          key_interval((it.qb * kNQ + q) * kTile + row, delta, it.lkv, a.mask, a.window, klo[q], khi[q]);
+          m_run[q] = -INFINITY;
+          l_run[q] = 0.0f;
         }
-        const int clo = klo - j * kTile, chi = khi - j * kTile;
-        const bool edge = clo > 0 || chi < kTile;
-        if constexpr (ACT == JATTN_SOFTMAX) {
-          if (edge) {
-#pragma unroll
-            for (int c = 0; c < kTile; ++c) s[c] = (c >= clo && c < chi) ? s[c] : -INFINITY;
-          }
-          // row maximum: four independent chains of three-input maxima
-          float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int c = 0; c < kTile; c += 8)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) mp[e] = fmax3(mp[e], s[c + 2 * e], s[c + 2 * e + 1]);
-          const float mx = fmax3(mp[0], mp[1], fmaxf(mp[2], mp[3]));
-          const float m_new = mx * a.scale_log2;
-          bool rescale = false;
-          float alpha = 1.0f;
-          if (m_run == -INFINITY) {
-            m_run = m_new;  // O and l hold nothing yet for this row
-          } else if (m_new > m_run + kRescaleLog2) {
-            alpha = ex2_approx(m_run - m_new);
-            rescale = true;
-            m_run = m_new;
-            l_run *= alpha;
-          }
-          if (__any_sync(0xffffffffu, rescale)) {
-            // The previous P V product of this tile has completed: the S tile
-            // just waited for was issued after it.
-#pragma unroll
-            for (int c = 0; c < D / 16; ++c) {
-              uint32_t o[16];
-              tmem_ld16(tO + c * 16, o);
+        for (int j = it.lo; ok && j < it.hi; ++j) {
+  #pragma unroll
+          for (int q = 0; q < kNQ; ++q) {
+            if (!ok) break;
+            if (j < it.t_lo[q] || j >= it.t_hi[q]) continue;
+            bool okw = wait_bar(&bars->s_full[q], s_cnt[q] & 1, abort_flag, a, 30);
+            okw = __all_sync(0xffffffffu, okw);
+            ++s_cnt[q];
+            const uint32_t tS = tmem + lane_base + q * kTile + half * kHalfCols;
+            float s[kHalfCols];
+            if (okw) {
+              tc_fence_after();
+              uint32_t* su = reinterpret_cast<uint32_t*>(s);
+              tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(su));
+              tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
               tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tmem_st16(tO + c * 16, o);
+            }
+            const int clo = klo[q] - j * kTile - half * kHalfCols, chi = khi[q] - j * kTile - half * kHalfCols;
+            const bool edge = clo > 0 || chi < kHalfCols;
+            if constexpr (ACT == JATTN_SOFTMAX) {
+              float mx = -INFINITY;
+              if (okw) {
+                if (edge) {
+  #pragma unroll
+                  for (int c = 0; c < kHalfCols; ++c) s[c] = (c >= clo && c < chi) ? s[c] : -INFINITY;
+                }
+                // row maximum of this half: four independent chains of three-input maxima
+                float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  #pragma unroll
+                for (int c = 0; c < kHalfCols; c += 8)
+  #pragma unroll
+                  for (int e = 0; e < 4; ++e) mp[e] = fmax3(mp[e], s[c + 2 * e], s[c + 2 * e + 1]);
+                mx = fmax3(mp[0], mp[1], fmaxf(mp[2], mp[3]));
+              }
+              mx = fmaxf(mx, exchange(mx, okw));
+              if (!okw) {
+                ok = false;
+                break;
+              }
+              const float m_new = mx * a.scale_log2;
+              bool rescale = false;
+              float alpha = 1.0f;
+              if (m_run[q] == -INFINITY) {
+                m_run[q] = m_new;  // O and l hold nothing yet for this row
+              } else if (m_new > m_run[q] + kRescaleLog2) {
+                alpha = ex2_approx(m_run[q] - m_new);
+                rescale = true;
+                m_run[q] = m_new;
+                l_run[q] *= alpha;
+              }
+              if (__any_sync(0xffffffffu, rescale)) {
+                // The previous P V product of this tile has completed: the S tile
+                // just waited for was issued after it.
+                const uint32_t tO = tmem + lane_base + C::kOCol + q * D + half * kOHalf;
+  #pragma unroll
+                for (int c = 0; c < kOHalf / 16; ++c) {
+                  uint32_t o[16];
+                  tmem_ld16(tO + c * 16, o);
+                  tmem_ld_wait();
+  #pragma unroll
+                  for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                  tmem_st16(tO + c * 16, o);
+                }
+                tmem_st_wait();
+              }
+              const float mref = (m_run[q] == -INFINITY) ? 0.0f : m_run[q];
+              // exponent arguments and row sums two lanes at a time (f32x2)
+              const uint64_t c2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-mref, -mref);
+              uint64_t ls2[4] = {0, 0, 0, 0};
+  #pragma unroll
+              for (int c0 = 0; c0 < kHalfCols; c0 += 32) {
+                uint32_t pk[16];
+  #pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                  float x0, x1;
+                  f2_split(ffma2(f2(s[c0 + e], s[c0 + e + 1]), c2, nm2), x0, x1);
+                  const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                  ls2[(e >> 1) & 3] = fadd2(ls2[(e >> 1) & 3], f2(p0, p1));
+                  pk[e / 2] = pack_bf16x2(p0, p1);
+                }
+                // P of this half goes to the first 32 columns of the half's own S
+                // columns, which this warp has already read
+                tmem_st16(tS + c0 / 2, pk);
+              }
+              float l0, l1;
+              f2_split(fadd2(fadd2(ls2[0], ls2[1]), fadd2(ls2[2], ls2[3])), l0, l1);
+              l_run[q] += l0 + l1;
+            } else {
+              if (!okw) {
+                ok = false;
+                break;
+              }
+  #pragma unroll
+              for (int c0 = 0; c0 < kHalfCols; c0 += 32) {
+                uint32_t pk[16];
+  #pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                  const int c = c0 + e;
+                  const float x0 = s[c] * a.scale, x1 = s[c + 1] * a.scale;
+                  float p0 = (ACT == JATTN_SILU) ? silu_f(x0) : gelu_f(x0);
+                  float p1 = (ACT == JATTN_SILU) ? silu_f(x1) : gelu_f(x1);
+                  if (edge) {
+                    p0 = (c >= clo && c < chi) ? p0 : 0.0f;
+                    p1 = (c + 1 >= clo && c + 1 < chi) ? p1 : 0.0f;
+                  }
+                  pk[e / 2] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tS + c0 / 2, pk);
+              }
             }
             tmem_st_wait();
-          }
-          const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
-          // exponent arguments and row sums two lanes at a time (f32x2)
-          const uint64_t c2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-mref, -mref);
-          uint64_t ls2[4] = {0, 0, 0, 0};
-#pragma unroll
-          for (int c0 = 0; c0 < kTile; c0 += 32) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float x0, x1;
-              f2_split(ffma2(f2(s[c0 + e], s[c0 + e + 1]), c2, nm2), x0, x1);
-              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-              ls2[(e >> 1) & 3] = fadd2(ls2[(e >> 1) & 3], f2(p0, p1));
-              pk[e / 2] = pack_bf16x2(p0, p1);
-            }
-            // P columns [c0/2, c0/2+16) only overlap S columns already read
-            tmem_st16(tS + c0 / 2, pk);
-          }
-          float l0, l1;
-          f2_split(fadd2(fadd2(ls2[0], ls2[1]), fadd2(ls2[2], ls2[3])), l0, l1);
-          l_run += l0 + l1;
-        } else {
-#pragma unroll
-          for (int c0 = 0; c0 < kTile; c0 += 32) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const int c = c0 + e;
-              const float x0 = s[c] * a.scale, x1 = s[c + 1] * a.scale;
-              float p0 = (ACT == JATTN_SILU) ? silu_f(x0) : gelu_f(x0);
-              float p1 = (ACT == JATTN_SILU) ? silu_f(x1) : gelu_f(x1);
-              if (edge) {
-                p0 = (c >= clo && c < chi) ? p0 : 0.0f;
-                p1 = (c + 1 >= clo && c + 1 < chi) ? p1 : 0.0f;
-              }
-              pk[e / 2] = pack_bf16x2(p0, p1);
-            }
-            tmem_st16(tS + c0 / 2, pk);
+            tc_fence_before();
+            mbar_arrive(&bars->p_full[q]);
           }
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars->p_full[q]);
-      }
-      if (!ok) break;
-      // ---------------- epilogue
-      float oscale;
-      if constexpr (ACT == JATTN_SOFTMAX) {
-        oscale = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-      } else {
-        oscale = (a.norm_by_lkv && it.lkv > 0) ? 1.0f / static_cast<float>(it.lkv) : 1.0f;
-      }
-      __nv_bfloat16* orow = a.out0 + (grow * a.H + it.h) * D;
-      if (n > 0) {
-        ok = wait_bar(&bars->o_full[q], o_cnt & 1, abort_flag, a, 31);
-        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        ++o_cnt;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait();
-          if (valid) {
-            uint32_t w[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * oscale, __uint_as_float(o[2 * e + 1]) * oscale);
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        // ---------------- epilogue: each half stores its O columns of each tile
+  #pragma unroll
+        for (int q = 0; q < kNQ; ++q) {
+          if (!ok) break;
+          if (!it.t_rows[q]) continue;
+          const int row_local = (it.qb * kNQ + q) * kTile + row;
+          const bool valid = row_local < it.lq;
+          const int64_t grow = it.q0 + row_local;
+          const int n = (it.hi > it.lo) ? (it.t_hi[q] - it.t_lo[q]) : 0;
+          bool okw = true;
+          if (n > 0) {
+            okw = wait_bar(&bars->o_full[q], o_cnt[q] & 1, abort_flag, a, 31);
+            okw = __all_sync(0xffffffffu, okw);
+            ++o_cnt[q];
+          }
+          float l_tot = l_run[q];
+          if constexpr (ACT == JATTN_SOFTMAX) l_tot += exchange(l_run[q], okw);
+          if (!okw) {
+            ok = false;
+            break;
+          }
+          float oscale;
+          if constexpr (ACT == JATTN_SOFTMAX) {
+            oscale = (l_tot > 0.0f) ? 1.0f / l_tot : 0.0f;
+          } else {
+            oscale = (a.norm_by_lkv && it.lkv > 0) ? 1.0f / static_cast<float>(it.lkv) : 1.0f;
+          }
+          __nv_bfloat16* orow = a.out0 + (grow * a.H + it.h) * D + half * kOHalf;
+          if (n > 0) {
+            tc_fence_after();
+            const uint32_t tO = tmem + lane_base + C::kOCol + q * D + half * kOHalf;
+  #pragma unroll
+            for (int c = 0; c < kOHalf / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_ld_wait();
+              if (valid) {
+                uint32_t w[16];
+  #pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * oscale, __uint_as_float(o[2 * e + 1]) * oscale);
+                uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+  #pragma unroll
+                for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+              }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars->o_empty[q]);
+          } else if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow);
+            for (int e = 0; e < kOHalf / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+          }
+          if constexpr (ACT == JATTN_SOFTMAX) {
+            if (valid && half == 0) {
+              const float lse = (l_tot > 0.0f) ? (m_run[q] + __log2f(l_tot)) * 0.6931471805599453f : -INFINITY;
+              a.f0[grow * a.H + it.h] = lse;
+            }
           }
         }
-        tc_fence_before();
-        mbar_arrive(&bars->o_empty[q]);
-      } else if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(orow);
-        for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
       }
-      if constexpr (ACT == JATTN_SOFTMAX) {
-        if (valid) {
-          const float lse = (l_run > 0.0f) ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
-          a.f0[grow * a.H + it.h] = lse;
+    } else {
+      // Ping-pong: warpgroup q owns query tile q of the item; while one turns
+      // its S tile into P, the tensor core works on the other tile.
+      // ------------------------------------------------------------ activation warpgroups
+      const int q = (warp - 4) >> 2;                 // query tile of this warpgroup
+      const int row = 32 * (warp & 3) + lane;         // TMEM lane == tile row
+      const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+      const uint32_t tS = tmem + lane_base + q * kTile;
+      const uint32_t tO = tmem + lane_base + C::kOCol + q * D;
+      uint32_t s_cnt = 0, o_cnt = 0;
+      ItemInfo it;
+      for (long long r = 0; load_item(a, r, it); ++r) {
+        const bool has_rows = q ? it.t_rows[1] : it.t_rows[0];
+        const int t_lo = q ? it.t_lo[1] : it.t_lo[0];
+        const int t_hi = q ? it.t_hi[1] : it.t_hi[0];
+        if (!has_rows) continue;
+        const int row_local = (it.qb * kNQ + q) * kTile + row;
+        const bool valid = row_local < it.lq;
+        const int64_t grow = it.q0 + row_local;
+        const int delta = it.lkv - it.lq;
+        int klo, khi;
+        key_interval(row_local, delta, it.lkv, a.mask, a.window, klo, khi);
+        const int n = (it.hi > it.lo) ? (t_hi - t_lo) : 0;
+        float m_run = -INFINITY, l_run = 0.0f;
+        bool ok = true;
+        for (int j = t_lo; j < t_lo + n; ++j) {
+          ok = wait_bar(&bars->s_full[q], s_cnt & 1, abort_flag, a, 30);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          ++s_cnt;
+          tc_fence_after();
+          float s[kTile];
+          {
+            uint32_t* su = reinterpret_cast<uint32_t*>(s);
+  #pragma unroll
+            for (int c = 0; c < kTile / 32; ++c)
+              tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(su + c * 32));
+            tmem_ld_wait();
+          }
+          const int clo = klo - j * kTile, chi = khi - j * kTile;
+          const bool edge = clo > 0 || chi < kTile;
+          if constexpr (ACT == JATTN_SOFTMAX) {
+            if (edge) {
+  #pragma unroll
+              for (int c = 0; c < kTile; ++c) s[c] = (c >= clo && c < chi) ? s[c] : -INFINITY;
+            }
+            // row maximum: four independent chains of three-input maxima
+            float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  #pragma unroll
+            for (int c = 0; c < kTile; c += 8)
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) mp[e] = fmax3(mp[e], s[c + 2 * e], s[c + 2 * e + 1]);
+            const float mx = fmax3(mp[0], mp[1], fmaxf(mp[2], mp[3]));
+            const float m_new = mx * a.scale_log2;
+            bool rescale = false;
+            float alpha = 1.0f;
+            if (m_run == -INFINITY) {
+              m_run = m_new;  // O and l hold nothing yet for this row
+            } else if (m_new > m_run + kRescaleLog2) {
+              alpha = ex2_approx(m_run - m_new);
+              rescale = true;
+              m_run = m_new;
+              l_run *= alpha;
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+              // The previous P V product of this tile has completed: the S tile
+              // just waited for was issued after it.
+  #pragma unroll
+              for (int c = 0; c < D / 16; ++c) {
+                uint32_t o[16];
+                tmem_ld16(tO + c * 16, o);
+                tmem_ld_wait();
+  #pragma unroll
+                for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                tmem_st16(tO + c * 16, o);
+              }
+              tmem_st_wait();
+            }
+            const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
+            // exponent arguments and row sums two lanes at a time (f32x2)
+            const uint64_t c2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-mref, -mref);
+            uint64_t ls2[4] = {0, 0, 0, 0};
+  #pragma unroll
+            for (int c0 = 0; c0 < kTile; c0 += 32) {
+              uint32_t pk[16];
+  #pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                float x0, x1;
+                f2_split(ffma2(f2(s[c0 + e], s[c0 + e + 1]), c2, nm2), x0, x1);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                ls2[(e >> 1) & 3] = fadd2(ls2[(e >> 1) & 3], f2(p0, p1));
+                pk[e / 2] = pack_bf16x2(p0, p1);
+              }
+              // P columns [c0/2, c0/2+16) only overlap S columns already read
+              tmem_st16(tS + c0 / 2, pk);
+            }
+            float l0, l1;
+            f2_split(fadd2(fadd2(ls2[0], ls2[1]), fadd2(ls2[2], ls2[3])), l0, l1);
+            l_run += l0 + l1;
+          } else {
+  #pragma unroll
+            for (int c0 = 0; c0 < kTile; c0 += 32) {
+              uint32_t pk[16];
+  #pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                const int c = c0 + e;
+                const float x0 = s[c] * a.scale, x1 = s[c + 1] * a.scale;
+                float p0 = (ACT == JATTN_SILU) ? silu_f(x0) : gelu_f(x0);
+                float p1 = (ACT == JATTN_SILU) ? silu_f(x1) : gelu_f(x1);
+                if (edge) {
+                  p0 = (c >= clo && c < chi) ? p0 : 0.0f;
+                  p1 = (c + 1 >= clo && c + 1 < chi) ? p1 : 0.0f;
+                }
+                pk[e / 2] = pack_bf16x2(p0, p1);
+              }
+              tmem_st16(tS + c0 / 2, pk);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->p_full[q]);
+        }
+        if (!ok) break;
+        // ---------------- epilogue
+        float oscale;
+        if constexpr (ACT == JATTN_SOFTMAX) {
+          oscale = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+        } else {
+          oscale = (a.norm_by_lkv && it.lkv > 0) ? 1.0f / static_cast<float>(it.lkv) : 1.0f;
+        }
+        __nv_bfloat16* orow = a.out0 + (grow * a.H + it.h) * D;
+        if (n > 0) {
+          ok = wait_bar(&bars->o_full[q], o_cnt & 1, abort_flag, a, 31);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          ++o_cnt;
+          tc_fence_after();
+  #pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait();
+            if (valid) {
+              uint32_t w[16];
+  #pragma unroll
+              for (int e = 0; e < 16; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * oscale, __uint_as_float(o[2 * e + 1]) * oscale);
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&bars->o_empty[q]);
+        } else if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+          for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+        }
+        if constexpr (ACT == JATTN_SOFTMAX) {
+          if (valid) {
+            const float lse = (l_run > 0.0f) ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+            a.f0[grow * a.H + it.h] = lse;
+          }
         }
       }
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
@@ -479,27 +715,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int D, int ACT>
+template <int D, int ACT, bool SPLIT>
 static cudaError_t launch_fwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                 const AttnArgs& a, int grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fwd_kernel<D, ACT>;
+  auto kern = fwd_kernel<D, ACT, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const AttnArgs& a, int grid, cudaStream_t stream) {
+template <int D, int ACT>
+static cudaError_t launch_fwd_s(bool split, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const AttnArgs& a, int grid, cudaStream_t stream) {
+  return split ? launch_fwd_t<D, ACT, true>(q, k, v, a, grid, stream)
+               : launch_fwd_t<D, ACT, false>(q, k, v, a, grid, stream);
+}
+
+cudaError_t launch_fwd(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
+                       const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream) {
   if (D == 128) {
-    if (act == JATTN_SOFTMAX) return launch_fwd_t<128, JATTN_SOFTMAX>(q, k, v, a, grid, stream);
-    if (act == JATTN_SILU) return launch_fwd_t<128, JATTN_SILU>(q, k, v, a, grid, stream);
-    return launch_fwd_t<128, JATTN_GELU_TANH>(q, k, v, a, grid, stream);
+    if (act == JATTN_SOFTMAX) return launch_fwd_s<128, JATTN_SOFTMAX>(split, q, k, v, a, grid, stream);
+    if (act == JATTN_SILU) return launch_fwd_s<128, JATTN_SILU>(split, q, k, v, a, grid, stream);
+    return launch_fwd_s<128, JATTN_GELU_TANH>(split, q, k, v, a, grid, stream);
   }
-  if (act == JATTN_SOFTMAX) return launch_fwd_t<64, JATTN_SOFTMAX>(q, k, v, a, grid, stream);
-  if (act == JATTN_SILU) return launch_fwd_t<64, JATTN_SILU>(q, k, v, a, grid, stream);
-  return launch_fwd_t<64, JATTN_GELU_TANH>(q, k, v, a, grid, stream);
+  if (act == JATTN_SOFTMAX) return launch_fwd_s<64, JATTN_SOFTMAX>(split, q, k, v, a, grid, stream);
+  if (act == JATTN_SILU) return launch_fwd_s<64, JATTN_SILU>(split, q, k, v, a, grid, stream);
+  return launch_fwd_s<64, JATTN_GELU_TANH>(split, q, k, v, a, grid, stream);
 }
 
 int fwd_rows_per_item() { return kNQ * kTile; }

@@ -7,9 +7,11 @@ namespace jattn {
 
 struct AttnArgs;
 
-// Forward: schedule rows are blocks of fwd_rows_per_item() query rows.
-cudaError_t launch_fwd(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const AttnArgs& a, int grid, cudaStream_t stream);
+// Forward: schedule rows are blocks of fwd_rows_per_item() query rows. `split`
+// selects the column-split arrangement of the activation warps (for items that
+// mostly hold one query tile) over the ping-pong one.
+cudaError_t launch_fwd(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
+                       const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream);
 int fwd_rows_per_item();
 
 // Backward: Di = rowsum(dO * O) (softmax only).

@@ -156,3 +156,35 @@ def test_cuda_graph_replay_matches_eager():
         for g_t, e_t in zip(got, (o, lse, dq, dk, dv)):
             assert torch.equal(g_t, e_t)
     assert J.device_status() == 0
+
+
+FWD_SPLIT, FWD_PINGPONG = 2, 4  # debug flag bits that force the forward's warp arrangement
+
+
+@pytest.mark.parametrize("arrangement", [FWD_SPLIT, FWD_PINGPONG])
+@pytest.mark.parametrize(
+    "act,mask,window,D,lq,lkv",
+    [
+        (SOFTMAX, WIN, 200, 128, SELF_LENS, SELF_LENS),
+        (SOFTMAX, CAUSAL, 0, 64, SELF_LENS, SELF_LENS),
+        (SOFTMAX, CAUSAL, 0, 128, [0, 5, 130, 1, 0, 200, 3], [4, 0, 130, 1, 0, 60, 9]),
+        (SOFTMAX, NONE, 0, 128, [32, 32, 32, 7], [100, 1000, 3000, 129]),
+        (GELU, NONE, 0, 128, [32, 32, 32, 32], [100, 1000, 3000, 129]),
+        (SILU, NONE, 0, 64, CROSS_LQ, CROSS_LKV),
+        (SILU, WIN, 7, 128, [0, 5, 130, 1, 0, 200, 3], [4, 0, 130, 1, 0, 60, 9]),
+    ],
+)
+def test_forward_arrangements(arrangement, act, mask, window, D, lq, lkv):
+    """Both arrangements of the forward's activation warps (two query tiles in
+    ping-pong, or every tile's key columns split over both warpgroups) match the
+    oracle on the same inputs, whichever one the shapes would pick."""
+    from jagged_attention_recsys_gdpa_gb300 import _binding as B
+
+    w = _w(act, mask, window, D, H=3, norm=act != SOFTMAX, std=1.0 if act == SOFTMAX else 0.5)
+    cpu = G.cpu_inputs(w, lq, lkv, seed=21)
+    B.debug_set(arrangement, 0)
+    try:
+        g = G.gpu_run(G.to_cuda(cpu), w, backward=False)
+    finally:
+        B.debug_set(0, 0)
+    G.compare(g, G.oracle_run(cpu, w, backward=False), w, backward=False)
