@@ -273,6 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_s(s);
           issue_dp(s);
+          // K and V feed only the S^T and dP^T products: once the item's last
+          // pair has completed, the next item's K/V copy may land.
+          if (it.hi - it.lo == 1) mma_commit(&bars->kv_empty);
         }
         for (int i = it.lo; i < it.hi; ++i, ++qd_it) {
           const int s = qd_it % C::kStages;
@@ -302,11 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    sdesc_sw128(sQ(s) + kk * 16 * 128, kTile * 128, 1024), idAcc, (kk > 0 || i > it.lo) ? 1u : 0u);
           mma_commit(&bars->qd_empty[s]);
           if (more) issue_dp(s1);
+          if (i + 2 == it.hi) mma_commit(&bars->kv_empty);
         }
         if (!ok) break;
         mma_commit(&bars->acc_full);
         ++acc_cnt;
-        mma_commit(&bars->kv_empty);
       }
       mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0, a.timeout_ns);
@@ -624,6 +627,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_s(s, step);
           issue_dp(s);
+          // Q and dO feed only the S and dP products: once the item's last pair
+          // has completed, the next item's Q/dO copy may land.
+          if (it.hi - it.lo == 1) mma_commit(&bars->qd_empty);
         }
         for (int j = it.lo; j < it.hi; ++j, ++kv_it, ++step) {
           const int s = kv_it % C::kStages;
@@ -646,11 +652,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    sdesc_sw128(sK(s) + kk * 16 * 128, kTile * 128, 1024), idAcc, (kk > 0 || j > it.lo) ? 1u : 0u);
           mma_commit(&bars->kv_empty[s]);
           if (more) issue_dp(s1);
+          if (j + 2 == it.hi) mma_commit(&bars->qd_empty);
         }
         if (!ok) break;
         mma_commit(&bars->acc_full);
         ++acc_cnt;
-        mma_commit(&bars->qd_empty);
       }
       mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0, a.timeout_ns);
