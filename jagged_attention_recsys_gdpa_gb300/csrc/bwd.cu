@@ -385,11 +385,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int clo = ilo - i * kTile - kCols * g, chi = ihi - i * kTile - kCols * g;
         const bool edge = clo > 0 || chi < kCols;
+        // 32-column chunks that no row of this warp sees (short or ragged query
+        // tiles, masked corners) skip the arithmetic: their P and dS are zero.
+        bool skip[kCols / 32];
+#pragma unroll
+        for (int k = 0; k < kCols / 32; ++k) skip[k] = __all_sync(0xffffffffu, max(clo, 32 * k) >= min(chi, 32 * k + 32));
         const uint64_t c2 = f2(a.scale_log2, a.scale_log2);
         const uint64_t* nlse2 = reinterpret_cast<const uint64_t*>(lse_buf);  // (-lse, -lse) pairs
 #pragma unroll
         for (int c0 = 0; c0 < kCols; c0 += 32) {
           uint32_t pk[16];
+          if (skip[c0 / 32]) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) p[c0 + e] = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = 0u;
+            tmem_st16(tSg + c0 / 2, pk);
+            continue;
+          }
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int c = c0 + e;
@@ -440,6 +453,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c0 = 0; c0 < kCols; c0 += 32) {
             uint32_t pk[16];
+            if (skip[c0 / 32]) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) pk[e] = 0u;
+              tmem_st16(tDPg + c0 / 2, pk);
+              continue;
+            }
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
               const int c = c0 + e;
@@ -706,26 +725,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int clo = klo - j * kTile - kCols * g, chi = khi - j * kTile - kCols * g;
         const bool edge = clo > 0 || chi < kCols;
+        // 32-column chunks that no row of this warp sees (rows past a short query
+        // tile, masked corners) skip the arithmetic: their dS is zero.
+        bool skip[kCols / 32];
+#pragma unroll
+        for (int k = 0; k < kCols / 32; ++k) skip[k] = __all_sync(0xffffffffu, max(clo, 32 * k) >= min(chi, 32 * k + 32));
         const uint64_t c2 = f2(a.scale_log2, a.scale_log2), nl2 = f2(-lse2, -lse2);
 #pragma unroll
-        for (int c = 0; c < kCols; c += 2) {
-          float v0, v1;
-          if constexpr (ACT == JATTN_SOFTMAX) {
-            float x0, x1;
-            f2_split(ffma2(f2(p[c], p[c + 1]), c2, nl2), x0, x1);
-            v0 = ex2_approx(x0);
-            v1 = ex2_approx(x1);
-          } else {
-            float f;
-            act_and_grad<ACT>(p[c] * a.scale, f, v0);
-            act_and_grad<ACT>(p[c + 1] * a.scale, f, v1);
+        for (int c0 = 0; c0 < kCols; c0 += 32) {
+          if (skip[c0 / 32]) continue;
+#pragma unroll
+          for (int c = c0; c < c0 + 32; c += 2) {
+            float v0, v1;
+            if constexpr (ACT == JATTN_SOFTMAX) {
+              float x0, x1;
+              f2_split(ffma2(f2(p[c], p[c + 1]), c2, nl2), x0, x1);
+              v0 = ex2_approx(x0);
+              v1 = ex2_approx(x1);
+            } else {
+              float f;
+              act_and_grad<ACT>(p[c] * a.scale, f, v0);
+              act_and_grad<ACT>(p[c + 1] * a.scale, f, v1);
+            }
+            if (edge) {
+              v0 = (c >= clo && c < chi) ? v0 : 0.0f;
+              v1 = (c + 1 >= clo && c + 1 < chi) ? v1 : 0.0f;
+            }
+            p[c] = v0;
+            p[c + 1] = v1;
           }
-          if (edge) {
-            v0 = (c >= clo && c < chi) ? v0 : 0.0f;
-            v1 = (c + 1 >= clo && c + 1 < chi) ? v1 : 0.0f;
-          }
-          p[c] = v0;
-          p[c + 1] = v1;
         }
         const uint64_t ndi2 = f2(-di, -di);
         ok = wait_bar(&bars->dp_full, dp_cnt & 1, abort_flag, a, 91);
@@ -741,6 +769,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c0 = 0; c0 < kCols; c0 += 32) {
             uint32_t pk[16];
+            if (skip[c0 / 32]) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) pk[e] = 0u;
+              tmem_st16(tDPg + c0 / 2, pk);
+              continue;
+            }
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
               const int c = c0 + e;

@@ -359,14 +359,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int delta = it.lkv - it.lq;
         int klo[kNQ], khi[kNQ];
         float m_run[kNQ], l_run[kNQ];
-  #pragma unroll
+#pragma unroll
         for (int q = 0; q < kNQ; ++q) {
           key_interval((it.qb * kNQ + q) * kTile + row, delta, it.lkv, a.mask, a.window, klo[q], khi[q]);
+          if ((it.qb * kNQ + q) * kTile + row >= it.lq) khi[q] = klo[q];  // rows past the sequence see nothing
           m_run[q] = -INFINITY;
           l_run[q] = 0.0f;
         }
         for (int j = it.lo; ok && j < it.hi; ++j) {
-  #pragma unroll
+#pragma unroll
           for (int q = 0; q < kNQ; ++q) {
             if (!ok) break;
             if (j < it.t_lo[q] || j >= it.t_hi[q]) continue;
@@ -384,19 +385,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int clo = klo[q] - j * kTile - half * kHalfCols, chi = khi[q] - j * kTile - half * kHalfCols;
             const bool edge = clo > 0 || chi < kHalfCols;
+            // 32-column chunks that no row of this warp sees (rows past a short query
+            // tile, masked corners) skip the arithmetic: their P is zero.
+            bool skip[kHalfCols / 32];
+#pragma unroll
+            for (int k = 0; k < kHalfCols / 32; ++k) skip[k] = __all_sync(0xffffffffu, max(clo, 32 * k) >= min(chi, 32 * k + 32));
             if constexpr (ACT == JATTN_SOFTMAX) {
               float mx = -INFINITY;
               if (okw) {
                 if (edge) {
-  #pragma unroll
-                  for (int c = 0; c < kHalfCols; ++c) s[c] = (c >= clo && c < chi) ? s[c] : -INFINITY;
+#pragma unroll
+                  for (int k = 0; k < kHalfCols / 32; ++k) {
+                    if (skip[k]) continue;
+#pragma unroll
+                    for (int c = 32 * k; c < 32 * k + 32; ++c) s[c] = (c >= clo && c < chi) ? s[c] : -INFINITY;
+                  }
                 }
                 // row maximum of this half: four independent chains of three-input maxima
                 float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  #pragma unroll
-                for (int c = 0; c < kHalfCols; c += 8)
-  #pragma unroll
-                  for (int e = 0; e < 4; ++e) mp[e] = fmax3(mp[e], s[c + 2 * e], s[c + 2 * e + 1]);
+#pragma unroll
+                for (int k = 0; k < kHalfCols / 32; ++k) {
+                  if (skip[k]) continue;
+#pragma unroll
+                  for (int c = 32 * k; c < 32 * k + 32; c += 8)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) mp[e] = fmax3(mp[e], s[c + 2 * e], s[c + 2 * e + 1]);
+                }
                 mx = fmax3(mp[0], mp[1], fmaxf(mp[2], mp[3]));
               }
               mx = fmaxf(mx, exchange(mx, okw));
@@ -419,12 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // The previous P V product of this tile has completed: the S tile
                 // just waited for was issued after it.
                 const uint32_t tO = tmem + lane_base + C::kOCol + q * D + half * kOHalf;
-  #pragma unroll
+#pragma unroll
                 for (int c = 0; c < kOHalf / 16; ++c) {
                   uint32_t o[16];
                   tmem_ld16(tO + c * 16, o);
                   tmem_ld_wait();
-  #pragma unroll
+#pragma unroll
                   for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                   tmem_st16(tO + c * 16, o);
                 }
@@ -434,10 +448,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               // exponent arguments and row sums two lanes at a time (f32x2)
               const uint64_t c2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-mref, -mref);
               uint64_t ls2[4] = {0, 0, 0, 0};
-  #pragma unroll
+#pragma unroll
               for (int c0 = 0; c0 < kHalfCols; c0 += 32) {
                 uint32_t pk[16];
-  #pragma unroll
+                if (skip[c0 / 32]) {
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                  tmem_st16(tS + c0 / 2, pk);
+                  continue;
+                }
+#pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                   float x0, x1;
                   f2_split(ffma2(f2(s[c0 + e], s[c0 + e + 1]), c2, nm2), x0, x1);
@@ -457,10 +477,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
               }
-  #pragma unroll
+#pragma unroll
               for (int c0 = 0; c0 < kHalfCols; c0 += 32) {
                 uint32_t pk[16];
-  #pragma unroll
+                if (skip[c0 / 32]) {
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                  tmem_st16(tS + c0 / 2, pk);
+                  continue;
+                }
+#pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                   const int c = c0 + e;
                   const float x0 = s[c] * a.scale, x1 = s[c + 1] * a.scale;
@@ -482,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         // ---------------- epilogue: each half stores its O columns of each tile
-  #pragma unroll
+#pragma unroll
         for (int q = 0; q < kNQ; ++q) {
           if (!ok) break;
           if (!it.t_rows[q]) continue;
@@ -512,18 +538,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (n > 0) {
             tc_fence_after();
             const uint32_t tO = tmem + lane_base + C::kOCol + q * D + half * kOHalf;
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < kOHalf / 32; ++c) {
               uint32_t o[32];
               tmem_ld32(tO + c * 32, o);
               tmem_ld_wait();
               if (valid) {
                 uint32_t w[16];
-  #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 16; ++e)
                   w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * oscale, __uint_as_float(o[2 * e + 1]) * oscale);
                 uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-  #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
               }
             }
@@ -575,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float s[kTile];
           {
             uint32_t* su = reinterpret_cast<uint32_t*>(s);
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < kTile / 32; ++c)
               tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(su + c * 32));
             tmem_ld_wait();
@@ -584,14 +610,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool edge = clo > 0 || chi < kTile;
           if constexpr (ACT == JATTN_SOFTMAX) {
             if (edge) {
-  #pragma unroll
+#pragma unroll
               for (int c = 0; c < kTile; ++c) s[c] = (c >= clo && c < chi) ? s[c] : -INFINITY;
             }
             // row maximum: four independent chains of three-input maxima
             float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < kTile; c += 8)
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 4; ++e) mp[e] = fmax3(mp[e], s[c + 2 * e], s[c + 2 * e + 1]);
             const float mx = fmax3(mp[0], mp[1], fmaxf(mp[2], mp[3]));
             const float m_new = mx * a.scale_log2;
@@ -608,12 +634,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (__any_sync(0xffffffffu, rescale)) {
               // The previous P V product of this tile has completed: the S tile
               // just waited for was issued after it.
-  #pragma unroll
+#pragma unroll
               for (int c = 0; c < D / 16; ++c) {
                 uint32_t o[16];
                 tmem_ld16(tO + c * 16, o);
                 tmem_ld_wait();
-  #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                 tmem_st16(tO + c * 16, o);
               }
@@ -623,10 +649,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // exponent arguments and row sums two lanes at a time (f32x2)
             const uint64_t c2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-mref, -mref);
             uint64_t ls2[4] = {0, 0, 0, 0};
-  #pragma unroll
+#pragma unroll
             for (int c0 = 0; c0 < kTile; c0 += 32) {
               uint32_t pk[16];
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 32; e += 2) {
                 float x0, x1;
                 f2_split(ffma2(f2(s[c0 + e], s[c0 + e + 1]), c2, nm2), x0, x1);
@@ -641,10 +667,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             f2_split(fadd2(fadd2(ls2[0], ls2[1]), fadd2(ls2[2], ls2[3])), l0, l1);
             l_run += l0 + l1;
           } else {
-  #pragma unroll
+#pragma unroll
             for (int c0 = 0; c0 < kTile; c0 += 32) {
               uint32_t pk[16];
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 32; e += 2) {
                 const int c = c0 + e;
                 const float x0 = s[c] * a.scale, x1 = s[c + 1] * a.scale;
@@ -678,18 +704,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           ++o_cnt;
           tc_fence_after();
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(tO + c * 32, o);
             tmem_ld_wait();
             if (valid) {
               uint32_t w[16];
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 16; ++e)
                 w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * oscale, __uint_as_float(o[2 * e + 1]) * oscale);
               uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
             }
           }
