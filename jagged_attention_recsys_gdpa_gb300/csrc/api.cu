@@ -95,6 +95,7 @@ int check_params(const jattn_params_t* p) {
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+bool aligned32(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 31u) == 0; }
 
 int check_ws(const jattn_params_t* p, void* ws, size_t ws_bytes) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return JATTN_ERR_WORKSPACE;
@@ -268,6 +269,7 @@ int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
   a.n_tiles = sv.n_tiles;
   a.out0 = reinterpret_cast<__nv_bfloat16*>(o);
   a.f0 = lse;
+  a.out_v8 = aligned32(o);
   prof(0, st);
   if ((e = launch_fwd(p->D, p->act, fwd_split(*p), mq, mk, mv, a, grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
     return cuda_fail("forward kernel launch", e);
@@ -316,6 +318,7 @@ int jattn_fwd_noalloc(const jattn_params_t* p, const int64_t* q_off, const int64
     a.n_tiles = sv.n_tiles;
     a.out0 = reinterpret_cast<__nv_bfloat16*>(o);
     a.f0 = lse;
+    a.out_v8 = aligned32(o);
     if ((e = launch_fwd(p->D, p->act, fwd_split(*p), mq, mk, mv, a, grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
       return cuda_fail("forward kernel launch", e);
   }
@@ -365,6 +368,7 @@ int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
     a.n_tiles = kv.n_tiles;
     a.out0 = reinterpret_cast<__nv_bfloat16*>(dk);
     a.out1 = reinterpret_cast<__nv_bfloat16*>(dv);
+    a.out_v8 = aligned32(dk) && aligned32(dv);
     prof(2, st);
     if ((e = launch_bwd_dkdv(p->D, p->act, mq, mk, mv, mdo, a, grid_for(dev, L.tiles_kv, p->H), st)) !=
         cudaSuccess)
@@ -380,6 +384,7 @@ int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
     a.n_tiles = qs.n_tiles;
     a.out0 = reinterpret_cast<__nv_bfloat16*>(dq);
     a.out1 = nullptr;
+    a.out_v8 = aligned32(dq);
     prof(4, st);
     if ((e = launch_bwd_dq(p->D, p->act, mq, mk, mv, mdo, a, grid_for(dev, L.tiles_q, p->H), st)) != cudaSuccess)
       return cuda_fail("dQ kernel launch", e);

@@ -68,13 +68,11 @@ __device__ __forceinline__ void act_and_grad(float x, float& f, float& g) {
 }
 
 // Store one 128-bit-vectorised bf16 row chunk of 32 fp32 values times `mul`.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&v)[32], float mul) {
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&v)[32], float mul, int v8) {
   uint32_t w[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) d[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+  store_words16(dst, w, v8);
 }
 
 __device__ __forceinline__ void zero_row(__nv_bfloat16* dst, int D) {
@@ -495,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[32];
           tmem_ld32(tAcc + c * 32, v);
           tmem_ld_wait();
-          if (valid) store_row32(out_row + c * 32, v, mul);
+          if (valid) store_row32(out_row + c * 32, v, mul, a.out_v8);
         }
         tc_fence_before();
         mbar_arrive(&bars->acc_empty);
@@ -808,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + C::kDQCol + (D / 2) * g + c * 32, v);
           tmem_ld_wait();
-          if (valid) store_row32(dq_half + c * 32, v, cn * a.scale);
+          if (valid) store_row32(dq_half + c * 32, v, cn * a.scale, a.out_v8);
         }
         tc_fence_before();
         mbar_arrive(&bars->acc_empty);

@@ -43,7 +43,28 @@ struct AttnArgs {
   DevStatus* status;
   uint64_t timeout_ns;
   int debug_flags;
+  int out_v8;              // output rows may be written with 32-byte stores (bases 32-byte aligned)
 };
+
+// Store 16 packed words (32 bf16 values, 64 bytes) of one output row: two
+// 32-byte stores when the output base is 32-byte aligned, else four 16-byte
+// stores. Every row start and column offset used with it is a multiple of
+// 32 bytes, so the base alone decides.
+__device__ __forceinline__ void store_words16(void* dst, const uint32_t (&w)[16], int v8) {
+  if (v8) {
+    uint32_t* p = reinterpret_cast<uint32_t*>(dst);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p + 8 * h), "r"(w[8 * h]),
+                   "r"(w[8 * h + 1]), "r"(w[8 * h + 2]), "r"(w[8 * h + 3]), "r"(w[8 * h + 4]), "r"(w[8 * h + 5]),
+                   "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
+                   : "memory");
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) d[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+  }
+}
 
 // Visible key interval [lo, hi) of sequence-local query row i
 // (bottom-right aligned, delta = Lkv - Lq). Window implies causal.

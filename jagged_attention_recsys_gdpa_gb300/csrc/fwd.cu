@@ -548,9 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                   w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * oscale, __uint_as_float(o[2 * e + 1]) * oscale);
-                uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                store_words16(orow + c * 32, w, a.out_v8);
               }
             }
             tc_fence_before();
@@ -714,9 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < 16; ++e)
                 w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * oscale, __uint_as_float(o[2 * e + 1]) * oscale);
-              uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+              store_words16(orow + c * 32, w, a.out_v8);
             }
           }
           tc_fence_before();

@@ -188,3 +188,33 @@ def test_forward_arrangements(arrangement, act, mask, window, D, lq, lkv):
     finally:
         B.debug_set(0, 0)
     G.compare(g, G.oracle_run(cpu, w, backward=False), w, backward=False)
+
+
+@pytest.mark.parametrize("act", [SOFTMAX, GELU])
+def test_outputs_16_byte_aligned_only(act):
+    """Output tensors that start 16 bytes past a 32-byte boundary (written
+    with 16-byte stores) get the same bits as 32-byte aligned ones (written
+    with 32-byte stores)."""
+    import jagged_attention_recsys_gdpa_gb300 as J
+
+    w = _w(act, CAUSAL if act == SOFTMAX else NONE, 0, 128, norm=act != SOFTMAX, std=1.0 if act == SOFTMAX else 0.5)
+    cpu = G.cpu_inputs(w, SELF_LENS, SELF_LENS, 16)
+    x = G.to_cuda(cpu)
+    kw = dict(act=G.ACT_NAME[act], causal=bool(w.mask & 1), norm_by_lkv=w.norm_by_lkv)
+
+    def shifted_like(t):
+        flat = torch.empty(t.numel() + 8, dtype=t.dtype, device=t.device)  # +8 bf16 = +16 bytes
+        v = flat[8:].view(t.shape)
+        assert v.data_ptr() % 32 == 16
+        return v
+
+    o_ref, lse = J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], **kw)
+    dq_ref, dk_ref, dv_ref = J.backward(x["q"], x["k"], x["v"], o_ref, lse, x["do"], x["q_off"], x["kv_off"], **kw)
+    o = shifted_like(o_ref)
+    J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], out=o, lse=lse, **kw)
+    dq, dk, dv = shifted_like(dq_ref), shifted_like(dk_ref), shifted_like(dv_ref)
+    J.backward(x["q"], x["k"], x["v"], o_ref, lse, x["do"], x["q_off"], x["kv_off"], dq=dq, dk=dk, dv=dv, **kw)
+    torch.cuda.synchronize()
+    for got, ref in ((o, o_ref), (dq, dq_ref), (dk, dk_ref), (dv, dv_ref)):
+        assert torch.equal(got, ref)
+    G.compare({"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}, G.oracle_run(cpu, w), w)
