@@ -353,9 +353,10 @@ int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
   cudaError_t e;
   if (di && (e = launch_bwd_di(o, dout, di, p->total_q, p->H, p->D, st)) != cudaSuccess)
     return cuda_fail("Di kernel launch", e);
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdk, mdv;
   if (make_map(&mq, q, p->total_q, p->H, p->D) || make_map(&mk, k, p->total_kv, p->H, p->D) ||
-      make_map(&mv, v, p->total_kv, p->H, p->D) || make_map(&mdo, dout, p->total_q, p->H, p->D))
+      make_map(&mv, v, p->total_kv, p->H, p->D) || make_map(&mdo, dout, p->total_q, p->H, p->D) ||
+      make_map(&mdk, dk, p->total_kv, p->H, p->D) || make_map(&mdv, dv, p->total_kv, p->H, p->D))
     return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   a.f0 = const_cast<float*>(lse);
   a.f1 = di;
@@ -370,7 +371,7 @@ int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
     a.out1 = reinterpret_cast<__nv_bfloat16*>(dv);
     a.out_v8 = aligned32(dk) && aligned32(dv);
     prof(2, st);
-    if ((e = launch_bwd_dkdv(p->D, p->act, mq, mk, mv, mdo, a, grid_for(dev, L.tiles_kv, p->H), st)) !=
+    if ((e = launch_bwd_dkdv(p->D, p->act, mq, mk, mv, mdo, mdk, mdv, a, grid_for(dev, L.tiles_kv, p->H), st)) !=
         cudaSuccess)
       return cuda_fail("dK/dV kernel launch", e);
     prof(3, st);

@@ -80,6 +80,59 @@ __device__ __forceinline__ void zero_row(__nv_bfloat16* dst, int D) {
   for (int e = 0; e < D / 8; ++e) d[e] = make_uint4(0, 0, 0, 0);
 }
 
+// All 128 threads of an activation warpgroup meet on an mbarrier (count 128);
+// the wait is bounded, so a warpgroup whose other warps have aborted gives up
+// instead of hanging.
+__device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, volatile int* abort_flag,
+                                           const AttnArgs& a, int where) {
+  mbar_arrive(bar);
+  const bool ok = wait_bar(bar, phase & 1, abort_flag, a, where);
+  ++phase;
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Epilogue of a tile whose 128 rows all lie inside the sequence: NCH chunks of
+// 64 accumulator columns. Each thread packs its row of a chunk into the
+// warpgroup's 16 KB staging buffer in the 128-byte-swizzled layout of the
+// tensor map (16-byte piece c of row r at piece c ^ (r mod 8)), and one thread
+// stores the 128 x 64 box with TMA: whole lines instead of one row per thread.
+// The accumulators are released as soon as they are read.
+template <int NCH>
+__device__ __forceinline__ bool staged_store(uint32_t tacc, float mul, uint8_t* stage, int row, bool leader,
+                                             const CUtensorMap* map, int x0, int y0, uint64_t* grp,
+                                             uint32_t& phase, uint64_t* acc_empty, volatile int* abort_flag,
+                                             const AttnArgs& a, int where) {
+  const uint32_t srow = smem_u32(stage) + row * 128;
+#pragma unroll
+  for (int hc = 0; hc < NCH; ++hc) {
+    uint32_t v[64];
+    tmem_ld32(tacc + hc * 64, *reinterpret_cast<uint32_t(*)[32]>(v));
+    tmem_ld32(tacc + hc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+    tmem_ld_wait();
+    if (hc == NCH - 1) {
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+    }
+    if (leader) bulk_wait_read_all();  // the previous store from this buffer has read it
+    if (!group_sync(grp, phase, abort_flag, a, where)) return false;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = pack_bf16x2(__uint_as_float(v[8 * ch + 2 * e]) * mul, __uint_as_float(v[8 * ch + 2 * e + 1]) * mul);
+      st_shared_v4(srow + ((ch ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+    }
+    fence_proxy_async_smem();
+    if (!group_sync(grp, phase, abort_flag, a, where)) return false;
+    if (leader) {
+      tma_store_2d(map, stage, x0 + hc * 64, y0);
+      bulk_commit();
+    }
+  }
+  return true;
+}
+
 struct BwdItem {
   int b, rt, lo, hi, h, lq, lkv;
   int64_t q0, k0;
@@ -142,7 +195,10 @@ struct DkdvCfg {
   static constexpr int kQOff = 2 * kTileBytes;                               // stage s: Q, then dO
   static constexpr int kLseOff = 2 * kTileBytes + kStages * 2 * kTileBytes;  // [2][128] lse2, [2][128] Di
   static constexpr int kBarOff = kLseOff + 4 * kTile * 4;
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  // D = 128: epilogue staging for TMA stores, 16 KB per activation warpgroup
+  static constexpr bool kTmaStore = (D == 128);
+  static constexpr int kStageOff = (kBarOff + 256 + 1023) / 1024 * 1024;
+  static constexpr int kSmemBytes = kStageOff + (kTmaStore ? 2 * 16384 : 0);  // base 1024-aligned (checked)
   static constexpr uint32_t kSCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
 };
 
@@ -151,18 +207,28 @@ struct DkdvBars {
   uint64_t qd_full[3], qd_empty[3];
   uint64_t s_full, dp_full, p_ready, ds_ready, acc_full, acc_empty;
   uint64_t drain;
+  uint64_t grp[2];  // activation warpgroup meeting points (epilogue staging)
   uint32_t tmem_base;
   int abort_flag;
 };
+
+static_assert(sizeof(DkdvBars) <= 256, "barrier block overflows its slot");
+static_assert(DkdvCfg<128>::kSmemBytes <= 227 * 1024 && DkdvCfg<64>::kSmemBytes <= 227 * 1024, "shared memory");
 
 template <int D, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                 const AttnArgs a) {
   using C = DkdvCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned tiles and no slack for realigning: a misaligned base is an error
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) record_error(a.status, JATTN_ERR_UNSUPPORTED, 19, blockIdx.x);
+    return;
+  }
+  uint8_t* sm = smem_raw;
   DkdvBars* bars = reinterpret_cast<DkdvBars*>(sm + C::kBarOff);
   float* s_lse = reinterpret_cast<float*>(sm + C::kLseOff);  // [2][128]
   float* s_di = s_lse + 2 * kTile;                           // [2][128]
@@ -183,6 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, kNG * kTile);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->grp[0], kTile);
+    mbar_init(&bars->grp[1], kTile);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -322,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tSg = tmem + lane_base + C::kSCol + kCols * g;
     const uint32_t tDPg = tmem + lane_base + C::kDPCol + kCols * g;
-    uint32_t s_cnt = 0, acc_cnt = 0, step = 0;
+    uint32_t s_cnt = 0, acc_cnt = 0, step = 0, grp_phase = 0;
     // LSE (log2 units) and Di of query row i*128 + 64g + gt (gt < 64) of an
     // item, loaded into registers one step before they are needed.
     auto fetch = [&](const BwdItem& x, int i, float& l2, float& dd) {
@@ -488,19 +556,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t tAcc = tmem + lane_base + (g == 0 ? C::kDVCol : C::kDKCol);
         const float mul = (g == 0) ? cn : cn * a.scale;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tAcc + c * 32, v);
-          tmem_ld_wait();
-          if (valid) store_row32(out_row + c * 32, v, mul, a.out_v8);
+        bool staged = false;
+        if constexpr (C::kTmaStore) {
+          if ((it.rt + 1) * kTile <= it.lkv) {  // every key row of the tile is in the sequence
+            staged = true;
+            ok = staged_store<D / 64>(tAcc, mul, sm + C::kStageOff + g * 16384, row, gt == 0, g == 0 ? &tmO1 : &tmO0,
+                                      it.h * D, static_cast<int>(it.k0) + it.rt * kTile, &bars->grp[g], grp_phase,
+                                      &bars->acc_empty, abort_flag, a, 63);
+            if (!ok) break;
+          }
         }
-        tc_fence_before();
-        mbar_arrive(&bars->acc_empty);
+        if (!staged) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tAcc + c * 32, v);
+            tmem_ld_wait();
+            if (valid) store_row32(out_row + c * 32, v, mul, a.out_v8);
+          }
+          tc_fence_before();
+          mbar_arrive(&bars->acc_empty);
+        }
       } else if (valid) {
         zero_row(out_row, D);
       }
     }
+    // the stores this thread started complete before the CTA's shared memory goes away
+    if (C::kTmaStore && gt == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -517,7 +599,7 @@ struct DqCfg {
   static constexpr int kDOOff = kTileBytes;
   static constexpr int kKOff = 2 * kTileBytes;  // stage s: K at kKOff + s * 2 tiles, V right after
   static constexpr int kBarOff = 2 * kTileBytes + kStages * 2 * kTileBytes;
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  static constexpr int kSmemBytes = kBarOff + 256;  // base 1024-aligned (checked)
   static constexpr uint32_t kSCol = 0, kDPCol = 256, kDQCol = 384;  // S double-buffered at 0 and 128
 };
 
@@ -530,14 +612,22 @@ struct DqBars {
   int abort_flag;
 };
 
+static_assert(sizeof(DqBars) <= 256, "barrier block overflows its slot");
+static_assert(DqCfg<128>::kSmemBytes <= 227 * 1024 && DqCfg<64>::kSmemBytes <= 227 * 1024, "shared memory");
+
 template <int D, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
               const AttnArgs a) {
   using C = DqCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned tiles and no slack for realigning: a misaligned base is an error
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) record_error(a.status, JATTN_ERR_UNSUPPORTED, 19, blockIdx.x);
+    return;
+  }
+  uint8_t* sm = smem_raw;
   DqBars* bars = reinterpret_cast<DqBars*>(sm + C::kBarOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &bars->abort_flag;
@@ -831,6 +921,16 @@ cudaError_t launch4(K kern, int smem, const CUtensorMap& q, const CUtensorMap& k
   return cudaGetLastError();
 }
 
+template <typename K>
+cudaError_t launch6(K kern, int smem, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                    const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1, const AttnArgs& a,
+                    int grid, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, stream>>>(q, k, v, dout, o0, o1, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_di(const void* o, const void* dout, float* di, int64_t rows, int H, int D,
@@ -845,17 +945,18 @@ cudaError_t launch_bwd_di(const void* o, const void* dout, float* di, int64_t ro
 }
 
 cudaError_t launch_bwd_dkdv(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream) {
+                            const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1, const AttnArgs& a,
+                            int grid, cudaStream_t stream) {
   if (D == 128) {
     constexpr int sm = DkdvCfg<128>::kSmemBytes;
-    if (act == JATTN_SOFTMAX) return launch4(dkdv_kernel<128, JATTN_SOFTMAX>, sm, q, k, v, dout, a, grid, stream);
-    if (act == JATTN_SILU) return launch4(dkdv_kernel<128, JATTN_SILU>, sm, q, k, v, dout, a, grid, stream);
-    return launch4(dkdv_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, a, grid, stream);
+    if (act == JATTN_SOFTMAX) return launch6(dkdv_kernel<128, JATTN_SOFTMAX>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+    if (act == JATTN_SILU) return launch6(dkdv_kernel<128, JATTN_SILU>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+    return launch6(dkdv_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, o0, o1, a, grid, stream);
   }
   constexpr int sm = DkdvCfg<64>::kSmemBytes;
-  if (act == JATTN_SOFTMAX) return launch4(dkdv_kernel<64, JATTN_SOFTMAX>, sm, q, k, v, dout, a, grid, stream);
-  if (act == JATTN_SILU) return launch4(dkdv_kernel<64, JATTN_SILU>, sm, q, k, v, dout, a, grid, stream);
-  return launch4(dkdv_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, a, grid, stream);
+  if (act == JATTN_SOFTMAX) return launch6(dkdv_kernel<64, JATTN_SOFTMAX>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+  if (act == JATTN_SILU) return launch6(dkdv_kernel<64, JATTN_SILU>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+  return launch6(dkdv_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, o0, o1, a, grid, stream);
 }
 
 cudaError_t launch_bwd_dq(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,

@@ -218,3 +218,28 @@ def test_outputs_16_byte_aligned_only(act):
     for got, ref in ((o, o_ref), (dq, dq_ref), (dk, dk_ref), (dv, dv_ref)):
         assert torch.equal(got, ref)
     G.compare({"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}, G.oracle_run(cpu, w), w)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_backward_outputs_only_touch_their_rows(D):
+    """Canary rows around dQ, dK and dV stay untouched: whole-tile stores (TMA
+    boxes of 128 rows) and per-row stores write only the tensors' own rows."""
+    import jagged_attention_recsys_gdpa_gb300 as J
+
+    w = _w(SOFTMAX, CAUSAL, 0, D)
+    lens = [128, 256, 129, 1, 300]
+    cpu = G.cpu_inputs(w, lens, lens, 17)
+    x = G.to_cuda(cpu)
+    T = x["q"].shape[0]
+    pad = 5
+    o, lse = J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], causal=True)
+    bigs = [torch.full((T + 2 * pad, 2, D), 7.0, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    dq, dk, dv = (b[pad : pad + T] for b in bigs)
+    J.backward(x["q"], x["k"], x["v"], o, lse, x["do"], x["q_off"], x["kv_off"], causal=True, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    for b in bigs:
+        assert torch.all(b[:pad] == 7.0) and torch.all(b[pad + T :] == 7.0)
+    r = G.oracle_run(cpu, w)
+    G.assert_close(G.to64(dq), r["dq"], "dQ")
+    G.assert_close(G.to64(dk), r["dk"], "dK")
+    G.assert_close(G.to64(dv), r["dv"], "dV")
