@@ -169,9 +169,10 @@ int jattn_fwd_noalloc(const jattn_params_t* p, const int64_t* q_off, const int64
                       void* stream);
 
 /* Profiling hook: `events` points to six cudaEvent_t (passed as void*) that
- * later calls record on their stream right before and right after the
- * forward, dK/dV and dQ kernel launches (in that order); NULL turns it off.
- * Used to time those kernels with events on the stream they run on. */
+ * later calls record on their stream: events[0] / [1] right before / after the
+ * forward kernel launch, [2] / [3] around the dK/dV kernel, [4] / [5] around
+ * the dQ kernel (which jattn_bwd launches first); NULL turns it off. Used to
+ * time those kernels with events on the stream they run on. */
 void jattn_profile_events(void* const* events);
 
 /* Test hook: after this call, bounded waits in the kernels give up after

@@ -351,15 +351,31 @@ int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
   AttnArgs a = base_args(*p, q_off, kv_off, ws);
   float* di = (p->act == JATTN_SOFTMAX) ? reinterpret_cast<float*>(base + L.di) : nullptr;
   cudaError_t e;
-  if (di && (e = launch_bwd_di(o, dout, di, p->total_q, p->H, p->D, st)) != cudaSuccess)
-    return cuda_fail("Di kernel launch", e);
-  CUtensorMap mq, mk, mv, mdo, mdk, mdv;
+  CUtensorMap mq, mk, mv, mdo, mdk, mdv, mo;
+  std::memset(&mo, 0, sizeof(mo));  // softmax only: the O tiles the dQ pass reads for Di
   if (make_map(&mq, q, p->total_q, p->H, p->D) || make_map(&mk, k, p->total_kv, p->H, p->D) ||
       make_map(&mv, v, p->total_kv, p->H, p->D) || make_map(&mdo, dout, p->total_q, p->H, p->D) ||
-      make_map(&mdk, dk, p->total_kv, p->H, p->D) || make_map(&mdv, dv, p->total_kv, p->H, p->D))
+      make_map(&mdk, dk, p->total_kv, p->H, p->D) || make_map(&mdv, dv, p->total_kv, p->H, p->D) ||
+      (p->act == JATTN_SOFTMAX && make_map(&mo, o, p->total_q, p->H, p->D)))
     return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   a.f0 = const_cast<float*>(lse);
   a.f1 = di;
+  // The dQ pass runs first: for softmax it also writes Di, which the dK/dV pass reads.
+  if (p->total_q > 0) {
+    const SchedView qs = sched_carve(base + L.sched_q, p->B, L.tiles_q);
+    if ((e = sched_launch(qs, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 0,
+                          a.status, st)) != cudaSuccess)
+      return cuda_fail("query-tile schedule launch", e);
+    a.tiles = qs.sorted;
+    a.n_tiles = qs.n_tiles;
+    a.out0 = reinterpret_cast<__nv_bfloat16*>(dq);
+    a.out1 = nullptr;
+    a.out_v8 = aligned32(dq);
+    prof(4, st);
+    if ((e = launch_bwd_dq(p->D, p->act, mq, mk, mv, mdo, mo, a, grid_for(dev, L.tiles_q, p->H), st)) != cudaSuccess)
+      return cuda_fail("dQ kernel launch", e);
+    prof(5, st);
+  }
   if (p->total_kv > 0) {
     const SchedView kv = sched_carve(base + L.sched_kv, p->B, L.tiles_kv);
     if ((e = sched_launch(kv, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 1,
@@ -375,21 +391,6 @@ int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
         cudaSuccess)
       return cuda_fail("dK/dV kernel launch", e);
     prof(3, st);
-  }
-  if (p->total_q > 0) {
-    const SchedView qs = sched_carve(base + L.sched_q, p->B, L.tiles_q);
-    if ((e = sched_launch(qs, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 0,
-                          a.status, st)) != cudaSuccess)
-      return cuda_fail("query-tile schedule launch", e);
-    a.tiles = qs.sorted;
-    a.n_tiles = qs.n_tiles;
-    a.out0 = reinterpret_cast<__nv_bfloat16*>(dq);
-    a.out1 = nullptr;
-    a.out_v8 = aligned32(dq);
-    prof(4, st);
-    if ((e = launch_bwd_dq(p->D, p->act, mq, mk, mv, mdo, a, grid_for(dev, L.tiles_q, p->H), st)) != cudaSuccess)
-      return cuda_fail("dQ kernel launch", e);
-    prof(5, st);
   }
   return JATTN_OK;
 }

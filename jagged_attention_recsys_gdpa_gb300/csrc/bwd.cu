@@ -155,31 +155,6 @@ __device__ __forceinline__ bool load_bwd_item(const AttnArgs& a, long long round
   return true;
 }
 
-// ---------------------------------------------------------------------------- Di
-// One group of D/8 threads per (row, head): each thread reads 16 bytes of O
-// and of dO, the group reduces with shuffles.
-__global__ void __launch_bounds__(256) di_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
-                                                 float* __restrict__ di, int64_t n_rowheads, int D) {
-  const int group = D / 8;
-  const int64_t gid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
-  const int64_t rh = gid / group;
-  const int part = static_cast<int>(gid % group);
-  float acc = 0.0f;
-  if (rh < n_rowheads) {
-    const uint4 x = o[rh * group + part], y = dout[rh * group + part];
-    const __nv_bfloat162* xa = reinterpret_cast<const __nv_bfloat162*>(&x);
-    const __nv_bfloat162* ya = reinterpret_cast<const __nv_bfloat162*>(&y);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 fx = __bfloat1622float2(xa[e]), fy = __bfloat1622float2(ya[e]);
-      acc = fmaf(fx.x, fy.x, acc);
-      acc = fmaf(fx.y, fy.y, acc);
-    }
-  }
-  for (int off = group / 2; off > 0; off >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, off, group);
-  if (rh < n_rowheads && part == 0) di[rh] = acc;
-}
-
 // ---------------------------------------------------------------------------- dK / dV
 // TMEM address of the A operand for K-step kk of a 128-column score tile
 // whose bf16 pairs were written by the two activation warpgroups: group g
@@ -599,7 +574,9 @@ struct DqCfg {
   static constexpr int kDOOff = kTileBytes;
   static constexpr int kKOff = 2 * kTileBytes;  // stage s: K at kKOff + s * 2 tiles, V right after
   static constexpr int kBarOff = 2 * kTileBytes + kStages * 2 * kTileBytes;
-  static constexpr int kSmemBytes = kBarOff + 256;  // base 1024-aligned (checked)
+  static constexpr int kDiOff = kBarOff + 256;  // [2][128] Di handed to the activation warpgroups
+  static constexpr int kOOff = (kDiOff + 2 * kTile * 4 + 1023) / 1024 * 1024;  // O tile (softmax: Di)
+  static constexpr int kSmemBytes = kOOff + kTileBytes;                        // base 1024-aligned (checked)
   static constexpr uint32_t kSCol = 0, kDPCol = 256, kDQCol = 384;  // S double-buffered at 0 and 128
 };
 
@@ -607,6 +584,8 @@ struct DqBars {
   uint64_t qd_full, qd_empty;
   uint64_t kv_full[3], kv_empty[3];
   uint64_t s_full[2], dp_full, ds_ready, acc_full, acc_empty;
+  uint64_t di_full[2], di_empty[2];  // Di slots (softmax)
+  uint64_t ot_full, ot_empty;         // O tile for Di (softmax)
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -619,7 +598,7 @@ template <int D, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-              const AttnArgs a) {
+              const __grid_constant__ CUtensorMap tmO, const AttnArgs a) {
   using C = DqCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned tiles and no slack for realigning: a misaligned base is an error
@@ -634,7 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->qd_full, 1);
-    mbar_init(&bars->qd_empty, 1);
+    // softmax: the Di warps read dO from this buffer too, so they also release it
+    mbar_init(&bars->qd_empty, ACT == JATTN_SOFTMAX ? 1 + 64 : 1);
+    mbar_init(&bars->ot_full, 1);
+    mbar_init(&bars->ot_empty, 64);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
@@ -645,6 +627,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->ds_ready, kNG * kTile);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, kNG * kTile);
+    for (int s2 = 0; s2 < 2; ++s2) {
+      mbar_init(&bars->di_full[s2], 64);
+      mbar_init(&bars->di_empty[s2], kNG * kTile);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -679,6 +665,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sm + C::kDOOff + c * kTile * 128, &tmDO, &bars->qd_full, it.h * D + c * 64, yq);
           }
           q_armed = true;
+          if constexpr (ACT == JATTN_SOFTMAX) {  // O tile for the Di warps
+            if (!(ok = wait_bar(&bars->ot_empty, (item_cnt - 1) & 1 ^ 1, abort_flag, a, 72))) break;
+            mbar_arrive_expect_tx(&bars->ot_full, C::kTileBytes);
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_2d(sm + C::kOOff + c * kTile * 128, &tmO, &bars->ot_full, it.h * D + c * 64, yq);
+          }
         }
         for (int j = it.lo; j < it.hi; ++j, ++kv_it) {
           const int s = kv_it % C::kStages;
@@ -693,6 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (q_armed) drain_wait(&bars->qd_full, (item_cnt - 1) & 1, a.timeout_ns);
+      if (q_armed && ACT == JATTN_SOFTMAX) drain_wait(&bars->ot_full, (item_cnt - 1) & 1, a.timeout_ns);
       for (uint32_t i = (kv_it > (uint32_t)C::kStages ? kv_it - C::kStages : 0); i < kv_it; ++i)
         drain_wait(&bars->kv_full[i % C::kStages], (i / C::kStages) & 1, a.timeout_ns);
     }
@@ -769,6 +762,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(&bars->drain, 0, a.timeout_ns);
     }
     __syncwarp();
+  } else if (ACT == JATTN_SOFTMAX) {
+    // ------------------------------------------------------------ Di warps (2, 3)
+    // Di = rowsum(dO * O) for each item's 128 query rows, from the dO tile the
+    // producer loaded for the MMAs and an O tile loaded for this purpose: into a
+    // shared-memory slot for the activation warpgroups and to global memory for
+    // the dK/dV pass, which runs after this one. Lane l of warp 2 + w owns tile
+    // rows 64w + l and 64w + 32 + l. Both tiles share the 128-byte-swizzled
+    // layout, so reading the same addresses pairs the same columns; walking a
+    // row's 16-byte pieces in swizzled order spreads the lanes over the banks.
+    const int dw = warp - 2;
+    float* di_s = reinterpret_cast<float*>(sm + C::kDiOff);
+    const uint32_t sO = smem_u32(sm + C::kOOff), sDO = smem_u32(sm + C::kDOOff);
+    uint32_t n_item = 0;
+    BwdItem it;
+    for (long long r = 0; load_bwd_item(a, r, it); ++r) {
+      if (it.hi <= it.lo) continue;  // no Q/dO/O copy for it, and nothing reads its Di
+      const int slot = n_item & 1;
+      bool ok = wait_bar(&bars->di_empty[slot], ((n_item >> 1) & 1) ^ 1, abort_flag, a, 75);
+      ok = ok && wait_bar(&bars->qd_full, n_item & 1, abort_flag, a, 76);
+      ok = ok && wait_bar(&bars->ot_full, n_item & 1, abort_flag, a, 77);
+      if (!__all_sync(0xffffffffu, ok)) break;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int rl = 64 * dw + 32 * h2 + lane;
+        float acc = 0.0f;
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb) {
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint32_t off = cb * (kTile * 128) + rl * 128 + ((ch ^ (rl & 7)) << 4);
+            uint32_t x[4], y[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                         : "r"(sO + off));
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(y[0]), "=r"(y[1]), "=r"(y[2]), "=r"(y[3])
+                         : "r"(sDO + off));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x[e]));
+              const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&y[e]));
+              acc = fmaf(xf.x, yf.x, fmaf(xf.y, yf.y, acc));
+            }
+          }
+        }
+        const int il = it.rt * kTile + rl;
+        di_s[slot * kTile + rl] = acc;
+        if (il < it.lq) a.f1[(it.q0 + il) * a.H + it.h] = acc;
+      }
+      mbar_arrive(&bars->di_full[slot]);
+      mbar_arrive(&bars->ot_empty);
+      mbar_arrive(&bars->qd_empty);
+      ++n_item;
+    }
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kActRegs));
@@ -776,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = 32 * (warp & 3) + lane;         // TMEM lane == query row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tDPg = tmem + lane_base + C::kDPCol + kCols * g;
-    uint32_t step = 0, dp_cnt = 0, acc_cnt = 0;
+    uint32_t step = 0, dp_cnt = 0, acc_cnt = 0, di_item = 0;
     BwdItem it, nit;
     bool have = load_bwd_item(a, 0, it), have_next = false;
     for (long long r = 0; have; ++r, it = nit, have = have_next) {
@@ -790,9 +835,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t gi = (it.q0 + il) * a.H + it.h;
       float lse2 = 0.0f, di = 0.0f;
       if constexpr (ACT == JATTN_SOFTMAX) {
-        if (valid && khi > klo) {
-          lse2 = a.f0[gi] * kLog2e;
-          di = a.f1[gi];
+        if (it.hi > it.lo) {  // items without a key tile use no Di and get no slot
+          // Di of this row from the Di warps' slot for this item
+          const int slot = di_item & 1;
+          bool okd = wait_bar(&bars->di_full[slot], (di_item >> 1) & 1, abort_flag, a, 94);
+          if (!__all_sync(0xffffffffu, okd)) break;
+          const float di_row = reinterpret_cast<const float*>(sm + C::kDiOff)[slot * kTile + row];
+          mbar_arrive(&bars->di_empty[slot]);
+          ++di_item;
+          if (valid && khi > klo) {
+            lse2 = a.f0[gi] * kLog2e;
+            di = di_row;
+          }
         }
       }
       __nv_bfloat16* dq_half = a.out0 + gi * D + (D / 2) * g;  // group g stores dQ columns [gD/2, (g+1)D/2)
@@ -913,11 +967,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <typename K>
-cudaError_t launch4(K kern, int smem, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                    const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream) {
+cudaError_t launch5(K kern, int smem, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                    const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a, int grid, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(q, k, v, dout, a);
+  kern<<<grid, kThreads, smem, stream>>>(q, k, v, dout, o, a);
   return cudaGetLastError();
 }
 
@@ -932,17 +986,6 @@ cudaError_t launch6(K kern, int smem, const CUtensorMap& q, const CUtensorMap& k
 }
 
 }  // namespace
-
-cudaError_t launch_bwd_di(const void* o, const void* dout, float* di, int64_t rows, int H, int D,
-                          cudaStream_t stream) {
-  const int64_t n = rows * H;
-  if (n == 0) return cudaSuccess;
-  const int64_t threads = n * (D / 8);
-  const int64_t blocks = (threads + 255) / 256;
-  di_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<const uint4*>(o),
-                                                               static_cast<const uint4*>(dout), di, n, D);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_bwd_dkdv(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1, const AttnArgs& a,
@@ -960,17 +1003,19 @@ cudaError_t launch_bwd_dkdv(int D, int act, const CUtensorMap& q, const CUtensor
 }
 
 cudaError_t launch_bwd_dq(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream) {
+                          const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a, int grid,
+                          cudaStream_t stream) {
   if (D == 128) {
-    constexpr int sm = DqCfg<128>::kSmemBytes;
-    if (act == JATTN_SOFTMAX) return launch4(dq_kernel<128, JATTN_SOFTMAX>, sm, q, k, v, dout, a, grid, stream);
-    if (act == JATTN_SILU) return launch4(dq_kernel<128, JATTN_SILU>, sm, q, k, v, dout, a, grid, stream);
-    return launch4(dq_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, a, grid, stream);
+    // the O tile for Di is only needed (and its shared memory only taken) for softmax
+    const int sm = act == JATTN_SOFTMAX ? DqCfg<128>::kSmemBytes : DqCfg<128>::kOOff;
+    if (act == JATTN_SOFTMAX) return launch5(dq_kernel<128, JATTN_SOFTMAX>, sm, q, k, v, dout, o, a, grid, stream);
+    if (act == JATTN_SILU) return launch5(dq_kernel<128, JATTN_SILU>, sm, q, k, v, dout, o, a, grid, stream);
+    return launch5(dq_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, o, a, grid, stream);
   }
-  constexpr int sm = DqCfg<64>::kSmemBytes;
-  if (act == JATTN_SOFTMAX) return launch4(dq_kernel<64, JATTN_SOFTMAX>, sm, q, k, v, dout, a, grid, stream);
-  if (act == JATTN_SILU) return launch4(dq_kernel<64, JATTN_SILU>, sm, q, k, v, dout, a, grid, stream);
-  return launch4(dq_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, a, grid, stream);
+  const int sm = act == JATTN_SOFTMAX ? DqCfg<64>::kSmemBytes : DqCfg<64>::kOOff;
+  if (act == JATTN_SOFTMAX) return launch5(dq_kernel<64, JATTN_SOFTMAX>, sm, q, k, v, dout, o, a, grid, stream);
+  if (act == JATTN_SILU) return launch5(dq_kernel<64, JATTN_SILU>, sm, q, k, v, dout, o, a, grid, stream);
+  return launch5(dq_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, o, a, grid, stream);
 }
 
 }  // namespace jattn

@@ -37,7 +37,7 @@ struct AttnArgs {
   __nv_bfloat16* out0;
   __nv_bfloat16* out1;
   float* f0;               // lse (fwd) / lse (bwd)
-  const float* f1;         // Di (bwd)
+  float* f1;               // Di (bwd): written by the dQ pass, read by the dK/dV pass
   const __nv_bfloat16* in0;
   const __nv_bfloat16* in1;
   DevStatus* status;

@@ -14,16 +14,16 @@ cudaError_t launch_fwd(int D, int act, bool split, const CUtensorMap& q, const C
                        const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream);
 int fwd_rows_per_item();
 
-// Backward: Di = rowsum(dO * O) (softmax only).
-cudaError_t launch_bwd_di(const void* o, const void* dout, float* di, int64_t rows, int H, int D,
-                          cudaStream_t stream);
 // dK, dV over key tiles (transposed schedule, 128-row key tiles). o0 / o1 map
 // dK / dV (tile stores of whole tiles).
 cudaError_t launch_bwd_dkdv(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1, const AttnArgs& a,
                             int grid, cudaStream_t stream);
-// dQ over query tiles (128-row query tiles).
+// dQ over query tiles (128-row query tiles). For softmax it also computes
+// Di = rowsum(dO * O) from the dO tiles and O tiles (map `o`) into a.f1, so
+// it runs before the dK/dV pass, which reads Di.
 cudaError_t launch_bwd_dq(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream);
+                          const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a, int grid,
+                          cudaStream_t stream);
 
 }  // namespace jattn
