@@ -39,9 +39,10 @@ def kernel_work(total_q: int, total_kv: int, pairs: int, H: int, D: int, softmax
     """Algorithmic FLOPs and HBM bytes of each kernel (each byte read or written once).
 
     forward: reads Q, K, V, writes O (+ LSE)
+    dq:      reads Q, K, V, dO (+ LSE), writes dQ; the dQ product (its score
+             and dP recompute are not algorithmic work). For softmax it also
+             reads O and writes Di = rowsum(dO * O), which the dK/dV pass uses.
     dkdv:    reads Q, K, V, dO (+ LSE, Di), writes dK, dV; products S, dP, dV, dK
-    dq:      reads Q, K, V, dO (+ LSE, Di), writes dQ; the dQ product (its score
-             and dP recompute are not algorithmic work)
     """
     e = 2 * H * D  # bytes of one row of a [total, H, D] bf16 tensor
     stats = 4 * H * total_q
@@ -49,5 +50,6 @@ def kernel_work(total_q: int, total_kv: int, pairs: int, H: int, D: int, softmax
         "fwd": {"flops": 4.0 * D * H * pairs, "bytes": e * (2 * total_q + 2 * total_kv) + (stats if softmax else 0)},
         "dkdv": {"flops": 8.0 * D * H * pairs,
                  "bytes": e * (2 * total_q + 4 * total_kv) + (2 * stats if softmax else 0)},
-        "dq": {"flops": 2.0 * D * H * pairs, "bytes": e * (3 * total_q + 2 * total_kv) + (2 * stats if softmax else 0)},
+        "dq": {"flops": 2.0 * D * H * pairs,
+               "bytes": e * (3 * total_q + 2 * total_kv) + ((e * total_q + 2 * stats) if softmax else 0)},
     }
