@@ -40,7 +40,7 @@ constexpr int kNQ = 2;          // query tiles per item
 constexpr int kThreads = 384;   // 12 warps: control warpgroup + two activation warpgroups
 constexpr float kRescaleLog2 = 8.0f;
 // Register split (setmaxnreg): 384 threads x 168 at launch = 64512 =
-// 128 x 40 (control warpgroup) + 256 x 232 (activation warpgroups).
+// 128 x 104 (control warpgroup) + 256 x 200 (activation warpgroups).
 constexpr int kCtlRegs = 104;
 constexpr int kActRegs = 200;
 
