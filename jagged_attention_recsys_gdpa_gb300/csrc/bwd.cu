@@ -19,6 +19,8 @@
 // transcendental and conversion instructions that one warp cannot.
 #include <cstdint>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -431,19 +433,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool skip[kCols / 32];
 #pragma unroll
         for (int k = 0; k < kCols / 32; ++k) skip[k] = __all_sync(0xffffffffu, max(clo, 32 * k) >= min(chi, 32 * k + 32));
+        // chunks that every row of the warp sees whole need no per-element mask
+        bool whole[kCols / 32];
+#pragma unroll
+        for (int k = 0; k < kCols / 32; ++k) whole[k] = __all_sync(0xffffffffu, clo <= 32 * k && chi >= 32 * k + 32);
         const uint64_t c2 = f2(a.scale_log2, a.scale_log2);
         const uint64_t* nlse2 = reinterpret_cast<const uint64_t*>(lse_buf);  // (-lse, -lse) pairs
-#pragma unroll
-        for (int c0 = 0; c0 < kCols; c0 += 32) {
-          uint32_t pk[16];
-          if (skip[c0 / 32]) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) p[c0 + e] = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) pk[e] = 0u;
-            tmem_st16(tSg + c0 / 2, pk);
-            continue;
-          }
+        // P (and act' for the pointwise activations) of one 32-column chunk
+        auto chunk_p = [&](int c0, uint32_t(&pk)[16], auto masked) {
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int c = c0 + e;
@@ -453,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               f2_split(ffma2(f2(p[c], p[c + 1]), c2, nlse2[c / 2]), x0, x1);
               f0 = ex2_approx(x0);
               f1 = ex2_approx(x1);
-              if (edge) {
+              if constexpr (decltype(masked)::value) {
                 f0 = (c >= clo && c < chi) ? f0 : 0.0f;
                 f1 = (c + 1 >= clo && c + 1 < chi) ? f1 : 0.0f;
               }
@@ -463,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               float g0, g1;
               act_and_grad<ACT>(p[c] * a.scale, f0, g0);
               act_and_grad<ACT>(p[c + 1] * a.scale, f1, g1);
-              if (edge) {
+              if (decltype(masked)::value && edge) {
                 const bool a0 = c >= clo && c < chi, a1 = c + 1 >= clo && c + 1 < chi;
                 f0 = a0 ? f0 : 0.0f;
                 g0 = a0 ? g0 : 0.0f;
@@ -475,6 +472,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pk[e / 2] = pack_bf16x2(f0, f1);
           }
+        };
+#pragma unroll
+        for (int c0 = 0; c0 < kCols; c0 += 32) {
+          uint32_t pk[16];
+          if (skip[c0 / 32]) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) p[c0 + e] = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = 0u;
+            tmem_st16(tSg + c0 / 2, pk);
+            continue;
+          }
+          // softmax: a second, unmasked copy for whole chunks; the longer pointwise
+          // bodies keep one copy (two would crowd the instruction cache)
+          if (ACT == JATTN_SOFTMAX && whole[c0 / 32])
+            chunk_p(c0, pk, std::integral_constant<bool, ACT != JATTN_SOFTMAX>{});
+          else
+            chunk_p(c0, pk, std::true_type{});
           tmem_st16(tSg + c0 / 2, pk);
         }
         tmem_st_wait();
@@ -872,10 +887,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool skip[kCols / 32];
 #pragma unroll
         for (int k = 0; k < kCols / 32; ++k) skip[k] = __all_sync(0xffffffffu, max(clo, 32 * k) >= min(chi, 32 * k + 32));
-        const uint64_t c2 = f2(a.scale_log2, a.scale_log2), nl2 = f2(-lse2, -lse2);
+        // chunks that every row of the warp sees whole need no per-element mask
+        bool whole[kCols / 32];
 #pragma unroll
-        for (int c0 = 0; c0 < kCols; c0 += 32) {
-          if (skip[c0 / 32]) continue;
+        for (int k = 0; k < kCols / 32; ++k) whole[k] = __all_sync(0xffffffffu, clo <= 32 * k && chi >= 32 * k + 32);
+        const uint64_t c2 = f2(a.scale_log2, a.scale_log2), nl2 = f2(-lse2, -lse2);
+        auto chunk_p = [&](int c0, auto masked) {
 #pragma unroll
           for (int c = c0; c < c0 + 32; c += 2) {
             float v0, v1;
@@ -889,13 +906,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               act_and_grad<ACT>(p[c] * a.scale, f, v0);
               act_and_grad<ACT>(p[c + 1] * a.scale, f, v1);
             }
-            if (edge) {
+            if (decltype(masked)::value && (ACT == JATTN_SOFTMAX || edge)) {
               v0 = (c >= clo && c < chi) ? v0 : 0.0f;
               v1 = (c + 1 >= clo && c + 1 < chi) ? v1 : 0.0f;
             }
             p[c] = v0;
             p[c + 1] = v1;
           }
+        };
+#pragma unroll
+        for (int c0 = 0; c0 < kCols; c0 += 32) {
+          if (skip[c0 / 32]) continue;
+          // softmax: a second, unmasked copy for whole chunks; the longer pointwise
+          // bodies keep one copy (two would crowd the instruction cache)
+          if (ACT == JATTN_SOFTMAX && whole[c0 / 32])
+            chunk_p(c0, std::integral_constant<bool, ACT != JATTN_SOFTMAX>{});
+          else
+            chunk_p(c0, std::true_type{});
         }
         const uint64_t ndi2 = f2(-di, -di);
         ok = wait_bar(&bars->dp_full, dp_cnt & 1, abort_flag, a, 91);
