@@ -37,9 +37,9 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # (profiles/<kernel>_kernel_jfa.md). Reported only while the kernel source
 # still has the sha1 prefix recorded at capture time; otherwise null.
 NCU_TRAFFIC = {
-    ("jfa", "fwd"): ("fwd.cu", "8bf195db9006", 944580352),
-    ("jfa", "dkdv"): ("bwd.cu", "376a537e1c7a", 1385640960),
-    ("jfa", "dq"): ("bwd.cu", "376a537e1c7a", 1407987480),
+    ("jfa", "fwd"): ("fwd.cu", "8bf195db9006", 944765184),
+    ("jfa", "dkdv"): ("bwd.cu", "ea5c93b31de3", 1389054464),
+    ("jfa", "dq"): ("bwd.cu", "ea5c93b31de3", 1408700344),
 }
 
 
