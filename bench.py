@@ -176,6 +176,13 @@ def cpu_oracle_step(x_cpu, w, seqs):
     return time.perf_counter() - t0
 
 
+def workload_desc(name, w, batch):
+    """The workload as both arms name it in `config.workload`."""
+    act = "softmax" if w.act == 0 else ("silu" if w.act == 1 else "gelu")
+    mask = "causal" if w.mask == 1 else ("causal+window" if w.mask == 3 else "none")
+    return f"{name}: B={batch}, H={w.H}, D={w.D}, {act}, mask={mask}" + (f" {w.window}" if w.mask & 2 else "")
+
+
 def run_reference(args, ws, rank):
     """The CPU oracle timed on this host's cores (rank 0 only)."""
     if rank != 0:
@@ -197,11 +204,12 @@ def run_reference(args, ws, rank):
     sample = (f"{len(seqs)} of {len(x['lq'])} sequences ({int(pairs[seqs].sum())} allowed pairs per head), "
               f"fwd+bwd in fp64")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 0,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded lengths and values)",
-        "config": {"workload": args.workload, "sample": sample},
+        "config": {"workload": workload_desc(args.workload, w, len(x["lq"])), "sample": sample,
+                   "device": f"host CPU, {cores} threads (the oracle; rank 0 only)"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -445,10 +453,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded lengths and values)",
             "config": {
-                "workload": f"{args.workload}: B={len(x['lq'])}, H={w.H}, D={w.D}, "
-                            f"{'softmax' if w.act == 0 else ('silu' if w.act == 1 else 'gelu')}, "
-                            f"mask={'causal' if w.mask == 1 else ('causal+window' if w.mask == 3 else 'none')}"
-                            + (f" {w.window}" if w.mask & 2 else ""),
+                "workload": workload_desc(args.workload, w, len(x["lq"])),
                 "total_q": tq, "total_kv": tk, "pairs_per_head": pairs,
                 "l2": f"inputs larger than L2 ({tq * w.H * w.D * 2 / 1e6:.0f} MB per bf16 tensor)",
                 "parallelism": f"replicas x{ws} (independent batches, no collective)",
