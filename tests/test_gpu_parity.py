@@ -243,3 +243,12 @@ def test_backward_outputs_only_touch_their_rows(D):
     G.assert_close(G.to64(dq), r["dq"], "dQ")
     G.assert_close(G.to64(dk), r["dk"], "dK")
     G.assert_close(G.to64(dv), r["dv"], "dV")
+
+
+@pytest.mark.parametrize("act", [SOFTMAX, SILU])
+@pytest.mark.parametrize("lq,lkv", [([5, 130, 0], [0, 0, 0]), ([0, 0], [7, 300])])
+def test_batch_without_keys_or_queries(act, lq, lkv):
+    """A batch with no key rows at all (every output row sees nothing: O = 0,
+    LSE = -inf, dQ = 0) or no query rows at all (dK = dV = 0)."""
+    w = _w(act, NONE, 0, 128, norm=act != SOFTMAX)
+    _check(w, lq, lkv, seed=18)
