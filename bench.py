@@ -38,8 +38,8 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # still has the sha1 prefix recorded at capture time; otherwise null.
 NCU_TRAFFIC = {
     ("jfa", "fwd"): ("fwd.cu", "8bf195db9006", 944765184),
-    ("jfa", "dkdv"): ("bwd.cu", "ea5c93b31de3", 1389054464),
-    ("jfa", "dq"): ("bwd.cu", "ea5c93b31de3", 1408700344),
+    ("jfa", "dkdv"): ("bwd.cu", "66ed76b6b2e7", 1389054464),
+    ("jfa", "dq"): ("bwd.cu", "66ed76b6b2e7", 1408700344),
 }
 
 

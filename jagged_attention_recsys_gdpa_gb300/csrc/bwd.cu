@@ -4,12 +4,16 @@
 // backward parallelisation: for many sequences x heads the fastest scheme is
 // not to split a sequence's key range across CTAs and to compute dQ in its
 // own pass (split dQ / dK-dV), so that no atomic adds are needed. Here:
-//   di    Di = rowsum(dO * O) per query row and head (softmax only)
+//   dq    one item = (sequence, 128-query tile, head); walks its key tiles:
+//         S = Q K^T, dP = dO V^T, dS, dQ += dS K. For softmax its warps 2-3
+//         also compute Di = rowsum(dO * O) per query row and head (section
+//         "BlockAttention" of the same post names the separate Di
+//         preprocessing pass of FlashAttention, which this removes), so it
+//         runs first and the dK/dV pass reads Di.
 //   dkdv  one item = (sequence, 128-key tile, head); walks the query tiles
 //         that can see it: S^T = K Q^T, dP^T = V dO^T, P^T and dS^T from the
-//         activation, dV += P^T dO, dK += dS^T Q (all accumulated in TMEM)
-//   dq    one item = (sequence, 128-query tile, head); walks its key tiles:
-//         S = Q K^T, dP = dO V^T, dS, dQ += dS K
+//         activation, dV += P^T dO, dK += dS^T Q (all accumulated in TMEM);
+//         whole tiles of dK and dV leave through shared memory and TMA stores
 // Both MMA kernels are persistent and warp-specialised: warp 0 issues TMA
 // copies, warp 1 issues tcgen05 MMAs, and two activation warpgroups (warps
 // 4-7 and 8-11; one TMEM lane per thread) split every 128-column score tile
@@ -28,7 +32,7 @@ namespace jattn {
 
 namespace {
 
-constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 2-3 idle, warps 4-7 and 8-11 activation
+constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 2-3 Di (dQ, softmax) or idle, warps 4-11 activation
 // Register split (setmaxnreg, per warpgroup): 384 x 168 at launch = 64512 =
 // 128 x 104 (control warpgroup) + 256 x 200 (activation warpgroups).
 constexpr int kCtlRegs = 104;
