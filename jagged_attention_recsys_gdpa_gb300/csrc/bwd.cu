@@ -445,13 +445,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t* nlse2 = reinterpret_cast<const uint64_t*>(lse_buf);  // (-lse, -lse) pairs
         // P (and act' for the pointwise activations) of one 32-column chunk
         auto chunk_p = [&](int c0, uint32_t(&pk)[16], auto masked) {
+          ulonglong2 nl4;  // two (-lse, -lse) pairs per 16-byte shared load
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int c = c0 + e;
             float f0, f1;
             if constexpr (ACT == JATTN_SOFTMAX) {
+              if ((e & 2) == 0) nl4 = reinterpret_cast<const ulonglong2*>(nlse2)[c / 4];
               float x0, x1;
-              f2_split(ffma2(f2(p[c], p[c + 1]), c2, nlse2[c / 2]), x0, x1);
+              f2_split(ffma2(f2(p[c], p[c + 1]), c2, (e & 2) ? nl4.y : nl4.x), x0, x1);
               f0 = ex2_approx(x0);
               f1 = ex2_approx(x1);
               if constexpr (decltype(masked)::value) {
@@ -519,12 +521,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_st16(tDPg + c0 / 2, pk);
               continue;
             }
+            ulonglong2 nd4;  // two (-Di, -Di) pairs per 16-byte shared load
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
               const int c = c0 + e;
               float d0, d1;
               if constexpr (ACT == JATTN_SOFTMAX) {
-                const uint64_t ndi2 = reinterpret_cast<const uint64_t*>(di_buf)[c / 2];
+                if ((e & 2) == 0) nd4 = reinterpret_cast<const ulonglong2*>(di_buf)[c / 4];
+                const uint64_t ndi2 = (e & 2) ? nd4.y : nd4.x;
                 f2_split(fmul2(f2(p[c], p[c + 1]),
                                fadd2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), ndi2)), d0, d1);
               } else {
