@@ -179,8 +179,8 @@ def cpu_oracle_step(x_cpu, w, seqs):
 def workload_desc(name, w, batch):
     """The workload as both arms name it in `config.workload`."""
     act = "softmax" if w.act == 0 else ("silu" if w.act == 1 else "gelu")
-    mask = "causal" if w.mask == 1 else ("causal+window" if w.mask == 3 else "none")
-    return f"{name}: B={batch}, H={w.H}, D={w.D}, {act}, mask={mask}" + (f" {w.window}" if w.mask & 2 else "")
+    mask = {0: "none", 1: "causal", 3: "causal+window", 4: "block", 5: "causal+block"}[w.mask]
+    return f"{name}: B={batch}, H={w.H}, D={w.D}, {act}, mask={mask}" + (f" {w.window}" if w.mask & 6 else "")
 
 
 def run_reference(args, ws, rank):
@@ -248,7 +248,8 @@ def main():
     x = inputs.make(args.workload, seed=rank, device=dev, lens=inputs.lengths(args.workload, 0))
     causal = bool(w.mask & 1)
     window = w.window if w.mask & 2 else 0
-    kw = dict(act=w.act, causal=causal, window=window, norm_by_lkv=w.norm_by_lkv)
+    block = w.window if w.mask & 4 else 0
+    kw = dict(act=w.act, causal=causal, window=window, block=block, norm_by_lkv=w.norm_by_lkv)
     pairs_b = flops.pairs_per_sequence(x["lq"], x["lkv"], w.mask, w.window)
     pairs = int(pairs_b.sum())
     f_fwd, f_bwd = flops.effective_flops(pairs, w.H, w.D)

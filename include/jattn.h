@@ -7,10 +7,12 @@
  * section "Generalized Dot-Product Attention (GDPA)": the same two matrix
  * products with an element-wise GELU or SiLU in place of the softmax, one
  * kernel for self-, cross- and pooling attention; section "BlockAttention":
- * sliding windows for long self-attention). For every sequence b and head h,
+ * sliding windows for long self-attention, then fixed blocks in which each
+ * query block sees only its own key block). For every sequence b and head h,
  * with query rows i < Lq(b), key rows j < Lkv(b), delta = Lkv - Lq:
  *
- *   allowed(i, j)  causal: j <= i + delta;  window W: 0 <= i + delta - j < W
+ *   allowed(i, j)  causal: j <= i + delta;  window W: 0 <= i + delta - j < W;
+ *                  block W: floor(j / W) == floor((i + delta) / W)
  *   s_ij = scale * <q_i, k_j>
  *   JATTN_SOFTMAX     o_i = sum_j softmax_j(s_ij) v_j over allowed j,
  *                     lse_i = ln sum_j exp(s_ij)  (no allowed key: o_i = 0,
@@ -56,8 +58,11 @@ enum {
   JATTN_GELU_TANH = 2  /* x/2 (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))) (GDPA) */
 };
 
-/* Mask bits. JATTN_MASK_WINDOW must be combined with JATTN_MASK_CAUSAL. */
-enum { JATTN_MASK_NONE = 0, JATTN_MASK_CAUSAL = 1, JATTN_MASK_WINDOW = 2 };
+/* Mask bits. JATTN_MASK_WINDOW must be combined with JATTN_MASK_CAUSAL;
+ * JATTN_MASK_BLOCK may be combined with JATTN_MASK_CAUSAL (causal inside each
+ * block) but not with JATTN_MASK_WINDOW. Both read their width W from
+ * jattn_params_t.window. */
+enum { JATTN_MASK_NONE = 0, JATTN_MASK_CAUSAL = 1, JATTN_MASK_WINDOW = 2, JATTN_MASK_BLOCK = 4 };
 
 enum {
   JATTN_OK = 0,
@@ -78,8 +83,8 @@ typedef struct {
   int H;              /* heads (>= 1) */
   int D;              /* head dim: 64 or 128 */
   int act;            /* JATTN_SOFTMAX / JATTN_SILU / JATTN_GELU_TANH */
-  int mask;           /* JATTN_MASK_* bits: 0, CAUSAL, or CAUSAL|WINDOW */
-  int window;         /* W >= 1 when the window bit is set, else ignored */
+  int mask;           /* JATTN_MASK_* bits: 0, CAUSAL, CAUSAL|WINDOW, BLOCK or CAUSAL|BLOCK */
+  int window;         /* W >= 1: window width (WINDOW) or block size (BLOCK); else ignored */
   float scale;        /* > 0; 0 selects 1/sqrt(D) */
   int norm_by_lkv;    /* pointwise activations only: multiply by 1/Lkv(b) */
 } jattn_params_t;

@@ -3,8 +3,13 @@
 Public API (thin wrappers over the C-ABI library ``libjattn``; every step of
 the computation runs in its CUDA kernels):
 
-* ``attention(q, k, v, q_off, kv_off, act=..., causal=..., window=..., scale=..., norm_by_lkv=...)``
+* ``attention(q, k, v, q_off, kv_off, act=..., causal=..., window=..., scale=..., norm_by_lkv=..., block=...)``
   autograd-enabled jagged attention returning O.
+
+Masks: ``causal``; ``window`` = W > 0 (sliding window of W keys ending at the
+query's own position, implies causal); ``block`` = W > 0 (each query sees only
+the keys of its own W-wide block, optionally causal inside it; not combined
+with ``window``).
 * ``forward(...)`` -> (O, LSE) and ``backward(...)`` -> (dQ, dK, dV): the raw passes.
 * ``schedule(...)``: the device-built longest-first tile list.
 
@@ -18,7 +23,7 @@ import torch
 from . import _binding as B
 
 SOFTMAX, SILU, GELU_TANH = B.SOFTMAX, B.SILU, B.GELU_TANH
-MASK_NONE, MASK_CAUSAL, MASK_WINDOW = B.MASK_NONE, B.MASK_CAUSAL, B.MASK_WINDOW
+MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK = B.MASK_NONE, B.MASK_CAUSAL, B.MASK_WINDOW, B.MASK_BLOCK
 JattnError = B.JattnError
 
 _ACTS = {"softmax": SOFTMAX, "silu": SILU, "gelu": GELU_TANH, "gelu_tanh": GELU_TANH}
@@ -30,10 +35,19 @@ def _act(a) -> int:
     return _ACTS[a] if isinstance(a, str) else int(a)
 
 
-def _mask(causal: bool, window: int) -> int:
+def _mask(causal: bool, window: int, block: int = 0) -> int:
+    if block and block > 0:
+        if window and window > 0:
+            raise ValueError("block and window masks do not combine")
+        return MASK_BLOCK | (MASK_CAUSAL if causal else 0)
     if window and window > 0:
         return MASK_CAUSAL | MASK_WINDOW
     return MASK_CAUSAL if causal else MASK_NONE
+
+
+def _width(window: int, block: int) -> int:
+    """The width the library reads from params.window: the block size or the window."""
+    return int(block) if block and block > 0 else (int(window) if window and window > 0 else 0)
 
 
 def _check(q, k, v, q_off, kv_off):
@@ -49,9 +63,9 @@ def _check(q, k, v, q_off, kv_off):
         raise ValueError("q, k, v must share H and D; k and v must have the same shape")
 
 
-def make_params(q, k, q_off, act, mask, window, scale, norm_by_lkv) -> B.Params:
+def make_params(q, k, q_off, act, mask, width, scale, norm_by_lkv) -> B.Params:
     return B.params(q_off.numel() - 1, q.shape[0], k.shape[0], q.shape[1], q.shape[2], act, mask,
-                    window if mask & MASK_WINDOW else 0, scale, norm_by_lkv)
+                    width if mask & (MASK_WINDOW | MASK_BLOCK) else 0, scale, norm_by_lkv)
 
 
 def workspace(p: B.Params, device) -> torch.Tensor:
@@ -71,11 +85,11 @@ def _stream(device) -> int:
 
 
 def forward(q, k, v, q_off, kv_off, act="softmax", causal=False, window=0, scale=None, norm_by_lkv=False,
-            out=None, lse=None):
+            out=None, lse=None, block=0):
     """Forward pass. Returns (O [total_q,H,D] bf16, LSE [total_q,H] fp32 or None)."""
     _check(q, k, v, q_off, kv_off)
     a = _act(act)
-    p = make_params(q, k, q_off, a, _mask(causal, window), window, scale, norm_by_lkv)
+    p = make_params(q, k, q_off, a, _mask(causal, window, block), _width(window, block), scale, norm_by_lkv)
     o = out if out is not None else torch.empty_like(q)
     if a == SOFTMAX and lse is None:
         lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
@@ -86,11 +100,11 @@ def forward(q, k, v, q_off, kv_off, act="softmax", causal=False, window=0, scale
 
 
 def backward(q, k, v, o, lse, do, q_off, kv_off, act="softmax", causal=False, window=0, scale=None,
-             norm_by_lkv=False, dq=None, dk=None, dv=None):
+             norm_by_lkv=False, dq=None, dk=None, dv=None, block=0):
     """Backward pass. Returns (dQ, dK, dV) bf16."""
     _check(q, k, v, q_off, kv_off)
     a = _act(act)
-    p = make_params(q, k, q_off, a, _mask(causal, window), window, scale, norm_by_lkv)
+    p = make_params(q, k, q_off, a, _mask(causal, window, block), _width(window, block), scale, norm_by_lkv)
     dq = dq if dq is not None else torch.empty_like(q)
     dk = dk if dk is not None else torch.empty_like(k)
     dv = dv if dv is not None else torch.empty_like(v)
@@ -103,32 +117,34 @@ def backward(q, k, v, o, lse, do, q_off, kv_off, act="softmax", causal=False, wi
 
 class _JaggedAttention(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv):
-        o, lse = forward(q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv)
+    def forward(ctx, q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv, block):
+        o, lse = forward(q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv, block=block)
         ctx.save_for_backward(q, k, v, o, lse if lse is not None else o.new_empty(0), q_off, kv_off)
-        ctx.cfg = (act, causal, window, scale, norm_by_lkv)
+        ctx.cfg = (act, causal, window, scale, norm_by_lkv, block)
         return o
 
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, lse, q_off, kv_off = ctx.saved_tensors
-        act, causal, window, scale, norm_by_lkv = ctx.cfg
+        act, causal, window, scale, norm_by_lkv, block = ctx.cfg
         dq, dk, dv = backward(q, k, v, o, lse if lse.numel() else None, do, q_off, kv_off, act, causal, window,
-                              scale, norm_by_lkv)
-        return dq, dk, dv, None, None, None, None, None, None, None
+                              scale, norm_by_lkv, block=block)
+        return dq, dk, dv, None, None, None, None, None, None, None, None
 
 
-def attention(q, k, v, q_off, kv_off, act="softmax", causal=False, window=0, scale=None, norm_by_lkv=False):
+def attention(q, k, v, q_off, kv_off, act="softmax", causal=False, window=0, scale=None, norm_by_lkv=False,
+              block=0):
     """Jagged attention with autograd: O = act(scale Q K^T masked) V per sequence."""
-    return _JaggedAttention.apply(q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv)
+    return _JaggedAttention.apply(q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv, block)
 
 
 def schedule(q_off, kv_off, H, D=128, causal=False, window=0, row_tile=128, col_tile=128, transposed=False,
-             total_q=None, total_kv=None):
+             total_q=None, total_kv=None, block=0):
     """The longest-first tile list the kernels consume: int32 [n, 4] (b, row tile, col lo, col hi)."""
     tq = int(total_q) if total_q is not None else int(q_off[-1].item())
     tk = int(total_kv) if total_kv is not None else int(kv_off[-1].item())
-    p = B.params(q_off.numel() - 1, tq, tk, H, D, SOFTMAX, _mask(causal, window), window, 0.0, False)
+    p = B.params(q_off.numel() - 1, tq, tk, H, D, SOFTMAX, _mask(causal, window, block), _width(window, block), 0.0,
+                 False)
     mt = B.max_tiles(p, row_tile, transposed)
     tiles = torch.zeros(mt, 4, dtype=torch.int32, device=q_off.device)
     n = torch.zeros(1, dtype=torch.int32, device=q_off.device)

@@ -13,7 +13,7 @@ import os
 from . import build as _build
 
 SOFTMAX, SILU, GELU_TANH = 0, 1, 2
-MASK_NONE, MASK_CAUSAL, MASK_WINDOW = 0, 1, 2
+MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK = 0, 1, 2, 4
 
 EXPORTED = (
     "jattn_workspace_size",

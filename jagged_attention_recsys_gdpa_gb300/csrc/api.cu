@@ -82,9 +82,10 @@ int check_params(const jattn_params_t* p) {
   if (p->D != 64 && p->D != 128) return JATTN_ERR_INVALID;
   if (p->act != JATTN_SOFTMAX && p->act != JATTN_SILU && p->act != JATTN_GELU_TANH) return JATTN_ERR_INVALID;
   if (p->mask != JATTN_MASK_NONE && p->mask != JATTN_MASK_CAUSAL &&
-      p->mask != (JATTN_MASK_CAUSAL | JATTN_MASK_WINDOW))
+      p->mask != (JATTN_MASK_CAUSAL | JATTN_MASK_WINDOW) && p->mask != JATTN_MASK_BLOCK &&
+      p->mask != (JATTN_MASK_CAUSAL | JATTN_MASK_BLOCK))
     return JATTN_ERR_INVALID;
-  if ((p->mask & JATTN_MASK_WINDOW) && p->window < 1) return JATTN_ERR_INVALID;
+  if ((p->mask & (JATTN_MASK_WINDOW | JATTN_MASK_BLOCK)) && p->window < 1) return JATTN_ERR_INVALID;
   if (!(p->scale >= 0.0f) || !std::isfinite(p->scale)) return JATTN_ERR_INVALID;
   if (p->norm_by_lkv != 0 && p->norm_by_lkv != 1) return JATTN_ERR_INVALID;
   if (p->norm_by_lkv && p->act == JATTN_SOFTMAX) return JATTN_ERR_INVALID;
@@ -169,7 +170,7 @@ AttnArgs base_args(const jattn_params_t& p, const int64_t* q_off, const int64_t*
   a.kv_off = kv_off;
   a.H = p.H;
   a.mask = p.mask;
-  a.window = (p.mask & JATTN_MASK_WINDOW) ? p.window : 0;
+  a.window = (p.mask & (JATTN_MASK_WINDOW | JATTN_MASK_BLOCK)) ? p.window : 0;
   const float scale = p.scale > 0.0f ? p.scale : 1.0f / std::sqrt(static_cast<float>(p.D));
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -411,7 +412,7 @@ int jattn_schedule(const jattn_params_t* p, const int64_t* q_off, const int64_t*
   // The row_tile = 128 regions are the largest; a coarser tiling fits in them.
   const SchedView sv = sched_carve(base + (transposed ? L.sched_kv : L.sched_q), p->B,
                                    transposed ? L.tiles_kv : L.tiles_q);
-  const int window = (p->mask & JATTN_MASK_WINDOW) ? p->window : 0;
+  const int window = (p->mask & (JATTN_MASK_WINDOW | JATTN_MASK_BLOCK)) ? p->window : 0;
   if (sched_launch(sv, q_off, kv_off, p->B, p->total_q, p->total_kv, row_tile, col_tile, p->mask, window,
                    transposed ? 1 : 0, reinterpret_cast<DevStatus*>(base), st) != cudaSuccess)
     return JATTN_ERR_CUDA;

@@ -66,13 +66,22 @@ __device__ __forceinline__ void store_words16(void* dst, const uint32_t (&w)[16]
   }
 }
 
+// floor(x / w) for w >= 1 and any sign of x
+__device__ __forceinline__ int floor_div(int x, int w) { return x >= 0 ? x / w : -((w - 1 - x) / w); }
+
 // Visible key interval [lo, hi) of sequence-local query row i
-// (bottom-right aligned, delta = Lkv - Lq). Window implies causal.
+// (bottom-right aligned, delta = Lkv - Lq). Window implies causal; a block
+// mask of width W keeps the keys of the block that holds position i + delta.
 __device__ __forceinline__ void key_interval(int i, int delta, int lkv, int mask, int window, int& lo, int& hi) {
   lo = 0;
   hi = lkv;
   if (mask & (JATTN_MASK_CAUSAL | JATTN_MASK_WINDOW)) hi = min(hi, i + delta + 1);
   if (mask & JATTN_MASK_WINDOW) lo = max(lo, i + delta - window + 1);
+  if (mask & JATTN_MASK_BLOCK) {
+    const int b0 = floor_div(i + delta, window) * window;
+    lo = max(lo, b0);
+    hi = min(hi, b0 + window);
+  }
 }
 
 // Visible query interval [lo, hi) of sequence-local key row j.
@@ -81,6 +90,11 @@ __device__ __forceinline__ void query_interval(int j, int delta, int lq, int mas
   hi = lq;
   if (mask & (JATTN_MASK_CAUSAL | JATTN_MASK_WINDOW)) lo = max(lo, j - delta);
   if (mask & JATTN_MASK_WINDOW) hi = min(hi, j - delta + window);
+  if (mask & JATTN_MASK_BLOCK) {
+    const int b0 = (j / window) * window;  // j >= 0
+    lo = max(lo, b0 - delta);
+    hi = min(hi, b0 + window - delta);
+  }
 }
 
 // Column-tile range of row tile rt (of row_tile rows) of one sequence (see the interval rules in
@@ -91,6 +105,7 @@ __device__ __forceinline__ void tile_range(int lq, int lkv, int rt, int row_tile
   const int delta = lkv - lq;
   const bool causal = mask & (JATTN_MASK_CAUSAL | JATTN_MASK_WINDOW);
   const bool win = mask & JATTN_MASK_WINDOW;
+  const bool blk = mask & JATTN_MASK_BLOCK;
   const int nrows = transposed ? lkv : lq;
   const int ncols = transposed ? lq : lkv;
   int first = rt * row_tile;
@@ -99,13 +114,16 @@ __device__ __forceinline__ void tile_range(int lq, int lkv, int rt, int row_tile
   if (ncols == 0 || first > last) return;
   int lo, hi, lo2, hi2;
   if (!transposed) {
-    if (causal) first = max(first, -delta);
+    // query rows before key position 0 see nothing under causal and block masks
+    if (causal || blk) first = max(first, -delta);
     if (win) last = min(last, lkv - 1 - delta + window - 1);
     if (first > last) return;
     key_interval(first, delta, lkv, mask, window, lo, hi);
     key_interval(last, delta, lkv, mask, window, lo2, hi2);
   } else {
     if (win) first = max(first, delta - window + 1);
+    // key blocks that end before the first query position (delta) see no query
+    if (blk) first = max(first, floor_div(delta, window) * window);
     if (causal) last = min(last, lq + delta - 1);
     if (first > last) return;
     query_interval(first, delta, lq, mask, window, lo, hi);

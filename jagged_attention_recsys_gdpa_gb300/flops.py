@@ -12,12 +12,14 @@ import numpy as np
 
 
 def pairs_per_sequence(lq, lkv, mask: int, window: int) -> np.ndarray:
-    """Allowed (i, j) pairs of each sequence (one head). mask bits: 1 causal, 2 window."""
+    """Allowed (i, j) pairs of each sequence (one head). mask bits: 1 causal,
+    2 window of W keys (implies causal), 4 blocks of W keys."""
     lq = np.asarray(lq, dtype=np.int64)
     lkv = np.asarray(lkv, dtype=np.int64)
     out = np.zeros(len(lq), dtype=np.int64)
     causal = bool(mask & 3)
     win = bool(mask & 2)
+    blk = bool(mask & 4)
     for b in range(len(lq)):
         n, m = int(lq[b]), int(lkv[b])
         if n == 0 or m == 0:
@@ -26,6 +28,10 @@ def pairs_per_sequence(lq, lkv, mask: int, window: int) -> np.ndarray:
         delta = m - n
         hi = np.minimum(m, i + delta + 1) if causal else np.full(n, m, dtype=np.int64)
         lo = np.maximum(0, i + delta - window + 1) if win else np.zeros(n, dtype=np.int64)
+        if blk:
+            start = np.floor_divide(i + delta, window) * window
+            lo = np.maximum(lo, start)
+            hi = np.minimum(hi, start + window)
         out[b] = int(np.maximum(hi - lo, 0).sum())
     return out
 

@@ -19,6 +19,9 @@ histories):
 * ``gdpa_pma``   B=512, 32 queries per sequence, Lkv lognormal(median 2048,
                  sigma 1) clipped to [100, 20000], H=8, D=128, N(0, 0.5^2),
                  tanh-GELU with 1/Lkv normaliser, no mask
+* ``jfa_block``  the ``jfa`` lengths with block attention instead of the
+                 window: each query sees only its own 64-key block (the
+                 "BlockAttention" step of the same post)
 * ``mixed``      B=1024, exactly round(0.3 B) long sequences uniform in
                  [4000, 32000] and the rest short, uniform in [50, 500],
                  shuffled; H=8, D=128, softmax, causal + window 512
@@ -36,7 +39,7 @@ from dataclasses import dataclass, replace
 import numpy as np
 
 SOFTMAX, SILU, GELU = 0, 1, 2
-MASK_NONE, MASK_CAUSAL, MASK_WINDOW = 0, 1, 2
+MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK = 0, 1, 2, 4
 
 
 @dataclass(frozen=True)
@@ -56,6 +59,7 @@ WORKLOADS = {
     "tiny": Workload("tiny", 2, 64, SOFTMAX, MASK_CAUSAL, 0, False, 1.0, True),
     "jfa": Workload("jfa", 4, 128, SOFTMAX, MASK_CAUSAL | MASK_WINDOW, 256, False, 1.0, True),
     "jfa_causal": Workload("jfa_causal", 4, 128, SOFTMAX, MASK_CAUSAL, 0, False, 1.0, True),
+    "jfa_block": Workload("jfa_block", 4, 128, SOFTMAX, MASK_BLOCK, 64, False, 1.0, True),
     "gdpa_cross": Workload("gdpa_cross", 8, 128, SILU, MASK_NONE, 0, True, 0.5, False),
     "gdpa_pma": Workload("gdpa_pma", 8, 128, GELU, MASK_NONE, 0, True, 0.5, False),
     "mixed": Workload("mixed", 8, 128, SOFTMAX, MASK_CAUSAL | MASK_WINDOW, 512, False, 1.0, True),
@@ -73,7 +77,7 @@ def lengths(name: str, seed: int = 0):
     if name == "tiny":
         lq = np.array([3, 17, 64, 130], dtype=np.int64)
         return lq, lq.copy()
-    if name in ("jfa", "jfa_causal"):
+    if name in ("jfa", "jfa_causal", "jfa_block"):
         lq = _lognormal_int(rng, 1024, 128, 64, 16384)
         return lq, lq.copy()
     if name == "gdpa_cross":

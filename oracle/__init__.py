@@ -29,7 +29,7 @@ _LIB_PATH = os.path.join(_BUILD, "libjattn_oracle.so")
 _SRC = os.path.join(_HERE, "jattn_oracle.c")
 
 SOFTMAX, SILU, GELU = 0, 1, 2
-MASK_NONE, MASK_CAUSAL, MASK_WINDOW = 0, 1, 2
+MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK = 0, 1, 2, 4
 
 
 def build(force: bool = False) -> str:
@@ -67,7 +67,7 @@ def _load():
         ptr = ctypes.c_void_p
         lib.oracle_fwd.argtypes = [ctypes.POINTER(_Params)] + [ptr] * 7
         lib.oracle_fwd.restype = ctypes.c_int
-        lib.oracle_bwd.argtypes = [ctypes.POINTER(_Params)] + [ptr] * 9
+        lib.oracle_bwd.argtypes = [ctypes.POINTER(_Params)] + [ptr] * 10
         lib.oracle_bwd.restype = ctypes.c_int
         lib.oracle_count_pairs.argtypes = [ctypes.c_int64, ptr, ptr, ctypes.c_int, ctypes.c_int64]
         lib.oracle_count_pairs.restype = ctypes.c_int64
@@ -127,17 +127,25 @@ def fwd(q_off, kv_off, q, k, v, *, H, D, act=SOFTMAX, mask=MASK_NONE, window=0, 
     return o, lse
 
 
-def bwd(q_off, kv_off, q, k, v, do, *, H, D, act=SOFTMAX, mask=MASK_NONE, window=0, scale=None, norm_by_lkv=False):
-    """Oracle backward. Returns (dq, dk, dv) as float64 arrays."""
+def bwd(q_off, kv_off, q, k, v, do, *, H, D, act=SOFTMAX, mask=MASK_NONE, window=0, scale=None, norm_by_lkv=False,
+        o=None):
+    """Oracle backward. Returns (dq, dk, dv) as float64 arrays.
+
+    ``o``: None, or the stored forward output [total_q,H,D] that softmax's
+    D_i = <dO_i, o_i> is formed from, as FlashAttention's backward does (None:
+    the output recomputed here in double, which gives the exact gradient)."""
     q_off, kv_off = _off(q_off), _off(kv_off)
     q, k, v, do = _dbl(q), _dbl(k), _dbl(v), _dbl(do)
+    o = None if o is None else _dbl(o)
     B = len(q_off) - 1
     tq, tk = int(q_off[-1]), int(kv_off[-1])
     dq = np.zeros((tq, H, D), dtype=np.float64)
     dk = np.zeros((tk, H, D), dtype=np.float64)
     dv = np.zeros((tk, H, D), dtype=np.float64)
     P = _params(B, H, D, act, mask, window, scale, norm_by_lkv)
-    _load().oracle_bwd(ctypes.byref(P), _p(q_off), _p(kv_off), _p(q), _p(k), _p(v), _p(do), _p(dq), _p(dk), _p(dv))
+    o_ptr = None if o is None else _p(o)
+    _load().oracle_bwd(ctypes.byref(P), _p(q_off), _p(kv_off), _p(q), _p(k), _p(v), _p(do), o_ptr, _p(dq), _p(dk),
+                       _p(dv))
     return dq, dk, dv
 
 
@@ -159,23 +167,33 @@ def _row_intervals(rows: np.ndarray, delta: int, ncols: int, mask: int, window: 
     """Half-open interval of visible columns for each row index.
 
     Not transposed: rows are queries i, columns keys j, allowed when
-    j <= i + delta (causal) and i + delta - j < window (window).
+    j <= i + delta (causal), i + delta - j < window (window) and
+    j // window == (i + delta) // window (block).
     Transposed: rows are keys j, columns queries i, same relation solved for i.
     """
     lo = np.zeros_like(rows)
     hi = np.full_like(rows, ncols)
     causal = bool(mask & (MASK_CAUSAL | MASK_WINDOW))
     win = bool(mask & MASK_WINDOW)
+    blk = bool(mask & MASK_BLOCK)
     if not transposed:
         if causal:
             hi = np.minimum(hi, rows + delta + 1)
         if win:
             lo = np.maximum(lo, rows + delta - window + 1)
+        if blk:
+            start = np.floor_divide(rows + delta, window) * window
+            lo = np.maximum(lo, start)
+            hi = np.minimum(hi, start + window)
     else:
         if causal:
             lo = np.maximum(lo, rows - delta)
         if win:
             hi = np.minimum(hi, rows - delta + window)
+        if blk:
+            start = np.floor_divide(rows, window) * window
+            lo = np.maximum(lo, start - delta)
+            hi = np.minimum(hi, start + window - delta)
     return lo, hi
 
 

@@ -11,12 +11,15 @@
  * tensors with asymmetric query/key lengths; section "Generalized Dot-Product
  * Attention (GDPA)" -- two matrix products with an element-wise activation,
  * softmax replaced by GELU or SiLU; section "BlockAttention" -- sliding
- * windows for long self-attention):
+ * windows for long self-attention, then fixed blocks where each query block
+ * attends only to its own key block):
  *
  *   for every sequence b and head h, rows i < Lq(b), keys j < Lkv(b),
  *   delta = Lkv - Lq (bottom-right alignment):
  *     allowed(i,j): causal  -> j <= i + delta
  *                   window  -> 0 <= i + delta - j < W  (implies causal)
+ *                   block   -> floor(j / W) == floor((i + delta) / W)
+ *                              (with causal: also j <= i + delta)
  *     s_ij = scale * <q_i, k_j>
  *     softmax:   p_ij = exp(s_ij - m_i) / l_i over allowed j,
  *                o_i = sum_j p_ij v_j,  lse_i = m_i + ln l_i
@@ -26,6 +29,10 @@
  *                   or tanh-GELU(x) = x/2 (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3)))
  *   backward (chain rule of the above):
  *     softmax:   D_i = <dO_i, o_i>, dS_ij = p_ij (<dO_i, v_j> - D_i)
+ *                (o_i is the forward's output: recomputed here in double, or
+ *                the stored output the caller passes in -- FlashAttention's
+ *                backward, which JFA's is, reads the output the forward
+ *                stored, so its rounding enters D_i and nothing else)
  *     pointwise: dS_ij = c act'(s_ij) <dO_i, v_j>,  p_ij = c act(s_ij)
  *     dV_j = sum_i p_ij dO_i, dQ_i = scale sum_j dS_ij k_j,
  *     dK_j = scale sum_i dS_ij q_i
@@ -46,11 +53,16 @@
 #define ORACLE_GELU 2
 #define ORACLE_CAUSAL 1
 #define ORACLE_WINDOW 2
+#define ORACLE_BLOCK 4
+
+/* Block index of position x for blocks of width w (rounds toward -inf). */
+static int64_t block_of(int64_t x, int64_t w) { return x >= 0 ? x / w : -((-x + w - 1) / w); }
 
 /* Is key j visible from query i (both sequence-local)? */
 static int allowed(int64_t i, int64_t j, int64_t delta, int mask, int64_t window) {
   if ((mask & (ORACLE_CAUSAL | ORACLE_WINDOW)) && j > i + delta) return 0;
   if ((mask & ORACLE_WINDOW) && i + delta - j >= window) return 0;
+  if ((mask & ORACLE_BLOCK) && block_of(j, window) != block_of(i + delta, window)) return 0;
   return 1;
 }
 
@@ -64,6 +76,11 @@ static void key_range(int64_t i, int64_t delta, int64_t lkv, int mask, int64_t w
   }
   if (mask & ORACLE_WINDOW) {
     if (i + delta - window + 1 > a) a = i + delta - window + 1;
+  }
+  if (mask & ORACLE_BLOCK) {
+    const int64_t start = block_of(i + delta, window) * window;
+    if (start > a) a = start;
+    if (start + window < b) b = start + window;
   }
   if (b < a) b = a;
   *lo = a;
@@ -182,9 +199,12 @@ int oracle_fwd(const oracle_params* P, const int64_t* q_off, const int64_t* kv_o
   return 0;
 }
 
-/* Backward. dq: [total_q,H,D], dk/dv: [total_kv,H,D] doubles, fully written. */
+/* Backward. dq: [total_q,H,D], dk/dv: [total_kv,H,D] doubles, fully written.
+ * o_stored: NULL (D_i from the output recomputed here) or the forward output
+ * [total_q,H,D] to form D_i from (softmax only; ignored otherwise). */
 int oracle_bwd(const oracle_params* P, const int64_t* q_off, const int64_t* kv_off, const double* q,
-               const double* k, const double* v, const double* dout, double* dq, double* dk, double* dv) {
+               const double* k, const double* v, const double* dout, const double* o_stored, double* dq,
+               double* dk, double* dv) {
   const int H = P->H, D = P->D;
   const int64_t nbh = P->B * (int64_t)H;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -218,10 +238,14 @@ int oracle_bwd(const oracle_params* P, const int64_t* q_off, const int64_t* kv_o
       row_probs(P, lkv, hi - lo, s, vis, p, NULL);
       double di = 0.0;
       if (P->act == ORACLE_SOFTMAX) {
-        for (int d = 0; d < D; ++d) oi[d] = 0.0;
-        for (int64_t t = 0; t < hi - lo; ++t)
-          if (vis[t])
-            for (int d = 0; d < D; ++d) oi[d] += p[t] * vb[(size_t)(lo + t) * D + d];
+        if (o_stored) {
+          load_vec(o_stored, q_off[b] + i, h, H, D, oi);
+        } else {
+          for (int d = 0; d < D; ++d) oi[d] = 0.0;
+          for (int64_t t = 0; t < hi - lo; ++t)
+            if (vis[t])
+              for (int d = 0; d < D; ++d) oi[d] += p[t] * vb[(size_t)(lo + t) * D + d];
+        }
         di = dot(gi, oi, D);
       }
       const double c = (P->norm_by_lkv && lkv > 0) ? 1.0 / (double)lkv : 1.0;

@@ -25,6 +25,8 @@ def mask_matrix(lq: int, lkv: int, mask: int, window: int) -> torch.Tensor:
         ok &= j <= i + delta
     if mask & 2:
         ok &= (i + delta - j) < window
+    if mask & 4:  # blocks of `window` keys; python // rounds toward -inf
+        ok &= (j // window) == ((i + delta) // window)
     return ok
 
 

@@ -15,30 +15,36 @@ RTOL = 1e-2
 ACT_NAME = {0: "softmax", 1: "silu", 2: "gelu"}
 
 
-def gpu_run(inp, w, backward=True):
-    """Forward (+ backward) through the public API on the tensors' device."""
+def gpu_run(inp, w, backward=True, stored=None):
+    """Forward (+ backward) through the public API on the tensors' device.
+    stored: None (the backward reads this forward's O and LSE) or (o, lse)
+    device tensors for the backward to read instead."""
     import jagged_attention_recsys_gdpa_gb300 as J
 
     causal = bool(w.mask & 1)
     window = w.window if w.mask & 2 else 0
+    block = w.window if w.mask & 4 else 0
     o, lse = J.forward(inp["q"], inp["k"], inp["v"], inp["q_off"], inp["kv_off"], act=w.act, causal=causal,
-                       window=window, norm_by_lkv=w.norm_by_lkv)
+                       window=window, block=block, norm_by_lkv=w.norm_by_lkv)
     out = {"o": o, "lse": lse}
     if backward:
+        if stored is not None:
+            o, lse = stored
         dq, dk, dv = J.backward(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], inp["q_off"], inp["kv_off"],
-                                act=w.act, causal=causal, window=window, norm_by_lkv=w.norm_by_lkv)
+                                act=w.act, causal=causal, window=window, block=block, norm_by_lkv=w.norm_by_lkv)
         out.update(dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     return out
 
 
-def oracle_run(inp, w, backward=True):
+def oracle_run(inp, w, backward=True, o_stored=None):
     kw = dict(H=w.H, D=w.D, act=w.act, mask=w.mask | (1 if w.mask & 2 else 0), window=w.window,
               norm_by_lkv=w.norm_by_lkv)
     o, lse = oracle.fwd(inp["q_off"], inp["kv_off"], inp["q"], inp["k"], inp["v"], **kw)
     out = {"o": o, "lse": lse}
     if backward:
-        dq, dk, dv = oracle.bwd(inp["q_off"], inp["kv_off"], inp["q"], inp["k"], inp["v"], inp["do"], **kw)
+        dq, dk, dv = oracle.bwd(inp["q_off"], inp["kv_off"], inp["q"], inp["k"], inp["v"], inp["do"], o=o_stored,
+                                **kw)
         out.update(dq=dq, dk=dk, dv=dv)
     return out
 
@@ -112,3 +118,18 @@ def subset(inp, seqs):
     if "do" in inp:
         sub["do"] = inp["do"].index_select(0, tq).cpu()
     return sub, rq, rk
+
+
+def run_both_stored(cpu, w, backward=True):
+    """GPU and oracle runs whose backward passes both read the same stored
+    forward output: the oracle's O rounded to bf16 and its LSE in fp32, as a
+    correct forward would have stored them. This isolates the backward kernels'
+    own arithmetic from the rounding of O, which enters D_i = <dO_i, O_i>
+    (large next to dQ for rows that see one or two keys)."""
+    r = oracle_run(cpu, w, backward=False)
+    o_st = torch.from_numpy(r["o"]).to(torch.bfloat16)
+    lse_st = torch.from_numpy(r["lse"]).to(torch.float32)
+    g = gpu_run(to_cuda(cpu), w, backward, stored=(o_st.cuda(), lse_st.cuda()))
+    if backward:
+        r.update({k: x for k, x in oracle_run(cpu, w, True, o_stored=o_st).items() if k.startswith("d")})
+    return g, r

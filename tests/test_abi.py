@@ -50,13 +50,15 @@ def test_workspace_size_and_validation(lib):
         dict(D=96), dict(D=0), dict(H=0), dict(B=0), dict(total_q=-1), dict(act=3), dict(mask=2), dict(mask=3),
         dict(mask=4), dict(scale=-1.0), dict(scale=float("nan")), dict(act=0, norm_by_lkv=1),
         dict(total_q=1 << 31),
+        # block masks need a width and do not combine with the window bit
+        dict(mask=5, window=0), dict(mask=6, window=4), dict(mask=7, window=4), dict(mask=8, window=4),
     ]
     for kw in bad:
         size = ctypes.c_size_t(0)
         p = _params(**kw)
         assert lib.jattn_workspace_size(ctypes.byref(p), ctypes.byref(size)) == 1, kw
-    ok = _params(mask=3, window=4)
-    assert B.workspace_size(ok) > 0
+    for ok in (_params(mask=3, window=4), _params(mask=4, window=64), _params(mask=5, window=1)):
+        assert B.workspace_size(ok) > 0
     # softmax needs room for Di; pointwise does not
     assert B.workspace_size(_params(total_q=100000)) > B.workspace_size(_params(total_q=100000, act=1))
 
@@ -94,3 +96,12 @@ def test_error_strings(lib):
     for code in range(9):
         assert B.error_string(code)
     assert B.error_string(99) == "unknown error code"
+
+
+def test_python_api_rejects_block_with_window():
+    import jagged_attention_recsys_gdpa_gb300 as J
+
+    with pytest.raises(ValueError):
+        J._mask(True, 16, 64)
+    assert J._mask(False, 0, 64) == 4 and J._mask(True, 0, 64) == 5
+    assert J._width(0, 64) == 64 and J._width(256, 0) == 256

@@ -11,6 +11,7 @@ pytestmark = pytest.mark.gpu
 
 SOFTMAX, SILU, GELU = 0, 1, 2
 NONE, CAUSAL, WIN = 0, 1, 3
+BLOCK, CBLOCK = 4, 5  # block mask; block mask with causal inside the blocks
 
 SELF_LENS = [1, 127, 128, 129, 255, 256, 257, 300, 513, 1000]
 CROSS_LQ = [100, 300, 5, 700, 257, 1]
@@ -21,10 +22,15 @@ def _w(act, mask, window, D, H=2, norm=False, std=1.0):
     return inputs.Workload("case", H, D, act, mask, window, norm, std, True)
 
 
-def _check(w, lq, lkv, seed=0, backward=True):
+def _check(w, lq, lkv, seed=0, backward=True, stored=False):
+    """stored: the backward reads the oracle's O (bf16) and LSE on both sides
+    instead of the GPU forward's O against the exact gradient."""
     cpu = G.cpu_inputs(w, lq, lkv, seed)
-    g = G.gpu_run(G.to_cuda(cpu), w, backward)
-    r = G.oracle_run(cpu, w, backward)
+    if stored:
+        g, r = G.run_both_stored(cpu, w, backward)
+    else:
+        g = G.gpu_run(G.to_cuda(cpu), w, backward)
+        r = G.oracle_run(cpu, w, backward)
     G.compare(g, r, w, backward)
 
 
@@ -252,3 +258,61 @@ def test_batch_without_keys_or_queries(act, lq, lkv):
     LSE = -inf, dQ = 0) or no query rows at all (dK = dV = 0)."""
     w = _w(act, NONE, 0, 128, norm=act != SOFTMAX)
     _check(w, lq, lkv, seed=18)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("act", [SOFTMAX, GELU])
+@pytest.mark.parametrize("mask", [BLOCK, CBLOCK])
+@pytest.mark.parametrize("W", [37, 64, 200])
+def test_block_attention_self(W, mask, act, D):
+    """Block masks whose edges fall inside, on and across the 128-row tiles.
+    Causal blocks hold many rows that see one or two keys, where the bf16
+    rounding of the stored O moves D_i by more than dQ's tolerance; the
+    backward is therefore checked on the oracle's stored O, the forward
+    against the oracle as everywhere."""
+    norm = act != SOFTMAX
+    _check(_w(act, mask, W, D, norm=norm, std=1.0 if act == SOFTMAX else 0.5), SELF_LENS, SELF_LENS, seed=31,
+           stored=True)
+
+
+@pytest.mark.parametrize("act", [SOFTMAX, SILU])
+@pytest.mark.parametrize("mask,W", [(BLOCK, 64), (CBLOCK, 50), (BLOCK, 1)])
+def test_block_attention_cross_and_degenerate(act, mask, W):
+    """Cross-attention (blocks aligned to the sequence ends, so Lq > Lkv leaves
+    queries before the first key block with nothing to see), empty sequences and
+    one-key blocks."""
+    norm = act != SOFTMAX
+    _check(_w(act, mask, W, 128, norm=norm), CROSS_LQ, CROSS_LKV, seed=33, stored=True)
+    _check(_w(act, mask, W, 64, norm=norm), [0, 5, 130, 1, 0, 200, 3], [4, 0, 130, 1, 0, 60, 9], seed=34,
+           stored=True)
+
+
+@pytest.mark.parametrize("arrangement", [FWD_SPLIT, FWD_PINGPONG])
+def test_block_attention_forward_arrangements(arrangement):
+    from jagged_attention_recsys_gdpa_gb300 import _binding as B
+
+    w = _w(SOFTMAX, BLOCK, 96, 128, H=3)
+    cpu = G.cpu_inputs(w, SELF_LENS, SELF_LENS, seed=35)
+    B.debug_set(arrangement, 0)
+    try:
+        g = G.gpu_run(G.to_cuda(cpu), w, backward=False)
+    finally:
+        B.debug_set(0, 0)
+    G.compare(g, G.oracle_run(cpu, w, backward=False), w, backward=False)
+
+
+@pytest.mark.parametrize("act", [SOFTMAX, SILU])
+def test_block_at_least_length_equals_unblocked(act):
+    """A block wider than every sequence allows what no mask (causal inside the
+    blocks: causal) allows, and the kernels take identical paths: bit-equal."""
+    for m_blk, m_ref in ((BLOCK, NONE), (CBLOCK, CAUSAL)):
+        w1 = _w(act, m_ref, 0, 128, norm=act != SOFTMAX)
+        w2 = _w(act, m_blk, 4096, 128, norm=act != SOFTMAX)
+        cpu = G.cpu_inputs(w1, SELF_LENS, SELF_LENS, 36)
+        a = G.gpu_run(G.to_cuda(cpu), w1)
+        b = G.gpu_run(G.to_cuda(cpu), w2)
+        for k in ("o", "lse", "dq", "dk", "dv"):
+            if a[k] is None:  # no LSE for pointwise activations
+                assert b[k] is None, k
+                continue
+            assert torch.equal(a[k], b[k]), (m_blk, k)

@@ -14,7 +14,8 @@ def _device_schedule(lq, lkv, mask, window, row_tile, col_tile, transposed, H=2)
 
     qo = torch.from_numpy(inputs.offsets(np.asarray(lq))).cuda()
     ko = torch.from_numpy(inputs.offsets(np.asarray(lkv))).cuda()
-    t = J.schedule(qo, ko, H, causal=bool(mask & 1), window=window if mask & 2 else 0, row_tile=row_tile,
+    t = J.schedule(qo, ko, H, causal=bool(mask & 1), window=window if mask & 2 else 0,
+                   block=window if mask & 4 else 0, row_tile=row_tile,
                    col_tile=col_tile, transposed=transposed)
     return t.cpu().numpy()
 
@@ -24,7 +25,7 @@ def _twin(lq, lkv, mask, window, row_tile, col_tile, transposed):
                            window=window, BM=row_tile, BN=col_tile, transposed=transposed, cost_cap=1023)
 
 
-@pytest.mark.parametrize("name", ["tiny", "jfa", "jfa_causal", "gdpa_cross", "gdpa_pma", "mixed"])
+@pytest.mark.parametrize("name", ["tiny", "jfa", "jfa_causal", "jfa_block", "gdpa_cross", "gdpa_pma", "mixed"])
 @pytest.mark.parametrize("row_tile,transposed", [(256, False), (128, False), (128, True)])
 def test_schedule_matches_twin_on_workloads(name, row_tile, transposed):
     w = inputs.WORKLOADS[name]
@@ -36,7 +37,7 @@ def test_schedule_matches_twin_on_workloads(name, row_tile, transposed):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("mask,window", [(0, 0), (1, 0), (3, 1), (3, 37)])
+@pytest.mark.parametrize("mask,window", [(0, 0), (1, 0), (3, 1), (3, 37), (4, 1), (4, 37), (5, 64)])
 def test_schedule_random_small(mask, window):
     rng = np.random.default_rng(mask * 100 + window)
     for trial in range(10):

@@ -19,6 +19,7 @@ from tests import dense_ref as R
 
 SOFTMAX, SILU, GELU = 0, 1, 2
 NONE, CAUSAL, WINDOW = 0, 1, 3  # WINDOW value as passed: causal | window bits
+BLOCK, CBLOCK = 4, 5  # block mask, and block mask with causal inside the blocks
 
 
 def _batch(lq, lkv, H, D, seed, std=1.0):
@@ -36,7 +37,8 @@ SELF_LENS = ([3, 17, 1, 40, 9], [3, 17, 1, 40, 9])
 CROSS_LENS = ([5, 12, 7, 1, 20], [9, 4, 30, 6, 2])
 
 
-@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 1), (WINDOW, 5), (WINDOW, 64)])
+@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 1), (WINDOW, 5), (WINDOW, 64),
+                                         (BLOCK, 1), (BLOCK, 4), (BLOCK, 64), (CBLOCK, 4)])
 @pytest.mark.parametrize("lens", [SELF_LENS, CROSS_LENS], ids=["self", "cross"])
 def test_softmax_matches_torch_sdpa(mask, window, lens):
     H, D = 2, 16
@@ -61,7 +63,7 @@ def test_softmax_matches_torch_sdpa(mask, window, lens):
 
 
 @pytest.mark.parametrize("act", [SILU, GELU])
-@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 4)])
+@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 4), (BLOCK, 4), (CBLOCK, 3)])
 @pytest.mark.parametrize("norm", [False, True])
 @pytest.mark.parametrize("lens", [SELF_LENS, CROSS_LENS], ids=["self", "cross"])
 def test_pointwise_matches_padded_dense(act, mask, window, norm, lens):
@@ -74,7 +76,7 @@ def test_pointwise_matches_padded_dense(act, mask, window, norm, lens):
 
 
 @pytest.mark.parametrize("act", [SOFTMAX, SILU, GELU])
-@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 3)])
+@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 3), (BLOCK, 4), (CBLOCK, 3)])
 @pytest.mark.parametrize("lens", [SELF_LENS, CROSS_LENS], ids=["self", "cross"])
 def test_grads_match_torch_autograd(act, mask, window, lens):
     H, D = 2, 8
@@ -90,7 +92,7 @@ def test_grads_match_torch_autograd(act, mask, window, lens):
 
 
 @pytest.mark.parametrize("act", [SOFTMAX, SILU, GELU])
-@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 2)])
+@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 2), (BLOCK, 2), (CBLOCK, 2)])
 def test_grads_finite_differences(act, mask, window):
     """Central differences of L = sum(o * dO) through the oracle's forward."""
     H, D = 1, 4
@@ -263,7 +265,8 @@ def _brute_schedule(qo, ko, mask, window, BM, BN, transposed):
 
 
 @pytest.mark.parametrize("transposed", [False, True])
-@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 3), (WINDOW, 9)])
+@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (WINDOW, 3), (WINDOW, 9), (BLOCK, 3), (BLOCK, 8),
+                                         (CBLOCK, 5)])
 def test_schedule_twin_brute_force(transposed, mask, window):
     rng = np.random.default_rng(17)
     for trial in range(6):
@@ -290,3 +293,100 @@ def test_schedule_cost_cap_orders_by_index():
     assert np.all(np.diff(costs) <= 0)
     capped = got[costs == 20]
     assert [tuple(r[:2]) for r in capped.tolist()] == sorted(tuple(r[:2]) for r in capped.tolist())
+
+
+# ---------------------------------------------------------------- block attention
+def _split_into_blocks(lens, W):
+    """Lengths of the W-wide blocks every sequence splits into (last one partial)."""
+    out = []
+    for L in lens:
+        out += [min(W, L - s) for s in range(0, L, W)] if L else [0]
+    return np.asarray(out, dtype=np.int64)
+
+
+@pytest.mark.parametrize("act", [SOFTMAX, SILU, GELU])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("W", [1, 3, 8])
+def test_block_mask_is_independent_blocks(act, causal, W):
+    """Self-attention with a block mask equals attention run on every block as
+    its own sequence (unmasked, or causal when the block mask is causal), for
+    O, LSE and all gradients; the 1/Lkv normaliser is the full sequence's."""
+    H, D = 2, 8
+    lens = np.array([3, 17, 1, 0, 40, 9])
+    qo = inputs.offsets(lens)
+    q = inputs.values((int(qo[-1]), H, D), 0.8, 31)
+    k = inputs.values((int(qo[-1]), H, D), 0.8, 32)
+    v = inputs.values((int(qo[-1]), H, D), 0.8, 33)
+    do = inputs.values((int(qo[-1]), H, D), 1.0, 34)
+    kw = dict(H=H, D=D, act=act, scale=0.3)
+    o, lse = oracle.fwd(qo, qo, q, k, v, mask=(CBLOCK if causal else BLOCK), window=W, **kw)
+    g = oracle.bwd(qo, qo, q, k, v, do, mask=(CBLOCK if causal else BLOCK), window=W, **kw)
+    bo = inputs.offsets(_split_into_blocks(lens, W))
+    o2, lse2 = oracle.fwd(bo, bo, q, k, v, mask=(CAUSAL if causal else NONE), window=0, **kw)
+    g2 = oracle.bwd(bo, bo, q, k, v, do, mask=(CAUSAL if causal else NONE), window=0, **kw)
+    np.testing.assert_allclose(o, o2, rtol=1e-13, atol=1e-14)
+    if act == SOFTMAX:
+        np.testing.assert_allclose(lse, lse2, rtol=1e-13, atol=1e-14)
+    for a, b in zip(g, g2):
+        np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-14)
+
+
+def test_block_mask_closed_forms():
+    H, D = 2, 16
+    lens = np.array([5, 33, 1, 12])
+    qo = inputs.offsets(lens)
+    q = inputs.values((int(qo[-1]), H, D), 1.0, 41)
+    k = inputs.values((int(qo[-1]), H, D), 1.0, 42)
+    v = inputs.values((int(qo[-1]), H, D), 1.0, 43)
+    kw = dict(H=H, D=D, act=SOFTMAX, scale=0.25)
+    # a block at least as wide as every sequence is no mask (causal inside it: causal)
+    for m_blk, m_ref in ((BLOCK, NONE), (CBLOCK, CAUSAL)):
+        o, lse = oracle.fwd(qo, qo, q, k, v, mask=m_blk, window=int(lens.max()), **kw)
+        o2, lse2 = oracle.fwd(qo, qo, q, k, v, mask=m_ref, window=0, **kw)
+        np.testing.assert_array_equal(o, o2)
+        np.testing.assert_array_equal(lse, lse2)
+    # blocks of one key: every query sees only its own key, so o_i = v_i and lse_i = s_ii
+    o, lse = oracle.fwd(qo, qo, q, k, v, mask=BLOCK, window=1, **kw)
+    qd, kd, vd = (R.to_f64(t).numpy() for t in (q, k, v))
+    np.testing.assert_allclose(o, vd, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(lse, 0.25 * np.einsum("thd,thd->th", qd, kd), rtol=1e-13, atol=1e-14)
+
+
+def test_block_mask_pair_counts():
+    lens = np.array([1, 7, 30, 129, 0, 64])
+    off = inputs.offsets(lens)
+    for W in (1, 5, 64, 200):
+        blocks = _split_into_blocks(lens, W)
+        assert oracle.count_pairs(off, off, BLOCK, W) == int((blocks * blocks).sum())
+        assert oracle.count_pairs(off, off, CBLOCK, W) == int((blocks * (blocks + 1) // 2).sum())
+    # cross-attention, Lq = 3 < Lkv = 8 (delta = 5), blocks of 4: queries sit at key positions 5, 6, 7,
+    # all in the block [4, 8), so each sees 4 keys; with causal, 2, 3 and 4
+    lq, lk = inputs.offsets(np.array([3])), inputs.offsets(np.array([8]))
+    assert oracle.count_pairs(lq, lk, BLOCK, 4) == 12
+    assert oracle.count_pairs(lq, lk, CBLOCK, 4) == 2 + 3 + 4
+
+
+# ---------------------------------------------------------------- stored forward output
+@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (CBLOCK, 3)])
+@pytest.mark.parametrize("lens", [SELF_LENS, CROSS_LENS], ids=["self", "cross"])
+def test_bwd_from_stored_output(mask, window, lens):
+    """D_i formed from a stored output O' = O + E: with E = 0 it is the exact
+    gradient; otherwise dV is unchanged and dQ_i moves by exactly
+    -scale <dO_i, E_i> sum_j p_ij k_j (sum_j p_ij k_j is the forward with V := K)."""
+    H, D, scale = 2, 8, 0.4
+    qo, ko, q, k, v, do = _batch(*lens, H, D, seed=51)
+    kw = dict(H=H, D=D, act=SOFTMAX, mask=mask, window=window, scale=scale)
+    o, _ = oracle.fwd(qo, ko, q, k, v, **kw)
+    exact = oracle.bwd(qo, ko, q, k, v, do, **kw)
+    for a, b in zip(oracle.bwd(qo, ko, q, k, v, do, o=o, **kw), exact):
+        np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
+    E = np.random.default_rng(5).normal(0.0, 0.01, size=o.shape)
+    dq2, _, dv2 = oracle.bwd(qo, ko, q, k, v, do, o=o + E, **kw)
+    pk, _ = oracle.fwd(qo, ko, q, k, k, **kw)
+    eps = np.einsum("thd,thd->th", R.to_f64(do).numpy(), E)
+    np.testing.assert_allclose(dq2, exact[0] - scale * eps[..., None] * pk, rtol=1e-11, atol=1e-13)
+    np.testing.assert_array_equal(dv2, exact[2])
+    # pointwise activations have no D_i: the stored output is ignored
+    kwp = dict(kw, act=SILU)
+    for a, b in zip(oracle.bwd(qo, ko, q, k, v, do, o=o + E, **kwp), oracle.bwd(qo, ko, q, k, v, do, **kwp)):
+        np.testing.assert_array_equal(a, b)
