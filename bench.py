@@ -178,9 +178,10 @@ def cpu_oracle_step(x_cpu, w, seqs):
 
 def workload_desc(name, w, batch):
     """The workload as both arms name it in `config.workload`."""
-    act = "softmax" if w.act == 0 else ("silu" if w.act == 1 else "gelu")
+    act = {0: "softmax", 1: "silu", 2: "gelu", 3: "gelu (degree-6 polynomial)"}[w.act]
     mask = {0: "none", 1: "causal", 3: "causal+window", 4: "block", 5: "causal+block"}[w.mask]
-    return f"{name}: B={batch}, H={w.H}, D={w.D}, {act}, mask={mask}" + (f" {w.window}" if w.mask & 6 else "")
+    qk = f", q/k rows normalised to |s| <= {w.qk_norm:g}" if w.qk_norm > 0 else ""
+    return f"{name}: B={batch}, H={w.H}, D={w.D}, {act}, mask={mask}" + (f" {w.window}" if w.mask & 6 else "") + qk
 
 
 def run_reference(args, ws, rank):

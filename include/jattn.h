@@ -17,7 +17,7 @@
  *   JATTN_SOFTMAX     o_i = sum_j softmax_j(s_ij) v_j over allowed j,
  *                     lse_i = ln sum_j exp(s_ij)  (no allowed key: o_i = 0,
  *                     lse_i = -inf)
- *   JATTN_SILU / JATTN_GELU_TANH
+ *   JATTN_SILU / JATTN_GELU_TANH / JATTN_GELU_POLY
  *                     o_i = c * sum_{allowed j} act(s_ij) v_j, c = 1/Lkv(b)
  *                     when norm_by_lkv, else 1
  *
@@ -55,7 +55,19 @@ extern "C" {
 enum {
   JATTN_SOFTMAX = 0,   /* row softmax (Jagged Flash Attention) */
   JATTN_SILU = 1,      /* x / (1 + e^-x) (GDPA) */
-  JATTN_GELU_TANH = 2  /* x/2 (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))) (GDPA) */
+  JATTN_GELU_TANH = 2, /* x/2 (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))) (GDPA) */
+  /* GDPA's ALU-only GELU: the tanh-GELU above replaced by its Taylor
+   * polynomial at 0 through x^6, evaluated with fused multiply-adds only
+   * (section "Generalized Dot-Product Attention (GDPA)": no tanh on the
+   * special-function unit, accurate on the score range that query/key
+   * normalisation bounds). With c = sqrt(2/pi), a = 0.044715:
+   *   act(x)  = x/2 + (c/2) x^2 + ((c a - c^3/3)/2) x^4 + ((2c^5/15 - c^3 a)/2) x^6
+   *   act'(x) = its derivative (the backward differentiates the polynomial).
+   * Within 1.2e-4 of tanh-GELU (derivative 1.3e-3) for |s| <= 0.75, and
+   * 1.2e-3 (derivative 9e-3) for |s| <= 1; outside that range it departs
+   * quickly (2.6e-2 at |s| = 1.5), so callers bound |s|, e.g. by normalising
+   * query and key rows. */
+  JATTN_GELU_POLY = 3
 };
 
 /* Mask bits. JATTN_MASK_WINDOW must be combined with JATTN_MASK_CAUSAL;
@@ -82,7 +94,7 @@ typedef struct {
   int64_t total_kv;   /* key/value rows = kv_off[B] (>= 0) */
   int H;              /* heads (>= 1) */
   int D;              /* head dim: 64 or 128 */
-  int act;            /* JATTN_SOFTMAX / JATTN_SILU / JATTN_GELU_TANH */
+  int act;            /* JATTN_SOFTMAX / JATTN_SILU / JATTN_GELU_TANH / JATTN_GELU_POLY */
   int mask;           /* JATTN_MASK_* bits: 0, CAUSAL, CAUSAL|WINDOW, BLOCK or CAUSAL|BLOCK */
   int window;         /* W >= 1: window width (WINDOW) or block size (BLOCK); else ignored */
   float scale;        /* > 0; 0 selects 1/sqrt(D) */

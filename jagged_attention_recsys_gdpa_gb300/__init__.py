@@ -22,11 +22,11 @@ import torch
 
 from . import _binding as B
 
-SOFTMAX, SILU, GELU_TANH = B.SOFTMAX, B.SILU, B.GELU_TANH
+SOFTMAX, SILU, GELU_TANH, GELU_POLY = B.SOFTMAX, B.SILU, B.GELU_TANH, B.GELU_POLY
 MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK = B.MASK_NONE, B.MASK_CAUSAL, B.MASK_WINDOW, B.MASK_BLOCK
 JattnError = B.JattnError
 
-_ACTS = {"softmax": SOFTMAX, "silu": SILU, "gelu": GELU_TANH, "gelu_tanh": GELU_TANH}
+_ACTS = {"softmax": SOFTMAX, "silu": SILU, "gelu": GELU_TANH, "gelu_tanh": GELU_TANH, "gelu_poly": GELU_POLY}
 
 _ws_cache: dict = {}
 

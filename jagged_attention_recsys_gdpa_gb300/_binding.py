@@ -12,7 +12,7 @@ import os
 
 from . import build as _build
 
-SOFTMAX, SILU, GELU_TANH = 0, 1, 2
+SOFTMAX, SILU, GELU_TANH, GELU_POLY = 0, 1, 2, 3
 MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK = 0, 1, 2, 4
 
 EXPORTED = (

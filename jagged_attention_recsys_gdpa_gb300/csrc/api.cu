@@ -80,7 +80,8 @@ int check_params(const jattn_params_t* p) {
   if (!p) return JATTN_ERR_INVALID;
   if (p->B < 1 || p->total_q < 0 || p->total_kv < 0 || p->H < 1) return JATTN_ERR_INVALID;
   if (p->D != 64 && p->D != 128) return JATTN_ERR_INVALID;
-  if (p->act != JATTN_SOFTMAX && p->act != JATTN_SILU && p->act != JATTN_GELU_TANH) return JATTN_ERR_INVALID;
+  if (p->act != JATTN_SOFTMAX && p->act != JATTN_SILU && p->act != JATTN_GELU_TANH && p->act != JATTN_GELU_POLY)
+    return JATTN_ERR_INVALID;
   if (p->mask != JATTN_MASK_NONE && p->mask != JATTN_MASK_CAUSAL &&
       p->mask != (JATTN_MASK_CAUSAL | JATTN_MASK_WINDOW) && p->mask != JATTN_MASK_BLOCK &&
       p->mask != (JATTN_MASK_CAUSAL | JATTN_MASK_BLOCK))

@@ -64,6 +64,9 @@ __device__ __forceinline__ void act_and_grad(float x, float& f, float& g) {
     const float sg = __fdividef(1.0f, 1.0f + ex2_approx(-x * kLog2e));
     f = x * sg;
     g = sg * fmaf(x, 1.0f - sg, 1.0f);
+  } else if constexpr (ACT == JATTN_GELU_POLY) {
+    f = gelu_poly(x);
+    g = gelu_poly_grad(x);
   } else {
     const float k0 = 0.7978845608028654f, k1 = 0.044715f;
     const float x2 = x * x;
@@ -1029,11 +1032,14 @@ cudaError_t launch_bwd_dkdv(int D, int act, const CUtensorMap& q, const CUtensor
     constexpr int sm = DkdvCfg<128>::kSmemBytes;
     if (act == JATTN_SOFTMAX) return launch6(dkdv_kernel<128, JATTN_SOFTMAX>, sm, q, k, v, dout, o0, o1, a, grid, stream);
     if (act == JATTN_SILU) return launch6(dkdv_kernel<128, JATTN_SILU>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+    if (act == JATTN_GELU_POLY)
+      return launch6(dkdv_kernel<128, JATTN_GELU_POLY>, sm, q, k, v, dout, o0, o1, a, grid, stream);
     return launch6(dkdv_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, o0, o1, a, grid, stream);
   }
   constexpr int sm = DkdvCfg<64>::kSmemBytes;
   if (act == JATTN_SOFTMAX) return launch6(dkdv_kernel<64, JATTN_SOFTMAX>, sm, q, k, v, dout, o0, o1, a, grid, stream);
   if (act == JATTN_SILU) return launch6(dkdv_kernel<64, JATTN_SILU>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+  if (act == JATTN_GELU_POLY) return launch6(dkdv_kernel<64, JATTN_GELU_POLY>, sm, q, k, v, dout, o0, o1, a, grid, stream);
   return launch6(dkdv_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, o0, o1, a, grid, stream);
 }
 
@@ -1045,11 +1051,13 @@ cudaError_t launch_bwd_dq(int D, int act, const CUtensorMap& q, const CUtensorMa
     const int sm = act == JATTN_SOFTMAX ? DqCfg<128>::kSmemBytes : DqCfg<128>::kOOff;
     if (act == JATTN_SOFTMAX) return launch5(dq_kernel<128, JATTN_SOFTMAX>, sm, q, k, v, dout, o, a, grid, stream);
     if (act == JATTN_SILU) return launch5(dq_kernel<128, JATTN_SILU>, sm, q, k, v, dout, o, a, grid, stream);
+    if (act == JATTN_GELU_POLY) return launch5(dq_kernel<128, JATTN_GELU_POLY>, sm, q, k, v, dout, o, a, grid, stream);
     return launch5(dq_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, o, a, grid, stream);
   }
   const int sm = act == JATTN_SOFTMAX ? DqCfg<64>::kSmemBytes : DqCfg<64>::kOOff;
   if (act == JATTN_SOFTMAX) return launch5(dq_kernel<64, JATTN_SOFTMAX>, sm, q, k, v, dout, o, a, grid, stream);
   if (act == JATTN_SILU) return launch5(dq_kernel<64, JATTN_SILU>, sm, q, k, v, dout, o, a, grid, stream);
+  if (act == JATTN_GELU_POLY) return launch5(dq_kernel<64, JATTN_GELU_POLY>, sm, q, k, v, dout, o, a, grid, stream);
   return launch5(dq_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, o, a, grid, stream);
 }
 

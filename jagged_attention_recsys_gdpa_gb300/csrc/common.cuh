@@ -66,6 +66,27 @@ __device__ __forceinline__ void store_words16(void* dst, const uint32_t (&w)[16]
   }
 }
 
+// tanh-GELU's Taylor polynomial at 0 through x^6 and its derivative, on the
+// FMA pipe only. With c = sqrt(2/pi), a = 0.044715 and u = c (x + a x^3),
+// tanh u = u - u^3/3 + 2u^5/15 - ..., so x/2 (1 + tanh u) = x/2 + g2 x^2 +
+// g4 x^4 + g6 x^6 + O(x^8) with the coefficients below (odd powers above 1
+// cancel: x tanh u is even).
+struct GeluPoly {
+  static constexpr double c = 0.7978845608028654;  // sqrt(2/pi)
+  static constexpr double a = 0.044715;
+  static constexpr float g2 = static_cast<float>(c / 2);
+  static constexpr float g4 = static_cast<float>((c * a - c * c * c / 3) / 2);
+  static constexpr float g6 = static_cast<float>((2 * c * c * c * c * c / 15 - c * c * c * a) / 2);
+};
+__device__ __forceinline__ float gelu_poly(float x) {
+  const float x2 = x * x;
+  return fmaf(x2, fmaf(x2, fmaf(x2, GeluPoly::g6, GeluPoly::g4), GeluPoly::g2), 0.5f * x);
+}
+__device__ __forceinline__ float gelu_poly_grad(float x) {
+  const float x2 = x * x;
+  return fmaf(x, fmaf(x2, fmaf(x2, 6.0f * GeluPoly::g6, 4.0f * GeluPoly::g4), 2.0f * GeluPoly::g2), 0.5f);
+}
+
 // floor(x / w) for w >= 1 and any sign of x
 __device__ __forceinline__ int floor_div(int x, int w) { return x >= 0 ? x / w : -((w - 1 - x) / w); }
 

@@ -86,6 +86,12 @@ __device__ __forceinline__ float gelu_f(float x) {
   const float u = 0.7978845608028654f * fmaf(0.044715f * x * x, x, x);
   return 0.5f * x * (1.0f + tanh_approx(u));
 }
+template <int ACT>
+__device__ __forceinline__ float pointwise_f(float x) {
+  if constexpr (ACT == JATTN_SILU) return silu_f(x);
+  else if constexpr (ACT == JATTN_GELU_POLY) return gelu_poly(x);
+  else return gelu_f(x);
+}
 
 // Wait bounded by time, ignoring the abort flag (teardown of in-flight copies).
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
@@ -490,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 32; e += 2) {
                   const int c = c0 + e;
                   const float x0 = s[c] * a.scale, x1 = s[c + 1] * a.scale;
-                  float p0 = (ACT == JATTN_SILU) ? silu_f(x0) : gelu_f(x0);
-                  float p1 = (ACT == JATTN_SILU) ? silu_f(x1) : gelu_f(x1);
+                  float p0 = pointwise_f<ACT>(x0);
+                  float p1 = pointwise_f<ACT>(x1);
                   if (edge) {
                     p0 = (c >= clo && c < chi) ? p0 : 0.0f;
                     p1 = (c + 1 >= clo && c + 1 < chi) ? p1 : 0.0f;
@@ -672,8 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 32; e += 2) {
                 const int c = c0 + e;
                 const float x0 = s[c] * a.scale, x1 = s[c + 1] * a.scale;
-                float p0 = (ACT == JATTN_SILU) ? silu_f(x0) : gelu_f(x0);
-                float p1 = (ACT == JATTN_SILU) ? silu_f(x1) : gelu_f(x1);
+                float p0 = pointwise_f<ACT>(x0);
+                float p1 = pointwise_f<ACT>(x1);
                 if (edge) {
                   p0 = (c >= clo && c < chi) ? p0 : 0.0f;
                   p1 = (c + 1 >= clo && c + 1 < chi) ? p1 : 0.0f;
@@ -760,10 +766,12 @@ cudaError_t launch_fwd(int D, int act, bool split, const CUtensorMap& q, const C
   if (D == 128) {
     if (act == JATTN_SOFTMAX) return launch_fwd_s<128, JATTN_SOFTMAX>(split, q, k, v, a, grid, stream);
     if (act == JATTN_SILU) return launch_fwd_s<128, JATTN_SILU>(split, q, k, v, a, grid, stream);
+    if (act == JATTN_GELU_POLY) return launch_fwd_s<128, JATTN_GELU_POLY>(split, q, k, v, a, grid, stream);
     return launch_fwd_s<128, JATTN_GELU_TANH>(split, q, k, v, a, grid, stream);
   }
   if (act == JATTN_SOFTMAX) return launch_fwd_s<64, JATTN_SOFTMAX>(split, q, k, v, a, grid, stream);
   if (act == JATTN_SILU) return launch_fwd_s<64, JATTN_SILU>(split, q, k, v, a, grid, stream);
+  if (act == JATTN_GELU_POLY) return launch_fwd_s<64, JATTN_GELU_POLY>(split, q, k, v, a, grid, stream);
   return launch_fwd_s<64, JATTN_GELU_TANH>(split, q, k, v, a, grid, stream);
 }
 

@@ -19,6 +19,10 @@ histories):
 * ``gdpa_pma``   B=512, 32 queries per sequence, Lkv lognormal(median 2048,
                  sigma 1) clipped to [100, 20000], H=8, D=128, N(0, 0.5^2),
                  tanh-GELU with 1/Lkv normaliser, no mask
+* ``gdpa_pma_poly`` the ``gdpa_pma`` lengths and shapes with GDPA's ALU-only
+                 GELU (tanh-GELU's degree-6 Taylor polynomial); query and key
+                 rows normalised so that every score has |s| <= 1, the range
+                 the polynomial is accurate on
 * ``jfa_block``  the ``jfa`` lengths with block attention instead of the
                  window: each query sees only its own 64-key block (the
                  "BlockAttention" step of the same post)
@@ -38,7 +42,7 @@ from dataclasses import dataclass, replace
 
 import numpy as np
 
-SOFTMAX, SILU, GELU = 0, 1, 2
+SOFTMAX, SILU, GELU, GELU_POLY = 0, 1, 2, 3
 MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK = 0, 1, 2, 4
 
 
@@ -53,6 +57,11 @@ class Workload:
     norm_by_lkv: bool
     std: float
     self_attn: bool
+    # > 0: query and key rows are scaled to L2 norm sqrt(qk_norm * sqrt(D)),
+    # as a query/key normalisation layer would leave them, so that with the
+    # default scale 1/sqrt(D) every score satisfies |s| <= qk_norm (up to the
+    # bf16 rounding of the rows)
+    qk_norm: float = 0.0
 
 
 WORKLOADS = {
@@ -62,6 +71,7 @@ WORKLOADS = {
     "jfa_block": Workload("jfa_block", 4, 128, SOFTMAX, MASK_BLOCK, 64, False, 1.0, True),
     "gdpa_cross": Workload("gdpa_cross", 8, 128, SILU, MASK_NONE, 0, True, 0.5, False),
     "gdpa_pma": Workload("gdpa_pma", 8, 128, GELU, MASK_NONE, 0, True, 0.5, False),
+    "gdpa_pma_poly": Workload("gdpa_pma_poly", 8, 128, GELU_POLY, MASK_NONE, 0, True, 0.5, False, 1.0),
     "mixed": Workload("mixed", 8, 128, SOFTMAX, MASK_CAUSAL | MASK_WINDOW, 512, False, 1.0, True),
 }
 
@@ -84,7 +94,7 @@ def lengths(name: str, seed: int = 0):
         lq = _lognormal_int(rng, 1024, 512, 128, 8192)
         lkv = rng.integers(16, 129, size=512).astype(np.int64)
         return lq, lkv
-    if name == "gdpa_pma":
+    if name in ("gdpa_pma", "gdpa_pma_poly"):
         lkv = _lognormal_int(rng, 2048, 512, 100, 20000)
         lq = np.full(512, 32, dtype=np.int64)
         return lq, lkv
@@ -105,8 +115,9 @@ def offsets(lens: np.ndarray) -> np.ndarray:
     return out
 
 
-def values(shape, std: float, seed: int, device="cpu"):
-    """bf16 tensor of N(0, std^2) draws from a seeded torch generator."""
+def values(shape, std: float, seed: int, device="cpu", row_norm: float = 0.0):
+    """bf16 tensor of N(0, std^2) draws from a seeded torch generator; with
+    row_norm > 0 every last-axis row is then scaled to that L2 norm."""
     import torch
 
     g = torch.Generator(device=device)
@@ -114,6 +125,8 @@ def values(shape, std: float, seed: int, device="cpu"):
     x = torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
     if std != 1.0:
         x.mul_(std)
+    if row_norm > 0:
+        x.mul_(row_norm / x.norm(dim=-1, keepdim=True).clamp_min(1e-30))
     return x.to(torch.bfloat16)
 
 
@@ -134,14 +147,15 @@ def make(name_or_workload, seed: int = 0, device="cpu", lens=None, with_grad_out
         lq, lkv = (np.asarray(lens[0], dtype=np.int64), np.asarray(lens[1], dtype=np.int64))
     qo, ko = offsets(lq), offsets(lkv)
     tq, tk = int(qo[-1]), int(ko[-1])
+    qk_row = float(np.sqrt(w.qk_norm * np.sqrt(w.D))) if w.qk_norm > 0 else 0.0
     out = {
         "workload": w,
         "lq": lq,
         "lkv": lkv,
         "q_off": torch.from_numpy(qo).to(device),
         "kv_off": torch.from_numpy(ko).to(device),
-        "q": values((tq, w.H, w.D), w.std, seed, device),
-        "k": values((tk, w.H, w.D), w.std, seed + 1, device),
+        "q": values((tq, w.H, w.D), w.std, seed, device, qk_row),
+        "k": values((tk, w.H, w.D), w.std, seed + 1, device, qk_row),
         "v": values((tk, w.H, w.D), w.std, seed + 2, device),
     }
     if with_grad_out:

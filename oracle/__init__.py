@@ -28,7 +28,7 @@ _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libjattn_oracle.so")
 _SRC = os.path.join(_HERE, "jattn_oracle.c")
 
-SOFTMAX, SILU, GELU = 0, 1, 2
+SOFTMAX, SILU, GELU, GELU_POLY = 0, 1, 2, 3  # GELU_POLY: tanh-GELU here (see the C header)
 MASK_NONE, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK = 0, 1, 2, 4
 
 

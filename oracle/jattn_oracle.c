@@ -51,6 +51,9 @@
 #define ORACLE_SOFTMAX 0
 #define ORACLE_SILU 1
 #define ORACLE_GELU 2
+/* GELU evaluated by the GPU with a polynomial: the function it stands for
+ * is tanh-GELU, which is what the oracle computes for it. */
+#define ORACLE_GELU_POLY 3
 #define ORACLE_CAUSAL 1
 #define ORACLE_WINDOW 2
 #define ORACLE_BLOCK 4
@@ -99,6 +102,7 @@ static double gelu_grad(double x) {
   double t = tanh(GELU_K * (x + GELU_C * x * x * x));
   return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * GELU_K * (1.0 + 3.0 * GELU_C * x * x);
 }
+/* act is ORACLE_SILU, ORACLE_GELU or ORACLE_GELU_POLY (the last two both tanh-GELU) */
 static double act_fn(int act, double x) { return act == ORACLE_SILU ? silu(x) : gelu(x); }
 static double act_grad(int act, double x) { return act == ORACLE_SILU ? silu_grad(x) : gelu_grad(x); }
 

@@ -13,7 +13,20 @@ import numpy as np
 import torch
 import torch.nn.functional as F
 
-SOFTMAX, SILU, GELU = 0, 1, 2
+SOFTMAX, SILU, GELU, GELU_POLY = 0, 1, 2, 3
+
+# tanh-GELU's Taylor polynomial at 0 through x^6 (activation GELU_POLY): with
+# c = sqrt(2/pi), a = 0.044715, the coefficients of x^2, x^4 and x^6
+_C, _A = float(np.sqrt(2.0 / np.pi)), 0.044715
+POLY_G2 = _C / 2
+POLY_G4 = (_C * _A - _C**3 / 3) / 2
+POLY_G6 = (2 * _C**5 / 15 - _C**3 * _A) / 2
+
+
+def gelu_poly(x):
+    """The polynomial, for torch tensors or numpy arrays (autograd-friendly)."""
+    x2 = x * x
+    return 0.5 * x + x2 * (POLY_G2 + x2 * (POLY_G4 + x2 * POLY_G6))
 
 
 def mask_matrix(lq: int, lkv: int, mask: int, window: int) -> torch.Tensor:
@@ -65,7 +78,7 @@ def dense_forward(q, k, v, q_off, kv_off, act, mask, window, scale, norm_by_lkv)
         P = torch.softmax(Sm, dim=-1)
         P = torch.nan_to_num(P, nan=0.0)
     else:
-        A = F.silu(S) if act == SILU else F.gelu(S, approximate="tanh")
+        A = F.silu(S) if act == SILU else (gelu_poly(S) if act == GELU_POLY else F.gelu(S, approximate="tanh"))
         c = torch.tensor([1.0 / x if (norm_by_lkv and x > 0) else 1.0 for x in lk], dtype=S.dtype)
         P = A * M * c.view(B, 1, 1, 1)
         lse = torch.zeros(B, q.shape[1], Lq, dtype=S.dtype)

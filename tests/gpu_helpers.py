@@ -12,7 +12,7 @@ from jagged_attention_recsys_gdpa_gb300 import inputs
 ATOL = 1e-2
 RTOL = 1e-2
 
-ACT_NAME = {0: "softmax", 1: "silu", 2: "gelu"}
+ACT_NAME = {0: "softmax", 1: "silu", 2: "gelu", 3: "gelu_poly"}
 
 
 def gpu_run(inp, w, backward=True, stored=None):

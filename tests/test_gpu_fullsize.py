@@ -14,7 +14,9 @@ from tests import gpu_helpers as G
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name", ["tiny", "jfa", "jfa_causal", "jfa_block", "gdpa_cross", "gdpa_pma", "mixed"])
+@pytest.mark.parametrize(
+    "name", ["tiny", "jfa", "jfa_causal", "jfa_block", "gdpa_cross", "gdpa_pma", "gdpa_pma_poly", "mixed"]
+)
 def test_fullsize_sampled_sequences(name):
     w = inputs.WORKLOADS[name]
     x = inputs.make(name, seed=0, device="cuda")

@@ -316,3 +316,78 @@ def test_block_at_least_length_equals_unblocked(act):
                 assert b[k] is None, k
                 continue
             assert torch.equal(a[k], b[k]), (m_blk, k)
+
+
+# ---------------------------------------------------------------- GDPA's ALU-only GELU
+POLY = 3
+
+
+def _wp(mask, window, D, H=2, norm=True, qk=1.0):
+    return inputs.Workload("case", H, D, POLY, mask, window, norm, 0.5, True, qk)
+
+
+def _spread_scores(cpu, R, rank=3):
+    """Confine query and key rows to a `rank`-dim subspace and scale them so
+    that scores fill [-R, R] instead of clustering near 0 (random directions
+    in D dims are nearly orthogonal)."""
+    D = cpu["q"].shape[-1]
+    for key in ("q", "k"):
+        x = cpu[key].float()
+        x[..., rank:] = 0
+        x = x * (float(np.sqrt(R * np.sqrt(D))) / x.norm(dim=-1, keepdim=True).clamp_min(1e-30))
+        cpu[key] = x.to(torch.bfloat16)
+    return cpu
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("mask,window", [(NONE, 0), (CAUSAL, 0), (BLOCK, 64)])
+def test_gelu_poly_self(mask, window, D):
+    """Query/key-normalised rows (|s| <= 1): the polynomial GELU matches the
+    oracle's tanh-GELU."""
+    _check(_wp(mask, window, D), SELF_LENS, SELF_LENS, seed=41)
+
+
+def test_gelu_poly_cross_and_pma():
+    _check(_wp(NONE, 0, 128), CROSS_LQ, CROSS_LKV, seed=42)
+    _check(_wp(NONE, 0, 128, H=3), [32, 32, 32, 32], [100, 1000, 3000, 129], seed=43)
+
+
+def test_gelu_poly_unnormalised_short():
+    """Without the 1/Lkv normaliser, dS = act'(s) <dO_i, v_j> is O(1) and its
+    bf16 rounding (before the dQ and dK products) alone accumulates to the
+    tolerance over a few hundred rows: an fp64 emulation of just that rounding
+    exceeds it on the cross-attention lengths above (dK, 7 elements) and on
+    the pooling lengths (dQ, twice the bound). Short sequences keep it at
+    about half the bound."""
+    _check(_wp(NONE, 0, 128, norm=False), [100, 60, 5, 130, 1], [20, 128, 1, 64, 64], seed=42)
+
+
+def test_gelu_poly_scores_spread_over_the_range():
+    """Scores spread over [-0.9, 0.9], where the polynomial still agrees with
+    tanh-GELU within the tolerance (1/Lkv normaliser, as GDPA uses it)."""
+    w = _wp(NONE, 0, 128)
+    cpu = _spread_scores(G.cpu_inputs(w, CROSS_LQ, CROSS_LKV, seed=44), 0.9)
+    G.compare(G.gpu_run(G.to_cuda(cpu), w), G.oracle_run(cpu, w), w)
+
+
+def test_gelu_poly_is_the_polynomial():
+    """With scores out to |s| = 1.5 the polynomial and tanh-GELU part; the
+    kernels must follow the polynomial (fp64 padded dense reference of it,
+    gradients by autograd), and the case must tell the two apart."""
+    from tests import dense_ref as R
+
+    w = _wp(NONE, 0, 128)
+    lq, lkv = [100, 5, 260, 1], [20, 128, 130, 64]
+    cpu = _spread_scores(G.cpu_inputs(w, lq, lkv, seed=45), 1.5)
+    g = G.gpu_run(G.to_cuda(cpu), w)
+    args = [R.to_f64(cpu[x]) for x in ("q", "k", "v")]
+    offs = (cpu["q_off"].numpy(), cpu["kv_off"].numpy())
+    kw = dict(act=POLY, mask=0, window=0, scale=1.0 / np.sqrt(128), norm_by_lkv=True)
+    o, _ = R.dense_forward(*args, *offs, **kw)
+    dq, dk, dv = R.dense_grads(*args, R.to_f64(cpu["do"]), *offs, **kw)
+    ref = {"o": o.numpy(), "dq": dq.numpy(), "dk": dk.numpy(), "dv": dv.numpy()}
+    for key, name in (("o", "O"), ("dq", "dQ"), ("dk", "dK"), ("dv", "dV")):
+        G.assert_close(G.to64(g[key]), ref[key], name)
+    tanh_ref = G.oracle_run(cpu, w)
+    err = np.abs(tanh_ref["dk"] - ref["dk"]) - (G.ATOL + G.RTOL * np.abs(ref["dk"]))
+    assert err.max() > 0, "case does not separate the polynomial from tanh-GELU"
