@@ -273,7 +273,8 @@ int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
   a.f0 = lse;
   a.out_v8 = aligned32(o);
   prof(0, st);
-  if ((e = launch_fwd(p->D, p->act, fwd_split(*p), mq, mk, mv, a, grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
+  if ((e = launch_fwd(p->D, p->act, fwd_split(*p), (p->mask & JATTN_MASK_BLOCK) != 0, mq, mk, mv, a,
+                        grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
     return cuda_fail("forward kernel launch", e);
   prof(1, st);
   return JATTN_OK;
@@ -321,7 +322,8 @@ int jattn_fwd_noalloc(const jattn_params_t* p, const int64_t* q_off, const int64
     a.out0 = reinterpret_cast<__nv_bfloat16*>(o);
     a.f0 = lse;
     a.out_v8 = aligned32(o);
-    if ((e = launch_fwd(p->D, p->act, fwd_split(*p), mq, mk, mv, a, grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
+    if ((e = launch_fwd(p->D, p->act, fwd_split(*p), (p->mask & JATTN_MASK_BLOCK) != 0, mq, mk, mv, a,
+                        grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
       return cuda_fail("forward kernel launch", e);
   }
   if (device_status &&

@@ -32,6 +32,14 @@
 #include "common.cuh"
 #include "kernels.h"
 
+// This file is compiled twice: on its own for masks without the block bit,
+// where the block-mask arithmetic folds away at compile time (left in, it
+// cost the window-256 forward about 4%), and through fwd_block.cu with
+// JATTN_FWD_BLOCK = 1 for block masks.
+#ifndef JATTN_FWD_BLOCK
+#define JATTN_FWD_BLOCK 0
+#endif
+
 namespace jattn {
 
 namespace {
@@ -109,6 +117,11 @@ struct ItemInfo {
   bool t_rows[kNQ];          // tile has at least one query row
 };
 
+// The mask bits this compilation handles (see the top of the file).
+__device__ __forceinline__ int kernel_mask(const AttnArgs& a) {
+  return JATTN_FWD_BLOCK ? a.mask : (a.mask & ~JATTN_MASK_BLOCK);
+}
+
 __device__ __forceinline__ bool load_item(const AttnArgs& a, long long round, ItemInfo& it) {
   const long long n_items = static_cast<long long>(*a.n_tiles) * a.H;
   const long long k = zigzag_item(round, blockIdx.x, gridDim.x);
@@ -127,7 +140,7 @@ __device__ __forceinline__ bool load_item(const AttnArgs& a, long long round, It
   for (int q = 0; q < kNQ; ++q) {
     const int rt = it.qb * kNQ + q;
     it.t_rows[q] = rt * kTile < it.lq;
-    tile_range(it.lq, it.lkv, rt, kTile, kTile, a.mask, a.window, 0, it.t_lo[q], it.t_hi[q]);
+    tile_range(it.lq, it.lkv, rt, kTile, kTile, kernel_mask(a), a.window, 0, it.t_lo[q], it.t_hi[q]);
   }
   return true;
 }
@@ -367,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_run[kNQ], l_run[kNQ];
 #pragma unroll
         for (int q = 0; q < kNQ; ++q) {
-          key_interval((it.qb * kNQ + q) * kTile + row, delta, it.lkv, a.mask, a.window, klo[q], khi[q]);
+          key_interval((it.qb * kNQ + q) * kTile + row, delta, it.lkv, kernel_mask(a), a.window, klo[q], khi[q]);
           if ((it.qb * kNQ + q) * kTile + row >= it.lq) khi[q] = klo[q];  // rows past the sequence see nothing
           m_run[q] = -INFINITY;
           l_run[q] = 0.0f;
@@ -592,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t grow = it.q0 + row_local;
         const int delta = it.lkv - it.lq;
         int klo, khi;
-        key_interval(row_local, delta, it.lkv, a.mask, a.window, klo, khi);
+        key_interval(row_local, delta, it.lkv, kernel_mask(a), a.window, klo, khi);
         const int n = (it.hi > it.lo) ? (t_hi - t_lo) : 0;
         float m_run = -INFINITY, l_run = 0.0f;
         bool ok = true;
@@ -761,8 +774,14 @@ static cudaError_t launch_fwd_s(bool split, const CUtensorMap& q, const CUtensor
                : launch_fwd_t<D, ACT, false>(q, k, v, a, grid, stream);
 }
 
-cudaError_t launch_fwd(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
+#if JATTN_FWD_BLOCK
+cudaError_t launch_fwd_block(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
+                             const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream) {
+#else
+cudaError_t launch_fwd(int D, int act, bool split, bool block, const CUtensorMap& q, const CUtensorMap& k,
                        const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream) {
+  if (block) return launch_fwd_block(D, act, split, q, k, v, a, grid, stream);
+#endif
   if (D == 128) {
     if (act == JATTN_SOFTMAX) return launch_fwd_s<128, JATTN_SOFTMAX>(split, q, k, v, a, grid, stream);
     if (act == JATTN_SILU) return launch_fwd_s<128, JATTN_SILU>(split, q, k, v, a, grid, stream);
@@ -775,6 +794,8 @@ cudaError_t launch_fwd(int D, int act, bool split, const CUtensorMap& q, const C
   return launch_fwd_s<64, JATTN_GELU_TANH>(split, q, k, v, a, grid, stream);
 }
 
+#if !JATTN_FWD_BLOCK
 int fwd_rows_per_item() { return kNQ * kTile; }
+#endif
 
 }  // namespace jattn

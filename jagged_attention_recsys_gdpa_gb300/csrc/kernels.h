@@ -9,9 +9,12 @@ struct AttnArgs;
 
 // Forward: schedule rows are blocks of fwd_rows_per_item() query rows. `split`
 // selects the column-split arrangement of the activation warps (for items that
-// mostly hold one query tile) over the ping-pong one.
-cudaError_t launch_fwd(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
+// mostly hold one query tile) over the ping-pong one; `block` selects the
+// kernels compiled for block masks (launch_fwd_block, fwd_block.cu).
+cudaError_t launch_fwd(int D, int act, bool split, bool block, const CUtensorMap& q, const CUtensorMap& k,
                        const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_block(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
+                             const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream);
 int fwd_rows_per_item();
 
 // dK, dV over key tiles (transposed schedule, 128-row key tiles). o0 / o1 map
