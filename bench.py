@@ -37,9 +37,9 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # (profiles/<kernel>_kernel_jfa.md). Reported only while the kernel source
 # still has the sha1 prefix recorded at capture time; otherwise null.
 NCU_TRAFFIC = {
-    ("jfa", "fwd"): ("fwd.cu", "8bf195db9006", 944236288),
-    ("jfa", "dkdv"): ("bwd.cu", "3524d39d9151", 1390776320),
-    ("jfa", "dq"): ("bwd.cu", "3524d39d9151", 1408058512),
+    ("jfa", "fwd"): ("fwd.cu", "36dc45854a7c", 943320320),
+    ("jfa", "dkdv"): ("bwd.cu", "ed2991e832fd", 1386662144),
+    ("jfa", "dq"): ("bwd.cu", "ed2991e832fd", 1402045440),
 }
 
 

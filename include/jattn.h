@@ -85,7 +85,8 @@ enum {
   JATTN_ERR_OFFSETS = 5,     /* device: offsets not a valid prefix sum of the totals */
   JATTN_ERR_TIMEOUT = 6,     /* device: a bounded pipeline wait expired */
   JATTN_ERR_UNSUPPORTED = 7, /* device is not sm_103 / no kernel image */
-  JATTN_ERR_TOO_LARGE = 8    /* jattn_fwd_noalloc: problem needs more than the library's scratch */
+  JATTN_ERR_TOO_LARGE = 8,   /* jattn_fwd_noalloc: problem needs more than the library's scratch */
+  JATTN_ERR_ROPE = 9         /* device: a rotary position at or beyond the cos/sin tables' rows */
 };
 
 typedef struct {
@@ -124,6 +125,45 @@ int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
 int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
               const uint16_t* k, const uint16_t* v, const uint16_t* o, const float* lse, const uint16_t* dout,
               uint16_t* dq, uint16_t* dk, uint16_t* dv, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Rotary position embedding (RoPE) around the attention ("GEM Training" post,
+ * section "BlockAttention": the rotary backward fused into the attention
+ * epilogue, so the gradients leave the kernel already rotated back, straight
+ * from the fp32 accumulators, with no separate memory-bound pass).
+ *
+ * Rotation (the RoFormer form): dimensions pair up as (2m, 2m+1), m < D/2,
+ * and R(pos) turns pair m by the angle pos * theta_m:
+ *   y_2m   = x_2m cos - x_2m+1 sin,   y_2m+1 = x_2m sin + x_2m+1 cos,
+ * with cos = rope_cos[pos * D/2 + m] and sin = rope_sin[pos * D/2 + m]: the
+ * caller's fp32 device tables [rope_rows, D/2] (so theta, its base and any
+ * scaling are the caller's), 16-byte aligned.
+ * Positions: the queries and keys of a sequence end at the same position and
+ * the longer side starts at 0 (the alignment of the masks):
+ *   query row i -> i + max(delta, 0),  key row j -> j + max(-delta, 0),
+ * delta = Lkv - Lq; every position must be < rope_rows (else the device
+ * status becomes JATTN_ERR_ROPE and the affected rows are not rotated).
+ *
+ * jattn_rope: y = R(pos) x (inverse = 0) or R(pos)^T x (inverse = 1) for a
+ * jagged tensor x of queries (keys = 0: [total_q,H,D]) or keys (keys = 1:
+ * [total_kv,H,D]); y may alias x. A plain bandwidth-bound pass for the
+ * forward side (the rotated q and k the forward reads).
+ *
+ * jattn_bwd_rope: jattn_bwd for attention on rotated queries and keys q' =
+ * R q and k' = R k. It takes q' and k' (what the forward read) and returns
+ * dq and dk with respect to the UNROTATED q and k: dq = R^T dL/dq',
+ * dk = R^T dL/dk', applied in the dQ and dK epilogues. dv is unchanged.
+ * Its workspace must hold jattn_bwd_rope_workspace_size bytes: the regular
+ * layout plus pair-major copies of the tables ([D/2, rope_rows], made on
+ * `stream` by the call), which let each warp of the epilogues read its 32
+ * consecutive positions as one line. */
+int jattn_bwd_rope_workspace_size(const jattn_params_t* p, int64_t rope_rows, size_t* bytes);
+int jattn_rope(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, int keys, int inverse,
+               const uint16_t* x, uint16_t* y, const float* rope_cos, const float* rope_sin, int64_t rope_rows,
+               void* workspace, size_t workspace_bytes, void* stream);
+int jattn_bwd_rope(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
+                   const uint16_t* k, const uint16_t* v, const uint16_t* o, const float* lse, const uint16_t* dout,
+                   const float* rope_cos, const float* rope_sin, int64_t rope_rows, uint16_t* dq, uint16_t* dk,
+                   uint16_t* dv, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Longest-first tile schedule ("GEM Training" post, GDPA section: valid tiles
  * are precomputed, empty ones skipped, and the rest spread over the SMs so

@@ -11,6 +11,10 @@ query's own position, implies causal); ``block`` = W > 0 (each query sees only
 the keys of its own W-wide block, optionally causal inside it; not combined
 with ``window``).
 * ``forward(...)`` -> (O, LSE) and ``backward(...)`` -> (dQ, dK, dV): the raw passes.
+* ``rope(x, q_off, kv_off, (cos, sin), keys=..., inverse=...)``: rotary
+  embedding of query or key rows; ``backward(..., rope=(cos, sin))`` and
+  ``attention(..., rope=(cos, sin))`` rotate dQ and dK back inside the
+  backward kernels' epilogues.
 * ``schedule(...)``: the device-built longest-first tile list.
 
 Tensors: q [total_q, H, D], k / v [total_kv, H, D] in bf16 on a CUDA device;
@@ -68,9 +72,10 @@ def make_params(q, k, q_off, act, mask, width, scale, norm_by_lkv) -> B.Params:
                     width if mask & (MASK_WINDOW | MASK_BLOCK) else 0, scale, norm_by_lkv)
 
 
-def workspace(p: B.Params, device) -> torch.Tensor:
-    """Cached zero-initialised workspace of at least the size ``p`` needs."""
-    need = B.workspace_size(p)
+def workspace(p: B.Params, device, need: int | None = None) -> torch.Tensor:
+    """Cached zero-initialised workspace of at least the size ``p`` needs
+    (or ``need`` bytes)."""
+    need = B.workspace_size(p) if need is None else need
     dev = torch.device(device)
     key = dev.index if dev.index is not None else torch.cuda.current_device()
     ws = _ws_cache.get(key)
@@ -99,9 +104,40 @@ def forward(q, k, v, q_off, kv_off, act="softmax", causal=False, window=0, scale
     return o, (lse if a == SOFTMAX else None)
 
 
+def _rope_tables(rope, D, device):
+    cos, sin = rope
+    for t in (cos, sin):
+        if t.dtype != torch.float32 or t.dim() != 2 or t.shape[1] != D // 2 or t.device != torch.device(device):
+            raise ValueError("rope tables must be fp32 [rows, D/2] on the tensors' device")
+    if cos.shape != sin.shape:
+        raise ValueError("rope cos and sin tables differ in shape")
+    return cos.contiguous(), sin.contiguous()
+
+
+def rope(x, q_off, kv_off, rope, keys=False, inverse=False, out=None):
+    """Rotary embedding of jagged query rows (or key rows with ``keys``):
+    y = R(pos) x, or R(pos)^T x with ``inverse``. ``rope`` = (cos, sin) fp32
+    tables [rows, D/2]; positions as in jattn.h (both sides of a sequence end
+    at the same position, the longer one starts at 0)."""
+    if q_off.numel() != kv_off.numel() or q_off.numel() < 2:
+        raise ValueError("q_off and kv_off must both have B+1 >= 2 entries")
+    H, D = x.shape[1], x.shape[2]
+    cos, sin = _rope_tables(rope, D, x.device)
+    x = x.contiguous()
+    y = out if out is not None else torch.empty_like(x)
+    # the pass reads only this side's total from the params
+    tq, tk = (0, x.shape[0]) if keys else (x.shape[0], 0)
+    p = B.params(q_off.numel() - 1, tq, tk, H, D, SOFTMAX, 0, 0, 0.0, False)
+    ws = workspace(p, x.device)
+    B.rope(p, q_off, kv_off, keys, inverse, x, y, cos, sin, ws.data_ptr(), ws.numel(), _stream(x.device))
+    return y
+
+
 def backward(q, k, v, o, lse, do, q_off, kv_off, act="softmax", causal=False, window=0, scale=None,
-             norm_by_lkv=False, dq=None, dk=None, dv=None, block=0):
-    """Backward pass. Returns (dQ, dK, dV) bf16."""
+             norm_by_lkv=False, dq=None, dk=None, dv=None, block=0, rope=None):
+    """Backward pass. Returns (dQ, dK, dV) bf16. With ``rope`` = (cos, sin)
+    tables, q and k are the rotated rows the forward read and dQ, dK are
+    returned for the unrotated ones (rotated back in the kernels' epilogues)."""
     _check(q, k, v, q_off, kv_off)
     a = _act(act)
     p = make_params(q, k, q_off, a, _mask(causal, window, block), _width(window, block), scale, norm_by_lkv)
@@ -109,6 +145,12 @@ def backward(q, k, v, o, lse, do, q_off, kv_off, act="softmax", causal=False, wi
     dk = dk if dk is not None else torch.empty_like(k)
     dv = dv if dv is not None else torch.empty_like(v)
     do = do.contiguous()
+    if rope is not None:
+        cos, sin = _rope_tables(rope, q.shape[2], q.device)
+        ws = workspace(p, q.device, B.bwd_rope_workspace_size(p, cos.shape[0]))
+        B.bwd_rope(p, q_off, kv_off, q, k, v, o if a == SOFTMAX else None, lse if a == SOFTMAX else None, do, cos,
+                   sin, dq, dk, dv, ws.data_ptr(), ws.numel(), _stream(q.device))
+        return dq, dk, dv
     ws = workspace(p, q.device)
     B.bwd(p, q_off, kv_off, q, k, v, o if a == SOFTMAX else None, lse if a == SOFTMAX else None, do, dq, dk,
           dv, ws.data_ptr(), ws.numel(), _stream(q.device))
@@ -117,25 +159,34 @@ def backward(q, k, v, o, lse, do, q_off, kv_off, act="softmax", causal=False, wi
 
 class _JaggedAttention(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv, block):
+    def forward(ctx, q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv, block, rope_cos, rope_sin):
+        rope_t = None
+        if rope_cos is not None:  # attention on R q and R k; the backward rotates dQ, dK back
+            rope_t = (rope_cos, rope_sin)
+            q = rope(q, q_off, kv_off, rope_t, keys=False)
+            k = rope(k, q_off, kv_off, rope_t, keys=True)
         o, lse = forward(q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv, block=block)
         ctx.save_for_backward(q, k, v, o, lse if lse is not None else o.new_empty(0), q_off, kv_off)
-        ctx.cfg = (act, causal, window, scale, norm_by_lkv, block)
+        ctx.cfg = (act, causal, window, scale, norm_by_lkv, block, rope_t)
         return o
 
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, lse, q_off, kv_off = ctx.saved_tensors
-        act, causal, window, scale, norm_by_lkv, block = ctx.cfg
+        act, causal, window, scale, norm_by_lkv, block, rope_t = ctx.cfg
         dq, dk, dv = backward(q, k, v, o, lse if lse.numel() else None, do, q_off, kv_off, act, causal, window,
-                              scale, norm_by_lkv, block=block)
-        return dq, dk, dv, None, None, None, None, None, None, None, None
+                              scale, norm_by_lkv, block=block, rope=rope_t)
+        return dq, dk, dv, None, None, None, None, None, None, None, None, None, None
 
 
 def attention(q, k, v, q_off, kv_off, act="softmax", causal=False, window=0, scale=None, norm_by_lkv=False,
-              block=0):
-    """Jagged attention with autograd: O = act(scale Q K^T masked) V per sequence."""
-    return _JaggedAttention.apply(q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv, block)
+              block=0, rope=None):
+    """Jagged attention with autograd: O = act(scale Q K^T masked) V per sequence.
+    With ``rope`` = (cos, sin) tables, queries and keys are rotated first
+    (jattn_rope) and the backward rotates their gradients back in its
+    epilogues (jattn_bwd_rope)."""
+    rc, rs = rope if rope is not None else (None, None)
+    return _JaggedAttention.apply(q, k, v, q_off, kv_off, act, causal, window, scale, norm_by_lkv, block, rc, rs)
 
 
 def schedule(q_off, kv_off, H, D=128, causal=False, window=0, row_tile=128, col_tile=128, transposed=False,

@@ -20,6 +20,9 @@ EXPORTED = (
     "jattn_fwd",
     "jattn_fwd_noalloc",
     "jattn_bwd",
+    "jattn_bwd_rope",
+    "jattn_bwd_rope_workspace_size",
+    "jattn_rope",
     "jattn_schedule",
     "jattn_max_tiles",
     "jattn_get_status",
@@ -83,6 +86,12 @@ def load(path: str | None = None):
     lib.jattn_fwd_noalloc.restype = i32
     lib.jattn_bwd.argtypes = [P] + [vp] * 11 + [vp, ctypes.c_size_t, vp]
     lib.jattn_bwd.restype = i32
+    lib.jattn_bwd_rope.argtypes = [P] + [vp] * 10 + [i64] + [vp] * 3 + [vp, ctypes.c_size_t, vp]
+    lib.jattn_bwd_rope.restype = i32
+    lib.jattn_rope.argtypes = [P, vp, vp, i32, i32, vp, vp, vp, vp, i64, vp, ctypes.c_size_t, vp]
+    lib.jattn_rope.restype = i32
+    lib.jattn_bwd_rope_workspace_size.argtypes = [P, i64, ctypes.POINTER(ctypes.c_size_t)]
+    lib.jattn_bwd_rope_workspace_size.restype = i32
     lib.jattn_schedule.argtypes = [P, vp, vp, i32, i32, i32, vp, i64, vp, vp, ctypes.c_size_t, vp]
     lib.jattn_schedule.restype = i32
     lib.jattn_max_tiles.argtypes = [P, i32, i32]
@@ -121,6 +130,13 @@ def workspace_size(p: Params) -> int:
     return int(n.value)
 
 
+def bwd_rope_workspace_size(p: Params, rope_rows: int) -> int:
+    n = ctypes.c_size_t(0)
+    check(load().jattn_bwd_rope_workspace_size(ctypes.byref(p), int(rope_rows), ctypes.byref(n)),
+          "jattn_bwd_rope_workspace_size")
+    return int(n.value)
+
+
 def ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
@@ -139,6 +155,22 @@ def fwd_noalloc(p: Params, q_off, kv_off, q, k, v, o, lse, device_status, stream
 def bwd(p: Params, q_off, kv_off, q, k, v, o, lse, do, dq, dk, dv, ws, ws_bytes: int, stream: int):
     check(load().jattn_bwd(ctypes.byref(p), ptr(q_off), ptr(kv_off), ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse),
                            ptr(do), ptr(dq), ptr(dk), ptr(dv), ws, ws_bytes, stream), "jattn_bwd")
+
+
+def bwd_rope(p: Params, q_off, kv_off, q, k, v, o, lse, do, rope_cos, rope_sin, dq, dk, dv, ws, ws_bytes: int,
+             stream: int):
+    """jattn_bwd_rope: q and k are the rotated inputs; dq and dk come back rotated by R^T."""
+    check(load().jattn_bwd_rope(ctypes.byref(p), ptr(q_off), ptr(kv_off), ptr(q), ptr(k), ptr(v), ptr(o),
+                                ptr(lse), ptr(do), ptr(rope_cos), ptr(rope_sin), int(rope_cos.shape[0]), ptr(dq),
+                                ptr(dk), ptr(dv), ws, ws_bytes, stream), "jattn_bwd_rope")
+
+
+def rope(p: Params, q_off, kv_off, keys: bool, inverse: bool, x, y, rope_cos, rope_sin, ws, ws_bytes: int,
+         stream: int):
+    """jattn_rope: y = R(pos) x (or R(pos)^T x) on query (keys=False) or key rows."""
+    check(load().jattn_rope(ctypes.byref(p), ptr(q_off), ptr(kv_off), int(bool(keys)), int(bool(inverse)), ptr(x),
+                            ptr(y), ptr(rope_cos), ptr(rope_sin), int(rope_cos.shape[0]), ws, ws_bytes, stream),
+          "jattn_rope")
 
 
 def schedule(p: Params, q_off, kv_off, row_tile, col_tile, transposed, tiles, max_tiles, n_tiles, ws, ws_bytes,

@@ -332,9 +332,27 @@ int jattn_fwd_noalloc(const jattn_params_t* p, const int64_t* q_off, const int64
   return JATTN_OK;
 }
 
-int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
-              const uint16_t* k, const uint16_t* v, const uint16_t* o, const float* lse, const uint16_t* dout,
-              uint16_t* dq, uint16_t* dk, uint16_t* dv, void* ws, size_t ws_bytes, void* stream) {
+namespace jattn {
+namespace {
+
+// Rotary tables: both present, 16-byte aligned, 1 <= rows <= INT_MAX.
+int check_rope(const float* c, const float* s, int64_t rows) {
+  if (!c || !s || rows < 1 || rows > INT32_MAX) return JATTN_ERR_INVALID;
+  if (!aligned16(c) || !aligned16(s)) return JATTN_ERR_ALIGN;
+  return JATTN_OK;
+}
+
+// Bytes of the pair-major table copies jattn_bwd_rope keeps after the
+// workspace's regular layout (256-byte rounded).
+size_t rope_extra_bytes(int D, int64_t rows) {
+  return (static_cast<size_t>(rows) * D * sizeof(float) + 255) & ~static_cast<size_t>(255);
+}
+
+// jattn_bwd and jattn_bwd_rope (rope_cos == nullptr: no rotation).
+int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
+             const uint16_t* k, const uint16_t* v, const uint16_t* o, const float* lse, const uint16_t* dout,
+             const float* rope_cos, const float* rope_sin, int64_t rope_rows, uint16_t* dq, uint16_t* dk,
+             uint16_t* dv, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_params(p);
   if (rc != JATTN_OK) return rc;
   if (!q_off || !kv_off) return JATTN_ERR_INVALID;
@@ -345,16 +363,28 @@ int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
       !aligned16(dk) || !aligned16(dv))
     return JATTN_ERR_ALIGN;
   if ((rc = check_ws(p, ws, ws_bytes)) != JATTN_OK) return rc;
+  const Layout L = layout_for(*p);
+  if (rope_cos && ws_bytes < L.total + rope_extra_bytes(p->D, rope_rows)) return JATTN_ERR_WORKSPACE;
   DeviceInfo dev;
   if ((rc = device_info(dev)) != JATTN_OK) return rc;
   if ((rc = encoder()) != JATTN_OK) return rc;
   clear_stale_error();
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const Layout L = layout_for(*p);
   char* base = static_cast<char*>(ws);
   AttnArgs a = base_args(*p, q_off, kv_off, ws);
-  float* di = (p->act == JATTN_SOFTMAX) ? reinterpret_cast<float*>(base + L.di) : nullptr;
   cudaError_t e;
+  if (rope_cos) {
+    // pair-major copies of the tables after the regular layout (L.total is 256-byte aligned)
+    float* cos_pm = reinterpret_cast<float*>(base + L.total);
+    float* sin_pm = cos_pm + static_cast<size_t>(rope_rows) * (p->D / 2);
+    if ((e = launch_rope_transpose(rope_cos, rope_sin, static_cast<int>(rope_rows), p->D / 2, cos_pm, sin_pm,
+                                   st)) != cudaSuccess)
+      return cuda_fail("rotary table transpose launch", e);
+    a.rope_cos = cos_pm;
+    a.rope_sin = sin_pm;
+    a.rope_rows = static_cast<int>(rope_rows);
+  }
+  float* di = (p->act == JATTN_SOFTMAX) ? reinterpret_cast<float*>(base + L.di) : nullptr;
   CUtensorMap mq, mk, mv, mdo, mdk, mdv, mo;
   std::memset(&mo, 0, sizeof(mo));  // softmax only: the O tiles the dQ pass reads for Di
   if (make_map(&mq, q, p->total_q, p->H, p->D) || make_map(&mk, k, p->total_kv, p->H, p->D) ||
@@ -397,6 +427,57 @@ int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
     prof(3, st);
   }
   return JATTN_OK;
+}
+
+}  // namespace
+}  // namespace jattn
+
+int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
+              const uint16_t* k, const uint16_t* v, const uint16_t* o, const float* lse, const uint16_t* dout,
+              uint16_t* dq, uint16_t* dk, uint16_t* dv, void* ws, size_t ws_bytes, void* stream) {
+  return jattn::bwd_impl(p, q_off, kv_off, q, k, v, o, lse, dout, nullptr, nullptr, 0, dq, dk, dv, ws, ws_bytes,
+                         stream);
+}
+
+int jattn_bwd_rope(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
+                   const uint16_t* k, const uint16_t* v, const uint16_t* o, const float* lse, const uint16_t* dout,
+                   const float* rope_cos, const float* rope_sin, int64_t rope_rows, uint16_t* dq, uint16_t* dk,
+                   uint16_t* dv, void* ws, size_t ws_bytes, void* stream) {
+  const int rc = jattn::check_rope(rope_cos, rope_sin, rope_rows);
+  if (rc != JATTN_OK) return rc;
+  return jattn::bwd_impl(p, q_off, kv_off, q, k, v, o, lse, dout, rope_cos, rope_sin, rope_rows, dq, dk, dv, ws,
+                         ws_bytes, stream);
+}
+
+int jattn_bwd_rope_workspace_size(const jattn_params_t* p, int64_t rope_rows, size_t* bytes) {
+  if (!bytes) return JATTN_ERR_INVALID;
+  int rc = check_params(p);
+  if (rc != JATTN_OK) return rc;
+  if (rope_rows < 1 || rope_rows > INT32_MAX) return JATTN_ERR_INVALID;
+  *bytes = jattn::layout_for(*p).total + jattn::rope_extra_bytes(p->D, rope_rows);
+  return JATTN_OK;
+}
+
+int jattn_rope(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, int keys, int inverse,
+               const uint16_t* x, uint16_t* y, const float* rope_cos, const float* rope_sin, int64_t rope_rows,
+               void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_params(p);
+  if (rc != JATTN_OK) return rc;
+  if ((rc = check_rope(rope_cos, rope_sin, rope_rows)) != JATTN_OK) return rc;
+  if (!q_off || !kv_off || (keys != 0 && keys != 1) || (inverse != 0 && inverse != 1)) return JATTN_ERR_INVALID;
+  const int64_t total = keys ? p->total_kv : p->total_q;
+  if (total > 0 && (!x || !y)) return JATTN_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(y)) return JATTN_ERR_ALIGN;
+  // only the status word at the start of the workspace is used
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256) return JATTN_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if ((rc = device_info(dev)) != JATTN_OK) return rc;
+  clear_stale_error();
+  const cudaError_t e =
+      launch_rope(keys ? kv_off : q_off, keys ? q_off : kv_off, static_cast<int>(p->B), keys, inverse, p->H, p->D,
+                  total, x, y, rope_cos, rope_sin, static_cast<int>(rope_rows), reinterpret_cast<DevStatus*>(ws),
+                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? JATTN_OK : cuda_fail("rotary kernel launch", e);
 }
 
 int jattn_schedule(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, int row_tile,
@@ -448,6 +529,7 @@ const char* jattn_error_string(int code) {
     case JATTN_ERR_TIMEOUT: return "a bounded pipeline wait expired";
     case JATTN_ERR_UNSUPPORTED: return "device is not sm_103";
     case JATTN_ERR_TOO_LARGE: return "problem needs more scratch than the allocation-free entry point holds";
+    case JATTN_ERR_ROPE: return "a rotary position lies at or beyond the cos/sin tables' rows";
     default: return "unknown error code";
   }
 }

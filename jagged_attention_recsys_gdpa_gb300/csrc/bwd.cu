@@ -110,7 +110,7 @@ template <int NCH>
 __device__ __forceinline__ bool staged_store(uint32_t tacc, float mul, uint8_t* stage, int row, bool leader,
                                              const CUtensorMap* map, int x0, int y0, uint64_t* grp,
                                              uint32_t& phase, uint64_t* acc_empty, volatile int* abort_flag,
-                                             const AttnArgs& a, int where) {
+                                             const AttnArgs& a, int where, const float* rc, const float* rs) {
   const uint32_t srow = smem_u32(stage) + row * 128;
 #pragma unroll
   for (int hc = 0; hc < NCH; ++hc) {
@@ -118,6 +118,11 @@ __device__ __forceinline__ bool staged_store(uint32_t tacc, float mul, uint8_t* 
     tmem_ld32(tacc + hc * 64, *reinterpret_cast<uint32_t(*)[32]>(v));
     tmem_ld32(tacc + hc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
     tmem_ld_wait();
+    if (rc != nullptr) {  // rotary backward: columns hc*64 .. hc*64+63 are pairs hc*32 ..
+      const int64_t st = a.rope_rows;
+      rope_back16(v, rc + hc * 32 * st, rs + hc * 32 * st, a.rope_rows);
+      rope_back16(v + 32, rc + (hc * 32 + 16) * st, rs + (hc * 32 + 16) * st, a.rope_rows);
+    }
     if (hc == NCH - 1) {
       tc_fence_before();
       mbar_arrive(acc_empty);
@@ -557,13 +562,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t tAcc = tmem + lane_base + (g == 0 ? C::kDVCol : C::kDKCol);
         const float mul = (g == 0) ? cn : cn * a.scale;
+        const float* rc = nullptr;  // rotary backward of dK (group 1)
+        const float* rs = nullptr;
+        if (g == 1 && valid) rope_rows_at(a, rope_pos_k(jl, delta), rc, rs);
         bool staged = false;
         if constexpr (C::kTmaStore) {
           if ((it.rt + 1) * kTile <= it.lkv) {  // every key row of the tile is in the sequence
             staged = true;
             ok = staged_store<D / 64>(tAcc, mul, sm + C::kStageOff + g * 16384, row, gt == 0, g == 0 ? &tmO1 : &tmO0,
                                       it.h * D, static_cast<int>(it.k0) + it.rt * kTile, &bars->grp[g], grp_phase,
-                                      &bars->acc_empty, abort_flag, a, 63);
+                                      &bars->acc_empty, abort_flag, a, 63, rc, rs);
             if (!ok) break;
           }
         }
@@ -573,6 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t v[32];
             tmem_ld32(tAcc + c * 32, v);
             tmem_ld_wait();
+            if (rc != nullptr)
+              rope_back16(v, rc + static_cast<int64_t>(16 * c) * a.rope_rows,
+                          rs + static_cast<int64_t>(16 * c) * a.rope_rows, a.rope_rows);
             if (valid) store_row32(out_row + c * 32, v, mul, a.out_v8);
           }
           tc_fence_before();
@@ -983,11 +994,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++acc_cnt;
         tc_fence_after();
+        const float* rc = nullptr;  // rotary backward of dQ
+        const float* rs = nullptr;
+        if (valid) rope_rows_at(a, rope_pos_q(il, it.lkv - it.lq), rc, rs);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + C::kDQCol + (D / 2) * g + c * 32, v);
           tmem_ld_wait();
+          // columns (D/2) g + 32 c .. are pairs (D/4) g + 16 c ..
+          if (rc != nullptr) {
+            const int64_t m0 = (D / 4) * g + 16 * c;
+            rope_back16(v, rc + m0 * a.rope_rows, rs + m0 * a.rope_rows, a.rope_rows);
+          }
           if (valid) store_row32(dq_half + c * 32, v, cn * a.scale, a.out_v8);
         }
         tc_fence_before();

@@ -44,6 +44,11 @@ struct AttnArgs {
   uint64_t timeout_ns;
   int debug_flags;
   int out_v8;              // output rows may be written with 32-byte stores (bases 32-byte aligned)
+  // rotary tables, pair-major [D/2][rope_rows] (dQ / dK epilogues rotate back
+  // by R(pos)^T; consecutive rows of a warp read consecutive words); nullptr: none
+  const float* rope_cos;
+  const float* rope_sin;
+  int rope_rows;
 };
 
 // Store 16 packed words (32 bf16 values, 64 bytes) of one output row: two
@@ -85,6 +90,30 @@ __device__ __forceinline__ float gelu_poly(float x) {
 __device__ __forceinline__ float gelu_poly_grad(float x) {
   const float x2 = x * x;
   return fmaf(x, fmaf(x2, fmaf(x2, 6.0f * GeluPoly::g6, 4.0f * GeluPoly::g4), 2.0f * GeluPoly::g2), 0.5f);
+}
+
+// Rotary positions of sequence-local query row i and key row j: both sides end
+// at the same position and the longer one starts at 0 (delta = Lkv - Lq).
+__device__ __forceinline__ int rope_pos_q(int i, int delta) { return i + max(delta, 0); }
+__device__ __forceinline__ int rope_pos_k(int j, int delta) { return j + max(-delta, 0); }
+
+// x = R(pos)^T y in place on 16 pairs of fp32 values (bit patterns in v):
+// pair e is turned back by the angle whose cos / sin are c[e * stride] /
+// s[e * stride] (pair-major tables: c and s point at the first pair's entry
+// for this row's position).
+__device__ __forceinline__ void rope_back16(uint32_t* v, const float* c, const float* s, int stride) {
+  float ca[16], sa[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    ca[e] = __ldg(c + static_cast<int64_t>(e) * stride);
+    sa[e] = __ldg(s + static_cast<int64_t>(e) * stride);
+  }
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float y0 = __uint_as_float(v[2 * e]), y1 = __uint_as_float(v[2 * e + 1]);
+    v[2 * e] = __float_as_uint(fmaf(y0, ca[e], y1 * sa[e]));
+    v[2 * e + 1] = __float_as_uint(fmaf(y1, ca[e], -y0 * sa[e]));
+  }
 }
 
 // floor(x / w) for w >= 1 and any sign of x
@@ -159,6 +188,20 @@ __device__ __forceinline__ void record_error(DevStatus* st, int code, int where,
     st->where = where;
     st->detail = detail;
   }
+}
+
+// Pair-0 entries of position pos in the pair-major tables (pair m is m *
+// rope_rows further on): nullptr when no rotation is asked for, or (after
+// recording JATTN_ERR_ROPE) when pos is past the tables.
+__device__ __forceinline__ void rope_rows_at(const AttnArgs& a, int pos, const float*& c, const float*& s) {
+  c = s = nullptr;
+  if (a.rope_cos == nullptr) return;
+  if (pos < 0 || pos >= a.rope_rows) {
+    record_error(a.status, JATTN_ERR_ROPE, 70, pos);
+    return;
+  }
+  c = a.rope_cos + pos;
+  s = a.rope_sin + pos;
 }
 
 // Bounded mbarrier wait. Returns false (and raises the CTA abort flag and the

@@ -1,11 +1,14 @@
 // Host-side launchers of the attention kernels.
 #pragma once
+#include <cstdint>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace jattn {
 
 struct AttnArgs;
+struct DevStatus;
 
 // Forward: schedule rows are blocks of fwd_rows_per_item() query rows. `split`
 // selects the column-split arrangement of the activation warps (for items that
@@ -28,5 +31,15 @@ cudaError_t launch_bwd_dkdv(int D, int act, const CUtensorMap& q, const CUtensor
 cudaError_t launch_bwd_dq(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a, int grid,
                           cudaStream_t stream);
+
+// Rotary embedding of a jagged tensor x ([total, H, D] bf16, rows described
+// by own_off; other_off describes the other side for the alignment):
+// y = R(pos) x, or R(pos)^T x with `inverse`. keys: x holds key rows.
+cudaError_t launch_rope(const int64_t* own_off, const int64_t* other_off, int B, int keys, int inverse, int H,
+                        int D, int64_t total, const void* x, void* y, const float* cos_t, const float* sin_t,
+                        int rows, DevStatus* status, cudaStream_t stream);
+// Row-major [rows, half] cos / sin tables to pair-major [half, rows] copies.
+cudaError_t launch_rope_transpose(const float* cos_t, const float* sin_t, int rows, int half, float* cos_pm,
+                                  float* sin_pm, cudaStream_t stream);
 
 }  // namespace jattn

@@ -14,6 +14,12 @@ of ``bench.py`` use it. It shares no code with the CUDA library.
   tiles its mask allows, ordered longest-first with ties in (sequence, tile)
   order.
 * ``count_pairs`` counts allowed (query, key) pairs by visiting every pair.
+* ``rope`` rotates jagged query or key rows by the rotary embedding (the
+  RoFormer pairing (2m, 2m+1), angles from the caller's cos / sin tables),
+  in double: the forward side of the rotary backward fused into the
+  attention epilogue ("GEM Training" post, section "BlockAttention"). The
+  gradient of attention on rotated rows w.r.t. the unrotated ones is this
+  rotation's transpose applied to ``bwd``'s dQ and dK.
 """
 from __future__ import annotations
 
@@ -147,6 +153,35 @@ def bwd(q_off, kv_off, q, k, v, do, *, H, D, act=SOFTMAX, mask=MASK_NONE, window
     _load().oracle_bwd(ctypes.byref(P), _p(q_off), _p(kv_off), _p(q), _p(k), _p(v), _p(do), o_ptr, _p(dq), _p(dk),
                        _p(dv))
     return dq, dk, dv
+
+
+def rope(x, q_off, kv_off, cos, sin, *, keys=False, inverse=False) -> np.ndarray:
+    """Rotary embedding of jagged rows x [total, H, D] (queries, or keys with
+    ``keys``), in double: pair m = (2m, 2m+1) of every head turns by the angle
+    at the row's position, y_2m = x_2m cos - x_2m+1 sin, y_2m+1 = x_2m sin +
+    x_2m+1 cos (``inverse``: the transpose, i.e. sin negated). cos / sin:
+    [rows, D/2] tables of that angle. Positions: the queries and keys of a
+    sequence end at the same position and the longer side starts at 0, so
+    query row i sits at i + max(delta, 0) and key row j at j + max(-delta, 0),
+    delta = Lkv - Lq."""
+    q_off, kv_off = _off(q_off), _off(kv_off)
+    x = _dbl(x)
+    cos = np.asarray(cos, dtype=np.float64)
+    sin = np.asarray(sin, dtype=np.float64) * (-1.0 if inverse else 1.0)
+    own, other = (kv_off, q_off) if keys else (q_off, kv_off)
+    y = np.empty_like(x)
+    for b in range(len(own) - 1):
+        n_own, n_other = int(own[b + 1] - own[b]), int(other[b + 1] - other[b])
+        delta = (n_own - n_other) if keys else (n_other - n_own)  # Lkv - Lq
+        shift = max(-delta, 0) if keys else max(delta, 0)
+        pos = np.arange(n_own) + shift
+        c = cos[pos][:, None, :]
+        s = sin[pos][:, None, :]
+        rows = slice(int(own[b]), int(own[b + 1]))
+        even, odd = x[rows, :, 0::2], x[rows, :, 1::2]
+        y[rows, :, 0::2] = even * c - odd * s
+        y[rows, :, 1::2] = even * s + odd * c
+    return y
 
 
 def count_pairs(q_off, kv_off, mask=MASK_NONE, window=0) -> int:

@@ -93,8 +93,8 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
 
 
 def test_error_strings(lib):
-    for code in range(9):
-        assert B.error_string(code)
+    for code in range(10):
+        assert B.error_string(code) != "unknown error code", code
     assert B.error_string(99) == "unknown error code"
 
 
@@ -105,3 +105,30 @@ def test_python_api_rejects_block_with_window():
         J._mask(True, 16, 64)
     assert J._mask(False, 0, 64) == 4 and J._mask(True, 0, 64) == 5
     assert J._width(0, 64) == 64 and J._width(256, 0) == 256
+
+
+def test_rope_entry_points_check_arguments(lib):
+    """Host-side argument checks of the rotary entry points (no launch)."""
+    p = _params(D=64)
+    ws = ctypes.c_void_p(256)  # never dereferenced: every call below fails its checks first
+    fake = ctypes.c_void_p(4096)
+    off = ctypes.c_void_p(8192)
+    # missing tables, bad row counts, unaligned tables
+    for cos, sin, rows, want in ((None, fake, 10, 1), (fake, None, 10, 1), (fake, fake, 0, 1),
+                                 (fake, fake, 1 << 31, 1), (ctypes.c_void_p(4100), fake, 10, 4)):
+        assert lib.jattn_rope(ctypes.byref(p), off, off, 0, 0, fake, fake, cos, sin, rows, ws, 256, None) == want
+        assert lib.jattn_bwd_rope(ctypes.byref(p), off, off, fake, fake, fake, fake, fake, fake, cos, sin, rows, fake,
+                                  fake, fake, ws, 1 << 30, None) == want
+    # keys / inverse must be 0 or 1; the workspace must hold the status word
+    assert lib.jattn_rope(ctypes.byref(p), off, off, 2, 0, fake, fake, fake, fake, 10, ws, 256, None) == 1
+    assert lib.jattn_rope(ctypes.byref(p), off, off, 0, 5, fake, fake, fake, fake, 10, ws, 256, None) == 1
+    assert lib.jattn_rope(ctypes.byref(p), off, off, 0, 0, fake, fake, fake, fake, 10, ws, 128, None) == 3
+
+
+def test_bwd_rope_workspace_size(lib):
+    p = _params(D=128, total_q=1000, total_kv=1000)
+    base = B.workspace_size(p)
+    assert B.bwd_rope_workspace_size(p, 4096) == base + 4096 * 128 * 4
+    assert B.bwd_rope_workspace_size(p, 3) == base + 1536  # two 3 x 64 fp32 tables
+    size = ctypes.c_size_t(0)
+    assert lib.jattn_bwd_rope_workspace_size(ctypes.byref(p), 0, ctypes.byref(size)) == 1

@@ -390,3 +390,98 @@ def test_bwd_from_stored_output(mask, window, lens):
     kwp = dict(kw, act=SILU)
     for a, b in zip(oracle.bwd(qo, ko, q, k, v, do, o=o + E, **kwp), oracle.bwd(qo, ko, q, k, v, do, **kwp)):
         np.testing.assert_array_equal(a, b)
+
+
+# ---------------------------------------------------------------- rotary embedding
+def rope_tables(rows, D, base=10000.0):
+    """RoFormer angles pos * base^(-2m/D) as cos / sin tables [rows, D/2]."""
+    theta = base ** (-2.0 * np.arange(D // 2) / D)
+    ang = np.arange(rows)[:, None] * theta[None, :]
+    return np.cos(ang), np.sin(ang), ang
+
+
+@pytest.mark.parametrize("keys", [False, True])
+def test_rope_is_complex_multiplication(keys):
+    """Pair m as the complex number x_2m + i x_2m+1 is multiplied by e^(i angle);
+    the inverse multiplies by e^(-i angle); positions follow the alignment."""
+    H, D = 2, 16
+    lq, lk = np.array([5, 0, 9, 3]), np.array([7, 4, 2, 3])
+    qo, ko = inputs.offsets(lq), inputs.offsets(lk)
+    n = int((ko if keys else qo)[-1])
+    x = inputs.values((n, H, D), 1.0, 71)
+    cos, sin, ang = rope_tables(16, D)
+    xd = R.to_f64(x).numpy()
+    for inverse in (False, True):
+        y = oracle.rope(x, qo, ko, cos, sin, keys=keys, inverse=inverse)
+        own, oth = (lk, lq) if keys else (lq, lk)
+        r0 = 0
+        for b in range(len(own)):
+            delta = (lk[b] - lq[b])
+            shift = max(-delta, 0) if keys else max(delta, 0)
+            for i in range(own[b]):
+                z = xd[r0 + i, :, 0::2] + 1j * xd[r0 + i, :, 1::2]
+                w = z * np.exp((-1j if inverse else 1j) * ang[i + shift])[None, :]
+                np.testing.assert_allclose(y[r0 + i, :, 0::2], w.real, rtol=1e-13, atol=1e-14)
+                np.testing.assert_allclose(y[r0 + i, :, 1::2], w.imag, rtol=1e-13, atol=1e-14)
+            r0 += own[b]
+        back = oracle.rope(y, qo, ko, cos, sin, keys=keys, inverse=not inverse)
+        np.testing.assert_allclose(back, xd, rtol=1e-13, atol=1e-14)
+
+
+def test_rope_scores_depend_on_relative_position():
+    """<R(p) q, R(p') k> depends on p - p' only: moving every position by 5
+    (tables read 5 rows later) leaves all scores unchanged."""
+    H, D = 1, 8
+    lq, lk = np.array([6, 3]), np.array([4, 8])
+    qo, ko = inputs.offsets(lq), inputs.offsets(lk)
+    q = inputs.values((int(qo[-1]), H, D), 1.0, 72)
+    k = inputs.values((int(ko[-1]), H, D), 1.0, 73)
+    cos, sin, _ = rope_tables(20, D)
+    def scores(c, s):
+        rq = oracle.rope(q, qo, ko, c, s)
+        rk = oracle.rope(k, qo, ko, c, s, keys=True)
+        return [rq[qo[b]:qo[b + 1], 0] @ rk[ko[b]:ko[b + 1], 0].T for b in range(2)]
+    for a, b in zip(scores(cos, sin), scores(cos[5:], sin[5:])):
+        np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("act,mask", [(SOFTMAX, CAUSAL), (GELU, NONE), (SOFTMAX, BLOCK)])
+def test_rope_backward_is_the_transposed_rotation_of_the_gradient(act, mask):
+    """Gradients of attention on rotated rows, w.r.t. the unrotated q and k
+    (torch fp64 autograd through a padded dense formulation with the rotation
+    written in torch), equal R^T applied to the oracle's dQ and dK."""
+    H, D, scale = 2, 8, 0.35
+    lq, lk = [3, 9, 0, 12], [5, 9, 4, 7]
+    qo, ko, q, k, v, do = _batch(lq, lk, H, D, seed=74)
+    cos, sin, _ = rope_tables(16, D)
+    window = 4 if mask == BLOCK else 0
+    kw = dict(H=H, D=D, act=act, mask=mask, window=window, scale=scale)
+    rq = oracle.rope(q, qo, ko, cos, sin)
+    rk = oracle.rope(k, qo, ko, cos, sin, keys=True)
+    dq_r, dk_r, dv = oracle.bwd(qo, ko, rq, rk, v, do, **kw)
+    dq = oracle.rope(dq_r, qo, ko, cos, sin, inverse=True)
+    dk = oracle.rope(dk_r, qo, ko, cos, sin, keys=True, inverse=True)
+
+    def rot_torch(x, off, oth, keys):
+        parts = []
+        for b in range(len(off) - 1):
+            n, m = off[b + 1] - off[b], oth[b + 1] - oth[b]
+            delta = (n - m) if keys else (m - n)
+            shift = max(-delta, 0) if keys else max(delta, 0)
+            pos = np.arange(n) + shift
+            c = torch.from_numpy(cos[pos])[:, None, :]
+            s = torch.from_numpy(sin[pos])[:, None, :]
+            xs = x[off[b]:off[b + 1]]
+            e, o = xs[..., 0::2], xs[..., 1::2]
+            parts.append(torch.stack((e * c - o * s, e * s + o * c), dim=-1).reshape(xs.shape))
+        return torch.cat(parts, 0)
+
+    tq = R.to_f64(q).requires_grad_(True)
+    tk = R.to_f64(k).requires_grad_(True)
+    tv = R.to_f64(v).requires_grad_(True)
+    o, _ = R.dense_forward(rot_torch(tq, qo, ko, False), rot_torch(tk, ko, qo, True), tv, qo, ko, act, mask, window,
+                           scale, False)
+    (o * R.to_f64(do)).sum().backward()
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-9, atol=1e-11)
