@@ -114,15 +114,15 @@ def _rope_tables(rope, D, device):
     return cos.contiguous(), sin.contiguous()
 
 
-def rope(x, q_off, kv_off, rope, keys=False, inverse=False, out=None):
+def rope(x, q_off, kv_off, tables, keys=False, inverse=False, out=None):
     """Rotary embedding of jagged query rows (or key rows with ``keys``):
-    y = R(pos) x, or R(pos)^T x with ``inverse``. ``rope`` = (cos, sin) fp32
-    tables [rows, D/2]; positions as in jattn.h (both sides of a sequence end
-    at the same position, the longer one starts at 0)."""
+    y = R(pos) x, or R(pos)^T x with ``inverse``. ``tables`` = (cos, sin) fp32
+    [rows, D/2]; positions as in jattn.h (both sides of a sequence end at the
+    same position, the longer one starts at 0)."""
     if q_off.numel() != kv_off.numel() or q_off.numel() < 2:
         raise ValueError("q_off and kv_off must both have B+1 >= 2 entries")
     H, D = x.shape[1], x.shape[2]
-    cos, sin = _rope_tables(rope, D, x.device)
+    cos, sin = _rope_tables(tables, D, x.device)
     x = x.contiguous()
     y = out if out is not None else torch.empty_like(x)
     # the pass reads only this side's total from the params
