@@ -165,6 +165,28 @@ int jattn_bwd_rope(const jattn_params_t* p, const int64_t* q_off, const int64_t*
                    const float* rope_cos, const float* rope_sin, int64_t rope_rows, uint16_t* dq, uint16_t* dk,
                    uint16_t* dv, void* workspace, size_t workspace_bytes, void* stream);
 
+/* MXFP8 quantization of a jagged tensor ("GEM Training" post, section "Low
+ * Precision Flash Attention": block-scaled FP8 operands, FP8 data kept at the
+ * unpadded positions with compact scales, and [32, 32] square blocks with one
+ * scale each, so that a tensor quantized once serves both orientations).
+ *
+ * x: bf16 [total, H, D] rows described by off (int64 [B+1] device prefix
+ * sums, checked like jattn_fwd's). codes: uint8 [total, H, D], the FP8 E4M3
+ * code of every element at its own position. scales: uint8 E8M0 exponents
+ * [jattn_mxfp8_scale_rows(B, total), H, D/32]; row block g of sequence b
+ * (its sequence-local rows 32r .. 32r+31, the last block ragged) is
+ * g = block_start[b] + r, and block_start (device int32 [B+1]) receives the
+ * exclusive prefix sum of ceil(L_b / 32). For a block with largest magnitude
+ * amax: E = max(0, floor(log2(amax)) - 8 + 127) (0 for an all-zero block),
+ * X = 2^(E - 127), code = E4M3(x / X) rounded to nearest even and saturated
+ * to +-448. Only the 32 * 32 block rows that exist are written. x and codes
+ * 16-byte aligned; the workspace needs 512 bytes (status word + a count).
+ * Bad offsets set JATTN_ERR_OFFSETS in the status word and write nothing. */
+int64_t jattn_mxfp8_scale_rows(int64_t B, int64_t total);
+int jattn_mxfp8_quantize(int64_t B, int64_t total, int H, int D, const int64_t* off, const uint16_t* x,
+                         uint8_t* codes, uint8_t* scales, int32_t* block_start, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
 /* Longest-first tile schedule ("GEM Training" post, GDPA section: valid tiles
  * are precomputed, empty ones skipped, and the rest spread over the SMs so
  * no SM gets a much longer share). Builds the schedule the kernels use into

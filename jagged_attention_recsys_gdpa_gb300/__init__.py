@@ -133,6 +133,26 @@ def rope(x, q_off, kv_off, tables, keys=False, inverse=False, out=None):
     return y
 
 
+def mxfp8_quantize(x, off):
+    """MXFP8 quantization of jagged bf16 rows x [total, H, D] (offsets ``off``):
+    returns (codes uint8 [total, H, D], scale exponents uint8 [rows, H, D/32],
+    block_start int32 [B+1]); row block r of sequence b is scale row
+    block_start[b] + r. See jattn_mxfp8_quantize."""
+    if x.dtype != torch.bfloat16 or x.dim() != 3 or off.dtype != torch.int64 or off.numel() < 2:
+        raise ValueError("x must be bf16 [total, H, D] and off int64 [B+1]")
+    x = x.contiguous()
+    total, H, D = x.shape
+    nb = off.numel() - 1
+    codes = torch.empty((total, H, D), dtype=torch.uint8, device=x.device)
+    scales = torch.zeros((B.mxfp8_scale_rows(nb, total), H, D // 32), dtype=torch.uint8, device=x.device)
+    block_start = torch.empty(nb + 1, dtype=torch.int32, device=x.device)
+    p = B.params(nb, total, total, H, D, SOFTMAX, 0, 0, 0.0, False)
+    ws = workspace(p, x.device, max(B.workspace_size(p), 512))
+    B.mxfp8_quantize(nb, total, H, D, off, x, codes, scales, block_start, ws.data_ptr(), ws.numel(),
+                     _stream(x.device))
+    return codes, scales, block_start
+
+
 def backward(q, k, v, o, lse, do, q_off, kv_off, act="softmax", causal=False, window=0, scale=None,
              norm_by_lkv=False, dq=None, dk=None, dv=None, block=0, rope=None):
     """Backward pass. Returns (dQ, dK, dV) bf16. With ``rope`` = (cos, sin)

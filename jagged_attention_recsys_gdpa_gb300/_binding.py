@@ -23,6 +23,8 @@ EXPORTED = (
     "jattn_bwd_rope",
     "jattn_bwd_rope_workspace_size",
     "jattn_rope",
+    "jattn_mxfp8_scale_rows",
+    "jattn_mxfp8_quantize",
     "jattn_schedule",
     "jattn_max_tiles",
     "jattn_get_status",
@@ -90,6 +92,10 @@ def load(path: str | None = None):
     lib.jattn_bwd_rope.restype = i32
     lib.jattn_rope.argtypes = [P, vp, vp, i32, i32, vp, vp, vp, vp, i64, vp, ctypes.c_size_t, vp]
     lib.jattn_rope.restype = i32
+    lib.jattn_mxfp8_scale_rows.argtypes = [i64, i64]
+    lib.jattn_mxfp8_scale_rows.restype = i64
+    lib.jattn_mxfp8_quantize.argtypes = [i64, i64, i32, i32] + [vp] * 5 + [vp, ctypes.c_size_t, vp]
+    lib.jattn_mxfp8_quantize.restype = i32
     lib.jattn_bwd_rope_workspace_size.argtypes = [P, i64, ctypes.POINTER(ctypes.c_size_t)]
     lib.jattn_bwd_rope_workspace_size.restype = i32
     lib.jattn_schedule.argtypes = [P, vp, vp, i32, i32, i32, vp, i64, vp, vp, ctypes.c_size_t, vp]
@@ -163,6 +169,16 @@ def bwd_rope(p: Params, q_off, kv_off, q, k, v, o, lse, do, rope_cos, rope_sin, 
     check(load().jattn_bwd_rope(ctypes.byref(p), ptr(q_off), ptr(kv_off), ptr(q), ptr(k), ptr(v), ptr(o),
                                 ptr(lse), ptr(do), ptr(rope_cos), ptr(rope_sin), int(rope_cos.shape[0]), ptr(dq),
                                 ptr(dk), ptr(dv), ws, ws_bytes, stream), "jattn_bwd_rope")
+
+
+def mxfp8_scale_rows(B: int, total: int) -> int:
+    return int(load().jattn_mxfp8_scale_rows(int(B), int(total)))
+
+
+def mxfp8_quantize(B: int, total: int, H: int, D: int, off, x, codes, scales, block_start, ws, ws_bytes: int,
+                   stream: int):
+    check(load().jattn_mxfp8_quantize(int(B), int(total), int(H), int(D), ptr(off), ptr(x), ptr(codes), ptr(scales),
+                                      ptr(block_start), ws, ws_bytes, stream), "jattn_mxfp8_quantize")
 
 
 def rope(p: Params, q_off, kv_off, keys: bool, inverse: bool, x, y, rope_cos, rope_sin, ws, ws_bytes: int,

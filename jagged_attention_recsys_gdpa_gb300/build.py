@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libjattn.so")
-SOURCES = ["api.cu", "sched.cu", "fwd.cu", "fwd_block.cu", "bwd.cu", "rope.cu"]
+SOURCES = ["api.cu", "sched.cu", "fwd.cu", "fwd_block.cu", "bwd.cu", "rope.cu", "mx.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "--expt-relaxed-constexpr"]
 

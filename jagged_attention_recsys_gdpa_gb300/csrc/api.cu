@@ -458,6 +458,33 @@ int jattn_bwd_rope_workspace_size(const jattn_params_t* p, int64_t rope_rows, si
   return JATTN_OK;
 }
 
+int64_t jattn_mxfp8_scale_rows(int64_t B, int64_t total) {
+  return (B < 0 || total < 0) ? 0 : total / 32 + B;
+}
+
+int jattn_mxfp8_quantize(int64_t B, int64_t total, int H, int D, const int64_t* off, const uint16_t* x,
+                         uint8_t* codes, uint8_t* scales, int32_t* block_start, void* ws, size_t ws_bytes,
+                         void* stream) {
+  if (B < 1 || B > INT32_MAX || total < 0 || total > INT32_MAX || H < 1 || (D != 64 && D != 128)) return JATTN_ERR_INVALID;
+  if (!off || !block_start || (total > 0 && (!x || !codes || !scales))) return JATTN_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(codes)) return JATTN_ERR_ALIGN;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 512) return JATTN_ERR_WORKSPACE;
+  DeviceInfo dev;
+  int rc;
+  if ((rc = device_info(dev)) != JATTN_OK) return rc;
+  clear_stale_error();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DevStatus* status = reinterpret_cast<DevStatus*>(ws);
+  int* n_blocks = reinterpret_cast<int*>(static_cast<char*>(ws) + 256);
+  cudaError_t e;
+  if ((e = sched_prefix_launch(off, B, total, 32, block_start, n_blocks, status, st)) != cudaSuccess)
+    return cuda_fail("row-block prefix launch", e);
+  if ((e = launch_mx_quant(off, static_cast<int>(B), H, D, jattn_mxfp8_scale_rows(B, total), x, codes, scales,
+                           block_start, n_blocks, st)) != cudaSuccess)
+    return cuda_fail("MXFP8 quantize launch", e);
+  return JATTN_OK;
+}
+
 int jattn_rope(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, int keys, int inverse,
                const uint16_t* x, uint16_t* y, const float* rope_cos, const float* rope_sin, int64_t rope_rows,
                void* ws, size_t ws_bytes, void* stream) {

@@ -38,6 +38,10 @@ cudaError_t launch_bwd_dq(int D, int act, const CUtensorMap& q, const CUtensorMa
 cudaError_t launch_rope(const int64_t* own_off, const int64_t* other_off, int B, int keys, int inverse, int H,
                         int D, int64_t total, const void* x, void* y, const float* cos_t, const float* sin_t,
                         int rows, DevStatus* status, cudaStream_t stream);
+// MXFP8 (E4M3 + one E8M0 scale per 32 x 32 block) quantization of a jagged
+// bf16 tensor; block_start / n_blocks come from sched_prefix_launch(32).
+cudaError_t launch_mx_quant(const int64_t* off, int B, int H, int D, int64_t max_blocks, const void* x, void* codes,
+                            uint8_t* scales, const int* block_start, const int* n_blocks, cudaStream_t stream);
 // Row-major [rows, half] cos / sin tables to pair-major [half, rows] copies.
 cudaError_t launch_rope_transpose(const float* cos_t, const float* sin_t, int rows, int half, float* cos_pm,
                                   float* sin_pm, cudaStream_t stream);

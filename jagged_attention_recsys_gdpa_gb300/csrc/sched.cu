@@ -215,6 +215,12 @@ SchedView sched_carve(void* base, int64_t B, int64_t max_tiles) {
   return v;
 }
 
+cudaError_t sched_prefix_launch(const int64_t* off, int64_t B, int64_t total, int row_tile, int* tile_start,
+                                int* n_tiles, DevStatus* status, cudaStream_t stream) {
+  sched_prep<<<1, 1024, 0, stream>>>(off, off, B, total, total, row_tile, 0, tile_start, n_tiles, status);
+  return cudaGetLastError();
+}
+
 cudaError_t sched_launch(const SchedView& v, const int64_t* q_off, const int64_t* kv_off, int64_t B,
                          int64_t total_q, int64_t total_kv, int row_tile, int col_tile, int mask, int window,
                          int transposed, DevStatus* status, cudaStream_t stream) {

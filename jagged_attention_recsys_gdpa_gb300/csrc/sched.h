@@ -22,6 +22,9 @@ struct SchedView {
 int64_t sched_max_tiles(int64_t B, int64_t rows_total, int row_tile);
 size_t sched_ws_bytes(int64_t B, int64_t max_tiles);
 SchedView sched_carve(void* base, int64_t B, int64_t max_tiles);
+// Only the checked offsets' prefix of ceil(L_b / row_tile) (no sort).
+cudaError_t sched_prefix_launch(const int64_t* off, int64_t B, int64_t total, int row_tile, int* tile_start,
+                                int* n_tiles, DevStatus* status, cudaStream_t stream);
 cudaError_t sched_launch(const SchedView& v, const int64_t* q_off, const int64_t* kv_off, int64_t B,
                          int64_t total_q, int64_t total_kv, int row_tile, int col_tile, int mask, int window,
                          int transposed, DevStatus* status, cudaStream_t stream);
