@@ -22,6 +22,11 @@ scale each so that a tensor quantized once serves both its orientations):
 Row block g of sequence b, row block r, is g = block_start[b] + r with
 block_start the exclusive prefix sum of ceil(L_b / 32); scales are laid out
 [row blocks, H, D/32].
+
+``attention_fwd`` / ``attention_bwd`` state softmax attention on MXFP8
+operands (P quantized in the softmax with the scale its row maximum fixes,
+dS quantized with [32, 32] blocks); they are the reference for a block-scaled
+attention kernel, which is not built yet.
 """
 from __future__ import annotations
 
@@ -128,3 +133,113 @@ def dequantize(codes, scales, off) -> np.ndarray:
             X = np.exp2(scales[bs[b] + r].astype(np.float64) - 127.0)  # [H, D/32]
             out[r0:r1] *= np.repeat(X, 32, axis=1)[None]
     return out
+
+
+# ---------------------------------------------------------------- MXFP8 attention
+# Softmax attention on MXFP8 operands, written from the same section: Q, K, V
+# (and dO in the backward) arrive as MXFP8 codes with [32, 32] block scales;
+# the products run on their exact values; the softmax output P is quantized
+# to E4M3 with the scale that the row maximum fixes (P <= 1 with equality at
+# the maximum, so X = 2^(0 - 8) for every row: no further reduction), and the
+# backward's dS is quantized with [32, 32] blocks over (query, key) tiles of
+# each sequence. The normaliser l and D_i stay in high precision. Masks are
+# those of the C oracle (causal, causal + window, block, causal + block).
+
+P_SCALE_EXP = 127 - E4M3_EMAX  # E of X = 2^-8
+
+
+def _allowed(lq: int, lkv: int, mask: int, window: int) -> np.ndarray:
+    i = np.arange(lq)[:, None]
+    j = np.arange(lkv)[None, :]
+    d = lkv - lq
+    ok = np.ones((lq, lkv), dtype=bool)
+    if mask & 3:
+        ok &= j <= i + d
+    if mask & 2:
+        ok &= i + d - j < window
+    if mask & 4:
+        ok &= np.floor_divide(j, window) == np.floor_divide(i + d, window)
+    return ok
+
+
+def quantize_p(p: np.ndarray) -> np.ndarray:
+    """P in [0, 1] to its E4M3 value with X = 2^-8."""
+    X = np.exp2(P_SCALE_EXP - 127.0)
+    return e4m3_decode(e4m3_encode(p / X)) * X
+
+
+def quantize_square(a: np.ndarray) -> np.ndarray:
+    """A 2-D array through [32, 32]-block MXFP8 (blocks from the origin,
+    ragged at the ends), back to values."""
+    out = np.empty_like(a)
+    for r0 in range(0, a.shape[0], 32):
+        for c0 in range(0, a.shape[1], 32):
+            q, E = quantize_block(a[r0:r0 + 32, c0:c0 + 32])
+            out[r0:r0 + 32, c0:c0 + 32] = e4m3_decode(q) * np.exp2(E - 127.0)
+    return out
+
+
+def attention_fwd(qd, kd, vd, q_off, kv_off, *, mask=0, window=0, scale=None, quant_p=True):
+    """Forward on dequantized operands qd / kd / vd [total, H, D] (float64,
+    e.g. from dequantize). Returns (o, lse); quant_p=False keeps P exact."""
+    q_off = np.asarray(q_off, dtype=np.int64)
+    kv_off = np.asarray(kv_off, dtype=np.int64)
+    H, D = qd.shape[1], qd.shape[2]
+    scale = 1.0 / np.sqrt(D) if scale is None else scale
+    o = np.zeros_like(qd)
+    lse = np.full(qd.shape[:2], -np.inf)
+    for b in range(len(q_off) - 1):
+        lq, lkv = int(q_off[b + 1] - q_off[b]), int(kv_off[b + 1] - kv_off[b])
+        if lq == 0 or lkv == 0:
+            continue
+        ok = _allowed(lq, lkv, mask, window)
+        rows = ok.any(axis=1)
+        for h in range(H):
+            s = scale * qd[q_off[b]:q_off[b + 1], h] @ kd[kv_off[b]:kv_off[b + 1], h].T
+            s = np.where(ok, s, -np.inf)
+            m = np.where(rows, s.max(axis=1, initial=-np.inf), 0.0)
+            p = np.where(ok, np.exp(s - m[:, None]), 0.0)
+            l = p.sum(axis=1)
+            pq = quantize_p(p) if quant_p else p
+            oh = np.zeros((lq, D))
+            oh[rows] = (pq @ vd[kv_off[b]:kv_off[b + 1], h])[rows] / l[rows, None]
+            o[q_off[b]:q_off[b + 1], h] = oh
+            lse[q_off[b]:q_off[b + 1], h] = np.where(rows, m + np.log(np.where(rows, l, 1.0)), -np.inf)
+    return o, lse
+
+
+def attention_bwd(qd, kd, vd, dod, q_off, kv_off, *, mask=0, window=0, scale=None, o=None, quant_p=True,
+                  quant_ds=True):
+    """Backward on dequantized operands (dod: dequantized dO). D_i = <dO_i,
+    o_i> with o the stored forward output (default: this module's forward).
+    dV = P~^T dO, dQ = scale dS~ K, dK = scale dS~^T Q with P~ as in the
+    forward and dS~ the [32, 32]-block quantization of dS = P (dP - D)."""
+    q_off = np.asarray(q_off, dtype=np.int64)
+    kv_off = np.asarray(kv_off, dtype=np.int64)
+    H, D = qd.shape[1], qd.shape[2]
+    scale = 1.0 / np.sqrt(D) if scale is None else scale
+    if o is None:
+        o, _ = attention_fwd(qd, kd, vd, q_off, kv_off, mask=mask, window=window, scale=scale, quant_p=quant_p)
+    dq, dk, dv = np.zeros_like(qd), np.zeros_like(kd), np.zeros_like(vd)
+    for b in range(len(q_off) - 1):
+        lq, lkv = int(q_off[b + 1] - q_off[b]), int(kv_off[b + 1] - kv_off[b])
+        if lq == 0 or lkv == 0:
+            continue
+        ok = _allowed(lq, lkv, mask, window)
+        rows = ok.any(axis=1)
+        qs, ks = slice(q_off[b], q_off[b + 1]), slice(kv_off[b], kv_off[b + 1])
+        for h in range(H):
+            s = np.where(ok, scale * qd[qs, h] @ kd[ks, h].T, -np.inf)
+            m = np.where(rows, s.max(axis=1, initial=-np.inf), 0.0)
+            e = np.where(ok, np.exp(s - m[:, None]), 0.0)
+            l = np.where(rows, e.sum(axis=1), 1.0)
+            p = e / l[:, None]  # normalised probabilities
+            pq = quantize_p(e) / l[:, None] if quant_p else p
+            di = np.einsum("id,id->i", dod[qs, h], o[qs, h])
+            dp = dod[qs, h] @ vd[ks, h].T
+            ds = np.where(ok, p * (dp - di[:, None]), 0.0)
+            dsq = quantize_square(ds) if quant_ds else ds
+            dv[ks, h] = pq.T @ dod[qs, h]
+            dq[qs, h] = scale * dsq @ kd[ks, h]
+            dk[ks, h] = scale * dsq.T @ qd[qs, h]
+    return dq, dk, dv

@@ -105,3 +105,57 @@ def test_representable_values_round_trip_exactly():
     got_codes, got_scales, _ = mx.quantize(x, off)
     assert np.array_equal(got_codes, codes)
     assert np.array_equal(got_scales[:, 0, 0], E[:, 0, 0])
+
+
+# ---------------------------------------------------------------- MXFP8 attention
+import oracle  # noqa: E402
+
+
+def _mx_inputs(lq, lk, H, D, seed):
+    rng = np.random.default_rng(seed)
+    qo = np.concatenate([[0], np.cumsum(lq)]).astype(np.int64)
+    ko = np.concatenate([[0], np.cumsum(lk)]).astype(np.int64)
+    def deq(n, off):
+        x = rng.normal(0, 1, (n, H, D))
+        c, s, _ = mx.quantize(x, off)
+        return mx.dequantize(c, s, off)
+    return qo, ko, deq(int(qo[-1]), qo), deq(int(ko[-1]), ko), deq(int(ko[-1]), ko), deq(int(qo[-1]), qo)
+
+
+@pytest.mark.parametrize("mask,window", [(0, 0), (1, 0), (3, 5), (4, 8), (5, 8)])
+def test_mx_attention_without_quantized_intermediates_is_the_oracle(mask, window):
+    """With P and dS kept exact, the MXFP8 attention of dequantized operands
+    is the C oracle's attention of the same values (forward and backward)."""
+    H, D = 2, 64
+    qo, ko, q, k, v, do = _mx_inputs([5, 40, 0, 33], [9, 40, 3, 33], H, D, 5)
+    kw = dict(mask=mask, window=window, scale=0.125)
+    o, lse = mx.attention_fwd(q, k, v, qo, ko, quant_p=False, **kw)
+    o_ref, lse_ref = oracle.fwd(qo, ko, q, k, v, H=H, D=D, **kw)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-13)
+    g = mx.attention_bwd(q, k, v, do, qo, ko, o=o_ref, quant_p=False, quant_ds=False, **kw)
+    g_ref = oracle.bwd(qo, ko, q, k, v, do, H=H, D=D, **kw)
+    for a, b in zip(g, g_ref):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-12)
+
+
+def test_mx_attention_quantized_p():
+    """P quantized with X = 2^-8: probabilities keep half an E4M3 ulp; a row
+    that sees one key (P = 1, exactly representable) returns that value row."""
+    p = np.linspace(0, 1, 100001)
+    pq = mx.quantize_p(p)
+    assert np.all(np.abs(pq - p) <= np.maximum(2.0**-4 * p, 2.0**-18) * (1 + 1e-12))
+    assert mx.quantize_p(np.array([1.0]))[0] == 1.0
+    qo, ko, q, k, v, _ = _mx_inputs([7], [7], 1, 64, 6)
+    o, _ = mx.attention_fwd(q, k, v, qo, ko, mask=1)
+    np.testing.assert_array_equal(o[0], v[0])  # causal row 0 sees key 0 only
+
+
+def test_square_quantization_matches_the_jagged_quantizer():
+    """quantize_square (dS blocks) and quantize (operands) agree on one
+    sequence, and quantize_square commutes with transposition."""
+    rng = np.random.default_rng(7)
+    a = rng.normal(0, 1, (70, 96)) * np.exp2(rng.integers(-5, 5, (70, 96)))
+    c, s, _ = mx.quantize(a[:, None, :], np.array([0, 70]))
+    np.testing.assert_array_equal(mx.quantize_square(a), mx.dequantize(c, s, np.array([0, 70]))[:, 0, :])
+    np.testing.assert_array_equal(mx.quantize_square(a.T), mx.quantize_square(a).T)
