@@ -146,7 +146,17 @@ int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
  * jattn_rope: y = R(pos) x (inverse = 0) or R(pos)^T x (inverse = 1) for a
  * jagged tensor x of queries (keys = 0: [total_q,H,D]) or keys (keys = 1:
  * [total_kv,H,D]); y may alias x. A plain bandwidth-bound pass for the
- * forward side (the rotated q and k the forward reads).
+ * forward side (the rotated q and k the forward reads). p supplies B, H, D
+ * and the total of the rotated side (total_q or total_kv); both offset
+ * arrays are read (the other side fixes the alignment). The workspace needs
+ * only its first 256 bytes (the status word). Device pointers: q_off,
+ * kv_off, x, y (16-byte aligned), rope_cos, rope_sin (16-byte aligned).
+ *
+ * Return codes (both rotary calls): JATTN_ERR_INVALID for bad params, a
+ * missing table or rope_rows outside [1, INT32_MAX], keys / inverse not 0 or
+ * 1; JATTN_ERR_ALIGN for misaligned tensors or tables; JATTN_ERR_WORKSPACE
+ * for a workspace that is missing, misaligned or too small; JATTN_ERR_CUDA
+ * when a launch fails. Nothing is launched when a host check fails.
  *
  * jattn_bwd_rope: jattn_bwd for attention on rotated queries and keys q' =
  * R q and k' = R k. It takes q' and k' (what the forward read) and returns
@@ -181,7 +191,12 @@ int jattn_bwd_rope(const jattn_params_t* p, const int64_t* q_off, const int64_t*
  * X = 2^(E - 127), code = E4M3(x / X) rounded to nearest even and saturated
  * to +-448. Only the 32 * 32 block rows that exist are written. x and codes
  * 16-byte aligned; the workspace needs 512 bytes (status word + a count).
- * Bad offsets set JATTN_ERR_OFFSETS in the status word and write nothing. */
+ * Bad offsets set JATTN_ERR_OFFSETS in the status word and write nothing.
+ * Return codes: JATTN_ERR_INVALID (B < 1, totals or B beyond INT32_MAX,
+ * H < 1, D not 64 / 128, a missing pointer), JATTN_ERR_ALIGN,
+ * JATTN_ERR_WORKSPACE, JATTN_ERR_CUDA (launch failed); the caller owns every
+ * buffer and scales has room for jattn_mxfp8_scale_rows(B, total) rows (an
+ * upper bound: total/32 + B). */
 int64_t jattn_mxfp8_scale_rows(int64_t B, int64_t total);
 int jattn_mxfp8_quantize(int64_t B, int64_t total, int H, int D, const int64_t* off, const uint16_t* x,
                          uint8_t* codes, uint8_t* scales, int32_t* block_start, void* workspace,

@@ -132,3 +132,18 @@ def test_bwd_rope_workspace_size(lib):
     assert B.bwd_rope_workspace_size(p, 3) == base + 1536  # two 3 x 64 fp32 tables
     size = ctypes.c_size_t(0)
     assert lib.jattn_bwd_rope_workspace_size(ctypes.byref(p), 0, ctypes.byref(size)) == 1
+
+
+def test_mxfp8_entry_checks_arguments(lib):
+    """Host-side checks of jattn_mxfp8_quantize (no launch) and the scale-row bound."""
+    assert lib.jattn_mxfp8_scale_rows(3, 100) == 100 // 32 + 3
+    assert lib.jattn_mxfp8_scale_rows(-1, 5) == 0
+    fake, off, ws = ctypes.c_void_p(4096), ctypes.c_void_p(8192), ctypes.c_void_p(256)
+    q = lib.jattn_mxfp8_quantize
+    assert q(0, 10, 2, 64, off, fake, fake, fake, fake, ws, 512, None) == 1      # B < 1
+    assert q(2, 10, 2, 96, off, fake, fake, fake, fake, ws, 512, None) == 1      # D
+    assert q(2, 10, 0, 64, off, fake, fake, fake, fake, ws, 512, None) == 1      # H
+    assert q(2, 10, 2, 64, None, fake, fake, fake, fake, ws, 512, None) == 1     # offsets
+    assert q(2, 10, 2, 64, off, ctypes.c_void_p(4100), fake, fake, fake, ws, 512, None) == 4  # alignment
+    assert q(2, 10, 2, 64, off, fake, fake, fake, fake, ws, 256, None) == 3      # workspace too small
+    assert q(2, 10, 2, 64, off, fake, fake, fake, fake, ctypes.c_void_p(300), 512, None) == 3  # misaligned
