@@ -3,19 +3,24 @@
 Public API (thin wrappers over the C-ABI library ``libjattn``; every step of
 the computation runs in its CUDA kernels):
 
-* ``attention(q, k, v, q_off, kv_off, act=..., causal=..., window=..., scale=..., norm_by_lkv=..., block=...)``
-  autograd-enabled jagged attention returning O.
-
-Masks: ``causal``; ``window`` = W > 0 (sliding window of W keys ending at the
-query's own position, implies causal); ``block`` = W > 0 (each query sees only
-the keys of its own W-wide block, optionally causal inside it; not combined
-with ``window``).
+* ``attention(q, k, v, q_off, kv_off, act=..., causal=..., window=..., scale=...,
+  norm_by_lkv=..., block=..., rope=...)``: autograd-enabled jagged attention
+  returning O.
 * ``forward(...)`` -> (O, LSE) and ``backward(...)`` -> (dQ, dK, dV): the raw passes.
 * ``rope(x, q_off, kv_off, (cos, sin), keys=..., inverse=...)``: rotary
   embedding of query or key rows; ``backward(..., rope=(cos, sin))`` and
   ``attention(..., rope=(cos, sin))`` rotate dQ and dK back inside the
   backward kernels' epilogues.
+* ``mxfp8_quantize(x, off)``: FP8 E4M3 codes plus one E8M0 scale per 32 x 32
+  block of a jagged tensor.
 * ``schedule(...)``: the device-built longest-first tile list.
+
+Activations (``act``): "softmax", "silu", "gelu" (tanh form) or "gelu_poly"
+(its degree-6 Taylor polynomial on the FMA pipe, for |scores| <= 1).
+Masks: ``causal``; ``window`` = W > 0 (sliding window of W keys ending at the
+query's own position, implies causal); ``block`` = W > 0 (each query sees only
+the keys of its own W-wide block, optionally causal inside it; not combined
+with ``window``).
 
 Tensors: q [total_q, H, D], k / v [total_kv, H, D] in bf16 on a CUDA device;
 q_off / kv_off int64 [B+1] prefix sums on the same device. D is 64 or 128.
