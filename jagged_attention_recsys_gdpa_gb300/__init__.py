@@ -79,7 +79,10 @@ def make_params(q, k, q_off, act, mask, width, scale, norm_by_lkv) -> B.Params:
 
 def workspace(p: B.Params, device, need: int | None = None) -> torch.Tensor:
     """Cached zero-initialised workspace of at least the size ``p`` needs
-    (or ``need`` bytes)."""
+    (or ``need`` bytes). One per device: calls through this module that run
+    at the same time on different streams of one device would share its
+    status word and schedules, so issue them from one stream (or call the
+    C ABI with a workspace per stream)."""
     need = B.workspace_size(p) if need is None else need
     dev = torch.device(device)
     key = dev.index if dev.index is not None else torch.cuda.current_device()
