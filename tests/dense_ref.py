@@ -125,3 +125,10 @@ def to_f64(x) -> torch.Tensor:
     if isinstance(x, np.ndarray):
         return torch.from_numpy(x)
     return x.detach().to(torch.float64).cpu()
+
+
+def rope_tables(rows, D, base=10000.0):
+    """RoFormer angles pos * base^(-2m/D) as cos / sin tables [rows, D/2] (and the angles)."""
+    theta = base ** (-2.0 * np.arange(D // 2) / D)
+    ang = np.arange(rows)[:, None] * theta[None, :]
+    return np.cos(ang), np.sin(ang), ang

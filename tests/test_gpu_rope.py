@@ -8,7 +8,7 @@ import torch
 import oracle
 from jagged_attention_recsys_gdpa_gb300 import inputs
 from tests import gpu_helpers as G
-from tests.test_oracle import rope_tables
+from tests.dense_ref import rope_tables
 
 pytestmark = pytest.mark.gpu
 

@@ -393,11 +393,7 @@ def test_bwd_from_stored_output(mask, window, lens):
 
 
 # ---------------------------------------------------------------- rotary embedding
-def rope_tables(rows, D, base=10000.0):
-    """RoFormer angles pos * base^(-2m/D) as cos / sin tables [rows, D/2]."""
-    theta = base ** (-2.0 * np.arange(D // 2) / D)
-    ang = np.arange(rows)[:, None] * theta[None, :]
-    return np.cos(ang), np.sin(ang), ang
+rope_tables = R.rope_tables
 
 
 @pytest.mark.parametrize("keys", [False, True])
