@@ -147,3 +147,34 @@ def test_mxfp8_entry_checks_arguments(lib):
     assert q(2, 10, 2, 64, off, ctypes.c_void_p(4100), fake, fake, fake, ws, 512, None) == 4  # alignment
     assert q(2, 10, 2, 64, off, fake, fake, fake, fake, ws, 256, None) == 3      # workspace too small
     assert q(2, 10, 2, 64, off, fake, fake, fake, fake, ctypes.c_void_p(300), 512, None) == 3  # misaligned
+
+
+def test_header_is_plain_c_and_links(tmp_path, lib):
+    """include/jattn.h compiles as C99 (no C++ in the boundary), and a C
+    program links against libjattn.so and calls entry points that need no GPU."""
+    import shutil
+    import subprocess
+
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "use_jattn.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "jattn.h"\n'
+        "int main(void) {\n"
+        "  jattn_params_t p = {2, 100, 100, 4, 128, JATTN_SOFTMAX, JATTN_MASK_CAUSAL, 0, 0.0f, 0};\n"
+        "  size_t bytes = 0;\n"
+        "  int rc = jattn_workspace_size(&p, &bytes);\n"
+        '  printf("%d %zu %s %lld\\n", rc, bytes, jattn_error_string(JATTN_ERR_OFFSETS),\n'
+        "         (long long)jattn_mxfp8_scale_rows(3, 100));\n"
+        "  return rc;\n}\n"
+    )
+    exe = tmp_path / "use_jattn"
+    libdir = os.path.dirname(B.library_path())
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe),
+                        "-L", libdir, "-ljattn", f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    rc, nbytes, rest = out.stdout.split(" ", 2)
+    assert rc == "0" and int(nbytes) == B.workspace_size(_params(B=2, total_q=100, total_kv=100, H=4, D=128, mask=1))
+    assert rest.strip().endswith(" 6") and "offsets" in rest
