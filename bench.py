@@ -1,13 +1,15 @@
 """Benchmark: jagged attention forward + backward on one GB300 per rank.
 
 One step = one pass of the whole hot path over one batch: device schedule,
-forward (O, LSE), and backward (dQ with Di, then dK/dV) of the JFA self-attention
-workload (128 jagged sequences, lognormal lengths with median 1024 clipped to
-[64, 16384], H=4, D=128, causal + sliding window 256, bf16, seed = rank).
+forward (O, LSE), and backward (dQ with Di, then dK/dV). The default workload
+is the largest self-attention batch: 1024 jagged sequences, 307 long ones
+uniform in [4000, 32000] and 717 short ones uniform in [50, 500], H=8, D=128,
+softmax, causal + sliding window 512, bf16 (``--workload`` picks another).
 
 Prints one JSON line. value = effective (unpadded, unmasked) TFLOP/s of the
-step (forward 4*D*H*pairs + backward 10*D*H*pairs) summed over ranks / max
-rank time. Inputs are already resident in HBM for `value`; `e2e` repeats the
+step (forward 4*D*H*pairs + backward 10*D*H*pairs) of the whole global batch
+over the slowest rank's time (N > 1: one batch per rank, drawn as one jagged
+batch and split over the ranks by allowed pairs). Inputs are already resident in HBM for `value`; `e2e` repeats the
 measurement through the public Python API with pinned host buffers and the
 host<->device copies inside the timed region. `--impl reference` times the
 CPU oracle instead, on a bounded sample of the same workload.
@@ -34,28 +36,29 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
-# DRAM bytes (read + write) per launch measured by ncu on the jfa workload
-# (profiles/<kernel>_kernel_jfa.md). Reported only while the kernel source
-# still has the sha1 prefix recorded at capture time; otherwise null.
-NCU_TRAFFIC = {
-    ("jfa", "fwd"): ("fwd.cu", "36dc45854a7c", 943320320),
-    ("jfa", "dkdv"): ("bwd.cu", "ed2991e832fd", 1386662144),
-    ("jfa", "dq"): ("bwd.cu", "ed2991e832fd", 1402045440),
-}
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
-def ncu_traffic(workload: str, kernel: str):
+def ncu_traffic(workload: str, kernel: str, algorithmic: float):
+    """DRAM bytes (read + write) per launch from the committed ncu table, scaled
+    from the captured case to this launch by algorithmic bytes; None when no
+    row matches or the kernel source changed since the capture (sha1 prefix)."""
     import hashlib
 
-    entry = NCU_TRAFFIC.get((workload, kernel))
-    if entry is None:
+    if not os.path.exists(TRAFFIC_TABLE):
         return None
-    src, sha, nbytes = entry
-    path = os.path.join(ROOT, "jagged_attention_recsys_gdpa_gb300", "csrc", src)
-    with open(path, "rb") as f:
-        if hashlib.sha1(f.read()).hexdigest()[:12] != sha:
-            return None
-    return nbytes
+    with open(TRAFFIC_TABLE) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    for r in rows:
+        if len(r) < 6 or r[0] != workload or r[1] != kernel:
+            continue
+        src, sha, dram, alg = r[2], r[3], float(r[4]), float(r[5])
+        path = os.path.join(ROOT, "jagged_attention_recsys_gdpa_gb300", "csrc", src)
+        with open(path, "rb") as fh:
+            if hashlib.sha1(fh.read()).hexdigest()[:12] != sha:
+                return None
+        return dram * algorithmic / alg
+    return None
 
 
 def load_peaks():
@@ -179,12 +182,24 @@ def cpu_oracle_step(x_cpu, w, seqs):
     return time.perf_counter() - t0
 
 
-def workload_desc(name, w, batch):
+def workload_desc(name, w, batch, of_batch=None):
     """The workload as both arms name it in `config.workload`."""
     act = {0: "softmax", 1: "silu", 2: "gelu", 3: "gelu (degree-6 polynomial)"}[w.act]
     mask = {0: "none", 1: "causal", 3: "causal+window", 4: "block", 5: "causal+block"}[w.mask]
     qk = f", q/k rows normalised to |s| <= {w.qk_norm:g}" if w.qk_norm > 0 else ""
-    return f"{name}: B={batch}, H={w.H}, D={w.D}, {act}, mask={mask}" + (f" {w.window}" if w.mask & 6 else "") + qk
+    sub = f" (the {batch} sequences with the most allowed pairs of B={of_batch})" if of_batch else ""
+    return (f"{name}: B={batch}, H={w.H}, D={w.D}, {act}, mask={mask}" + (f" {w.window}" if w.mask & 6 else "")
+            + qk + sub)
+
+
+def subset_lengths(lens, w, k):
+    """The k sequences with the most allowed pairs (ties: lower index), in batch order."""
+    from jagged_attention_recsys_gdpa_gb300 import flops
+
+    lq, lkv = np.asarray(lens[0]), np.asarray(lens[1])
+    pairs = flops.pairs_per_sequence(lq, lkv, w.mask, w.window)
+    keep = np.sort(np.argsort(-pairs, kind="stable")[:k])
+    return lq[keep], lkv[keep]
 
 
 def run_reference(args, ws, rank):
@@ -226,11 +241,13 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="jfa")
+    ap.add_argument("--workload", default="mixed")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph of the step")
     ap.add_argument("--cpu-flops", type=float, default=1.5e11, help="effective FLOPs of the CPU-baseline sample")
     ap.add_argument("--ref-step-flops", type=float, default=2.0e10, help="effective FLOPs per reference step")
+    ap.add_argument("--subset", type=int, default=0,
+                    help="keep only the K sequences with the most allowed pairs (small cases for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = setup_dist()
@@ -242,14 +259,26 @@ def main():
 
     import jagged_attention_recsys_gdpa_gb300 as J
     from jagged_attention_recsys_gdpa_gb300 import _binding as BND
-    from jagged_attention_recsys_gdpa_gb300 import flops, inputs
+    from jagged_attention_recsys_gdpa_gb300 import flops, inputs, partition
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     BND.load()
     w = inputs.WORKLOADS[args.workload]
-    # weak scaling: every rank gets the same lengths (seed 0), its own values (seed = rank)
-    x = inputs.make(args.workload, seed=rank, device=dev, lens=inputs.lengths(args.workload, 0))
+    # Weak scaling by data parallelism: the global batch holds one draw of the
+    # workload's lengths per rank (seeds 0 .. N-1), and the split of that one
+    # jagged batch by allowed pairs (longest first onto the least-loaded rank)
+    # gives every rank about one batch of work; at N = 1 it is the batch itself.
+    draws = [inputs.lengths(args.workload, s) for s in range(ws)]
+    n_all = len(draws[0][0])
+    if args.subset > 0:
+        draws = [subset_lengths(d, w, args.subset) for d in draws]
+    g_lq = np.concatenate([d[0] for d in draws])
+    g_lkv = np.concatenate([d[1] for d in draws])
+    rank_of, rank_pairs = partition.split(inputs.offsets(g_lq), inputs.offsets(g_lkv), ws, w.mask, w.window)
+    mine = rank_of == rank
+    lens = (g_lq[mine], g_lkv[mine])
+    x = inputs.make(args.workload, seed=rank, device=dev, lens=lens)
     causal = bool(w.mask & 1)
     window = w.window if w.mask & 2 else 0
     block = w.window if w.mask & 4 else 0
@@ -258,7 +287,10 @@ def main():
     pairs = int(pairs_b.sum())
     f_fwd, f_bwd = flops.effective_flops(pairs, w.H, w.D)
     tq, tk = int(x["lq"].sum()), int(x["lkv"].sum())
-    work = flops.kernel_work(tq, tk, pairs, w.H, w.D, w.act == 0)
+    # BlockAttention with blocks that divide the tile on self-attention: the
+    # backward takes its statistics from the tile (no O or LSE read)
+    in_tile = w.act == 0 and bool(w.mask & 4) and 128 % w.window == 0 and x["kv_off"] is x["q_off"]
+    work = flops.kernel_work(tq, tk, pairs, w.H, w.D, w.act == 0, in_tile=in_tile)
     o = torch.empty_like(x["q"])
     lse = torch.empty(tq, w.H, dtype=torch.float32, device=dev) if w.act == 0 else None
     dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
@@ -334,7 +366,8 @@ def main():
     if st != 0:
         raise RuntimeError(f"device status after timing: {BND.error_string(st)}")
     fwd_ms_all = ms  # whole step
-    value = (f_fwd + f_bwd) * ws / (ms_max * 1e-3) / 1e12
+    g_fwd, g_bwd = flops.effective_flops(int(rank_pairs.sum()), w.H, w.D)  # the whole global batch
+    value = (g_fwd + g_bwd) / (ms_max * 1e-3) / 1e12
     peaks = load_peaks()
 
     # roofline of the dominant kernel
@@ -349,7 +382,7 @@ def main():
         roof = {"bound": "tensor", "achieved": wk["flops"] / t_s / 1e12, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = ncu_traffic(args.workload, dom)
+    roof["traffic"] = ncu_traffic(args.workload, dom, wk["bytes"])
     roof["traffic_unit"] = "bytes per launch (ncu dram read + write)"
     roof["algorithmic"] = wk["bytes"] if roof["bound"] == "hbm" else wk["flops"]
     roof["kernel"] = dom
@@ -436,7 +469,7 @@ def main():
     torch.cuda.synchronize()
     barrier(ws)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, ws, dev)
-    e2e_value = (f_fwd + f_bwd) * ws / (e2e_ms * 1e-3) / 1e12
+    e2e_value = (g_fwd + g_bwd) / (e2e_ms * 1e-3) / 1e12
 
     cpu_base = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -458,10 +491,12 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded lengths and values)",
             "config": {
-                "workload": workload_desc(args.workload, w, len(x["lq"])),
+                "workload": workload_desc(args.workload, w, len(x["lq"]), n_all if args.subset > 0 else None),
                 "total_q": tq, "total_kv": tk, "pairs_per_head": pairs,
                 "l2": f"inputs larger than L2 ({tq * w.H * w.D * 2 / 1e6:.0f} MB per bf16 tensor)",
-                "parallelism": f"replicas x{ws} (independent batches, no collective)",
+                "parallelism": (f"data-parallel x{ws}: one jagged batch of {len(g_lq)} sequences split by allowed "
+                                f"pairs (longest first onto the least-loaded rank), no collective" if ws > 1
+                                else "one GPU"),
                 "execution": execution,
             },
             "fwd_tflops": f_fwd / (kt["fwd"] * 1e-3) / 1e12,

@@ -90,7 +90,7 @@ enum {
 };
 
 typedef struct {
-  int64_t B;          /* number of sequences (>= 1) */
+  int64_t B;          /* number of sequences (1 .. 2^31 - 1) */
   int64_t total_q;    /* query rows = q_off[B] (>= 0) */
   int64_t total_kv;   /* key/value rows = kv_off[B] (>= 0) */
   int H;              /* heads (>= 1) */
@@ -102,8 +102,17 @@ typedef struct {
   int norm_by_lkv;    /* pointwise activations only: multiply by 1/Lkv(b) */
 } jattn_params_t;
 
+/* Precision. Products take bf16 operands with fp32 accumulation; P (and in
+ * the backward dS) are rounded to bf16 before the second products, except
+ * for pointwise activations with norm_by_lkv = 0: there every output sums
+ * up to Lkv (or Lq) unscaled terms, so P and dS enter those products as two
+ * bf16 parts, hi = bf16(x) and lo = bf16(x - hi), accumulating into the same
+ * fp32 result (twice the tensor-core work of the second products). Results
+ * then stay within |d| <= 1e-2 + 1e-2 |ref| of the exact attention at the
+ * lengths tested (20000 keys per pooling query, 8000 queries per key). */
+
 /* Bytes of workspace jattn_fwd / jattn_bwd need for these sizes (depends on
- * B, total_q, total_kv, H and act only). The workspace must be 256-byte
+ * B, total_q, total_kv, H, act and the block bit of mask only). The workspace must be 256-byte
  * aligned device memory whose first 256 bytes (the device status word) are
  * zero before its first use; jattn_get_status clears them again. Returns
  * JATTN_ERR_INVALID on bad params. */
@@ -111,7 +120,8 @@ int jattn_workspace_size(const jattn_params_t* p, size_t* bytes);
 
 /* Forward. Reads q [total_q,H,D], k and v [total_kv,H,D]; writes every row of
  * o [total_q,H,D] and, for JATTN_SOFTMAX, lse [total_q,H] (must be non-NULL
- * then; ignored otherwise). Host-side checks return JATTN_ERR_INVALID /
+ * then, except with JATTN_MASK_BLOCK, where NULL leaves LSE out; ignored for
+ * pointwise activations). Host-side checks return JATTN_ERR_INVALID /
  * JATTN_ERR_ALIGN / JATTN_ERR_WORKSPACE without launching. Device-side
  * offset errors leave o unspecified and set the status word. */
 int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
@@ -121,7 +131,21 @@ int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
 /* Backward. Inputs as for jattn_fwd plus the forward's o and lse (softmax
  * only; ignored for pointwise activations) and dout [total_q,H,D]. Writes
  * every row of dq [total_q,H,D], dk and dv [total_kv,H,D]; key rows that no
- * query sees get zero gradients. The workspace may be the forward's. */
+ * query sees get zero gradients. The workspace may be the forward's.
+ *
+ * Softmax's D_i = <dO_i, O_i> is formed, for every 128-row query tile whose
+ * allowed keys lie in one 128-row key tile, as sum_j P_ij dP_ij in fp32 from
+ * that tile (exact, without the bf16 rounding of the stored O, which matters
+ * for rows that see a few keys), and from o elsewhere.
+ *
+ * BlockAttention ("GEM Training" post, section "BlockAttention": blocks that
+ * need no online softmax correction, no logsumexp traffic and no separate
+ * D_i pass): with JATTN_MASK_BLOCK, a width that divides 128 (1, 2, 4, ...,
+ * 128), softmax and self-attention passed as ONE offsets pointer (q_off ==
+ * kv_off), every query tile meets exactly one key tile; the backward then
+ * takes the row maximum, sum and D_i from that tile, reads neither o nor
+ * lse (both may be NULL) and keeps the statistics it hands its dK/dV pass in
+ * the workspace. */
 int jattn_bwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint16_t* q,
               const uint16_t* k, const uint16_t* v, const uint16_t* o, const float* lse, const uint16_t* dout,
               uint16_t* dq, uint16_t* dk, uint16_t* dv, void* workspace, size_t workspace_bytes, void* stream);
@@ -215,6 +239,24 @@ int jattn_schedule(const jattn_params_t* p, const int64_t* q_off, const int64_t*
                    int col_tile, int transposed, int32_t* tiles, int64_t max_tiles, int32_t* n_tiles,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* Split of one jagged batch over n_ranks data-parallel ranks (host code;
+ * every pointer is a HOST pointer). Sequences are independent problems, so
+ * a batch shards by sequence with no exchange inside attention; the cost of
+ * a sequence is its number of allowed (query, key) pairs under `mask` /
+ * `window` (the jattn_params_t rules), and the split balances that cost the
+ * way the GEM training summary's "Base Batch Shuffling" takeaway balances
+ * sequence lengths (sort, then spread the heaviest first): sequences in
+ * order of decreasing cost (ties: lower index first) each go to the rank
+ * with the least cost so far (ties: lower rank). This longest-first greedy
+ * rule keeps every rank within one sequence's cost of the mean.
+ * q_off, kv_off: int64 [B+1] host prefix sums (off[0] = 0, non-decreasing).
+ * rank_of: int32 [B] out, the rank of each sequence. rank_pairs: int64
+ * [n_ranks] out, each rank's total allowed pairs per head. Returns
+ * JATTN_ERR_INVALID for B outside [1, 2^31), n_ranks < 1, a NULL pointer,
+ * an invalid mask or width, or offsets that are not prefix sums. */
+int jattn_partition(int64_t B, const int64_t* q_off, const int64_t* kv_off, int mask, int window, int n_ranks,
+                    int32_t* rank_of, int64_t* rank_pairs);
+
 /* Upper bound on the number of tiles jattn_schedule can produce. */
 int64_t jattn_max_tiles(const jattn_params_t* p, int row_tile, int transposed);
 
@@ -252,7 +294,12 @@ const char* jattn_last_error(void);
  *    jattn_last_error says how much) without launching anything.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture. The array has its own address in every CUDA
+ *    context, so the address is cached together with the id of the context
+ *    current at the call (cuCtxGetId), and a call made under another context
+ *    of the device (a runtime that owns its contexts, or the primary context
+ *    created again after cudaDeviceReset) looks it up again: make the first
+ *    call under each context before any capture on it too.
  *  - Every call reuses the same array; each call clears the status word
  *    first. Calls whose work overlaps on the GPU (other streams, other host
  *    threads) race on the array: serialise them.
@@ -262,14 +309,18 @@ int jattn_fwd_noalloc(const jattn_params_t* p, const int64_t* q_off, const int64
                       const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse, int* device_status,
                       void* stream);
 
-/* Profiling hook: `events` points to six cudaEvent_t (passed as void*) that
- * later calls record on their stream: events[0] / [1] right before / after the
- * forward kernel launch, [2] / [3] around the dK/dV kernel, [4] / [5] around
- * the dQ kernel (which jattn_bwd launches first); NULL turns it off. Used to
- * time those kernels with events on the stream they run on. */
+/* Profiling hook, per host thread: `events` points to six cudaEvent_t
+ * (passed as void*) that later calls made from the calling thread record on
+ * their stream (calls from other threads record nothing): events[0] / [1]
+ * right before / after the forward kernel launch, [2] / [3] around the dK/dV
+ * kernel, [4] / [5] around the dQ kernel (which jattn_bwd launches first);
+ * NULL turns it off. The library keeps the handles, not copies: turn the hook
+ * off before destroying the events. Used to time those kernels with events
+ * on the stream they run on. */
 void jattn_profile_events(void* const* events);
 
-/* Test hook: after this call, bounded waits in the kernels give up after
+/* Test hook, per host thread (launches made from other threads keep their
+ * own settings): after this call, bounded waits in the kernels give up after
  * `timeout_ns` nanoseconds (0 restores the default of two seconds), and
  * flag bit 0 makes the next launches skip the query-tile copy so that the
  * first wait on it runs out. Used to check that an expired wait reports

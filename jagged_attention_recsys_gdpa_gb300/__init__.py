@@ -88,7 +88,11 @@ def workspace(p: B.Params, device, need: int | None = None) -> torch.Tensor:
     key = dev.index if dev.index is not None else torch.cuda.current_device()
     ws = _ws_cache.get(key)
     if ws is None or ws.numel() < need:
-        ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+        grown = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+        if ws is not None:
+            # keep an error status that an earlier call left and nobody has read yet
+            grown[:256].copy_(ws[:256])
+        ws = grown
         _ws_cache[key] = ws
     return ws
 

@@ -26,6 +26,7 @@ EXPORTED = (
     "jattn_mxfp8_scale_rows",
     "jattn_mxfp8_quantize",
     "jattn_schedule",
+    "jattn_partition",
     "jattn_max_tiles",
     "jattn_get_status",
     "jattn_error_string",
@@ -100,6 +101,8 @@ def load(path: str | None = None):
     lib.jattn_bwd_rope_workspace_size.restype = i32
     lib.jattn_schedule.argtypes = [P, vp, vp, i32, i32, i32, vp, i64, vp, vp, ctypes.c_size_t, vp]
     lib.jattn_schedule.restype = i32
+    lib.jattn_partition.argtypes = [i64, vp, vp, i32, i32, i32, vp, vp]
+    lib.jattn_partition.restype = i32
     lib.jattn_max_tiles.argtypes = [P, i32, i32]
     lib.jattn_max_tiles.restype = i64
     lib.jattn_get_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
@@ -194,6 +197,13 @@ def schedule(p: Params, q_off, kv_off, row_tile, col_tile, transposed, tiles, ma
     check(load().jattn_schedule(ctypes.byref(p), ptr(q_off), ptr(kv_off), int(row_tile), int(col_tile),
                                 int(bool(transposed)), ptr(tiles), int(max_tiles), ptr(n_tiles), ws, ws_bytes,
                                 stream), "jattn_schedule")
+
+
+def partition(q_off, kv_off, mask: int, window: int, n_ranks: int, rank_of, rank_pairs):
+    """Host arrays (numpy): q_off, kv_off int64 [B+1]; rank_of int32 [B], rank_pairs int64 [n_ranks] out."""
+    B = len(q_off) - 1
+    check(load().jattn_partition(B, q_off.ctypes.data, kv_off.ctypes.data, int(mask), int(window), int(n_ranks),
+                                 rank_of.ctypes.data, rank_pairs.ctypes.data), "jattn_partition")
 
 
 def max_tiles(p: Params, row_tile: int, transposed: bool) -> int:

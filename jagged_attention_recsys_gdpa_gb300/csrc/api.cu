@@ -20,7 +20,9 @@ namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 thread_local char g_last_error[256] = "";
-int g_debug_flags = 0;
+// Test and profiling hooks are per host thread: a hook set on one thread
+// never changes the launches another thread makes.
+thread_local int g_debug_flags = 0;
 
 // Forward activation arrangement: the column split when sequences average at
 // most one 128-row query tile (most items then hold a single tile), else the
@@ -30,9 +32,9 @@ bool fwd_split(const jattn_params_t& p) {
   if (g_debug_flags & 4) return false;
   return p.total_q <= static_cast<int64_t>(kTile) * p.B;
 }
-uint64_t g_timeout_ns = kDefaultTimeoutNs;
+thread_local uint64_t g_timeout_ns = kDefaultTimeoutNs;
 // Optional events recorded around the main kernels: [fwd, dkdv, dq] x [begin, end].
-cudaEvent_t g_prof[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+thread_local cudaEvent_t g_prof[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
 
 void prof(int i, cudaStream_t st) {
   if (g_prof[i]) cudaEventRecord(g_prof[i], st);
@@ -51,7 +53,7 @@ int cuda_fail(const char* what, cudaError_t e) {
 void clear_stale_error() { (void)cudaGetLastError(); }
 
 struct Layout {
-  size_t status, sched_fwd, sched_q, sched_kv, di, total;
+  size_t status, sched_fwd, sched_q, sched_kv, di, lse, total;
   int64_t tiles_fwd, tiles_q, tiles_kv;
 };
 
@@ -72,13 +74,28 @@ Layout layout_for(const jattn_params_t& p) {
   off += al256(sched_ws_bytes(p.B, L.tiles_kv));
   L.di = off;
   if (p.act == JATTN_SOFTMAX) off += al256(sizeof(float) * static_cast<size_t>(p.total_q) * p.H);
+  // block masks: the LSE that a backward with in-tile statistics writes for its dK/dV pass
+  L.lse = off;
+  if (p.act == JATTN_SOFTMAX && (p.mask & JATTN_MASK_BLOCK))
+    off += al256(sizeof(float) * static_cast<size_t>(p.total_q) * p.H);
   L.total = off;
   return L;
+}
+
+// BlockAttention with blocks that divide the 128-row tile, on self-attention
+// (one offsets array for both sides, so every sequence has delta = 0): every
+// query tile then meets exactly one key tile, so the backward takes the
+// softmax statistics and Di from that tile and needs neither O nor LSE.
+bool block_in_tile(const jattn_params_t& p, const int64_t* q_off, const int64_t* kv_off) {
+  return p.act == JATTN_SOFTMAX && (p.mask & JATTN_MASK_BLOCK) && p.window >= 1 && kTile % p.window == 0 &&
+         q_off == kv_off && p.total_q == p.total_kv;
 }
 
 int check_params(const jattn_params_t* p) {
   if (!p) return JATTN_ERR_INVALID;
   if (p->B < 1 || p->total_q < 0 || p->total_kv < 0 || p->H < 1) return JATTN_ERR_INVALID;
+  // The schedule keeps sequence indices and per-sequence tile counts in 32 bits.
+  if (p->B >= (int64_t(1) << 31)) return JATTN_ERR_INVALID;
   if (p->D != 64 && p->D != 128) return JATTN_ERR_INVALID;
   if (p->act != JATTN_SOFTMAX && p->act != JATTN_SILU && p->act != JATTN_GELU_TANH && p->act != JATTN_GELU_POLY)
     return JATTN_ERR_INVALID;
@@ -176,6 +193,7 @@ AttnArgs base_args(const jattn_params_t& p, const int64_t* q_off, const int64_t*
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.norm_by_lkv = p.norm_by_lkv;
+  a.hilo = (p.act != JATTN_SOFTMAX && !p.norm_by_lkv) ? 1 : 0;
   a.status = reinterpret_cast<DevStatus*>(static_cast<char*>(ws));
   a.timeout_ns = g_timeout_ns;
   a.debug_flags = g_debug_flags;
@@ -198,24 +216,69 @@ static __device__ __align__(256) unsigned char jattn_noalloc_scratch[JATTN_NOALL
 namespace jattn {
 namespace {
 
-// Device address of the scratch array, looked up once per device (with that
-// device current). Host code may not use the symbol itself as an address.
-void* g_noalloc_addr[64] = {};
+// Device address of the scratch array. A module-scope __device__ array has
+// its own address in every CUDA context (and a new one after a context is
+// destroyed and created again), so the address is looked up with the device
+// current and cached per device together with the id of the context it
+// belongs to (cuCtxGetId: unique for the life of the process); a call from
+// another context of the same device looks it up again. Host code may not
+// use the symbol itself as an address.
+struct NoallocSlot {
+  unsigned long long ctx_id;
+  void* addr;
+};
+NoallocSlot g_noalloc[64] = {};
 std::mutex g_noalloc_mu;
+
+typedef CUresult (*PFN_ctx_get_current)(CUcontext*);
+typedef CUresult (*PFN_ctx_get_id)(CUcontext, unsigned long long*);
+PFN_ctx_get_current g_ctx_current = nullptr;
+PFN_ctx_get_id g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+// Id of the context current on this thread (device_info has made the
+// device's primary context current if there was none).
+int current_ctx_id(unsigned long long* id) {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_ctx_get_current>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_ctx_get_id>(fn);
+  });
+  if (!g_ctx_current || !g_ctx_id) {
+    snprintf(g_last_error, sizeof(g_last_error), "driver entry points cuCtxGetCurrent / cuCtxGetId not found");
+    return JATTN_ERR_CUDA;
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || g_ctx_id(ctx, id) != CUDA_SUCCESS) {
+    snprintf(g_last_error, sizeof(g_last_error), "no current CUDA context for the scratch lookup");
+    return JATTN_ERR_CUDA;
+  }
+  return JATTN_OK;
+}
 
 int noalloc_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
   if (dev < 0 || dev >= 64) return JATTN_ERR_CUDA;
+  unsigned long long id = 0;
+  const int rc = current_ctx_id(&id);
+  if (rc != JATTN_OK) return rc;
   std::lock_guard<std::mutex> g(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
+  if (!g_noalloc[dev].addr || g_noalloc[dev].ctx_id != id) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, jattn_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
-    g_noalloc_addr[dev] = ptr;
+    g_noalloc[dev].addr = ptr;
+    g_noalloc[dev].ctx_id = id;
   }
-  *out = g_noalloc_addr[dev];
+  *out = g_noalloc[dev].addr;
   return JATTN_OK;
 }
 
@@ -246,7 +309,7 @@ int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
   if (rc != JATTN_OK) return rc;
   if (!q_off || !kv_off) return JATTN_ERR_INVALID;
   if ((p->total_q > 0 && (!q || !o)) || (p->total_kv > 0 && (!k || !v))) return JATTN_ERR_INVALID;
-  if (p->act == JATTN_SOFTMAX && p->total_q > 0 && !lse) return JATTN_ERR_INVALID;
+  if (p->act == JATTN_SOFTMAX && p->total_q > 0 && !lse && !(p->mask & JATTN_MASK_BLOCK)) return JATTN_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return JATTN_ERR_ALIGN;
   if ((rc = check_ws(p, ws, ws_bytes)) != JATTN_OK) return rc;
   DeviceInfo dev;
@@ -358,12 +421,14 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
   if (!q_off || !kv_off) return JATTN_ERR_INVALID;
   if (p->total_q > 0 && (!q || !dout || !dq)) return JATTN_ERR_INVALID;
   if (p->total_kv > 0 && (!k || !v || !dk || !dv)) return JATTN_ERR_INVALID;
-  if (p->act == JATTN_SOFTMAX && p->total_q > 0 && (!o || !lse)) return JATTN_ERR_INVALID;
+  const bool in_tile = block_in_tile(*p, q_off, kv_off);
+  if (p->act == JATTN_SOFTMAX && p->total_q > 0 && !in_tile && (!o || !lse)) return JATTN_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv))
     return JATTN_ERR_ALIGN;
   if ((rc = check_ws(p, ws, ws_bytes)) != JATTN_OK) return rc;
   const Layout L = layout_for(*p);
+  if (in_tile) o = nullptr;  // neither O nor the forward's LSE is read
   if (rope_cos && ws_bytes < L.total + rope_extra_bytes(p->D, rope_rows)) return JATTN_ERR_WORKSPACE;
   DeviceInfo dev;
   if ((rc = device_info(dev)) != JATTN_OK) return rc;
@@ -390,10 +455,12 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
   if (make_map(&mq, q, p->total_q, p->H, p->D) || make_map(&mk, k, p->total_kv, p->H, p->D) ||
       make_map(&mv, v, p->total_kv, p->H, p->D) || make_map(&mdo, dout, p->total_q, p->H, p->D) ||
       make_map(&mdk, dk, p->total_kv, p->H, p->D) || make_map(&mdv, dv, p->total_kv, p->H, p->D) ||
-      (p->act == JATTN_SOFTMAX && make_map(&mo, o, p->total_q, p->H, p->D)))
+      (p->act == JATTN_SOFTMAX && !in_tile && make_map(&mo, o, p->total_q, p->H, p->D)))
     return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
-  a.f0 = const_cast<float*>(lse);
+  // in-tile statistics: the dQ pass writes LSE and Di into the workspace for the dK/dV pass
+  a.f0 = in_tile ? reinterpret_cast<float*>(base + L.lse) : const_cast<float*>(lse);
   a.f1 = di;
+  a.in_tile_stats = in_tile ? 1 : 0;
   // The dQ pass runs first: for softmax it also writes Di, which the dK/dV pass reads.
   if (p->total_q > 0) {
     const SchedView qs = sched_carve(base + L.sched_q, p->B, L.tiles_q);

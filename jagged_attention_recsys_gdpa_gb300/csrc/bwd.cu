@@ -48,9 +48,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
-// Named barrier of one activation warpgroup (ids 1 and 2).
-__device__ __forceinline__ void wg_sync(int g) { asm volatile("bar.sync %0, 128;" ::"r"(g + 1) : "memory"); }
-
 __device__ __forceinline__ float tanh_approx(float x) {
   float y;
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -197,6 +194,7 @@ struct DkdvBars {
   uint64_t s_full, dp_full, p_ready, ds_ready, acc_full, acc_empty;
   uint64_t drain;
   uint64_t grp[2];  // activation warpgroup meeting points (epilogue staging)
+  uint64_t lgrp[2]; // activation warpgroup meeting points (per-step LSE / Di publish, softmax)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -240,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->grp[0], kTile);
     mbar_init(&bars->grp[1], kTile);
+    mbar_init(&bars->lgrp[0], kTile);
+    mbar_init(&bars->lgrp[1], kTile);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -343,9 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++p_cnt;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + C::kDVCol, split_a(tmem + C::kSCol, kk),
-                   sdesc_sw128(sDO(s) + kk * 16 * 128, kTile * 128, 1024), idAcc, (kk > 0 || i > it.lo) ? 1u : 0u);
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint64_t bd = sdesc_sw128(sDO(s) + kk * 16 * 128, kTile * 128, 1024);
+            mma_ts(tmem + C::kDVCol, split_a(tmem + C::kSCol, kk), bd, idAcc, (kk > 0 || i > it.lo) ? 1u : 0u);
+            // unnormalised pointwise: P^T's lo parts, 32 columns after the hi parts
+            if (ACT != JATTN_SOFTMAX && a.hilo) mma_ts(tmem + C::kDVCol, split_a(tmem + C::kSCol + 32, kk), bd, idAcc, 1u);
+          }
           if (more) {
             if (!(ok = wait_bar(&bars->qd_full[s1], ((qd_it + 1) / C::kStages) & 1, abort_flag, a, 54))) break;
             tc_fence_after();
@@ -355,9 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++ds_cnt;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + C::kDKCol, split_a(tmem + C::kDPCol, kk),
-                   sdesc_sw128(sQ(s) + kk * 16 * 128, kTile * 128, 1024), idAcc, (kk > 0 || i > it.lo) ? 1u : 0u);
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint64_t bd = sdesc_sw128(sQ(s) + kk * 16 * 128, kTile * 128, 1024);
+            mma_ts(tmem + C::kDKCol, split_a(tmem + C::kDPCol, kk), bd, idAcc, (kk > 0 || i > it.lo) ? 1u : 0u);
+            // unnormalised pointwise: dS^T's lo parts
+            if (ACT != JATTN_SOFTMAX && a.hilo) mma_ts(tmem + C::kDKCol, split_a(tmem + C::kDPCol + 32, kk), bd, idAcc, 1u);
+          }
           mma_commit(&bars->qd_empty[s]);
           if (more) issue_dp(s1);
           if (i + 2 == it.hi) mma_commit(&bars->kv_empty);
@@ -379,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tSg = tmem + lane_base + C::kSCol + kCols * g;
     const uint32_t tDPg = tmem + lane_base + C::kDPCol + kCols * g;
-    uint32_t s_cnt = 0, acc_cnt = 0, step = 0, grp_phase = 0;
+    uint32_t s_cnt = 0, acc_cnt = 0, step = 0, grp_phase = 0, lgrp_phase = 0;
     // LSE (log2 units) and Di of query row i*128 + 64g + gt (gt < 64) of an
     // item, loaded into registers one step before they are needed.
     auto fetch = [&](const BwdItem& x, int i, float& l2, float& dd) {
@@ -424,7 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             fetch(nit, nit.lo, pf_l2, pf_dd);
             pf_item = r + 1;
           }
-          wg_sync(g);
+          // the group's 128 threads have published this step's values (bounded meeting)
+          if (!group_sync(&bars->lgrp[g], lgrp_phase, abort_flag, a, 64)) {
+            ok = false;
+            break;
+          }
         }
         ok = wait_bar(&bars->s_full, s_cnt & 1, abort_flag, a, 60);
         ok = __all_sync(0xffffffffu, ok);
@@ -451,7 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < kCols / 32; ++k) whole[k] = __all_sync(0xffffffffu, clo <= 32 * k && chi >= 32 * k + 32);
         const uint64_t c2 = f2(a.scale_log2, a.scale_log2);
         const uint64_t* nlse2 = reinterpret_cast<const uint64_t*>(lse_buf);  // (-lse, -lse) pairs
-        // P (and act' for the pointwise activations) of one 32-column chunk
+        // P (and act' for the pointwise activations) of one 32-column chunk;
+        // unnormalised pointwise: P's lo parts go to the group's other 32 S
+        // columns (already read)
         auto chunk_p = [&](int c0, uint32_t(&pk)[16], auto masked) {
           ulonglong2 nl4;  // two (-lse, -lse) pairs per 16-byte shared load
 #pragma unroll
@@ -485,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               p[c + 1] = g1;
             }
             pk[e / 2] = pack_bf16x2(f0, f1);
+            if (ACT != JATTN_SOFTMAX && a.hilo) tmem_st1(tSg + 32 + (c0 + e) / 2, bf16x2_lo(f0, f1, pk[e / 2]));
           }
         };
 #pragma unroll
@@ -496,6 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) pk[e] = 0u;
             tmem_st16(tSg + c0 / 2, pk);
+            if (ACT != JATTN_SOFTMAX && a.hilo) tmem_st16(tSg + 32 + c0 / 2, pk);
             continue;
           }
           // softmax: a second, unmasked copy for whole chunks; the longer pointwise
@@ -527,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < 16; ++e) pk[e] = 0u;
               tmem_st16(tDPg + c0 / 2, pk);
+              if (ACT != JATTN_SOFTMAX && a.hilo) tmem_st16(tDPg + 32 + c0 / 2, pk);
               continue;
             }
             ulonglong2 nd4;  // two (-Di, -Di) pairs per 16-byte shared load
@@ -539,11 +554,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t ndi2 = (e & 2) ? nd4.y : nd4.x;
                 f2_split(fmul2(f2(p[c], p[c + 1]),
                                fadd2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), ndi2)), d0, d1);
+                pk[e / 2] = pack_bf16x2(d0, d1);
               } else {
                 d0 = p[c] * __uint_as_float(dp[c]);
                 d1 = p[c + 1] * __uint_as_float(dp[c + 1]);
+                pk[e / 2] = pack_bf16x2(d0, d1);
+                // unnormalised: dS's lo parts in the group's other 32 dP columns (already read)
+                if (a.hilo) tmem_st1(tDPg + 32 + (c0 + e) / 2, bf16x2_lo(d0, d1, pk[e / 2]));
               }
-              pk[e / 2] = pack_bf16x2(d0, d1);
             }
             tmem_st16(tDPg + c0 / 2, pk);
           }
@@ -611,8 +629,9 @@ struct DqCfg {
   static constexpr int kDOOff = kTileBytes;
   static constexpr int kKOff = 2 * kTileBytes;  // stage s: K at kKOff + s * 2 tiles, V right after
   static constexpr int kBarOff = 2 * kTileBytes + kStages * 2 * kTileBytes;
-  static constexpr int kDiOff = kBarOff + 256;  // [2][128] Di handed to the activation warpgroups
-  static constexpr int kOOff = (kDiOff + 2 * kTile * 4 + 1023) / 1024 * 1024;  // O tile (softmax: Di)
+  // [2][128] Di, then [2][128] LSE, handed to the activation warpgroups (softmax)
+  static constexpr int kDiOff = kBarOff + 256;
+  static constexpr int kOOff = (kDiOff + 4 * kTile * 4 + 1023) / 1024 * 1024;  // O tile (softmax: Di)
   static constexpr int kSmemBytes = kOOff + kTileBytes;                        // base 1024-aligned (checked)
   static constexpr uint32_t kSCol = 0, kDPCol = 256, kDQCol = 384;  // S double-buffered at 0 and 128
 };
@@ -623,6 +642,7 @@ struct DqBars {
   uint64_t s_full[2], dp_full, ds_ready, acc_full, acc_empty;
   uint64_t di_full[2], di_empty[2];  // Di slots (softmax)
   uint64_t ot_full, ot_empty;         // O tile for Di (softmax)
+  uint64_t xbar[4];                   // per lane quarter: row exchange between the activation groups, 64 arrivals
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -651,7 +671,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->qd_full, 1);
     // softmax: the Di warps read dO from this buffer too, so they also release it
-    mbar_init(&bars->qd_empty, ACT == JATTN_SOFTMAX ? 1 + 64 : 1);
+    mbar_init(&bars->qd_empty, (ACT == JATTN_SOFTMAX && !a.in_tile_stats) ? 1 + 64 : 1);
+    for (int x = 0; x < 4; ++x) mbar_init(&bars->xbar[x], 64);
     mbar_init(&bars->ot_full, 1);
     mbar_init(&bars->ot_empty, 64);
     for (int s = 0; s < C::kStages; ++s) {
@@ -702,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sm + C::kDOOff + c * kTile * 128, &tmDO, &bars->qd_full, it.h * D + c * 64, yq);
           }
           q_armed = true;
-          if constexpr (ACT == JATTN_SOFTMAX) {  // O tile for the Di warps
+          if (ACT == JATTN_SOFTMAX && !a.in_tile_stats) {  // O tile for the Di warps
             if (!(ok = wait_bar(&bars->ot_empty, (item_cnt - 1) & 1 ^ 1, abort_flag, a, 72))) break;
             mbar_arrive_expect_tx(&bars->ot_full, C::kTileBytes);
             for (int c = 0; c < D / 64; ++c)
@@ -722,7 +743,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (q_armed) drain_wait(&bars->qd_full, (item_cnt - 1) & 1, a.timeout_ns);
-      if (q_armed && ACT == JATTN_SOFTMAX) drain_wait(&bars->ot_full, (item_cnt - 1) & 1, a.timeout_ns);
+      if (q_armed && ACT == JATTN_SOFTMAX && !a.in_tile_stats)
+        drain_wait(&bars->ot_full, (item_cnt - 1) & 1, a.timeout_ns);
       for (uint32_t i = (kv_it > (uint32_t)C::kStages ? kv_it - C::kStages : 0); i < kv_it; ++i)
         drain_wait(&bars->kv_full[i % C::kStages], (i / C::kStages) & 1, a.timeout_ns);
     }
@@ -784,9 +806,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++ds_cnt;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + C::kDQCol, split_a(tmem + C::kDPCol, kk),
-                   sdesc_sw128(sK(s) + kk * 16 * 128, kTile * 128, 1024), idAcc, (kk > 0 || j > it.lo) ? 1u : 0u);
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint64_t bd = sdesc_sw128(sK(s) + kk * 16 * 128, kTile * 128, 1024);
+            mma_ts(tmem + C::kDQCol, split_a(tmem + C::kDPCol, kk), bd, idAcc, (kk > 0 || j > it.lo) ? 1u : 0u);
+            // unnormalised pointwise: dS's lo parts, 32 columns after the hi parts
+            if (ACT != JATTN_SOFTMAX && a.hilo) mma_ts(tmem + C::kDQCol, split_a(tmem + C::kDPCol + 32, kk), bd, idAcc, 1u);
+          }
           mma_commit(&bars->kv_empty[s]);
           if (more) issue_dp(s1);
           if (j + 2 == it.hi) mma_commit(&bars->qd_empty);
@@ -799,12 +824,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(&bars->drain, 0, a.timeout_ns);
     }
     __syncwarp();
-  } else if (ACT == JATTN_SOFTMAX) {
+  } else if (ACT == JATTN_SOFTMAX && !a.in_tile_stats) {
     // ------------------------------------------------------------ Di warps (2, 3)
     // Di = rowsum(dO * O) for each item's 128 query rows, from the dO tile the
     // producer loaded for the MMAs and an O tile loaded for this purpose: into a
     // shared-memory slot for the activation warpgroups and to global memory for
-    // the dK/dV pass, which runs after this one. Lane l of warp 2 + w owns tile
+    // the dK/dV pass, which runs after this one. The same slot carries each
+    // row's LSE, loaded here, off the activation warps' critical path. Items
+    // with a single key tile get an exact Di from the activation warps
+    // instead (sum of P * dP over the tile), so here they only pass the LSE. Lane l of warp 2 + w owns tile
     // rows 64w + l and 64w + 32 + l. Both tiles share the 128-byte-swizzled
     // layout, so reading the same addresses pairs the same columns; walking a
     // row's 16-byte pieces in swizzled order spreads the lanes over the banks.
@@ -820,12 +848,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = ok && wait_bar(&bars->qd_full, n_item & 1, abort_flag, a, 76);
       ok = ok && wait_bar(&bars->ot_full, n_item & 1, abort_flag, a, 77);
       if (!__all_sync(0xffffffffu, ok)) break;
+      float lse_rows[2];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {  // issued before the dot products, used after them
+        const int il = it.rt * kTile + 64 * dw + 32 * h2 + lane;
+        lse_rows[h2] = (il < it.lq) ? a.f0[(it.q0 + il) * a.H + it.h] : 0.0f;
+      }
+#pragma unroll
+      const bool single = it.hi - it.lo == 1;
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         const int rl = 64 * dw + 32 * h2 + lane;
         float acc = 0.0f;
 #pragma unroll
-        for (int cb = 0; cb < D / 64; ++cb) {
+        for (int cb = 0; cb < (single ? 0 : D / 64); ++cb) {
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             const uint32_t off = cb * (kTile * 128) + rl * 128 + ((ch ^ (rl & 7)) << 4);
@@ -844,7 +880,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int il = it.rt * kTile + rl;
         di_s[slot * kTile + rl] = acc;
-        if (il < it.lq) a.f1[(it.q0 + il) * a.H + it.h] = acc;
+        di_s[(2 + slot) * kTile + rl] = lse_rows[h2];
+        if (il < it.lq && !single) a.f1[(it.q0 + il) * a.H + it.h] = acc;
       }
       mbar_arrive(&bars->di_full[slot]);
       mbar_arrive(&bars->ot_empty);
@@ -858,7 +895,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = 32 * (warp & 3) + lane;         // TMEM lane == query row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tDPg = tmem + lane_base + C::kDPCol + kCols * g;
-    uint32_t step = 0, dp_cnt = 0, acc_cnt = 0, di_item = 0;
+    const int quarter = warp & 3;
+    uint32_t step = 0, dp_cnt = 0, acc_cnt = 0, di_item = 0, x_cnt = 0;
+    // Row exchange with the partner warp of the other group (same TMEM lanes):
+    // each writes its value into column k of its own half of the current S
+    // buffer, whose scores it has already read, they meet on the quarter's
+    // mbarrier (bounded wait), and each reads the partner's column. The S
+    // buffer is not rewritten before this step's dS is handed over.
+    auto exchange = [&](float v, int k, uint32_t sbuf, bool& okx) -> float {
+      const uint32_t col = tmem + lane_base + C::kSCol + sbuf * kTile + k;
+      tmem_st1(col + kCols * g, __float_as_uint(v));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->xbar[quarter]);
+      okx = __all_sync(0xffffffffu, wait_bar(&bars->xbar[quarter], x_cnt & 1, abort_flag, a, 95));
+      ++x_cnt;
+      if (!okx) return 0.0f;
+      tc_fence_after();
+      const float r = __uint_as_float(tmem_ld1(col + kCols * (g ^ 1)));
+      tmem_ld_wait();
+      return r;
+    };
     BwdItem it, nit;
     bool have = load_bwd_item(a, 0, it), have_next = false;
     for (long long r = 0; have; ++r, it = nit, have = have_next) {
@@ -871,17 +928,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!valid) khi = klo;
       const int64_t gi = (it.q0 + il) * a.H + it.h;
       float lse2 = 0.0f, di = 0.0f;
+      const bool single = it.hi - it.lo == 1;  // softmax: Di (and with in-tile stats, LSE) from the tile
       if constexpr (ACT == JATTN_SOFTMAX) {
-        if (it.hi > it.lo) {  // items without a key tile use no Di and get no slot
-          // Di of this row from the Di warps' slot for this item
+        if (it.hi > it.lo && !a.in_tile_stats) {  // items without a key tile use no Di and get no slot
+          // Di and LSE of this row from the Di warps' slot for this item
           const int slot = di_item & 1;
           bool okd = wait_bar(&bars->di_full[slot], (di_item >> 1) & 1, abort_flag, a, 94);
           if (!__all_sync(0xffffffffu, okd)) break;
-          const float di_row = reinterpret_cast<const float*>(sm + C::kDiOff)[slot * kTile + row];
+          const float* di_s = reinterpret_cast<const float*>(sm + C::kDiOff);
+          const float di_row = di_s[slot * kTile + row];
+          const float lse_row = di_s[(2 + slot) * kTile + row];
           mbar_arrive(&bars->di_empty[slot]);
           ++di_item;
           if (valid && khi > klo) {
-            lse2 = a.f0[gi] * kLog2e;
+            lse2 = lse_row * kLog2e;
             di = di_row;
           }
         }
@@ -914,6 +974,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kCols / 32; ++k) whole[k] = __all_sync(0xffffffffu, clo <= 32 * k && chi >= 32 * k + 32);
         const uint64_t c2 = f2(a.scale_log2, a.scale_log2), nl2 = f2(-lse2, -lse2);
+        const uint32_t sbuf = step & 1;
+        float row_lse = -INFINITY;  // in-tile statistics: natural-log LSE of this row
         auto chunk_p = [&](int c0, auto masked) {
 #pragma unroll
           for (int c = c0; c < c0 + 32; c += 2) {
@@ -936,17 +998,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             p[c + 1] = v1;
           }
         };
+        if (ACT == JATTN_SOFTMAX && a.in_tile_stats) {
+          // the row's whole key range lies in this tile: its maximum and sum
+          // come from the two groups' halves, P = exp(s - m) / l exactly
+          float mx = -INFINITY;
 #pragma unroll
-        for (int c0 = 0; c0 < kCols; c0 += 32) {
-          if (skip[c0 / 32]) continue;
-          // softmax: a second, unmasked copy for whole chunks; the longer pointwise
-          // bodies keep one copy (two would crowd the instruction cache)
-          if (ACT == JATTN_SOFTMAX && whole[c0 / 32])
-            chunk_p(c0, std::integral_constant<bool, ACT != JATTN_SOFTMAX>{});
-          else
-            chunk_p(c0, std::true_type{});
+          for (int c = 0; c < kCols; ++c) {
+            const float v = (c >= clo && c < chi) ? p[c] : -INFINITY;
+            p[c] = v;
+            mx = fmaxf(mx, v);
+          }
+          mx = fmaxf(mx, exchange(mx, 0, sbuf, ok));
+          if (!ok) break;
+          const float mref = (mx == -INFINITY) ? 0.0f : mx * a.scale_log2;
+          float l = 0.0f;
+#pragma unroll
+          for (int c = 0; c < kCols; ++c) {
+            p[c] = ex2_approx(fmaf(p[c], a.scale_log2, -mref));
+            l += p[c];
+          }
+          l += exchange(l, 1, sbuf, ok);
+          if (!ok) break;
+          const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+#pragma unroll
+          for (int c = 0; c < kCols; ++c) p[c] *= inv;
+          row_lse = (l > 0.0f) ? (mref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+        } else {
+#pragma unroll
+          for (int c0 = 0; c0 < kCols; c0 += 32) {
+            if (skip[c0 / 32]) continue;
+            // softmax: a second, unmasked copy for whole chunks; the longer pointwise
+            // bodies keep one copy (two would crowd the instruction cache)
+            if (ACT == JATTN_SOFTMAX && whole[c0 / 32])
+              chunk_p(c0, std::integral_constant<bool, ACT != JATTN_SOFTMAX>{});
+            else
+              chunk_p(c0, std::true_type{});
+          }
         }
-        const uint64_t ndi2 = f2(-di, -di);
         ok = wait_bar(&bars->dp_full, dp_cnt & 1, abort_flag, a, 91);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -957,6 +1045,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kCols / 32; ++c) tmem_ld32(tDPg + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dp + c * 32));
           tmem_ld_wait();
+          if (ACT == JATTN_SOFTMAX && single) {
+            // Di = sum_j P_ij dP_ij over the row's whole key range, in fp32: exact
+            // where a Di from the stored bf16 O would carry O's rounding (rows that
+            // see a few keys, where that rounding is large next to dQ)
+            float part = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kCols / 32; ++k) {
+              if (skip[k] && !a.in_tile_stats) continue;  // chunk not computed: P is zero there
+#pragma unroll
+              for (int c = 32 * k; c < 32 * k + 32; ++c) part = fmaf(p[c], __uint_as_float(dp[c]), part);
+            }
+            di = part + exchange(part, 2, sbuf, ok);
+            if (!ok) break;
+            if (g == 0 && valid) {
+              a.f1[gi] = di;
+              if (a.in_tile_stats) a.f0[gi] = row_lse;
+            }
+          }
+          const uint64_t ndi2 = f2(-di, -di);
 #pragma unroll
           for (int c0 = 0; c0 < kCols; c0 += 32) {
             uint32_t pk[16];
@@ -964,6 +1071,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < 16; ++e) pk[e] = 0u;
               tmem_st16(tDPg + c0 / 2, pk);
+              if (ACT != JATTN_SOFTMAX && a.hilo) tmem_st16(tDPg + 32 + c0 / 2, pk);
               continue;
             }
 #pragma unroll
@@ -973,11 +1081,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if constexpr (ACT == JATTN_SOFTMAX) {
                 f2_split(fmul2(f2(p[c], p[c + 1]),
                                fadd2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), ndi2)), d0, d1);
+                pk[e / 2] = pack_bf16x2(d0, d1);
               } else {
                 d0 = p[c] * __uint_as_float(dp[c]);
                 d1 = p[c + 1] * __uint_as_float(dp[c + 1]);
+                pk[e / 2] = pack_bf16x2(d0, d1);
+                // unnormalised: dS's lo parts in the group's other 32 dP columns (already read)
+                if (a.hilo) tmem_st1(tDPg + 32 + (c0 + e) / 2, bf16x2_lo(d0, d1, pk[e / 2]));
               }
-              pk[e / 2] = pack_bf16x2(d0, d1);
             }
             tmem_st16(tDPg + c0 / 2, pk);
           }
@@ -1014,6 +1125,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (valid) {
         uint4* d = reinterpret_cast<uint4*>(dq_half);
         for (int e = 0; e < D / 16; ++e) d[e] = make_uint4(0, 0, 0, 0);
+        if (ACT == JATTN_SOFTMAX && a.in_tile_stats && g == 0) {  // a row that sees no key
+          a.f0[gi] = -INFINITY;
+          a.f1[gi] = 0.0f;
+        }
       }
     }
   }

@@ -49,7 +49,24 @@ struct AttnArgs {
   const float* rope_cos;
   const float* rope_sin;
   int rope_rows;
+  // dQ pass of softmax attention whose every item holds a single key tile
+  // (self-attention with blocks that divide the tile): the row maximum, sum
+  // and Di come from the tile itself, no O or LSE is read, and the pass writes
+  // LSE (a.f0) and Di (a.f1) for the dK/dV pass.
+  int in_tile_stats;
+  // Pointwise activations without the 1/Lkv normaliser: P and dS enter the
+  // second products as two bf16 parts (hi = bf16(x), lo = bf16(x - hi)) that
+  // accumulate into the same fp32 result, so their rounding does not grow
+  // with the sequence length (it would break the element-wise tolerance on
+  // long sequences, where outputs sum thousands of unscaled terms).
+  int hilo;
 };
+
+// The bf16 pair of what the bf16 pair `hi` of (x0, x1) leaves out.
+__device__ __forceinline__ uint32_t bf16x2_lo(float x0, float x1, uint32_t hi) {
+  const float2 hf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
+  return pack_bf16x2(x0 - hf.x, x1 - hf.y);
+}
 
 // Store 16 packed words (32 bf16 values, 64 bytes) of one output row: two
 // 32-byte stores when the output base is 32-byte aligned, else four 16-byte

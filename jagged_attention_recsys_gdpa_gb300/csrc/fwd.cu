@@ -72,6 +72,7 @@ struct FwdBars {
   uint64_t k_full[6], k_empty[6], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t drain;
+  uint64_t xbar[2][4];        // column split: row-exchange meeting per (slot, lane quarter), 64 arrivals
   uint32_t tmem_base;
   int abort_flag;
   volatile int okx[2][2][4];  // exchange slot, column half, lane quarter: partner still ok
@@ -180,6 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->o_empty[t], (SPLIT ? 2 : 1) * kTile);
     }
     mbar_init(&bars->drain, 1);
+    for (int x = 0; x < 2; ++x)
+      for (int qq = 0; qq < 4; ++qq) mbar_init(&bars->xbar[x][qq], 64);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -321,6 +324,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                        sdesc_sw128(sV + vs * C::kTileBytes + kk * 16 * 128, kTile * 128, 1024), idPV,
                        (kk > 0 || j > it.t_lo[q]) ? 1u : 0u);
               }
+              if (ACT != JATTN_SOFTMAX && a.hilo) {
+                // unnormalised pointwise: P's lo parts, 64 columns further (ping-pong)
+                // or 32 further (column split); a rolled loop keeps the issuer's
+                // registers within its share
+#pragma unroll 1
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                  mma_ts(tmem + C::kOCol + q * D,
+                         tmem + q * kTile + kk * 8 + ((SPLIT && kk >= kTile / 32) ? 32 : 0) + (SPLIT ? 32 : 64),
+                         sdesc_sw128(sV + vs * C::kTileBytes + kk * 16 * 128, kTile * 128, 1024), idPV, 1u);
+              }
               if (j + 1 == it.t_hi[q]) {
                 mma_commit(&bars->o_full[q]);
                 ++o_cnt[q];
@@ -360,16 +373,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int kOHalf = D / 2;                   // O columns of one half
       float* xch = reinterpret_cast<float*>(sm + C::kXchOff);
       uint32_t s_cnt[kNQ] = {0, 0}, o_cnt[kNQ] = {0, 0}, x_cnt = 0;
-      // Row exchange with the partner warp. Both partners always reach the named
-      // barrier and leave it with the same `okr`. Two slots, alternating: a slot is
-      // rewritten only after the partner has passed the barrier that follows its read.
+      // Row exchange with the partner warp: both write their value and ok flag,
+      // then meet on the (slot, quarter) mbarrier with a bounded wait, so a warp
+      // whose partner has aborted gives up instead of waiting for it. Two slots,
+      // alternating: a slot is rewritten only after the partner has arrived at
+      // the meeting that follows its read.
       auto exchange = [&](float v, bool& okr) -> float {
         const int slot = x_cnt & 1;
+        const uint32_t par = (x_cnt >> 1) & 1;
         ++x_cnt;
         xch[(slot * 2 + half) * kTile + row] = v;
         if (lane == 0) bars->okx[slot][half][quarter] = okr ? 1 : 0;
-        asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
-        okr = okr && (bars->okx[slot][half ^ 1][quarter] != 0);
+        mbar_arrive(&bars->xbar[slot][quarter]);
+        const bool met = __all_sync(0xffffffffu, wait_bar(&bars->xbar[slot][quarter], par, abort_flag, a, 32));
+        okr = okr && met && (bars->okx[slot][half ^ 1][quarter] != 0);
         return xch[(slot * 2 + (half ^ 1)) * kTile + row];
       };
       bool ok = true;
@@ -503,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                   for (int e = 0; e < 16; ++e) pk[e] = 0u;
                   tmem_st16(tS + c0 / 2, pk);
+                  if (a.hilo) tmem_st16(tS + 32 + c0 / 2, pk);
                   continue;
                 }
 #pragma unroll
@@ -516,6 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p1 = (c + 1 >= clo && c + 1 < chi) ? p1 : 0.0f;
                   }
                   pk[e / 2] = pack_bf16x2(p0, p1);
+                  // lo parts (unnormalised mode) in the half's other 32 columns, already read
+                  if (a.hilo) tmem_st1(tS + 32 + (c0 + e) / 2, bf16x2_lo(p0, p1, pk[e / 2]));
                 }
                 tmem_st16(tS + c0 / 2, pk);
               }
@@ -577,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < kOHalf / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
           }
           if constexpr (ACT == JATTN_SOFTMAX) {
-            if (valid && half == 0) {
+            if (valid && half == 0 && a.f0 != nullptr) {  // block masks may leave LSE out
               const float lse = (l_tot > 0.0f) ? (m_run[q] + __log2f(l_tot)) * 0.6931471805599453f : -INFINITY;
               a.f0[grow * a.H + it.h] = lse;
             }
@@ -698,6 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   p1 = (c + 1 >= clo && c + 1 < chi) ? p1 : 0.0f;
                 }
                 pk[e / 2] = pack_bf16x2(p0, p1);
+                // lo parts (unnormalised mode) in columns 64.., whose scores are in registers
+                if (a.hilo) tmem_st1(tS + 64 + (c0 + e) / 2, bf16x2_lo(p0, p1, pk[e / 2]));
               }
               tmem_st16(tS + c0 / 2, pk);
             }
@@ -741,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
         }
         if constexpr (ACT == JATTN_SOFTMAX) {
-          if (valid) {
+          if (valid && a.f0 != nullptr) {  // block masks may leave LSE out
             const float lse = (l_run > 0.0f) ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
             a.f0[grow * a.H + it.h] = lse;
           }

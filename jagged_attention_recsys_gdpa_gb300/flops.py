@@ -41,21 +41,25 @@ def effective_flops(pairs: int, H: int, D: int):
     return 4.0 * D * H * pairs, 10.0 * D * H * pairs
 
 
-def kernel_work(total_q: int, total_kv: int, pairs: int, H: int, D: int, softmax: bool):
+def kernel_work(total_q: int, total_kv: int, pairs: int, H: int, D: int, softmax: bool, in_tile: bool = False):
     """Algorithmic FLOPs and HBM bytes of each kernel (each byte read or written once).
 
     forward: reads Q, K, V, writes O (+ LSE)
     dq:      reads Q, K, V, dO (+ LSE), writes dQ; the dQ product (its score
              and dP recompute are not algorithmic work). For softmax it also
              reads O and writes Di = rowsum(dO * O), which the dK/dV pass uses.
+             With in-tile statistics (BlockAttention whose blocks divide the
+             tile) it reads neither O nor LSE and writes LSE and Di instead.
     dkdv:    reads Q, K, V, dO (+ LSE, Di), writes dK, dV; products S, dP, dV, dK
     """
     e = 2 * H * D  # bytes of one row of a [total, H, D] bf16 tensor
     stats = 4 * H * total_q
+    dq_extra = 0
+    if softmax:
+        dq_extra = 2 * stats if in_tile else e * total_q + 2 * stats
     return {
         "fwd": {"flops": 4.0 * D * H * pairs, "bytes": e * (2 * total_q + 2 * total_kv) + (stats if softmax else 0)},
         "dkdv": {"flops": 8.0 * D * H * pairs,
                  "bytes": e * (2 * total_q + 4 * total_kv) + (2 * stats if softmax else 0)},
-        "dq": {"flops": 2.0 * D * H * pairs,
-               "bytes": e * (3 * total_q + 2 * total_kv) + ((e * total_q + 2 * stats) if softmax else 0)},
+        "dq": {"flops": 2.0 * D * H * pairs, "bytes": e * (3 * total_q + 2 * total_kv) + dq_extra},
     }

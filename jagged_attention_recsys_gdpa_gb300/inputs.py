@@ -133,7 +133,8 @@ def values(shape, std: float, seed: int, device="cpu", row_norm: float = 0.0):
 def make(name_or_workload, seed: int = 0, device="cpu", lens=None, with_grad_out=True):
     """Build a full input set.
 
-    Returns dict with q_off, kv_off (int64 torch tensors on ``device``),
+    Returns dict with q_off, kv_off (int64 torch tensors on ``device``; one
+    shared tensor for self-attention with equal lengths),
     q, k, v, do (bf16 [total, H, D]) and the Workload. ``lens`` overrides the
     sampled (Lq, Lkv) lengths. Each tensor uses its own generator seeded
     from ``seed`` (q: seed, k: seed+1, v: seed+2, dO: seed+3).
@@ -148,12 +149,15 @@ def make(name_or_workload, seed: int = 0, device="cpu", lens=None, with_grad_out
     qo, ko = offsets(lq), offsets(lkv)
     tq, tk = int(qo[-1]), int(ko[-1])
     qk_row = float(np.sqrt(w.qk_norm * np.sqrt(w.D))) if w.qk_norm > 0 else 0.0
+    q_off = torch.from_numpy(qo).to(device)
+    # self-attention with equal lengths shares one offsets tensor for both sides
+    same = w.self_attn and np.array_equal(lq, lkv)
     out = {
         "workload": w,
         "lq": lq,
         "lkv": lkv,
-        "q_off": torch.from_numpy(qo).to(device),
-        "kv_off": torch.from_numpy(ko).to(device),
+        "q_off": q_off,
+        "kv_off": q_off if same else torch.from_numpy(ko).to(device),
         "q": values((tq, w.H, w.D), w.std, seed, device, qk_row),
         "k": values((tk, w.H, w.D), w.std, seed + 1, device, qk_row),
         "v": values((tk, w.H, w.D), w.std, seed + 2, device),

@@ -14,6 +14,12 @@ of ``bench.py`` use it. It shares no code with the CUDA library.
   tiles its mask allows, ordered longest-first with ties in (sequence, tile)
   order.
 * ``count_pairs`` counts allowed (query, key) pairs by visiting every pair.
+* ``partition`` is a plain-Python statement of the data-parallel split of a
+  batch over ranks: cost of a sequence = its allowed pairs (visited one by
+  one), sequences taken in order of decreasing cost (ties by index), each
+  given to the rank with the least cost so far (ties by rank) -- the
+  sort-then-balance rule of the GEM training summary's "Base Batch
+  Shuffling" takeaway applied to attention cost.
 * ``rope`` rotates jagged query or key rows by the rotary embedding (the
   RoFormer pairing (2m, 2m+1), angles from the caller's cos / sin tables),
   in double: the forward side of the rotary backward fused into the
@@ -266,3 +272,22 @@ def schedule(q_off, kv_off, *, mask=MASK_NONE, window=0, BM=128, BN=128, transpo
     cost = np.minimum(arr[:, 3] - arr[:, 2], cost_cap)
     order = np.lexsort((np.arange(len(arr)), -cost))
     return arr[order].astype(np.int32)
+
+
+def partition(q_off, kv_off, n_ranks: int, mask=MASK_NONE, window=0):
+    """(rank of each sequence, total allowed pairs of each rank) as Python lists."""
+    q_off, kv_off = _off(q_off), _off(kv_off)
+    B = len(q_off) - 1
+    cost = []
+    for b in range(B):
+        qo = np.array([0, q_off[b + 1] - q_off[b]], dtype=np.int64)
+        ko = np.array([0, kv_off[b + 1] - kv_off[b]], dtype=np.int64)
+        cost.append(count_pairs(qo, ko, mask, window))
+    order = sorted(range(B), key=lambda b: (-cost[b], b))
+    load = [0] * n_ranks
+    rank_of = [0] * B
+    for b in order:
+        r = min(range(n_ranks), key=lambda i: (load[i], i))
+        rank_of[b] = r
+        load[r] += cost[b]
+    return rank_of, load

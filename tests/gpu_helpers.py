@@ -95,6 +95,8 @@ def to_cuda(inp):
     for k in ("q_off", "kv_off", "q", "k", "v", "do"):
         if k in inp:
             out[k] = inp[k].cuda()
+    if inp.get("kv_off") is inp.get("q_off"):  # self-attention: keep one offsets tensor
+        out["kv_off"] = out["q_off"]
     return out
 
 
@@ -120,16 +122,36 @@ def subset(inp, seqs):
     return sub, rq, rk
 
 
+def backward_o(cpu, w, o_ref):
+    """The output that softmax's D_i = <dO_i, O_i> is formed from, row by row,
+    the way the backward kernels form it: a 128-row query tile whose allowed
+    keys all lie in one 128-row key tile gets D_i = sum_j P_ij dP_ij in fp32,
+    which equals D_i of the exact O; every other tile reads the stored O.
+    Returns (the stored O as bf16 for the GPU, the per-row O for the oracle)."""
+    o_st = torch.from_numpy(o_ref).to(torch.bfloat16)
+    hyb = o_st.double().numpy()
+    if w.act == 0:
+        mask = w.mask | (1 if w.mask & 2 else 0)
+        qo = cpu["q_off"].numpy()
+        for b, t, lo, hi in oracle.schedule(cpu["q_off"], cpu["kv_off"], mask=mask, window=w.window):
+            if hi - lo == 1:
+                r0 = int(qo[b]) + 128 * int(t)
+                r1 = min(r0 + 128, int(qo[b + 1]))
+                hyb[r0:r1] = o_ref[r0:r1]
+    return o_st, hyb
+
+
 def run_both_stored(cpu, w, backward=True):
     """GPU and oracle runs whose backward passes both read the same stored
     forward output: the oracle's O rounded to bf16 and its LSE in fp32, as a
-    correct forward would have stored them. This isolates the backward kernels'
-    own arithmetic from the rounding of O, which enters D_i = <dO_i, O_i>
-    (large next to dQ for rows that see one or two keys)."""
+    correct forward would have stored them (the oracle forms D_i from it where
+    the kernels do, see backward_o). This isolates the backward kernels' own
+    arithmetic from the rounding of O, which enters D_i = <dO_i, O_i> (large
+    next to dQ for rows that see one or two keys)."""
     r = oracle_run(cpu, w, backward=False)
-    o_st = torch.from_numpy(r["o"]).to(torch.bfloat16)
+    o_st, o_rows = backward_o(cpu, w, r["o"])
     lse_st = torch.from_numpy(r["lse"]).to(torch.float32)
     g = gpu_run(to_cuda(cpu), w, backward, stored=(o_st.cuda(), lse_st.cuda()))
     if backward:
-        r.update({k: x for k, x in oracle_run(cpu, w, True, o_stored=o_st).items() if k.startswith("d")})
+        r.update({k: x for k, x in oracle_run(cpu, w, True, o_stored=o_rows).items() if k.startswith("d")})
     return g, r

@@ -49,7 +49,7 @@ def test_workspace_size_and_validation(lib):
     bad = [
         dict(D=96), dict(D=0), dict(H=0), dict(B=0), dict(total_q=-1), dict(act=4), dict(mask=2), dict(mask=3),
         dict(mask=4), dict(scale=-1.0), dict(scale=float("nan")), dict(act=0, norm_by_lkv=1),
-        dict(total_q=1 << 31),
+        dict(total_q=1 << 31), dict(B=1 << 31),
         # block masks need a width and do not combine with the window bit
         dict(mask=5, window=0), dict(mask=6, window=4), dict(mask=7, window=4), dict(mask=8, window=4),
     ]

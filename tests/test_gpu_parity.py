@@ -263,16 +263,51 @@ def test_batch_without_keys_or_queries(act, lq, lkv):
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("act", [SOFTMAX, GELU])
 @pytest.mark.parametrize("mask", [BLOCK, CBLOCK])
-@pytest.mark.parametrize("W", [37, 64, 200])
+@pytest.mark.parametrize("W", [1, 16, 37, 64, 128, 200])
 def test_block_attention_self(W, mask, act, D):
     """Block masks whose edges fall inside, on and across the 128-row tiles.
-    Causal blocks hold many rows that see one or two keys, where the bf16
-    rounding of the stored O moves D_i by more than dQ's tolerance; the
-    backward is therefore checked on the oracle's stored O, the forward
-    against the oracle as everywhere."""
+    Widths that divide the tile (1, 16, 64, 128) take the BlockAttention path
+    of the backward: every query tile meets one key tile, and the softmax
+    statistics and D_i come from that tile in fp32, so GPU forward -> GPU
+    backward is compared with the exact gradient. Other widths read the
+    stored O, whose bf16 rounding moves D_i of rows that see one or two keys
+    by more than dQ's tolerance: there the backward is checked on the
+    oracle's stored O, the forward against the oracle as everywhere."""
     norm = act != SOFTMAX
     _check(_w(act, mask, W, D, norm=norm, std=1.0 if act == SOFTMAX else 0.5), SELF_LENS, SELF_LENS, seed=31,
-           stored=True)
+           stored=(128 % W != 0))
+
+
+@pytest.mark.parametrize("mask", [BLOCK, CBLOCK])
+def test_block_attention_backward_reads_no_o_or_lse(mask):
+    """The BlockAttention backward (self-attention, width dividing the tile)
+    takes its statistics from the tile: garbage in place of O and LSE, or
+    no LSE from the forward at all, leaves every gradient exact."""
+    import jagged_attention_recsys_gdpa_gb300 as J
+    from jagged_attention_recsys_gdpa_gb300 import _binding as B
+
+    w = _w(SOFTMAX, mask, 64, 128, H=3)
+    cpu = G.cpu_inputs(w, SELF_LENS, SELF_LENS, seed=37)
+    x = G.to_cuda(cpu)
+    assert x["kv_off"] is x["q_off"]
+    r = G.oracle_run(cpu, w)
+    causal = bool(mask & 1)
+    o, lse = J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], causal=causal, block=64)
+    # the forward may leave LSE out for block masks
+    p = J.make_params(x["q"], x["k"], x["q_off"], SOFTMAX, J._mask(causal, 0, 64), 64, None, False)
+    o2 = torch.empty_like(o)
+    ws = J.workspace(p, "cuda")
+    B.fwd(p, x["q_off"], x["kv_off"], x["q"], x["k"], x["v"], o2, None, ws.data_ptr(), ws.numel(),
+          torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2)
+    junk_o = torch.full_like(o, 7.0)
+    junk_lse = torch.full_like(lse, -3.0)
+    dq, dk, dv = J.backward(x["q"], x["k"], x["v"], junk_o, junk_lse, x["do"], x["q_off"], x["kv_off"],
+                            causal=causal, block=64)
+    torch.cuda.synchronize()
+    assert J.device_status() == 0
+    G.compare({"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}, r, w)
 
 
 @pytest.mark.parametrize("act", [SOFTMAX, SILU])
@@ -353,13 +388,54 @@ def test_gelu_poly_cross_and_pma():
 
 
 def test_gelu_poly_unnormalised_short():
-    """Without the 1/Lkv normaliser, dS = act'(s) <dO_i, v_j> is O(1) and its
-    bf16 rounding (before the dQ and dK products) alone accumulates to the
-    tolerance over a few hundred rows: an fp64 emulation of just that rounding
-    exceeds it on the cross-attention lengths above (dK, 7 elements) and on
-    the pooling lengths (dQ, twice the bound). Short sequences keep it at
-    about half the bound."""
+    """The polynomial GELU without the 1/Lkv normaliser on short sequences."""
     _check(_wp(NONE, 0, 128, norm=False), [100, 60, 5, 130, 1], [20, 128, 1, 64, 64], seed=42)
+
+
+UNNORM_CASES = [
+    # pooling: 32 queries over long key sequences (outputs O and dQ sum thousands of terms)
+    ([32, 32, 32, 32], [20000, 5000, 130, 1]),
+    # cross-attention: long queries over short keys (dK and dV sum thousands of terms)
+    ([8000, 3000, 129, 5], [128, 16, 100, 1]),
+]
+
+
+@pytest.mark.parametrize("case", [0, 1])
+@pytest.mark.parametrize("act", [SILU, GELU, POLY])
+def test_unnormalised_pointwise_long_sequences(act, case):
+    """Without the 1/Lkv normaliser, each output sums thousands of unscaled
+    terms act(s) v or act'(s) dP: rounding P and dS to bf16 before the second
+    products would then miss the element-wise tolerance (an fp64 emulation of
+    that one rounding misses it by 3-6x on these lengths). P and dS therefore
+    enter those products as bf16 hi + lo parts accumulating into the same fp32
+    result; every output is compared with the oracle."""
+    lq, lkv = UNNORM_CASES[case]
+    if act == POLY:
+        w = _wp(NONE, 0, 128, norm=False)
+    else:
+        w = inputs.Workload("case", 2, 128, act, NONE, 0, False, 0.5, False)
+    _check(w, lq, lkv, seed=60 + case)
+
+
+@pytest.mark.parametrize("arrangement", [FWD_SPLIT, FWD_PINGPONG])
+def test_unnormalised_forward_arrangements(arrangement):
+    """The lo parts of P sit 32 (column split) or 64 (ping-pong) TMEM columns
+    after the hi parts: both arrangements on pooling lengths."""
+    from jagged_attention_recsys_gdpa_gb300 import _binding as B
+
+    w = inputs.Workload("case", 3, 128, GELU, NONE, 0, False, 0.5, False)
+    cpu = G.cpu_inputs(w, [32, 300, 32, 7], [20000, 3000, 129, 1], seed=64)
+    B.debug_set(arrangement, 0)
+    try:
+        g = G.gpu_run(G.to_cuda(cpu), w, backward=False)
+    finally:
+        B.debug_set(0, 0)
+    G.compare(g, G.oracle_run(cpu, w, backward=False), w, backward=False)
+
+
+@pytest.mark.parametrize("act", [SILU, GELU])
+def test_unnormalised_self_attention_causal(act):
+    _check(inputs.Workload("case", 2, 64, act, CAUSAL, 0, False, 0.5, True), SELF_LENS, SELF_LENS, seed=66)
 
 
 def test_gelu_poly_scores_spread_over_the_range():

@@ -48,7 +48,9 @@ def test_rope_pass(D, lens):
 def _check_bwd_rope(act, mask, window, D, lq, lkv, seed):
     """GPU: forward on q' = R q, k' = R k (the oracle's, rounded to bf16), then
     the rotary backward. Oracle: its backward on the same q', k', then R^T on
-    dQ and dK. Softmax's backward reads the oracle's stored O on both sides."""
+    dQ and dK. Softmax's backward reads the oracle's stored O on both sides
+    (gpu_helpers.backward_o: where the kernels take D_i from the tile, the
+    oracle takes it from the exact O)."""
     import jagged_attention_recsys_gdpa_gb300 as J
 
     norm = act != SOFTMAX
@@ -60,9 +62,9 @@ def _check_bwd_rope(act, mask, window, D, lq, lkv, seed):
     rot = dict(cpu, q=rq, k=rk)
     kw = dict(H=w.H, D=D, act=act, mask=mask, window=window, norm_by_lkv=norm)
     o_ref, lse_ref = oracle.fwd(rot["q_off"], rot["kv_off"], rq, rk, rot["v"], **kw)
-    o_st = torch.from_numpy(o_ref).to(torch.bfloat16)
-    dq_r, dk_r, dv = oracle.bwd(rot["q_off"], rot["kv_off"], rq, rk, rot["v"], rot["do"], o=o_st if act == SOFTMAX else None,
-                                **kw)
+    o_st, o_rows = G.backward_o(rot, w, o_ref)
+    dq_r, dk_r, dv = oracle.bwd(rot["q_off"], rot["kv_off"], rq, rk, rot["v"], rot["do"],
+                                o=o_rows if act == SOFTMAX else None, **kw)
     ref = {"dq": oracle.rope(dq_r, cpu["q_off"], cpu["kv_off"], cos, sin, inverse=True),
            "dk": oracle.rope(dk_r, cpu["q_off"], cpu["kv_off"], cos, sin, keys=True, inverse=True), "dv": dv}
     x = G.to_cuda(rot)
