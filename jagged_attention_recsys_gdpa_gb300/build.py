@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libjattn.so")
-SOURCES = ["api.cu", "sched.cu", "fwd.cu", "fwd_block.cu", "bwd.cu", "rope.cu", "mx.cu", "partition.cpp"]
+SOURCES = ["api.cu", "sched.cu", "fwd.cu", "fwd_block.cu", "fwd_hilo.cu", "fwd_block_hilo.cu", "bwd.cu",
+           "bwd_hilo.cu", "rope.cu", "mx.cu", "partition.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "--expt-relaxed-constexpr"]
 

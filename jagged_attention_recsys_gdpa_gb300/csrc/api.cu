@@ -182,6 +182,12 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int H, int D) {
   return r == CUDA_SUCCESS ? JATTN_OK : JATTN_ERR_CUDA;
 }
 
+// Pointwise activations without the 1/Lkv normaliser: P and dS enter the
+// second products as two bf16 parts (hi = bf16(x), lo = bf16(x - hi)) that
+// accumulate into the same fp32 result, so their rounding does not grow with
+// the sequence length (outputs there sum thousands of unscaled terms).
+bool hilo_for(const jattn_params_t& p) { return p.act != JATTN_SOFTMAX && !p.norm_by_lkv; }
+
 AttnArgs base_args(const jattn_params_t& p, const int64_t* q_off, const int64_t* kv_off, void* ws) {
   AttnArgs a{};
   a.q_off = q_off;
@@ -193,7 +199,6 @@ AttnArgs base_args(const jattn_params_t& p, const int64_t* q_off, const int64_t*
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.norm_by_lkv = p.norm_by_lkv;
-  a.hilo = (p.act != JATTN_SOFTMAX && !p.norm_by_lkv) ? 1 : 0;
   a.status = reinterpret_cast<DevStatus*>(static_cast<char*>(ws));
   a.timeout_ns = g_timeout_ns;
   a.debug_flags = g_debug_flags;
@@ -336,7 +341,7 @@ int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
   a.f0 = lse;
   a.out_v8 = aligned32(o);
   prof(0, st);
-  if ((e = launch_fwd(p->D, p->act, fwd_split(*p), (p->mask & JATTN_MASK_BLOCK) != 0, mq, mk, mv, a,
+  if ((e = launch_fwd(p->D, p->act, fwd_split(*p), (p->mask & JATTN_MASK_BLOCK) != 0, hilo_for(*p), mq, mk, mv, a,
                         grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
     return cuda_fail("forward kernel launch", e);
   prof(1, st);
@@ -385,7 +390,7 @@ int jattn_fwd_noalloc(const jattn_params_t* p, const int64_t* q_off, const int64
     a.out0 = reinterpret_cast<__nv_bfloat16*>(o);
     a.f0 = lse;
     a.out_v8 = aligned32(o);
-    if ((e = launch_fwd(p->D, p->act, fwd_split(*p), (p->mask & JATTN_MASK_BLOCK) != 0, mq, mk, mv, a,
+    if ((e = launch_fwd(p->D, p->act, fwd_split(*p), (p->mask & JATTN_MASK_BLOCK) != 0, hilo_for(*p), mq, mk, mv, a,
                         grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
       return cuda_fail("forward kernel launch", e);
   }
@@ -473,7 +478,7 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
     a.out1 = nullptr;
     a.out_v8 = aligned32(dq);
     prof(4, st);
-    if ((e = launch_bwd_dq(p->D, p->act, mq, mk, mv, mdo, mo, a, grid_for(dev, L.tiles_q, p->H), st)) != cudaSuccess)
+    if ((e = launch_bwd_dq(p->D, p->act, hilo_for(*p), mq, mk, mv, mdo, mo, a, grid_for(dev, L.tiles_q, p->H), st)) != cudaSuccess)
       return cuda_fail("dQ kernel launch", e);
     prof(5, st);
   }
@@ -488,7 +493,7 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
     a.out1 = reinterpret_cast<__nv_bfloat16*>(dv);
     a.out_v8 = aligned32(dk) && aligned32(dv);
     prof(2, st);
-    if ((e = launch_bwd_dkdv(p->D, p->act, mq, mk, mv, mdo, mdk, mdv, a, grid_for(dev, L.tiles_kv, p->H), st)) !=
+    if ((e = launch_bwd_dkdv(p->D, p->act, hilo_for(*p), mq, mk, mv, mdo, mdk, mdv, a, grid_for(dev, L.tiles_kv, p->H), st)) !=
         cudaSuccess)
       return cuda_fail("dK/dV kernel launch", e);
     prof(3, st);

@@ -28,6 +28,14 @@
 #include "common.cuh"
 #include "kernels.h"
 
+// Compiled twice: on its own, and through bwd_hilo.cu with JATTN_HILO = 1 for
+// pointwise activations without the 1/Lkv normaliser, whose P and dS enter the
+// second products as bf16 hi + lo parts (kept out of the other kernels, where
+// even untaken branches for them cost code quality in the activation loops).
+#ifndef JATTN_HILO
+#define JATTN_HILO 0
+#endif
+
 namespace jattn {
 
 namespace {
@@ -209,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                 const AttnArgs a) {
   using C = DkdvCfg<D>;
+  constexpr bool kHilo = JATTN_HILO && ACT != JATTN_SOFTMAX;  // P and dS as bf16 hi + lo parts
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned tiles and no slack for realigning: a misaligned base is an error
   if (smem_u32(smem_raw) & 1023u) {
@@ -347,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = sdesc_sw128(sDO(s) + kk * 16 * 128, kTile * 128, 1024);
             mma_ts(tmem + C::kDVCol, split_a(tmem + C::kSCol, kk), bd, idAcc, (kk > 0 || i > it.lo) ? 1u : 0u);
             // unnormalised pointwise: P^T's lo parts, 32 columns after the hi parts
-            if (ACT != JATTN_SOFTMAX && a.hilo) mma_ts(tmem + C::kDVCol, split_a(tmem + C::kSCol + 32, kk), bd, idAcc, 1u);
+            if constexpr (kHilo) mma_ts(tmem + C::kDVCol, split_a(tmem + C::kSCol + 32, kk), bd, idAcc, 1u);
           }
           if (more) {
             if (!(ok = wait_bar(&bars->qd_full[s1], ((qd_it + 1) / C::kStages) & 1, abort_flag, a, 54))) break;
@@ -362,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = sdesc_sw128(sQ(s) + kk * 16 * 128, kTile * 128, 1024);
             mma_ts(tmem + C::kDKCol, split_a(tmem + C::kDPCol, kk), bd, idAcc, (kk > 0 || i > it.lo) ? 1u : 0u);
             // unnormalised pointwise: dS^T's lo parts
-            if (ACT != JATTN_SOFTMAX && a.hilo) mma_ts(tmem + C::kDKCol, split_a(tmem + C::kDPCol + 32, kk), bd, idAcc, 1u);
+            if constexpr (kHilo) mma_ts(tmem + C::kDKCol, split_a(tmem + C::kDPCol + 32, kk), bd, idAcc, 1u);
           }
           mma_commit(&bars->qd_empty[s]);
           if (more) issue_dp(s1);
@@ -497,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               p[c + 1] = g1;
             }
             pk[e / 2] = pack_bf16x2(f0, f1);
-            if (ACT != JATTN_SOFTMAX && a.hilo) tmem_st1(tSg + 32 + (c0 + e) / 2, bf16x2_lo(f0, f1, pk[e / 2]));
+            if constexpr (kHilo) tmem_st1(tSg + 32 + (c0 + e) / 2, bf16x2_lo(f0, f1, pk[e / 2]));
           }
         };
 #pragma unroll
@@ -509,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) pk[e] = 0u;
             tmem_st16(tSg + c0 / 2, pk);
-            if (ACT != JATTN_SOFTMAX && a.hilo) tmem_st16(tSg + 32 + c0 / 2, pk);
+            if constexpr (kHilo) tmem_st16(tSg + 32 + c0 / 2, pk);
             continue;
           }
           // softmax: a second, unmasked copy for whole chunks; the longer pointwise
@@ -541,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < 16; ++e) pk[e] = 0u;
               tmem_st16(tDPg + c0 / 2, pk);
-              if (ACT != JATTN_SOFTMAX && a.hilo) tmem_st16(tDPg + 32 + c0 / 2, pk);
+              if constexpr (kHilo) tmem_st16(tDPg + 32 + c0 / 2, pk);
               continue;
             }
             ulonglong2 nd4;  // two (-Di, -Di) pairs per 16-byte shared load
@@ -560,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 d1 = p[c + 1] * __uint_as_float(dp[c + 1]);
                 pk[e / 2] = pack_bf16x2(d0, d1);
                 // unnormalised: dS's lo parts in the group's other 32 dP columns (already read)
-                if (a.hilo) tmem_st1(tDPg + 32 + (c0 + e) / 2, bf16x2_lo(d0, d1, pk[e / 2]));
+                if constexpr (kHilo) tmem_st1(tDPg + 32 + (c0 + e) / 2, bf16x2_lo(d0, d1, pk[e / 2]));
               }
             }
             tmem_st16(tDPg + c0 / 2, pk);
@@ -657,6 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
               const __grid_constant__ CUtensorMap tmO, const AttnArgs a) {
   using C = DqCfg<D>;
+  constexpr bool kHilo = JATTN_HILO && ACT != JATTN_SOFTMAX;  // dS as bf16 hi + lo parts
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned tiles and no slack for realigning: a misaligned base is an error
   if (smem_u32(smem_raw) & 1023u) {
@@ -810,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = sdesc_sw128(sK(s) + kk * 16 * 128, kTile * 128, 1024);
             mma_ts(tmem + C::kDQCol, split_a(tmem + C::kDPCol, kk), bd, idAcc, (kk > 0 || j > it.lo) ? 1u : 0u);
             // unnormalised pointwise: dS's lo parts, 32 columns after the hi parts
-            if (ACT != JATTN_SOFTMAX && a.hilo) mma_ts(tmem + C::kDQCol, split_a(tmem + C::kDPCol + 32, kk), bd, idAcc, 1u);
+            if constexpr (kHilo) mma_ts(tmem + C::kDQCol, split_a(tmem + C::kDPCol + 32, kk), bd, idAcc, 1u);
           }
           mma_commit(&bars->kv_empty[s]);
           if (more) issue_dp(s1);
@@ -1071,7 +1081,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < 16; ++e) pk[e] = 0u;
               tmem_st16(tDPg + c0 / 2, pk);
-              if (ACT != JATTN_SOFTMAX && a.hilo) tmem_st16(tDPg + 32 + c0 / 2, pk);
+              if constexpr (kHilo) tmem_st16(tDPg + 32 + c0 / 2, pk);
               continue;
             }
 #pragma unroll
@@ -1087,7 +1097,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 d1 = p[c + 1] * __uint_as_float(dp[c + 1]);
                 pk[e / 2] = pack_bf16x2(d0, d1);
                 // unnormalised: dS's lo parts in the group's other 32 dP columns (already read)
-                if (a.hilo) tmem_st1(tDPg + 32 + (c0 + e) / 2, bf16x2_lo(d0, d1, pk[e / 2]));
+                if constexpr (kHilo) tmem_st1(tDPg + 32 + (c0 + e) / 2, bf16x2_lo(d0, d1, pk[e / 2]));
               }
             }
             tmem_st16(tDPg + c0 / 2, pk);
@@ -1159,40 +1169,63 @@ cudaError_t launch6(K kern, int smem, const CUtensorMap& q, const CUtensorMap& k
 
 }  // namespace
 
-cudaError_t launch_bwd_dkdv(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1, const AttnArgs& a,
-                            int grid, cudaStream_t stream) {
+#if JATTN_HILO
+cudaError_t launch_bwd_dkdv_hilo(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                 const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1,
+                                 const AttnArgs& a, int grid, cudaStream_t stream) {
+#else
+cudaError_t launch_bwd_dkdv(int D, int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k,
+                            const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1,
+                            const AttnArgs& a, int grid, cudaStream_t stream) {
+  if (hilo && act != JATTN_SOFTMAX) return launch_bwd_dkdv_hilo(D, act, q, k, v, dout, o0, o1, a, grid, stream);
+  if (act == JATTN_SOFTMAX)
+    return D == 128 ? launch6(dkdv_kernel<128, JATTN_SOFTMAX>, DkdvCfg<128>::kSmemBytes, q, k, v, dout, o0, o1, a,
+                              grid, stream)
+                    : launch6(dkdv_kernel<64, JATTN_SOFTMAX>, DkdvCfg<64>::kSmemBytes, q, k, v, dout, o0, o1, a, grid,
+                              stream);
+#endif
   if (D == 128) {
     constexpr int sm = DkdvCfg<128>::kSmemBytes;
-    if (act == JATTN_SOFTMAX) return launch6(dkdv_kernel<128, JATTN_SOFTMAX>, sm, q, k, v, dout, o0, o1, a, grid, stream);
     if (act == JATTN_SILU) return launch6(dkdv_kernel<128, JATTN_SILU>, sm, q, k, v, dout, o0, o1, a, grid, stream);
     if (act == JATTN_GELU_POLY)
       return launch6(dkdv_kernel<128, JATTN_GELU_POLY>, sm, q, k, v, dout, o0, o1, a, grid, stream);
-    return launch6(dkdv_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+    if (act == JATTN_GELU_TANH)
+      return launch6(dkdv_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+    return cudaErrorInvalidValue;
   }
   constexpr int sm = DkdvCfg<64>::kSmemBytes;
-  if (act == JATTN_SOFTMAX) return launch6(dkdv_kernel<64, JATTN_SOFTMAX>, sm, q, k, v, dout, o0, o1, a, grid, stream);
   if (act == JATTN_SILU) return launch6(dkdv_kernel<64, JATTN_SILU>, sm, q, k, v, dout, o0, o1, a, grid, stream);
   if (act == JATTN_GELU_POLY) return launch6(dkdv_kernel<64, JATTN_GELU_POLY>, sm, q, k, v, dout, o0, o1, a, grid, stream);
-  return launch6(dkdv_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+  if (act == JATTN_GELU_TANH) return launch6(dkdv_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+  return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_bwd_dq(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+#if JATTN_HILO
+cudaError_t launch_bwd_dq_hilo(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a, int grid,
+                               cudaStream_t stream) {
+#else
+cudaError_t launch_bwd_dq(int D, int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a, int grid,
                           cudaStream_t stream) {
+  if (hilo && act != JATTN_SOFTMAX) return launch_bwd_dq_hilo(D, act, q, k, v, dout, o, a, grid, stream);
+  // the O tile for Di is only needed (and its shared memory only taken) for softmax
+  if (act == JATTN_SOFTMAX)
+    return D == 128 ? launch5(dq_kernel<128, JATTN_SOFTMAX>, DqCfg<128>::kSmemBytes, q, k, v, dout, o, a, grid, stream)
+                    : launch5(dq_kernel<64, JATTN_SOFTMAX>, DqCfg<64>::kSmemBytes, q, k, v, dout, o, a, grid, stream);
+#endif
   if (D == 128) {
-    // the O tile for Di is only needed (and its shared memory only taken) for softmax
-    const int sm = act == JATTN_SOFTMAX ? DqCfg<128>::kSmemBytes : DqCfg<128>::kOOff;
-    if (act == JATTN_SOFTMAX) return launch5(dq_kernel<128, JATTN_SOFTMAX>, sm, q, k, v, dout, o, a, grid, stream);
+    constexpr int sm = DqCfg<128>::kOOff;
     if (act == JATTN_SILU) return launch5(dq_kernel<128, JATTN_SILU>, sm, q, k, v, dout, o, a, grid, stream);
     if (act == JATTN_GELU_POLY) return launch5(dq_kernel<128, JATTN_GELU_POLY>, sm, q, k, v, dout, o, a, grid, stream);
-    return launch5(dq_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, o, a, grid, stream);
+    if (act == JATTN_GELU_TANH) return launch5(dq_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, o, a, grid, stream);
+    return cudaErrorInvalidValue;
   }
-  const int sm = act == JATTN_SOFTMAX ? DqCfg<64>::kSmemBytes : DqCfg<64>::kOOff;
-  if (act == JATTN_SOFTMAX) return launch5(dq_kernel<64, JATTN_SOFTMAX>, sm, q, k, v, dout, o, a, grid, stream);
+  constexpr int sm = DqCfg<64>::kOOff;
   if (act == JATTN_SILU) return launch5(dq_kernel<64, JATTN_SILU>, sm, q, k, v, dout, o, a, grid, stream);
   if (act == JATTN_GELU_POLY) return launch5(dq_kernel<64, JATTN_GELU_POLY>, sm, q, k, v, dout, o, a, grid, stream);
-  return launch5(dq_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, o, a, grid, stream);
+  if (act == JATTN_GELU_TANH) return launch5(dq_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, o, a, grid, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace jattn

@@ -54,12 +54,6 @@ struct AttnArgs {
   // and Di come from the tile itself, no O or LSE is read, and the pass writes
   // LSE (a.f0) and Di (a.f1) for the dK/dV pass.
   int in_tile_stats;
-  // Pointwise activations without the 1/Lkv normaliser: P and dS enter the
-  // second products as two bf16 parts (hi = bf16(x), lo = bf16(x - hi)) that
-  // accumulate into the same fp32 result, so their rounding does not grow
-  // with the sequence length (it would break the element-wise tolerance on
-  // long sequences, where outputs sum thousands of unscaled terms).
-  int hilo;
 };
 
 // The bf16 pair of what the bf16 pair `hi` of (x0, x1) leaves out.

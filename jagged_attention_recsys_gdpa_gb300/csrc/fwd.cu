@@ -32,12 +32,19 @@
 #include "common.cuh"
 #include "kernels.h"
 
-// This file is compiled twice: on its own for masks without the block bit,
-// where the block-mask arithmetic folds away at compile time (left in, it
-// cost the window-256 forward about 4%), and through fwd_block.cu with
-// JATTN_FWD_BLOCK = 1 for block masks.
+// This file is compiled four times: on its own for masks without the block
+// bit, where the block-mask arithmetic folds away at compile time (left in, it
+// cost the window-256 forward about 4%), through fwd_block.cu with
+// JATTN_FWD_BLOCK = 1 for block masks, and through fwd_hilo.cu /
+// fwd_block_hilo.cu with JATTN_HILO = 1 for pointwise activations without the
+// 1/Lkv normaliser, whose P enters the PV product as bf16 hi + lo parts (the
+// extra stores, even as branches not taken, slowed the normalised pooling
+// forward by a quarter).
 #ifndef JATTN_FWD_BLOCK
 #define JATTN_FWD_BLOCK 0
+#endif
+#ifndef JATTN_HILO
+#define JATTN_HILO 0
 #endif
 
 namespace jattn {
@@ -151,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
   using C = FwdCfg<D>;
+  constexpr bool kHilo = JATTN_HILO && ACT != JATTN_SOFTMAX;  // P as bf16 hi + lo parts
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // The tiles need 1024-byte alignment and the layout leaves no slack for
   // realigning, so a misaligned dynamic shared memory base is an error.
@@ -228,7 +236,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++v_it;
         return true;
       };
-      for (long long r = 0; ok && load_item(a, r, it); ++r) {
+      // the next item's descriptor is loaded while this one is served (its
+      // global loads would otherwise stall every item start)
+      ItemInfo nit;
+      bool have = load_item(a, 0, it), have_next = false;
+      for (long long r = 0; ok && have; ++r, it = nit, have = have_next) {
+        have_next = load_item(a, r + 1, nit);
         if (it.hi <= it.lo) continue;
         if (!(ok = wait_bar(&bars->q_empty, (q_it & 1) ^ 1, abort_flag, a, 10))) break;
         if (!(a.debug_flags & 1)) {
@@ -287,7 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&bars->s_full[q]);
       };
-      for (long long r = 0; ok && load_item(a, r, it); ++r) {
+      ItemInfo nit;
+      bool have = load_item(a, 0, it), have_next = false;
+      for (long long r = 0; ok && have; ++r, it = nit, have = have_next) {
+        have_next = load_item(a, r + 1, nit);
         if (it.hi <= it.lo) continue;
         if (!(ok = wait_bar(&bars->q_full, q_it & 1, abort_flag, a, 20))) break;
         ++q_it;
@@ -324,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        sdesc_sw128(sV + vs * C::kTileBytes + kk * 16 * 128, kTile * 128, 1024), idPV,
                        (kk > 0 || j > it.t_lo[q]) ? 1u : 0u);
               }
-              if (ACT != JATTN_SOFTMAX && a.hilo) {
+              if constexpr (kHilo) {
                 // unnormalised pointwise: P's lo parts, 64 columns further (ping-pong)
                 // or 32 further (column split); a rolled loop keeps the issuer's
                 // registers within its share
@@ -520,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                   for (int e = 0; e < 16; ++e) pk[e] = 0u;
                   tmem_st16(tS + c0 / 2, pk);
-                  if (a.hilo) tmem_st16(tS + 32 + c0 / 2, pk);
+                  if constexpr (kHilo) tmem_st16(tS + 32 + c0 / 2, pk);
                   continue;
                 }
 #pragma unroll
@@ -535,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   }
                   pk[e / 2] = pack_bf16x2(p0, p1);
                   // lo parts (unnormalised mode) in the half's other 32 columns, already read
-                  if (a.hilo) tmem_st1(tS + 32 + (c0 + e) / 2, bf16x2_lo(p0, p1, pk[e / 2]));
+                  if constexpr (kHilo) tmem_st1(tS + 32 + (c0 + e) / 2, bf16x2_lo(p0, p1, pk[e / 2]));
                 }
                 tmem_st16(tS + c0 / 2, pk);
               }
@@ -719,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 pk[e / 2] = pack_bf16x2(p0, p1);
                 // lo parts (unnormalised mode) in columns 64.., whose scores are in registers
-                if (a.hilo) tmem_st1(tS + 64 + (c0 + e) / 2, bf16x2_lo(p0, p1, pk[e / 2]));
+                if constexpr (kHilo) tmem_st1(tS + 64 + (c0 + e) / 2, bf16x2_lo(p0, p1, pk[e / 2]));
               }
               tmem_st16(tS + c0 / 2, pk);
             }
@@ -796,27 +812,40 @@ static cudaError_t launch_fwd_s(bool split, const CUtensorMap& q, const CUtensor
                : launch_fwd_t<D, ACT, false>(q, k, v, a, grid, stream);
 }
 
-#if JATTN_FWD_BLOCK
+#if JATTN_FWD_BLOCK && JATTN_HILO
+cudaError_t launch_fwd_block_hilo(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
+                                  const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream) {
+#elif JATTN_FWD_BLOCK
 cudaError_t launch_fwd_block(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
                              const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream) {
+#elif JATTN_HILO
+cudaError_t launch_fwd_hilo(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
+                            const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream) {
 #else
-cudaError_t launch_fwd(int D, int act, bool split, bool block, const CUtensorMap& q, const CUtensorMap& k,
+cudaError_t launch_fwd(int D, int act, bool split, bool block, bool hilo, const CUtensorMap& q, const CUtensorMap& k,
                        const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream) {
+  if (hilo && act != JATTN_SOFTMAX)
+    return block ? launch_fwd_block_hilo(D, act, split, q, k, v, a, grid, stream)
+                 : launch_fwd_hilo(D, act, split, q, k, v, a, grid, stream);
   if (block) return launch_fwd_block(D, act, split, q, k, v, a, grid, stream);
 #endif
+#if !JATTN_HILO
+  if (D == 128 && act == JATTN_SOFTMAX) return launch_fwd_s<128, JATTN_SOFTMAX>(split, q, k, v, a, grid, stream);
+  if (D == 64 && act == JATTN_SOFTMAX) return launch_fwd_s<64, JATTN_SOFTMAX>(split, q, k, v, a, grid, stream);
+#endif
   if (D == 128) {
-    if (act == JATTN_SOFTMAX) return launch_fwd_s<128, JATTN_SOFTMAX>(split, q, k, v, a, grid, stream);
     if (act == JATTN_SILU) return launch_fwd_s<128, JATTN_SILU>(split, q, k, v, a, grid, stream);
     if (act == JATTN_GELU_POLY) return launch_fwd_s<128, JATTN_GELU_POLY>(split, q, k, v, a, grid, stream);
-    return launch_fwd_s<128, JATTN_GELU_TANH>(split, q, k, v, a, grid, stream);
+    if (act == JATTN_GELU_TANH) return launch_fwd_s<128, JATTN_GELU_TANH>(split, q, k, v, a, grid, stream);
+    return cudaErrorInvalidValue;
   }
-  if (act == JATTN_SOFTMAX) return launch_fwd_s<64, JATTN_SOFTMAX>(split, q, k, v, a, grid, stream);
   if (act == JATTN_SILU) return launch_fwd_s<64, JATTN_SILU>(split, q, k, v, a, grid, stream);
   if (act == JATTN_GELU_POLY) return launch_fwd_s<64, JATTN_GELU_POLY>(split, q, k, v, a, grid, stream);
-  return launch_fwd_s<64, JATTN_GELU_TANH>(split, q, k, v, a, grid, stream);
+  if (act == JATTN_GELU_TANH) return launch_fwd_s<64, JATTN_GELU_TANH>(split, q, k, v, a, grid, stream);
+  return cudaErrorInvalidValue;
 }
 
-#if !JATTN_FWD_BLOCK
+#if !JATTN_FWD_BLOCK && !JATTN_HILO
 int fwd_rows_per_item() { return kNQ * kTile; }
 #endif
 

@@ -13,24 +13,36 @@ struct DevStatus;
 // Forward: schedule rows are blocks of fwd_rows_per_item() query rows. `split`
 // selects the column-split arrangement of the activation warps (for items that
 // mostly hold one query tile) over the ping-pong one; `block` selects the
-// kernels compiled for block masks (launch_fwd_block, fwd_block.cu).
-cudaError_t launch_fwd(int D, int act, bool split, bool block, const CUtensorMap& q, const CUtensorMap& k,
+// kernels compiled for block masks (fwd_block.cu) and `hilo` those that pass P
+// as bf16 hi + lo parts (pointwise activations without the 1/Lkv normaliser,
+// fwd_hilo.cu, fwd_block_hilo.cu).
+cudaError_t launch_fwd(int D, int act, bool split, bool block, bool hilo, const CUtensorMap& q, const CUtensorMap& k,
                        const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream);
 cudaError_t launch_fwd_block(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
                              const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_hilo(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
+                            const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_block_hilo(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
+                                  const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream);
 int fwd_rows_per_item();
 
 // dK, dV over key tiles (transposed schedule, 128-row key tiles). o0 / o1 map
 // dK / dV (tile stores of whole tiles).
-cudaError_t launch_bwd_dkdv(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1, const AttnArgs& a,
-                            int grid, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(int D, int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k,
+                            const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1,
+                            const AttnArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv_hilo(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                 const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1,
+                                 const AttnArgs& a, int grid, cudaStream_t stream);
 // dQ over query tiles (128-row query tiles). For softmax it also computes
 // Di = rowsum(dO * O) from the dO tiles and O tiles (map `o`) into a.f1, so
 // it runs before the dK/dV pass, which reads Di.
-cudaError_t launch_bwd_dq(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_bwd_dq(int D, int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a, int grid,
                           cudaStream_t stream);
+cudaError_t launch_bwd_dq_hilo(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a, int grid,
+                               cudaStream_t stream);
 
 // Rotary embedding of a jagged tensor x ([total, H, D] bf16, rows described
 // by own_off; other_off describes the other side for the alignment):
