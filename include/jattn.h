@@ -226,6 +226,33 @@ int jattn_mxfp8_quantize(int64_t B, int64_t total, int H, int D, const int64_t* 
                          uint8_t* codes, uint8_t* scales, int32_t* block_start, void* workspace,
                          size_t workspace_bytes, void* stream);
 
+/* MXFP8 attention forward ("GEM Training" post, section "Low Precision Flash
+ * Attention": FlashAttention on block-scaled FP8 operands, scale factors held
+ * in tensor memory beside the accumulators, and the softmax output quantized
+ * to FP8 inside the softmax with the scale its row maximum fixes).
+ *
+ * Softmax attention (p->act = JATTN_SOFTMAX, p->D = 128, norm_by_lkv = 0, any
+ * mask of jattn_fwd) whose Q, K and V arrive as jattn_mxfp8_quantize output:
+ * E4M3 codes [total, H, 128] (16-byte aligned) with E8M0 scales [row blocks,
+ * H, 4] (4-byte aligned) and the row-block starts (int32 [B+1]) of their
+ * offsets; K and V share kv_block_start (quantized with the same offsets).
+ * Both products run as block-scaled tensor-core MMAs on the exact values the
+ * codes and scales stand for, accumulating in fp32. P is quantized per key
+ * tile against the running row maximum m, which the kernel moves whenever it
+ * grows, so P = exp(s - m) <= 1 and its scale is 2^-8 (E4M3's largest power
+ * of two is 2^8): P~ = E4M3(256 P) / 256. The row sum l and LSE use the
+ * unquantized P in fp32; o = (sum_j P~_ij v_j) / l (bf16), lse as jattn_fwd.
+ * Against the same definition with the exact final maximum, each P~ differs
+ * by at most one E4M3 rounding step (2^-3 P relative, 2^-17 absolute below
+ * E4M3's normal range), so |o - o_ref| <= sum_j (2^-3 p_ij + 2^-17 / l_i)
+ * |v_j| plus bf16 rounding of o. The workspace is jattn_fwd's (it uses the
+ * 128-row query-tile schedule). Return codes as jattn_fwd, plus
+ * JATTN_ERR_INVALID for another activation, D != 128 or norm_by_lkv. */
+int jattn_fwd_mxfp8(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint8_t* q,
+                    const uint8_t* q_scales, const int32_t* q_block_start, const uint8_t* k, const uint8_t* k_scales,
+                    const uint8_t* v, const uint8_t* v_scales, const int32_t* kv_block_start, uint16_t* o, float* lse,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* Longest-first tile schedule ("GEM Training" post, GDPA section: valid tiles
  * are precomputed, empty ones skipped, and the rest spread over the SMs so
  * no SM gets a much longer share). Builds the schedule the kernels use into

@@ -12,7 +12,8 @@ the computation runs in its CUDA kernels):
   ``attention(..., rope=(cos, sin))`` rotate dQ and dK back inside the
   backward kernels' epilogues.
 * ``mxfp8_quantize(x, off)``: FP8 E4M3 codes plus one E8M0 scale per 32 x 32
-  block of a jagged tensor.
+  block of a jagged tensor; ``forward_mxfp8(qm, km, vm, q_off, kv_off, ...)``:
+  the softmax forward on such operands (block-scaled FP8 tensor-core products).
 * ``schedule(...)``: the device-built longest-first tile list.
 
 Activations (``act``): "softmax", "silu", "gelu" (tanh form) or "gelu_poly"
@@ -163,6 +164,22 @@ def mxfp8_quantize(x, off):
     B.mxfp8_quantize(nb, total, H, D, off, x, codes, scales, block_start, ws.data_ptr(), ws.numel(),
                      _stream(x.device))
     return codes, scales, block_start
+
+
+def forward_mxfp8(qm, km, vm, q_off, kv_off, causal=False, window=0, block=0, scale=None, out=None, lse=None):
+    """Softmax attention forward on MXFP8 operands: qm, km, vm are the
+    (codes, scales, block_start) triples mxfp8_quantize returns (km and vm
+    quantized with kv_off). D must be 128. Returns (O bf16, LSE fp32)."""
+    (qc, qs, qbs), (kc, ks, kbs), (vc, vs, _) = qm, km, vm
+    total_q, H, D = qc.shape
+    p = B.params(q_off.numel() - 1, total_q, kc.shape[0], H, D, SOFTMAX, _mask(causal, window, block),
+                 _width(window, block), scale, False)
+    o = out if out is not None else torch.empty((total_q, H, D), dtype=torch.bfloat16, device=qc.device)
+    lse = lse if lse is not None else torch.empty((total_q, H), dtype=torch.float32, device=qc.device)
+    ws = workspace(p, qc.device)
+    B.fwd_mxfp8(p, q_off, kv_off, qc, qs, qbs, kc, ks, vc, vs, kbs, o, lse, ws.data_ptr(), ws.numel(),
+                _stream(qc.device))
+    return o, lse
 
 
 def backward(q, k, v, o, lse, do, q_off, kv_off, act="softmax", causal=False, window=0, scale=None,

@@ -188,6 +188,21 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int H, int D) {
 // the sequence length (outputs there sum thousands of unscaled terms).
 bool hilo_for(const jattn_params_t& p) { return p.act != JATTN_SOFTMAX && !p.norm_by_lkv; }
 
+// 2-D view [rows, H*D] of jagged E4M3 codes (one byte each); boxes of 128
+// rows x 128 bytes with the 128-byte swizzle (D = 128: one box per head row).
+int make_map_u8(CUtensorMap* m, const void* ptr, int64_t rows, int H, int D) {
+  std::memset(m, 0, sizeof(*m));
+  if (rows == 0) return JATTN_OK;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * D, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * D};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? JATTN_OK : JATTN_ERR_CUDA;
+}
+
 AttnArgs base_args(const jattn_params_t& p, const int64_t* q_off, const int64_t* kv_off, void* ws) {
   AttnArgs a{};
   a.q_off = q_off;
@@ -397,6 +412,54 @@ int jattn_fwd_noalloc(const jattn_params_t* p, const int64_t* q_off, const int64
   if (device_status &&
       (e = cudaMemcpyAsync(device_status, scratch, sizeof(int), cudaMemcpyDeviceToDevice, st)) != cudaSuccess)
     return cuda_fail("status copy", e);
+  return JATTN_OK;
+}
+
+int jattn_fwd_mxfp8(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint8_t* q,
+                    const uint8_t* q_scales, const int32_t* q_block_start, const uint8_t* k, const uint8_t* k_scales,
+                    const uint8_t* v, const uint8_t* v_scales, const int32_t* kv_block_start, uint16_t* o, float* lse,
+                    void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_params(p);
+  if (rc != JATTN_OK) return rc;
+  if (p->act != JATTN_SOFTMAX || p->D != 128 || p->norm_by_lkv) return JATTN_ERR_INVALID;
+  if (!q_off || !kv_off || !q_block_start || !kv_block_start) return JATTN_ERR_INVALID;
+  if (p->total_q > 0 && (!q || !q_scales || !o || !lse)) return JATTN_ERR_INVALID;
+  if (p->total_kv > 0 && (!k || !k_scales || !v || !v_scales)) return JATTN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return JATTN_ERR_ALIGN;
+  auto aligned4 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 3u) == 0; };
+  if (!aligned4(q_scales) || !aligned4(k_scales) || !aligned4(v_scales)) return JATTN_ERR_ALIGN;
+  if ((rc = check_ws(p, ws, ws_bytes)) != JATTN_OK) return rc;
+  DeviceInfo dev;
+  if ((rc = device_info(dev)) != JATTN_OK) return rc;
+  if ((rc = encoder()) != JATTN_OK) return rc;
+  clear_stale_error();
+  if (p->total_q == 0) return JATTN_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Layout L = layout_for(*p);
+  const SchedView sv = sched_carve(static_cast<char*>(ws) + L.sched_q, p->B, L.tiles_q);
+  AttnArgs a = base_args(*p, q_off, kv_off, ws);
+  cudaError_t e;
+  if ((e = sched_launch(sv, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 0,
+                        a.status, st)) != cudaSuccess)
+    return cuda_fail("schedule launch", e);
+  CUtensorMap mq, mk, mv;
+  if (make_map_u8(&mq, q, p->total_q, p->H, p->D) || make_map_u8(&mk, k, p->total_kv, p->H, p->D) ||
+      make_map_u8(&mv, v, p->total_kv, p->H, p->D))
+    return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+  a.tiles = sv.sorted;
+  a.n_tiles = sv.n_tiles;
+  a.out0 = reinterpret_cast<__nv_bfloat16*>(o);
+  a.f0 = lse;
+  a.out_v8 = aligned32(o);
+  a.sf_q = q_scales;
+  a.sf_k = k_scales;
+  a.sf_v = v_scales;
+  a.bs_q = q_block_start;
+  a.bs_kv = kv_block_start;
+  prof(0, st);
+  if ((e = launch_fwd_mx(mq, mk, mv, a, grid_for(dev, L.tiles_q, p->H), st)) != cudaSuccess)
+    return cuda_fail("MXFP8 forward kernel launch", e);
+  prof(1, st);
   return JATTN_OK;
 }
 

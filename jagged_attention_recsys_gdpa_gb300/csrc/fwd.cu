@@ -290,14 +290,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         k_waited = idx + 1;
         return true;
       };
+      // Shared-memory descriptors of the tile bases, computed once: the kk-th
+      // 16-wide slice of a K-major tile lies (kk / 4) 64-column boxes and
+      // (kk % 4) * 32 bytes further, and the next V slice 16 rows further,
+      // which are additions to the descriptor's address field (16-byte units).
+      // Each MMA then costs its issuing thread one add per operand.
+      const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024), dK0 = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(sV, kTile * 128, 1024);
+      constexpr uint64_t kTileUnits = C::kTileBytes >> 4;
+      auto kslice = [](int kk) -> uint64_t { return static_cast<uint64_t>(((kk >> 2) * (kTile * 128) + (kk & 3) * 32) >> 4); };
       auto issue_s = [&](int q, uint32_t kidx) {
-        const uint32_t kb = sK + (kidx % C::kKStages) * C::kTileBytes;
+        const uint64_t kd = dK0 + (kidx % C::kKStages) * kTileUnits, qd = dQ0 + q * kTileUnits;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_ss(tmem + q * kTile, sdesc_sw128(sQ + q * C::kTileBytes + off, 16, 1024),
-                 sdesc_sw128(kb + off, 16, 1024), idS, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + q * kTile, qd + kslice(kk), kd + kslice(kk), idS, kk > 0);
         mma_commit(&bars->s_full[q]);
       };
       ItemInfo nit;
@@ -332,13 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(ok = wait_bar(&bars->p_full[q], p_cnt[q] & 1, abort_flag, a, 24))) break;
               ++p_cnt[q];
               tc_fence_after();
+              const uint64_t vd = dV0 + vs * kTileUnits;
 #pragma unroll
               for (int kk = 0; kk < kTile / 16; ++kk) {
                 // P of key columns 16kk.. sits at column 8kk; with the column split,
                 // at 8kk + 32 for the second half
                 mma_ts(tmem + C::kOCol + q * D, tmem + q * kTile + kk * 8 + ((SPLIT && kk >= kTile / 32) ? 32 : 0),
-                       sdesc_sw128(sV + vs * C::kTileBytes + kk * 16 * 128, kTile * 128, 1024), idPV,
-                       (kk > 0 || j > it.t_lo[q]) ? 1u : 0u);
+                       vd + kk * (16 * 128 / 16), idPV, (kk > 0 || j > it.t_lo[q]) ? 1u : 0u);
               }
               if constexpr (kHilo) {
                 // unnormalised pointwise: P's lo parts, 64 columns further (ping-pong)
@@ -348,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kTile / 16; ++kk)
                   mma_ts(tmem + C::kOCol + q * D,
                          tmem + q * kTile + kk * 8 + ((SPLIT && kk >= kTile / 32) ? 32 : 0) + (SPLIT ? 32 : 64),
-                         sdesc_sw128(sV + vs * C::kTileBytes + kk * 16 * 128, kTile * 128, 1024), idPV, 1u);
+                         vd + kk * (16 * 128 / 16), idPV, 1u);
               }
               if (j + 1 == it.t_hi[q]) {
                 mma_commit(&bars->o_full[q]);

@@ -26,6 +26,11 @@ cudaError_t launch_fwd_block_hilo(int D, int act, bool split, const CUtensorMap&
                                   const CUtensorMap& v, const AttnArgs& a, int grid, cudaStream_t stream);
 int fwd_rows_per_item();
 
+// MXFP8 forward (softmax, D = 128): maps of the E4M3 codes (uint8 [rows, H*128],
+// boxes of 128 rows x 128 bytes); a.sf_* / a.bs_* carry the block scales.
+cudaError_t launch_fwd_mx(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const AttnArgs& a,
+                          int grid, cudaStream_t stream);
+
 // dK, dV over key tiles (transposed schedule, 128-row key tiles). o0 / o1 map
 // dK / dV (tile stores of whole tiles).
 cudaError_t launch_bwd_dkdv(int D, int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k,

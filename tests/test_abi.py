@@ -92,6 +92,23 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
     assert b"bytes of scratch" in lib.jattn_last_error()
 
 
+def test_mxfp8_forward_checks_arguments(lib):
+    f = 1 << 20  # never dereferenced: every call below must fail on the host first
+    big = 1 << 30
+
+    def call(pp=None, q=f, qs=f, k=f, ks=f, v=f, vs=f, o=f, lse=f):
+        pp = pp if pp is not None else _params(mask=1)
+        return lib.jattn_fwd_mxfp8(ctypes.byref(pp), f, f, q, qs, f, k, ks, v, vs, f, o, lse, f, big, None)
+
+    assert call(pp=_params(act=1, norm_by_lkv=1)) == 1  # softmax only
+    assert call(pp=_params(D=64)) == 1                  # D = 128 only
+    assert call(lse=None) == 1
+    assert call(qs=None) == 1
+    assert call(q=f + 8) == 4
+    assert call(vs=f + 2) == 4                          # scale words are read 4 bytes at a time
+    assert lib.jattn_fwd_mxfp8(ctypes.byref(_params()), f, f, f, f, None, f, f, f, f, f, f, f, f, big, None) == 1
+
+
 def test_error_strings(lib):
     for code in range(10):
         assert B.error_string(code) != "unknown error code", code

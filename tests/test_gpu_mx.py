@@ -47,3 +47,87 @@ def test_quantize_wide_magnitudes_zeros_and_saturation():
     x[64:70, 0, 0:32] = 500.0  # block max 500: X = 1, so 500 (and 479 -> bf16 480) saturate to 448
     x[64, 0, 1] = 479.0
     _check(x.to(torch.bfloat16), off)
+
+
+# ---------------------------------------------------------------- MXFP8 attention forward
+def _mx_inputs(w, lq, lkv, seed):
+    """Seeded bf16 inputs, quantized by the ORACLE's quantizer (the GPU's is
+    bit-exact with it, tested above): codes, scales and block starts for both
+    sides, as host numpy arrays and as device tensors."""
+    cpu = G.cpu_inputs(w, lq, lkv, seed)
+    qo, ko = cpu["q_off"].numpy(), cpu["kv_off"].numpy()
+    host = {n: mx.quantize(cpu[n], qo if n == "q" else ko) for n in ("q", "k", "v")}
+    dev = {n: (torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda(), torch.from_numpy(bs.astype(np.int32)).cuda())
+           for n, (c, s, bs) in host.items()}
+    return cpu, host, dev
+
+
+def _mx_bound(host, cpu, w, o_ref):
+    """Per-element bound |o - o_ref| <= sum_j (2^-3 e_ij + 2^-17) |v_jd| / l_i
+    + 2^-8 |o_ref| + 1e-3: the kernel quantizes P against its running maximum,
+    the oracle against the final one, so each P~ may differ by one E4M3
+    rounding step (2^-4 relative each way, 2^-18 absolute below the normal
+    range); the rest covers the bf16 rounding of o and fp32 accumulation.
+    e_ij = exp(s_ij - m_i) and l_i = sum_j e_ij from the dequantized operands."""
+    qo, ko = cpu["q_off"].numpy(), cpu["kv_off"].numpy()
+    qd, kd, vd = (mx.dequantize(*host[n][:2], qo if n == "q" else ko) for n in ("q", "k", "v"))
+    bound = 2.0**-8 * np.abs(o_ref) + 1e-3
+    scale = 1.0 / np.sqrt(w.D)
+    mask = w.mask | (1 if w.mask & 2 else 0)
+    for b in range(len(qo) - 1):
+        lq, lkv = int(qo[b + 1] - qo[b]), int(ko[b + 1] - ko[b])
+        if lq == 0 or lkv == 0:
+            continue
+        ok = mx._allowed(lq, lkv, mask, w.window)
+        for h in range(w.H):
+            s = np.where(ok, scale * qd[qo[b]:qo[b + 1], h] @ kd[ko[b]:ko[b + 1], h].T, -np.inf)
+            m = np.where(ok.any(1), s.max(1, initial=-np.inf), 0.0)
+            e = np.where(ok, np.exp(s - m[:, None]), 0.0)
+            l = np.maximum(e.sum(1), 1e-300)
+            term = ((2.0**-3 * e + 2.0**-17 * ok) @ np.abs(vd[ko[b]:ko[b + 1], h])) / l[:, None]
+            bound[qo[b]:qo[b + 1], h] += term
+    return bound
+
+
+MX_CASES = [
+    # (mask, window, lq, lkv, std)
+    (1, 0, [1, 127, 128, 129, 300, 513], None, 1.0),
+    (3, 200, [1, 127, 128, 129, 300, 513], None, 1.0),
+    (0, 0, [100, 300, 5, 1], [20, 700, 129, 300], 1.0),
+    (4, 64, [1, 127, 128, 129, 300, 513], None, 1.0),
+    (1, 0, [0, 5, 130, 0], [7, 0, 130, 3], 1.0),
+    (1, 0, [300, 700], None, 2.0),  # peaky rows: the running maximum moves often
+]
+
+
+@pytest.mark.parametrize("case", range(len(MX_CASES)))
+def test_mxfp8_forward_matches_oracle(case):
+    """The block-scaled FP8 forward against oracle/mx.py's attention_fwd on the
+    operands the codes and scales stand for, under the per-element bound the
+    kernel's P quantization allows (see _mx_bound and jattn.h); LSE, which
+    uses the unquantized P, within the bf16 tolerance."""
+    import jagged_attention_recsys_gdpa_gb300 as J
+
+    mask, window, lq, lkv, std = MX_CASES[case]
+    lkv = lq if lkv is None else lkv
+    w = inputs.Workload("case", 2, 128, 0, mask, window, False, std, lq == lkv)
+    cpu, host, dev = _mx_inputs(w, lq, lkv, seed=95 + case)
+    qo, ko = cpu["q_off"].numpy(), cpu["kv_off"].numpy()
+    qd, kd, vd = (mx.dequantize(*host[n][:2], qo if n == "q" else ko) for n in ("q", "k", "v"))
+    o_ref, lse_ref = mx.attention_fwd(qd, kd, vd, qo, ko, mask=mask | (1 if mask & 2 else 0), window=window)
+    o, lse = J.forward_mxfp8(dev["q"], dev["k"], dev["v"], cpu["q_off"].cuda(), cpu["kv_off"].cuda(),
+                             causal=bool(mask & 1), window=window if mask & 2 else 0,
+                             block=window if mask & 4 else 0)
+    torch.cuda.synchronize()
+    assert J.device_status() == 0
+    got = G.to64(o)
+    assert np.all(np.isfinite(got))
+    bound = _mx_bound(host, cpu, w, o_ref)
+    err = np.abs(got - o_ref)
+    bad = err > bound
+    assert not bad.any(), (int(bad.sum()), float((err - bound).max()))
+    lg = lse.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isneginf(lg), np.isneginf(lse_ref))
+    fin = np.isfinite(lse_ref)
+    G.assert_close(lg[fin], lse_ref[fin], "LSE")
+
