@@ -237,15 +237,16 @@ int jattn_mxfp8_quantize(int64_t B, int64_t total, int H, int D, const int64_t* 
  * H, 4] (4-byte aligned) and the row-block starts (int32 [B+1]) of their
  * offsets; K and V share kv_block_start (quantized with the same offsets).
  * Both products run as block-scaled tensor-core MMAs on the exact values the
- * codes and scales stand for, accumulating in fp32. P is quantized per key
- * tile against the running row maximum m, which the kernel moves whenever it
- * grows, so P = exp(s - m) <= 1 and its scale is 2^-8 (E4M3's largest power
- * of two is 2^8): P~ = E4M3(256 P) / 256. The row sum l and LSE use the
- * unquantized P in fp32; o = (sum_j P~_ij v_j) / l (bf16), lse as jattn_fwd.
- * Against the same definition with the exact final maximum, each P~ differs
- * by at most one E4M3 rounding step (2^-3 P relative, 2^-17 absolute below
- * E4M3's normal range), so |o - o_ref| <= sum_j (2^-3 p_ij + 2^-17 / l_i)
- * |v_j| plus bf16 rounding of o. The workspace is jattn_fwd's (it uses the
+ * codes and scales stand for, accumulating in fp32. P = exp(s - m), m the
+ * running row maximum (moved when a row's maximum grows by more than 2^8), is
+ * quantized per row and 32-key block with the scale 2^(ceil(log2 x) - 8), x
+ * the block's largest P, so codes stay within E4M3's range and small values
+ * keep their precision. The row sum l and LSE use the unquantized P in fp32;
+ * o = (sum_j P~_ij v_j) / l (bf16), lse as jattn_fwd. Against quantizing with
+ * the exact final maximum (the definition, scale 2^-8), each P~ differs by at
+ * most one E4M3 rounding step (2^-3 P relative, below 2^-16 absolute in E4M3's
+ * subnormal range), so |o - o_ref| <= sum_j (2^-3 p_ij + 2^-16 / l_i) |v_j|
+ * plus the bf16 rounding of o. The workspace is jattn_fwd's (it uses the
  * 128-row query-tile schedule). Return codes as jattn_fwd, plus
  * JATTN_ERR_INVALID for another activation, D != 128 or norm_by_lkv. */
 int jattn_fwd_mxfp8(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint8_t* q,
