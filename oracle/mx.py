@@ -25,8 +25,9 @@ block_start the exclusive prefix sum of ceil(L_b / 32); scales are laid out
 
 ``attention_fwd`` / ``attention_bwd`` state softmax attention on MXFP8
 operands (P quantized in the softmax with the scale its row maximum fixes,
-dS quantized with [32, 32] blocks); they are the reference for a block-scaled
-attention kernel, which is not built yet.
+dS quantized with [32, 32] blocks); ``attention_fwd`` is the reference of the
+block-scaled forward kernel (jattn_fwd_mxfp8), ``attention_bwd`` of a
+backward that is not built.
 """
 from __future__ import annotations
 
