@@ -35,6 +35,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "mx_common.cuh"
 
 namespace jattn {
 
@@ -77,58 +78,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer_ns() - t0 > timeout_ns) return;
   }
-}
-
-struct MxItem {
-  int b, qt, lo, hi, h, lq, lkv;
-  int64_t q0, k0;
-};
-
-__device__ __forceinline__ bool load_mx_item(const AttnArgs& a, long long round, MxItem& it) {
-  const long long n_items = static_cast<long long>(*a.n_tiles) * a.H;
-  const long long k = zigzag_item(round, blockIdx.x, gridDim.x);
-  if (k >= n_items) return false;
-  const int4 t = a.tiles[k / a.H];
-  it.h = static_cast<int>(k % a.H);
-  it.b = t.x;
-  it.qt = t.y;
-  it.lo = t.z;
-  it.hi = t.w;
-  it.q0 = a.q_off[it.b];
-  it.k0 = a.kv_off[it.b];
-  it.lq = static_cast<int>(a.q_off[it.b + 1] - it.q0);
-  it.lkv = static_cast<int>(a.kv_off[it.b + 1] - it.k0);
-  return true;
-}
-
-// The 4 scale bytes of row block g (head h, D / 32 = 4 column blocks) as one word.
-__device__ __forceinline__ uint32_t sf_word(const uint8_t* sf, int g, int H, int h) {
-  return __ldg(reinterpret_cast<const uint32_t*>(sf + (static_cast<int64_t>(g) * H + h) * 4));
-}
-
-// Row block r of sequence b, clamped to the sequence's blocks (tile rows past
-// the sequence read some finite scale; their scores are masked).
-__device__ __forceinline__ int row_block(const int* bs, int b, int r) {
-  const int first = bs[b], last = bs[b + 1] - 1;
-  return min(first + r, max(last, first));
-}
-
-// The 4 scale words of row blocks 4j .. 4j + 3 (key tile j) of one head, the
-// block indices clamped to the sequence's [first, last] (loads only; they are
-// issued a step before their use).
-__device__ __forceinline__ void kv_scale_load(const uint8_t* sf, int first, int last, int j, int H, int h,
-                                              uint32_t (&r)[4]) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) r[c] = sf_word(sf, min(first + 4 * j + c, last), H, h);
-}
-// In the replicated layout (lane l of every quarter, column c = index 32c + l)
-// a K tile's words are the row blocks' words as they are (4 column blocks in
-// the bytes); a V tile's column block c takes byte c of each row block's word.
-__device__ __forceinline__ void v_scale_words(const uint32_t (&r)[4], uint32_t (&w)[4]) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-    w[c] = ((r[0] >> (8 * c)) & 0xffu) | (((r[1] >> (8 * c)) & 0xffu) << 8) | (((r[2] >> (8 * c)) & 0xffu) << 16) |
-           (((r[3] >> (8 * c)) & 0xffu) << 24);
 }
 
 // Scale exponent of a 32-key block of P = 2^x whose largest exponent argument
@@ -194,8 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmV);
         uint32_t q_it = 0, kv_it = 0;
         bool ok = true;
-        MxItem it;
-        for (long long r = 0; ok && load_mx_item(a, r, it); ++r) {
+        mx::Item it;
+        for (long long r = 0; ok && mx::load_item(a, r, it); ++r) {
           if (it.hi <= it.lo) continue;
           const int qs = q_it % kQStages;
           if (!(ok = wait_bar(&bars->q_empty[qs], ((q_it / kQStages) & 1) ^ 1, abort_flag, a, 110))) break;
@@ -233,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint64_t kTileUnits = kTileBytes >> 4;
         uint32_t q_it = 0, kv_it = 0, sf_cnt = 0, o_cnt = 0, g = 0;  // g: key tiles so far
         bool ok = true;
-        MxItem it;
+        mx::Item it;
         // S(t) of global key tile t into buffer t & 1 from ring stage ks
         auto issue_s = [&](int qs, uint32_t t, int ks) {
           const uint32_t b = t & 1;
@@ -243,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       idesc_mx_e4m3(kTile, kTile, false, false, kb, kb), tmem + kSfQ, tmem + kSfK + 4 * b, kb > 0);
           mma_commit(&bars->s_full[b]);
         };
-        for (long long r = 0; ok && load_mx_item(a, r, it); ++r) {
+        for (long long r = 0; ok && mx::load_item(a, r, it); ++r) {
           if (it.hi <= it.lo) continue;
           const int qs = q_it % kQStages;
           const int n = it.hi - it.lo;
@@ -313,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       return xch[(slot * 2 + (half ^ 1)) * kTile + row];
     };
     bool ok = true;
-    MxItem it;
-    for (long long r = 0; ok && load_mx_item(a, r, it); ++r) {
+    mx::Item it;
+    for (long long r = 0; ok && mx::load_item(a, r, it); ++r) {
       const int il = it.qt * kTile + row;
       const bool valid = il < it.lq;
       const int64_t grow = it.q0 + il;
@@ -337,10 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (half == 0) {  // scales of Q and of the item's first two K tiles
         uint32_t w[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) w[c] = sf_word(a.sf_q, row_block(a.bs_q, it.b, 4 * it.qt + c), a.H, it.h);
+        for (int c = 0; c < 4; ++c) w[c] = mx::sf_word(a.sf_q, mx::row_block(a.bs_q, it.b, 4 * it.qt + c), a.H, it.h);
         tmem_st4(tmem + lane_base + kSfQ, w[0], w[1], w[2], w[3]);
         for (int t = 0; t < 2 && t < n; ++t) {
-          kv_scale_load(a.sf_k, kv_first, kv_last, it.lo + t, a.H, it.h, w);
+          mx::kv_scale_load(a.sf_k, kv_first, kv_last, it.lo + t, a.H, it.h, w);
           tmem_st4(tmem + lane_base + kSfK + 4 * ((g + t) & 1), w[0], w[1], w[2], w[3]);
         }
         tmem_st_wait();
@@ -354,8 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // scale words this step hands over (warpgroup 1: V tile j; warpgroup 0:
         // K tile j + 2), loaded before the wait so their latency is hidden
         uint32_t sw[4] = {0, 0, 0, 0};
-        if (half == 1) kv_scale_load(a.sf_v, kv_first, kv_last, j, a.H, it.h, sw);
-        else if (t + 2 < n) kv_scale_load(a.sf_k, kv_first, kv_last, j + 2, a.H, it.h, sw);
+        if (half == 1) mx::kv_scale_load(a.sf_v, kv_first, kv_last, j, a.H, it.h, sw);
+        else if (t + 2 < n) mx::kv_scale_load(a.sf_k, kv_first, kv_last, j + 2, a.H, it.h, sw);
         ok = __all_sync(0xffffffffu, wait_bar(&bars->s_full[b], (gt >> 1) & 1, abort_flag, a, 130));
         if (!ok) break;
         tc_fence_after();
@@ -451,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // previous contents have completed (S(t) was issued after them)
         if (half == 1) {
           uint32_t w[4];
-          v_scale_words(sw, w);
+          mx::v_scale_words(sw, w);
           tmem_st4(tmem + lane_base + kSfV + 4 * b, w[0], w[1], w[2], w[3]);
         } else if (t + 2 < n) {
           tmem_st4(tmem + lane_base + kSfK + 4 * b, sw[0], sw[1], sw[2], sw[3]);
