@@ -254,6 +254,39 @@ int jattn_fwd_mxfp8(const jattn_params_t* p, const int64_t* q_off, const int64_t
                     const uint8_t* v, const uint8_t* v_scales, const int32_t* kv_block_start, uint16_t* o, float* lse,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* MXFP8 attention backward (the same section: block-scaled FP8 MMAs in the
+ * backward too, dS quantized online with [32, 32] square blocks so that one
+ * quantization serves dS and its transpose).
+ *
+ * Gradients of jattn_fwd_mxfp8's attention: q, k, v (and their scales and
+ * block starts) as there; dout = dO as jattn_mxfp8_quantize output with the
+ * query side's offsets (codes [total_q, H, 128] 16-byte aligned, scales
+ * [row blocks, H, 4] 4-byte aligned, sharing q_block_start); o (bf16
+ * [total_q, H, 128]) and lse (fp32 [total_q, H]) from the forward. Every
+ * product is a block-scaled tensor-core MMA on the exact values of its FP8
+ * operands with fp32 accumulation:
+ *   D_i = <dO~_i, o_i>,  P = exp(s - lse),  dS = P (dP - D),  dP = dO~ V~^T,
+ *   dV = P~^T dO~,  dQ = scale dS~ K~,  dK = scale dS~^T Q~,
+ * with P~ = P quantized per key and 32-query block with the scale
+ * 2^(ceil(log2 x) - 8), x the block's largest P (as the forward), and dS~
+ * = dS quantized per [32, 32] block of (query, key) pairs counted from the
+ * sequence starts, with the Microscaling rule of jattn_mxfp8_quantize (scale
+ * 2^(floor(log2 amax) - 8), saturating at +-448). dq, dk, dv are bf16
+ * [total, H, 128], 16-byte aligned; rows that see nothing get zeros. Against
+ * the definition with P quantized at the final row maximum (scale 2^-8 of
+ * exp(s - m), divided by l), |dv - dv_ref| <= sum_i (2^-3 p_ij + 2^-16 / l_i)
+ * |dO~_i| plus bf16 rounding; dq and dk differ from the definition by the
+ * quantization steps of dS~ that either side's fp32 rounding can move.
+ * The workspace is jattn_bwd's (jattn_workspace_size with act softmax): it
+ * holds D and the two tile schedules. The passes run in order D, dQ, dK/dV
+ * on `stream`. Return codes as jattn_bwd, plus JATTN_ERR_INVALID for another
+ * activation, D != 128 or norm_by_lkv. */
+int jattn_bwd_mxfp8(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint8_t* q,
+                    const uint8_t* q_scales, const int32_t* q_block_start, const uint8_t* k, const uint8_t* k_scales,
+                    const uint8_t* v, const uint8_t* v_scales, const int32_t* kv_block_start, const uint16_t* o,
+                    const float* lse, const uint8_t* dout, const uint8_t* dout_scales, uint16_t* dq, uint16_t* dk,
+                    uint16_t* dv, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Longest-first tile schedule ("GEM Training" post, GDPA section: valid tiles
  * are precomputed, empty ones skipped, and the rest spread over the SMs so
  * no SM gets a much longer share). Builds the schedule the kernels use into

@@ -182,6 +182,26 @@ def forward_mxfp8(qm, km, vm, q_off, kv_off, causal=False, window=0, block=0, sc
     return o, lse
 
 
+def backward_mxfp8(qm, km, vm, o, lse, dom, q_off, kv_off, causal=False, window=0, block=0, scale=None, dq=None,
+                   dk=None, dv=None):
+    """Softmax attention backward on MXFP8 operands: qm, km, vm, dom are
+    mxfp8_quantize triples (dom quantized with q_off), o and lse the
+    forward's outputs. D must be 128. Returns (dQ, dK, dV) bf16."""
+    (qc, qs, qbs), (kc, ks, kbs), (vc, vs, _), (dc, ds, _) = qm, km, vm, dom
+    total_q, H, D = qc.shape
+    total_kv = kc.shape[0]
+    p = B.params(q_off.numel() - 1, total_q, total_kv, H, D, SOFTMAX, _mask(causal, window, block),
+                 _width(window, block), scale, False)
+    dev = qc.device
+    dq = dq if dq is not None else torch.empty((total_q, H, D), dtype=torch.bfloat16, device=dev)
+    dk = dk if dk is not None else torch.empty((total_kv, H, D), dtype=torch.bfloat16, device=dev)
+    dv = dv if dv is not None else torch.empty((total_kv, H, D), dtype=torch.bfloat16, device=dev)
+    ws = workspace(p, dev)
+    B.bwd_mxfp8(p, q_off, kv_off, qc, qs, qbs, kc, ks, vc, vs, kbs, o, lse, dc, ds, dq, dk, dv, ws.data_ptr(),
+                ws.numel(), _stream(dev))
+    return dq, dk, dv
+
+
 def backward(q, k, v, o, lse, do, q_off, kv_off, act="softmax", causal=False, window=0, scale=None,
              norm_by_lkv=False, dq=None, dk=None, dv=None, block=0, rope=None):
     """Backward pass. Returns (dQ, dK, dV) bf16. With ``rope`` = (cos, sin)

@@ -26,6 +26,7 @@ EXPORTED = (
     "jattn_mxfp8_scale_rows",
     "jattn_mxfp8_quantize",
     "jattn_fwd_mxfp8",
+    "jattn_bwd_mxfp8",
     "jattn_schedule",
     "jattn_partition",
     "jattn_max_tiles",
@@ -100,6 +101,8 @@ def load(path: str | None = None):
     lib.jattn_mxfp8_quantize.restype = i32
     lib.jattn_fwd_mxfp8.argtypes = [P] + [vp] * 12 + [vp, ctypes.c_size_t, vp]
     lib.jattn_fwd_mxfp8.restype = i32
+    lib.jattn_bwd_mxfp8.argtypes = [P] + [vp] * 17 + [vp, ctypes.c_size_t, vp]
+    lib.jattn_bwd_mxfp8.restype = i32
     lib.jattn_bwd_rope_workspace_size.argtypes = [P, i64, ctypes.POINTER(ctypes.c_size_t)]
     lib.jattn_bwd_rope_workspace_size.restype = i32
     lib.jattn_schedule.argtypes = [P, vp, vp, i32, i32, i32, vp, i64, vp, vp, ctypes.c_size_t, vp]
@@ -192,6 +195,14 @@ def fwd_mxfp8(p: Params, q_off, kv_off, q, q_scales, q_bs, k, k_scales, v, v_sca
     check(load().jattn_fwd_mxfp8(ctypes.byref(p), ptr(q_off), ptr(kv_off), ptr(q), ptr(q_scales), ptr(q_bs), ptr(k),
                                  ptr(k_scales), ptr(v), ptr(v_scales), ptr(kv_bs), ptr(o), ptr(lse), ws, ws_bytes,
                                  stream), "jattn_fwd_mxfp8")
+
+
+def bwd_mxfp8(p: Params, q_off, kv_off, q, q_scales, q_bs, k, k_scales, v, v_scales, kv_bs, o, lse, dout,
+              dout_scales, dq, dk, dv, ws, ws_bytes: int, stream: int):
+    check(load().jattn_bwd_mxfp8(ctypes.byref(p), ptr(q_off), ptr(kv_off), ptr(q), ptr(q_scales), ptr(q_bs), ptr(k),
+                                 ptr(k_scales), ptr(v), ptr(v_scales), ptr(kv_bs), ptr(o), ptr(lse), ptr(dout),
+                                 ptr(dout_scales), ptr(dq), ptr(dk), ptr(dv), ws, ws_bytes, stream),
+          "jattn_bwd_mxfp8")
 
 
 def rope(p: Params, q_off, kv_off, keys: bool, inverse: bool, x, y, rope_cos, rope_sin, ws, ws_bytes: int,

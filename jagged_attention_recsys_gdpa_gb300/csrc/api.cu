@@ -188,14 +188,15 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int H, int D) {
 // the sequence length (outputs there sum thousands of unscaled terms).
 bool hilo_for(const jattn_params_t& p) { return p.act != JATTN_SOFTMAX && !p.norm_by_lkv; }
 
-// 2-D view [rows, H*D] of jagged E4M3 codes (one byte each); boxes of 128
-// rows x 128 bytes with the 128-byte swizzle (D = 128: one box per head row).
-int make_map_u8(CUtensorMap* m, const void* ptr, int64_t rows, int H, int D) {
+// 2-D view [rows, H*D] of jagged E4M3 codes (one byte each); boxes of
+// box_rows rows x 128 bytes with the 128-byte swizzle (D = 128: one box per
+// head row).
+int make_map_u8(CUtensorMap* m, const void* ptr, int64_t rows, int H, int D, int box_rows = kTile) {
   std::memset(m, 0, sizeof(*m));
   if (rows == 0) return JATTN_OK;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * D, static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * D};
-  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -460,6 +461,84 @@ int jattn_fwd_mxfp8(const jattn_params_t* p, const int64_t* q_off, const int64_t
   if ((e = launch_fwd_mx(mq, mk, mv, a, grid_for(dev, L.tiles_q, p->H), st)) != cudaSuccess)
     return cuda_fail("MXFP8 forward kernel launch", e);
   prof(1, st);
+  return JATTN_OK;
+}
+
+int jattn_bwd_mxfp8(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_off, const uint8_t* q,
+                    const uint8_t* q_scales, const int32_t* q_block_start, const uint8_t* k, const uint8_t* k_scales,
+                    const uint8_t* v, const uint8_t* v_scales, const int32_t* kv_block_start, const uint16_t* o,
+                    const float* lse, const uint8_t* dout, const uint8_t* dout_scales, uint16_t* dq, uint16_t* dk,
+                    uint16_t* dv, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_params(p);
+  if (rc != JATTN_OK) return rc;
+  if (p->act != JATTN_SOFTMAX || p->D != 128 || p->norm_by_lkv) return JATTN_ERR_INVALID;
+  if (!q_off || !kv_off || !q_block_start || !kv_block_start) return JATTN_ERR_INVALID;
+  if (p->total_q > 0 && (!q || !q_scales || !o || !lse || !dout || !dout_scales || !dq)) return JATTN_ERR_INVALID;
+  if (p->total_kv > 0 && (!k || !k_scales || !v || !v_scales || !dk || !dv)) return JATTN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv))
+    return JATTN_ERR_ALIGN;
+  auto aligned4 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 3u) == 0; };
+  if (!aligned4(q_scales) || !aligned4(k_scales) || !aligned4(v_scales) || !aligned4(dout_scales))
+    return JATTN_ERR_ALIGN;
+  if ((rc = check_ws(p, ws, ws_bytes)) != JATTN_OK) return rc;
+  DeviceInfo dev;
+  if ((rc = device_info(dev)) != JATTN_OK) return rc;
+  if ((rc = encoder()) != JATTN_OK) return rc;
+  clear_stale_error();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  const Layout L = layout_for(*p);
+  AttnArgs a = base_args(*p, q_off, kv_off, ws);
+  float* di = reinterpret_cast<float*>(base + L.di);
+  cudaError_t e;
+  CUtensorMap mq, mk, mv, mdo, mq96, mdo96;
+  if (make_map_u8(&mq, q, p->total_q, p->H, p->D) || make_map_u8(&mk, k, p->total_kv, p->H, p->D) ||
+      make_map_u8(&mv, v, p->total_kv, p->H, p->D) || make_map_u8(&mdo, dout, p->total_q, p->H, p->D) ||
+      make_map_u8(&mq96, q, p->total_q, p->H, p->D, 96) || make_map_u8(&mdo96, dout, p->total_q, p->H, p->D, 96))
+    return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+  a.f0 = const_cast<float*>(lse);
+  a.f1 = di;
+  a.sf_q = q_scales;
+  a.sf_k = k_scales;
+  a.sf_v = v_scales;
+  a.sf_do = dout_scales;
+  a.bs_q = q_block_start;
+  a.bs_kv = kv_block_start;
+  // D first: both passes read it
+  if (p->total_q > 0) {
+    if ((e = launch_mx_di(q_off, static_cast<int>(p->B), p->H, jattn_mxfp8_scale_rows(p->B, p->total_q), dout,
+                          dout_scales, q_block_start, o, di, st)) != cudaSuccess)
+      return cuda_fail("D kernel launch", e);
+    const SchedView qs = sched_carve(base + L.sched_q, p->B, L.tiles_q);
+    if ((e = sched_launch(qs, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 0,
+                          a.status, st)) != cudaSuccess)
+      return cuda_fail("query-tile schedule launch", e);
+    a.tiles = qs.sorted;
+    a.n_tiles = qs.n_tiles;
+    a.out0 = reinterpret_cast<__nv_bfloat16*>(dq);
+    a.out1 = nullptr;
+    a.out_v8 = aligned32(dq);
+    prof(4, st);
+    if ((e = launch_bwd_dq_mx(mq, mk, mv, mdo, a, grid_for(dev, L.tiles_q, p->H), st)) != cudaSuccess)
+      return cuda_fail("MXFP8 dQ kernel launch", e);
+    prof(5, st);
+  }
+  if (p->total_kv > 0) {
+    const SchedView kv = sched_carve(base + L.sched_kv, p->B, L.tiles_kv);
+    if ((e = sched_launch(kv, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 1,
+                          a.status, st)) != cudaSuccess)
+      return cuda_fail("key-tile schedule launch", e);
+    a.tiles = kv.sorted;
+    a.n_tiles = kv.n_tiles;
+    a.out0 = reinterpret_cast<__nv_bfloat16*>(dk);
+    a.out1 = reinterpret_cast<__nv_bfloat16*>(dv);
+    a.out_v8 = aligned32(dk) && aligned32(dv);
+    prof(2, st);
+    if ((e = launch_bwd_dkdv_mx(mq96, mk, mv, mdo96, a, grid_for(dev, L.tiles_kv, p->H), st)) != cudaSuccess)
+      return cuda_fail("MXFP8 dK/dV kernel launch", e);
+    prof(3, st);
+  }
   return JATTN_OK;
 }
 

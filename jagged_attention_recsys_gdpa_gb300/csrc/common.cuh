@@ -54,13 +54,15 @@ struct AttnArgs {
   // and Di come from the tile itself, no O or LSE is read, and the pass writes
   // LSE (a.f0) and Di (a.f1) for the dK/dV pass.
   int in_tile_stats;
-  // MXFP8 forward: E8M0 scales [row blocks, H, D/32] of Q and of K / V, and
+  // MXFP8 passes: E8M0 scales [row blocks, H, D/32] of Q and of K / V, and
   // the first row block of each sequence (int32 [B+1]) of the two sides
   const uint8_t* sf_q;
   const uint8_t* sf_k;
   const uint8_t* sf_v;
   const int* bs_q;
   const int* bs_kv;
+  // MXFP8 backward: E8M0 scales of dO (row blocks of the query side)
+  const uint8_t* sf_do;
 };
 
 // The bf16 pair of what the bf16 pair `hi` of (x0, x1) leaves out.

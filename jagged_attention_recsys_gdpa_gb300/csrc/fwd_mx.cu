@@ -73,21 +73,6 @@ struct MxBars {
 static_assert(sizeof(MxBars) <= 512, "barrier block overflows its slot");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > timeout_ns) return;
-  }
-}
-
-// Scale exponent of a 32-key block of P = 2^x whose largest exponent argument
-// is xmax: e = ceil(xmax) - 8, so the block's P / 2^e lie in (0, 256] with the
-// largest in (128, 256]; clamped to keep 2^e a normal float (a block with no
-// allowed key takes any scale, its codes are 0).
-__device__ __forceinline__ int p_block_exp(float xmax) {
-  return (xmax == -INFINITY) ? -8 : max(-100, min(100, static_cast<int>(ceilf(xmax)) - 8));
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_mx_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
@@ -166,9 +151,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // let every copy this thread started land before the CTA can exit
         if (!(a.debug_flags & 1))
           for (uint32_t i = (q_it > kQStages ? q_it - kQStages : 0); i < q_it; ++i)
-            drain_wait(&bars->q_full[i % kQStages], (i / kQStages) & 1, a.timeout_ns);
+            mx::drain_wait(&bars->q_full[i % kQStages], (i / kQStages) & 1, a.timeout_ns);
         for (uint32_t i = (kv_it > kKVStages ? kv_it - kKVStages : 0); i < kv_it; ++i)
-          drain_wait(&bars->kv_full[i % kKVStages], (i / kKVStages) & 1, a.timeout_ns);
+          mx::drain_wait(&bars->kv_full[i % kKVStages], (i / kKVStages) & 1, a.timeout_ns);
       }
       __syncwarp();
     } else if (warp == 1) {
@@ -236,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           g += n;
         }
         mma_commit(&bars->drain);
-        drain_wait(&bars->drain, 0, a.timeout_ns);
+        mx::drain_wait(&bars->drain, 0, a.timeout_ns);
       }
       __syncwarp();
     }
@@ -370,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t c2 = f2(a.scale_log2, a.scale_log2);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          const int e = p_block_exp(fmaf(bm[k], a.scale_log2, -mref));
+          const int e = mx::p_block_exp(fmaf(bm[k], a.scale_log2, -mref));
           sfb |= static_cast<uint32_t>(127 + e) << (8 * (2 * half + k));
           const float off = mref + static_cast<float>(e);
           const uint64_t no2 = f2(-off, -off);

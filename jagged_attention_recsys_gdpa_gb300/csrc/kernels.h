@@ -31,6 +31,19 @@ int fwd_rows_per_item();
 cudaError_t launch_fwd_mx(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const AttnArgs& a,
                           int grid, cudaStream_t stream);
 
+// MXFP8 backward (softmax, D = 128). launch_mx_di: D_i = <dO~_i, O_i> per
+// query row and head into di (row blocks from block_start, at most
+// max_blocks of them). dq: over 128-row query tiles (maps of 128-row boxes);
+// dkdv: over 128-row key tiles, queries in steps of 96 (the Q and dO maps
+// have 96-row boxes). a.f0 = LSE, a.f1 = D; a.sf_* / a.bs_* the block scales.
+cudaError_t launch_mx_di(const int64_t* q_off, int B, int H, int64_t max_blocks, const uint8_t* dout,
+                         const uint8_t* dout_scales, const int* block_start, const void* o, float* di,
+                         cudaStream_t stream);
+cudaError_t launch_bwd_dq_mx(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                             const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv_mx(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream);
+
 // dK, dV over key tiles (transposed schedule, 128-row key tiles). o0 / o1 map
 // dK / dV (tile stores of whole tiles).
 cudaError_t launch_bwd_dkdv(int D, int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k,

@@ -60,6 +60,40 @@ __device__ __forceinline__ void v_scale_words(const uint32_t (&r)[4], uint32_t (
            (((r[3] >> (8 * c)) & 0xffu) << 24);
 }
 
+// Bounded wait of a role's last step (its copies or MMAs in flight landing
+// before the CTA exits): gives up silently after timeout_ns.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+// Scale exponent of a 32-element block of P = 2^x whose largest exponent
+// argument is xmax: e = ceil(xmax) - 8, so the block's P / 2^e lie in (0, 256]
+// with the largest in (128, 256]; clamped to keep 2^e a normal float (a block
+// with no allowed entry takes any scale, its codes are 0).
+__device__ __forceinline__ int p_block_exp(float xmax) {
+  return (xmax == -INFINITY) ? -8 : max(-100, min(100, static_cast<int>(ceilf(xmax)) - 8));
+}
+
+// Words of row blocks r0 .. r0 + N - 1 of one sequence and head, the indices
+// clamped to the sequence's blocks [first, last] (rows past the sequence read
+// some finite scale; their entries are masked).
+template <int N>
+__device__ __forceinline__ void block_words(const uint8_t* sf, int first, int last, int r0, int H, int h,
+                                            uint32_t (&w)[N]) {
+#pragma unroll
+  for (int c = 0; c < N; ++c) w[c] = sf_word(sf, min(first + r0 + c, last), H, h);
+}
+
+// E8M0 exponent of a [32, 32] block from its largest magnitude's bit pattern
+// (OCP Microscaling rule): E - 127 = floor(log2 amax) - 8, E >= 0; zero and
+// tiny blocks get E = 0.
+__device__ __forceinline__ int block_exponent(uint32_t amax_bits) {
+  const int efield = static_cast<int>(amax_bits >> 23);
+  return efield > 8 ? efield - 8 : 0;
+}
 
 }  // namespace mx
 }  // namespace jattn

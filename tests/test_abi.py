@@ -109,6 +109,24 @@ def test_mxfp8_forward_checks_arguments(lib):
     assert lib.jattn_fwd_mxfp8(ctypes.byref(_params()), f, f, f, f, None, f, f, f, f, f, f, f, f, big, None) == 1
 
 
+def test_mxfp8_backward_checks_arguments(lib):
+    f = 1 << 20  # never dereferenced: every call below must fail on the host first
+    big = 1 << 30
+
+    def call(pp=None, q=f, qs=f, k=f, ks=f, v=f, vs=f, o=f, lse=f, do=f, dos=f, dq=f, dk=f, dv=f, qbs=f):
+        pp = pp if pp is not None else _params(mask=1)
+        return lib.jattn_bwd_mxfp8(ctypes.byref(pp), f, f, q, qs, qbs, k, ks, v, vs, f, o, lse, do, dos, dq, dk, dv,
+                                   f, big, None)
+
+    assert call(pp=_params(act=1, norm_by_lkv=1)) == 1  # softmax only
+    assert call(pp=_params(D=64)) == 1                  # D = 128 only
+    for name in ("lse", "o", "do", "dos", "dq", "dk", "qbs"):
+        assert call(**{name: None}) == 1, name
+    assert call(do=f + 8) == 4
+    assert call(dv=f + 8) == 4
+    assert call(dos=f + 2) == 4                         # scale words are read 4 bytes at a time
+
+
 def test_error_strings(lib):
     for code in range(10):
         assert B.error_string(code) != "unknown error code", code
