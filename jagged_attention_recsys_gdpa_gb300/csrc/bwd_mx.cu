@@ -45,21 +45,28 @@ constexpr float kLog2e = 1.4426950408889634f;
 // 2^e as a float, e in [-126, 127]
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
 
-// Largest magnitude of 32 values, as the bit pattern of |x| (non-negative
-// floats order like their bit patterns).
+// Largest magnitude of 32 values (three-input maxima of magnitudes, four
+// chains), as its bit pattern: non-negative floats order like their bits.
 __device__ __forceinline__ uint32_t amax_bits32(const float* x) {
-  uint32_t m = 0;
+  float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-  for (int c = 0; c < 32; ++c) m = max(m, __float_as_uint(x[c]) & 0x7fffffffu);
-  return m;
+  for (int c = 0; c < 32; c += 8)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) m[e] = fmax3(m[e], fabsf(x[c + 2 * e]), fabsf(x[c + 2 * e + 1]));
+  return __float_as_uint(fmax3(m[0], m[1], fmaxf(m[2], m[3])));
 }
 
 // 32 values times 2^(127 - E) as E4M3 codes, 4 per word (value 4w + b in byte b).
 __device__ __forceinline__ void codes32(const float* x, int E, uint32_t (&pk)[8]) {
   const float inv = __uint_as_float(static_cast<uint32_t>(254 - E) << 23);
+  const uint64_t inv2 = f2(inv, inv);
 #pragma unroll
-  for (int w = 0; w < 8; ++w)
-    pk[w] = pack_e4m3x2(x[4 * w] * inv, x[4 * w + 1] * inv) | (pack_e4m3x2(x[4 * w + 2] * inv, x[4 * w + 3] * inv) << 16);
+  for (int w = 0; w < 8; ++w) {
+    float a0, a1, a2, a3;
+    f2_split(fmul2(f2(x[4 * w], x[4 * w + 1]), inv2), a0, a1);
+    f2_split(fmul2(f2(x[4 * w + 2], x[4 * w + 3]), inv2), a2, a3);
+    pk[w] = pack_e4m3x2(a0, a1) | (pack_e4m3x2(a2, a3) << 16);
+  }
 }
 
 // MN-major B-operand scale words of a tile whose K dimension runs over row
@@ -784,21 +791,32 @@ __global__ void __launch_bounds__(kvc::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) p[c] = (c >= clo && c < chi) ? p[c] : -INFINITY;
         }
+        {  // three-input maxima, four chains
+          float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) xmax = fmax3(xmax, fmaxf(p[c], p[c + 1]), fmaxf(p[c + 2], p[c + 3]));
+          for (int c = 0; c < 32; c += 8)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mp[e] = fmax3(mp[e], p[c + 2 * e], p[c + 2 * e + 1]);
+          xmax = fmax3(mp[0], mp[1], fmaxf(mp[2], mp[3]));
+        }
         // P~ of this key row's 32 queries: one scale 2^e from the largest P,
         // codes of P / 2^e; P itself (for dS) is the scaled value times 2^e
         const int e = mx::p_block_exp(xmax);
-        const float pe = pow2i(e);
+        const uint64_t ne2 = f2(-static_cast<float>(e), -static_cast<float>(e)), pe2 = f2(pow2i(e), pow2i(e));
         uint32_t pk[8];
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
           float y[4];
 #pragma unroll
-          for (int b = 0; b < 4; ++b) y[b] = ex2_approx(p[4 * w + b] - static_cast<float>(e));
+          for (int b = 0; b < 4; b += 2) {
+            float x0, x1;
+            f2_split(fadd2(f2(p[4 * w + b], p[4 * w + b + 1]), ne2), x0, x1);
+            y[b] = ex2_approx(x0);
+            y[b + 1] = ex2_approx(x1);
+          }
           pk[w] = pack_e4m3x2(y[0], y[1]) | (pack_e4m3x2(y[2], y[3]) << 16);
 #pragma unroll
-          for (int b = 0; b < 4; ++b) p[4 * w + b] = y[b] * pe;
+          for (int b = 0; b < 4; b += 2) f2_split(fmul2(f2(y[b], y[b + 1]), pe2), p[4 * w + b], p[4 * w + b + 1]);
         }
         tmem_st8(tmem + lane_base + kSCol + 32 * grp, pk);
         tmem_st1(tmem + lane_base + kSfP + 4 * grp + quarter, static_cast<uint32_t>(127 + e));
