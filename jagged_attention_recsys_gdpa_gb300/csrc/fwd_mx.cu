@@ -19,11 +19,11 @@
 //               [64h, 64h + 64) of every S tile and O columns [64h, 64h + 64);
 //               warps w and w + 4 hold the same rows and combine row maxima and
 //               sums through shared memory
-// The issuing thread spends 75-200 cycles on every tcgen05 operation (MMA or
-// commit) and on every barrier wait, so each key tile costs it 8 MMAs, three
-// commits and two waits: K and V share a ring stage, one barrier and one
-// release, and the S buffers make the MMAs of tile j + 2 independent of the
-// softmax of tile j.
+// One thread issues a tcgen05 operation (MMA or commit) about every 60
+// cycles at best, and every barrier wait adds more, so each key tile costs it
+// 8 MMAs, three commits and two waits: K and V share a ring stage, one barrier
+// and one release, and the S buffers make the MMAs of tile j + 2 independent
+// of the softmax of tile j.
 // TMEM columns: S0 [0, 128), S1 [128, 256), O [256, 384), scale factors from
 // 384. P of warpgroup h overwrites columns [64h, 64h + 16) of its S buffer as
 // E4M3 codes, 4 per column; every 32-key block of a row has its own scale,
