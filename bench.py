@@ -507,7 +507,9 @@ def main():
             "roofline": roof,
             "cpu_baseline": cpu_base,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": (5 + (11 if w.act == 0 else 10)) * args.steps,
+            # per step: three tile schedules of four kernels each, the forward,
+            # dQ (which also computes softmax's Di) and dK/dV
+            "gpu_launches": 15 * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
