@@ -40,7 +40,7 @@ namespace jattn {
 
 namespace {
 
-constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 2-3 Di (dQ, softmax) or idle, warps 4-11 activation
+constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 2-3 Di (dQ) or LSE / Di staging (dK/dV; softmax), warps 4-11 activation
 // Register split (setmaxnreg, per warpgroup): 384 x 168 at launch = 64512 =
 // 128 x 104 (control warpgroup) + 256 x 200 (activation warpgroups).
 constexpr int kCtlRegs = 104;
@@ -202,7 +202,7 @@ struct DkdvBars {
   uint64_t s_full, dp_full, p_ready, ds_ready, acc_full, acc_empty;
   uint64_t drain;
   uint64_t grp[2];  // activation warpgroup meeting points (epilogue staging)
-  uint64_t lgrp[2]; // activation warpgroup meeting points (per-step LSE / Di publish, softmax)
+  uint64_t ld_full[2], ld_empty[2];  // per-step LSE / Di slots (softmax), filled by warps 2-3
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -247,8 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->grp[0], kTile);
     mbar_init(&bars->grp[1], kTile);
-    mbar_init(&bars->lgrp[0], kTile);
-    mbar_init(&bars->lgrp[1], kTile);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars->ld_full[x], 64);
+      mbar_init(&bars->ld_empty[x], kNG * kTile);
+    }
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -385,6 +387,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(&bars->drain, 0, a.timeout_ns);
     }
     __syncwarp();
+  } else if (ACT == JATTN_SOFTMAX) {
+    // ------------------------------------------------------------ LSE / Di staging (warps 2, 3)
+    // Per step: -LSE log2(e) and -Di of the step's 128 query rows into one of
+    // two shared-memory slots, a step ahead of the activation warpgroups, which
+    // then only wait on the slot's barrier (bounded) and release it after
+    // their dS. Rows past the sequence get 0 (their columns are masked).
+    const int t = threadIdx.x - 64;  // 0 .. 63: rows t and t + 64 of each step
+    uint32_t st = 0;
+    bool ok = true;
+    BwdItem it;
+    for (long long r = 0; ok && load_bwd_item(a, r, it); ++r) {
+      for (int i = it.lo; i < it.hi; ++i, ++st) {
+        const int slot = st & 1;
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->ld_empty[slot], ((st >> 1) & 1) ^ 1, abort_flag, a, 65));
+        if (!ok) break;
+        float l2[2] = {0.0f, 0.0f}, dd[2] = {0.0f, 0.0f};
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {  // all four loads in flight before the stores
+          const int iq = i * kTile + t + 64 * k2;
+          if (iq < it.lq) {
+            const int64_t gi = (it.q0 + iq) * a.H + it.h;
+            l2[k2] = a.f0[gi] * kLog2e;
+            dd[k2] = a.f1[gi];
+          }
+        }
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {  // stored negated: the activation adds them pairwise
+          s_lse[slot * kTile + t + 64 * k2] = -l2[k2];
+          s_di[slot * kTile + t + 64 * k2] = -dd[k2];
+        }
+        mbar_arrive(&bars->ld_full[slot]);
+      }
+    }
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kActRegs));
@@ -394,28 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tSg = tmem + lane_base + C::kSCol + kCols * g;
     const uint32_t tDPg = tmem + lane_base + C::kDPCol + kCols * g;
-    uint32_t s_cnt = 0, acc_cnt = 0, step = 0, grp_phase = 0, lgrp_phase = 0;
-    // LSE (log2 units) and Di of query row i*128 + 64g + gt (gt < 64) of an
-    // item, loaded into registers one step before they are needed.
-    auto fetch = [&](const BwdItem& x, int i, float& l2, float& dd) {
-      l2 = 0.0f;
-      dd = 0.0f;
-      if constexpr (ACT == JATTN_SOFTMAX) {
-        const int iq = i * kTile + kCols * g + gt;
-        if (gt < kCols && iq < x.lq) {
-          const int64_t gi = (x.q0 + iq) * a.H + x.h;
-          l2 = a.f0[gi] * kLog2e;
-          dd = a.f1[gi];
-        }
-      }
-    };
-    float pf_l2 = 0.0f, pf_dd = 0.0f;
-    long long pf_item = -1;  // round whose first step the prefetched values belong to
+    uint32_t s_cnt = 0, acc_cnt = 0, step = 0, grp_phase = 0;
     BwdItem it, nit;
     bool have = load_bwd_item(a, 0, it), have_next = false;
     for (long long r = 0; have; ++r, it = nit, have = have_next) {
       have_next = load_bwd_item(a, r + 1, nit);
-      if (it.hi > it.lo && pf_item != r) fetch(it, it.lo, pf_l2, pf_dd);
       const int jl = it.rt * kTile + row;  // sequence-local key row of this thread
       const bool valid = jl < it.lkv;
       const int delta = it.lkv - it.lq;
@@ -428,22 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = it.lo; i < it.hi; ++i, ++step) {
         float* lse_buf = s_lse + (step & 1) * kTile + kCols * g;
         float* di_buf = s_di + (step & 1) * kTile + kCols * g;
-        if constexpr (ACT == JATTN_SOFTMAX) {
-          if (gt < kCols) {  // stored negated: the activation adds them pairwise
-            lse_buf[gt] = -pf_l2;
-            di_buf[gt] = -pf_dd;
-          }
-          if (i + 1 < it.hi) {
-            fetch(it, i + 1, pf_l2, pf_dd);
-          } else if (have_next && nit.hi > nit.lo) {
-            fetch(nit, nit.lo, pf_l2, pf_dd);
-            pf_item = r + 1;
-          }
-          // the group's 128 threads have published this step's values (bounded meeting)
-          if (!group_sync(&bars->lgrp[g], lgrp_phase, abort_flag, a, 64)) {
-            ok = false;
-            break;
-          }
+        if constexpr (ACT == JATTN_SOFTMAX) {  // this step's LSE / Di slot is filled
+          ok = __all_sync(0xffffffffu, wait_bar(&bars->ld_full[step & 1], (step >> 1) & 1, abort_flag, a, 64));
+          if (!ok) break;
         }
         ok = wait_bar(&bars->s_full, s_cnt & 1, abort_flag, a, 60);
         ok = __all_sync(0xffffffffu, ok);
@@ -578,6 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->ds_ready);
+        if constexpr (ACT == JATTN_SOFTMAX) mbar_arrive(&bars->ld_empty[step & 1]);
       }
       if (!ok) break;
       const float cn = (ACT != JATTN_SOFTMAX && a.norm_by_lkv && it.lkv > 0) ? 1.0f / it.lkv : 1.0f;
@@ -660,13 +666,15 @@ struct DqBars {
 static_assert(sizeof(DqBars) <= 256, "barrier block overflows its slot");
 static_assert(DqCfg<128>::kSmemBytes <= 227 * 1024 && DqCfg<64>::kSmemBytes <= 227 * 1024, "shared memory");
 
-template <int D, int ACT>
+template <int D, int ACT, bool IN_TILE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
               const __grid_constant__ CUtensorMap tmO, const AttnArgs a) {
   using C = DqCfg<D>;
   constexpr bool kHilo = JATTN_HILO && ACT != JATTN_SOFTMAX;  // dS as bf16 hi + lo parts
+  // IN_TILE (softmax, a.in_tile_stats): statistics and Di from the single key
+  // tile of every item, compiled apart so the general path carries none of it
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned tiles and no slack for realigning: a misaligned base is an error
   if (smem_u32(smem_raw) & 1023u) {
@@ -681,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->qd_full, 1);
     // softmax: the Di warps read dO from this buffer too, so they also release it
-    mbar_init(&bars->qd_empty, (ACT == JATTN_SOFTMAX && !a.in_tile_stats) ? 1 + 64 : 1);
+    mbar_init(&bars->qd_empty, (ACT == JATTN_SOFTMAX && !IN_TILE) ? 1 + 64 : 1);
     for (int x = 0; x < 4; ++x) mbar_init(&bars->xbar[x], 64);
     mbar_init(&bars->ot_full, 1);
     mbar_init(&bars->ot_empty, 64);
@@ -733,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sm + C::kDOOff + c * kTile * 128, &tmDO, &bars->qd_full, it.h * D + c * 64, yq);
           }
           q_armed = true;
-          if (ACT == JATTN_SOFTMAX && !a.in_tile_stats) {  // O tile for the Di warps
+          if (ACT == JATTN_SOFTMAX && !IN_TILE) {  // O tile for the Di warps
             if (!(ok = wait_bar(&bars->ot_empty, (item_cnt - 1) & 1 ^ 1, abort_flag, a, 72))) break;
             mbar_arrive_expect_tx(&bars->ot_full, C::kTileBytes);
             for (int c = 0; c < D / 64; ++c)
@@ -753,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (q_armed) drain_wait(&bars->qd_full, (item_cnt - 1) & 1, a.timeout_ns);
-      if (q_armed && ACT == JATTN_SOFTMAX && !a.in_tile_stats)
+      if (q_armed && ACT == JATTN_SOFTMAX && !IN_TILE)
         drain_wait(&bars->ot_full, (item_cnt - 1) & 1, a.timeout_ns);
       for (uint32_t i = (kv_it > (uint32_t)C::kStages ? kv_it - C::kStages : 0); i < kv_it; ++i)
         drain_wait(&bars->kv_full[i % C::kStages], (i / C::kStages) & 1, a.timeout_ns);
@@ -834,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(&bars->drain, 0, a.timeout_ns);
     }
     __syncwarp();
-  } else if (ACT == JATTN_SOFTMAX && !a.in_tile_stats) {
+  } else if (ACT == JATTN_SOFTMAX && !IN_TILE) {
     // ------------------------------------------------------------ Di warps (2, 3)
     // Di = rowsum(dO * O) for each item's 128 query rows, from the dO tile the
     // producer loaded for the MMAs and an O tile loaded for this purpose: into a
@@ -940,7 +948,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float lse2 = 0.0f, di = 0.0f;
       const bool single = it.hi - it.lo == 1;  // softmax: Di (and with in-tile stats, LSE) from the tile
       if constexpr (ACT == JATTN_SOFTMAX) {
-        if (it.hi > it.lo && !a.in_tile_stats) {  // items without a key tile use no Di and get no slot
+        if (it.hi > it.lo && !IN_TILE) {  // items without a key tile use no Di and get no slot
           // Di and LSE of this row from the Di warps' slot for this item
           const int slot = di_item & 1;
           bool okd = wait_bar(&bars->di_full[slot], (di_item >> 1) & 1, abort_flag, a, 94);
@@ -1008,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p[c + 1] = v1;
           }
         };
-        if (ACT == JATTN_SOFTMAX && a.in_tile_stats) {
+        if (ACT == JATTN_SOFTMAX && IN_TILE) {
           // the row's whole key range lies in this tile: its maximum and sum
           // come from the two groups' halves, P = exp(s - m) / l exactly
           float mx = -INFINITY;
@@ -1062,7 +1070,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float part = 0.0f;
 #pragma unroll
             for (int k = 0; k < kCols / 32; ++k) {
-              if (skip[k] && !a.in_tile_stats) continue;  // chunk not computed: P is zero there
+              if (skip[k] && !IN_TILE) continue;  // chunk not computed: P is zero there
 #pragma unroll
               for (int c = 32 * k; c < 32 * k + 32; ++c) part = fmaf(p[c], __uint_as_float(dp[c]), part);
             }
@@ -1070,7 +1078,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             if (g == 0 && valid) {
               a.f1[gi] = di;
-              if (a.in_tile_stats) a.f0[gi] = row_lse;
+              if (IN_TILE) a.f0[gi] = row_lse;
             }
           }
           const uint64_t ndi2 = f2(-di, -di);
@@ -1135,7 +1143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (valid) {
         uint4* d = reinterpret_cast<uint4*>(dq_half);
         for (int e = 0; e < D / 16; ++e) d[e] = make_uint4(0, 0, 0, 0);
-        if (ACT == JATTN_SOFTMAX && a.in_tile_stats && g == 0) {  // a row that sees no key
+        if (ACT == JATTN_SOFTMAX && IN_TILE && g == 0) {  // a row that sees no key
           a.f0[gi] = -INFINITY;
           a.f1[gi] = 0.0f;
         }
@@ -1211,8 +1219,15 @@ cudaError_t launch_bwd_dq(int D, int act, bool hilo, const CUtensorMap& q, const
   if (hilo && act != JATTN_SOFTMAX) return launch_bwd_dq_hilo(D, act, q, k, v, dout, o, a, grid, stream);
   // the O tile for Di is only needed (and its shared memory only taken) for softmax
   if (act == JATTN_SOFTMAX)
-    return D == 128 ? launch5(dq_kernel<128, JATTN_SOFTMAX>, DqCfg<128>::kSmemBytes, q, k, v, dout, o, a, grid, stream)
-                    : launch5(dq_kernel<64, JATTN_SOFTMAX>, DqCfg<64>::kSmemBytes, q, k, v, dout, o, a, grid, stream);
+    return a.in_tile_stats
+               ? (D == 128 ? launch5(dq_kernel<128, JATTN_SOFTMAX, true>, DqCfg<128>::kSmemBytes, q, k, v, dout, o, a,
+                                     grid, stream)
+                           : launch5(dq_kernel<64, JATTN_SOFTMAX, true>, DqCfg<64>::kSmemBytes, q, k, v, dout, o, a,
+                                     grid, stream))
+               : (D == 128 ? launch5(dq_kernel<128, JATTN_SOFTMAX>, DqCfg<128>::kSmemBytes, q, k, v, dout, o, a, grid,
+                                     stream)
+                           : launch5(dq_kernel<64, JATTN_SOFTMAX>, DqCfg<64>::kSmemBytes, q, k, v, dout, o, a, grid,
+                                     stream));
 #endif
   if (D == 128) {
     constexpr int sm = DqCfg<128>::kOOff;
