@@ -597,11 +597,10 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
     a.rope_rows = static_cast<int>(rope_rows);
   }
   float* di = (p->act == JATTN_SOFTMAX) ? reinterpret_cast<float*>(base + L.di) : nullptr;
-  CUtensorMap mq, mk, mv, mdo, mdk, mdv, mo;
+  CUtensorMap mq, mk, mv, mdo, mo;
   std::memset(&mo, 0, sizeof(mo));  // softmax only: the O tiles the dQ pass reads for Di
   if (make_map(&mq, q, p->total_q, p->H, p->D) || make_map(&mk, k, p->total_kv, p->H, p->D) ||
       make_map(&mv, v, p->total_kv, p->H, p->D) || make_map(&mdo, dout, p->total_q, p->H, p->D) ||
-      make_map(&mdk, dk, p->total_kv, p->H, p->D) || make_map(&mdv, dv, p->total_kv, p->H, p->D) ||
       (p->act == JATTN_SOFTMAX && !in_tile && make_map(&mo, o, p->total_q, p->H, p->D)))
     return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   // in-tile statistics: the dQ pass writes LSE and Di into the workspace for the dK/dV pass
@@ -635,7 +634,7 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
     a.out1 = reinterpret_cast<__nv_bfloat16*>(dv);
     a.out_v8 = aligned32(dk) && aligned32(dv);
     prof(2, st);
-    if ((e = launch_bwd_dkdv(p->D, p->act, hilo_for(*p), mq, mk, mv, mdo, mdk, mdv, a, grid_for(dev, L.tiles_kv, p->H), st)) !=
+    if ((e = launch_bwd_dkdv(p->D, p->act, hilo_for(*p), mq, mk, mv, mdo, a, grid_for(dev, L.tiles_kv, p->H), st)) !=
         cudaSuccess)
       return cuda_fail("dK/dV kernel launch", e);
     prof(3, st);

@@ -12,15 +12,17 @@
 //         runs first and the dK/dV pass reads Di.
 //   dkdv  one item = (sequence, 128-key tile, head); walks the query tiles
 //         that can see it: S^T = K Q^T, dP^T = V dO^T, P^T and dS^T from the
-//         activation, dV += P^T dO, dK += dS^T Q (all accumulated in TMEM);
-//         whole tiles of dK and dV leave through shared memory and TMA stores
+//         activation, dV += P^T dO, dK += dS^T Q (all accumulated in TMEM)
 // Both MMA kernels are persistent and warp-specialised: warp 0 issues TMA
 // copies, warp 1 issues tcgen05 MMAs, and two activation warpgroups (warps
 // 4-7 and 8-11; one TMEM lane per thread) split every 128-column score tile
 // in halves, apply the activation and its derivative, and write P / dS back
 // to TMEM as bf16 in their own column ranges, where the next MMA reads them
 // as its A operand. Two warps per scheduler hide the latency of the
-// transcendental and conversion instructions that one warp cannot.
+// transcendental and conversion instructions that one warp cannot. An
+// epilogue warpgroup (warps 12-15) drains each item's accumulators (dQ, or
+// dV then dK, each released to the MMAs as soon as it is read) while the
+// activation warpgroups already work on the next item.
 #include <cstdint>
 
 #include <type_traits>
@@ -40,11 +42,22 @@ namespace jattn {
 
 namespace {
 
-constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 2-3 Di (dQ) or LSE / Di staging (dK/dV; softmax), warps 4-11 activation
-// Register split (setmaxnreg, per warpgroup): 384 x 168 at launch = 64512 =
-// 128 x 104 (control warpgroup) + 256 x 200 (activation warpgroups).
+// warp 0 TMA, warp 1 MMA, warps 2-3 Di (dQ) or LSE / Di staging (dK/dV;
+// softmax), warps 4-11 activation, warps 12-15 epilogue
+constexpr int kThreads = 512;
+// Register split (setmaxnreg, per warpgroup): 512 x 128 at launch = 65536 =
+// 128 x control + 256 x activation + 128 x epilogue, shares that compile
+// without spills: the hi + lo kernels' MMA issuer needs more, their
+// activation less.
+#if JATTN_HILO
 constexpr int kCtlRegs = 104;
-constexpr int kActRegs = 200;
+constexpr int kActRegs = 168;
+#else
+constexpr int kCtlRegs = 88;
+constexpr int kActRegs = 176;
+#endif
+constexpr int kEpiRegs = 72;
+static_assert(128 * kCtlRegs + 256 * kActRegs + 128 * kEpiRegs <= 65536, "register split");
 constexpr int kNG = 2;          // activation warpgroups; they split each score tile's columns
 constexpr int kCols = kTile / kNG;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -105,51 +118,28 @@ __device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, volat
   return __all_sync(0xffffffffu, ok);
 }
 
-// Epilogue of a tile whose 128 rows all lie inside the sequence: NCH chunks of
-// 64 accumulator columns. Each thread packs its row of a chunk into the
-// warpgroup's 16 KB staging buffer in the 128-byte-swizzled layout of the
-// tensor map (16-byte piece c of row r at piece c ^ (r mod 8)), and one thread
-// stores the 128 x 64 box with TMA: whole lines instead of one row per thread.
-// The accumulators are released as soon as they are read.
-template <int NCH>
-__device__ __forceinline__ bool staged_store(uint32_t tacc, float mul, uint8_t* stage, int row, bool leader,
-                                             const CUtensorMap* map, int x0, int y0, uint64_t* grp,
-                                             uint32_t& phase, uint64_t* acc_empty, volatile int* abort_flag,
-                                             const AttnArgs& a, int where, const float* rc, const float* rs) {
-  const uint32_t srow = smem_u32(stage) + row * 128;
-#pragma unroll
-  for (int hc = 0; hc < NCH; ++hc) {
-    uint32_t v[64];
-    tmem_ld32(tacc + hc * 64, *reinterpret_cast<uint32_t(*)[32]>(v));
-    tmem_ld32(tacc + hc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+// Epilogue warpgroup: each thread stores its accumulator row, D/32 chunks of
+// 32 columns read, rotated back (rc != nullptr), scaled and written with
+// 32-byte stores; `release` is arrived once every column is read. (Staging
+// whole tiles through shared memory for TMA stores, as the activation warps
+// once did, made this warpgroup slow enough to stall the next item's MMAs.)
+template <int D>
+__device__ __forceinline__ void epi_rows(uint32_t tacc, float mul, __nv_bfloat16* dst, bool valid, uint64_t* release,
+                                         const AttnArgs& a, const float* rc, const float* rs) {
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(tacc + c * 32, v);
     tmem_ld_wait();
-    if (rc != nullptr) {  // rotary backward: columns hc*64 .. hc*64+63 are pairs hc*32 ..
-      const int64_t st = a.rope_rows;
-      rope_back16(v, rc + hc * 32 * st, rs + hc * 32 * st, a.rope_rows);
-      rope_back16(v + 32, rc + (hc * 32 + 16) * st, rs + (hc * 32 + 16) * st, a.rope_rows);
-    }
-    if (hc == NCH - 1) {
+    if (c == D / 32 - 1) {
       tc_fence_before();
-      mbar_arrive(acc_empty);
+      mbar_arrive(release);
     }
-    if (leader) bulk_wait_read_all();  // the previous store from this buffer has read it
-    if (!group_sync(grp, phase, abort_flag, a, where)) return false;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        w[e] = pack_bf16x2(__uint_as_float(v[8 * ch + 2 * e]) * mul, __uint_as_float(v[8 * ch + 2 * e + 1]) * mul);
-      st_shared_v4(srow + ((ch ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
-    }
-    fence_proxy_async_smem();
-    if (!group_sync(grp, phase, abort_flag, a, where)) return false;
-    if (leader) {
-      tma_store_2d(map, stage, x0 + hc * 64, y0);
-      bulk_commit();
-    }
+    if (rc != nullptr)
+      rope_back16(v, rc + static_cast<int64_t>(16 * c) * a.rope_rows, rs + static_cast<int64_t>(16 * c) * a.rope_rows,
+                  a.rope_rows);
+    if (valid) store_row32(dst + c * 32, v, mul, a.out_v8);
   }
-  return true;
 }
 
 struct BwdItem {
@@ -189,19 +179,16 @@ struct DkdvCfg {
   static constexpr int kQOff = 2 * kTileBytes;                               // stage s: Q, then dO
   static constexpr int kLseOff = 2 * kTileBytes + kStages * 2 * kTileBytes;  // [2][128] lse2, [2][128] Di
   static constexpr int kBarOff = kLseOff + 4 * kTile * 4;
-  // D = 128: epilogue staging for TMA stores, 16 KB per activation warpgroup
-  static constexpr bool kTmaStore = (D == 128);
-  static constexpr int kStageOff = (kBarOff + 256 + 1023) / 1024 * 1024;
-  static constexpr int kSmemBytes = kStageOff + (kTmaStore ? 2 * 16384 : 0);  // base 1024-aligned (checked)
+  static constexpr int kSmemBytes = kBarOff + 256;  // base 1024-aligned (checked)
   static constexpr uint32_t kSCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
 };
 
 struct DkdvBars {
   uint64_t kv_full, kv_empty;
   uint64_t qd_full[3], qd_empty[3];
-  uint64_t s_full, dp_full, p_ready, ds_ready, acc_full, acc_empty;
+  uint64_t s_full, dp_full, p_ready, ds_ready;
+  uint64_t dv_full, dk_full, dv_empty, dk_empty;  // accumulators handed to / back from the epilogue warpgroup
   uint64_t drain;
-  uint64_t grp[2];  // activation warpgroup meeting points (epilogue staging)
   uint64_t ld_full[2], ld_empty[2];  // per-step LSE / Di slots (softmax), filled by warps 2-3
   uint32_t tmem_base;
   int abort_flag;
@@ -213,9 +200,7 @@ static_assert(DkdvCfg<128>::kSmemBytes <= 227 * 1024 && DkdvCfg<64>::kSmemBytes 
 template <int D, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
-                const AttnArgs a) {
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const AttnArgs a) {
   using C = DkdvCfg<D>;
   constexpr bool kHilo = JATTN_HILO && ACT != JATTN_SOFTMAX;  // P and dS as bf16 hi + lo parts
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -242,11 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_ready, kNG * kTile);
     mbar_init(&bars->ds_ready, kNG * kTile);
-    mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, kNG * kTile);
+    mbar_init(&bars->dv_full, 1);
+    mbar_init(&bars->dk_full, 1);
+    mbar_init(&bars->dv_empty, kTile);  // the epilogue warpgroup's threads
+    mbar_init(&bars->dk_empty, kTile);
     mbar_init(&bars->drain, 1);
-    mbar_init(&bars->grp[0], kTile);
-    mbar_init(&bars->grp[1], kTile);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars->ld_full[x], 64);
       mbar_init(&bars->ld_empty[x], kNG * kTile);
@@ -347,9 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = qd_it % C::kStages;
           const bool more = i + 1 < it.hi;
           const int s1 = (qd_it + 1) % C::kStages;
-          if (i == it.lo) {
-            if (!(ok = wait_bar(&bars->acc_empty, (acc_cnt & 1) ^ 1, abort_flag, a, 52))) break;
-          }
+          // the epilogue warpgroup has read the previous item's dV (dK below)
+          if (i == it.lo && !(ok = wait_bar(&bars->dv_empty, (acc_cnt & 1) ^ 1, abort_flag, a, 52))) break;
           if (!(ok = wait_bar(&bars->p_ready, p_cnt & 1, abort_flag, a, 53))) break;
           ++p_cnt;
           tc_fence_after();
@@ -360,11 +344,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // unnormalised pointwise: P^T's lo parts, 32 columns after the hi parts
             if constexpr (kHilo) mma_ts(tmem + C::kDVCol, split_a(tmem + C::kSCol + 32, kk), bd, idAcc, 1u);
           }
+          if (!more) mma_commit(&bars->dv_full);  // the item's dV is complete
           if (more) {
             if (!(ok = wait_bar(&bars->qd_full[s1], ((qd_it + 1) / C::kStages) & 1, abort_flag, a, 54))) break;
             tc_fence_after();
             issue_s(s1);
           }
+          if (i == it.lo && !(ok = wait_bar(&bars->dk_empty, (acc_cnt & 1) ^ 1, abort_flag, a, 56))) break;
           if (!(ok = wait_bar(&bars->ds_ready, ds_cnt & 1, abort_flag, a, 55))) break;
           ++ds_cnt;
           tc_fence_after();
@@ -380,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i + 2 == it.hi) mma_commit(&bars->kv_empty);
         }
         if (!ok) break;
-        mma_commit(&bars->acc_full);
+        mma_commit(&bars->dk_full);
         ++acc_cnt;
       }
       mma_commit(&bars->drain);
@@ -421,15 +407,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  } else {
+  } else if (warp < 12) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kActRegs));
     const int g = (warp - 4) >> 2;                   // activation group: score columns [64g, 64g+64)
-    const int gt = threadIdx.x - 128 - kTile * g;    // 0..127 within the group
     const int row = 32 * (warp & 3) + lane;          // TMEM lane == key row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tSg = tmem + lane_base + C::kSCol + kCols * g;
     const uint32_t tDPg = tmem + lane_base + C::kDPCol + kCols * g;
-    uint32_t s_cnt = 0, acc_cnt = 0, step = 0, grp_phase = 0;
+    uint32_t s_cnt = 0, step = 0;
     BwdItem it, nit;
     bool have = load_bwd_item(a, 0, it), have_next = false;
     for (long long r = 0; have; ++r, it = nit, have = have_next) {
@@ -440,8 +425,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ilo, ihi;
       query_interval(jl, delta, it.lq, a.mask, a.window, ilo, ihi);
       if (!valid) ihi = ilo;  // rows past the sequence contribute nothing
-      const int64_t gk = it.k0 + jl;
-      __nv_bfloat16* out_row = (g == 0 ? a.out1 : a.out0) + (gk * a.H + it.h) * D;  // group 0: dV, 1: dK
       bool ok = true;
       for (int i = it.lo; i < it.hi; ++i, ++step) {
         float* lse_buf = s_lse + (step & 1) * kTile + kCols * g;
@@ -586,48 +569,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (ACT == JATTN_SOFTMAX) mbar_arrive(&bars->ld_empty[step & 1]);
       }
       if (!ok) break;
-      const float cn = (ACT != JATTN_SOFTMAX && a.norm_by_lkv && it.lkv > 0) ? 1.0f / it.lkv : 1.0f;
-      if (it.hi > it.lo) {
-        ok = wait_bar(&bars->acc_full, acc_cnt & 1, abort_flag, a, 62);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        ++acc_cnt;
-        tc_fence_after();
-        const uint32_t tAcc = tmem + lane_base + (g == 0 ? C::kDVCol : C::kDKCol);
-        const float mul = (g == 0) ? cn : cn * a.scale;
-        const float* rc = nullptr;  // rotary backward of dK (group 1)
-        const float* rs = nullptr;
-        if (g == 1 && valid) rope_rows_at(a, rope_pos_k(jl, delta), rc, rs);
-        bool staged = false;
-        if constexpr (C::kTmaStore) {
-          if ((it.rt + 1) * kTile <= it.lkv) {  // every key row of the tile is in the sequence
-            staged = true;
-            ok = staged_store<D / 64>(tAcc, mul, sm + C::kStageOff + g * 16384, row, gt == 0, g == 0 ? &tmO1 : &tmO0,
-                                      it.h * D, static_cast<int>(it.k0) + it.rt * kTile, &bars->grp[g], grp_phase,
-                                      &bars->acc_empty, abort_flag, a, 63, rc, rs);
-            if (!ok) break;
-          }
-        }
-        if (!staged) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tAcc + c * 32, v);
-            tmem_ld_wait();
-            if (rc != nullptr)
-              rope_back16(v, rc + static_cast<int64_t>(16 * c) * a.rope_rows,
-                          rs + static_cast<int64_t>(16 * c) * a.rope_rows, a.rope_rows);
-            if (valid) store_row32(out_row + c * 32, v, mul, a.out_v8);
-          }
-          tc_fence_before();
-          mbar_arrive(&bars->acc_empty);
-        }
-      } else if (valid) {
-        zero_row(out_row, D);
-      }
     }
-    // the stores this thread started complete before the CTA's shared memory goes away
-    if (C::kTmaStore && gt == 0) bulk_wait_all();
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
+    // ------------------------------------------------------------ epilogue warpgroup (warps 12-15)
+    // Drains each item's dV and dK while the activation warpgroups start the
+    // next item; items that no query sees get zero rows.
+    const int row = 32 * (warp & 3) + lane;  // TMEM lane == key row of the tile
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    uint32_t acc_cnt = 0;
+    BwdItem it;
+    for (long long r = 0; load_bwd_item(a, r, it); ++r) {
+      const int jl = it.rt * kTile + row;
+      const bool valid = jl < it.lkv;
+      const int64_t gk = it.k0 + jl;
+      __nv_bfloat16* dv_row = a.out1 + (gk * a.H + it.h) * D;
+      __nv_bfloat16* dk_row = a.out0 + (gk * a.H + it.h) * D;
+      if (it.hi <= it.lo) {
+        if (valid) {
+          zero_row(dv_row, D);
+          zero_row(dk_row, D);
+        }
+        continue;
+      }
+      const float cn = (ACT != JATTN_SOFTMAX && a.norm_by_lkv && it.lkv > 0) ? 1.0f / it.lkv : 1.0f;
+      if (!__all_sync(0xffffffffu, wait_bar(&bars->dv_full, acc_cnt & 1, abort_flag, a, 62))) break;
+      tc_fence_after();
+      epi_rows<D>(tmem + lane_base + C::kDVCol, cn, dv_row, valid, &bars->dv_empty, a, nullptr, nullptr);
+      const float* rc = nullptr;  // rotary backward of dK
+      const float* rs = nullptr;
+      if (valid) rope_rows_at(a, rope_pos_k(jl, it.lkv - it.lq), rc, rs);
+      if (!__all_sync(0xffffffffu, wait_bar(&bars->dk_full, acc_cnt & 1, abort_flag, a, 66))) break;
+      ++acc_cnt;
+      tc_fence_after();
+      epi_rows<D>(tmem + lane_base + C::kDKCol, cn * a.scale, dk_row, valid, &bars->dk_empty, a, rc, rs);
+    }
   }
 
   tc_fence_before();
@@ -702,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->ds_ready, kNG * kTile);
     mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, kNG * kTile);
+    mbar_init(&bars->acc_empty, kTile);  // the epilogue warpgroup's threads
     for (int s2 = 0; s2 < 2; ++s2) {
       mbar_init(&bars->di_full[s2], 64);
       mbar_init(&bars->di_empty[s2], kNG * kTile);
@@ -872,7 +848,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int il = it.rt * kTile + 64 * dw + 32 * h2 + lane;
         lse_rows[h2] = (il < it.lq) ? a.f0[(it.q0 + il) * a.H + it.h] : 0.0f;
       }
-#pragma unroll
       const bool single = it.hi - it.lo == 1;
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
@@ -907,14 +882,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n_item;
     }
   }
-  } else {
+  } else if (warp < 12) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kActRegs));
     const int g = (warp - 4) >> 2;                  // activation group: score columns [64g, 64g+64)
     const int row = 32 * (warp & 3) + lane;         // TMEM lane == query row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tDPg = tmem + lane_base + C::kDPCol + kCols * g;
     const int quarter = warp & 3;
-    uint32_t step = 0, dp_cnt = 0, acc_cnt = 0, di_item = 0, x_cnt = 0;
+    uint32_t step = 0, dp_cnt = 0, di_item = 0, x_cnt = 0;
     // Row exchange with the partner warp of the other group (same TMEM lanes):
     // each writes its value into column k of its own half of the current S
     // buffer, whose scores it has already read, they meet on the quarter's
@@ -964,7 +939,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      __nv_bfloat16* dq_half = a.out0 + gi * D + (D / 2) * g;  // group g stores dQ columns [gD/2, (g+1)D/2)
       bool ok = true;
       for (int j = it.lo; j < it.hi; ++j, ++step) {
         ok = wait_bar(&bars->s_full[step & 1], (step >> 1) & 1, abort_flag, a, 90);
@@ -1116,38 +1090,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars->ds_ready);
       }
       if (!ok) break;
-      const float cn = (ACT != JATTN_SOFTMAX && a.norm_by_lkv && it.lkv > 0) ? 1.0f / it.lkv : 1.0f;
-      if (it.hi > it.lo) {
-        ok = wait_bar(&bars->acc_full, acc_cnt & 1, abort_flag, a, 92);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        ++acc_cnt;
-        tc_fence_after();
-        const float* rc = nullptr;  // rotary backward of dQ
-        const float* rs = nullptr;
-        if (valid) rope_rows_at(a, rope_pos_q(il, it.lkv - it.lq), rc, rs);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + C::kDQCol + (D / 2) * g + c * 32, v);
-          tmem_ld_wait();
-          // columns (D/2) g + 32 c .. are pairs (D/4) g + 16 c ..
-          if (rc != nullptr) {
-            const int64_t m0 = (D / 4) * g + 16 * c;
-            rope_back16(v, rc + m0 * a.rope_rows, rs + m0 * a.rope_rows, a.rope_rows);
+    }
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
+    // ------------------------------------------------------------ epilogue warpgroup (warps 12-15)
+    // Drains each item's dQ (one row per thread, rotated back when asked)
+    // while the activation warpgroups start the next item; rows that see no
+    // key get zeros (and, with in-tile statistics, LSE = -inf and Di = 0).
+    const int row = 32 * (warp & 3) + lane;  // TMEM lane == query row of the tile
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    uint32_t acc_cnt = 0;
+    BwdItem it;
+    for (long long r = 0; load_bwd_item(a, r, it); ++r) {
+      const int il = it.rt * kTile + row;
+      const bool valid = il < it.lq;
+      const int64_t gi = (it.q0 + il) * a.H + it.h;
+      __nv_bfloat16* dq_row = a.out0 + gi * D;
+      if (it.hi <= it.lo) {
+        if (valid) {
+          zero_row(dq_row, D);
+          if (ACT == JATTN_SOFTMAX && IN_TILE) {
+            a.f0[gi] = -INFINITY;
+            a.f1[gi] = 0.0f;
           }
-          if (valid) store_row32(dq_half + c * 32, v, cn * a.scale, a.out_v8);
         }
-        tc_fence_before();
-        mbar_arrive(&bars->acc_empty);
-      } else if (valid) {
-        uint4* d = reinterpret_cast<uint4*>(dq_half);
-        for (int e = 0; e < D / 16; ++e) d[e] = make_uint4(0, 0, 0, 0);
-        if (ACT == JATTN_SOFTMAX && IN_TILE && g == 0) {  // a row that sees no key
-          a.f0[gi] = -INFINITY;
-          a.f1[gi] = 0.0f;
-        }
+        continue;
       }
+      const float cn = (ACT != JATTN_SOFTMAX && a.norm_by_lkv && it.lkv > 0) ? 1.0f / it.lkv : 1.0f;
+      const float* rc = nullptr;  // rotary backward of dQ
+      const float* rs = nullptr;
+      if (valid) rope_rows_at(a, rope_pos_q(il, it.lkv - it.lq), rc, rs);
+      if (!__all_sync(0xffffffffu, wait_bar(&bars->acc_full, acc_cnt & 1, abort_flag, a, 92))) break;
+      ++acc_cnt;
+      tc_fence_after();
+      epi_rows<D>(tmem + lane_base + C::kDQCol, cn * a.scale, dq_row, valid, &bars->acc_empty, a, rc, rs);
     }
   }
 
@@ -1166,12 +1142,11 @@ cudaError_t launch5(K kern, int smem, const CUtensorMap& q, const CUtensorMap& k
 }
 
 template <typename K>
-cudaError_t launch6(K kern, int smem, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                    const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1, const AttnArgs& a,
-                    int grid, cudaStream_t stream) {
+cudaError_t launch4(K kern, int smem, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                    const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(q, k, v, dout, o0, o1, a);
+  kern<<<grid, kThreads, smem, stream>>>(q, k, v, dout, a);
   return cudaGetLastError();
 }
 
@@ -1179,32 +1154,32 @@ cudaError_t launch6(K kern, int smem, const CUtensorMap& q, const CUtensorMap& k
 
 #if JATTN_HILO
 cudaError_t launch_bwd_dkdv_hilo(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                 const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1,
-                                 const AttnArgs& a, int grid, cudaStream_t stream) {
+                                 const CUtensorMap& dout, const AttnArgs& a, int grid,
+                                 cudaStream_t stream) {
 #else
 cudaError_t launch_bwd_dkdv(int D, int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k,
-                            const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1,
-                            const AttnArgs& a, int grid, cudaStream_t stream) {
-  if (hilo && act != JATTN_SOFTMAX) return launch_bwd_dkdv_hilo(D, act, q, k, v, dout, o0, o1, a, grid, stream);
+                            const CUtensorMap& v, const CUtensorMap& dout, const AttnArgs& a, int grid,
+                            cudaStream_t stream) {
+  if (hilo && act != JATTN_SOFTMAX) return launch_bwd_dkdv_hilo(D, act, q, k, v, dout, a, grid, stream);
   if (act == JATTN_SOFTMAX)
-    return D == 128 ? launch6(dkdv_kernel<128, JATTN_SOFTMAX>, DkdvCfg<128>::kSmemBytes, q, k, v, dout, o0, o1, a,
+    return D == 128 ? launch4(dkdv_kernel<128, JATTN_SOFTMAX>, DkdvCfg<128>::kSmemBytes, q, k, v, dout, a,
                               grid, stream)
-                    : launch6(dkdv_kernel<64, JATTN_SOFTMAX>, DkdvCfg<64>::kSmemBytes, q, k, v, dout, o0, o1, a, grid,
+                    : launch4(dkdv_kernel<64, JATTN_SOFTMAX>, DkdvCfg<64>::kSmemBytes, q, k, v, dout, a, grid,
                               stream);
 #endif
   if (D == 128) {
     constexpr int sm = DkdvCfg<128>::kSmemBytes;
-    if (act == JATTN_SILU) return launch6(dkdv_kernel<128, JATTN_SILU>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+    if (act == JATTN_SILU) return launch4(dkdv_kernel<128, JATTN_SILU>, sm, q, k, v, dout, a, grid, stream);
     if (act == JATTN_GELU_POLY)
-      return launch6(dkdv_kernel<128, JATTN_GELU_POLY>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+      return launch4(dkdv_kernel<128, JATTN_GELU_POLY>, sm, q, k, v, dout, a, grid, stream);
     if (act == JATTN_GELU_TANH)
-      return launch6(dkdv_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+      return launch4(dkdv_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, a, grid, stream);
     return cudaErrorInvalidValue;
   }
   constexpr int sm = DkdvCfg<64>::kSmemBytes;
-  if (act == JATTN_SILU) return launch6(dkdv_kernel<64, JATTN_SILU>, sm, q, k, v, dout, o0, o1, a, grid, stream);
-  if (act == JATTN_GELU_POLY) return launch6(dkdv_kernel<64, JATTN_GELU_POLY>, sm, q, k, v, dout, o0, o1, a, grid, stream);
-  if (act == JATTN_GELU_TANH) return launch6(dkdv_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, o0, o1, a, grid, stream);
+  if (act == JATTN_SILU) return launch4(dkdv_kernel<64, JATTN_SILU>, sm, q, k, v, dout, a, grid, stream);
+  if (act == JATTN_GELU_POLY) return launch4(dkdv_kernel<64, JATTN_GELU_POLY>, sm, q, k, v, dout, a, grid, stream);
+  if (act == JATTN_GELU_TANH) return launch4(dkdv_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, a, grid, stream);
   return cudaErrorInvalidValue;
 }
 

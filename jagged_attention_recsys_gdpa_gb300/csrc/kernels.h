@@ -44,14 +44,13 @@ cudaError_t launch_bwd_dq_mx(const CUtensorMap& q, const CUtensorMap& k, const C
 cudaError_t launch_bwd_dkdv_mx(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream);
 
-// dK, dV over key tiles (transposed schedule, 128-row key tiles). o0 / o1 map
-// dK / dV (tile stores of whole tiles).
+// dK, dV over key tiles (transposed schedule, 128-row key tiles); a.out0 /
+// a.out1 receive dK / dV.
 cudaError_t launch_bwd_dkdv(int D, int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k,
-                            const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1,
-                            const AttnArgs& a, int grid, cudaStream_t stream);
+                            const CUtensorMap& v, const CUtensorMap& dout, const AttnArgs& a, int grid,
+                            cudaStream_t stream);
 cudaError_t launch_bwd_dkdv_hilo(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                 const CUtensorMap& dout, const CUtensorMap& o0, const CUtensorMap& o1,
-                                 const AttnArgs& a, int grid, cudaStream_t stream);
+                                 const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream);
 // dQ over query tiles (128-row query tiles). For softmax it also computes
 // Di = rowsum(dO * O) from the dO tiles and O tiles (map `o`) into a.f1, so
 // it runs before the dK/dV pass, which reads Di.
