@@ -1,5 +1,6 @@
 // C-ABI entry points of libjattn: argument checks, workspace layout, TMA
 // descriptors and kernel launches on the caller's stream.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -187,6 +188,24 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int H, int D) {
 // accumulate into the same fp32 result, so their rounding does not grow with
 // the sequence length (outputs there sum thousands of unscaled terms).
 bool hilo_for(const jattn_params_t& p) { return p.act != JATTN_SOFTMAX && !p.norm_by_lkv; }
+
+// The dQ pass's K / V layout: two rings (K deeper than V) when query tiles
+// see many key tiles on average, where each tile's K latency would otherwise
+// show, one ring otherwise, where the second ring's barrier and release cost
+// more than they hide. Estimated from the mask and the mean key length: with
+// a window, min(W, L) / 128 + 1 tiles; causal, L / 256 + 1; none, L / 128 + 1.
+// Debug flag bits 8 / 16 force two rings / one ring.
+bool dq_split_rings(const jattn_params_t& p) {
+  if (g_debug_flags & 8) return true;
+  if (g_debug_flags & 16) return false;
+  if (p.B < 1 || (p.mask & JATTN_MASK_BLOCK)) return false;
+  const double lkv = static_cast<double>(p.total_kv) / static_cast<double>(p.B);
+  double tiles;
+  if (p.mask & JATTN_MASK_WINDOW) tiles = std::min(static_cast<double>(p.window), lkv) / 128.0 + 1.0;
+  else if (p.mask & JATTN_MASK_CAUSAL) tiles = lkv / 256.0 + 1.0;
+  else tiles = lkv / 128.0 + 1.0;
+  return tiles >= 6.0;
+}
 
 // 2-D view [rows, H*D] of jagged E4M3 codes (one byte each); boxes of
 // box_rows rows x 128 bytes with the 128-byte swizzle (D = 128: one box per
@@ -598,11 +617,13 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
   }
   float* di = (p->act == JATTN_SOFTMAX) ? reinterpret_cast<float*>(base + L.di) : nullptr;
   CUtensorMap mq, mk, mv, mdo, mo;
-  std::memset(&mo, 0, sizeof(mo));  // softmax only: the O tiles the dQ pass reads for Di
+  std::memset(&mo, 0, sizeof(mo));  // softmax only: the O tiles the dQ pass reads for Di (one-ring layout)
   if (make_map(&mq, q, p->total_q, p->H, p->D) || make_map(&mk, k, p->total_kv, p->H, p->D) ||
       make_map(&mv, v, p->total_kv, p->H, p->D) || make_map(&mdo, dout, p->total_q, p->H, p->D) ||
       (p->act == JATTN_SOFTMAX && !in_tile && make_map(&mo, o, p->total_q, p->H, p->D)))
     return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+  // softmax: the rows of O the dQ pass reads for Di (two-ring layout)
+  a.in0 = (p->act == JATTN_SOFTMAX && !in_tile) ? reinterpret_cast<const __nv_bfloat16*>(o) : nullptr;
   // in-tile statistics: the dQ pass writes LSE and Di into the workspace for the dK/dV pass
   a.f0 = in_tile ? reinterpret_cast<float*>(base + L.lse) : const_cast<float*>(lse);
   a.f1 = di;
@@ -619,7 +640,8 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
     a.out1 = nullptr;
     a.out_v8 = aligned32(dq);
     prof(4, st);
-    if ((e = launch_bwd_dq(p->D, p->act, hilo_for(*p), mq, mk, mv, mdo, mo, a, grid_for(dev, L.tiles_q, p->H), st)) != cudaSuccess)
+    if ((e = launch_bwd_dq(p->D, p->act, hilo_for(*p), dq_split_rings(*p), mq, mk, mv, mdo, mo, a,
+                             grid_for(dev, L.tiles_q, p->H), st)) != cudaSuccess)
       return cuda_fail("dQ kernel launch", e);
     prof(5, st);
   }

@@ -612,27 +612,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------- dQ
-template <int D>
+// Two layouts of the K / V tiles, picked per call (dq_split_rings in the
+// host code) from the key tiles an item holds on average:
+//   one ring (SPLIT = false): stage s holds K(j) and V(j), one barrier and one
+//     release per tile for the MMA issuer; the softmax Di warps also get the
+//     item's O tile in shared memory;
+//   two rings (SPLIT = true): K tiles, needed first (by S, a tile ahead) and
+//     read last (by dQ), in a deeper ring than V tiles (read by dP only). With
+//     one two-stage ring each K copy could only start once dQ had read the
+//     tile two before, so long items saw its latency on every tile; items of
+//     few tiles pay more for the extra barrier and release than they gain.
+//     The Di warps read O from global memory (prefetched into L2).
+template <int D, bool SPLIT>
 struct DqCfg {
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kKStages = SPLIT ? 3 : ((D == 128) ? 2 : 3);
+  static constexpr int kVStages = SPLIT ? ((D == 128) ? 2 : 3) : kKStages;
   static constexpr int kQOff = 0;
   static constexpr int kDOOff = kTileBytes;
-  static constexpr int kKOff = 2 * kTileBytes;  // stage s: K at kKOff + s * 2 tiles, V right after
-  static constexpr int kBarOff = 2 * kTileBytes + kStages * 2 * kTileBytes;
+  static constexpr int kKOff = 2 * kTileBytes;
+  static constexpr int kKStride = SPLIT ? kTileBytes : 2 * kTileBytes;  // K stage s at kKOff + s strides
+  static constexpr int kVOff = SPLIT ? kKOff + kKStages * kTileBytes : kKOff + kTileBytes;
+  static constexpr int kVStride = kKStride;                             // V stage s at kVOff + s strides
+  static constexpr int kBarOff = SPLIT ? kVOff + kVStages * kTileBytes : kKOff + kKStages * 2 * kTileBytes;
   // [2][128] Di, then [2][128] LSE, handed to the activation warpgroups (softmax)
   static constexpr int kDiOff = kBarOff + 256;
-  static constexpr int kOOff = (kDiOff + 4 * kTile * 4 + 1023) / 1024 * 1024;  // O tile (softmax: Di)
-  static constexpr int kSmemBytes = kOOff + kTileBytes;                        // base 1024-aligned (checked)
+  static constexpr int kOOff = (kDiOff + 4 * kTile * 4 + 1023) / 1024 * 1024;  // O tile (one ring, softmax)
+  static constexpr int kSmemBytes = SPLIT ? kDiOff + 4 * kTile * 4 : kOOff + kTileBytes;  // base 1024-aligned
   static constexpr uint32_t kSCol = 0, kDPCol = 256, kDQCol = 384;  // S double-buffered at 0 and 128
 };
 
 struct DqBars {
   uint64_t qd_full, qd_empty;
-  uint64_t kv_full[3], kv_empty[3];
+  uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
   uint64_t s_full[2], dp_full, ds_ready, acc_full, acc_empty;
   uint64_t di_full[2], di_empty[2];  // Di slots (softmax)
-  uint64_t ot_full, ot_empty;         // O tile for Di (softmax)
+  uint64_t ot_full, ot_empty;         // O tile for Di (one ring, softmax)
   uint64_t xbar[4];                   // per lane quarter: row exchange between the activation groups, 64 arrivals
   uint64_t drain;
   uint32_t tmem_base;
@@ -640,14 +655,17 @@ struct DqBars {
 };
 
 static_assert(sizeof(DqBars) <= 256, "barrier block overflows its slot");
-static_assert(DqCfg<128>::kSmemBytes <= 227 * 1024 && DqCfg<64>::kSmemBytes <= 227 * 1024, "shared memory");
+static_assert(DqCfg<128, false>::kSmemBytes <= 227 * 1024 && DqCfg<64, false>::kSmemBytes <= 227 * 1024 &&
+                  DqCfg<128, true>::kSmemBytes <= 227 * 1024 && DqCfg<64, true>::kSmemBytes <= 227 * 1024,
+              "shared memory");
 
-template <int D, int ACT, bool IN_TILE = false>
+template <int D, int ACT, bool IN_TILE, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
               const __grid_constant__ CUtensorMap tmO, const AttnArgs a) {
-  using C = DqCfg<D>;
+  using C = DqCfg<D, SPLIT>;
+  constexpr bool kOTile = ACT == JATTN_SOFTMAX && !IN_TILE && !SPLIT;  // Di from an O tile in shared memory
   constexpr bool kHilo = JATTN_HILO && ACT != JATTN_SOFTMAX;  // dS as bf16 hi + lo parts
   // IN_TILE (softmax, a.in_tile_stats): statistics and Di from the single key
   // tile of every item, compiled apart so the general path carries none of it
@@ -669,9 +687,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int x = 0; x < 4; ++x) mbar_init(&bars->xbar[x], 64);
     mbar_init(&bars->ot_full, 1);
     mbar_init(&bars->ot_empty, 64);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     mbar_init(&bars->s_full[0], 1);
     mbar_init(&bars->s_full[1], 1);
@@ -717,41 +739,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sm + C::kDOOff + c * kTile * 128, &tmDO, &bars->qd_full, it.h * D + c * 64, yq);
           }
           q_armed = true;
-          if (ACT == JATTN_SOFTMAX && !IN_TILE) {  // O tile for the Di warps
-            if (!(ok = wait_bar(&bars->ot_empty, (item_cnt - 1) & 1 ^ 1, abort_flag, a, 72))) break;
+          if constexpr (kOTile) {  // O tile for the Di warps
+            if (!(ok = wait_bar(&bars->ot_empty, ((item_cnt - 1) & 1) ^ 1, abort_flag, a, 74))) break;
             mbar_arrive_expect_tx(&bars->ot_full, C::kTileBytes);
             for (int c = 0; c < D / 64; ++c)
               tma_load_2d(sm + C::kOOff + c * kTile * 128, &tmO, &bars->ot_full, it.h * D + c * 64, yq);
           }
         }
         for (int j = it.lo; j < it.hi; ++j, ++kv_it) {
-          const int s = kv_it % C::kStages;
-          if (!(ok = wait_bar(&bars->kv_empty[s], ((kv_it / C::kStages) & 1) ^ 1, abort_flag, a, 71))) break;
+          const int sk = kv_it % C::kKStages, sv = kv_it % C::kVStages;
           const int yk = static_cast<int>(it.k0) + j * kTile;
-          mbar_arrive_expect_tx(&bars->kv_full[s], 2 * C::kTileBytes);
-          uint8_t* st = sm + C::kKOff + s * 2 * C::kTileBytes;
-          for (int c = 0; c < D / 64; ++c) {
-            tma_load_2d(st + c * kTile * 128, &tmK, &bars->kv_full[s], it.h * D + c * 64, yk);
-            tma_load_2d(st + C::kTileBytes + c * kTile * 128, &tmV, &bars->kv_full[s], it.h * D + c * 64, yk);
+          if (!(ok = wait_bar(&bars->k_empty[sk], ((kv_it / C::kKStages) & 1) ^ 1, abort_flag, a, 71))) break;
+          mbar_arrive_expect_tx(&bars->k_full[sk], (SPLIT ? 1 : 2) * C::kTileBytes);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(sm + C::kKOff + sk * C::kKStride + c * kTile * 128, &tmK, &bars->k_full[sk],
+                        it.h * D + c * 64, yk);
+          uint64_t* vbar = &bars->k_full[sk];  // one ring: V lands on its stage's barrier
+          if constexpr (SPLIT) {
+            if (!(ok = wait_bar(&bars->v_empty[sv], ((kv_it / C::kVStages) & 1) ^ 1, abort_flag, a, 72))) break;
+            vbar = &bars->v_full[sv];
+            mbar_arrive_expect_tx(vbar, C::kTileBytes);
           }
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(sm + C::kVOff + sv * C::kVStride + c * kTile * 128, &tmV, vbar, it.h * D + c * 64, yk);
         }
       }
       if (q_armed) drain_wait(&bars->qd_full, (item_cnt - 1) & 1, a.timeout_ns);
-      if (q_armed && ACT == JATTN_SOFTMAX && !IN_TILE)
-        drain_wait(&bars->ot_full, (item_cnt - 1) & 1, a.timeout_ns);
-      for (uint32_t i = (kv_it > (uint32_t)C::kStages ? kv_it - C::kStages : 0); i < kv_it; ++i)
-        drain_wait(&bars->kv_full[i % C::kStages], (i / C::kStages) & 1, a.timeout_ns);
+      if (q_armed && kOTile) drain_wait(&bars->ot_full, (item_cnt - 1) & 1, a.timeout_ns);
+      for (uint32_t i = (kv_it > (uint32_t)C::kKStages ? kv_it - C::kKStages : 0); i < kv_it; ++i)
+        drain_wait(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1, a.timeout_ns);
+      if (SPLIT)
+        for (uint32_t i = (kv_it > (uint32_t)C::kVStages ? kv_it - C::kVStages : 0); i < kv_it; ++i)
+          drain_wait(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1, a.timeout_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kTile, kTile, false, false);
       constexpr uint32_t idAcc = idesc_bf16_f32(kTile, D, false, true);
-      const uint32_t sQ = smem_u32(sm + C::kQOff), sDO = smem_u32(sm + C::kDOOff), sKV = smem_u32(sm + C::kKOff);
+      const uint32_t sQ = smem_u32(sm + C::kQOff), sDO = smem_u32(sm + C::kDOOff);
+      const uint32_t sK0 = smem_u32(sm + C::kKOff), sV0 = smem_u32(sm + C::kVOff);
       uint32_t item_cnt = 0, kv_it = 0, ds_cnt = 0, acc_cnt = 0, step = 0;
       bool ok = true;
-      auto sK = [&](int s) { return sKV + s * 2 * C::kTileBytes; };
-      auto sV = [&](int s) { return sKV + s * 2 * C::kTileBytes + C::kTileBytes; };
+      auto sK = [&](int s) { return sK0 + s * C::kKStride; };
+      auto sV = [&](int s) { return sV0 + s * C::kVStride; };
+      // the V tile of global tile t is present (two rings: its own barrier;
+      // one ring: the stage's barrier, already waited for S)
+      auto wait_v = [&](uint32_t t) {
+        if constexpr (SPLIT) {
+          if (!wait_bar(&bars->v_full[t % C::kVStages], (t / C::kVStages) & 1, abort_flag, a, 86)) return false;
+          tc_fence_after();
+        }
+        return true;
+      };
       auto kmajor = [](uint32_t base, int kk) {
         return sdesc_sw128(base + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
       };
@@ -765,6 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kDPCol, kmajor(sDO, kk), kmajor(sV(s), kk), idS, kk > 0);
         mma_commit(&bars->dp_full);
+        if constexpr (SPLIT) mma_commit(&bars->v_empty[s]);  // V(j) feeds dP(j) only
       };
       BwdItem it, nit;
       bool have = load_bwd_item(a, 0, it), have_next = false;
@@ -775,23 +816,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++item_cnt;
         tc_fence_after();
         {
-          const int s = kv_it % C::kStages;
-          if (!(ok = wait_bar(&bars->kv_full[s], (kv_it / C::kStages) & 1, abort_flag, a, 81))) break;
+          const int sk = kv_it % C::kKStages, sv = kv_it % C::kVStages;
+          if (!(ok = wait_bar(&bars->k_full[sk], (kv_it / C::kKStages) & 1, abort_flag, a, 81))) break;
           tc_fence_after();
-          issue_s(s, step);
-          issue_dp(s);
+          issue_s(sk, step);
+          if (!(ok = wait_v(kv_it))) break;
+          issue_dp(sv);
           // Q and dO feed only the S and dP products: once the item's last pair
           // has completed, the next item's Q/dO copy may land.
           if (it.hi - it.lo == 1) mma_commit(&bars->qd_empty);
         }
         for (int j = it.lo; j < it.hi; ++j, ++kv_it, ++step) {
-          const int s = kv_it % C::kStages;
+          const int s = kv_it % C::kKStages;
           const bool more = j + 1 < it.hi;
-          const int s1 = (kv_it + 1) % C::kStages;
+          const uint32_t k1 = kv_it + 1;
           if (more) {
-            if (!(ok = wait_bar(&bars->kv_full[s1], ((kv_it + 1) / C::kStages) & 1, abort_flag, a, 82))) break;
+            if (!(ok = wait_bar(&bars->k_full[k1 % C::kKStages], (k1 / C::kKStages) & 1, abort_flag, a, 82))) break;
             tc_fence_after();
-            issue_s(s1, step + 1);
+            issue_s(k1 % C::kKStages, step + 1);
           }
           if (j == it.lo) {
             if (!(ok = wait_bar(&bars->acc_empty, (acc_cnt & 1) ^ 1, abort_flag, a, 83))) break;
@@ -806,8 +848,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // unnormalised pointwise: dS's lo parts, 32 columns after the hi parts
             if constexpr (kHilo) mma_ts(tmem + C::kDQCol, split_a(tmem + C::kDPCol + 32, kk), bd, idAcc, 1u);
           }
-          mma_commit(&bars->kv_empty[s]);
-          if (more) issue_dp(s1);
+          mma_commit(&bars->k_empty[s]);  // K(j) was read by S(j) and, last, by dQ(j)
+          if (more) {
+            if (!(ok = wait_v(k1))) break;
+            issue_dp(k1 % C::kVStages);
+          }
           if (j + 2 == it.hi) mma_commit(&bars->qd_empty);
         }
         if (!ok) break;
@@ -821,63 +866,92 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (ACT == JATTN_SOFTMAX && !IN_TILE) {
     // ------------------------------------------------------------ Di warps (2, 3)
     // Di = rowsum(dO * O) for each item's 128 query rows, from the dO tile the
-    // producer loaded for the MMAs and an O tile loaded for this purpose: into a
-    // shared-memory slot for the activation warpgroups and to global memory for
-    // the dK/dV pass, which runs after this one. The same slot carries each
-    // row's LSE, loaded here, off the activation warps' critical path. Items
-    // with a single key tile get an exact Di from the activation warps
-    // instead (sum of P * dP over the tile), so here they only pass the LSE. Lane l of warp 2 + w owns tile
-    // rows 64w + l and 64w + 32 + l. Both tiles share the 128-byte-swizzled
-    // layout, so reading the same addresses pairs the same columns; walking a
-    // row's 16-byte pieces in swizzled order spreads the lanes over the banks.
+    // producer loaded for the MMAs and O (one ring: a tile the producer loads
+    // for this purpose; two rings: the rows in global memory, a.in0, with a
+    // prefetch into L2 before the waits): into a shared-memory slot for the
+    // activation warpgroups and to global memory for the dK/dV pass, which
+    // runs after this one. The same slot carries each row's LSE, loaded here,
+    // off the activation warps' critical path. Items with a single key tile
+    // get an exact Di from the activation warps instead (sum of P * dP over
+    // the tile), so here they only pass the LSE. Lane l of warp 2 + w owns tile
+    // rows 64w + l and 64w + 32 + l; walking a row's 16-byte pieces of the
+    // 128-byte-swizzled tiles in swizzled order spreads the lanes over the
+    // banks (the O tile shares the layout, so the same addresses pair columns).
     const int dw = warp - 2;
     float* di_s = reinterpret_cast<float*>(sm + C::kDiOff);
-    const uint32_t sO = smem_u32(sm + C::kOOff), sDO = smem_u32(sm + C::kDOOff);
+    const uint32_t sDO = smem_u32(sm + C::kDOOff);
+    const uint32_t sO = smem_u32(sm + (kOTile ? C::kOOff : 0));
     uint32_t n_item = 0;
     BwdItem it;
     for (long long r = 0; load_bwd_item(a, r, it); ++r) {
       if (it.hi <= it.lo) continue;  // no Q/dO/O copy for it, and nothing reads its Di
       const int slot = n_item & 1;
-      bool ok = wait_bar(&bars->di_empty[slot], ((n_item >> 1) & 1) ^ 1, abort_flag, a, 75);
-      ok = ok && wait_bar(&bars->qd_full, n_item & 1, abort_flag, a, 76);
-      ok = ok && wait_bar(&bars->ot_full, n_item & 1, abort_flag, a, 77);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      float lse_rows[2];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {  // issued before the dot products, used after them
-        const int il = it.rt * kTile + 64 * dw + 32 * h2 + lane;
-        lse_rows[h2] = (il < it.lq) ? a.f0[(it.q0 + il) * a.H + it.h] : 0.0f;
-      }
       const bool single = it.hi - it.lo == 1;
+      int rl[2];
+      bool dot[2];
+      float lse_rows[2], acc[2] = {0.0f, 0.0f};
+      const uint4* orow[2];
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
-        const int rl = 64 * dw + 32 * h2 + lane;
-        float acc = 0.0f;
+        rl[h2] = 64 * dw + 32 * h2 + lane;
+        const int il = it.rt * kTile + rl[h2];
+        const int64_t gi = (it.q0 + il) * a.H + it.h;
+        dot[h2] = il < it.lq && !single;  // rows past the sequence: their Di is never read
+        orow[h2] = reinterpret_cast<const uint4*>(a.in0 + gi * D);
+        lse_rows[h2] = (il < it.lq) ? a.f0[gi] : 0.0f;
+      }
+      if constexpr (!kOTile) {  // both rows of O on their way into L2 while the waits below pass
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+          if (dot[h2])
+#pragma unroll
+            for (int line = 0; line < D * 2 / 128; ++line)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(orow[h2]) + 128 * line));
+      }
+      bool ok = wait_bar(&bars->di_empty[slot], ((n_item >> 1) & 1) ^ 1, abort_flag, a, 75);
+      ok = ok && wait_bar(&bars->qd_full, n_item & 1, abort_flag, a, 76);
+      if (kOTile) ok = ok && wait_bar(&bars->ot_full, n_item & 1, abort_flag, a, 77);
+      if (!__all_sync(0xffffffffu, ok)) break;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
         for (int cb = 0; cb < (single ? 0 : D / 64); ++cb) {
+          uint4 ov[8];  // 64 columns of O, loaded before the dot product
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
-            const uint32_t off = cb * (kTile * 128) + rl * 128 + ((ch ^ (rl & 7)) << 4);
-            uint32_t x[4], y[4];
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
-                         : "r"(sO + off));
+            if constexpr (kOTile) {
+              const uint32_t off = cb * (kTile * 128) + rl[h2] * 128 + ((ch ^ (rl[h2] & 7)) << 4);
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(ov[ch].x), "=r"(ov[ch].y), "=r"(ov[ch].z), "=r"(ov[ch].w)
+                           : "r"(sO + off));
+            } else {
+              ov[ch] = dot[h2] ? __ldg(orow[h2] + 8 * cb + ch) : make_uint4(0, 0, 0, 0);
+            }
+          }
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint32_t off = cb * (kTile * 128) + rl[h2] * 128 + ((ch ^ (rl[h2] & 7)) << 4);
+            const uint32_t x[4] = {ov[ch].x, ov[ch].y, ov[ch].z, ov[ch].w};
+            uint32_t y[4];
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(y[0]), "=r"(y[1]), "=r"(y[2]), "=r"(y[3])
                          : "r"(sDO + off));
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x[e]));
               const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&y[e]));
-              acc = fmaf(xf.x, yf.x, fmaf(xf.y, yf.y, acc));
+              acc[h2] = fmaf(xf.x, yf.x, fmaf(xf.y, yf.y, acc[h2]));
             }
           }
         }
-        const int il = it.rt * kTile + rl;
-        di_s[slot * kTile + rl] = acc;
-        di_s[(2 + slot) * kTile + rl] = lse_rows[h2];
-        if (il < it.lq && !single) a.f1[(it.q0 + il) * a.H + it.h] = acc;
+      }
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        di_s[slot * kTile + rl[h2]] = acc[h2];
+        di_s[(2 + slot) * kTile + rl[h2]] = lse_rows[h2];
+        if (dot[h2]) a.f1[(it.q0 + it.rt * kTile + rl[h2]) * a.H + it.h] = acc[h2];
       }
       mbar_arrive(&bars->di_full[slot]);
-      mbar_arrive(&bars->ot_empty);
+      if constexpr (kOTile) mbar_arrive(&bars->ot_empty);
       mbar_arrive(&bars->qd_empty);
       ++n_item;
     }
@@ -1141,6 +1215,21 @@ cudaError_t launch5(K kern, int smem, const CUtensorMap& q, const CUtensorMap& k
   return cudaGetLastError();
 }
 
+// dQ kernel of one activation and head dimension, in the chosen K / V layout
+// (two rings only at D = 128, where one ring holds two stages).
+template <int D, int ACT, bool IN_TILE>
+cudaError_t launch_dq_layout(bool split, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                             const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a, int grid,
+                             cudaStream_t stream) {
+  if constexpr (D == 128 && !IN_TILE) {
+    if (split)
+      return launch5(dq_kernel<D, ACT, IN_TILE, true>, DqCfg<D, true>::kSmemBytes, q, k, v, dout, o, a, grid, stream);
+  }
+  // the O tile only for softmax's Di warps (the rest of the on-chip memory stays L1)
+  constexpr int smem = (ACT == JATTN_SOFTMAX && !IN_TILE) ? DqCfg<D, false>::kSmemBytes : DqCfg<D, false>::kOOff;
+  return launch5(dq_kernel<D, ACT, IN_TILE, false>, smem, q, k, v, dout, o, a, grid, stream);
+}
+
 template <typename K>
 cudaError_t launch4(K kern, int smem, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                     const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream) {
@@ -1184,37 +1273,35 @@ cudaError_t launch_bwd_dkdv(int D, int act, bool hilo, const CUtensorMap& q, con
 }
 
 #if JATTN_HILO
-cudaError_t launch_bwd_dq_hilo(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                               const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a, int grid,
-                               cudaStream_t stream) {
+cudaError_t launch_bwd_dq_hilo(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
+                               const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a,
+                               int grid, cudaStream_t stream) {
 #else
-cudaError_t launch_bwd_dq(int D, int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a, int grid,
-                          cudaStream_t stream) {
-  if (hilo && act != JATTN_SOFTMAX) return launch_bwd_dq_hilo(D, act, q, k, v, dout, o, a, grid, stream);
-  // the O tile for Di is only needed (and its shared memory only taken) for softmax
-  if (act == JATTN_SOFTMAX)
-    return a.in_tile_stats
-               ? (D == 128 ? launch5(dq_kernel<128, JATTN_SOFTMAX, true>, DqCfg<128>::kSmemBytes, q, k, v, dout, o, a,
-                                     grid, stream)
-                           : launch5(dq_kernel<64, JATTN_SOFTMAX, true>, DqCfg<64>::kSmemBytes, q, k, v, dout, o, a,
-                                     grid, stream))
-               : (D == 128 ? launch5(dq_kernel<128, JATTN_SOFTMAX>, DqCfg<128>::kSmemBytes, q, k, v, dout, o, a, grid,
-                                     stream)
-                           : launch5(dq_kernel<64, JATTN_SOFTMAX>, DqCfg<64>::kSmemBytes, q, k, v, dout, o, a, grid,
-                                     stream));
+cudaError_t launch_bwd_dq(int D, int act, bool hilo, bool split, const CUtensorMap& q, const CUtensorMap& k,
+                          const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a,
+                          int grid, cudaStream_t stream) {
+  if (hilo && act != JATTN_SOFTMAX) return launch_bwd_dq_hilo(D, act, split, q, k, v, dout, o, a, grid, stream);
+  if (act == JATTN_SOFTMAX) {
+    if (a.in_tile_stats)
+      return D == 128 ? launch_dq_layout<128, JATTN_SOFTMAX, true>(false, q, k, v, dout, o, a, grid, stream)
+                      : launch_dq_layout<64, JATTN_SOFTMAX, true>(false, q, k, v, dout, o, a, grid, stream);
+    return D == 128 ? launch_dq_layout<128, JATTN_SOFTMAX, false>(split, q, k, v, dout, o, a, grid, stream)
+                    : launch_dq_layout<64, JATTN_SOFTMAX, false>(split, q, k, v, dout, o, a, grid, stream);
+  }
 #endif
   if (D == 128) {
-    constexpr int sm = DqCfg<128>::kOOff;
-    if (act == JATTN_SILU) return launch5(dq_kernel<128, JATTN_SILU>, sm, q, k, v, dout, o, a, grid, stream);
-    if (act == JATTN_GELU_POLY) return launch5(dq_kernel<128, JATTN_GELU_POLY>, sm, q, k, v, dout, o, a, grid, stream);
-    if (act == JATTN_GELU_TANH) return launch5(dq_kernel<128, JATTN_GELU_TANH>, sm, q, k, v, dout, o, a, grid, stream);
+    if (act == JATTN_SILU) return launch_dq_layout<128, JATTN_SILU, false>(split, q, k, v, dout, o, a, grid, stream);
+    if (act == JATTN_GELU_POLY)
+      return launch_dq_layout<128, JATTN_GELU_POLY, false>(split, q, k, v, dout, o, a, grid, stream);
+    if (act == JATTN_GELU_TANH)
+      return launch_dq_layout<128, JATTN_GELU_TANH, false>(split, q, k, v, dout, o, a, grid, stream);
     return cudaErrorInvalidValue;
   }
-  constexpr int sm = DqCfg<64>::kOOff;
-  if (act == JATTN_SILU) return launch5(dq_kernel<64, JATTN_SILU>, sm, q, k, v, dout, o, a, grid, stream);
-  if (act == JATTN_GELU_POLY) return launch5(dq_kernel<64, JATTN_GELU_POLY>, sm, q, k, v, dout, o, a, grid, stream);
-  if (act == JATTN_GELU_TANH) return launch5(dq_kernel<64, JATTN_GELU_TANH>, sm, q, k, v, dout, o, a, grid, stream);
+  if (act == JATTN_SILU) return launch_dq_layout<64, JATTN_SILU, false>(split, q, k, v, dout, o, a, grid, stream);
+  if (act == JATTN_GELU_POLY)
+    return launch_dq_layout<64, JATTN_GELU_POLY, false>(split, q, k, v, dout, o, a, grid, stream);
+  if (act == JATTN_GELU_TANH)
+    return launch_dq_layout<64, JATTN_GELU_TANH, false>(split, q, k, v, dout, o, a, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -52,14 +52,16 @@ cudaError_t launch_bwd_dkdv(int D, int act, bool hilo, const CUtensorMap& q, con
 cudaError_t launch_bwd_dkdv_hilo(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                  const CUtensorMap& dout, const AttnArgs& a, int grid, cudaStream_t stream);
 // dQ over query tiles (128-row query tiles). For softmax it also computes
-// Di = rowsum(dO * O) from the dO tiles and O tiles (map `o`) into a.f1, so
-// it runs before the dK/dV pass, which reads Di.
-cudaError_t launch_bwd_dq(int D, int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a, int grid,
-                          cudaStream_t stream);
-cudaError_t launch_bwd_dq_hilo(int D, int act, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                               const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a, int grid,
-                               cudaStream_t stream);
+// Di = rowsum(dO * O) from the dO tiles and O (the map `o` in the one-ring
+// layout, the rows at a.in0 in the two-ring one) into a.f1, so it runs before
+// the dK/dV pass, which reads Di. `split`: K and V tiles in two rings (used at
+// D = 128, for items of many key tiles).
+cudaError_t launch_bwd_dq(int D, int act, bool hilo, bool split, const CUtensorMap& q, const CUtensorMap& k,
+                          const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a,
+                          int grid, cudaStream_t stream);
+cudaError_t launch_bwd_dq_hilo(int D, int act, bool split, const CUtensorMap& q, const CUtensorMap& k,
+                               const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a,
+                               int grid, cudaStream_t stream);
 
 // Rotary embedding of a jagged tensor x ([total, H, D] bf16, rows described
 // by own_off; other_off describes the other side for the alignment):

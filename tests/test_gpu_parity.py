@@ -196,6 +196,39 @@ def test_forward_arrangements(arrangement, act, mask, window, D, lq, lkv):
     G.compare(g, G.oracle_run(cpu, w, backward=False), w, backward=False)
 
 
+DQ_TWO_RINGS, DQ_ONE_RING = 8, 16  # debug flag bits that force the dQ pass's K / V layout
+
+
+@pytest.mark.parametrize("layout", [DQ_TWO_RINGS, DQ_ONE_RING])
+@pytest.mark.parametrize(
+    "act,mask,window,D,lq,lkv",
+    [
+        (SOFTMAX, CAUSAL, 0, 128, [700, 1, 129, 513, 300], None),
+        (SOFTMAX, WIN, 200, 128, SELF_LENS, SELF_LENS),
+        (SOFTMAX, CAUSAL, 0, 64, SELF_LENS, SELF_LENS),
+        (SOFTMAX, CAUSAL, 0, 128, [0, 5, 130, 1, 0, 200, 3], [4, 0, 130, 1, 0, 60, 9]),
+        (GELU, NONE, 0, 128, [32, 32, 32, 7], [100, 1000, 3000, 129]),
+        (SILU, NONE, 0, 128, CROSS_LQ, CROSS_LKV),
+    ],
+)
+def test_backward_dq_layouts(layout, act, mask, window, D, lq, lkv):
+    """Both layouts of the dQ pass's K / V tiles (two rings with K deeper than
+    V, or one ring of K + V stages; the host picks one from the key tiles an
+    item holds on average) give the oracle's gradients, whichever the shapes
+    would pick."""
+    from jagged_attention_recsys_gdpa_gb300 import _binding as B
+
+    lkv = lq if lkv is None else lkv
+    w = _w(act, mask, window, D, H=2, norm=act != SOFTMAX, std=1.0 if act == SOFTMAX else 0.5)
+    cpu = G.cpu_inputs(w, lq, lkv, seed=23)
+    B.debug_set(layout, 0)
+    try:
+        g, r = G.run_both_stored(cpu, w, backward=True)
+    finally:
+        B.debug_set(0, 0)
+    G.compare(g, r, w, backward=True)
+
+
 @pytest.mark.parametrize("act", [SOFTMAX, GELU])
 def test_outputs_16_byte_aligned_only(act):
     """Output tensors that start 16 bytes past a 32-byte boundary (written
