@@ -17,7 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libjattn.so")
 SOURCES = ["api.cu", "sched.cu", "fwd.cu", "fwd_block.cu", "fwd_hilo.cu", "fwd_block_hilo.cu", "bwd.cu",
-           "bwd_hilo.cu", "fwd_mx.cu", "bwd_mx.cu", "rope.cu", "mx.cu", "partition.cpp"]
+           "bwd_hilo.cu", "fwd_mx.cu", "bwd_mx.cu", "pma.cu", "rope.cu", "mx.cu", "partition.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "--expt-relaxed-constexpr"]
 

@@ -53,9 +53,20 @@ int cuda_fail(const char* what, cudaError_t e) {
 // mistaken for a failed launch of ours.
 void clear_stale_error() { (void)cudaGetLastError(); }
 
+// Pooling-shaped calls (pointwise activation, no mask, D = 128, at most 64
+// queries per sequence on average) run the short-query kernels, which put the
+// keys on the MMA's M dimension (pma.cu). The workspace holds their schedule
+// and gate word whenever the shape allows them; debug flag bit 32 keeps the
+// general kernels.
+bool short_q_shape(const jattn_params_t& p) {
+  return p.act != JATTN_SOFTMAX && p.mask == JATTN_MASK_NONE && p.D == 128 &&
+         p.total_q <= static_cast<int64_t>(pma_rows_per_item()) * p.B;
+}
+bool use_short_q(const jattn_params_t& p) { return short_q_shape(p) && !(g_debug_flags & 32); }
+
 struct Layout {
-  size_t status, sched_fwd, sched_q, sched_kv, di, lse, total;
-  int64_t tiles_fwd, tiles_q, tiles_kv;
+  size_t status, sched_fwd, sched_q, sched_kv, sched_s, gate, di, lse, total;
+  int64_t tiles_fwd, tiles_q, tiles_kv, tiles_s;
 };
 
 Layout layout_for(const jattn_params_t& p) {
@@ -73,6 +84,14 @@ Layout layout_for(const jattn_params_t& p) {
   off += al256(sched_ws_bytes(p.B, L.tiles_q));
   L.sched_kv = off;
   off += al256(sched_ws_bytes(p.B, L.tiles_kv));
+  L.sched_s = L.gate = off;
+  L.tiles_s = 0;
+  if (short_q_shape(p)) {
+    L.tiles_s = sched_max_tiles(p.B, p.total_q, pma_rows_per_item());
+    off += al256(sched_ws_bytes(p.B, L.tiles_s));
+    L.gate = off;
+    off += 256;
+  }
   L.di = off;
   if (p.act == JATTN_SOFTMAX) off += al256(sizeof(float) * static_cast<size_t>(p.total_q) * p.H);
   // block masks: the LSE that a backward with in-tile statistics writes for its dK/dV pass
@@ -168,14 +187,14 @@ int encoder() {
   return g_encode ? JATTN_OK : JATTN_ERR_CUDA;
 }
 
-// 2-D view [rows, H*D] of a jagged bf16 tensor; boxes of 128 rows x 64
+// 2-D view [rows, H*D] of a jagged bf16 tensor; boxes of box_rows rows x 64
 // columns (128 bytes) with the 128-byte swizzle the MMA descriptors expect.
-int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int H, int D) {
+int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int H, int D, int box_rows = kTile) {
   std::memset(m, 0, sizeof(*m));
   if (rows == 0) return JATTN_OK;  // never dereferenced: no tile is scheduled
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * D, static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * D * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -360,9 +379,29 @@ int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const Layout L = layout_for(*p);
   char* base = static_cast<char*>(ws);
-  const SchedView sv = sched_carve(base + L.sched_fwd, p->B, L.tiles_fwd);
   AttnArgs a = base_args(*p, q_off, kv_off, ws);
   cudaError_t e;
+  if (use_short_q(*p)) {
+    const SchedView ss = sched_carve(base + L.sched_s, p->B, L.tiles_s);
+    if ((e = sched_launch(ss, q_off, kv_off, p->B, p->total_q, p->total_kv, pma_rows_per_item(), kTile, p->mask,
+                          a.window, 0, a.status, st)) != cudaSuccess)
+      return cuda_fail("schedule launch", e);
+    CUtensorMap mq, mk, mv;
+    if (make_map(&mq, q, p->total_q, p->H, p->D, pma_rows_per_item()) ||
+        make_map(&mk, k, p->total_kv, p->H, p->D) || make_map(&mv, v, p->total_kv, p->H, p->D))
+      return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+    a.tiles = ss.sorted;
+    a.n_tiles = ss.n_tiles;
+    a.out0 = reinterpret_cast<__nv_bfloat16*>(o);
+    a.out_v8 = aligned32(o);
+    prof(0, st);
+    if ((e = launch_pma_fwd(p->act, hilo_for(*p), mq, mk, mv, a, grid_for(dev, L.tiles_s, p->H), st)) !=
+        cudaSuccess)
+      return cuda_fail("short-query forward kernel launch", e);
+    prof(1, st);
+    return JATTN_OK;
+  }
+  const SchedView sv = sched_carve(base + L.sched_fwd, p->B, L.tiles_fwd);
   if ((e = sched_launch(sv, q_off, kv_off, p->B, p->total_q, p->total_kv, fwd_rows_per_item(), kTile, p->mask,
                         a.window, 0, a.status, st)) != cudaSuccess)
     return cuda_fail("schedule launch", e);
@@ -628,11 +667,45 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
   a.f0 = in_tile ? reinterpret_cast<float*>(base + L.lse) : const_cast<float*>(lse);
   a.f1 = di;
   a.in_tile_stats = in_tile ? 1 : 0;
+  const SchedView qs = sched_carve(base + L.sched_q, p->B, L.tiles_q);
+  const SchedView kv = sched_carve(base + L.sched_kv, p->B, L.tiles_kv);
+  // Short-query (pooling) shapes: the fused pass runs first and, when the gate
+  // finds every sequence within its limits, the general passes below find
+  // empty schedules. The profiling events of the dK/dV slot bracket it.
+  const bool sq = use_short_q(*p) && !rope_cos && p->total_q > 0 && p->total_kv > 0;
+  if (sq) {
+    const SchedView ss = sched_carve(base + L.sched_s, p->B, L.tiles_s);
+    if ((e = sched_launch(ss, q_off, kv_off, p->B, p->total_q, p->total_kv, pma_rows_per_item(), kTile, p->mask,
+                          a.window, 0, a.status, st)) != cudaSuccess ||
+        (e = sched_launch(qs, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 0,
+                          a.status, st)) != cudaSuccess ||
+        (e = sched_launch(kv, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 1,
+                          a.status, st)) != cudaSuccess)
+      return cuda_fail("schedule launch", e);
+    int* gate = reinterpret_cast<int*>(base + L.gate);
+    if ((e = launch_pma_gate(q_off, kv_off, p->B, gate, qs.n_tiles, kv.n_tiles, st)) != cudaSuccess)
+      return cuda_fail("short-query gate launch", e);
+    CUtensorMap sq_q, sq_do;
+    if (make_map(&sq_q, q, p->total_q, p->H, p->D, pma_rows_per_item()) ||
+        make_map(&sq_do, dout, p->total_q, p->H, p->D, pma_rows_per_item()))
+      return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+    AttnArgs b = a;
+    b.tiles = ss.sorted;
+    b.n_tiles = ss.n_tiles;
+    b.out0 = reinterpret_cast<__nv_bfloat16*>(dq);
+    b.out1 = reinterpret_cast<__nv_bfloat16*>(dv);
+    b.out2 = reinterpret_cast<__nv_bfloat16*>(dk);
+    b.out_v8 = aligned32(dk) && aligned32(dv);
+    prof(2, st);
+    if ((e = launch_pma_bwd(p->act, hilo_for(*p), sq_q, mk, mv, sq_do, b, gate, grid_for(dev, L.tiles_s, p->H),
+                            st)) != cudaSuccess)
+      return cuda_fail("short-query backward kernel launch", e);
+    prof(3, st);
+  }
   // The dQ pass runs first: for softmax it also writes Di, which the dK/dV pass reads.
   if (p->total_q > 0) {
-    const SchedView qs = sched_carve(base + L.sched_q, p->B, L.tiles_q);
-    if ((e = sched_launch(qs, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 0,
-                          a.status, st)) != cudaSuccess)
+    if (!sq && (e = sched_launch(qs, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window,
+                                 0, a.status, st)) != cudaSuccess)
       return cuda_fail("query-tile schedule launch", e);
     a.tiles = qs.sorted;
     a.n_tiles = qs.n_tiles;
@@ -646,20 +719,19 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
     prof(5, st);
   }
   if (p->total_kv > 0) {
-    const SchedView kv = sched_carve(base + L.sched_kv, p->B, L.tiles_kv);
-    if ((e = sched_launch(kv, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 1,
-                          a.status, st)) != cudaSuccess)
+    if (!sq && (e = sched_launch(kv, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window,
+                                 1, a.status, st)) != cudaSuccess)
       return cuda_fail("key-tile schedule launch", e);
     a.tiles = kv.sorted;
     a.n_tiles = kv.n_tiles;
     a.out0 = reinterpret_cast<__nv_bfloat16*>(dk);
     a.out1 = reinterpret_cast<__nv_bfloat16*>(dv);
     a.out_v8 = aligned32(dk) && aligned32(dv);
-    prof(2, st);
+    if (!sq) prof(2, st);
     if ((e = launch_bwd_dkdv(p->D, p->act, hilo_for(*p), mq, mk, mv, mdo, a, grid_for(dev, L.tiles_kv, p->H), st)) !=
         cudaSuccess)
       return cuda_fail("dK/dV kernel launch", e);
-    prof(3, st);
+    if (!sq) prof(3, st);
   }
   return JATTN_OK;
 }

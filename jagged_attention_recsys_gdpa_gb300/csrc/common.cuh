@@ -63,6 +63,8 @@ struct AttnArgs {
   const int* bs_kv;
   // MXFP8 backward: E8M0 scales of dO (row blocks of the query side)
   const uint8_t* sf_do;
+  // third output of the fused short-query backward (dK; out0 = dQ, out1 = dV)
+  __nv_bfloat16* out2;
 };
 
 // The bf16 pair of what the bf16 pair `hi` of (x0, x1) leaves out.

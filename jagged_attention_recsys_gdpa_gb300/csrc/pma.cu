@@ -1,0 +1,906 @@
+// Short-query attention (pooling: a few queries per sequence against long key
+// sequences) with the keys on the MMA's M dimension, on sm_103a.
+//
+// "GEM Training" post, section "Generalized Dot-Product Attention (GDPA)":
+// pooling attention (PMA) runs a few learned queries per sequence against the
+// sequence's keys with a pointwise activation. A 128-row query tile holding 32
+// queries leaves three quarters of every MMA's M rows empty. Here the products
+// are transposed so that 128 keys fill M and an item's queries (at most 64)
+// are the N dimension:
+//   forward   S^T = K Q^T; P^T = act(scale S^T) goes to shared memory as
+//             bf16; O^T += V^T P^T (M = head dim) accumulates in TMEM over the
+//             key tiles, and O is written from O^T at the item's end.
+//   backward  one item = (sequence, head) with all of the sequence's queries.
+//             Per key tile: S^T = K Q^T and dP^T = V dO^T; P^T and
+//             dS^T = act'(scale S^T) * dP^T; dV = P^T dO and dK = dS^T Q, each
+//             complete for the tile since every query is in the item; and
+//             dQ^T += K^T dS^T, accumulated in TMEM over the key tiles. K and
+//             V are read once and dK / dV written once: there is no second
+//             pass that reads K and V again for dQ.
+// Items come from the 64-row query-tile schedule, longest first. The forward
+// takes any query length (a longer sequence gives several items, each of
+// which reads its key tiles again). The backward needs every sequence to hold
+// at most 64 queries, and at least one when it has keys; a gate kernel checks
+// that on the device and either clears the general dQ and dK/dV schedules
+// (their passes then find no work) or leaves them to run while this pass
+// finds the gate closed and returns.
+//
+// Roles: warp 0 issues TMA copies, warp 1 issues tcgen05 MMAs; the forward's
+// two activation warpgroups (warps 4-7, 8-11) take alternate key tiles, the
+// backward has one activation warpgroup (warps 4-7) and an epilogue
+// warpgroup (warps 8-11) that drains dV / dK per key tile and dQ per item.
+// Thread i of a warpgroup owns TMEM lane i: a key row of S^T / dP^T / dV /
+// dK, or a head-dim row of O^T / dQ^T.
+//
+// Pointwise activations without the 1/Lkv normaliser pass P and dS to the
+// second products as bf16 hi + lo parts (template HILO), as the general
+// kernels do: outputs there sum thousands of unscaled terms.
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace jattn {
+
+namespace {
+
+constexpr int kD = 128;                      // head dim (the only one this path takes)
+constexpr int kQC = 64;                      // query rows of an item: the MMAs' N
+constexpr int kThreads = 384;                // 12 warps
+constexpr int kBoxK = kTile * 128;           // one [128 rows][64 columns] bf16 box (16 KB)
+constexpr int kBoxQ = kQC * 128;             // one [64 rows][64 columns] bf16 box (8 KB)
+constexpr int kTileBytes = 2 * kBoxK;        // K or V tile: [128 keys][128]
+constexpr int kChunkBytes = 2 * kBoxQ;       // Q or dO chunk: [64 queries][128]
+constexpr int kPBytes = kTile * kQC * 2;     // P^T or dS^T: [128 keys][64 queries] bf16
+constexpr float kLog2e = 1.4426950408889634f;
+// Backward register split (setmaxnreg, per warpgroup): 384 x 168 at launch =
+// 64512 >= 128 x (control + activation + epilogue). The activation threads
+// hold a key row's 64 scores and 64 activation derivatives. A warpgroup that
+// ends below the launch count lowers its share (.dec), one above it raises
+// it (.inc): .inc may not ask for fewer registers than the warp holds.
+constexpr int kLaunchRegs = 168;
+constexpr int kCtlRegs = 136;
+constexpr int kActRegs = 216;
+constexpr int kEpiRegs = 152;
+static_assert(128 * (kCtlRegs + kActRegs + kEpiRegs) <= kThreads * kLaunchRegs, "register split");
+static_assert(kCtlRegs <= kLaunchRegs && kEpiRegs <= kLaunchRegs && kActRegs >= kLaunchRegs,
+              "dec / inc directions of the split");
+
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// act(x) and act'(x) of the pointwise activations (SiLU, tanh-GELU, and
+// tanh-GELU's Taylor polynomial).
+template <int ACT>
+__device__ __forceinline__ void act_and_grad(float x, float& f, float& g) {
+  if constexpr (ACT == JATTN_SILU) {
+    const float sg = __fdividef(1.0f, 1.0f + ex2_approx(-x * kLog2e));
+    f = x * sg;
+    g = sg * fmaf(x, 1.0f - sg, 1.0f);
+  } else if constexpr (ACT == JATTN_GELU_POLY) {
+    f = gelu_poly(x);
+    g = gelu_poly_grad(x);
+  } else {
+    const float k0 = 0.7978845608028654f, k1 = 0.044715f;
+    const float x2 = x * x;
+    const float t = tanh_approx(k0 * fmaf(k1 * x2, x, x));
+    f = 0.5f * x * (1.0f + t);
+    g = fmaf(0.5f * x * (1.0f - t * t) * k0, fmaf(3.0f * k1, x2, 1.0f), 0.5f * (1.0f + t));
+  }
+}
+template <int ACT>
+__device__ __forceinline__ float act_f(float x) {
+  if constexpr (ACT == JATTN_SILU) {
+    const float h = 0.5f * x;  // x sigmoid(x) = h (1 + tanh h)
+    return fmaf(h, tanh_approx(h), h);
+  } else if constexpr (ACT == JATTN_GELU_POLY) {
+    return gelu_poly(x);
+  } else {
+    const float u = 0.7978845608028654f * fmaf(0.044715f * x * x, x, x);
+    return 0.5f * x * (1.0f + tanh_approx(u));
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// 16 packed bf16 pairs (queries c0 .. c0 + 31 of key row `row`) into a
+// [128 keys][64 queries] tile in the 128-byte-swizzled layout an MN-major MMA
+// operand reads: row r at r * 128 bytes, its 16-byte piece p at (p ^ (r & 7)).
+__device__ __forceinline__ void st_pt_row(uint32_t tile, int row, int c0, const uint32_t (&w)[16]) {
+  const uint32_t base = tile + static_cast<uint32_t>(row) * 128;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int piece = (c0 >> 3) + i;
+    st_shared_v4(base + ((piece ^ (row & 7)) << 4), w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  }
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+// Descriptor offsets (16-byte units). K-major operands: the kk-th 16-wide
+// slice of a 128-column row lies (kk / 4) boxes and (kk % 4) * 32 bytes
+// further. MN-major operands: the kk-th 16-row slice lies 16 rows further.
+__device__ __forceinline__ uint64_t kslice(int kk, int box_bytes) {
+  return static_cast<uint64_t>(((kk >> 2) * box_bytes + (kk & 3) * 32) >> 4);
+}
+__device__ __forceinline__ uint64_t mnslice(int kk) { return static_cast<uint64_t>((kk * 16 * 128) >> 4); }
+
+struct PItem {
+  int b, rt, lo, hi, h, lq, lkv;  // lq: query rows of this item (at most kQC)
+  int64_t q0, k0;                 // first query row of the item, first key row of the sequence
+};
+
+__device__ __forceinline__ bool load_pitem(const AttnArgs& a, long long round, PItem& it) {
+  const long long n_items = static_cast<long long>(*a.n_tiles) * a.H;
+  const long long k = zigzag_item(round, blockIdx.x, gridDim.x);
+  if (k >= n_items) return false;
+  const int4 t = a.tiles[k / a.H];
+  it.h = static_cast<int>(k % a.H);
+  it.b = t.x;
+  it.rt = t.y;
+  it.lo = t.z;
+  it.hi = t.w;
+  const int64_t qs = a.q_off[it.b];
+  it.q0 = qs + static_cast<int64_t>(it.rt) * kQC;
+  const int64_t rest = a.q_off[it.b + 1] - it.q0;
+  it.lq = static_cast<int>(rest < kQC ? rest : kQC);
+  it.k0 = a.kv_off[it.b];
+  it.lkv = static_cast<int>(a.kv_off[it.b + 1] - it.k0);
+  return true;
+}
+
+// One output element per (query, head-dim row): thread d of a warpgroup
+// writes O[q][h][d] (or dQ) for the queries [c0, c0 + 32) below lq, from 32
+// fp32 accumulator columns (nullptr: zeros). A warp's 32 lanes write 64
+// contiguous bytes per query.
+__device__ __forceinline__ void store_cols(__nv_bfloat16* out, const PItem& it, int H, int d, int c0,
+                                           const uint32_t* v, float mul) {
+  for (int e = 0; e < 32; ++e) {
+    const int q = c0 + e;
+    if (q >= it.lq) break;
+    const float x = v ? __uint_as_float(v[e]) * mul : 0.0f;
+    out[((it.q0 + q) * H + it.h) * kD + d] = __float2bfloat16_rn(x);
+  }
+}
+
+// ---------------------------------------------------------------------------- forward
+template <bool HILO>
+struct PfCfg {
+  static constexpr int kKStages = HILO ? 2 : 3;
+  static constexpr int kVStages = 2;
+  static constexpr int kNP = HILO ? 2 : 1;  // P^T tiles per buffer (hi, lo)
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kChunkBytes;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kPOff = kVOff + kVStages * kTileBytes;  // [2 buffers][kNP] P^T tiles
+  static constexpr int kBarOff = kPOff + 2 * kNP * kPBytes;
+  static constexpr int kSmemBytes = kBarOff + 256;
+  static constexpr uint32_t kOCol = 2 * kQC;  // S^T buffers at 0 and 64, O^T after them
+};
+static_assert(PfCfg<false>::kSmemBytes <= 227 * 1024 && PfCfg<true>::kSmemBytes <= 227 * 1024, "shared memory");
+
+struct PfBars {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t o_full, o_empty, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(PfBars) <= 256, "barrier block overflows its slot");
+
+template <int ACT, bool HILO>
+__global__ void __launch_bounds__(kThreads, 1)
+    pma_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+  using C = PfCfg<HILO>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) record_error(a.status, JATTN_ERR_UNSUPPORTED, 80, blockIdx.x);
+    return;
+  }
+  uint8_t* sm = smem_raw;
+  PfBars* bars = reinterpret_cast<PfBars*>(sm + C::kBarOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &bars->abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&bars->s_full[g], 1);
+      mbar_init(&bars->s_free[g], kTile);
+      mbar_init(&bars->p_full[g], kTile);
+      mbar_init(&bars->p_free[g], 1);
+    }
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->o_empty, 2 * kTile);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t k_it = 0, v_it = 0, q_it = 0;
+      bool q_armed = false, ok = true;
+      PItem it;
+      auto load_kv = [&](const CUtensorMap* map, uint64_t* full, uint64_t* empty, int stages, int off, uint32_t& cnt,
+                         int j, int where) -> bool {
+        const int s = cnt % stages;
+        if (!wait_bar(&empty[s], ((cnt / stages) & 1) ^ 1, abort_flag, a, where)) return false;
+        mbar_arrive_expect_tx(&full[s], kTileBytes);
+        for (int c = 0; c < 2; ++c)
+          tma_load_2d(sm + off + s * kTileBytes + c * kBoxK, map, &full[s], it.h * kD + c * 64,
+                      static_cast<int>(it.k0) + j * kTile);
+        ++cnt;
+        return true;
+      };
+      for (long long r = 0; ok && load_pitem(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!(ok = wait_bar(&bars->q_empty, (q_it & 1) ^ 1, abort_flag, a, 81))) break;
+        if (!(a.debug_flags & 1)) {
+          mbar_arrive_expect_tx(&bars->q_full, kChunkBytes);
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d(sm + C::kQOff + c * kBoxQ, &tmQ, &bars->q_full, it.h * kD + c * 64, static_cast<int>(it.q0));
+          q_armed = true;
+        }
+        ++q_it;
+        // K runs a tile ahead of V: S^T(j + 1) is issued before O^T's product with P^T(j).
+        if (!(ok = load_kv(&tmK, bars->k_full, bars->k_empty, C::kKStages, C::kKOff, k_it, it.lo, 82))) break;
+        for (int j = it.lo; j < it.hi && ok; ++j) {
+          if (j + 1 < it.hi && !(ok = load_kv(&tmK, bars->k_full, bars->k_empty, C::kKStages, C::kKOff, k_it, j + 1, 82)))
+            break;
+          ok = load_kv(&tmV, bars->v_full, bars->v_empty, C::kVStages, C::kVOff, v_it, j, 83);
+        }
+      }
+      // every copy this thread started lands before the CTA can exit
+      if (q_armed) drain_wait(&bars->q_full, (q_it - 1) & 1, a.timeout_ns);
+      for (uint32_t i = (k_it > (uint32_t)C::kKStages ? k_it - C::kKStages : 0); i < k_it; ++i)
+        drain_wait(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1, a.timeout_ns);
+      for (uint32_t i = (v_it > (uint32_t)C::kVStages ? v_it - C::kVStages : 0); i < v_it; ++i)
+        drain_wait(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1, a.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kTile, kQC, false, false);  // S^T = K Q^T
+      constexpr uint32_t idO = idesc_bf16_f32(kD, kQC, true, true);       // O^T += V^T P^T
+      const uint32_t sQ = smem_u32(sm + C::kQOff), sK = smem_u32(sm + C::kKOff), sV = smem_u32(sm + C::kVOff);
+      const uint32_t sP = smem_u32(sm + C::kPOff);
+      const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), dK0 = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dVt0 = sdesc_sw128(sV, kBoxK, 1024), dP0 = sdesc_sw128(sP, kPBytes, 1024);
+      uint32_t k_used = 0, v_used = 0, q_it = 0, o_cnt = 0, n = 0;
+      bool ok = true;
+      PItem it;
+      // O^T += V^T P^T of the item's t-th key tile (global tile index nt)
+      auto issue_o = [&](int t, uint32_t nt) -> bool {
+        const uint32_t vi = v_used + t, g = nt & 1, u = nt >> 1;
+        const int vs = vi % C::kVStages;
+        if (!wait_bar(&bars->v_full[vs], (vi / C::kVStages) & 1, abort_flag, a, 84)) return false;
+        if (!wait_bar(&bars->p_full[g], u & 1, abort_flag, a, 85)) return false;
+        if (t == 0 && !wait_bar(&bars->o_empty, (o_cnt & 1) ^ 1, abort_flag, a, 86)) return false;
+        tc_fence_after();
+        const uint64_t vd = dVt0 + vs * (kTileBytes >> 4);
+#pragma unroll
+        for (int hl = 0; hl < C::kNP; ++hl) {
+          const uint64_t pd = dP0 + (g * C::kNP + hl) * (kPBytes >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ss(tmem + C::kOCol, vd + mnslice(kk), pd + mnslice(kk), idO, (t > 0 || hl > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars->p_free[g]);
+        mma_commit(&bars->v_empty[vs]);
+        return true;
+      };
+      for (long long r = 0; ok && load_pitem(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!(ok = wait_bar(&bars->q_full, q_it & 1, abort_flag, a, 87))) break;
+        ++q_it;
+        tc_fence_after();
+        const int nk = it.hi - it.lo;
+        for (int t = 0; t < nk && ok; ++t) {
+          const uint32_t ki = k_used + t, nt = n + t, g = nt & 1, u = nt >> 1;
+          const int ks = ki % C::kKStages;
+          if (!(ok = wait_bar(&bars->k_full[ks], (ki / C::kKStages) & 1, abort_flag, a, 88))) break;
+          if (!(ok = wait_bar(&bars->s_free[g], (u & 1) ^ 1, abort_flag, a, 89))) break;
+          tc_fence_after();
+          const uint64_t kd = dK0 + ks * (kTileBytes >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_ss(tmem + g * kQC, kd + kslice(kk, kBoxK), dQ + kslice(kk, kBoxQ), idS, kk > 0 ? 1u : 0u);
+          mma_commit(&bars->s_full[g]);
+          mma_commit(&bars->k_empty[ks]);
+          if (t == nk - 1) mma_commit(&bars->q_empty);  // Q is read by the S^T products only
+          if (t > 0) ok = issue_o(t - 1, nt - 1);
+        }
+        if (ok) ok = issue_o(nk - 1, n + nk - 1);
+        if (!ok) break;
+        mma_commit(&bars->o_full);
+        ++o_cnt;
+        n += nk;
+        k_used += nk;
+        v_used += nk;
+      }
+      // every MMA this thread issued completes before TMEM is released
+      mma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0, a.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ activation warpgroups
+    // Warpgroup g takes the key tiles of odd / even global index: S^T buffer
+    // g in TMEM, P^T buffer g in shared memory. At an item's end both read
+    // O^T, queries [32 g, 32 g + 32) each.
+    const int g = (warp - 4) >> 2;
+    const int row = 32 * (warp & 3) + lane;  // key row of S^T; head-dim row of O^T
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t sP = smem_u32(sm + C::kPOff);
+    uint32_t n = 0, o_cnt = 0;
+    bool ok = true;
+    PItem it;
+    for (long long r = 0; ok && load_pitem(a, r, it); ++r) {
+      __nv_bfloat16* out = a.out0;
+      if (it.hi <= it.lo) {  // no keys: the item's output rows are zero
+        store_cols(out, it, a.H, row, 32 * g, nullptr, 0.0f);
+        continue;
+      }
+      const int nk = it.hi - it.lo;
+      for (int t = 0; t < nk; ++t) {
+        const uint32_t nt = n + t;
+        if ((nt & 1) != static_cast<uint32_t>(g)) continue;
+        const uint32_t u = nt >> 1;
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->s_full[g], u & 1, abort_flag, a, 90));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t s[kQC];
+#pragma unroll
+        for (int c = 0; c < kQC / 32; ++c)
+          if (32 * c < it.lq) tmem_ld32(tmem + lane_base + g * kQC + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->s_free[g]);
+        // keys past the sequence (a ragged last tile) give P = 0; columns past
+        // the item's queries only reach O^T columns that are never stored
+        const bool valid = (it.lo + t) * kTile + row < it.lkv;
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->p_free[g], (u & 1) ^ 1, abort_flag, a, 91));
+        if (!ok) break;
+#pragma unroll
+        for (int c = 0; c < kQC / 32; ++c) {
+          if (32 * c >= it.lq) continue;
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float f0 = valid ? act_f<ACT>(__uint_as_float(s[32 * c + 2 * e]) * a.scale) : 0.0f;
+            const float f1 = valid ? act_f<ACT>(__uint_as_float(s[32 * c + 2 * e + 1]) * a.scale) : 0.0f;
+            hi[e] = pack_bf16x2(f0, f1);
+            if constexpr (HILO) lo[e] = bf16x2_lo(f0, f1, hi[e]);
+          }
+          st_pt_row(sP + (g * C::kNP) * kPBytes, row, 32 * c, hi);
+          if constexpr (HILO) st_pt_row(sP + (g * C::kNP + 1) * kPBytes, row, 32 * c, lo);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->p_full[g]);
+      }
+      if (!ok) break;
+      n += nk;
+      // epilogue: O^T columns [32 g, 32 g + 32), times 1/Lkv when asked
+      ok = __all_sync(0xffffffffu, wait_bar(&bars->o_full, o_cnt & 1, abort_flag, a, 92));
+      if (!ok) break;
+      ++o_cnt;
+      tc_fence_after();
+      const float cn = (a.norm_by_lkv && it.lkv > 0) ? 1.0f / it.lkv : 1.0f;
+      uint32_t v[32];
+      if (32 * g < it.lq) {
+        tmem_ld32(tmem + lane_base + C::kOCol + 32 * g, v);
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_empty);
+      if (32 * g < it.lq) store_cols(out, it, a.H, row, 32 * g, v, cn);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------- backward
+template <bool HILO>
+struct PbCfg {
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 2;
+  static constexpr int kNP = HILO ? 2 : 1;  // dS^T tiles in shared memory (hi, lo)
+  static constexpr int kQOff = 0;
+  static constexpr int kDOOff = kChunkBytes;
+  static constexpr int kKOff = 2 * kChunkBytes;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kDSOff = kVOff + kVStages * kTileBytes;
+  static constexpr int kBarOff = kDSOff + kNP * kPBytes;
+  static constexpr int kSmemBytes = kBarOff + 256;
+  // TMEM: S^T (P^T as bf16 over its first columns), dP^T (dS^T likewise), dV, dK, dQ^T
+  static constexpr uint32_t kSCol = 0, kDPCol = 64, kDVCol = 128, kDKCol = 256, kDQCol = 384;
+};
+static_assert(PbCfg<false>::kSmemBytes <= 227 * 1024 && PbCfg<true>::kSmemBytes <= 227 * 1024, "shared memory");
+
+struct PbBars {
+  uint64_t q_full, q_empty;  // Q and dO chunks of an item
+  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
+  uint64_t s_full, dp_full, p_ready, ds_ready, dsm_free;
+  uint64_t acc_full, acc_empty, dq_full, dq_empty, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(PbBars) <= 256, "barrier block overflows its slot");
+
+template <int ACT, bool HILO>
+__global__ void __launch_bounds__(kThreads, 1)
+    pma_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                   const AttnArgs a, const int* gate) {
+  using C = PbCfg<HILO>;
+  if (*gate == 0) return;  // some sequence holds more than 64 queries: the general passes run
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) record_error(a.status, JATTN_ERR_UNSUPPORTED, 93, blockIdx.x);
+    return;
+  }
+  uint8_t* sm = smem_raw;
+  PbBars* bars = reinterpret_cast<PbBars*>(sm + C::kBarOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &bars->abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, kTile);
+    mbar_init(&bars->ds_ready, kTile);
+    mbar_init(&bars->dsm_free, 1);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, kTile);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_empty, kTile);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp < 4) {
+  // each warpgroup sets its register share in the branch that holds its code
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      uint32_t k_it = 0, v_it = 0, q_it = 0;
+      bool q_armed = false, ok = true;
+      PItem it;
+      auto load_kv = [&](const CUtensorMap* map, uint64_t* full, uint64_t* empty, int stages, int off, uint32_t& cnt,
+                         int j, int where) -> bool {
+        const int s = cnt % stages;
+        if (!wait_bar(&empty[s], ((cnt / stages) & 1) ^ 1, abort_flag, a, where)) return false;
+        mbar_arrive_expect_tx(&full[s], kTileBytes);
+        for (int c = 0; c < 2; ++c)
+          tma_load_2d(sm + off + s * kTileBytes + c * kBoxK, map, &full[s], it.h * kD + c * 64,
+                      static_cast<int>(it.k0) + j * kTile);
+        ++cnt;
+        return true;
+      };
+      for (long long r = 0; ok && load_pitem(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!(ok = wait_bar(&bars->q_empty, (q_it & 1) ^ 1, abort_flag, a, 94))) break;
+        if (!(a.debug_flags & 1)) {
+          mbar_arrive_expect_tx(&bars->q_full, 2 * kChunkBytes);
+          for (int c = 0; c < 2; ++c) {
+            tma_load_2d(sm + C::kQOff + c * kBoxQ, &tmQ, &bars->q_full, it.h * kD + c * 64, static_cast<int>(it.q0));
+            tma_load_2d(sm + C::kDOOff + c * kBoxQ, &tmDO, &bars->q_full, it.h * kD + c * 64, static_cast<int>(it.q0));
+          }
+          q_armed = true;
+        }
+        ++q_it;
+        for (int j = it.lo; j < it.hi && ok; ++j) {
+          if (!(ok = load_kv(&tmK, bars->k_full, bars->k_empty, C::kKStages, C::kKOff, k_it, j, 95))) break;
+          ok = load_kv(&tmV, bars->v_full, bars->v_empty, C::kVStages, C::kVOff, v_it, j, 96);
+        }
+      }
+      if (q_armed) drain_wait(&bars->q_full, (q_it - 1) & 1, a.timeout_ns);
+      for (uint32_t i = (k_it > (uint32_t)C::kKStages ? k_it - C::kKStages : 0); i < k_it; ++i)
+        drain_wait(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1, a.timeout_ns);
+      for (uint32_t i = (v_it > (uint32_t)C::kVStages ? v_it - C::kVStages : 0); i < v_it; ++i)
+        drain_wait(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1, a.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kTile, kQC, false, false);  // S^T = K Q^T, dP^T = V dO^T
+      constexpr uint32_t idG = idesc_bf16_f32(kTile, kD, false, true);    // dV = P^T dO, dK = dS^T Q
+      constexpr uint32_t idQ = idesc_bf16_f32(kD, kQC, true, true);       // dQ^T += K^T dS^T
+      const uint32_t sQ = smem_u32(sm + C::kQOff), sDO = smem_u32(sm + C::kDOOff);
+      const uint32_t sK = smem_u32(sm + C::kKOff), sV = smem_u32(sm + C::kVOff), sDS = smem_u32(sm + C::kDSOff);
+      const uint64_t dQk = sdesc_sw128(sQ, 16, 1024), dDOk = sdesc_sw128(sDO, 16, 1024);    // K-major views
+      const uint64_t dQm = sdesc_sw128(sQ, kBoxQ, 1024), dDOm = sdesc_sw128(sDO, kBoxQ, 1024);  // MN-major views
+      const uint64_t dK0 = sdesc_sw128(sK, 16, 1024), dKt0 = sdesc_sw128(sK, kBoxK, 1024);
+      const uint64_t dV0 = sdesc_sw128(sV, 16, 1024), dDS0 = sdesc_sw128(sDS, kPBytes, 1024);
+      uint32_t k_used = 0, v_used = 0, q_it = 0, dq_cnt = 0, n = 0;
+      bool ok = true;
+      PItem it;
+      for (long long r = 0; ok && load_pitem(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!(ok = wait_bar(&bars->q_full, q_it & 1, abort_flag, a, 97))) break;
+        ++q_it;
+        tc_fence_after();
+        const int nk = it.hi - it.lo;
+        for (int t = 0; t < nk; ++t) {
+          const uint32_t ki = k_used + t, vi = v_used + t, nt = n + t;
+          const int ks = ki % C::kKStages, vs = vi % C::kVStages;
+          const uint64_t kd = dK0 + ks * (kTileBytes >> 4), ktd = dKt0 + ks * (kTileBytes >> 4);
+          if (!(ok = wait_bar(&bars->k_full[ks], (ki / C::kKStages) & 1, abort_flag, a, 98))) break;
+          tc_fence_after();
+          // S^T and dP^T overwrite the P^T / dS^T columns of the tile before,
+          // which the dV / dK products issued before them have read (in order).
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_ss(tmem + C::kSCol, kd + kslice(kk, kBoxK), dQk + kslice(kk, kBoxQ), idS, kk > 0 ? 1u : 0u);
+          mma_commit(&bars->s_full);
+          if (!(ok = wait_bar(&bars->v_full[vs], (vi / C::kVStages) & 1, abort_flag, a, 99))) break;
+          tc_fence_after();
+          const uint64_t vd = dV0 + vs * (kTileBytes >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_ss(tmem + C::kDPCol, vd + kslice(kk, kBoxK), dDOk + kslice(kk, kBoxQ), idS, kk > 0 ? 1u : 0u);
+          mma_commit(&bars->dp_full);
+          mma_commit(&bars->v_empty[vs]);
+          // dV = P^T dO once P^T is in TMEM and the epilogue has drained the tile before
+          if (!(ok = wait_bar(&bars->p_ready, nt & 1, abort_flag, a, 100))) break;
+          if (!(ok = wait_bar(&bars->acc_empty, (nt & 1) ^ 1, abort_flag, a, 101))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int hl = 0; hl < C::kNP; ++hl)
+#pragma unroll
+            for (int kk = 0; kk < kQC / 16; ++kk)
+              mma_ts(tmem + C::kDVCol, tmem + C::kSCol + 32 * hl + kk * 8, dDOm + mnslice(kk), idG,
+                     (hl > 0 || kk > 0) ? 1u : 0u);
+          if (!(ok = wait_bar(&bars->ds_ready, nt & 1, abort_flag, a, 102))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int hl = 0; hl < C::kNP; ++hl)
+#pragma unroll
+            for (int kk = 0; kk < kQC / 16; ++kk)
+              mma_ts(tmem + C::kDKCol, tmem + C::kDPCol + 32 * hl + kk * 8, dQm + mnslice(kk), idG,
+                     (hl > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars->acc_full);
+          if (t == 0 && !(ok = wait_bar(&bars->dq_empty, (dq_cnt & 1) ^ 1, abort_flag, a, 103))) break;
+#pragma unroll
+          for (int hl = 0; hl < C::kNP; ++hl)
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ss(tmem + C::kDQCol, ktd + mnslice(kk), dDS0 + hl * (kPBytes >> 4) + mnslice(kk), idQ,
+                     (t > 0 || hl > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars->dsm_free);
+          mma_commit(&bars->k_empty[ks]);
+        }
+        if (!ok) break;
+        mma_commit(&bars->q_empty);
+        mma_commit(&bars->dq_full);
+        ++dq_cnt;
+        n += nk;
+        k_used += nk;
+        v_used += nk;
+      }
+      mma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0, a.timeout_ns);
+    }
+    __syncwarp();
+  }
+  } else if (warp < 8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kActRegs));
+    // ------------------------------------------------------------ activation warpgroup
+    const int row = 32 * (warp & 3) + lane;  // key row of the tile
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t sDS = smem_u32(sm + C::kDSOff);
+    uint32_t n = 0;
+    bool ok = true;
+    PItem it;
+    for (long long r = 0; ok && load_pitem(a, r, it); ++r) {
+      if (it.hi <= it.lo) continue;
+      const int nk = it.hi - it.lo;
+      for (int t = 0; t < nk; ++t) {
+        const uint32_t nt = n + t;
+        const bool valid = (it.lo + t) * kTile + row < it.lkv;
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->s_full, nt & 1, abort_flag, a, 104));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t s[kQC];
+        float gr[kQC];  // act'(x) of the item's query columns
+#pragma unroll
+        for (int c = 0; c < kQC / 32; ++c)
+          if (32 * c < it.lq) tmem_ld32(tmem + lane_base + C::kSCol + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c));
+        tmem_ld_wait();
+        // P^T (bf16) over S^T's first 32 columns (hi) and the next 32 (lo).
+        // Query columns past the item and key rows past the sequence are zero:
+        // dV and dK sum over the query columns.
+#pragma unroll
+        for (int c = 0; c < kQC / 32; ++c) {
+          uint32_t hi[16], lo[16];
+          if (32 * c < it.lq) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int q = 32 * c + 2 * e;
+              float f0, f1, g0, g1;
+              act_and_grad<ACT>(__uint_as_float(s[q]) * a.scale, f0, g0);
+              act_and_grad<ACT>(__uint_as_float(s[q + 1]) * a.scale, f1, g1);
+              const bool a0 = valid && q < it.lq, a1 = valid && q + 1 < it.lq;
+              f0 = a0 ? f0 : 0.0f;
+              f1 = a1 ? f1 : 0.0f;
+              gr[q] = a0 ? g0 : 0.0f;
+              gr[q + 1] = a1 ? g1 : 0.0f;
+              hi[e] = pack_bf16x2(f0, f1);
+              if constexpr (HILO) lo[e] = bf16x2_lo(f0, f1, hi[e]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
+          }
+          tmem_st16(tmem + lane_base + C::kSCol + 16 * c, hi);
+          if constexpr (HILO) tmem_st16(tmem + lane_base + C::kSCol + 32 + 16 * c, lo);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_ready);
+
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->dp_full, nt & 1, abort_flag, a, 105));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kQC / 32; ++c)
+          if (32 * c < it.lq) tmem_ld32(tmem + lane_base + C::kDPCol + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c));
+        tmem_ld_wait();
+        // the dQ^T products of the tile before have read the shared dS^T tile
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->dsm_free, (nt & 1) ^ 1, abort_flag, a, 106));
+        if (!ok) break;
+#pragma unroll
+        for (int c = 0; c < kQC / 32; ++c) {
+          uint32_t hi[16], lo[16];
+          if (32 * c < it.lq) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int q = 32 * c + 2 * e;
+              const float d0 = gr[q] * __uint_as_float(s[q]), d1 = gr[q + 1] * __uint_as_float(s[q + 1]);
+              hi[e] = pack_bf16x2(d0, d1);
+              if constexpr (HILO) lo[e] = bf16x2_lo(d0, d1, hi[e]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
+          }
+          tmem_st16(tmem + lane_base + C::kDPCol + 16 * c, hi);
+          if constexpr (HILO) tmem_st16(tmem + lane_base + C::kDPCol + 32 + 16 * c, lo);
+          st_pt_row(sDS, row, 32 * c, hi);
+          if constexpr (HILO) st_pt_row(sDS + kPBytes, row, 32 * c, lo);
+        }
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->ds_ready);
+      }
+      if (!ok) break;
+      n += nk;
+    }
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
+    // ------------------------------------------------------------ epilogue warpgroup
+    // dV and dK rows of every key tile; dQ of every item from dQ^T (thread =
+    // head-dim row). Items without keys get zero dQ rows.
+    const int row = 32 * (warp & 3) + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    uint32_t n = 0, dq_cnt = 0;
+    PItem it;
+    bool ok = true;
+    for (long long r = 0; ok && load_pitem(a, r, it); ++r) {
+      if (it.hi <= it.lo) {
+        store_cols(a.out0, it, a.H, row, 0, nullptr, 0.0f);
+        store_cols(a.out0, it, a.H, row, 32, nullptr, 0.0f);
+        continue;
+      }
+      const int nk = it.hi - it.lo;
+      const float cn = (a.norm_by_lkv && it.lkv > 0) ? 1.0f / it.lkv : 1.0f;
+      for (int t = 0; t < nk; ++t) {
+        const uint32_t nt = n + t;
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->acc_full, nt & 1, abort_flag, a, 107));
+        if (!ok) break;
+        tc_fence_after();
+        const int jl = (it.lo + t) * kTile + row;
+        const bool valid = jl < it.lkv;
+        const int64_t gk = it.k0 + jl;
+        __nv_bfloat16* dv_row = a.out1 + (gk * a.H + it.h) * kD;
+        __nv_bfloat16* dk_row = a.out2 + (gk * a.H + it.h) * kD;
+#pragma unroll 1
+        for (int c = 0; c < 2 * kD / 32; ++c) {
+          const bool is_dk = c >= kD / 32;
+          const int cc = is_dk ? c - kD / 32 : c;
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + (is_dk ? C::kDKCol : C::kDVCol) + 32 * cc, v);
+          tmem_ld_wait();
+          if (c == 2 * kD / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&bars->acc_empty);
+          }
+          if (valid) {
+            uint32_t w[16];
+            const float mul = is_dk ? cn * a.scale : cn;
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+            store_words16((is_dk ? dk_row : dv_row) + 32 * cc, w, a.out_v8);
+          }
+        }
+      }
+      if (!ok) break;
+      n += nk;
+      ok = __all_sync(0xffffffffu, wait_bar(&bars->dq_full, dq_cnt & 1, abort_flag, a, 108));
+      if (!ok) break;
+      ++dq_cnt;
+      tc_fence_after();
+      uint32_t v[kQC];
+#pragma unroll
+      for (int c = 0; c < kQC / 32; ++c)
+        if (32 * c < it.lq) tmem_ld32(tmem + lane_base + C::kDQCol + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->dq_empty);
+#pragma unroll
+      for (int c = 0; c < kQC / 32; ++c)
+        if (32 * c < it.lq) store_cols(a.out0, it, a.H, row, 32 * c, v + 32 * c, cn * a.scale);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// Whether every sequence suits the fused backward (1 <= Lq <= 64, or no keys
+// at all). If so, the general dQ and dK/dV schedules are emptied so their
+// passes find no work; else the gate stays closed and the fused pass returns.
+__global__ void __launch_bounds__(1024) pma_gate_kernel(const int64_t* q_off, const int64_t* kv_off, int64_t B,
+                                                        int* gate, int* n_tiles_q, int* n_tiles_kv) {
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  for (int64_t b = threadIdx.x; b < B; b += blockDim.x) {
+    const int64_t lq = q_off[b + 1] - q_off[b], lkv = kv_off[b + 1] - kv_off[b];
+    if (lq > kQC || lq < 0 || lkv < 0 || (lq == 0 && lkv > 0)) bad = 1;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    *gate = bad ? 0 : 1;
+    if (!bad) {
+      *n_tiles_q = 0;
+      *n_tiles_kv = 0;
+    }
+  }
+}
+
+template <typename K>
+cudaError_t launch_k(K kernel, int smem, int grid, cudaStream_t st, const CUtensorMap& q, const CUtensorMap& k,
+                     const CUtensorMap& v, const AttnArgs& a) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kThreads, smem, st>>>(q, k, v, a);
+  return cudaGetLastError();
+}
+
+template <int ACT>
+cudaError_t fwd_act(bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const AttnArgs& a,
+                    int grid, cudaStream_t st) {
+  if (hilo) return launch_k(pma_fwd_kernel<ACT, true>, PfCfg<true>::kSmemBytes, grid, st, q, k, v, a);
+  return launch_k(pma_fwd_kernel<ACT, false>, PfCfg<false>::kSmemBytes, grid, st, q, k, v, a);
+}
+
+template <int ACT, bool HILO>
+cudaError_t bwd_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
+                    const AttnArgs& a, const int* gate, int grid, cudaStream_t st) {
+  auto kernel = pma_bwd_kernel<ACT, HILO>;
+  constexpr int smem = PbCfg<HILO>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kThreads, smem, st>>>(q, k, v, dout, a, gate);
+  return cudaGetLastError();
+}
+
+template <int ACT>
+cudaError_t bwd_act(bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                    const CUtensorMap& dout, const AttnArgs& a, const int* gate, int grid, cudaStream_t st) {
+  return hilo ? bwd_one<ACT, true>(q, k, v, dout, a, gate, grid, st)
+              : bwd_one<ACT, false>(q, k, v, dout, a, gate, grid, st);
+}
+
+}  // namespace
+
+cudaError_t launch_pma_fwd(int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                           const AttnArgs& a, int grid, cudaStream_t stream) {
+  switch (act) {
+    case JATTN_SILU: return fwd_act<JATTN_SILU>(hilo, q, k, v, a, grid, stream);
+    case JATTN_GELU_TANH: return fwd_act<JATTN_GELU_TANH>(hilo, q, k, v, a, grid, stream);
+    case JATTN_GELU_POLY: return fwd_act<JATTN_GELU_POLY>(hilo, q, k, v, a, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_pma_gate(const int64_t* q_off, const int64_t* kv_off, int64_t B, int* gate, int* n_tiles_q,
+                            int* n_tiles_kv, cudaStream_t stream) {
+  pma_gate_kernel<<<1, 1024, 0, stream>>>(q_off, kv_off, B, gate, n_tiles_q, n_tiles_kv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pma_bwd(int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                           const CUtensorMap& dout, const AttnArgs& a, const int* gate, int grid,
+                           cudaStream_t stream) {
+  switch (act) {
+    case JATTN_SILU: return bwd_act<JATTN_SILU>(hilo, q, k, v, dout, a, gate, grid, stream);
+    case JATTN_GELU_TANH: return bwd_act<JATTN_GELU_TANH>(hilo, q, k, v, dout, a, gate, grid, stream);
+    case JATTN_GELU_POLY: return bwd_act<JATTN_GELU_POLY>(hilo, q, k, v, dout, a, gate, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int pma_rows_per_item() { return kQC; }
+
+}  // namespace jattn

@@ -1,0 +1,134 @@
+"""The short-query (pooling) kernels: keys on the MMA's M dimension for
+pointwise attention without a mask at D = 128 when sequences average at most
+64 queries. CUDA path vs the oracle element by element, a gate that hands
+batches with longer (or empty) query sequences back to the general backward,
+the rows the stores touch, and the bounded waits."""
+import numpy as np
+import pytest
+import torch
+
+from jagged_attention_recsys_gdpa_gb300 import inputs
+from tests import gpu_helpers as G
+
+pytestmark = pytest.mark.gpu
+
+SILU, GELU, POLY = 1, 2, 3
+NO_SHORT_Q = 32  # debug flag bit: the general kernels even for pooling shapes
+JATTN_ERR_TIMEOUT = 6
+
+# every sequence 1 <= Lq <= 64 (or no keys): the fused backward runs
+OPEN_LQ = [32, 1, 64, 33, 31, 5, 64, 17, 3]
+OPEN_LKV = [1000, 129, 128, 1, 3000, 0, 257, 700, 0]
+# one sequence of 100 queries (two 64-row items in the forward) and one with
+# keys but no queries: the forward still takes the short-query kernels, the
+# backward the general ones
+CLOSED_LQ = [32, 100, 0, 7, 20, 1, 30, 2]
+CLOSED_LKV = [500, 300, 129, 1000, 0, 64, 2000, 5]
+
+
+def _w(act, norm=True, H=3, qk=0.0):
+    return inputs.Workload("case", H, 128, act, 0, 0, norm, 0.5, False, qk)
+
+
+def _check(w, lq, lkv, seed, flags=0):
+    from jagged_attention_recsys_gdpa_gb300 import _binding as B
+
+    assert sum(lq) <= 64 * len(lq)  # the shape the short-query kernels take
+    cpu = G.cpu_inputs(w, lq, lkv, seed)
+    B.debug_set(flags, 0)
+    try:
+        g = G.gpu_run(G.to_cuda(cpu), w)
+    finally:
+        B.debug_set(0, 0)
+    G.compare(g, G.oracle_run(cpu, w), w)
+    return g
+
+
+@pytest.mark.parametrize("norm", [True, False])
+@pytest.mark.parametrize("act", [SILU, GELU])
+def test_short_query_matches_oracle(act, norm):
+    """Ragged key tiles (1, 127-129 keys), sequences without keys (zero O and
+    dQ), 1 to 64 queries per sequence; with and without the 1/Lkv normaliser
+    (P and dS as bf16 hi + lo parts without it)."""
+    _check(_w(act, norm), OPEN_LQ, OPEN_LKV, seed=80 + act + 2 * norm)
+
+
+def test_short_query_gelu_poly():
+    """The ALU-only GELU on query/key-normalised rows (|s| <= 1)."""
+    _check(_w(POLY, qk=1.0), OPEN_LQ, OPEN_LKV, seed=85)
+
+
+@pytest.mark.parametrize("act", [SILU, GELU])
+def test_short_query_pooling_long_keys(act):
+    """Pooling lengths: 32 learned queries against up to 20,000 keys."""
+    _check(_w(act, H=2), [32, 32, 32, 32, 32], [20000, 5000, 1, 128, 4097], seed=86)
+
+
+@pytest.mark.parametrize("act", [SILU, GELU])
+def test_short_query_gate_closed(act):
+    """A sequence of 100 queries and one with keys but no queries: the
+    forward's items split the 100 queries in two, and the gate leaves the
+    backward (dK = dV = 0 for the keys no query sees) to the general kernels."""
+    _check(_w(act), CLOSED_LQ, CLOSED_LKV, seed=87)
+
+
+@pytest.mark.parametrize("norm", [True, False])
+def test_short_query_agrees_with_general_kernels(norm):
+    """The same inputs through the short-query and the general kernels: both
+    within the tolerance of the oracle, and close to each other."""
+    w = _w(GELU, norm)
+    a = _check(w, OPEN_LQ, OPEN_LKV, seed=88)
+    b = _check(w, OPEN_LQ, OPEN_LKV, seed=88, flags=NO_SHORT_Q)
+    for k in ("o", "dq", "dk", "dv"):
+        G.assert_close(G.to64(a[k]), G.to64(b[k]), k)
+
+
+def test_short_query_outputs_only_touch_their_rows():
+    """Canary rows around O, dQ, dK and dV stay untouched."""
+    import jagged_attention_recsys_gdpa_gb300 as J
+
+    w = _w(GELU)
+    cpu = G.cpu_inputs(w, OPEN_LQ, OPEN_LKV, 89)
+    x = G.to_cuda(cpu)
+    TQ, TK, pad = x["q"].shape[0], x["k"].shape[0], 5
+    big = lambda T: torch.full((T + 2 * pad, w.H, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    bo, bq, bk, bv = big(TQ), big(TQ), big(TK), big(TK)
+    o, dq, dk, dv = bo[pad : pad + TQ], bq[pad : pad + TQ], bk[pad : pad + TK], bv[pad : pad + TK]
+    kw = dict(act=GELU, norm_by_lkv=True)
+    J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], out=o, **kw)
+    J.backward(x["q"], x["k"], x["v"], o, None, x["do"], x["q_off"], x["kv_off"], dq=dq, dk=dk, dv=dv, **kw)
+    torch.cuda.synchronize()
+    for b, T in ((bo, TQ), (bq, TQ), (bk, TK), (bv, TK)):
+        assert torch.all(b[:pad] == 7.0) and torch.all(b[pad + T :] == 7.0)
+    G.compare({"o": o, "lse": None, "dq": dq, "dk": dk, "dv": dv}, G.oracle_run(cpu, w), w)
+
+
+def test_short_query_waits_time_out_then_recover():
+    """With the query copies skipped, the short-query forward and backward give
+    up their bounded waits, report TIMEOUT and return; clean calls on the same
+    context afterwards are correct."""
+    import jagged_attention_recsys_gdpa_gb300 as J
+    from jagged_attention_recsys_gdpa_gb300 import _binding as B
+
+    w = _w(SILU)
+    cpu = G.cpu_inputs(w, OPEN_LQ, OPEN_LKV, 90)
+    x = G.to_cuda(cpu)
+    kw = dict(act=SILU, norm_by_lkv=True)
+    J.device_status()
+    try:
+        B.debug_set(1, 50_000_000)
+        J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], **kw)
+        assert J.device_status() == JATTN_ERR_TIMEOUT
+    finally:
+        B.debug_set(0, 0)
+    o, _ = J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], **kw)
+    assert J.device_status() == 0
+    try:
+        B.debug_set(1, 50_000_000)
+        J.backward(x["q"], x["k"], x["v"], o, None, x["do"], x["q_off"], x["kv_off"], **kw)
+        assert J.device_status() == JATTN_ERR_TIMEOUT
+    finally:
+        B.debug_set(0, 0)
+    g = G.gpu_run(x, w)
+    assert J.device_status() == 0
+    G.compare(g, G.oracle_run(cpu, w), w)
