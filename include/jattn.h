@@ -112,11 +112,22 @@ typedef struct {
  * lengths tested (20000 keys per pooling query, 8000 queries per key). */
 
 /* Bytes of workspace jattn_fwd / jattn_bwd need for these sizes (depends on
- * B, total_q, total_kv, H, act and the block bit of mask only). The workspace must be 256-byte
+ * B, total_q, total_kv, H, D, act and mask only). The workspace must be 256-byte
  * aligned device memory whose first 256 bytes (the device status word) are
  * zero before its first use; jattn_get_status clears them again. Returns
  * JATTN_ERR_INVALID on bad params. */
 int jattn_workspace_size(const jattn_params_t* p, size_t* bytes);
+
+/* Pooling-shaped calls ("GEM Training" post, section "Generalized Dot-Product
+ * Attention (GDPA)": a few learned queries per sequence against long key
+ * sequences) run on kernels that put 128 keys on the MMA's M dimension
+ * instead of a 128-row query tile that would be mostly padding: a pointwise
+ * activation, mask JATTN_MASK_NONE, D = 128 and total_q <= 64 B. The forward
+ * takes every such call (a sequence of more than 64 queries is served in
+ * 64-row pieces). The backward fuses dQ, dK and dV into one pass over the
+ * keys when every sequence has 1 <= Lq <= 64 or no keys (checked on the
+ * device, without a host round trip), else it runs the general passes.
+ * Results and their precision are the same as on the general kernels. */
 
 /* Forward. Reads q [total_q,H,D], k and v [total_kv,H,D]; writes every row of
  * o [total_q,H,D] and, for JATTN_SOFTMAX, lse [total_q,H] (must be non-NULL

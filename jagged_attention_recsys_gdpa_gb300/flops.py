@@ -41,7 +41,20 @@ def effective_flops(pairs: int, H: int, D: int):
     return 4.0 * D * H * pairs, 10.0 * D * H * pairs
 
 
-def kernel_work(total_q: int, total_kv: int, pairs: int, H: int, D: int, softmax: bool, in_tile: bool = False):
+def short_query_path(act: int, mask: int, D: int, lq, lkv) -> bool:
+    """Whether the library runs a batch on its short-query (pooling) kernels
+    in both directions: a pointwise activation, no mask, D = 128, at most 64
+    queries per sequence on average (the forward's rule) and every sequence
+    with 1 <= Lq <= 64 or no keys (the backward's device-side gate)."""
+    lq = np.asarray(lq, dtype=np.int64)
+    lkv = np.asarray(lkv, dtype=np.int64)
+    if act == 0 or mask != 0 or D != 128 or len(lq) == 0 or int(lq.sum()) > 64 * len(lq):
+        return False
+    return bool(np.all(((lq >= 1) & (lq <= 64)) | (lkv == 0)))
+
+
+def kernel_work(total_q: int, total_kv: int, pairs: int, H: int, D: int, softmax: bool, in_tile: bool = False,
+                short_q: bool = False):
     """Algorithmic FLOPs and HBM bytes of each kernel (each byte read or written once).
 
     forward: reads Q, K, V, writes O (+ LSE)
@@ -51,12 +64,22 @@ def kernel_work(total_q: int, total_kv: int, pairs: int, H: int, D: int, softmax
              With in-tile statistics (BlockAttention whose blocks divide the
              tile) it reads neither O nor LSE and writes LSE and Di instead.
     dkdv:    reads Q, K, V, dO (+ LSE, Di), writes dK, dV; products S, dP, dV, dK
+
+    short_q (the short-query kernels): the fused backward, timed in the dK/dV
+    slot, reads Q, dO, K, V once and writes dQ, dK, dV, computing all five
+    products; the general dQ pass then finds no work.
     """
     e = 2 * H * D  # bytes of one row of a [total, H, D] bf16 tensor
     stats = 4 * H * total_q
     dq_extra = 0
     if softmax:
         dq_extra = 2 * stats if in_tile else e * total_q + 2 * stats
+    if short_q:
+        return {
+            "fwd": {"flops": 4.0 * D * H * pairs, "bytes": e * (2 * total_q + 2 * total_kv)},
+            "dkdv": {"flops": 10.0 * D * H * pairs, "bytes": e * (3 * total_q + 4 * total_kv)},
+            "dq": {"flops": 0.0, "bytes": 0.0},
+        }
     return {
         "fwd": {"flops": 4.0 * D * H * pairs, "bytes": e * (2 * total_q + 2 * total_kv) + (stats if softmax else 0)},
         "dkdv": {"flops": 8.0 * D * H * pairs,

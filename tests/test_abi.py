@@ -213,3 +213,29 @@ def test_header_is_plain_c_and_links(tmp_path, lib):
     rc, nbytes, rest = out.stdout.split(" ", 2)
     assert rc == "0" and int(nbytes) == B.workspace_size(_params(B=2, total_q=100, total_kv=100, H=4, D=128, mask=1))
     assert rest.strip().endswith(" 6") and "offsets" in rest
+
+
+def test_short_query_shapes_hold_their_schedule(lib):
+    """Pooling-shaped parameters (pointwise, no mask, D = 128, at most 64
+    queries per sequence on average) reserve the short-query schedule and gate
+    word in the workspace; other shapes do not."""
+    pma = dict(B=512, total_q=16384, total_kv=1_600_000, H=8, D=128, act=2, mask=0, norm_by_lkv=1)
+    base = B.workspace_size(_params(**pma))
+    assert base > B.workspace_size(_params(**{**pma, "mask": 1}))                  # causal: general kernels only
+    assert base > B.workspace_size(_params(**{**pma, "total_q": 64 * 512 + 1}))    # longer queries on average
+    assert B.workspace_size(_params(**{**pma, "D": 64})) < base
+
+
+def test_short_query_path_rule():
+    """bench.py's accounting mirrors the library's rule for the short-query path."""
+    from jagged_attention_recsys_gdpa_gb300 import flops
+
+    assert flops.short_query_path(2, 0, 128, [32, 32, 1], [2000, 0, 5])
+    assert flops.short_query_path(1, 0, 128, [64, 3], [1, 1])
+    assert flops.short_query_path(1, 0, 128, [5, 0], [7, 0])        # no queries and no keys: fine
+    assert not flops.short_query_path(0, 0, 128, [32], [100])       # softmax
+    assert not flops.short_query_path(1, 1, 128, [32], [100])       # causal
+    assert not flops.short_query_path(1, 0, 64, [32], [100])        # D = 64
+    assert not flops.short_query_path(1, 0, 128, [65, 1], [10, 10])  # a sequence beyond 64 queries (gate)
+    assert not flops.short_query_path(1, 0, 128, [0, 32], [10, 10])  # keys no query sees (gate)
+    assert not flops.short_query_path(1, 0, 128, [100, 100], [1, 1])  # average beyond 64
