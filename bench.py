@@ -290,9 +290,11 @@ def main():
     # BlockAttention with blocks that divide the tile on self-attention: the
     # backward takes its statistics from the tile (no O or LSE read)
     in_tile = w.act == 0 and bool(w.mask & 4) and 128 % w.window == 0 and x["kv_off"] is x["q_off"]
-    # pooling shapes run on the short-query kernels (a fused backward)
+    # pooling shapes run on the short-query kernels, cross-attention over short
+    # key sequences on the general forward; both on the fused backward
     short_q = flops.short_query_path(w.act, w.mask, w.D, x["lq"], x["lkv"])
-    work = flops.kernel_work(tq, tk, pairs, w.H, w.D, w.act == 0, in_tile=in_tile, short_q=short_q)
+    fused = short_q or flops.short_key_path(w.act, w.mask, w.D, x["lq"], x["lkv"])
+    work = flops.kernel_work(tq, tk, pairs, w.H, w.D, w.act == 0, in_tile=in_tile, fused_bwd=fused)
     o = torch.empty_like(x["q"])
     lse = torch.empty(tq, w.H, dtype=torch.float32, device=dev) if w.act == 0 else None
     dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
@@ -329,7 +331,7 @@ def main():
     }
 
     # The step (15 launches: three tile schedules of four kernels, the forward,
-    # dQ with Di, dK/dV; 21 on the short-query path) captured once as a CUDA graph and replayed, so launch
+    # dQ with Di, dK/dV; 21 with the fused backward) captured once as a CUDA graph and replayed, so launch
     # gaps between its short kernels disappear; eager launches are used if
     # capture is not possible.
     run = step
@@ -388,8 +390,9 @@ def main():
     roof["traffic_unit"] = "bytes per launch (ncu dram read + write)"
     roof["algorithmic"] = wk["bytes"] if roof["bound"] == "hbm" else wk["flops"]
     roof["kernel"] = dom
-    if short_q:
-        roof["kernel_name"] = {"fwd": "pma_fwd_kernel", "dkdv": "pma_bwd_kernel (fused dQ, dK, dV)"}.get(dom, dom)
+    if fused:
+        roof["kernel_name"] = {"fwd": "pma_fwd_kernel" if short_q else "fwd_kernel",
+                               "dkdv": "pma_bwd_kernel (fused dQ, dK, dV)"}.get(dom, dom)
     roof["peak_source"] = peaks["source"] + " (burst)"
 
     # end to end through the public API: pinned host inputs, copies inside the timed region
@@ -512,10 +515,10 @@ def main():
             "cpu_baseline": cpu_base,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             # per step: three tile schedules of four kernels each, the forward,
-            # dQ (which also computes softmax's Di) and dK/dV; the short-query
-            # path adds a fourth schedule, the gate and the fused backward (the
-            # general dQ and dK/dV passes still launch and find no work)
-            "gpu_launches": (21 if short_q else 15) * args.steps,
+            # dQ (which also computes softmax's Di) and dK/dV; the fused
+            # backward adds a fourth schedule, the gate and itself (the general
+            # dQ and dK/dV passes still launch and find no work)
+            "gpu_launches": (21 if fused else 15) * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -53,16 +53,28 @@ int cuda_fail(const char* what, cudaError_t e) {
 // mistaken for a failed launch of ours.
 void clear_stale_error() { (void)cudaGetLastError(); }
 
-// Pooling-shaped calls (pointwise activation, no mask, D = 128, at most 64
-// queries per sequence on average) run the short-query kernels, which put the
-// keys on the MMA's M dimension (pma.cu). The workspace holds their schedule
-// and gate word whenever the shape allows them; debug flag bit 32 keeps the
-// general kernels.
+// Pointwise attention without a mask at D = 128 runs on the kernels that put
+// the keys on the MMA's M dimension (pma.cu) when its sequences are short on
+// one side: pooling (at most 64 queries per sequence on average: forward and
+// fused backward) or cross-attention over short key sequences (at most 128
+// keys per sequence on average: fused backward; the general forward). The
+// workspace holds their schedule and gate word whenever the shape allows
+// them. Debug flag bit 32 keeps the general kernels; bit 64 also runs the
+// short-key shapes' forward on the short-query kernel (for comparisons).
+bool pointwise_unmasked(const jattn_params_t& p) {
+  return p.act != JATTN_SOFTMAX && p.mask == JATTN_MASK_NONE && p.D == 128;
+}
 bool short_q_shape(const jattn_params_t& p) {
-  return p.act != JATTN_SOFTMAX && p.mask == JATTN_MASK_NONE && p.D == 128 &&
-         p.total_q <= static_cast<int64_t>(pma_rows_per_item()) * p.B;
+  return pointwise_unmasked(p) && p.total_q <= static_cast<int64_t>(pma_rows_per_item()) * p.B;
+}
+bool short_kv_shape(const jattn_params_t& p) {
+  return pointwise_unmasked(p) && !short_q_shape(p) && p.total_kv <= static_cast<int64_t>(kTile) * p.B;
 }
 bool use_short_q(const jattn_params_t& p) { return short_q_shape(p) && !(g_debug_flags & 32); }
+bool use_short_kv(const jattn_params_t& p) { return short_kv_shape(p) && !(g_debug_flags & 32); }
+bool use_short_q_fwd(const jattn_params_t& p) {
+  return use_short_q(p) || (use_short_kv(p) && (g_debug_flags & 64));
+}
 
 struct Layout {
   size_t status, sched_fwd, sched_q, sched_kv, sched_s, gate, di, lse, total;
@@ -86,8 +98,11 @@ Layout layout_for(const jattn_params_t& p) {
   off += al256(sched_ws_bytes(p.B, L.tiles_kv));
   L.sched_s = L.gate = off;
   L.tiles_s = 0;
-  if (short_q_shape(p)) {
-    L.tiles_s = sched_max_tiles(p.B, p.total_q, pma_rows_per_item());
+  if (short_q_shape(p) || short_kv_shape(p)) {
+    // pooling: 64-row query tiles; cross: 128-row key tiles (and, under debug
+    // flag bit 64, the forward's 64-row query tiles)
+    L.tiles_s = std::max(sched_max_tiles(p.B, p.total_q, pma_rows_per_item()),
+                         short_kv_shape(p) ? sched_max_tiles(p.B, p.total_kv, kTile) : int64_t(0));
     off += al256(sched_ws_bytes(p.B, L.tiles_s));
     L.gate = off;
     off += 256;
@@ -381,7 +396,7 @@ int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
   char* base = static_cast<char*>(ws);
   AttnArgs a = base_args(*p, q_off, kv_off, ws);
   cudaError_t e;
-  if (use_short_q(*p)) {
+  if (use_short_q_fwd(*p)) {
     const SchedView ss = sched_carve(base + L.sched_s, p->B, L.tiles_s);
     if ((e = sched_launch(ss, q_off, kv_off, p->B, p->total_q, p->total_kv, pma_rows_per_item(), kTile, p->mask,
                           a.window, 0, a.status, st)) != cudaSuccess)
@@ -669,21 +684,26 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
   a.in_tile_stats = in_tile ? 1 : 0;
   const SchedView qs = sched_carve(base + L.sched_q, p->B, L.tiles_q);
   const SchedView kv = sched_carve(base + L.sched_kv, p->B, L.tiles_kv);
-  // Short-query (pooling) shapes: the fused pass runs first and, when the gate
-  // finds every sequence within its limits, the general passes below find
-  // empty schedules. The profiling events of the dK/dV slot bracket it.
-  const bool sq = use_short_q(*p) && !rope_cos && p->total_q > 0 && p->total_kv > 0;
+  // Short-query (pooling) and short-key (cross) shapes: the fused pass runs
+  // first and, when the gate finds every sequence within its mode's limits,
+  // the general passes below find empty schedules. The profiling events of
+  // the dK/dV slot bracket it.
+  const bool cross = use_short_kv(*p);
+  const bool sq = (use_short_q(*p) || cross) && !rope_cos && p->total_q > 0 && p->total_kv > 0;
   if (sq) {
     const SchedView ss = sched_carve(base + L.sched_s, p->B, L.tiles_s);
-    if ((e = sched_launch(ss, q_off, kv_off, p->B, p->total_q, p->total_kv, pma_rows_per_item(), kTile, p->mask,
-                          a.window, 0, a.status, st)) != cudaSuccess ||
+    // pooling: 64-row query tiles over the key tiles; cross: 128-row key tiles
+    // over 64-row query chunks
+    const int srow = cross ? kTile : pma_rows_per_item(), scol = cross ? pma_rows_per_item() : kTile;
+    if ((e = sched_launch(ss, q_off, kv_off, p->B, p->total_q, p->total_kv, srow, scol, p->mask, a.window,
+                          cross ? 1 : 0, a.status, st)) != cudaSuccess ||
         (e = sched_launch(qs, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 0,
                           a.status, st)) != cudaSuccess ||
         (e = sched_launch(kv, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 1,
                           a.status, st)) != cudaSuccess)
       return cuda_fail("schedule launch", e);
     int* gate = reinterpret_cast<int*>(base + L.gate);
-    if ((e = launch_pma_gate(q_off, kv_off, p->B, gate, qs.n_tiles, kv.n_tiles, st)) != cudaSuccess)
+    if ((e = launch_pma_gate(q_off, kv_off, p->B, cross, gate, qs.n_tiles, kv.n_tiles, st)) != cudaSuccess)
       return cuda_fail("short-query gate launch", e);
     CUtensorMap sq_q, sq_do;
     if (make_map(&sq_q, q, p->total_q, p->H, p->D, pma_rows_per_item()) ||
@@ -697,8 +717,8 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
     b.out2 = reinterpret_cast<__nv_bfloat16*>(dk);
     b.out_v8 = aligned32(dk) && aligned32(dv);
     prof(2, st);
-    if ((e = launch_pma_bwd(p->act, hilo_for(*p), sq_q, mk, mv, sq_do, b, gate, grid_for(dev, L.tiles_s, p->H),
-                            st)) != cudaSuccess)
+    if ((e = launch_pma_bwd(p->act, hilo_for(*p), cross, sq_q, mk, mv, sq_do, b, gate,
+                            grid_for(dev, L.tiles_s, p->H), st)) != cudaSuccess)
       return cuda_fail("short-query backward kernel launch", e);
     prof(3, st);
   }

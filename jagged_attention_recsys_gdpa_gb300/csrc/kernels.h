@@ -63,20 +63,24 @@ cudaError_t launch_bwd_dq_hilo(int D, int act, bool split, const CUtensorMap& q,
                                const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& o, const AttnArgs& a,
                                int grid, cudaStream_t stream);
 
-// Short-query attention (pooling; pma.cu): pointwise activations, no mask,
-// D = 128, items of at most 64 query rows from the 64-row query-tile
-// schedule, keys on the MMA's M dimension. The forward's Q map has 64-row
-// boxes (a.out0 = O). The backward (Q and dO maps with 64-row boxes; a.out0 =
-// dQ, a.out1 = dV, a.out2 = dK) runs only when launch_pma_gate found every
-// sequence with 1 <= Lq <= 64 (or no keys); the gate then empties the general
-// dQ and dK/dV schedules.
+// Short-query / short-key attention (pma.cu): pointwise activations, no
+// mask, D = 128, keys on the MMA's M dimension and at most 64 queries per
+// product. The forward takes items of at most 64 query rows from the 64-row
+// query-tile schedule; its Q map has 64-row boxes (a.out0 = O). The fused
+// backward (Q and dO maps with 64-row boxes; a.out0 = dQ, a.out1 = dV, a.out2
+// = dK) has a pooling mode (items from the 64-row query-tile schedule, every
+// sequence with 1 <= Lq <= 64 or no keys) and a cross mode (`cross`: items
+// from the 128-row key-tile schedule with 64-column query ranges, every
+// sequence with Lkv <= 128 and keys whenever it has queries). It runs only
+// when launch_pma_gate found the batch within its mode's limits; the gate
+// then empties the general dQ and dK/dV schedules.
 cudaError_t launch_pma_fwd(int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                            const AttnArgs& a, int grid, cudaStream_t stream);
-cudaError_t launch_pma_gate(const int64_t* q_off, const int64_t* kv_off, int64_t B, int* gate, int* n_tiles_q,
-                            int* n_tiles_kv, cudaStream_t stream);
-cudaError_t launch_pma_bwd(int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                           const CUtensorMap& dout, const AttnArgs& a, const int* gate, int grid,
-                           cudaStream_t stream);
+cudaError_t launch_pma_gate(const int64_t* q_off, const int64_t* kv_off, int64_t B, bool cross, int* gate,
+                            int* n_tiles_q, int* n_tiles_kv, cudaStream_t stream);
+cudaError_t launch_pma_bwd(int act, bool hilo, bool cross, const CUtensorMap& q, const CUtensorMap& k,
+                           const CUtensorMap& v, const CUtensorMap& dout, const AttnArgs& a, const int* gate,
+                           int grid, cudaStream_t stream);
 int pma_rows_per_item();
 
 // Rotary embedding of a jagged tensor x ([total, H, D] bf16, rows described

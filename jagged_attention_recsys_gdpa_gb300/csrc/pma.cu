@@ -53,17 +53,19 @@ constexpr int kTileBytes = 2 * kBoxK;        // K or V tile: [128 keys][128]
 constexpr int kChunkBytes = 2 * kBoxQ;       // Q or dO chunk: [64 queries][128]
 constexpr int kPBytes = kTile * kQC * 2;     // P^T or dS^T: [128 keys][64 queries] bf16
 constexpr float kLog2e = 1.4426950408889634f;
-// Backward register split (setmaxnreg, per warpgroup): 384 x 168 at launch =
-// 64512 >= 128 x (control + activation + epilogue). The activation threads
-// hold a key row's 64 scores and 64 activation derivatives. A warpgroup that
-// ends below the launch count lowers its share (.dec), one above it raises
-// it (.inc): .inc may not ask for fewer registers than the warp holds.
-constexpr int kLaunchRegs = 168;
+// Backward: 16 warps, register split (setmaxnreg, per warpgroup): 512 x 128
+// at launch = 65536 >= 128 x (control + 2 activation + epilogue). Each
+// activation thread holds a key row's 32 scores and 32 activation
+// derivatives. A warpgroup that ends below the launch count lowers its share
+// (.dec), one above it raises it (.inc): .inc may not ask for fewer registers
+// than the warp holds.
+constexpr int kBwdThreads = 512;
+constexpr int kLaunchRegs = 128;
 constexpr int kCtlRegs = 136;
-constexpr int kActRegs = 216;
-constexpr int kEpiRegs = 152;
-static_assert(128 * (kCtlRegs + kActRegs + kEpiRegs) <= kThreads * kLaunchRegs, "register split");
-static_assert(kCtlRegs <= kLaunchRegs && kEpiRegs <= kLaunchRegs && kActRegs >= kLaunchRegs,
+constexpr int kActRegs = 128;
+constexpr int kEpiRegs = 120;
+static_assert(128 * (kCtlRegs + 2 * kActRegs + kEpiRegs) <= kBwdThreads * kLaunchRegs, "register split");
+static_assert(kCtlRegs >= kLaunchRegs && kEpiRegs <= kLaunchRegs && kActRegs == kLaunchRegs,
               "dec / inc directions of the split");
 
 __device__ __forceinline__ float tanh_approx(float x) {
@@ -441,14 +443,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------- backward
-template <bool HILO>
+// Two modes share the kernel. Pooling (CROSS = false): an item is (sequence,
+// head) with at most 64 queries, loaded once, and its key tiles are the steps;
+// dV and dK are complete per step, dQ^T accumulates over the item. Cross
+// attention over short key sequences (CROSS = true): an item is (sequence,
+// head) with at most 128 keys, loaded once, and its 64-query chunks are the
+// steps; dQ^T is complete per step, dV and dK accumulate over the item.
+template <bool HILO, bool CROSS>
 struct PbCfg {
-  static constexpr int kKStages = 3;
-  static constexpr int kVStages = 2;
+  static constexpr int kQDStages = CROSS ? 4 : 1;  // Q + dO chunk pairs
+  static constexpr int kKStages = CROSS ? 1 : 3;
+  static constexpr int kVStages = CROSS ? 1 : 2;
   static constexpr int kNP = HILO ? 2 : 1;  // dS^T tiles in shared memory (hi, lo)
-  static constexpr int kQOff = 0;
-  static constexpr int kDOOff = kChunkBytes;
-  static constexpr int kKOff = 2 * kChunkBytes;
+  static constexpr int kQDOff = 0;          // stage s: Q chunk, then dO chunk
+  static constexpr int kKOff = kQDStages * 2 * kChunkBytes;
   static constexpr int kVOff = kKOff + kKStages * kTileBytes;
   static constexpr int kDSOff = kVOff + kVStages * kTileBytes;
   static constexpr int kBarOff = kDSOff + kNP * kPBytes;
@@ -456,10 +464,12 @@ struct PbCfg {
   // TMEM: S^T (P^T as bf16 over its first columns), dP^T (dS^T likewise), dV, dK, dQ^T
   static constexpr uint32_t kSCol = 0, kDPCol = 64, kDVCol = 128, kDKCol = 256, kDQCol = 384;
 };
-static_assert(PbCfg<false>::kSmemBytes <= 227 * 1024 && PbCfg<true>::kSmemBytes <= 227 * 1024, "shared memory");
+static_assert(PbCfg<false, false>::kSmemBytes <= 227 * 1024 && PbCfg<true, false>::kSmemBytes <= 227 * 1024 &&
+                  PbCfg<false, true>::kSmemBytes <= 227 * 1024 && PbCfg<true, true>::kSmemBytes <= 227 * 1024,
+              "shared memory");
 
 struct PbBars {
-  uint64_t q_full, q_empty;  // Q and dO chunks of an item
+  uint64_t qd_full[4], qd_empty[4];  // Q and dO chunks
   uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
   uint64_t s_full, dp_full, p_ready, ds_ready, dsm_free;
   uint64_t acc_full, acc_empty, dq_full, dq_empty, drain;
@@ -468,13 +478,58 @@ struct PbBars {
 };
 static_assert(sizeof(PbBars) <= 256, "barrier block overflows its slot");
 
-template <int ACT, bool HILO>
-__global__ void __launch_bounds__(kThreads, 1)
+// Item of the fused backward: pooling items come from the 64-row query-tile
+// schedule (one tile per sequence; [lo, hi) = key tiles), cross items from
+// the 128-row key-tile schedule with 64-column query ranges (one tile per
+// sequence; [lo, hi) = query chunks).
+template <bool CROSS>
+__device__ __forceinline__ bool load_bitem(const AttnArgs& a, long long round, PItem& it) {
+  if constexpr (!CROSS) {
+    return load_pitem(a, round, it);
+  } else {
+    const long long n_items = static_cast<long long>(*a.n_tiles) * a.H;
+    const long long k = zigzag_item(round, blockIdx.x, gridDim.x);
+    if (k >= n_items) return false;
+    const int4 t = a.tiles[k / a.H];
+    it.h = static_cast<int>(k % a.H);
+    it.b = t.x;
+    it.rt = t.y;  // key tile (0: the gate admits at most 128 keys)
+    it.lo = t.z;
+    it.hi = t.w;
+    it.q0 = a.q_off[it.b];
+    it.lq = static_cast<int>(a.q_off[it.b + 1] - it.q0);
+    it.k0 = a.kv_off[it.b];
+    it.lkv = static_cast<int>(a.kv_off[it.b + 1] - it.k0);
+    return true;
+  }
+}
+
+// Queries [c0, c0 + 32) of a chunk whose first row is q_first and which holds
+// nq rows: thread d writes out[q][h][d] from 32 fp32 accumulator columns
+// times mul (nullptr: zeros). A warp's lanes write 64 contiguous bytes per query.
+__device__ __forceinline__ void store_chunk_cols(__nv_bfloat16* out, int64_t q_first, int nq, int H, int h, int d,
+                                                 int c0, const uint32_t* v, float mul) {
+  for (int e = 0; e < 32; ++e) {
+    const int q = c0 + e;
+    if (q >= nq) break;
+    const float x = v ? __uint_as_float(v[e]) * mul : 0.0f;
+    out[((q_first + q) * H + h) * kD + d] = __float2bfloat16_rn(x);
+  }
+}
+
+// P^T / dS^T as bf16 A operands: activation warpgroup g packs its 32 query
+// columns over the first 16 of its own 32 fp32 columns (hi parts) and the
+// next 16 (lo parts), so neither warpgroup writes where the other still
+// reads; the kk-th 16-query slice of the hi parts sits at a_col(kk).
+__device__ __forceinline__ uint32_t a_col(int kk) { return static_cast<uint32_t>((kk >> 1) * 32 + (kk & 1) * 8); }
+
+template <int ACT, bool HILO, bool CROSS>
+__global__ void __launch_bounds__(kBwdThreads, 1)
     pma_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                    const AttnArgs a, const int* gate) {
-  using C = PbCfg<HILO>;
-  if (*gate == 0) return;  // some sequence holds more than 64 queries: the general passes run
+  using C = PbCfg<HILO, CROSS>;
+  if (*gate == 0) return;  // some sequence is outside this mode's limits: the general passes run
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {
     if (threadIdx.x == 0) record_error(a.status, JATTN_ERR_UNSUPPORTED, 93, blockIdx.x);
@@ -486,8 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &bars->abort_flag;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < C::kQDStages; ++s) {
+      mbar_init(&bars->qd_full[s], 1);
+      mbar_init(&bars->qd_empty[s], 1);
+    }
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
@@ -498,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_ready, kTile);
-    mbar_init(&bars->ds_ready, kTile);
+    mbar_init(&bars->p_ready, 2 * kTile);
+    mbar_init(&bars->ds_ready, 2 * kTile);
     mbar_init(&bars->dsm_free, 1);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, kTile);
@@ -520,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
   // each warpgroup sets its register share in the branch that holds its code
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -528,42 +585,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
-      uint32_t k_it = 0, v_it = 0, q_it = 0;
-      bool q_armed = false, ok = true;
+      uint32_t k_it = 0, v_it = 0, qd_it = 0;
+      bool ok = true;
       PItem it;
+      // the copy an item loads once (pooling: Q and dO; cross: K and V) is
+      // skipped under debug flag bit 1, so that the waits for it time out
+      const bool skip_once = (a.debug_flags & 1) != 0;
       auto load_kv = [&](const CUtensorMap* map, uint64_t* full, uint64_t* empty, int stages, int off, uint32_t& cnt,
-                         int j, int where) -> bool {
+                         int j, int where, bool skip) -> bool {
         const int s = cnt % stages;
         if (!wait_bar(&empty[s], ((cnt / stages) & 1) ^ 1, abort_flag, a, where)) return false;
-        mbar_arrive_expect_tx(&full[s], kTileBytes);
-        for (int c = 0; c < 2; ++c)
-          tma_load_2d(sm + off + s * kTileBytes + c * kBoxK, map, &full[s], it.h * kD + c * 64,
-                      static_cast<int>(it.k0) + j * kTile);
+        if (!skip) {
+          mbar_arrive_expect_tx(&full[s], kTileBytes);
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d(sm + off + s * kTileBytes + c * kBoxK, map, &full[s], it.h * kD + c * 64,
+                        static_cast<int>(it.k0) + j * kTile);
+        }
         ++cnt;
         return true;
       };
-      for (long long r = 0; ok && load_pitem(a, r, it); ++r) {
-        if (it.hi <= it.lo) continue;
-        if (!(ok = wait_bar(&bars->q_empty, (q_it & 1) ^ 1, abort_flag, a, 94))) break;
-        if (!(a.debug_flags & 1)) {
-          mbar_arrive_expect_tx(&bars->q_full, 2 * kChunkBytes);
+      auto load_qd = [&](int64_t row, bool skip) -> bool {
+        const int s = qd_it % C::kQDStages;
+        if (!wait_bar(&bars->qd_empty[s], ((qd_it / C::kQDStages) & 1) ^ 1, abort_flag, a, 94)) return false;
+        if (!skip) {
+          mbar_arrive_expect_tx(&bars->qd_full[s], 2 * kChunkBytes);
+          uint8_t* dst = sm + C::kQDOff + s * 2 * kChunkBytes;
           for (int c = 0; c < 2; ++c) {
-            tma_load_2d(sm + C::kQOff + c * kBoxQ, &tmQ, &bars->q_full, it.h * kD + c * 64, static_cast<int>(it.q0));
-            tma_load_2d(sm + C::kDOOff + c * kBoxQ, &tmDO, &bars->q_full, it.h * kD + c * 64, static_cast<int>(it.q0));
+            tma_load_2d(dst + c * kBoxQ, &tmQ, &bars->qd_full[s], it.h * kD + c * 64, static_cast<int>(row));
+            tma_load_2d(dst + kChunkBytes + c * kBoxQ, &tmDO, &bars->qd_full[s], it.h * kD + c * 64,
+                        static_cast<int>(row));
           }
-          q_armed = true;
         }
-        ++q_it;
-        for (int j = it.lo; j < it.hi && ok; ++j) {
-          if (!(ok = load_kv(&tmK, bars->k_full, bars->k_empty, C::kKStages, C::kKOff, k_it, j, 95))) break;
-          ok = load_kv(&tmV, bars->v_full, bars->v_empty, C::kVStages, C::kVOff, v_it, j, 96);
+        ++qd_it;
+        return true;
+      };
+      for (long long r = 0; ok && load_bitem<CROSS>(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if constexpr (CROSS) {
+          if (!(ok = load_kv(&tmK, bars->k_full, bars->k_empty, 1, C::kKOff, k_it, it.rt, 95, skip_once))) break;
+          if (!(ok = load_kv(&tmV, bars->v_full, bars->v_empty, 1, C::kVOff, v_it, it.rt, 96, skip_once))) break;
+          for (int c = it.lo; c < it.hi && ok; ++c) ok = load_qd(it.q0 + static_cast<int64_t>(c) * kQC, false);
+        } else {
+          if (!(ok = load_qd(it.q0, skip_once))) break;
+          for (int j = it.lo; j < it.hi && ok; ++j) {
+            if (!(ok = load_kv(&tmK, bars->k_full, bars->k_empty, C::kKStages, C::kKOff, k_it, j, 95, false))) break;
+            ok = load_kv(&tmV, bars->v_full, bars->v_empty, C::kVStages, C::kVOff, v_it, j, 96, false);
+          }
         }
       }
-      if (q_armed) drain_wait(&bars->q_full, (q_it - 1) & 1, a.timeout_ns);
-      for (uint32_t i = (k_it > (uint32_t)C::kKStages ? k_it - C::kKStages : 0); i < k_it; ++i)
-        drain_wait(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1, a.timeout_ns);
-      for (uint32_t i = (v_it > (uint32_t)C::kVStages ? v_it - C::kVStages : 0); i < v_it; ++i)
-        drain_wait(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1, a.timeout_ns);
+      // every copy this thread started lands before the CTA can exit (skipped
+      // copies started nothing)
+      if (!(skip_once && !CROSS))
+        for (uint32_t i = (qd_it > (uint32_t)C::kQDStages ? qd_it - C::kQDStages : 0); i < qd_it; ++i)
+          drain_wait(&bars->qd_full[i % C::kQDStages], (i / C::kQDStages) & 1, a.timeout_ns);
+      if (!(skip_once && CROSS)) {
+        for (uint32_t i = (k_it > (uint32_t)C::kKStages ? k_it - C::kKStages : 0); i < k_it; ++i)
+          drain_wait(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1, a.timeout_ns);
+        for (uint32_t i = (v_it > (uint32_t)C::kVStages ? v_it - C::kVStages : 0); i < v_it; ++i)
+          drain_wait(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1, a.timeout_ns);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -572,135 +652,180 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idS = idesc_bf16_f32(kTile, kQC, false, false);  // S^T = K Q^T, dP^T = V dO^T
       constexpr uint32_t idG = idesc_bf16_f32(kTile, kD, false, true);    // dV = P^T dO, dK = dS^T Q
       constexpr uint32_t idQ = idesc_bf16_f32(kD, kQC, true, true);       // dQ^T += K^T dS^T
-      const uint32_t sQ = smem_u32(sm + C::kQOff), sDO = smem_u32(sm + C::kDOOff);
+      const uint32_t sQD = smem_u32(sm + C::kQDOff);
       const uint32_t sK = smem_u32(sm + C::kKOff), sV = smem_u32(sm + C::kVOff), sDS = smem_u32(sm + C::kDSOff);
-      const uint64_t dQk = sdesc_sw128(sQ, 16, 1024), dDOk = sdesc_sw128(sDO, 16, 1024);    // K-major views
-      const uint64_t dQm = sdesc_sw128(sQ, kBoxQ, 1024), dDOm = sdesc_sw128(sDO, kBoxQ, 1024);  // MN-major views
       const uint64_t dK0 = sdesc_sw128(sK, 16, 1024), dKt0 = sdesc_sw128(sK, kBoxK, 1024);
       const uint64_t dV0 = sdesc_sw128(sV, 16, 1024), dDS0 = sdesc_sw128(sDS, kPBytes, 1024);
-      uint32_t k_used = 0, v_used = 0, q_it = 0, dq_cnt = 0, n = 0;
+      uint32_t k_used = 0, v_used = 0, qd_used = 0, acc_n = 0, dq_n = 0, n = 0;
       bool ok = true;
       PItem it;
-      for (long long r = 0; ok && load_pitem(a, r, it); ++r) {
-        if (it.hi <= it.lo) continue;
-        if (!(ok = wait_bar(&bars->q_full, q_it & 1, abort_flag, a, 97))) break;
-        ++q_it;
+      // stages of step t's tiles: key tile (ks, vs) and query chunk (qs)
+      auto k_idx = [&](int t) { return CROSS ? k_used : k_used + t; };
+      auto v_idx = [&](int t) { return CROSS ? v_used : v_used + t; };
+      auto q_idx = [&](int t) { return CROSS ? qd_used + t : qd_used; };
+      auto q_base = [&](int t) { return sQD + (q_idx(t) % C::kQDStages) * 2 * kChunkBytes; };
+      // S^T = K Q^T and dP^T = V dO^T of step t, once its tiles have landed. They
+      // overwrite the P^T / dS^T columns of the step before, which the dV / dK
+      // products issued before them have read (in order).
+      auto issue_sdp = [&](int t) -> bool {
+        const uint32_t ki = k_idx(t), vi = v_idx(t), qi = q_idx(t);
+        const int ks = ki % C::kKStages, vs = vi % C::kVStages, qs = qi % C::kQDStages;
+        if ((CROSS || t == 0) && !wait_bar(&bars->qd_full[qs], (qi / C::kQDStages) & 1, abort_flag, a, 97))
+          return false;
+        if ((!CROSS || t == 0) && !wait_bar(&bars->k_full[ks], (ki / C::kKStages) & 1, abort_flag, a, 98))
+          return false;
         tc_fence_after();
-        const int nk = it.hi - it.lo;
-        for (int t = 0; t < nk; ++t) {
-          const uint32_t ki = k_used + t, vi = v_used + t, nt = n + t;
-          const int ks = ki % C::kKStages, vs = vi % C::kVStages;
-          const uint64_t kd = dK0 + ks * (kTileBytes >> 4), ktd = dKt0 + ks * (kTileBytes >> 4);
-          if (!(ok = wait_bar(&bars->k_full[ks], (ki / C::kKStages) & 1, abort_flag, a, 98))) break;
-          tc_fence_after();
-          // S^T and dP^T overwrite the P^T / dS^T columns of the tile before,
-          // which the dV / dK products issued before them have read (in order).
+        const uint64_t dQk = sdesc_sw128(q_base(t), 16, 1024), dDOk = sdesc_sw128(q_base(t) + kChunkBytes, 16, 1024);
+        const uint64_t kd = dK0 + ks * (kTileBytes >> 4), vd = dV0 + vs * (kTileBytes >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_ss(tmem + C::kSCol, kd + kslice(kk, kBoxK), dQk + kslice(kk, kBoxQ), idS, kk > 0 ? 1u : 0u);
-          mma_commit(&bars->s_full);
-          if (!(ok = wait_bar(&bars->v_full[vs], (vi / C::kVStages) & 1, abort_flag, a, 99))) break;
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + C::kSCol, kd + kslice(kk, kBoxK), dQk + kslice(kk, kBoxQ), idS, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->s_full);
+        if (!CROSS || t == 0) {
+          if (!wait_bar(&bars->v_full[vs], (vi / C::kVStages) & 1, abort_flag, a, 99)) return false;
           tc_fence_after();
-          const uint64_t vd = dV0 + vs * (kTileBytes >> 4);
+        }
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_ss(tmem + C::kDPCol, vd + kslice(kk, kBoxK), dDOk + kslice(kk, kBoxQ), idS, kk > 0 ? 1u : 0u);
-          mma_commit(&bars->dp_full);
-          mma_commit(&bars->v_empty[vs]);
-          // dV = P^T dO once P^T is in TMEM and the epilogue has drained the tile before
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + C::kDPCol, vd + kslice(kk, kBoxK), dDOk + kslice(kk, kBoxQ), idS, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->dp_full);
+        if constexpr (!CROSS) mma_commit(&bars->v_empty[vs]);
+        return true;
+      };
+      for (long long r = 0; ok && load_bitem<CROSS>(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        const int ns = it.hi - it.lo;
+        if (!(ok = issue_sdp(0))) break;
+        for (int t = 0; t < ns; ++t) {
+          const uint32_t nt = n + t;
+          const int ks = k_idx(t) % C::kKStages, qs = q_idx(t) % C::kQDStages;
+          const uint64_t dQm = sdesc_sw128(q_base(t), kBoxQ, 1024), dDOm = sdesc_sw128(q_base(t) + kChunkBytes, kBoxQ, 1024);
+          const uint64_t ktd = dKt0 + ks * (kTileBytes >> 4);
+          // dV = P^T dO once P^T is in TMEM and the epilogue has drained the
+          // accumulators of the group before (pooling: each step; cross: each item)
+          const bool acc_first = CROSS ? t == 0 : true;
           if (!(ok = wait_bar(&bars->p_ready, nt & 1, abort_flag, a, 100))) break;
-          if (!(ok = wait_bar(&bars->acc_empty, (nt & 1) ^ 1, abort_flag, a, 101))) break;
+          if (acc_first && !(ok = wait_bar(&bars->acc_empty, (acc_n & 1) ^ 1, abort_flag, a, 101))) break;
           tc_fence_after();
 #pragma unroll
           for (int hl = 0; hl < C::kNP; ++hl)
 #pragma unroll
             for (int kk = 0; kk < kQC / 16; ++kk)
-              mma_ts(tmem + C::kDVCol, tmem + C::kSCol + 32 * hl + kk * 8, dDOm + mnslice(kk), idG,
-                     (hl > 0 || kk > 0) ? 1u : 0u);
+              mma_ts(tmem + C::kDVCol, tmem + C::kSCol + 16 * hl + a_col(kk), dDOm + mnslice(kk), idG,
+                     (!acc_first || hl > 0 || kk > 0) ? 1u : 0u);
           if (!(ok = wait_bar(&bars->ds_ready, nt & 1, abort_flag, a, 102))) break;
           tc_fence_after();
 #pragma unroll
           for (int hl = 0; hl < C::kNP; ++hl)
 #pragma unroll
             for (int kk = 0; kk < kQC / 16; ++kk)
-              mma_ts(tmem + C::kDKCol, tmem + C::kDPCol + 32 * hl + kk * 8, dQm + mnslice(kk), idG,
-                     (hl > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars->acc_full);
-          if (t == 0 && !(ok = wait_bar(&bars->dq_empty, (dq_cnt & 1) ^ 1, abort_flag, a, 103))) break;
+              mma_ts(tmem + C::kDKCol, tmem + C::kDPCol + 16 * hl + a_col(kk), dQm + mnslice(kk), idG,
+                     (!acc_first || hl > 0 || kk > 0) ? 1u : 0u);
+          if constexpr (!CROSS) {
+            mma_commit(&bars->acc_full);
+            ++acc_n;
+          }
+          // the next step's S^T and dP^T go ahead of this step's dQ^T, so the
+          // activation of the next step overlaps it
+          if (t + 1 < ns && !(ok = issue_sdp(t + 1))) break;
+          // dQ^T += K^T dS^T (pooling: over the item's steps; cross: one step)
+          const bool dq_first = CROSS ? true : t == 0;
+          if (dq_first && !(ok = wait_bar(&bars->dq_empty, (dq_n & 1) ^ 1, abort_flag, a, 103))) break;
 #pragma unroll
           for (int hl = 0; hl < C::kNP; ++hl)
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
               mma_ss(tmem + C::kDQCol, ktd + mnslice(kk), dDS0 + hl * (kPBytes >> 4) + mnslice(kk), idQ,
-                     (t > 0 || hl > 0 || kk > 0) ? 1u : 0u);
+                     (!dq_first || hl > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars->dsm_free);
-          mma_commit(&bars->k_empty[ks]);
+          if constexpr (CROSS) {
+            mma_commit(&bars->qd_empty[qs]);
+            mma_commit(&bars->dq_full);
+            ++dq_n;
+          } else {
+            mma_commit(&bars->k_empty[ks]);
+          }
         }
         if (!ok) break;
-        mma_commit(&bars->q_empty);
-        mma_commit(&bars->dq_full);
-        ++dq_cnt;
-        n += nk;
-        k_used += nk;
-        v_used += nk;
+        if constexpr (CROSS) {
+          mma_commit(&bars->acc_full);
+          ++acc_n;
+          mma_commit(&bars->k_empty[0]);
+          mma_commit(&bars->v_empty[0]);
+          ++k_used;
+          ++v_used;
+          qd_used += ns;
+        } else {
+          mma_commit(&bars->qd_empty[qd_used % C::kQDStages]);
+          mma_commit(&bars->dq_full);
+          ++dq_n;
+          ++qd_used;
+          k_used += ns;
+          v_used += ns;
+        }
+        n += ns;
       }
       mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0, a.timeout_ns);
     }
     __syncwarp();
   }
-  } else if (warp < 8) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kActRegs));
-    // ------------------------------------------------------------ activation warpgroup
+  } else if (warp < 12) {
+    // ------------------------------------------------------------ activation warpgroups
+    // warpgroup g takes query columns [32 g, 32 g + 32) of every step (the
+    // launch's register count is its share)
+    const int g = (warp - 4) >> 2;
     const int row = 32 * (warp & 3) + lane;  // key row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t tS = tmem + lane_base + C::kSCol + 32 * g, tDP = tmem + lane_base + C::kDPCol + 32 * g;
     const uint32_t sDS = smem_u32(sm + C::kDSOff);
     uint32_t n = 0;
     bool ok = true;
     PItem it;
-    for (long long r = 0; ok && load_pitem(a, r, it); ++r) {
+    for (long long r = 0; ok && load_bitem<CROSS>(a, r, it); ++r) {
       if (it.hi <= it.lo) continue;
-      const int nk = it.hi - it.lo;
-      for (int t = 0; t < nk; ++t) {
+      const int ns = it.hi - it.lo;
+      for (int t = 0; t < ns; ++t) {
         const uint32_t nt = n + t;
-        const bool valid = (it.lo + t) * kTile + row < it.lkv;
+        // key rows past the sequence and query columns past the chunk are
+        // zero in P^T and dS^T: dV and dK sum over the query columns, dQ^T
+        // over the key rows
+        const int j = CROSS ? it.rt : it.lo + t;
+        const bool valid = j * kTile + row < it.lkv;
+        const int nq = (CROSS ? min(kQC, it.lq - (it.lo + t) * kQC) : it.lq) - 32 * g;  // this group's columns
+        const bool any = nq > 0;
         ok = __all_sync(0xffffffffu, wait_bar(&bars->s_full, nt & 1, abort_flag, a, 104));
         if (!ok) break;
         tc_fence_after();
-        uint32_t s[kQC];
-        float gr[kQC];  // act'(x) of the item's query columns
-#pragma unroll
-        for (int c = 0; c < kQC / 32; ++c)
-          if (32 * c < it.lq) tmem_ld32(tmem + lane_base + C::kSCol + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c));
-        tmem_ld_wait();
-        // P^T (bf16) over S^T's first 32 columns (hi) and the next 32 (lo).
-        // Query columns past the item and key rows past the sequence are zero:
-        // dV and dK sum over the query columns.
-#pragma unroll
-        for (int c = 0; c < kQC / 32; ++c) {
-          uint32_t hi[16], lo[16];
-          if (32 * c < it.lq) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int q = 32 * c + 2 * e;
-              float f0, f1, g0, g1;
-              act_and_grad<ACT>(__uint_as_float(s[q]) * a.scale, f0, g0);
-              act_and_grad<ACT>(__uint_as_float(s[q + 1]) * a.scale, f1, g1);
-              const bool a0 = valid && q < it.lq, a1 = valid && q + 1 < it.lq;
-              f0 = a0 ? f0 : 0.0f;
-              f1 = a1 ? f1 : 0.0f;
-              gr[q] = a0 ? g0 : 0.0f;
-              gr[q + 1] = a1 ? g1 : 0.0f;
-              hi[e] = pack_bf16x2(f0, f1);
-              if constexpr (HILO) lo[e] = bf16x2_lo(f0, f1, hi[e]);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
-          }
-          tmem_st16(tmem + lane_base + C::kSCol + 16 * c, hi);
-          if constexpr (HILO) tmem_st16(tmem + lane_base + C::kSCol + 32 + 16 * c, lo);
+        uint32_t s[32];
+        float gr[32];  // act'(x) of the group's query columns
+        if (any) {
+          tmem_ld32(tS, s);
+          tmem_ld_wait();
         }
+        // P^T as bf16: hi parts over the group's first 16 columns, lo parts the next 16
+        uint32_t hi[16], lo[16];
+        if (any) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int q = 2 * e;
+            float f0, f1, g0, g1;
+            act_and_grad<ACT>(__uint_as_float(s[q]) * a.scale, f0, g0);
+            act_and_grad<ACT>(__uint_as_float(s[q + 1]) * a.scale, f1, g1);
+            const bool a0 = valid && q < nq, a1 = valid && q + 1 < nq;
+            f0 = a0 ? f0 : 0.0f;
+            f1 = a1 ? f1 : 0.0f;
+            gr[q] = a0 ? g0 : 0.0f;
+            gr[q + 1] = a1 ? g1 : 0.0f;
+            hi[e] = pack_bf16x2(f0, f1);
+            if constexpr (HILO) lo[e] = bf16x2_lo(f0, f1, hi[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
+        }
+        tmem_st16(tS, hi);
+        if constexpr (HILO) tmem_st16(tS + 16, lo);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->p_ready);
@@ -708,106 +833,123 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, wait_bar(&bars->dp_full, nt & 1, abort_flag, a, 105));
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < kQC / 32; ++c)
-          if (32 * c < it.lq) tmem_ld32(tmem + lane_base + C::kDPCol + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c));
-        tmem_ld_wait();
-        // the dQ^T products of the tile before have read the shared dS^T tile
+        if (any) {
+          tmem_ld32(tDP, s);
+          tmem_ld_wait();
+        }
+        // the dQ^T products of the step before have read the shared dS^T tile
         ok = __all_sync(0xffffffffu, wait_bar(&bars->dsm_free, (nt & 1) ^ 1, abort_flag, a, 106));
         if (!ok) break;
+        if (any) {
 #pragma unroll
-        for (int c = 0; c < kQC / 32; ++c) {
-          uint32_t hi[16], lo[16];
-          if (32 * c < it.lq) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int q = 32 * c + 2 * e;
-              const float d0 = gr[q] * __uint_as_float(s[q]), d1 = gr[q + 1] * __uint_as_float(s[q + 1]);
-              hi[e] = pack_bf16x2(d0, d1);
-              if constexpr (HILO) lo[e] = bf16x2_lo(d0, d1, hi[e]);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
+          for (int e = 0; e < 16; ++e) {
+            const int q = 2 * e;
+            const float d0 = gr[q] * __uint_as_float(s[q]), d1 = gr[q + 1] * __uint_as_float(s[q + 1]);
+            hi[e] = pack_bf16x2(d0, d1);
+            if constexpr (HILO) lo[e] = bf16x2_lo(d0, d1, hi[e]);
           }
-          tmem_st16(tmem + lane_base + C::kDPCol + 16 * c, hi);
-          if constexpr (HILO) tmem_st16(tmem + lane_base + C::kDPCol + 32 + 16 * c, lo);
-          st_pt_row(sDS, row, 32 * c, hi);
-          if constexpr (HILO) st_pt_row(sDS + kPBytes, row, 32 * c, lo);
         }
+        tmem_st16(tDP, hi);
+        if constexpr (HILO) tmem_st16(tDP + 16, lo);
+        st_pt_row(sDS, row, 32 * g, hi);
+        if constexpr (HILO) st_pt_row(sDS + kPBytes, row, 32 * g, lo);
         fence_proxy_async_smem();
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->ds_ready);
       }
       if (!ok) break;
-      n += nk;
+      n += ns;
     }
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
     // ------------------------------------------------------------ epilogue warpgroup
-    // dV and dK rows of every key tile; dQ of every item from dQ^T (thread =
-    // head-dim row). Items without keys get zero dQ rows.
+    // dV and dK rows (thread = key row) after each accumulation group, dQ
+    // rows (thread = head-dim row) from dQ^T after each of its groups. Items
+    // without keys (pooling) get zero dQ rows; items without queries (cross)
+    // zero dK and dV rows.
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    uint32_t n = 0, dq_cnt = 0;
+    uint32_t acc_n = 0, dq_n = 0;
     PItem it;
     bool ok = true;
-    for (long long r = 0; ok && load_pitem(a, r, it); ++r) {
+    auto drain_kv = [&](int j, float cn) -> bool {
+      if (!__all_sync(0xffffffffu, wait_bar(&bars->acc_full, acc_n & 1, abort_flag, a, 107))) return false;
+      ++acc_n;
+      tc_fence_after();
+      const int jl = j * kTile + row;
+      const bool valid = jl < it.lkv;
+      const int64_t gk = it.k0 + jl;
+      __nv_bfloat16* dv_row = a.out1 + (gk * a.H + it.h) * kD;
+      __nv_bfloat16* dk_row = a.out2 + (gk * a.H + it.h) * kD;
+#pragma unroll 1
+      for (int c = 0; c < 2 * kD / 32; ++c) {
+        const bool is_dk = c >= kD / 32;
+        const int cc = is_dk ? c - kD / 32 : c;
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + (is_dk ? C::kDKCol : C::kDVCol) + 32 * cc, v);
+        tmem_ld_wait();
+        if (c == 2 * kD / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(&bars->acc_empty);
+        }
+        if (valid) {
+          uint32_t w[16];
+          const float mul = is_dk ? cn * a.scale : cn;
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+          store_words16((is_dk ? dk_row : dv_row) + 32 * cc, w, a.out_v8);
+        }
+      }
+      return true;
+    };
+    auto drain_q = [&](int64_t q_first, int nq, float mul) -> bool {
+      if (!__all_sync(0xffffffffu, wait_bar(&bars->dq_full, dq_n & 1, abort_flag, a, 108))) return false;
+      ++dq_n;
+      tc_fence_after();
+      const int halves = nq > 32 ? 2 : 1;
+#pragma unroll 1
+      for (int c = 0; c < halves; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + C::kDQCol + 32 * c, v);
+        tmem_ld_wait();
+        if (c == halves - 1) {  // dQ^T is free for the next group once read
+          tc_fence_before();
+          mbar_arrive(&bars->dq_empty);
+        }
+        store_chunk_cols(a.out0, q_first, nq, a.H, it.h, row, 32 * c, v, mul);
+      }
+      return true;
+    };
+    for (long long r = 0; ok && load_bitem<CROSS>(a, r, it); ++r) {
       if (it.hi <= it.lo) {
-        store_cols(a.out0, it, a.H, row, 0, nullptr, 0.0f);
-        store_cols(a.out0, it, a.H, row, 32, nullptr, 0.0f);
+        if constexpr (CROSS) {
+          const int jl = it.rt * kTile + row;
+          if (jl < it.lkv) {
+            const int64_t gk = it.k0 + jl;
+            uint4* dv = reinterpret_cast<uint4*>(a.out1 + (gk * a.H + it.h) * kD);
+            uint4* dk = reinterpret_cast<uint4*>(a.out2 + (gk * a.H + it.h) * kD);
+            for (int e = 0; e < kD / 8; ++e) dv[e] = dk[e] = make_uint4(0, 0, 0, 0);
+          }
+        } else {
+          store_chunk_cols(a.out0, it.q0, it.lq, a.H, it.h, row, 0, nullptr, 0.0f);
+          store_chunk_cols(a.out0, it.q0, it.lq, a.H, it.h, row, 32, nullptr, 0.0f);
+        }
         continue;
       }
-      const int nk = it.hi - it.lo;
+      const int ns = it.hi - it.lo;
       const float cn = (a.norm_by_lkv && it.lkv > 0) ? 1.0f / it.lkv : 1.0f;
-      for (int t = 0; t < nk; ++t) {
-        const uint32_t nt = n + t;
-        ok = __all_sync(0xffffffffu, wait_bar(&bars->acc_full, nt & 1, abort_flag, a, 107));
-        if (!ok) break;
-        tc_fence_after();
-        const int jl = (it.lo + t) * kTile + row;
-        const bool valid = jl < it.lkv;
-        const int64_t gk = it.k0 + jl;
-        __nv_bfloat16* dv_row = a.out1 + (gk * a.H + it.h) * kD;
-        __nv_bfloat16* dk_row = a.out2 + (gk * a.H + it.h) * kD;
-#pragma unroll 1
-        for (int c = 0; c < 2 * kD / 32; ++c) {
-          const bool is_dk = c >= kD / 32;
-          const int cc = is_dk ? c - kD / 32 : c;
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + (is_dk ? C::kDKCol : C::kDVCol) + 32 * cc, v);
-          tmem_ld_wait();
-          if (c == 2 * kD / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive(&bars->acc_empty);
-          }
-          if (valid) {
-            uint32_t w[16];
-            const float mul = is_dk ? cn * a.scale : cn;
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-            store_words16((is_dk ? dk_row : dv_row) + 32 * cc, w, a.out_v8);
-          }
+      for (int t = 0; t < ns && ok; ++t) {
+        if constexpr (CROSS) {
+          const int c = it.lo + t;
+          ok = drain_q(it.q0 + static_cast<int64_t>(c) * kQC, min(kQC, it.lq - c * kQC), cn * a.scale);
+        } else {
+          ok = drain_kv(it.lo + t, cn);
         }
       }
       if (!ok) break;
-      n += nk;
-      ok = __all_sync(0xffffffffu, wait_bar(&bars->dq_full, dq_cnt & 1, abort_flag, a, 108));
-      if (!ok) break;
-      ++dq_cnt;
-      tc_fence_after();
-      uint32_t v[kQC];
-#pragma unroll
-      for (int c = 0; c < kQC / 32; ++c)
-        if (32 * c < it.lq) tmem_ld32(tmem + lane_base + C::kDQCol + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->dq_empty);
-#pragma unroll
-      for (int c = 0; c < kQC / 32; ++c)
-        if (32 * c < it.lq) store_cols(a.out0, it, a.H, row, 32 * c, v + 32 * c, cn * a.scale);
+      ok = CROSS ? drain_kv(it.rt, cn) : drain_q(it.q0, it.lq, cn * a.scale);
     }
   }
 
@@ -816,17 +958,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// Whether every sequence suits the fused backward (1 <= Lq <= 64, or no keys
-// at all). If so, the general dQ and dK/dV schedules are emptied so their
-// passes find no work; else the gate stays closed and the fused pass returns.
+// Whether every sequence suits the fused backward's mode. Pooling: 1 <= Lq
+// <= 64, or no keys. Cross: Lkv <= 128, and keys whenever there are queries.
+// If so, the general dQ and dK/dV schedules are emptied so their passes find
+// no work; else the gate stays closed and the fused pass returns.
 __global__ void __launch_bounds__(1024) pma_gate_kernel(const int64_t* q_off, const int64_t* kv_off, int64_t B,
-                                                        int* gate, int* n_tiles_q, int* n_tiles_kv) {
+                                                        int cross, int* gate, int* n_tiles_q, int* n_tiles_kv) {
   __shared__ int bad;
   if (threadIdx.x == 0) bad = 0;
   __syncthreads();
   for (int64_t b = threadIdx.x; b < B; b += blockDim.x) {
     const int64_t lq = q_off[b + 1] - q_off[b], lkv = kv_off[b + 1] - kv_off[b];
-    if (lq > kQC || lq < 0 || lkv < 0 || (lq == 0 && lkv > 0)) bad = 1;
+    bool ok = lq >= 0 && lkv >= 0;
+    if (cross) ok = ok && lkv <= kTile && (lkv > 0 || lq == 0);
+    else ok = ok && lq <= kQC && (lq > 0 || lkv == 0);
+    if (!ok) bad = 1;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -854,22 +1000,25 @@ cudaError_t fwd_act(bool hilo, const CUtensorMap& q, const CUtensorMap& k, const
   return launch_k(pma_fwd_kernel<ACT, false>, PfCfg<false>::kSmemBytes, grid, st, q, k, v, a);
 }
 
-template <int ACT, bool HILO>
+template <int ACT, bool HILO, bool CROSS>
 cudaError_t bwd_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
                     const AttnArgs& a, const int* gate, int grid, cudaStream_t st) {
-  auto kernel = pma_bwd_kernel<ACT, HILO>;
-  constexpr int smem = PbCfg<HILO>::kSmemBytes;
+  auto kernel = pma_bwd_kernel<ACT, HILO, CROSS>;
+  constexpr int smem = PbCfg<HILO, CROSS>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreads, smem, st>>>(q, k, v, dout, a, gate);
+  kernel<<<grid, kBwdThreads, smem, st>>>(q, k, v, dout, a, gate);
   return cudaGetLastError();
 }
 
 template <int ACT>
-cudaError_t bwd_act(bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t bwd_act(bool hilo, bool cross, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                     const CUtensorMap& dout, const AttnArgs& a, const int* gate, int grid, cudaStream_t st) {
-  return hilo ? bwd_one<ACT, true>(q, k, v, dout, a, gate, grid, st)
-              : bwd_one<ACT, false>(q, k, v, dout, a, gate, grid, st);
+  if (cross)
+    return hilo ? bwd_one<ACT, true, true>(q, k, v, dout, a, gate, grid, st)
+                : bwd_one<ACT, false, true>(q, k, v, dout, a, gate, grid, st);
+  return hilo ? bwd_one<ACT, true, false>(q, k, v, dout, a, gate, grid, st)
+              : bwd_one<ACT, false, false>(q, k, v, dout, a, gate, grid, st);
 }
 
 }  // namespace
@@ -884,19 +1033,19 @@ cudaError_t launch_pma_fwd(int act, bool hilo, const CUtensorMap& q, const CUten
   }
 }
 
-cudaError_t launch_pma_gate(const int64_t* q_off, const int64_t* kv_off, int64_t B, int* gate, int* n_tiles_q,
-                            int* n_tiles_kv, cudaStream_t stream) {
-  pma_gate_kernel<<<1, 1024, 0, stream>>>(q_off, kv_off, B, gate, n_tiles_q, n_tiles_kv);
+cudaError_t launch_pma_gate(const int64_t* q_off, const int64_t* kv_off, int64_t B, bool cross, int* gate,
+                            int* n_tiles_q, int* n_tiles_kv, cudaStream_t stream) {
+  pma_gate_kernel<<<1, 1024, 0, stream>>>(q_off, kv_off, B, cross ? 1 : 0, gate, n_tiles_q, n_tiles_kv);
   return cudaGetLastError();
 }
 
-cudaError_t launch_pma_bwd(int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                           const CUtensorMap& dout, const AttnArgs& a, const int* gate, int grid,
-                           cudaStream_t stream) {
+cudaError_t launch_pma_bwd(int act, bool hilo, bool cross, const CUtensorMap& q, const CUtensorMap& k,
+                           const CUtensorMap& v, const CUtensorMap& dout, const AttnArgs& a, const int* gate,
+                           int grid, cudaStream_t stream) {
   switch (act) {
-    case JATTN_SILU: return bwd_act<JATTN_SILU>(hilo, q, k, v, dout, a, gate, grid, stream);
-    case JATTN_GELU_TANH: return bwd_act<JATTN_GELU_TANH>(hilo, q, k, v, dout, a, gate, grid, stream);
-    case JATTN_GELU_POLY: return bwd_act<JATTN_GELU_POLY>(hilo, q, k, v, dout, a, gate, grid, stream);
+    case JATTN_SILU: return bwd_act<JATTN_SILU>(hilo, cross, q, k, v, dout, a, gate, grid, stream);
+    case JATTN_GELU_TANH: return bwd_act<JATTN_GELU_TANH>(hilo, cross, q, k, v, dout, a, gate, grid, stream);
+    case JATTN_GELU_POLY: return bwd_act<JATTN_GELU_POLY>(hilo, cross, q, k, v, dout, a, gate, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

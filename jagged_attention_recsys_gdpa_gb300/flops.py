@@ -53,8 +53,23 @@ def short_query_path(act: int, mask: int, D: int, lq, lkv) -> bool:
     return bool(np.all(((lq >= 1) & (lq <= 64)) | (lkv == 0)))
 
 
+def short_key_path(act: int, mask: int, D: int, lq, lkv) -> bool:
+    """Whether the library's backward runs a batch as cross-attention over
+    short key sequences on the fused kernel: a pointwise activation, no mask,
+    D = 128, more than 64 queries but at most 128 keys per sequence on average
+    (the host's rule) and every sequence with Lkv <= 128 and keys whenever it
+    has queries (the device-side gate). The forward stays on the general kernel."""
+    lq = np.asarray(lq, dtype=np.int64)
+    lkv = np.asarray(lkv, dtype=np.int64)
+    if act == 0 or mask != 0 or D != 128 or len(lq) == 0:
+        return False
+    if int(lq.sum()) <= 64 * len(lq) or int(lkv.sum()) > 128 * len(lq):
+        return False
+    return bool(np.all((lkv <= 128) & ((lkv >= 1) | (lq == 0))))
+
+
 def kernel_work(total_q: int, total_kv: int, pairs: int, H: int, D: int, softmax: bool, in_tile: bool = False,
-                short_q: bool = False):
+                fused_bwd: bool = False):
     """Algorithmic FLOPs and HBM bytes of each kernel (each byte read or written once).
 
     forward: reads Q, K, V, writes O (+ LSE)
@@ -65,16 +80,16 @@ def kernel_work(total_q: int, total_kv: int, pairs: int, H: int, D: int, softmax
              tile) it reads neither O nor LSE and writes LSE and Di instead.
     dkdv:    reads Q, K, V, dO (+ LSE, Di), writes dK, dV; products S, dP, dV, dK
 
-    short_q (the short-query kernels): the fused backward, timed in the dK/dV
-    slot, reads Q, dO, K, V once and writes dQ, dK, dV, computing all five
-    products; the general dQ pass then finds no work.
+    fused_bwd (short_query_path or short_key_path): the fused backward, timed
+    in the dK/dV slot, reads Q, dO, K, V once and writes dQ, dK, dV, computing
+    all five products; the general dQ pass then finds no work.
     """
     e = 2 * H * D  # bytes of one row of a [total, H, D] bf16 tensor
     stats = 4 * H * total_q
     dq_extra = 0
     if softmax:
         dq_extra = 2 * stats if in_tile else e * total_q + 2 * stats
-    if short_q:
+    if fused_bwd:
         return {
             "fwd": {"flops": 4.0 * D * H * pairs, "bytes": e * (2 * total_q + 2 * total_kv)},
             "dkdv": {"flops": 10.0 * D * H * pairs, "bytes": e * (3 * total_q + 4 * total_kv)},

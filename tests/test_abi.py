@@ -224,6 +224,8 @@ def test_short_query_shapes_hold_their_schedule(lib):
     assert base > B.workspace_size(_params(**{**pma, "mask": 1}))                  # causal: general kernels only
     assert base > B.workspace_size(_params(**{**pma, "total_q": 64 * 512 + 1}))    # longer queries on average
     assert B.workspace_size(_params(**{**pma, "D": 64})) < base
+    cross = dict(B=512, total_q=800_000, total_kv=37_000, H=8, D=128, act=1, mask=0, norm_by_lkv=1)
+    assert B.workspace_size(_params(**cross)) > B.workspace_size(_params(**{**cross, "total_kv": 128 * 512 + 1}))
 
 
 def test_short_query_path_rule():
@@ -239,3 +241,9 @@ def test_short_query_path_rule():
     assert not flops.short_query_path(1, 0, 128, [65, 1], [10, 10])  # a sequence beyond 64 queries (gate)
     assert not flops.short_query_path(1, 0, 128, [0, 32], [10, 10])  # keys no query sees (gate)
     assert not flops.short_query_path(1, 0, 128, [100, 100], [1, 1])  # average beyond 64
+    # cross-attention over short key sequences: the fused backward's cross mode
+    assert flops.short_key_path(1, 0, 128, [1000, 300, 0], [16, 128, 40])
+    assert not flops.short_key_path(1, 0, 128, [32, 32], [100, 100])   # pooling shape (short queries)
+    assert not flops.short_key_path(1, 0, 128, [1000, 300], [129, 5])  # a sequence beyond 128 keys (gate)
+    assert not flops.short_key_path(1, 0, 128, [1000, 300], [0, 5])    # queries without keys (gate)
+    assert not flops.short_key_path(0, 0, 128, [1000], [16])           # softmax

@@ -1,8 +1,10 @@
-"""The short-query (pooling) kernels: keys on the MMA's M dimension for
-pointwise attention without a mask at D = 128 when sequences average at most
-64 queries. CUDA path vs the oracle element by element, a gate that hands
-batches with longer (or empty) query sequences back to the general backward,
-the rows the stores touch, and the bounded waits."""
+"""The kernels that put the keys on the MMA's M dimension, for pointwise
+attention without a mask at D = 128: the short-query (pooling) forward and
+fused backward when sequences average at most 64 queries, and the fused
+backward's cross mode when they average more queries but at most 128 keys.
+CUDA path vs the oracle element by element, the gates that hand batches
+outside a mode's limits back to the general backward, the rows the stores
+touch, and the bounded waits."""
 import numpy as np
 import pytest
 import torch
@@ -33,7 +35,8 @@ def _w(act, norm=True, H=3, qk=0.0):
 def _check(w, lq, lkv, seed, flags=0):
     from jagged_attention_recsys_gdpa_gb300 import _binding as B
 
-    assert sum(lq) <= 64 * len(lq)  # the shape the short-query kernels take
+    n = len(lq)  # a shape these kernels take: short queries, or else short keys, on average
+    assert sum(lq) <= 64 * n or sum(lkv) <= 128 * n
     cpu = G.cpu_inputs(w, lq, lkv, seed)
     B.debug_set(flags, 0)
     try:
@@ -121,6 +124,99 @@ def test_short_query_waits_time_out_then_recover():
         assert J.device_status() == JATTN_ERR_TIMEOUT
     finally:
         B.debug_set(0, 0)
+    o, _ = J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], **kw)
+    assert J.device_status() == 0
+    try:
+        B.debug_set(1, 50_000_000)
+        J.backward(x["q"], x["k"], x["v"], o, None, x["do"], x["q_off"], x["kv_off"], **kw)
+        assert J.device_status() == JATTN_ERR_TIMEOUT
+    finally:
+        B.debug_set(0, 0)
+    g = G.gpu_run(x, w)
+    assert J.device_status() == 0
+    G.compare(g, G.oracle_run(cpu, w), w)
+
+
+# ---------------------------------------------------------------- cross-attention over short key sequences
+# every sequence Lkv <= 128 (and keys whenever it has queries): the fused
+# backward's cross mode; more than 64 queries per sequence on average
+CROSS_LQ = [1000, 1, 64, 65, 300, 0, 129, 700, 5]
+CROSS_LKV = [16, 128, 1, 127, 100, 40, 64, 128, 3]
+FWD_ON_SHORT_Q = 64  # debug flag bit: the short-key shapes' forward on the short-query kernel
+
+
+@pytest.mark.parametrize("norm", [True, False])
+@pytest.mark.parametrize("act", [SILU, GELU])
+def test_short_key_matches_oracle(act, norm):
+    """Chunks of 1 to 64 queries (ragged last chunk), 1 to 128 keys, a
+    sequence with keys but no queries (zero dK and dV)."""
+    _check(_w(act, norm), CROSS_LQ, CROSS_LKV, seed=91 + act + 2 * norm)
+
+
+def test_short_key_gelu_poly():
+    _check(_w(POLY, qk=1.0), CROSS_LQ, CROSS_LKV, seed=95)
+
+
+@pytest.mark.parametrize("act", [SILU, GELU])
+def test_short_key_long_queries(act):
+    """Cross-attention lengths: thousands of queries per 16-128 keys (dK and dV
+    accumulate over up to 128 chunks in TMEM)."""
+    _check(_w(act, H=2), [8000, 3000, 129, 5], [128, 16, 100, 1], seed=96)
+
+
+@pytest.mark.parametrize("act", [SILU, GELU])
+def test_short_key_gate_closed(act):
+    """One sequence with 200 keys and one with queries but no keys: the gate
+    leaves the backward to the general kernels (dQ = 0 for the rows that see
+    nothing)."""
+    _check(_w(act), [300, 500, 20, 7], [100, 200, 0, 50], seed=97)
+
+
+@pytest.mark.parametrize("norm", [True, False])
+def test_short_key_forward_on_short_query_kernel(norm):
+    """The short-query forward (items of 64 queries) on cross shapes, behind a
+    debug flag; the fused backward as usual."""
+    _check(_w(GELU, norm), CROSS_LQ, CROSS_LKV, seed=98, flags=FWD_ON_SHORT_Q)
+
+
+def test_short_key_agrees_with_general_kernels():
+    w = _w(SILU)
+    a = _check(w, CROSS_LQ, CROSS_LKV, seed=99)
+    b = _check(w, CROSS_LQ, CROSS_LKV, seed=99, flags=NO_SHORT_Q)
+    for k in ("o", "dq", "dk", "dv"):
+        G.assert_close(G.to64(a[k]), G.to64(b[k]), k)
+
+
+def test_short_key_outputs_only_touch_their_rows():
+    import jagged_attention_recsys_gdpa_gb300 as J
+
+    w = _w(SILU)
+    cpu = G.cpu_inputs(w, CROSS_LQ, CROSS_LKV, 100)
+    x = G.to_cuda(cpu)
+    TQ, TK, pad = x["q"].shape[0], x["k"].shape[0], 5
+    big = lambda T: torch.full((T + 2 * pad, w.H, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    bq, bk, bv = big(TQ), big(TK), big(TK)
+    dq, dk, dv = bq[pad : pad + TQ], bk[pad : pad + TK], bv[pad : pad + TK]
+    kw = dict(act=SILU, norm_by_lkv=True)
+    o, _ = J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], **kw)
+    J.backward(x["q"], x["k"], x["v"], o, None, x["do"], x["q_off"], x["kv_off"], dq=dq, dk=dk, dv=dv, **kw)
+    torch.cuda.synchronize()
+    for b, T in ((bq, TQ), (bk, TK), (bv, TK)):
+        assert torch.all(b[:pad] == 7.0) and torch.all(b[pad + T :] == 7.0)
+    G.compare({"o": o, "lse": None, "dq": dq, "dk": dk, "dv": dv}, G.oracle_run(cpu, w), w)
+
+
+def test_short_key_backward_times_out_then_recovers():
+    """With the key copies skipped, the cross-mode backward gives up its bounded
+    waits, reports TIMEOUT and returns; a clean call afterwards is correct."""
+    import jagged_attention_recsys_gdpa_gb300 as J
+    from jagged_attention_recsys_gdpa_gb300 import _binding as B
+
+    w = _w(SILU)
+    cpu = G.cpu_inputs(w, CROSS_LQ, CROSS_LKV, 101)
+    x = G.to_cuda(cpu)
+    kw = dict(act=SILU, norm_by_lkv=True)
+    J.device_status()
     o, _ = J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], **kw)
     assert J.device_status() == 0
     try:
