@@ -1,36 +1,39 @@
-// Short-query attention (pooling: a few queries per sequence against long key
-// sequences) with the keys on the MMA's M dimension, on sm_103a.
+// Attention with the keys on the MMA's M dimension, for sequences that are
+// short on one side, on sm_103a.
 //
 // "GEM Training" post, section "Generalized Dot-Product Attention (GDPA)":
 // pooling attention (PMA) runs a few learned queries per sequence against the
-// sequence's keys with a pointwise activation. A 128-row query tile holding 32
-// queries leaves three quarters of every MMA's M rows empty. Here the products
-// are transposed so that 128 keys fill M and an item's queries (at most 64)
-// are the N dimension:
+// sequence's keys with a pointwise activation, and cross-attention often sees
+// short K/V. A 128-row query tile holding 32 queries leaves three quarters of
+// every MMA's M rows empty. Here the products are transposed so that 128 keys
+// fill M and at most 64 queries are the N dimension:
 //   forward   S^T = K Q^T; P^T = act(scale S^T) goes to shared memory as
 //             bf16; O^T += V^T P^T (M = head dim) accumulates in TMEM over the
-//             key tiles, and O is written from O^T at the item's end.
-//   backward  one item = (sequence, head) with all of the sequence's queries.
-//             Per key tile: S^T = K Q^T and dP^T = V dO^T; P^T and
-//             dS^T = act'(scale S^T) * dP^T; dV = P^T dO and dK = dS^T Q, each
-//             complete for the tile since every query is in the item; and
-//             dQ^T += K^T dS^T, accumulated in TMEM over the key tiles. K and
-//             V are read once and dK / dV written once: there is no second
-//             pass that reads K and V again for dQ.
-// Items come from the 64-row query-tile schedule, longest first. The forward
-// takes any query length (a longer sequence gives several items, each of
-// which reads its key tiles again). The backward needs every sequence to hold
-// at most 64 queries, and at least one when it has keys; a gate kernel checks
-// that on the device and either clears the general dQ and dK/dV schedules
-// (their passes then find no work) or leaves them to run while this pass
-// finds the gate closed and returns.
+//             key tiles, and O is written from O^T at the item's end. Items
+//             are 64-query pieces from the 64-row query-tile schedule.
+//   backward  one item = (sequence, head); each step computes S^T = K Q^T and
+//             dP^T = V dO^T, P^T and dS^T = act'(scale S^T) * dP^T, then
+//             dV += P^T dO, dK += dS^T Q and dQ^T += K^T dS^T, with all five
+//             products once (none recomputed). Two modes:
+//     pooling   (every sequence 1 <= Lq <= 64, or no keys): the queries are
+//               loaded once, the key tiles are the steps; dV and dK of a tile
+//               are complete after its step, dQ^T accumulates over the item.
+//               K and V are read once and dK / dV written once: there is no
+//               second pass that reads K and V again for dQ.
+//     cross     (every sequence Lkv <= 128, and keys when it has queries): the
+//               K / V tile is loaded once, the 64-query chunks are the steps;
+//               dQ of a chunk is complete after its step, dV and dK
+//               accumulate over the item. Q and dO are read once.
+// A gate kernel checks the chosen mode's limits on the device and either
+// clears the general dQ and dK/dV schedules (their passes then find no work)
+// or leaves them to run while this pass finds the gate closed and returns.
 //
-// Roles: warp 0 issues TMA copies, warp 1 issues tcgen05 MMAs; the forward's
-// two activation warpgroups (warps 4-7, 8-11) take alternate key tiles, the
-// backward has one activation warpgroup (warps 4-7) and an epilogue
-// warpgroup (warps 8-11) that drains dV / dK per key tile and dQ per item.
-// Thread i of a warpgroup owns TMEM lane i: a key row of S^T / dP^T / dV /
-// dK, or a head-dim row of O^T / dQ^T.
+// Roles: warp 0 issues TMA copies, warp 1 issues tcgen05 MMAs. The forward's
+// two activation warpgroups (warps 4-7, 8-11) take alternate key tiles; the
+// backward's (same warps) split every step's 64 query columns, and an
+// epilogue warpgroup (warps 12-15) drains dV / dK and dQ. Thread i of a
+// warpgroup owns TMEM lane i: a key row of S^T / dP^T / dV / dK, or a
+// head-dim row of O^T / dQ^T.
 //
 // Pointwise activations without the 1/Lkv normaliser pass P and dS to the
 // second products as bf16 hi + lo parts (template HILO), as the general
