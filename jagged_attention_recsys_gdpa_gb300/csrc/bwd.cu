@@ -635,10 +635,12 @@ struct DqCfg {
   static constexpr int kVOff = SPLIT ? kKOff + kKStages * kTileBytes : kKOff + kTileBytes;
   static constexpr int kVStride = kKStride;                             // V stage s at kVOff + s strides
   static constexpr int kBarOff = SPLIT ? kVOff + kVStages * kTileBytes : kKOff + kKStages * 2 * kTileBytes;
-  // [2][128] Di, then [2][128] LSE, handed to the activation warpgroups (softmax)
+  // [2][128] Di, then [2][128] LSE, handed to the activation warpgroups
+  // (softmax), then the two barriers that publish a slot's LSE ahead of its Di
   static constexpr int kDiOff = kBarOff + 256;
-  static constexpr int kOOff = (kDiOff + 4 * kTile * 4 + 1023) / 1024 * 1024;  // O tile (one ring, softmax)
-  static constexpr int kSmemBytes = SPLIT ? kDiOff + 4 * kTile * 4 : kOOff + kTileBytes;  // base 1024-aligned
+  static constexpr int kLseBarOff = kDiOff + 4 * kTile * 4;
+  static constexpr int kOOff = (kLseBarOff + 16 + 1023) / 1024 * 1024;  // O tile (one ring, softmax)
+  static constexpr int kSmemBytes = SPLIT ? kLseBarOff + 16 : kOOff + kTileBytes;  // base 1024-aligned
   static constexpr uint32_t kSCol = 0, kDPCol = 256, kDQCol = 384;  // S double-buffered at 0 and 128
 };
 
@@ -703,6 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->acc_empty, kTile);  // the epilogue warpgroup's threads
     for (int s2 = 0; s2 < 2; ++s2) {
       mbar_init(&bars->di_full[s2], 64);
+      mbar_init(reinterpret_cast<uint64_t*>(sm + C::kLseBarOff) + s2, 64);
       mbar_init(&bars->di_empty[s2], kNG * kTile);
     }
     mbar_init(&bars->drain, 1);
@@ -909,7 +912,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(orow[h2]) + 128 * line));
       }
       bool ok = wait_bar(&bars->di_empty[slot], ((n_item >> 1) & 1) ^ 1, abort_flag, a, 75);
-      ok = ok && wait_bar(&bars->qd_full, n_item & 1, abort_flag, a, 76);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      // the rows' LSE first: the activation warps need it for P, Di only for dS
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) di_s[(2 + slot) * kTile + rl[h2]] = lse_rows[h2];
+      mbar_arrive(reinterpret_cast<uint64_t*>(sm + C::kLseBarOff) + slot);
+      ok = wait_bar(&bars->qd_full, n_item & 1, abort_flag, a, 76);
       if (kOTile) ok = ok && wait_bar(&bars->ot_full, n_item & 1, abort_flag, a, 77);
       if (!__all_sync(0xffffffffu, ok)) break;
 #pragma unroll
@@ -947,7 +955,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         di_s[slot * kTile + rl[h2]] = acc[h2];
-        di_s[(2 + slot) * kTile + rl[h2]] = lse_rows[h2];
         if (dot[h2]) a.f1[(it.q0 + it.rt * kTile + rl[h2]) * a.H + it.h] = acc[h2];
       }
       mbar_arrive(&bars->di_full[slot]);
@@ -996,21 +1003,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t gi = (it.q0 + il) * a.H + it.h;
       float lse2 = 0.0f, di = 0.0f;
       const bool single = it.hi - it.lo == 1;  // softmax: Di (and with in-tile stats, LSE) from the tile
+      // softmax: the Di slot whose Di this item still has to read before its
+      // first dS (the LSE, needed for P, is read here)
+      int di_slot = -1;
+      uint32_t di_par = 0;
+      const float* di_s = reinterpret_cast<const float*>(sm + C::kDiOff);
       if constexpr (ACT == JATTN_SOFTMAX) {
         if (it.hi > it.lo && !IN_TILE) {  // items without a key tile use no Di and get no slot
-          // Di and LSE of this row from the Di warps' slot for this item
           const int slot = di_item & 1;
-          bool okd = wait_bar(&bars->di_full[slot], (di_item >> 1) & 1, abort_flag, a, 94);
+          bool okd = wait_bar(reinterpret_cast<uint64_t*>(sm + C::kLseBarOff) + slot, (di_item >> 1) & 1, abort_flag,
+                              a, 94);
           if (!__all_sync(0xffffffffu, okd)) break;
-          const float* di_s = reinterpret_cast<const float*>(sm + C::kDiOff);
-          const float di_row = di_s[slot * kTile + row];
           const float lse_row = di_s[(2 + slot) * kTile + row];
-          mbar_arrive(&bars->di_empty[slot]);
-          ++di_item;
-          if (valid && khi > klo) {
-            lse2 = lse_row * kLog2e;
-            di = di_row;
+          if (valid && khi > klo) lse2 = lse_row * kLog2e;
+          if (single) {
+            mbar_arrive(&bars->di_empty[slot]);  // Di comes from the tile itself
+          } else {
+            di_slot = slot;
+            di_par = (di_item >> 1) & 1;
           }
+          ++di_item;
         }
       }
       bool ok = true;
@@ -1111,6 +1123,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kCols / 32; ++c) tmem_ld32(tDPg + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dp + c * 32));
           tmem_ld_wait();
+          if (ACT == JATTN_SOFTMAX && !IN_TILE && di_slot >= 0) {  // the item's first dS: its Di
+            ok = __all_sync(0xffffffffu, wait_bar(&bars->di_full[di_slot], di_par, abort_flag, a, 96));
+            if (!ok) break;
+            const float di_row = di_s[di_slot * kTile + row];
+            if (valid && khi > klo) di = di_row;
+            mbar_arrive(&bars->di_empty[di_slot]);
+            di_slot = -1;
+          }
           if (ACT == JATTN_SOFTMAX && single) {
             // Di = sum_j P_ij dP_ij over the row's whole key range, in fp32: exact
             // where a Di from the stored bf16 O would carry O's rounding (rows that
