@@ -143,3 +143,36 @@ def test_short_tables_report_status():
     assert J.device_status() == JATTN_ERR_ROPE
     J.backward(x["q"], x["k"], x["v"], o, lse, x["do"], x["q_off"], x["kv_off"], causal=True, rope=t)
     assert J.device_status() == 0
+
+
+def test_attention_autograd_with_rope_softmax():
+    """Softmax, causal: attention(..., rope=...) end to end (GPU rotation, GPU
+    forward, GPU rotary backward reading that forward's O and LSE) against the
+    exact gradient of attention on rotated rows. Rows that see one or two keys
+    lie in each sequence's first query tile, whose keys fit one key tile, so
+    their D_i comes from the tile itself and the bf16 rounding of the stored O
+    does not reach dQ there."""
+    import jagged_attention_recsys_gdpa_gb300 as J
+
+    D = 128
+    w = inputs.Workload("case", 2, D, SOFTMAX, CAUSAL, 0, False, 1.0, True)
+    cpu = G.cpu_inputs(w, SELF_LENS, SELF_LENS, seed=85)
+    cos, sin, t = _tables(D)
+    x = G.to_cuda(cpu)
+    q = x["q"].clone().requires_grad_(True)
+    k = x["k"].clone().requires_grad_(True)
+    v = x["v"].clone().requires_grad_(True)
+    o = J.attention(q, k, v, x["q_off"], x["kv_off"], causal=True, rope=t)
+    o.backward(x["do"])
+    torch.cuda.synchronize()
+    assert J.device_status() == 0
+    rq = oracle.rope(cpu["q"], cpu["q_off"], cpu["kv_off"], cos, sin)
+    rk = oracle.rope(cpu["k"], cpu["q_off"], cpu["kv_off"], cos, sin, keys=True)
+    kw = dict(H=2, D=D, act=SOFTMAX, mask=CAUSAL, window=0, norm_by_lkv=False)
+    o_ref, _ = oracle.fwd(cpu["q_off"], cpu["kv_off"], rq, rk, cpu["v"], **kw)
+    dq_r, dk_r, dv = oracle.bwd(cpu["q_off"], cpu["kv_off"], rq, rk, cpu["v"], cpu["do"], **kw)
+    G.assert_close(G.to64(o), o_ref, "O")
+    G.assert_close(G.to64(q.grad), oracle.rope(dq_r, cpu["q_off"], cpu["kv_off"], cos, sin, inverse=True), "dQ")
+    G.assert_close(G.to64(k.grad), oracle.rope(dk_r, cpu["q_off"], cpu["kv_off"], cos, sin, keys=True,
+                                               inverse=True), "dK")
+    G.assert_close(G.to64(v.grad), dv, "dV")
