@@ -291,9 +291,10 @@ def main():
     # backward takes its statistics from the tile (no O or LSE read)
     in_tile = w.act == 0 and bool(w.mask & 4) and 128 % w.window == 0 and x["kv_off"] is x["q_off"]
     # pooling shapes run on the short-query kernels, cross-attention over short
-    # key sequences on the general forward; both on the fused backward
+    # key sequences on the short-key forward; both on the fused backward
     short_q = flops.short_query_path(w.act, w.mask, w.D, x["lq"], x["lkv"])
-    fused = short_q or flops.short_key_path(w.act, w.mask, w.D, x["lq"], x["lkv"])
+    short_k = flops.short_key_path(w.act, w.mask, w.D, x["lq"], x["lkv"])
+    fused = short_q or short_k
     work = flops.kernel_work(tq, tk, pairs, w.H, w.D, w.act == 0, in_tile=in_tile, fused_bwd=fused)
     o = torch.empty_like(x["q"])
     lse = torch.empty(tq, w.H, dtype=torch.float32, device=dev) if w.act == 0 else None
@@ -331,7 +332,7 @@ def main():
     }
 
     # The step (15 launches: three tile schedules of four kernels, the forward,
-    # dQ with Di, dK/dV; 21 with the fused backward) captured once as a CUDA graph and replayed, so launch
+    # dQ with Di, dK/dV; 21 with the fused backward, 27 with the short-key forward too) captured once as a CUDA graph and replayed, so launch
     # gaps between its short kernels disappear; eager launches are used if
     # capture is not possible.
     run = step
@@ -391,7 +392,7 @@ def main():
     roof["algorithmic"] = wk["bytes"] if roof["bound"] == "hbm" else wk["flops"]
     roof["kernel"] = dom
     if fused:
-        roof["kernel_name"] = {"fwd": "pma_fwd_kernel" if short_q else "fwd_kernel",
+        roof["kernel_name"] = {"fwd": "pma_fwd_kernel" if short_q else "skv_fwd_kernel",
                                "dkdv": "pma_bwd_kernel (fused dQ, dK, dV)"}.get(dom, dom)
     roof["peak_source"] = peaks["source"] + " (burst)"
 
@@ -517,8 +518,9 @@ def main():
             # per step: three tile schedules of four kernels each, the forward,
             # dQ (which also computes softmax's Di) and dK/dV; the fused
             # backward adds a fourth schedule, the gate and itself (the general
-            # dQ and dK/dV passes still launch and find no work)
-            "gpu_launches": (21 if fused else 15) * args.steps,
+            # dQ and dK/dV passes still launch and find no work), and so does
+            # the short-key forward (the general forward finds no work)
+            "gpu_launches": (15 + (6 if fused else 0) + (6 if short_k else 0)) * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

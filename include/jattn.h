@@ -127,11 +127,13 @@ int jattn_workspace_size(const jattn_params_t* p, size_t* bytes);
  * 64-row pieces). The backward fuses dQ, dK and dV into one pass over the
  * keys when every sequence has 1 <= Lq <= 64 or no keys. Cross-attention
  * over short key sequences (the same activation, mask and D, total_q > 64 B
- * and total_kv <= 128 B) keeps the general forward; its backward fuses the
- * three gradients into one pass over 64-query chunks when every sequence has
- * Lkv <= 128, and keys whenever it has queries. Both conditions are checked
- * on the device, without a host round trip; outside them the general passes
- * run. Results and their precision are the same as on the general kernels. */
+ * and total_kv <= 128 B) runs a forward that keeps each sequence's one K/V
+ * tile resident while its query tiles stream past, and a backward that fuses
+ * the three gradients into one pass over 64-query chunks, when every
+ * sequence has Lkv <= 128, and keys whenever it has queries. These
+ * conditions are checked on the device, without a host round trip; outside
+ * them the general passes run. Results and their precision are the same as
+ * on the general kernels. */
 
 /* Forward. Reads q [total_q,H,D], k and v [total_kv,H,D]; writes every row of
  * o [total_q,H,D] and, for JATTN_SOFTMAX, lse [total_q,H] (must be non-NULL

@@ -53,13 +53,13 @@ int cuda_fail(const char* what, cudaError_t e) {
 // mistaken for a failed launch of ours.
 void clear_stale_error() { (void)cudaGetLastError(); }
 
-// Pointwise attention without a mask at D = 128 runs on the kernels that put
-// the keys on the MMA's M dimension (pma.cu) when its sequences are short on
-// one side: pooling (at most 64 queries per sequence on average: forward and
-// fused backward) or cross-attention over short key sequences (at most 128
-// keys per sequence on average: fused backward; the general forward). The
+// Pointwise attention without a mask at D = 128 runs on the kernels of
+// pma.cu when its sequences are short on one side: pooling (at most 64
+// queries per sequence on average: the keys-on-M forward and the fused
+// backward) or cross-attention over short key sequences (at most 128 keys per
+// sequence on average: the short-key forward and the fused backward). The
 // workspace holds their schedule and gate word whenever the shape allows
-// them. Debug flag bit 32 keeps the general kernels; bit 64 also runs the
+// them. Debug flag bit 32 keeps the general kernels; bit 64 runs the
 // short-key shapes' forward on the short-query kernel (for comparisons).
 bool pointwise_unmasked(const jattn_params_t& p) {
   return p.act != JATTN_SOFTMAX && p.mask == JATTN_MASK_NONE && p.D == 128;
@@ -424,12 +424,30 @@ int jattn_fwd(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_o
   if (make_map(&mq, q, p->total_q, p->H, p->D) || make_map(&mk, k, p->total_kv, p->H, p->D) ||
       make_map(&mv, v, p->total_kv, p->H, p->D))
     return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
-  a.tiles = sv.sorted;
-  a.n_tiles = sv.n_tiles;
   a.out0 = reinterpret_cast<__nv_bfloat16*>(o);
   a.f0 = lse;
   a.out_v8 = aligned32(o);
   prof(0, st);
+  // Cross-attention over short key sequences: the short-key forward runs first
+  // and, when the gate finds every sequence within 128 keys, the general
+  // forward below finds an empty schedule.
+  if (use_short_kv(*p) && p->total_kv > 0) {
+    const SchedView ss = sched_carve(base + L.sched_s, p->B, L.tiles_s);
+    if ((e = sched_launch(ss, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 1,
+                          a.status, st)) != cudaSuccess)
+      return cuda_fail("schedule launch", e);
+    int* gate = reinterpret_cast<int*>(base + L.gate);
+    if ((e = launch_pma_gate(q_off, kv_off, p->B, true, gate, sv.n_tiles, sv.n_tiles, st)) != cudaSuccess)
+      return cuda_fail("short-key gate launch", e);
+    AttnArgs b = a;
+    b.tiles = ss.sorted;
+    b.n_tiles = ss.n_tiles;
+    if ((e = launch_skv_fwd(p->act, hilo_for(*p), mq, mk, mv, b, gate, grid_for(dev, L.tiles_s, p->H), st)) !=
+        cudaSuccess)
+      return cuda_fail("short-key forward kernel launch", e);
+  }
+  a.tiles = sv.sorted;
+  a.n_tiles = sv.n_tiles;
   if ((e = launch_fwd(p->D, p->act, fwd_split(*p), (p->mask & JATTN_MASK_BLOCK) != 0, hilo_for(*p), mq, mk, mv, a,
                         grid_for(dev, L.tiles_fwd, p->H), st)) != cudaSuccess)
     return cuda_fail("forward kernel launch", e);

@@ -76,6 +76,11 @@ cudaError_t launch_bwd_dq_hilo(int D, int act, bool split, const CUtensorMap& q,
 // then empties the general dQ and dK/dV schedules.
 cudaError_t launch_pma_fwd(int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                            const AttnArgs& a, int grid, cudaStream_t stream);
+// Short-key forward (pma.cu): cross-attention whose every sequence has at
+// most 128 keys (the gate's cross mode), items from the 128-row key-tile
+// schedule with 128-row query ranges; Q map with 128-row boxes, a.out0 = O.
+cudaError_t launch_skv_fwd(int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                           const AttnArgs& a, const int* gate, int grid, cudaStream_t stream);
 cudaError_t launch_pma_gate(const int64_t* q_off, const int64_t* kv_off, int64_t B, bool cross, int* gate,
                             int* n_tiles_q, int* n_tiles_kv, cudaStream_t stream);
 cudaError_t launch_pma_bwd(int act, bool hilo, bool cross, const CUtensorMap& q, const CUtensorMap& k,

@@ -24,6 +24,9 @@
 //               K / V tile is loaded once, the 64-query chunks are the steps;
 //               dQ of a chunk is complete after its step, dV and dK
 //               accumulate over the item. Q and dO are read once.
+// The same short-key shapes have a forward in the usual orientation
+// (skv_fwd_kernel): each sequence's K / V tile stays in shared memory while
+// its 128-row query tiles stream through a ring.
 // A gate kernel checks the chosen mode's limits on the device and either
 // clears the general dQ and dK/dV schedules (their passes then find no work)
 // or leaves them to run while this pass finds the gate closed and returns.
@@ -445,42 +448,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
-// ---------------------------------------------------------------------------- backward
-// Two modes share the kernel. Pooling (CROSS = false): an item is (sequence,
-// head) with at most 64 queries, loaded once, and its key tiles are the steps;
-// dV and dK are complete per step, dQ^T accumulates over the item. Cross
-// attention over short key sequences (CROSS = true): an item is (sequence,
-// head) with at most 128 keys, loaded once, and its 64-query chunks are the
-// steps; dQ^T is complete per step, dV and dK accumulate over the item.
-template <bool HILO, bool CROSS>
-struct PbCfg {
-  static constexpr int kQDStages = CROSS ? 4 : 1;  // Q + dO chunk pairs
-  static constexpr int kKStages = CROSS ? 1 : 3;
-  static constexpr int kVStages = CROSS ? 1 : 2;
-  static constexpr int kNP = HILO ? 2 : 1;  // dS^T tiles in shared memory (hi, lo)
-  static constexpr int kQDOff = 0;          // stage s: Q chunk, then dO chunk
-  static constexpr int kKOff = kQDStages * 2 * kChunkBytes;
-  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
-  static constexpr int kDSOff = kVOff + kVStages * kTileBytes;
-  static constexpr int kBarOff = kDSOff + kNP * kPBytes;
-  static constexpr int kSmemBytes = kBarOff + 256;
-  // TMEM: S^T (P^T as bf16 over its first columns), dP^T (dS^T likewise), dV, dK, dQ^T
-  static constexpr uint32_t kSCol = 0, kDPCol = 64, kDVCol = 128, kDKCol = 256, kDQCol = 384;
-};
-static_assert(PbCfg<false, false>::kSmemBytes <= 227 * 1024 && PbCfg<true, false>::kSmemBytes <= 227 * 1024 &&
-                  PbCfg<false, true>::kSmemBytes <= 227 * 1024 && PbCfg<true, true>::kSmemBytes <= 227 * 1024,
-              "shared memory");
-
-struct PbBars {
-  uint64_t qd_full[4], qd_empty[4];  // Q and dO chunks
-  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
-  uint64_t s_full, dp_full, p_ready, ds_ready, dsm_free;
-  uint64_t acc_full, acc_empty, dq_full, dq_empty, drain;
-  uint32_t tmem_base;
-  int abort_flag;
-};
-static_assert(sizeof(PbBars) <= 256, "barrier block overflows its slot");
-
 // Item of the fused backward: pooling items come from the 64-row query-tile
 // schedule (one tile per sequence; [lo, hi) = key tiles), cross items from
 // the 128-row key-tile schedule with 64-column query ranges (one tile per
@@ -525,6 +492,306 @@ __device__ __forceinline__ void store_chunk_cols(__nv_bfloat16* out, int64_t q_f
 // next 16 (lo parts), so neither warpgroup writes where the other still
 // reads; the kk-th 16-query slice of the hi parts sits at a_col(kk).
 __device__ __forceinline__ uint32_t a_col(int kk) { return static_cast<uint32_t>((kk >> 1) * 32 + (kk & 1) * 8); }
+
+// ---------------------------------------------------------------------------- short-key forward
+// Cross-attention over short key sequences (every sequence at most 128 keys):
+// one item = (sequence, head) with all of its 128-row query tiles, in the
+// usual orientation (S = Q K^T, M = queries). The item's one K / V tile is
+// loaded once; its query tiles stream through a 4-stage ring, and the two
+// activation warpgroups take alternate tiles: S and O are double-buffered in
+// TMEM ([S0 | S1 | O0 | O1]), so one warpgroup's activation and epilogue
+// overlap the other's products. With a single key tile O = P V needs no
+// online accumulation: the product overwrites O.
+constexpr int kSkvQStages = 4;
+constexpr int kSkvCtlRegs = 104;  // 384 x 168 at launch = 128 x 104 + 256 x 200
+constexpr int kSkvActRegs = 200;
+static_assert(128 * kSkvCtlRegs + 256 * kSkvActRegs <= kThreads * 168, "register split");
+
+template <bool HILO>
+struct SfCfg {
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kQOff = 2 * kTileBytes;  // stage s at kQOff + s * kTileBytes
+  static constexpr int kBarOff = kQOff + kSkvQStages * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 256;
+  static constexpr uint32_t kOCol = 2 * kTile;  // S_g at g * 128, O_g at kOCol + g * 128
+};
+static_assert(SfCfg<false>::kSmemBytes <= 227 * 1024, "shared memory");
+
+struct SfBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[kSkvQStages], q_empty[kSkvQStages];
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(SfBars) <= 256, "barrier block overflows its slot");
+
+template <int ACT, bool HILO>
+__global__ void __launch_bounds__(kThreads, 1)
+    skv_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const AttnArgs a, const int* gate) {
+  using C = SfCfg<HILO>;
+  if (*gate == 0) return;  // some sequence holds more than 128 keys: the general forward runs
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) record_error(a.status, JATTN_ERR_UNSUPPORTED, 110, blockIdx.x);
+    return;
+  }
+  uint8_t* sm = smem_raw;
+  SfBars* bars = reinterpret_cast<SfBars*>(sm + C::kBarOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &bars->abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
+    for (int s = 0; s < kSkvQStages; ++s) {
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&bars->s_full[g], 1);
+      mbar_init(&bars->p_full[g], kTile);
+      mbar_init(&bars->o_full[g], 1);
+      mbar_init(&bars->o_empty[g], kTile);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSkvCtlRegs));
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t kv_it = 0, q_it = 0;
+      bool ok = true, kv_armed = false;
+      // the item's K / V copy is skipped under debug flag bit 1, so that the
+      // waits for it time out
+      const bool skip = (a.debug_flags & 1) != 0;
+      PItem it;
+      for (long long r = 0; ok && load_bitem<true>(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!(ok = wait_bar(&bars->kv_empty, (kv_it & 1) ^ 1, abort_flag, a, 111))) break;
+        if (!skip) {
+          mbar_arrive_expect_tx(&bars->kv_full, 2 * kTileBytes);
+          for (int c = 0; c < 2; ++c) {
+            tma_load_2d(sm + C::kKOff + c * kBoxK, &tmK, &bars->kv_full, it.h * kD + c * 64, static_cast<int>(it.k0));
+            tma_load_2d(sm + C::kVOff + c * kBoxK, &tmV, &bars->kv_full, it.h * kD + c * 64, static_cast<int>(it.k0));
+          }
+          kv_armed = true;
+        }
+        ++kv_it;
+        for (int t = it.lo; t < it.hi && ok; ++t, ++q_it) {
+          const int s = q_it % kSkvQStages;
+          if (!(ok = wait_bar(&bars->q_empty[s], ((q_it / kSkvQStages) & 1) ^ 1, abort_flag, a, 112))) break;
+          mbar_arrive_expect_tx(&bars->q_full[s], kTileBytes);
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d(sm + C::kQOff + s * kTileBytes + c * kBoxK, &tmQ, &bars->q_full[s], it.h * kD + c * 64,
+                        static_cast<int>(it.q0) + t * kTile);
+        }
+      }
+      if (kv_armed) drain_wait(&bars->kv_full, (kv_it - 1) & 1, a.timeout_ns);
+      for (uint32_t i = (q_it > (uint32_t)kSkvQStages ? q_it - kSkvQStages : 0); i < q_it; ++i)
+        drain_wait(&bars->q_full[i % kSkvQStages], (i / kSkvQStages) & 1, a.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kTile, kTile, false, false);  // S = Q K^T
+      constexpr uint32_t idO = idesc_bf16_f32(kTile, kD, false, true);      // O = P V
+      const uint64_t dK = sdesc_sw128(smem_u32(sm + C::kKOff), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(sm + C::kVOff), kBoxK, 1024);
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(sm + C::kQOff), 16, 1024);
+      uint32_t kv_it = 0, q_used = 0, n = 0;
+      bool ok = true;
+      PItem it;
+      // O_g = P_g V for the item's t-th query tile (global tile nt)
+      auto issue_pv = [&](uint32_t nt) -> bool {
+        const uint32_t g = nt & 1, u = nt >> 1;
+        if (!wait_bar(&bars->p_full[g], u & 1, abort_flag, a, 113)) return false;
+        if (!wait_bar(&bars->o_empty[g], (u & 1) ^ 1, abort_flag, a, 114)) return false;
+        tc_fence_after();
+        constexpr int kNP = HILO ? 2 : 1;
+#pragma unroll
+        for (int hl = 0; hl < kNP; ++hl)
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tmem + C::kOCol + g * kD, tmem + g * kTile + 64 * hl + kk * 8, dV + mnslice(kk), idO,
+                   (hl > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->o_full[g]);
+        return true;
+      };
+      for (long long r = 0; ok && load_bitem<true>(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!(ok = wait_bar(&bars->kv_full, kv_it & 1, abort_flag, a, 115))) break;
+        ++kv_it;
+        const int nq = it.hi - it.lo;
+        for (int t = 0; t < nq && ok; ++t) {
+          const uint32_t nt = n + t, g = nt & 1, qi = q_used + t;
+          const int qs = qi % kSkvQStages;
+          if (!(ok = wait_bar(&bars->q_full[qs], (qi / kSkvQStages) & 1, abort_flag, a, 116))) break;
+          tc_fence_after();
+          // S_g overwrites P_g of tile nt - 2, which its PV product (issued
+          // before) has read
+          const uint64_t qd = dQ0 + qs * (kTileBytes >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_ss(tmem + g * kTile, qd + kslice(kk, kBoxK), dK + kslice(kk, kBoxK), idS, kk > 0 ? 1u : 0u);
+          mma_commit(&bars->s_full[g]);
+          mma_commit(&bars->q_empty[qs]);
+          if (t > 0) ok = issue_pv(nt - 1);
+        }
+        if (ok) ok = issue_pv(n + nq - 1);
+        if (!ok) break;
+        mma_commit(&bars->kv_empty);  // K read by the S products, V by the PV products
+        n += nq;
+        q_used += nq;
+      }
+      mma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0, a.timeout_ns);
+    }
+    __syncwarp();
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSkvActRegs));
+    // ------------------------------------------------------------ activation warpgroups
+    // Warpgroup g takes the query tiles of global index g mod 2: its S_g
+    // becomes P_g (bf16 hi parts over S_g's first 64 columns, lo parts over
+    // the next 64), then it stores O_g's rows.
+    const int g = (warp - 4) >> 2;
+    const int row = 32 * (warp & 3) + lane;  // query row of the tile
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t tS = tmem + lane_base + g * kTile, tO = tmem + lane_base + C::kOCol + g * kD;
+    uint32_t n = 0;
+    bool ok = true;
+    PItem it;
+    for (long long r = 0; ok && load_bitem<true>(a, r, it); ++r) {
+      const int nq = it.hi - it.lo;
+      if (nq <= 0) continue;  // no queries: nothing to write (the gate admits no queries without keys)
+      const float cn = (a.norm_by_lkv && it.lkv > 0) ? 1.0f / it.lkv : 1.0f;
+      const int nkc = (it.lkv + 31) / 32;  // 32-key chunks that hold keys
+      for (int t = 0; t < nq; ++t) {
+        const uint32_t nt = n + t;
+        if ((nt & 1) != static_cast<uint32_t>(g)) continue;
+        const uint32_t u = nt >> 1;
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->s_full[g], u & 1, abort_flag, a, 117));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sv[kTile];
+#pragma unroll
+        for (int c = 0; c < kTile / 32; ++c)
+          if (c < nkc) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
+        tmem_ld_wait();
+        // P over the keys of the sequence; zero past its end (V rows there
+        // belong to other sequences)
+#pragma unroll
+        for (int c = 0; c < kTile / 32; ++c) {
+          uint32_t hi[16], lo[16];
+          if (c < nkc) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int kc = 32 * c + 2 * e;
+              const float f0 = kc < it.lkv ? act_f<ACT>(__uint_as_float(sv[kc]) * a.scale) : 0.0f;
+              const float f1 = kc + 1 < it.lkv ? act_f<ACT>(__uint_as_float(sv[kc + 1]) * a.scale) : 0.0f;
+              hi[e] = pack_bf16x2(f0, f1);
+              if constexpr (HILO) lo[e] = bf16x2_lo(f0, f1, hi[e]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
+          }
+          tmem_st16(tS + 16 * c, hi);
+          if constexpr (HILO) tmem_st16(tS + 64 + 16 * c, lo);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[g]);
+        // O_g = P_g V, times 1/Lkv when asked, to the tile's rows of the sequence
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->o_full[g], u & 1, abort_flag, a, 118));
+        if (!ok) break;
+        tc_fence_after();
+        const int ql = (it.lo + t) * kTile + row;
+        const bool valid = ql < it.lq;
+        __nv_bfloat16* orow = a.out0 + ((it.q0 + ql) * a.H + it.h) * kD;
+#pragma unroll 1
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + 32 * c, v);
+          tmem_ld_wait();
+          if (c == kD / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&bars->o_empty[g]);
+          }
+          if (valid) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * cn, __uint_as_float(v[2 * e + 1]) * cn);
+            store_words16(orow + 32 * c, w, a.out_v8);
+          }
+        }
+      }
+      if (!ok) break;
+      n += nq;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------- backward
+// Two modes share the kernel. Pooling (CROSS = false): an item is (sequence,
+// head) with at most 64 queries, loaded once, and its key tiles are the steps;
+// dV and dK are complete per step, dQ^T accumulates over the item. Cross
+// attention over short key sequences (CROSS = true): an item is (sequence,
+// head) with at most 128 keys, loaded once, and its 64-query chunks are the
+// steps; dQ^T is complete per step, dV and dK accumulate over the item.
+template <bool HILO, bool CROSS>
+struct PbCfg {
+  static constexpr int kQDStages = CROSS ? 4 : 1;  // Q + dO chunk pairs
+  static constexpr int kKStages = CROSS ? 1 : 3;
+  static constexpr int kVStages = CROSS ? 1 : 2;
+  static constexpr int kNP = HILO ? 2 : 1;  // dS^T tiles in shared memory (hi, lo)
+  static constexpr int kQDOff = 0;          // stage s: Q chunk, then dO chunk
+  static constexpr int kKOff = kQDStages * 2 * kChunkBytes;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kDSOff = kVOff + kVStages * kTileBytes;
+  static constexpr int kBarOff = kDSOff + kNP * kPBytes;
+  static constexpr int kSmemBytes = kBarOff + 256;
+  // TMEM: S^T (P^T as bf16 over its first columns), dP^T (dS^T likewise), dV, dK, dQ^T
+  static constexpr uint32_t kSCol = 0, kDPCol = 64, kDVCol = 128, kDKCol = 256, kDQCol = 384;
+};
+static_assert(PbCfg<false, false>::kSmemBytes <= 227 * 1024 && PbCfg<true, false>::kSmemBytes <= 227 * 1024 &&
+                  PbCfg<false, true>::kSmemBytes <= 227 * 1024 && PbCfg<true, true>::kSmemBytes <= 227 * 1024,
+              "shared memory");
+
+struct PbBars {
+  uint64_t qd_full[4], qd_empty[4];  // Q and dO chunks
+  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
+  uint64_t s_full, dp_full, p_ready, ds_ready, dsm_free;
+  uint64_t acc_full, acc_empty, dq_full, dq_empty, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(PbBars) <= 256, "barrier block overflows its slot");
 
 template <int ACT, bool HILO, bool CROSS>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -1024,6 +1291,17 @@ cudaError_t bwd_act(bool hilo, bool cross, const CUtensorMap& q, const CUtensorM
               : bwd_one<ACT, false, false>(q, k, v, dout, a, gate, grid, st);
 }
 
+template <int ACT>
+cudaError_t skv_act(bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const AttnArgs& a,
+                    const int* gate, int grid, cudaStream_t st) {
+  auto kernel = hilo ? skv_fwd_kernel<ACT, true> : skv_fwd_kernel<ACT, false>;
+  constexpr int smem = SfCfg<false>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kThreads, smem, st>>>(q, k, v, a, gate);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_pma_fwd(int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
@@ -1032,6 +1310,16 @@ cudaError_t launch_pma_fwd(int act, bool hilo, const CUtensorMap& q, const CUten
     case JATTN_SILU: return fwd_act<JATTN_SILU>(hilo, q, k, v, a, grid, stream);
     case JATTN_GELU_TANH: return fwd_act<JATTN_GELU_TANH>(hilo, q, k, v, a, grid, stream);
     case JATTN_GELU_POLY: return fwd_act<JATTN_GELU_POLY>(hilo, q, k, v, a, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_skv_fwd(int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                           const AttnArgs& a, const int* gate, int grid, cudaStream_t stream) {
+  switch (act) {
+    case JATTN_SILU: return skv_act<JATTN_SILU>(hilo, q, k, v, a, gate, grid, stream);
+    case JATTN_GELU_TANH: return skv_act<JATTN_GELU_TANH>(hilo, q, k, v, a, gate, grid, stream);
+    case JATTN_GELU_POLY: return skv_act<JATTN_GELU_POLY>(hilo, q, k, v, a, gate, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -54,11 +54,11 @@ def short_query_path(act: int, mask: int, D: int, lq, lkv) -> bool:
 
 
 def short_key_path(act: int, mask: int, D: int, lq, lkv) -> bool:
-    """Whether the library's backward runs a batch as cross-attention over
-    short key sequences on the fused kernel: a pointwise activation, no mask,
-    D = 128, more than 64 queries but at most 128 keys per sequence on average
-    (the host's rule) and every sequence with Lkv <= 128 and keys whenever it
-    has queries (the device-side gate). The forward stays on the general kernel."""
+    """Whether the library runs a batch as cross-attention over short key
+    sequences: the short-key forward and the fused backward's cross mode. A
+    pointwise activation, no mask, D = 128, more than 64 queries but at most
+    128 keys per sequence on average (the host's rule) and every sequence with
+    Lkv <= 128 and keys whenever it has queries (the device-side gate)."""
     lq = np.asarray(lq, dtype=np.int64)
     lkv = np.asarray(lkv, dtype=np.int64)
     if act == 0 or mask != 0 or D != 128 or len(lq) == 0:

@@ -228,3 +228,40 @@ def test_short_key_backward_times_out_then_recovers():
     g = G.gpu_run(x, w)
     assert J.device_status() == 0
     G.compare(g, G.oracle_run(cpu, w), w)
+
+
+def test_short_key_forward_times_out_then_recovers():
+    """With the key copies skipped, the short-key forward gives up its bounded
+    waits, reports TIMEOUT and returns; a clean forward afterwards is correct."""
+    import jagged_attention_recsys_gdpa_gb300 as J
+    from jagged_attention_recsys_gdpa_gb300 import _binding as B
+
+    w = _w(GELU)
+    cpu = G.cpu_inputs(w, CROSS_LQ, CROSS_LKV, 102)
+    x = G.to_cuda(cpu)
+    kw = dict(act=GELU, norm_by_lkv=True)
+    J.device_status()
+    try:
+        B.debug_set(1, 50_000_000)
+        J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], **kw)
+        assert J.device_status() == JATTN_ERR_TIMEOUT
+    finally:
+        B.debug_set(0, 0)
+    g = G.gpu_run(x, w)
+    assert J.device_status() == 0
+    G.compare(g, G.oracle_run(cpu, w), w)
+
+
+def test_short_key_forward_outputs_only_touch_their_rows():
+    import jagged_attention_recsys_gdpa_gb300 as J
+
+    w = _w(SILU, norm=False)
+    cpu = G.cpu_inputs(w, CROSS_LQ, CROSS_LKV, 103)
+    x = G.to_cuda(cpu)
+    TQ, pad = x["q"].shape[0], 5
+    bo = torch.full((TQ + 2 * pad, w.H, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    o = bo[pad : pad + TQ]
+    J.forward(x["q"], x["k"], x["v"], x["q_off"], x["kv_off"], act=SILU, norm_by_lkv=False, out=o)
+    torch.cuda.synchronize()
+    assert torch.all(bo[:pad] == 7.0) and torch.all(bo[pad + TQ :] == 7.0)
+    G.assert_close(G.to64(o), G.oracle_run(cpu, w, backward=False)["o"], "O")
