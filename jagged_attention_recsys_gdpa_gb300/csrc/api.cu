@@ -711,8 +711,11 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
   if (sq) {
     const SchedView ss = sched_carve(base + L.sched_s, p->B, L.tiles_s);
     // pooling: 64-row query tiles over the key tiles; cross: 128-row key tiles
-    // over 64-row query chunks
-    const int srow = cross ? kTile : pma_rows_per_item(), scol = cross ? pma_rows_per_item() : kTile;
+    // over 128-row query tiles (debug flag bit 128: the keys-on-M cross mode,
+    // over 64-row query chunks)
+    const bool cross_t = cross && (g_debug_flags & 128);
+    const int srow = cross ? kTile : pma_rows_per_item();
+    const int scol = cross && !cross_t ? kTile : cross ? pma_rows_per_item() : kTile;
     if ((e = sched_launch(ss, q_off, kv_off, p->B, p->total_q, p->total_kv, srow, scol, p->mask, a.window,
                           cross ? 1 : 0, a.status, st)) != cudaSuccess ||
         (e = sched_launch(qs, q_off, kv_off, p->B, p->total_q, p->total_kv, kTile, kTile, p->mask, a.window, 0,
@@ -735,9 +738,12 @@ int bwd_impl(const jattn_params_t* p, const int64_t* q_off, const int64_t* kv_of
     b.out2 = reinterpret_cast<__nv_bfloat16*>(dk);
     b.out_v8 = aligned32(dk) && aligned32(dv);
     prof(2, st);
-    if ((e = launch_pma_bwd(p->act, hilo_for(*p), cross, sq_q, mk, mv, sq_do, b, gate,
-                            grid_for(dev, L.tiles_s, p->H), st)) != cudaSuccess)
-      return cuda_fail("short-query backward kernel launch", e);
+    if (cross && !cross_t)
+      e = launch_skv_bwd(p->act, hilo_for(*p), mq, mk, mv, mdo, b, gate, grid_for(dev, L.tiles_s, p->H), st);
+    else
+      e = launch_pma_bwd(p->act, hilo_for(*p), cross, sq_q, mk, mv, sq_do, b, gate, grid_for(dev, L.tiles_s, p->H),
+                         st);
+    if (e != cudaSuccess) return cuda_fail("fused backward kernel launch", e);
     prof(3, st);
   }
   // The dQ pass runs first: for softmax it also writes Di, which the dK/dV pass reads.

@@ -81,6 +81,12 @@ cudaError_t launch_pma_fwd(int act, bool hilo, const CUtensorMap& q, const CUten
 // schedule with 128-row query ranges; Q map with 128-row boxes, a.out0 = O.
 cudaError_t launch_skv_fwd(int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                            const AttnArgs& a, const int* gate, int grid, cudaStream_t stream);
+// Short-key backward (pma.cu): the same shapes and schedule as
+// launch_skv_fwd (128-row query ranges), Q / dO maps with 128-row boxes;
+// a.out0 = dQ, a.out1 = dV, a.out2 = dK.
+cudaError_t launch_skv_bwd(int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                           const CUtensorMap& dout, const AttnArgs& a, const int* gate, int grid,
+                           cudaStream_t stream);
 cudaError_t launch_pma_gate(const int64_t* q_off, const int64_t* kv_off, int64_t B, bool cross, int* gate,
                             int* n_tiles_q, int* n_tiles_kv, cudaStream_t stream);
 cudaError_t launch_pma_bwd(int act, bool hilo, bool cross, const CUtensorMap& q, const CUtensorMap& k,

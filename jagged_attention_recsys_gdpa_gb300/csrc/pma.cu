@@ -757,6 +757,438 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// ---------------------------------------------------------------------------- short-key backward
+// Cross-attention over short key sequences, backward, with 128 queries per
+// step so that every product runs at N = 128. One item = (sequence, head):
+// its K / V tile stays in shared memory, its 128-row Q / dO tiles stream
+// through a 2-stage ring. Per step (query tile t):
+//   S^T = K Q^T, dP^T = V dO^T            (TMEM lanes = keys)
+//   P^T, dS^T = act'(scale S^T) * dP^T     (bf16, back into TMEM as A operands)
+//   dV += P^T dO, dK += dS^T Q             (accumulated over the item)
+//   dQ = dS K                              (A = dS^T from shared memory, MN-major;
+//                                           into the dP^T columns once dK has
+//                                           read dS^T: lanes = queries)
+// and the epilogue warpgroup writes dQ's rows each step and dK / dV's rows at
+// the item's end. TMEM [S^T | dP^T, then dQ | dV | dK] = 512 columns; the next
+// step's S^T is issued right after this step's dQ, its dP^T once the
+// epilogue has read dQ.
+constexpr int kSbCtlRegs = 120;  // 512 x 128 at launch = 128 x (120 + 2 x 160 + 72)
+constexpr int kSbActRegs = 160;
+constexpr int kSbEpiRegs = 72;
+static_assert(128 * (kSbCtlRegs + 2 * kSbActRegs + kSbEpiRegs) <= kBwdThreads * 128, "register split");
+constexpr int kSbMaxStages = 2;
+
+// setmaxnreg toward R registers from the 128 at launch: .inc above, .dec below.
+template <int R>
+__device__ __forceinline__ void sb_set_regs() {
+  if constexpr (R > 128) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+  if constexpr (R < 128) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+
+template <bool HILO>
+struct SbCfg {
+  static constexpr int kStages = HILO ? 1 : 2;  // Q / dO ring (the hi + lo dS^T tiles take the second stage's room)
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kQDOff = 2 * kTileBytes;  // stage s: Q tile, then dO tile
+  static constexpr int kNP = HILO ? 2 : 1;
+  static constexpr int kDSOff = kQDOff + kStages * 2 * kTileBytes;  // dS^T [keys][queries] (hi, lo)
+  static constexpr int kBarOff = kDSOff + kNP * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 256;
+  static constexpr uint32_t kSCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 384;  // dQ over kDPCol
+};
+static_assert(SbCfg<false>::kSmemBytes <= 227 * 1024 && SbCfg<true>::kSmemBytes <= 227 * 1024, "shared memory");
+
+struct SbBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t qd_full[kSbMaxStages], qd_empty[kSbMaxStages];
+  uint64_t s_full, dp_full, p_ready, ds_ready, dsm_free;
+  uint64_t acc_full, acc_empty, dq_full, dq_empty, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(SbBars) <= 256, "barrier block overflows its slot");
+
+// A operand column of the kk-th 16-query slice (hi parts hl = 0, lo parts
+// hl = 1) of P^T / dS^T: activation warpgroup g owns fp32 columns
+// [64 g, 64 g + 64) and packs each 32-query half in place of its own 32
+// columns, hi parts over the first 16 and lo parts over the next 16.
+__device__ __forceinline__ uint32_t sb_acol(int kk, int hl) {
+  return static_cast<uint32_t>((kk >> 2) * 64 + ((kk >> 1) & 1) * 32 + hl * 16 + (kk & 1) * 8);
+}
+
+// 16 packed bf16 pairs (queries c0 .. c0 + 31 of key row `row`) into a
+// [128 keys][128 queries] tile made of two [128][64] 128-byte-swizzled boxes.
+__device__ __forceinline__ void st_dst_row(uint32_t tile, int row, int c0, const uint32_t (&w)[16]) {
+  st_pt_row(tile + (c0 >> 6) * kBoxK, row, c0 & 63, w);
+}
+
+template <int ACT, bool HILO>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    skv_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                   const AttnArgs a, const int* gate) {
+  using C = SbCfg<HILO>;
+  if (*gate == 0) return;  // some sequence holds more than 128 keys: the general passes run
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) record_error(a.status, JATTN_ERR_UNSUPPORTED, 120, blockIdx.x);
+    return;
+  }
+  uint8_t* sm = smem_raw;
+  SbBars* bars = reinterpret_cast<SbBars*>(sm + C::kBarOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &bars->abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->qd_full[s], 1);
+      mbar_init(&bars->qd_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, 2 * kTile);
+    mbar_init(&bars->ds_ready, 2 * kTile);
+    mbar_init(&bars->dsm_free, 1);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, kTile);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_empty, kTile);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp < 4) {
+  sb_set_regs<kSbCtlRegs>();
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      uint32_t kv_it = 0, qd_it = 0;
+      bool ok = true, kv_armed = false;
+      const bool skip = (a.debug_flags & 1) != 0;  // the item's K / V copy, so that its waits time out
+      PItem it;
+      for (long long r = 0; ok && load_bitem<true>(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!(ok = wait_bar(&bars->kv_empty, (kv_it & 1) ^ 1, abort_flag, a, 121))) break;
+        if (!skip) {
+          mbar_arrive_expect_tx(&bars->kv_full, 2 * kTileBytes);
+          for (int c = 0; c < 2; ++c) {
+            tma_load_2d(sm + C::kKOff + c * kBoxK, &tmK, &bars->kv_full, it.h * kD + c * 64, static_cast<int>(it.k0));
+            tma_load_2d(sm + C::kVOff + c * kBoxK, &tmV, &bars->kv_full, it.h * kD + c * 64, static_cast<int>(it.k0));
+          }
+          kv_armed = true;
+        }
+        ++kv_it;
+        for (int t = it.lo; t < it.hi && ok; ++t, ++qd_it) {
+          const int s = qd_it % C::kStages;
+          if (!(ok = wait_bar(&bars->qd_empty[s], ((qd_it / C::kStages) & 1) ^ 1, abort_flag, a, 122))) break;
+          mbar_arrive_expect_tx(&bars->qd_full[s], 2 * kTileBytes);
+          uint8_t* dst = sm + C::kQDOff + s * 2 * kTileBytes;
+          const int y = static_cast<int>(it.q0) + t * kTile;
+          for (int c = 0; c < 2; ++c) {
+            tma_load_2d(dst + c * kBoxK, &tmQ, &bars->qd_full[s], it.h * kD + c * 64, y);
+            tma_load_2d(dst + kTileBytes + c * kBoxK, &tmDO, &bars->qd_full[s], it.h * kD + c * 64, y);
+          }
+        }
+      }
+      if (kv_armed) drain_wait(&bars->kv_full, (kv_it - 1) & 1, a.timeout_ns);
+      for (uint32_t i = (qd_it > (uint32_t)C::kStages ? qd_it - C::kStages : 0); i < qd_it; ++i)
+        drain_wait(&bars->qd_full[i % C::kStages], (i / C::kStages) & 1, a.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kTile, kTile, false, false);  // S^T = K Q^T, dP^T = V dO^T
+      constexpr uint32_t idG = idesc_bf16_f32(kTile, kD, false, true);      // dV = P^T dO, dK = dS^T Q
+      constexpr uint32_t idQ = idesc_bf16_f32(kTile, kD, true, true);       // dQ = dS K
+      const uint32_t sK = smem_u32(sm + C::kKOff), sV = smem_u32(sm + C::kVOff), sQD = smem_u32(sm + C::kQDOff);
+      const uint64_t dKk = sdesc_sw128(sK, 16, 1024), dVk = sdesc_sw128(sV, 16, 1024);
+      const uint64_t dKm = sdesc_sw128(sK, kBoxK, 1024);
+      const uint64_t dDS = sdesc_sw128(smem_u32(sm + C::kDSOff), kBoxK, 1024);
+      uint32_t kv_it = 0, qd_used = 0, acc_n = 0, n = 0;
+      bool ok = true;
+      PItem it;
+      auto qbase = [&](uint32_t qi) { return sQD + (qi % C::kStages) * 2 * kTileBytes; };
+      // S^T of step t (query tile qi)
+      auto issue_s = [&](uint32_t qi) -> bool {
+        const int qs = qi % C::kStages;
+        if (!wait_bar(&bars->qd_full[qs], (qi / C::kStages) & 1, abort_flag, a, 123)) return false;
+        tc_fence_after();
+        const uint64_t dQk = sdesc_sw128(qbase(qi), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + C::kSCol, dKk + kslice(kk, kBoxK), dQk + kslice(kk, kBoxK), idS, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->s_full);
+        return true;
+      };
+      // dP^T of step t (overwrites the dQ of the step before, once read)
+      auto issue_dp = [&](uint32_t qi, uint32_t nt) -> bool {
+        if (!wait_bar(&bars->dq_empty, (nt & 1) ^ 1, abort_flag, a, 124)) return false;
+        tc_fence_after();
+        const uint64_t dDOk = sdesc_sw128(qbase(qi) + kTileBytes, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + C::kDPCol, dVk + kslice(kk, kBoxK), dDOk + kslice(kk, kBoxK), idS, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->dp_full);
+        return true;
+      };
+      for (long long r = 0; ok && load_bitem<true>(a, r, it); ++r) {
+        if (it.hi <= it.lo) continue;
+        if (!(ok = wait_bar(&bars->kv_full, kv_it & 1, abort_flag, a, 125))) break;
+        ++kv_it;
+        tc_fence_after();
+        const int ns = it.hi - it.lo;
+        if (!(ok = issue_s(qd_used) && issue_dp(qd_used, n))) break;
+        for (int t = 0; t < ns; ++t) {
+          const uint32_t nt = n + t, qi = qd_used + t;
+          const uint32_t qb = qbase(qi);
+          const uint64_t dQm = sdesc_sw128(qb, kBoxK, 1024), dDOm = sdesc_sw128(qb + kTileBytes, kBoxK, 1024);
+          // dV += P^T dO, once P^T is in TMEM (and, on the item's first step,
+          // the epilogue has drained the item before's dV / dK)
+          if (!(ok = wait_bar(&bars->p_ready, nt & 1, abort_flag, a, 126))) break;
+          if (t == 0 && !(ok = wait_bar(&bars->acc_empty, (acc_n & 1) ^ 1, abort_flag, a, 127))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int hl = 0; hl < C::kNP; ++hl)
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ts(tmem + C::kDVCol, tmem + C::kSCol + sb_acol(kk, hl), dDOm + mnslice(kk), idG,
+                     (t > 0 || hl > 0 || kk > 0) ? 1u : 0u);
+          if (!(ok = wait_bar(&bars->ds_ready, nt & 1, abort_flag, a, 128))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int hl = 0; hl < C::kNP; ++hl)
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ts(tmem + C::kDKCol, tmem + C::kDPCol + sb_acol(kk, hl), dQm + mnslice(kk), idG,
+                     (t > 0 || hl > 0 || kk > 0) ? 1u : 0u);
+          // dQ = dS K into the dP^T columns (dK has been issued: in order, it
+          // reads dS^T first); then the shared dS^T tile and Q / dO are free
+#pragma unroll
+          for (int hl = 0; hl < C::kNP; ++hl)
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ss(tmem + C::kDPCol, dDS + hl * (kTileBytes >> 4) + mnslice(kk), dKm + mnslice(kk), idQ,
+                     (hl > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars->dq_full);
+          mma_commit(&bars->dsm_free);
+          mma_commit(&bars->qd_empty[qi % C::kStages]);
+          if (t + 1 < ns) {
+            if (!(ok = issue_s(qi + 1))) break;
+            if (!(ok = issue_dp(qi + 1, nt + 1))) break;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bars->acc_full);
+        ++acc_n;
+        mma_commit(&bars->kv_empty);
+        n += ns;
+        qd_used += ns;
+      }
+      mma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0, a.timeout_ns);
+    }
+    __syncwarp();
+  }
+  } else if (warp < 12) {
+    sb_set_regs<kSbActRegs>();
+    // ------------------------------------------------------------ activation warpgroups
+    // warpgroup g takes queries [64 g, 64 g + 64) of every step
+    const int g = (warp - 4) >> 2;
+    const int row = 32 * (warp & 3) + lane;  // key row
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t tS = tmem + lane_base + C::kSCol + 64 * g, tDP = tmem + lane_base + C::kDPCol + 64 * g;
+    const uint32_t sDS = smem_u32(sm + C::kDSOff);
+    uint32_t n = 0;
+    bool ok = true;
+    PItem it;
+    for (long long r = 0; ok && load_bitem<true>(a, r, it); ++r) {
+      if (it.hi <= it.lo) continue;
+      const int ns = it.hi - it.lo;
+      const bool valid = row < it.lkv;
+      for (int t = 0; t < ns; ++t) {
+        const uint32_t nt = n + t;
+        const int nq = min(kTile, it.lq - (it.lo + t) * kTile) - 64 * g;  // this group's query columns
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->s_full, nt & 1, abort_flag, a, 129));
+        if (!ok) break;
+        tc_fence_after();
+        // One 32-column half at a time, so that only the derivatives stay live
+        // across the dP^T wait; each half's hi and lo parts go in place of
+        // its own 32 columns.
+        float gr[64];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t hi[16], lo[16];
+          if (32 * c < nq) {
+            uint32_t sv[32];
+            tmem_ld32(tS + 32 * c, sv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int q = 32 * c + 2 * e;
+              float f0, f1, g0, g1;
+              act_and_grad<ACT>(__uint_as_float(sv[2 * e]) * a.scale, f0, g0);
+              act_and_grad<ACT>(__uint_as_float(sv[2 * e + 1]) * a.scale, f1, g1);
+              const bool a0 = valid && q < nq, a1 = valid && q + 1 < nq;
+              f0 = a0 ? f0 : 0.0f;
+              f1 = a1 ? f1 : 0.0f;
+              gr[q] = a0 ? g0 : 0.0f;
+              gr[q + 1] = a1 ? g1 : 0.0f;
+              hi[e] = pack_bf16x2(f0, f1);
+              if constexpr (HILO) lo[e] = bf16x2_lo(f0, f1, hi[e]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
+          }
+          tmem_st16(tS + 32 * c, hi);
+          if constexpr (HILO) tmem_st16(tS + 32 * c + 16, lo);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_ready);
+
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->dp_full, nt & 1, abort_flag, a, 130));
+        if (!ok) break;
+        // the dQ product of the step before has read the shared dS^T tile
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->dsm_free, (nt & 1) ^ 1, abort_flag, a, 131));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t hi[16], lo[16];
+          if (32 * c < nq) {
+            uint32_t dv[32];
+            tmem_ld32(tDP + 32 * c, dv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int q = 32 * c + 2 * e;
+              const float d0 = gr[q] * __uint_as_float(dv[2 * e]), d1 = gr[q + 1] * __uint_as_float(dv[2 * e + 1]);
+              hi[e] = pack_bf16x2(d0, d1);
+              if constexpr (HILO) lo[e] = bf16x2_lo(d0, d1, hi[e]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
+          }
+          tmem_st16(tDP + 32 * c, hi);
+          st_dst_row(sDS, row, 64 * g + 32 * c, hi);
+          if constexpr (HILO) {
+            tmem_st16(tDP + 32 * c + 16, lo);
+            st_dst_row(sDS + kTileBytes, row, 64 * g + 32 * c, lo);
+          }
+        }
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->ds_ready);
+      }
+      if (!ok) break;
+      n += ns;
+    }
+  } else {
+    sb_set_regs<kSbEpiRegs>();
+    // ------------------------------------------------------------ epilogue warpgroup
+    // dQ rows (thread = query row) every step, dV / dK rows (thread = key row)
+    // at the item's end; items without queries get zero dK / dV rows.
+    const int row = 32 * (warp & 3) + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    uint32_t acc_n = 0, n = 0;
+    bool ok = true;
+    PItem it;
+    for (long long r = 0; ok && load_bitem<true>(a, r, it); ++r) {
+      const bool kvalid = row < it.lkv;
+      const int64_t gk = it.k0 + row;
+      __nv_bfloat16* dv_row = a.out1 + (gk * a.H + it.h) * kD;
+      __nv_bfloat16* dk_row = a.out2 + (gk * a.H + it.h) * kD;
+      if (it.hi <= it.lo) {
+        if (kvalid) {
+          uint4* dv = reinterpret_cast<uint4*>(dv_row);
+          uint4* dk = reinterpret_cast<uint4*>(dk_row);
+          for (int e = 0; e < kD / 8; ++e) dv[e] = dk[e] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      const int ns = it.hi - it.lo;
+      const float cn = (a.norm_by_lkv && it.lkv > 0) ? 1.0f / it.lkv : 1.0f;
+      for (int t = 0; t < ns && ok; ++t) {
+        const uint32_t nt = n + t;
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->dq_full, nt & 1, abort_flag, a, 132));
+        if (!ok) break;
+        tc_fence_after();
+        const int ql = (it.lo + t) * kTile + row;
+        const bool qvalid = ql < it.lq;
+        __nv_bfloat16* dq_row = a.out0 + ((it.q0 + ql) * a.H + it.h) * kD;
+#pragma unroll 1
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + C::kDPCol + 32 * c, v);
+          tmem_ld_wait();
+          if (c == kD / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&bars->dq_empty);
+          }
+          if (qvalid) {
+            uint32_t w[16];
+            const float mul = cn * a.scale;
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+            store_words16(dq_row + 32 * c, w, a.out_v8);
+          }
+        }
+      }
+      if (!ok) break;
+      n += ns;
+      ok = __all_sync(0xffffffffu, wait_bar(&bars->acc_full, acc_n & 1, abort_flag, a, 133));
+      if (!ok) break;
+      ++acc_n;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 2 * kD / 32; ++c) {
+        const bool is_dk = c >= kD / 32;
+        const int cc = is_dk ? c - kD / 32 : c;
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + (is_dk ? C::kDKCol : C::kDVCol) + 32 * cc, v);
+        tmem_ld_wait();
+        if (c == 2 * kD / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(&bars->acc_empty);
+        }
+        if (kvalid) {
+          uint32_t w[16];
+          const float mul = is_dk ? cn * a.scale : cn;
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+          store_words16((is_dk ? dk_row : dv_row) + 32 * cc, w, a.out_v8);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
 // ---------------------------------------------------------------------------- backward
 // Two modes share the kernel. Pooling (CROSS = false): an item is (sequence,
 // head) with at most 64 queries, loaded once, and its key tiles are the steps;
@@ -1302,7 +1734,29 @@ cudaError_t skv_act(bool hilo, const CUtensorMap& q, const CUtensorMap& k, const
   return cudaGetLastError();
 }
 
+template <int ACT>
+cudaError_t skvb_act(bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                     const CUtensorMap& dout, const AttnArgs& a, const int* gate, int grid, cudaStream_t st) {
+  auto kernel = hilo ? skv_bwd_kernel<ACT, true> : skv_bwd_kernel<ACT, false>;
+  const int smem = hilo ? SbCfg<true>::kSmemBytes : SbCfg<false>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kBwdThreads, smem, st>>>(q, k, v, dout, a, gate);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_skv_bwd(int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                           const CUtensorMap& dout, const AttnArgs& a, const int* gate, int grid,
+                           cudaStream_t stream) {
+  switch (act) {
+    case JATTN_SILU: return skvb_act<JATTN_SILU>(hilo, q, k, v, dout, a, gate, grid, stream);
+    case JATTN_GELU_TANH: return skvb_act<JATTN_GELU_TANH>(hilo, q, k, v, dout, a, gate, grid, stream);
+    case JATTN_GELU_POLY: return skvb_act<JATTN_GELU_POLY>(hilo, q, k, v, dout, a, gate, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_pma_fwd(int act, bool hilo, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                            const AttnArgs& a, int grid, cudaStream_t stream) {

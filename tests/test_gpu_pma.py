@@ -1,7 +1,9 @@
 """The kernels that put the keys on the MMA's M dimension, for pointwise
 attention without a mask at D = 128: the short-query (pooling) forward and
-fused backward when sequences average at most 64 queries, and the fused
-backward's cross mode when they average more queries but at most 128 keys.
+fused backward when sequences average at most 64 queries, and the short-key
+forward and fused backward when they average more queries but hold at most
+128 keys (and, behind a debug flag, the short-query backward's keys-on-M cross
+mode for those shapes).
 CUDA path vs the oracle element by element, the gates that hand batches
 outside a mode's limits back to the general backward, the rows the stores
 touch, and the bounded waits."""
@@ -138,17 +140,18 @@ def test_short_query_waits_time_out_then_recover():
 
 
 # ---------------------------------------------------------------- cross-attention over short key sequences
-# every sequence Lkv <= 128 (and keys whenever it has queries): the fused
-# backward's cross mode; more than 64 queries per sequence on average
+# every sequence Lkv <= 128 (and keys whenever it has queries): the short-key
+# forward and backward; more than 64 queries per sequence on average
 CROSS_LQ = [1000, 1, 64, 65, 300, 0, 129, 700, 5]
 CROSS_LKV = [16, 128, 1, 127, 100, 40, 64, 128, 3]
 FWD_ON_SHORT_Q = 64  # debug flag bit: the short-key shapes' forward on the short-query kernel
+KEYS_ON_M_CROSS = 128  # debug flag bit: their backward on the short-query kernel's cross mode
 
 
 @pytest.mark.parametrize("norm", [True, False])
 @pytest.mark.parametrize("act", [SILU, GELU])
 def test_short_key_matches_oracle(act, norm):
-    """Chunks of 1 to 64 queries (ragged last chunk), 1 to 128 keys, a
+    """Steps of 1 to 128 queries (ragged last step), 1 to 128 keys, a
     sequence with keys but no queries (zero dK and dV)."""
     _check(_w(act, norm), CROSS_LQ, CROSS_LKV, seed=91 + act + 2 * norm)
 
@@ -160,8 +163,16 @@ def test_short_key_gelu_poly():
 @pytest.mark.parametrize("act", [SILU, GELU])
 def test_short_key_long_queries(act):
     """Cross-attention lengths: thousands of queries per 16-128 keys (dK and dV
-    accumulate over up to 128 chunks in TMEM)."""
+    accumulate over up to 63 query tiles in TMEM)."""
     _check(_w(act, H=2), [8000, 3000, 129, 5], [128, 16, 100, 1], seed=96)
+
+
+@pytest.mark.parametrize("norm", [True, False])
+def test_short_key_keys_on_m_cross_mode(norm):
+    """The short-query backward's cross mode (keys on M, 64-query chunks) on
+    the same shapes, behind a debug flag; long and ragged sequences."""
+    _check(_w(SILU, norm), CROSS_LQ, CROSS_LKV, seed=104, flags=KEYS_ON_M_CROSS)
+    _check(_w(GELU, norm, H=2), [8000, 129, 5], [128, 100, 1], seed=105, flags=KEYS_ON_M_CROSS)
 
 
 @pytest.mark.parametrize("act", [SILU, GELU])
