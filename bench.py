@@ -393,7 +393,8 @@ def main():
     roof["kernel"] = dom
     if fused:
         roof["kernel_name"] = {"fwd": "pma_fwd_kernel" if short_q else "skv_fwd_kernel",
-                               "dkdv": "pma_bwd_kernel (fused dQ, dK, dV)"}.get(dom, dom)
+                               "dkdv": ("pma_bwd_kernel" if short_q else "skv_bwd_kernel")
+                               + " (fused dQ, dK, dV)"}.get(dom, dom)
     roof["peak_source"] = peaks["source"] + " (burst)"
 
     # end to end through the public API: pinned host inputs, copies inside the timed region

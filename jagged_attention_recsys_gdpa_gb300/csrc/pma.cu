@@ -85,9 +85,12 @@ __device__ __forceinline__ float tanh_approx(float x) {
 template <int ACT>
 __device__ __forceinline__ void act_and_grad(float x, float& f, float& g) {
   if constexpr (ACT == JATTN_SILU) {
-    const float sg = __fdividef(1.0f, 1.0f + ex2_approx(-x * kLog2e));
-    f = x * sg;
-    g = sg * fmaf(x, 1.0f - sg, 1.0f);
+    // with h = x / 2 and t = tanh h: sigmoid(x) = (1 + t) / 2, so
+    // f = h (1 + t) and f' = (1 + t + h (1 - t^2)) / 2 (one MUFU operation)
+    const float h = 0.5f * x;
+    const float t = tanh_approx(h);
+    f = fmaf(h, t, h);
+    g = fmaf(0.5f, t + fmaf(-h, t * t, h), 0.5f);
   } else if constexpr (ACT == JATTN_GELU_POLY) {
     f = gelu_poly(x);
     g = gelu_poly_grad(x);
@@ -884,17 +887,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       PItem it;
       for (long long r = 0; ok && load_bitem<true>(a, r, it); ++r) {
         if (it.hi <= it.lo) continue;
-        if (!(ok = wait_bar(&bars->kv_empty, (kv_it & 1) ^ 1, abort_flag, a, 121))) break;
-        if (!skip) {
-          mbar_arrive_expect_tx(&bars->kv_full, 2 * kTileBytes);
-          for (int c = 0; c < 2; ++c) {
-            tma_load_2d(sm + C::kKOff + c * kBoxK, &tmK, &bars->kv_full, it.h * kD + c * 64, static_cast<int>(it.k0));
-            tma_load_2d(sm + C::kVOff + c * kBoxK, &tmV, &bars->kv_full, it.h * kD + c * 64, static_cast<int>(it.k0));
+        // the item's first Q / dO copies go out before its K / V copy, which
+        // waits for the item before to finish
+        auto load_kv = [&]() -> bool {
+          if (!wait_bar(&bars->kv_empty, (kv_it & 1) ^ 1, abort_flag, a, 121)) return false;
+          if (!skip) {
+            mbar_arrive_expect_tx(&bars->kv_full, 2 * kTileBytes);
+            for (int c = 0; c < 2; ++c) {
+              tma_load_2d(sm + C::kKOff + c * kBoxK, &tmK, &bars->kv_full, it.h * kD + c * 64,
+                          static_cast<int>(it.k0));
+              tma_load_2d(sm + C::kVOff + c * kBoxK, &tmV, &bars->kv_full, it.h * kD + c * 64,
+                          static_cast<int>(it.k0));
+            }
+            kv_armed = true;
           }
-          kv_armed = true;
-        }
-        ++kv_it;
+          ++kv_it;
+          return true;
+        };
+        const int pre = min(it.hi - it.lo, C::kStages);
         for (int t = it.lo; t < it.hi && ok; ++t, ++qd_it) {
+          if (t == it.lo + pre && !(ok = load_kv())) break;
           const int s = qd_it % C::kStages;
           if (!(ok = wait_bar(&bars->qd_empty[s], ((qd_it / C::kStages) & 1) ^ 1, abort_flag, a, 122))) break;
           mbar_arrive_expect_tx(&bars->qd_full[s], 2 * kTileBytes);
@@ -905,6 +917,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_load_2d(dst + kTileBytes + c * kBoxK, &tmDO, &bars->qd_full[s], it.h * kD + c * 64, y);
           }
         }
+        if (ok && pre == it.hi - it.lo) ok = load_kv();
       }
       if (kv_armed) drain_wait(&bars->kv_full, (kv_it - 1) & 1, a.timeout_ns);
       for (uint32_t i = (qd_it > (uint32_t)C::kStages ? qd_it - C::kStages : 0); i < qd_it; ++i)
@@ -978,8 +991,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int kk = 0; kk < kTile / 16; ++kk)
               mma_ts(tmem + C::kDKCol, tmem + C::kDPCol + sb_acol(kk, hl), dQm + mnslice(kk), idG,
                      (t > 0 || hl > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars->qd_empty[qi % C::kStages]);  // dK was the last product to read Q / dO
           // dQ = dS K into the dP^T columns (dK has been issued: in order, it
-          // reads dS^T first); then the shared dS^T tile and Q / dO are free
+          // reads dS^T first); then the shared dS^T tile is free
 #pragma unroll
           for (int hl = 0; hl < C::kNP; ++hl)
 #pragma unroll
@@ -988,7 +1002,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      (hl > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars->dq_full);
           mma_commit(&bars->dsm_free);
-          mma_commit(&bars->qd_empty[qi % C::kStages]);
           if (t + 1 < ns) {
             if (!(ok = issue_s(qi + 1))) break;
             if (!(ok = issue_dp(qi + 1, nt + 1))) break;
@@ -1022,6 +1035,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (it.hi <= it.lo) continue;
       const int ns = it.hi - it.lo;
       const bool valid = row < it.lkv;
+      const bool live = 32 * (warp & 3) < it.lkv;  // the warp holds one of the item's key rows
       for (int t = 0; t < ns; ++t) {
         const uint32_t nt = n + t;
         const int nq = min(kTile, it.lq - (it.lo + t) * kTile) - 64 * g;  // this group's query columns
@@ -1030,28 +1044,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         // One 32-column half at a time, so that only the derivatives stay live
         // across the dP^T wait; each half's hi and lo parts go in place of
-        // its own 32 columns.
+        // its own 32 columns. A warp whose 32 key rows all lie past the
+        // item's keys computes nothing and writes zeros. P^T rows of keys
+        // past the end are left unmasked (they reach only dV rows that are
+        // never stored); dS^T rows are masked, since dQ sums over keys.
         float gr[64];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t hi[16], lo[16];
-          if (32 * c < nq) {
+          if (live && 32 * c < nq) {
             uint32_t sv[32];
             tmem_ld32(tS + 32 * c, sv);
             tmem_ld_wait();
+            if (32 * c + 32 <= nq) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int q = 32 * c + 2 * e;
-              float f0, f1, g0, g1;
-              act_and_grad<ACT>(__uint_as_float(sv[2 * e]) * a.scale, f0, g0);
-              act_and_grad<ACT>(__uint_as_float(sv[2 * e + 1]) * a.scale, f1, g1);
-              const bool a0 = valid && q < nq, a1 = valid && q + 1 < nq;
-              f0 = a0 ? f0 : 0.0f;
-              f1 = a1 ? f1 : 0.0f;
-              gr[q] = a0 ? g0 : 0.0f;
-              gr[q + 1] = a1 ? g1 : 0.0f;
-              hi[e] = pack_bf16x2(f0, f1);
-              if constexpr (HILO) lo[e] = bf16x2_lo(f0, f1, hi[e]);
+              for (int e = 0; e < 16; ++e) {
+                float f0, f1;
+                act_and_grad<ACT>(__uint_as_float(sv[2 * e]) * a.scale, f0, gr[32 * c + 2 * e]);
+                act_and_grad<ACT>(__uint_as_float(sv[2 * e + 1]) * a.scale, f1, gr[32 * c + 2 * e + 1]);
+                hi[e] = pack_bf16x2(f0, f1);
+                if constexpr (HILO) lo[e] = bf16x2_lo(f0, f1, hi[e]);
+              }
+            } else {  // the item's last query tile: columns past its queries are zero
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int q = 32 * c + 2 * e;
+                float f0, f1, g0, g1;
+                act_and_grad<ACT>(__uint_as_float(sv[2 * e]) * a.scale, f0, g0);
+                act_and_grad<ACT>(__uint_as_float(sv[2 * e + 1]) * a.scale, f1, g1);
+                const bool a0 = q < nq, a1 = q + 1 < nq;
+                f0 = a0 ? f0 : 0.0f;
+                f1 = a1 ? f1 : 0.0f;
+                gr[q] = a0 ? g0 : 0.0f;
+                gr[q + 1] = a1 ? g1 : 0.0f;
+                hi[e] = pack_bf16x2(f0, f1);
+                if constexpr (HILO) lo[e] = bf16x2_lo(f0, f1, hi[e]);
+              }
             }
           } else {
 #pragma unroll
@@ -1073,7 +1101,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t hi[16], lo[16];
-          if (32 * c < nq) {
+          if (live && 32 * c < nq) {
             uint32_t dv[32];
             tmem_ld32(tDP + 32 * c, dv);
             tmem_ld_wait();
@@ -1081,8 +1109,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int e = 0; e < 16; ++e) {
               const int q = 32 * c + 2 * e;
               const float d0 = gr[q] * __uint_as_float(dv[2 * e]), d1 = gr[q + 1] * __uint_as_float(dv[2 * e + 1]);
-              hi[e] = pack_bf16x2(d0, d1);
-              if constexpr (HILO) lo[e] = bf16x2_lo(d0, d1, hi[e]);
+              hi[e] = valid ? pack_bf16x2(d0, d1) : 0u;
+              if constexpr (HILO) lo[e] = valid ? bf16x2_lo(d0, d1, hi[e]) : 0u;
             }
           } else {
 #pragma unroll
