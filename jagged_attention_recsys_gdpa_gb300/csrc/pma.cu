@@ -121,6 +121,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
 
 // 16 packed bf16 pairs (queries c0 .. c0 + 31 of key row `row`) into a
 // [128 keys][64 queries] tile in the 128-byte-swizzled layout an MN-major MMA
@@ -775,9 +780,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the item's end. TMEM [S^T | dP^T, then dQ | dV | dK] = 512 columns; the next
 // step's S^T is issued right after this step's dQ, its dP^T once the
 // epilogue has read dQ.
-constexpr int kSbCtlRegs = 120;  // 512 x 128 at launch = 128 x (120 + 2 x 160 + 72)
+constexpr int kSbCtlRegs = 128;  // 512 x 128 at launch = 128 x (128 + 2 x 160 + 64)
 constexpr int kSbActRegs = 160;
-constexpr int kSbEpiRegs = 72;
+constexpr int kSbEpiRegs = 64;
 static_assert(128 * (kSbCtlRegs + 2 * kSbActRegs + kSbEpiRegs) <= kBwdThreads * 128, "register split");
 constexpr int kSbMaxStages = 2;
 
@@ -806,7 +811,7 @@ struct SbBars {
   uint64_t kv_full, kv_empty;
   uint64_t qd_full[kSbMaxStages], qd_empty[kSbMaxStages];
   uint64_t s_full, dp_full, p_ready, ds_ready, dsm_free;
-  uint64_t acc_full, acc_empty, dq_full, dq_empty, drain;
+  uint64_t acc_full, acc_empty, dq_full, dq_empty, drain, epi_sync, dsm_ready;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -854,7 +859,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_ready, 2 * kTile);
     mbar_init(&bars->ds_ready, 2 * kTile);
-    mbar_init(&bars->dsm_free, 1);
+    mbar_init(&bars->dsm_ready, 2 * kTile);
+    mbar_init(&bars->dsm_free, kTile);  // the epilogue has stored the dQ rows staged there
+    mbar_init(&bars->epi_sync, kTile);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, kTile);
     mbar_init(&bars->dq_full, 1);
@@ -992,6 +999,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               mma_ts(tmem + C::kDKCol, tmem + C::kDPCol + sb_acol(kk, hl), dQm + mnslice(kk), idG,
                      (t > 0 || hl > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars->qd_empty[qi % C::kStages]);  // dK was the last product to read Q / dO
+          if (!(ok = wait_bar(&bars->dsm_ready, nt & 1, abort_flag, a, 135))) break;
           // dQ = dS K into the dP^T columns (dK has been issued: in order, it
           // reads dS^T first); then the shared dS^T tile is free
 #pragma unroll
@@ -1001,7 +1009,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               mma_ss(tmem + C::kDPCol, dDS + hl * (kTileBytes >> 4) + mnslice(kk), dKm + mnslice(kk), idQ,
                      (hl > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars->dq_full);
-          mma_commit(&bars->dsm_free);
           if (t + 1 < ns) {
             if (!(ok = issue_s(qi + 1))) break;
             if (!(ok = issue_dp(qi + 1, nt + 1))) break;
@@ -1094,13 +1101,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
         ok = __all_sync(0xffffffffu, wait_bar(&bars->dp_full, nt & 1, abort_flag, a, 130));
         if (!ok) break;
-        // the dQ product of the step before has read the shared dS^T tile
-        ok = __all_sync(0xffffffffu, wait_bar(&bars->dsm_free, (nt & 1) ^ 1, abort_flag, a, 131));
-        if (!ok) break;
         tc_fence_after();
+        // dS^T into TMEM first (dK may start), then, once the epilogue has
+        // stored the step before's dQ rows from the shared tile's room, into
+        // the shared tile (dQ may start)
+        uint32_t hh[2][16], ll[2][16];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t hi[16], lo[16];
           if (live && 32 * c < nq) {
             uint32_t dv[32];
             tmem_ld32(tDP + 32 * c, dv);
@@ -1109,24 +1116,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int e = 0; e < 16; ++e) {
               const int q = 32 * c + 2 * e;
               const float d0 = gr[q] * __uint_as_float(dv[2 * e]), d1 = gr[q + 1] * __uint_as_float(dv[2 * e + 1]);
-              hi[e] = valid ? pack_bf16x2(d0, d1) : 0u;
-              if constexpr (HILO) lo[e] = valid ? bf16x2_lo(d0, d1, hi[e]) : 0u;
+              hh[c][e] = valid ? pack_bf16x2(d0, d1) : 0u;
+              if constexpr (HILO) ll[c][e] = valid ? bf16x2_lo(d0, d1, hh[c][e]) : 0u;
             }
           } else {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
+            for (int e = 0; e < 16; ++e) hh[c][e] = ll[c][e] = 0u;
           }
-          tmem_st16(tDP + 32 * c, hi);
-          st_dst_row(sDS, row, 64 * g + 32 * c, hi);
-          if constexpr (HILO) {
-            tmem_st16(tDP + 32 * c + 16, lo);
-            st_dst_row(sDS + kTileBytes, row, 64 * g + 32 * c, lo);
-          }
+          tmem_st16(tDP + 32 * c, hh[c]);
+          if constexpr (HILO) tmem_st16(tDP + 32 * c + 16, ll[c]);
         }
-        fence_proxy_async_smem();
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->ds_ready);
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->dsm_free, (nt & 1) ^ 1, abort_flag, a, 131));
+        if (!ok) break;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          st_dst_row(sDS, row, 64 * g + 32 * c, hh[c]);
+          if constexpr (HILO) st_dst_row(sDS + kTileBytes, row, 64 * g + 32 * c, ll[c]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->dsm_ready);
       }
       if (!ok) break;
       n += ns;
@@ -1138,6 +1149,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // at the item's end; items without queries get zero dK / dV rows.
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t sDQ = smem_u32(sm + C::kDSOff);
     uint32_t acc_n = 0, n = 0;
     bool ok = true;
     PItem it;
@@ -1161,9 +1173,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = __all_sync(0xffffffffu, wait_bar(&bars->dq_full, nt & 1, abort_flag, a, 132));
         if (!ok) break;
         tc_fence_after();
-        const int ql = (it.lo + t) * kTile + row;
-        const bool qvalid = ql < it.lq;
-        __nv_bfloat16* dq_row = a.out0 + ((it.q0 + ql) * a.H + it.h) * kD;
+        // dQ's rows (thread = query row) as bf16 into the dS^T tile's room,
+        // which the dQ product has finished reading: row r at r * 256 bytes,
+        // its 16-byte piece p at p ^ (r & 7). The TMEM columns are released
+        // after the last load, before any global store.
+        const float mul = cn * a.scale;
 #pragma unroll 1
         for (int c = 0; c < kD / 32; ++c) {
           uint32_t v[32];
@@ -1173,15 +1187,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_before();
             mbar_arrive(&bars->dq_empty);
           }
-          if (qvalid) {
-            uint32_t w[16];
-            const float mul = cn * a.scale;
+          uint32_t w[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-            store_words16(dq_row + 32 * c, w, a.out_v8);
-          }
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+          const uint32_t rb = sDQ + static_cast<uint32_t>(row) * 256;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            st_shared_v4(rb + (((4 * c + i) ^ (row & 7)) << 4), w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
+        // all 128 rows staged; then warp w stores rows 32 w .. 32 w + 31, two
+        // 256-byte rows per instruction, and the tile's room goes back to the
+        // activation
+        mbar_arrive(&bars->epi_sync);
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->epi_sync, nt & 1, abort_flag, a, 134));
+        if (!ok) break;
+        const int q_tile0 = (it.lo + t) * kTile;
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          const int r = 32 * (warp & 3) + 2 * i + (lane >> 4), pc = lane & 15;
+          const uint4 val = ld_shared_v4(sDQ + static_cast<uint32_t>(r) * 256 + ((pc ^ (r & 7)) << 4));
+          const int ql = q_tile0 + r;
+          if (ql < it.lq) *reinterpret_cast<uint4*>(a.out0 + ((it.q0 + ql) * a.H + it.h) * kD + 8 * pc) = val;
+        }
+        mbar_arrive(&bars->dsm_free);
       }
       if (!ok) break;
       n += ns;
