@@ -129,8 +129,9 @@ int jattn_workspace_size(const jattn_params_t* p, size_t* bytes);
  * over short key sequences (the same activation, mask and D, total_q > 64 B
  * and total_kv <= 128 B) runs a forward that keeps each sequence's one K/V
  * tile resident while its query tiles stream past, and a backward that fuses
- * the three gradients into one pass over 64-query chunks, when every
- * sequence has Lkv <= 128, and keys whenever it has queries. These
+ * the three gradients into one pass over 128-query tiles (dQ complete per
+ * tile, dK and dV accumulated over the sequence), when every sequence has
+ * Lkv <= 128, and keys whenever it has queries. These
  * conditions are checked on the device, without a host round trip; outside
  * them the general passes run. Results and their precision are the same as
  * on the general kernels. */
