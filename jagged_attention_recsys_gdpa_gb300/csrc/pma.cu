@@ -23,10 +23,14 @@
 //     cross     (every sequence Lkv <= 128, and keys when it has queries): the
 //               K / V tile is loaded once, the 64-query chunks are the steps;
 //               dQ of a chunk is complete after its step, dV and dK
-//               accumulate over the item. Q and dO are read once.
-// The same short-key shapes have a forward in the usual orientation
-// (skv_fwd_kernel): each sequence's K / V tile stays in shared memory while
-// its 128-row query tiles stream through a ring.
+//               accumulate over the item. Q and dO are read once. Only
+//               behind debug flag bit 128: the short-key backward below
+//               takes these shapes.
+// The same short-key shapes run in the usual orientation (queries on N):
+// skv_fwd_kernel keeps each sequence's K / V tile in shared memory while its
+// 128-row query tiles stream through a ring, and skv_bwd_kernel does the same
+// for the backward, with 128 queries per step so that all five products run
+// at N = 128.
 // A gate kernel checks the chosen mode's limits on the device and either
 // clears the general dQ and dK/dV schedules (their passes then find no work)
 // or leaves them to run while this pass finds the gate closed and returns.
