@@ -160,11 +160,21 @@ def test_short_key_gelu_poly():
     _check(_w(POLY, qk=1.0), CROSS_LQ, CROSS_LKV, seed=95)
 
 
+@pytest.mark.parametrize("norm", [True, False])
 @pytest.mark.parametrize("act", [SILU, GELU])
-def test_short_key_long_queries(act):
+def test_short_key_long_queries(act, norm):
     """Cross-attention lengths: thousands of queries per 16-128 keys (dK and dV
-    accumulate over up to 63 query tiles in TMEM)."""
-    _check(_w(act, H=2), [8000, 3000, 129, 5], [128, 16, 100, 1], seed=96)
+    accumulate over up to 63 query tiles in TMEM; without the normaliser, P and
+    dS enter the products as bf16 hi + lo parts)."""
+    _check(_w(act, norm, H=2), [8000, 3000, 129, 5], [128, 16, 100, 1], seed=96)
+
+
+def test_short_key_warp_and_tile_boundaries():
+    """Key counts at the 32-row warp boundaries (a warp whose rows all lie past
+    the keys skips the activation) and query counts that fill whole 128-row
+    tiles or miss by one."""
+    _check(_w(SILU, H=2), [128, 256, 384, 129, 127, 300], [32, 33, 65, 96, 97, 64], seed=106)
+    _check(_w(GELU, False, H=2), [128, 256, 384, 129, 127, 300], [32, 33, 65, 96, 97, 64], seed=107)
 
 
 @pytest.mark.parametrize("norm", [True, False])
