@@ -55,7 +55,7 @@ def short_query_path(act: int, mask: int, D: int, lq, lkv) -> bool:
 
 def short_key_path(act: int, mask: int, D: int, lq, lkv) -> bool:
     """Whether the library runs a batch as cross-attention over short key
-    sequences: the short-key forward and the fused backward's cross mode. A
+    sequences: the short-key forward and the short-key fused backward. A
     pointwise activation, no mask, D = 128, more than 64 queries but at most
     128 keys per sequence on average (the host's rule) and every sequence with
     Lkv <= 128 and keys whenever it has queries (the device-side gate)."""
