@@ -406,7 +406,12 @@ void jattn_profile_events(void* const* events);
  * JATTN_ERR_TIMEOUT and leaves the context usable. Flag bit 1 (bit 2) makes
  * the forward use the column-split (ping-pong) arrangement of its activation
  * warps whatever the shapes, so both can be checked on the same inputs;
- * results agree within floating-point rounding order. */
+ * results agree within floating-point rounding order. The other bits pick
+ * between code paths that compute the same results in the same way: bit 3
+ * (bit 4) makes the dQ pass hold K and V in two rings (one ring); bit 5 runs
+ * pooling and short-key shapes on the general kernels; bit 6 runs the
+ * short-key shapes' forward on the short-query (keys-on-M) kernel; bit 7 runs
+ * their backward on the short-query backward's cross mode (64-query chunks). */
 void jattn_debug_set(int flags, uint64_t timeout_ns);
 
 #ifdef __cplusplus
