@@ -783,7 +783,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // and the epilogue warpgroup writes dQ's rows each step and dK / dV's rows at
 // the item's end. TMEM [S^T | dP^T, then dQ | dV | dK] = 512 columns; the next
 // step's S^T is issued right after this step's dQ, its dP^T once the
-// epilogue has read dQ.
+// epilogue has read dQ. dS^T reaches TMEM first (dK may start) and the shared
+// tile second (dQ waits for it); the epilogue stages dQ's rows as bf16 in that
+// tile's room once dQ has read it, stores them row-coalesced, and only then
+// lets the activation write the next step's dS^T there. Warps whose 32 key
+// rows all lie past the item's keys skip the activation and write zeros.
 constexpr int kSbCtlRegs = 128;  // 512 x 128 at launch = 128 x (128 + 2 x 160 + 64)
 constexpr int kSbActRegs = 160;
 constexpr int kSbEpiRegs = 64;
