@@ -39,12 +39,41 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
+def code_hash(path: str) -> str:
+    """sha1 (hex) of a C / CUDA source with its comments, trailing blanks and
+    empty lines removed, so that a counter row stays attached to a kernel
+    whose code has not changed when only its comments have."""
+    import hashlib
+
+    with open(path, encoding="utf-8") as fh:
+        text = fh.read()
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # string or character literal, copied with its escapes
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            while i < n and text[i] != "\n":
+                i += 1
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).split("\n")]
+    return hashlib.sha1("\n".join(ln for ln in lines if ln).encode()).hexdigest()
+
+
 def ncu_traffic(workload: str, kernel: str, algorithmic: float):
     """DRAM bytes (read + write) per launch from the committed ncu table, scaled
     from the captured case to this launch by algorithmic bytes; None when no
-    row matches or the kernel source changed since the capture (sha1 prefix)."""
-    import hashlib
-
+    row matches or the kernel's code changed since the capture (prefix of
+    code_hash, which ignores comments)."""
     if not os.path.exists(TRAFFIC_TABLE):
         return None
     with open(TRAFFIC_TABLE) as f:
@@ -54,9 +83,8 @@ def ncu_traffic(workload: str, kernel: str, algorithmic: float):
             continue
         src, sha, dram, alg = r[2], r[3], float(r[4]), float(r[5])
         path = os.path.join(ROOT, "jagged_attention_recsys_gdpa_gb300", "csrc", src)
-        with open(path, "rb") as fh:
-            if hashlib.sha1(fh.read()).hexdigest()[:12] != sha:
-                return None
+        if code_hash(path)[:12] != sha:
+            return None
         return dram * algorithmic / alg
     return None
 
