@@ -25,13 +25,28 @@ thread_local char g_last_error[256] = "";
 // never changes the launches another thread makes.
 thread_local int g_debug_flags = 0;
 
+// Key tiles a 128-row query tile visits on average, from the mask and the
+// mean key length: with a window, min(W, L) / 128 + 1; causal, L / 256 + 1;
+// none, L / 128 + 1; a block mask (blocks dividing the tile), one.
+double key_tiles_per_query_tile(const jattn_params_t& p) {
+  if (p.B < 1) return 0.0;
+  if (p.mask & JATTN_MASK_BLOCK) return 1.0;
+  const double lkv = static_cast<double>(p.total_kv) / static_cast<double>(p.B);
+  if (p.mask & JATTN_MASK_WINDOW) return std::min(static_cast<double>(p.window), lkv) / 128.0 + 1.0;
+  if (p.mask & JATTN_MASK_CAUSAL) return lkv / 256.0 + 1.0;
+  return lkv / 128.0 + 1.0;
+}
+
 // Forward activation arrangement: the column split when sequences average at
-// most one 128-row query tile (most items then hold a single tile), else the
-// ping-pong between two query tiles. Debug flag bits 1 / 2 force either one.
+// most one 128-row query tile (most items then hold a single tile) or query
+// tiles visit fewer than six key tiles (windows, blocks: the split's two
+// warpgroups finish each tile's softmax sooner, which matters more than the
+// ping-pong's overlap over so few tiles), else the ping-pong between two
+// query tiles. Debug flag bits 1 / 2 force either one.
 bool fwd_split(const jattn_params_t& p) {
   if (g_debug_flags & 2) return true;
   if (g_debug_flags & 4) return false;
-  return p.total_q <= static_cast<int64_t>(kTile) * p.B;
+  return p.total_q <= static_cast<int64_t>(kTile) * p.B || key_tiles_per_query_tile(p) < 6.0;
 }
 thread_local uint64_t g_timeout_ns = kDefaultTimeoutNs;
 // Optional events recorded around the main kernels: [fwd, dkdv, dq] x [begin, end].
@@ -224,21 +239,15 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int H, int D, int bo
 bool hilo_for(const jattn_params_t& p) { return p.act != JATTN_SOFTMAX && !p.norm_by_lkv; }
 
 // The dQ pass's K / V layout: two rings (K deeper than V) when query tiles
-// see many key tiles on average, where each tile's K latency would otherwise
-// show, one ring otherwise, where the second ring's barrier and release cost
-// more than they hide. Estimated from the mask and the mean key length: with
-// a window, min(W, L) / 128 + 1 tiles; causal, L / 256 + 1; none, L / 128 + 1.
-// Debug flag bits 8 / 16 force two rings / one ring.
+// see many key tiles on average (six or more), where each tile's K latency
+// would otherwise show, one ring otherwise, where the second ring's barrier
+// and release cost more than they hide. Debug flag bits 8 / 16 force two
+// rings / one ring.
 bool dq_split_rings(const jattn_params_t& p) {
   if (g_debug_flags & 8) return true;
   if (g_debug_flags & 16) return false;
   if (p.B < 1 || (p.mask & JATTN_MASK_BLOCK)) return false;
-  const double lkv = static_cast<double>(p.total_kv) / static_cast<double>(p.B);
-  double tiles;
-  if (p.mask & JATTN_MASK_WINDOW) tiles = std::min(static_cast<double>(p.window), lkv) / 128.0 + 1.0;
-  else if (p.mask & JATTN_MASK_CAUSAL) tiles = lkv / 256.0 + 1.0;
-  else tiles = lkv / 128.0 + 1.0;
-  return tiles >= 6.0;
+  return key_tiles_per_query_tile(p) >= 6.0;
 }
 
 // 2-D view [rows, H*D] of jagged E4M3 codes (one byte each); boxes of
