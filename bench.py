@@ -518,9 +518,16 @@ def main():
         import oracle
 
         oracle.build()
-        x_cpu = {k: (x[k].cpu() if hasattr(x[k], "cpu") else x[k]) for k in ("q_off", "kv_off", "q", "k", "v", "do")}
         seqs, eff = sample_sequences(x["lq"], x["lkv"], pairs_b, w.H, w.D, args.cpu_flops)
-        secs = cpu_oracle_step(x_cpu, w, seqs)
+        # only the sampled sequences' rows come to the host
+        qo, ko = x["q_off"].cpu().numpy(), x["kv_off"].cpu().numpy()
+        rq = torch.from_numpy(np.concatenate([np.arange(qo[b], qo[b + 1]) for b in seqs])).to(dev)
+        rk = torch.from_numpy(np.concatenate([np.arange(ko[b], ko[b + 1]) for b in seqs])).to(dev)
+        x_cpu = {"q_off": torch.from_numpy(inputs.offsets(np.array([qo[b + 1] - qo[b] for b in seqs]))),
+                 "kv_off": torch.from_numpy(inputs.offsets(np.array([ko[b + 1] - ko[b] for b in seqs])))}
+        x_cpu.update({k: x[k].index_select(0, rq).cpu() for k in ("q", "do")})
+        x_cpu.update({k: x[k].index_select(0, rk).cpu() for k in ("k", "v")})
+        secs = cpu_oracle_step(x_cpu, w, list(range(len(seqs))))
         cpu_base = {
             "value": eff / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{len(seqs)} of {len(x['lq'])} sequences, fwd+bwd in fp64, {secs:.1f} s",
